@@ -1,0 +1,230 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv: decode-phase paged attention on one GPU.
+ *
+ * The cache of every sequence lives in fixed-size blocks of a shared physical
+ * pool, and a per-sequence block table maps its logical blocks to physical
+ * ones (“让 Agent 跑得快：LLM 推理服务”, §二 and §五 “Block 级管理的优雅性”;
+ * “LLM 推理优化技术全景”, PagedAttention).  Each decode step appends the new
+ * token's K/V through a slot mapping and then attends with one query token per
+ * sequence under GQA, using the online (m, l) softmax recurrence (“LLM 推理优化
+ * 技术全景”, 在线 Softmax) so the score row is never materialised.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Pool tensors (K and V, separate): [num_blocks, block_size, num_kv_heads,
+ *    head_dim], row-major, elements bf16 or int8 (“LLM 推理引擎深度解析”,
+ *    §2.1: key_cache / value_cache of that shape).  The base of each pool must
+ *    be 16-byte aligned.
+ *  - int8 pools carry fp32 scales [num_blocks, num_kv_heads] for K and for V;
+ *    the stored value of element x is code * scale.
+ *  - Token slot: slot = physical_block * block_size + row.
+ *  - GQA: query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *  - seq_lens[b] counts every cached token of sequence b INCLUDING the one
+ *    appended this step; the step appends first and then attends.
+ *  - Supported geometry: head_dim in {64, 128}; block_size in {16, 32};
+ *    num_q_heads a multiple of num_kv_heads with a group of at most 8 query
+ *    heads per KV head.
+ *  - Pointers named "device" are CUDA device pointers of the current device;
+ *    "host" pointers are CPU memory.  The caller owns every buffer; the
+ *    library allocates no device memory.
+ *  - Calls that launch work are asynchronous on `stream` (a cudaStream_t
+ *    passed as void*; NULL = the legacy default stream) and return as soon as
+ *    the work is queued.
+ *
+ * Errors
+ * ------
+ *  - Problems visible on the host (null pointers, unsupported geometry, a
+ *    workspace that is too small) return a kv_status != KV_OK at once and
+ *    launch nothing; pagedkv_last_error() then describes it.
+ *  - Index problems only visible on the device (a slot past the pool, a block
+ *    id outside [0, num_blocks), a sequence length <= 0 or past the table or
+ *    past max_seq_len) never fault: the kernel skips the element, writes zeros
+ *    for that sequence's output rows and sets a bit in a per-device status
+ *    word, read with pagedkv_get_status().
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KV_OK = 0,
+    KV_ERR_INVALID_ARG = 1,    /* bad pointer, size or geometry           */
+    KV_ERR_OUT_OF_BLOCKS = 2,  /* the pool has too few free blocks        */
+    KV_ERR_CUDA = 3,           /* a CUDA runtime/driver call failed       */
+    KV_ERR_DEVICE_INDEX = 4,   /* device status word reported an index    */
+    KV_ERR_NOT_IMPLEMENTED = 5
+} kv_status;
+
+typedef enum { KV_DTYPE_BF16 = 0, KV_DTYPE_INT8 = 1 } kv_dtype;
+
+/* Bits of the device status word (pagedkv_get_status). */
+#define PAGEDKV_FLAG_BAD_SLOT 0x1u     /* slot >= num_blocks * block_size     */
+#define PAGEDKV_FLAG_BAD_BLOCK 0x2u    /* block id outside [0, num_blocks)    */
+#define PAGEDKV_FLAG_BAD_SEQ_LEN 0x4u  /* seq_len <= 0 or beyond table/hint   */
+#define PAGEDKV_FLAG_WAIT_TIMEOUT 0x8u /* a bounded in-kernel wait gave up    */
+
+/* ------------------------------------------------------------------------ */
+/* Block pool (host bookkeeping)                                            */
+/* ------------------------------------------------------------------------ */
+
+/* Opaque host object: pool geometry plus the free list.  It owns no device
+ * memory: the caller allocates the K/V pool tensors (pagedkv_pool_tensor_bytes
+ * each) and the scales. */
+typedef struct kv_pool kv_pool;
+
+/* Create a pool of num_blocks blocks.  Every id is free, in ascending order
+ * (“LLM 推理引擎深度解析”, §2.1: the free list starts as every block id).
+ * Returns KV_ERR_INVALID_ARG for non-positive sizes or a null `out`. */
+kv_status kv_pool_create(int num_blocks, int block_size, int num_kv_heads,
+                         int head_dim, kv_dtype dtype, kv_pool **out);
+
+/* Free the host object (NULL is allowed). */
+void kv_pool_destroy(kv_pool *pool);
+
+/* Bytes of one block holding K and V, scales excluded:
+ * 2 * block_size * num_kv_heads * head_dim * dtype_size
+ * (“让 Agent 跑得快：LLM 推理服务”, §二, the block_memory formula). */
+size_t kv_pool_block_bytes(const kv_pool *pool);
+
+/* Allocate n blocks, all or none, from the front of the free list, writing
+ * their ids to host array out_ids[n] (“LLM 推理引擎深度解析”, §2.1: allocation
+ * takes ids in free-list order and fails when too few are free).
+ * KV_ERR_OUT_OF_BLOCKS leaves the pool unchanged. */
+kv_status kv_pool_alloc(kv_pool *pool, int n, int32_t *out_ids);
+
+/* Return n block ids (host array) to the back of the free list (same page:
+ * finishing a request returns all its blocks).  Ids that are not currently
+ * allocated, or repeated, make the whole call fail with KV_ERR_INVALID_ARG
+ * and change nothing. */
+kv_status kv_pool_free(kv_pool *pool, const int32_t *ids, int n);
+
+/* Number of allocated and free blocks (either pointer may be NULL). */
+kv_status kv_pool_stats(const kv_pool *pool, int *used, int *free_blocks);
+
+/* Bytes of one pool tensor (K or V): num_blocks * block_size * num_kv_heads
+ * * head_dim * dtype_size. */
+size_t pagedkv_pool_tensor_bytes(int num_blocks, int block_size,
+                                 int num_kv_heads, int head_dim, kv_dtype dtype);
+
+/* ------------------------------------------------------------------------ */
+/* Slot mapping                                                             */
+/* ------------------------------------------------------------------------ */
+
+/* Decode-step slots: for every sequence b, the slot of position
+ * seq_lens[b] - 1, i.e. block_tables[b][(L-1) / bs] * bs + (L-1) % bs
+ * (“让 Agent 跑得快”, §五: a new block is taken every block_size tokens and the
+ * block table maps logical to physical blocks).
+ *   block_tables  device int32 [batch, max_blocks_per_seq]
+ *   seq_lens      device int32 [batch]
+ *   slot_mapping  device int64 [batch] (output)
+ * A length <= 0 or past the table, or a table entry outside
+ * [0, num_blocks), gives slot -1 and sets a status bit. */
+kv_status pagedkv_slot_mapping(const int32_t *block_tables,
+                               int max_blocks_per_seq, const int32_t *seq_lens,
+                               int batch, int block_size, int num_blocks,
+                               int64_t *slot_mapping, void *stream);
+
+/* General slots for a token list: token i of sequence seq_idx[i] (or i when
+ * seq_idx is NULL) at 0-based position positions[i] (e.g. a prefill).
+ *   seq_idx, positions  device int32 [num_tokens]
+ *   slot_mapping        device int64 [num_tokens] (output)
+ * Negative positions give slot -1 silently; bad indices as above. */
+kv_status pagedkv_token_slot_mapping(const int32_t *block_tables,
+                                     int max_blocks_per_seq,
+                                     const int32_t *seq_idx,
+                                     const int32_t *positions, int num_tokens,
+                                     int block_size, int num_blocks,
+                                     int64_t *slot_mapping, void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* Append                                                                   */
+/* ------------------------------------------------------------------------ */
+
+/* Write each token's new K/V into its slot (“让 Agent 跑得快”, §一 KV Cache:
+ * decode appends the new token's K/V; §五 “共享前缀”: only the current token
+ * writes).
+ *   k, v          device bf16 [num_tokens, num_kv_heads, head_dim]
+ *   k_cache, v_cache  device pool tensors (bf16 or int8, see above)
+ *   k_scale, v_scale  device fp32 [num_blocks, num_kv_heads] for int8 pools;
+ *                     must be NULL for bf16 pools
+ *   slot_mapping  device int64 [num_tokens]; slot < 0 skips the token
+ * bf16 pools receive the bits unchanged.  int8 pools receive
+ * clamp(round_half_even(fp32(x) / scale), -127, 127) computed with an IEEE
+ * fp32 divide (scale 0 is read as 1, NaN gives 0), with the scale of the
+ * slot's block and head.  A slot >= num_blocks * block_size is skipped and
+ * sets PAGEDKV_FLAG_BAD_SLOT. */
+kv_status reshape_and_cache(const void *k, const void *v, void *k_cache,
+                            void *v_cache, const float *k_scale,
+                            const float *v_scale, const int64_t *slot_mapping,
+                            int num_tokens, int num_blocks, int block_size,
+                            int num_kv_heads, int head_dim, kv_dtype dtype,
+                            void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* Attention                                                                */
+/* ------------------------------------------------------------------------ */
+
+/* Workspace bytes paged_attention_decode may need for the split-K partials of
+ * this shape (an upper bound over every partition size the library picks). */
+size_t pagedkv_workspace_bytes(int batch, int num_q_heads, int head_dim,
+                               int max_seq_len, int block_size);
+
+/* out[b, h, :] = softmax(scale * q[b, h, :] . K_t) . V_t over the
+ * t < seq_lens[b] tokens of sequence b (“LLM 推理优化技术全景”: 在线 Softmax,
+ * computed with the recurrence m' = max(m, max s), l' = l e^(m-m') + sum
+ * e^(s-m'), and the rescale deferred to the end as in “Flash Attention v2 的
+ * 改进”; long sequences are split into token partitions whose partials
+ * (m, l, unnormalised acc) are merged by log-sum-exp in a second kernel).
+ *   out           device bf16 [batch, num_q_heads, head_dim] (output)
+ *   q             device bf16 [batch, num_q_heads, head_dim]
+ *   k_cache, v_cache, k_scale, v_scale   as for reshape_and_cache
+ *   block_tables  device int32 [batch, max_blocks_per_seq]; entries past
+ *                 ceil(seq_lens[b] / block_size) are never read
+ *   seq_lens      device int32 [batch]
+ *   max_seq_len   host bound on every seq_lens[b] (sizes the partitions)
+ *   scale         softmax scale (1/sqrt(head_dim) for the usual attention)
+ *   workspace     device memory of at least pagedkv_workspace_bytes(...)
+ *                 bytes, 16-byte aligned; may be NULL when that size is 0
+ * Rows past seq_lens[b] inside the last block and blocks not in the table
+ * are never used, whatever they hold. */
+kv_status paged_attention_decode(void *out, const void *q, const void *k_cache,
+                                 const void *v_cache, const float *k_scale,
+                                 const float *v_scale,
+                                 const int32_t *block_tables,
+                                 int max_blocks_per_seq,
+                                 const int32_t *seq_lens, int batch,
+                                 int num_q_heads, int num_kv_heads,
+                                 int head_dim, int num_blocks, int block_size,
+                                 int max_seq_len, float scale, kv_dtype dtype,
+                                 void *workspace, size_t workspace_bytes,
+                                 void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* Status                                                                   */
+/* ------------------------------------------------------------------------ */
+
+/* Wait for `stream`, then read and clear the current device's status word
+ * into *device_flags (PAGEDKV_FLAG_* bits).  Returns KV_ERR_DEVICE_INDEX
+ * when any bit was set, KV_ERR_CUDA when a CUDA call failed, else KV_OK. */
+kv_status pagedkv_get_status(void *stream, unsigned int *device_flags);
+
+/* Message for the last error of the calling thread ("" if none). */
+const char *pagedkv_last_error(void);
+
+/* Token partition size paged_attention_decode would use for this shape on
+ * the current device (0 on error); partitions of more than one per sequence
+ * go through the merge kernel. */
+int pagedkv_partition_tokens(int batch, int num_kv_heads, int max_seq_len,
+                             int block_size);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -1,0 +1,306 @@
+"""Plain CPU oracle for decode-phase paged attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline legs of
+``bench.py`` may import this package.  The product (``paged_kv_cache_97_gb300``)
+never imports it, and it imports nothing from the product.
+
+Contents, each citing the passage it follows (page titles as printed):
+
+* size formulas -- ``block_memory_bytes`` (“让 Agent 跑得快：LLM 推理服务”, §二
+  PagedAttention, the block_memory formula), ``kv_bytes_per_token`` (same page,
+  §一 “KV Cache”), ``kv_cache_bytes`` (“LLM 推理优化技术全景”, KV Cache 大小公式),
+  ``blocks_needed`` / ``internal_waste_tokens`` (“LLM 推理引擎深度解析”, §2.1
+  PagedKVCache.allocate; “让 Agent 跑得快”, §五: waste only in the last block);
+* ``BlockPoolModel`` -- the block pool's allocation rules (“LLM 推理引擎深度解析”,
+  §2.1: FIFO free list, all-or-nothing allocation that fails when short,
+  free returns every block);
+* ``token_slots``, ``append_bf16``, ``append_int8``, ``quantize_int8``,
+  ``paged_attention`` (three-pass or online), ``attention_partials``,
+  ``lse_merge`` -- thin ctypes wrappers over ``pagedkv_oracle.c`` (plain C,
+  fp64), whose header cites the passages it follows.
+
+Parity pins: every function here is pinned by tests under ``tests/`` that run
+without a GPU (``-m "not gpu"``) against values the pages print, closed forms,
+brute force and a library routine; none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass, field
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pagedkv_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_liboracle_pagedkv.so")
+_lib = None
+
+OK, INVALID, INDEX = 0, 1, 4
+
+
+# --------------------------------------------------------------------------
+# Build / load
+# --------------------------------------------------------------------------
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle with gcc (no fast-math, no FMA contraction)."""
+    if force or not os.path.exists(_LIB_PATH) or (
+            os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+               "-ffp-contract=off", "-fno-fast-math", "-D_GNU_SOURCE",
+               "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    _lib = _bind(ctypes.CDLL(_LIB_PATH))
+    return _lib
+
+
+def _bind(lib):
+    """Declare the C signatures on a loaded copy of the oracle library."""
+    P = ctypes.c_void_p
+    I = ctypes.c_int
+    D = ctypes.c_double
+    lib.oracle_token_slots.argtypes = [P, I, P, P, I, I, I, P]
+    lib.oracle_append_bf16.argtypes = [P, P, P, P, P, I, I, I, I, I]
+    lib.oracle_append_int8.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I]
+    lib.oracle_quantize_int8.argtypes = [ctypes.c_float, ctypes.c_float]
+    lib.oracle_paged_attention.argtypes = [P, P, P, P, P, P, I, P, I, P, I, I,
+                                           I, I, I, I, D, P, I, I, I]
+    lib.oracle_attention_partials.argtypes = [P, P, P, P, P, P, P, I, P, I, P,
+                                              I, I, I, I, I, I, D, I, I, I]
+    lib.oracle_lse_merge.argtypes = [P, P, I, I, P]
+    lib.oracle_lse_merge.restype = None
+    return lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# --------------------------------------------------------------------------
+# Size formulas
+# --------------------------------------------------------------------------
+
+def block_memory_bytes(block_size: int, num_kv_heads: int, head_size: int,
+                       dtype_size: int) -> int:
+    """Bytes of one physical block holding K and V.
+
+    “让 Agent 跑得快：LLM 推理服务”, §二 PagedAttention: block_memory =
+    2 × block_size × num_kv_heads × head_size × dtype_size, the 2 counting
+    K and V.
+    """
+    return 2 * block_size * num_kv_heads * head_size * dtype_size
+
+
+def kv_bytes_per_token(num_layers: int, num_kv_heads: int, head_dim: int,
+                       dtype_size: int) -> int:
+    """KV bytes one token occupies over all layers.
+
+    “让 Agent 跑得快：LLM 推理服务”, §一 KV Cache: 2 × L × H × head_dim ×
+    dtype_size (H = KV heads).
+    """
+    return 2 * num_layers * num_kv_heads * head_dim * dtype_size
+
+
+def kv_cache_bytes(num_layers: int, num_kv_heads: int, head_dim: int,
+                   seq_len: int, batch: int, dtype_size: int) -> int:
+    """Whole KV cache of a batch.
+
+    “LLM 推理优化技术全景”, KV Cache 大小公式: 2 × n_layers × n_kv_heads ×
+    d_head × seq_len × batch × dtype_bytes.
+    """
+    return 2 * num_layers * num_kv_heads * head_dim * seq_len * batch * dtype_size
+
+
+def blocks_needed(seq_len: int, block_size: int) -> int:
+    """ceil(seq_len / block_size) (“LLM 推理引擎深度解析”, §2.1 allocate)."""
+    return (seq_len + block_size - 1) // block_size
+
+
+def internal_waste_tokens(seq_len: int, block_size: int) -> int:
+    """Unused token slots, all in the last block (“让 Agent 跑得快”, §五)."""
+    return blocks_needed(seq_len, block_size) * block_size - seq_len
+
+
+# --------------------------------------------------------------------------
+# Block pool model
+# --------------------------------------------------------------------------
+
+@dataclass
+class BlockPoolModel:
+    """Allocation rules of the physical block pool.
+
+    “LLM 推理引擎深度解析”, §2.1 (PagedKVCache): the pool starts with every
+    block id free in ascending order; allocation takes ids from the front of
+    the free list, all or none, and fails when too few are free; freeing
+    appends the ids to the back.  Freeing an id that is not allocated is an
+    error here (the page's sketch frees per sequence and never sees it).
+    """
+    num_blocks: int
+    free_list: list = field(default_factory=list)
+    allocated: set = field(default_factory=set)
+
+    def __post_init__(self):
+        self.free_list = list(range(self.num_blocks))
+
+    def alloc(self, n: int) -> list:
+        if n < 0:
+            raise ValueError("negative block count")
+        if len(self.free_list) < n:
+            raise MemoryError("block pool exhausted")
+        ids, self.free_list = self.free_list[:n], self.free_list[n:]
+        self.allocated.update(ids)
+        return ids
+
+    def alloc_sequence(self, seq_len: int, block_size: int) -> list:
+        return self.alloc(blocks_needed(seq_len, block_size))
+
+    def free(self, ids) -> None:
+        ids = list(ids)
+        if len(set(ids)) != len(ids) or any(i not in self.allocated for i in ids):
+            raise ValueError("freeing a block that is not allocated")
+        for i in ids:
+            self.allocated.discard(i)
+        self.free_list.extend(ids)
+
+    def stats(self):
+        return len(self.allocated), len(self.free_list)
+
+
+# --------------------------------------------------------------------------
+# Slot mapping and append
+# --------------------------------------------------------------------------
+
+def token_slots(block_tables, positions, block_size, num_blocks, seq_idx=None):
+    """slot = block_tables[s][p // bs] * bs + p % bs; -1 for p < 0 or a bad
+    index.  Returns (slots int64, status)."""
+    lib = _load()
+    bt = _c(block_tables, np.int32)
+    pos = _c(positions, np.int32)
+    si = None if seq_idx is None else _c(seq_idx, np.int32)
+    out = np.empty(pos.shape[0], np.int64)
+    rc = lib.oracle_token_slots(_ptr(bt), bt.shape[1], _ptr(si), _ptr(pos),
+                                pos.shape[0], block_size, num_blocks, _ptr(out))
+    return out, rc
+
+
+def append_bf16(k, v, k_cache, v_cache, slots):
+    """Copy bf16 bits of k, v [n, Hkv, d] into the pools (in place)."""
+    lib = _load()
+    k, v, s = _c(k, np.uint16), _c(v, np.uint16), _c(slots, np.int64)
+    nb, bs, hkv, d = k_cache.shape
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    return lib.oracle_append_bf16(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
+                                  _ptr(s), k.shape[0], nb, bs, hkv, d)
+
+
+def append_int8(k, v, k_cache, v_cache, k_scale, v_scale, slots):
+    """Store int8 codes of bf16 k, v under the slot's block scales."""
+    lib = _load()
+    k, v, s = _c(k, np.uint16), _c(v, np.uint16), _c(slots, np.int64)
+    ks, vs = _c(k_scale, np.float32), _c(v_scale, np.float32)
+    nb, bs, hkv, d = k_cache.shape
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    return lib.oracle_append_int8(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
+                                  _ptr(ks), _ptr(vs), _ptr(s), k.shape[0], nb,
+                                  bs, hkv, d)
+
+
+def quantize_int8(x: float, s: float) -> int:
+    """fp32 clamp(round_half_even(x / s), -127, 127); NaN -> 0; s = 0 -> 1."""
+    return _load().oracle_quantize_int8(float(x), float(s))
+
+
+# --------------------------------------------------------------------------
+# Attention
+# --------------------------------------------------------------------------
+
+def paged_attention(q, k_cache, v_cache, block_tables, seq_lens, scale, *,
+                    num_kv_heads=None, k_scale=None, v_scale=None, rows=None,
+                    mode="three_pass", threads=1):
+    """fp64 decode attention through the block table.
+
+    q: bf16 bits [B, Hq, d]; k_cache / v_cache: bf16 bits (uint16) or int8
+    [NB, bs, Hkv, d]; block_tables int32 [B, MB]; seq_lens int32 [B].
+    rows: optional int array [n, 2] of (b, h) to compute; default all, in
+    b-major order.  Returns (out fp64 [n, d] or [B, Hq, d], status).
+    """
+    lib = _load()
+    q = _c(q, np.uint16)
+    B, Hq, d = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    assert d2 == d and v_cache.shape == k_cache.shape
+    kv_int8 = k_cache.dtype == np.int8
+    if kv_int8:
+        k_scale, v_scale = _c(k_scale, np.float32), _c(v_scale, np.float32)
+    else:
+        assert k_cache.dtype == np.uint16
+    kc, vc = np.ascontiguousarray(k_cache), np.ascontiguousarray(v_cache)
+    bt, sl = _c(block_tables, np.int32), _c(seq_lens, np.int32)
+    r = None if rows is None else _c(rows, np.int32).reshape(-1, 2)
+    n = B * Hq if r is None else r.shape[0]
+    out = np.zeros((n, d), np.float64)
+    m = {"three_pass": 0, "online": 1}[mode]
+    rc = lib.oracle_paged_attention(
+        _ptr(out), _ptr(q), _ptr(kc), _ptr(vc),
+        _ptr(k_scale) if kv_int8 else None, _ptr(v_scale) if kv_int8 else None,
+        int(kv_int8), _ptr(bt), bt.shape[1], _ptr(sl), B, Hq, hkv, d, nb, bs,
+        float(scale), _ptr(r), n, m, int(threads))
+    if r is None:
+        out = out.reshape(B, Hq, d)
+    return out, rc
+
+
+def attention_partials(q, k_cache, v_cache, block_tables, seq_lens, scale, b, h,
+                       part, *, k_scale=None, v_scale=None):
+    """Per-partition (m_i, l_i) [np, 2] and unnormalised acc_i [np, d] of query
+    row (b, h), partitions of ``part`` consecutive logical tokens."""
+    lib = _load()
+    q = _c(q, np.uint16)
+    B, Hq, d = q.shape
+    nb, bs, hkv, _ = k_cache.shape
+    kv_int8 = k_cache.dtype == np.int8
+    if kv_int8:
+        k_scale, v_scale = _c(k_scale, np.float32), _c(v_scale, np.float32)
+    kc, vc = np.ascontiguousarray(k_cache), np.ascontiguousarray(v_cache)
+    bt, sl = _c(block_tables, np.int32), _c(seq_lens, np.int32)
+    npart = (int(sl[b]) + part - 1) // part
+    ml = np.zeros((max(npart, 1), 2), np.float64)
+    acc = np.zeros((max(npart, 1), d), np.float64)
+    rc = lib.oracle_attention_partials(
+        _ptr(ml), _ptr(acc), _ptr(q), _ptr(kc), _ptr(vc),
+        _ptr(k_scale) if kv_int8 else None, _ptr(v_scale) if kv_int8 else None,
+        int(kv_int8), _ptr(bt), bt.shape[1], _ptr(sl), B, Hq, hkv, d, nb, bs,
+        float(scale), int(b), int(h), int(part))
+    if rc < 0:
+        raise ValueError(f"oracle_attention_partials failed ({-rc})")
+    return ml[:rc], acc[:rc]
+
+
+def lse_merge(ml, acc):
+    """o = sum_i exp(m_i - M) acc_i / sum_i exp(m_i - M) l_i, M = max m_i."""
+    lib = _load()
+    ml, acc = _c(ml, np.float64), _c(acc, np.float64)
+    out = np.zeros(acc.shape[1], np.float64)
+    lib.oracle_lse_merge(_ptr(ml), _ptr(acc), ml.shape[0], acc.shape[1], _ptr(out))
+    return out
+
+
+def bf16_bits_to_float(a) -> np.ndarray:
+    """Widen bf16 bits (uint16) to float32 exactly."""
+    return (np.asarray(a, np.uint16).astype(np.uint32) << 16).view(np.float32)

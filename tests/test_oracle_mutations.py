@@ -1,0 +1,71 @@
+"""Planted mistakes: each test compiles a copy of the C oracle with one
+plausible mistake (a wrong index, a dropped term, a swapped operand, another
+rounding) and checks that the pins reject it.  The mistakes are planted in
+the oracle, on the CPU, in a temporary copy; the real oracle is untouched."""
+import ctypes
+import subprocess
+
+import pytest
+
+import oracle
+from test_oracle_append import check_fp32_decision, check_rounding
+from test_oracle_attention import check_against_sdpa, check_int8_against_sdpa, small
+
+
+def _sdpa():
+    check_against_sdpa(small([1, 2, 3, 15, 16, 17, 31, 33, 100, 250], hq=8, hkv=2, d=64, bs=16, seed=11))
+
+
+def _sdpa_int8():
+    check_int8_against_sdpa(small([1, 5, 32, 33, 70, 200], hq=16, hkv=2, d=128, bs=32, kv="int8", seed=3))
+
+
+def _rounding():
+    check_rounding(oracle.quantize_int8)
+
+
+def _fp32():
+    check_fp32_decision(oracle.quantize_int8)
+
+
+MUTANTS = {
+    "gqa_modulo_mapping": ("int hk = h / (P->num_q_heads / P->num_kv_heads);",
+                           "int hk = h % P->num_kv_heads;", _sdpa),
+    "row_off_by_one": ("K[(int64_t)t * d + e] = pool_value(P, 0, block, t % bs, hk, e);",
+                       "K[(int64_t)t * d + e] = pool_value(P, 0, block, (t + 1) % bs, hk, e);", _sdpa),
+    "scale_dropped": ("s[t] = P->scale * acc;", "s[t] = acc;", _sdpa),
+    "v_reads_k": ("V[(int64_t)t * d + e] = pool_value(P, 1, block",
+                  "V[(int64_t)t * d + e] = pool_value(P, 0, block", _sdpa),
+    "last_token_dropped": ("for (int t = 0; t < L; ++t) {\n        double w = exp(s[t] - m) / Z;",
+                           "for (int t = 0; t < L - 1; ++t) {\n        double w = exp(s[t] - m) / Z;", _sdpa),
+    "table_index_transposed": ("P->block_tables[(int64_t)b * P->max_blocks + t / bs]",
+                               "P->block_tables[(int64_t)b * P->max_blocks + t % bs]", _sdpa),
+    "slot_row_wrong": ("slots[i] = (int64_t)physical * block_size + (p % block_size);",
+                       "slots[i] = (int64_t)physical * block_size + (p / block_size);", _sdpa),
+    "sum_sign_flipped": ("Z += exp(s[t] - m);", "Z += exp(m - s[t]);", _sdpa),
+    "dequant_scale_dropped": ("return (double)c[idx] * (double)s[(int64_t)block * P->num_kv_heads + hk];",
+                              "return (double)c[idx];", _sdpa_int8),
+    "round_half_away": ("float r = nearbyintf(x / s);", "float r = roundf(x / s);", _rounding),
+    "fp64_decision": ("float r = nearbyintf(x / s);",
+                      "float r = (float)nearbyint((double)x / (double)s);", _fp32),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(oracle_mod, tmp_path, name):
+    old, new, check = MUTANTS[name]
+    src = open(oracle._SRC).read()
+    assert src.count(old) == 1, "mutation site not found"
+    c = tmp_path / "mutant.c"
+    c.write_text(src.replace(old, new))
+    so = tmp_path / "mutant.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off",
+                    "-D_GNU_SOURCE", "-o", str(so), str(c), "-lm"], check=True)
+    check()                                   # the real oracle passes
+    saved = oracle._lib
+    oracle._lib = oracle._bind(ctypes.CDLL(str(so)))
+    try:
+        with pytest.raises(AssertionError):
+            check()
+    finally:
+        oracle._lib = saved

@@ -1,0 +1,267 @@
+"""Seeded synthetic decode batches for paged attention (inputs only).
+
+This module draws inputs and nothing else: sequence lengths, the random
+physical placement of each sequence's blocks, q, the K/V values of every
+cached token, the new token's k/v and (for int8 pools) the per-(block, KV
+head) scales.  It holds none of the method's arithmetic: it never computes a
+slot, never writes a pool, never quantises and never attends.  Each side of a
+parity check (the CUDA path, the CPU oracle) fills its own pool from the
+``fill_chunks`` this module yields, with its own slot mapping and append.
+
+Workloads follow the shapes of the pages' examples (Llama-3.1-8B-like GQA with
+32 query / 8 KV heads and head_dim 128; a Llama-2-70B-like 64 / 8 layout; a
+shared 800-token system prompt; 16-token blocks, 32 for the int8 case):
+
+  1 tiny           B 4,   8/2 heads,  d 64,  bs 16, L ~ U{1..200}, pool 64 blocks
+  2 8B-like        B 64,  32/8 heads, d 128, bs 16, L ~ U{512..4096}
+  3 long split-K   B 8,   32/8 heads, d 128, bs 16, L ~ U{32768..131072}
+  4 shared prefix  B 256, 32/8 heads, d 128, bs 16, L = 800 + clip(round(
+                   lognormal(6, 1)), 16, 2048); blocks 0..49 shared by all
+  5 70B-like INT8  B 128, 64/8 heads, d 128, bs 32, L ~ U{1024..8192},
+                   int8 pool, scale = max|x| / 127 per (block, KV head)
+
+Recipe: ``numpy.random.Generator(PCG64)`` streams spawned from
+``SeedSequence(20260000 + config)``: stream 0 draws lengths then placement,
+stream 1 draws q, stream 2 the new tokens' k and v, stream 3 a shared prefix,
+and stream 4 + b the cached tokens of sequence b (so one sequence can be
+regenerated alone).  Values are N(0, 1) in fp32 rounded to the nearest-even
+bf16.  The pool holds ceil(1.25 x needed blocks) unless the config fixes it;
+placement is a seeded random permutation of the pool, each sequence taking
+the next ``ceil(L_b / bs)`` entries.  Unused pool memory starts poisoned
+(bf16 NaN, int8 127) and table padding is -1.  ``L_b`` counts the token
+appended in this step; cached tokens are positions ``0 .. L_b - 2``.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+from typing import Iterator, Optional, Sequence
+
+import numpy as np
+
+BF16_NAN = np.uint16(0x7FC0)
+INT8_POISON = np.int8(127)
+SEED_BASE = 20260000
+
+
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round fp32 to the nearest-even bf16 and return the 16-bit patterns."""
+    u = np.ascontiguousarray(x, np.float32).view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    return ((u + np.uint32(0x7FFF) + lsb) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (np.asarray(b, np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+@dataclass
+class Spec:
+    name: str
+    batch: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    kv_dtype: str                      # "bf16" | "int8"
+    lens: tuple                        # ("uniform", lo, hi) | ("prefix_lognormal", ...) | ("fixed", [..])
+    num_blocks: Optional[int] = None   # None: ceil(1.25 * needed)
+    max_blocks_per_seq: Optional[int] = None
+    shared_prefix_tokens: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+
+CONFIGS = {
+    1: Spec("tiny paged decode (B4, 8/2 heads, d64, bs16, L 1..200, 64 blocks)",
+            4, 8, 2, 64, 16, "bf16", ("uniform", 1, 200), num_blocks=64,
+            max_blocks_per_seq=13),
+    2: Spec("Llama-3.1-8B-like decode layer (B64, 32/8 heads, d128, bs16, L 512..4096)",
+            64, 32, 8, 128, 16, "bf16", ("uniform", 512, 4096),
+            max_blocks_per_seq=256),
+    3: Spec("long-context split-K (B8, 32/8 heads, d128, bs16, L 32768..131072)",
+            8, 32, 8, 128, 16, "bf16", ("uniform", 32768, 131072),
+            max_blocks_per_seq=8192),
+    4: Spec("shared-prefix mixed batch (B256, 32/8 heads, d128, bs16, 800-token shared prefix)",
+            256, 32, 8, 128, 16, "bf16", ("prefix_lognormal", 6.0, 1.0, 16, 2048),
+            max_blocks_per_seq=(800 + 2048 + 15) // 16, shared_prefix_tokens=800),
+    5: Spec("Llama-2-70B-like INT8 KV (B128, 64/8 heads, d128, bs32, L 1024..8192)",
+            128, 64, 8, 128, 32, "int8", ("uniform", 1024, 8192),
+            max_blocks_per_seq=256),
+}
+
+
+@dataclass
+class FillChunk:
+    """Cached tokens to append before the decode step: token i belongs to
+    sequence ``seq_idx[i]`` at position ``positions[i]``."""
+    seq_idx: np.ndarray    # int32 [n]
+    positions: np.ndarray  # int32 [n]
+    k: np.ndarray          # bf16 bits [n, Hkv, d]
+    v: np.ndarray
+
+
+class Workload:
+    """One synthetic decode step."""
+
+    def __init__(self, spec: Spec, seed: int, seq_lens: Optional[Sequence[int]] = None):
+        self.spec = spec
+        self.seed = seed
+        ss = np.random.SeedSequence(seed)
+        self._children = ss.spawn(4)
+        self._seq_root = self._children[3]
+        s0 = np.random.Generator(np.random.PCG64(self._children[0]))
+        B, bs = spec.batch, spec.block_size
+        P = spec.shared_prefix_tokens
+        if seq_lens is not None:
+            lens = np.asarray(seq_lens, np.int64)
+            assert lens.shape == (B,)
+        elif spec.lens[0] == "uniform":
+            lens = s0.integers(spec.lens[1], spec.lens[2], size=B, endpoint=True)
+        elif spec.lens[0] == "prefix_lognormal":
+            _, mu, sigma, lo, hi = spec.lens
+            suffix = np.clip(np.rint(s0.lognormal(mu, sigma, size=B)), lo, hi)
+            lens = P + suffix.astype(np.int64)
+        else:
+            raise ValueError(spec.lens)
+        self.seq_lens = lens.astype(np.int32)
+        nblk = [(int(L) + bs - 1) // bs for L in self.seq_lens]
+        shared = P // bs
+        needed = sum(nblk) - shared * max(B - 1, 0) if shared else sum(nblk)
+        NB = spec.num_blocks or int(math.ceil(1.25 * needed))
+        self.num_blocks = NB
+        MB = spec.max_blocks_per_seq or max(max(nblk), 1)
+        assert max(nblk) <= MB, "a sequence needs more blocks than the table holds"
+        self.max_blocks_per_seq = MB
+        perm = s0.permutation(NB).astype(np.int32)
+        bt = np.full((B, MB), -1, np.int32)
+        nxt = shared
+        for b in range(B):
+            bt[b, :shared] = perm[:shared]
+            own = nblk[b] - shared
+            bt[b, shared:nblk[b]] = perm[nxt:nxt + own]
+            nxt += own
+        assert nxt <= NB
+        self.block_tables = bt
+        s1 = np.random.Generator(np.random.PCG64(self._children[1]))
+        self.q = to_bf16_bits(s1.standard_normal((B, spec.num_q_heads, spec.head_dim), np.float32))
+        s2 = np.random.Generator(np.random.PCG64(self._children[2]))
+        shp = (B, spec.num_kv_heads, spec.head_dim)
+        self.new_k = to_bf16_bits(s2.standard_normal(shp, np.float32))
+        self.new_v = to_bf16_bits(s2.standard_normal(shp, np.float32))
+        self._prefix = None
+        self._scales = None
+
+    # -- shapes ----------------------------------------------------------
+    @property
+    def pool_shape(self):
+        s = self.spec
+        return (self.num_blocks, s.block_size, s.num_kv_heads, s.head_dim)
+
+    @property
+    def kv_elem_bytes(self) -> int:
+        return 1 if self.spec.kv_dtype == "int8" else 2
+
+    def poisoned_pool(self) -> np.ndarray:
+        if self.spec.kv_dtype == "int8":
+            return np.full(self.pool_shape, INT8_POISON, np.int8)
+        return np.full(self.pool_shape, BF16_NAN, np.uint16)
+
+    # -- cached token values ---------------------------------------------
+    def _stream(self, which: int) -> np.random.Generator:
+        child = np.random.SeedSequence(self.seed, spawn_key=(3, which))
+        return np.random.Generator(np.random.PCG64(child))
+
+    def _prefix_kv(self):
+        if self._prefix is None:
+            P, s = self.spec.shared_prefix_tokens, self.spec
+            g = self._stream(0)
+            shp = (P, s.num_kv_heads, s.head_dim)
+            self._prefix = (to_bf16_bits(g.standard_normal(shp, np.float32)),
+                            to_bf16_bits(g.standard_normal(shp, np.float32)))
+        return self._prefix
+
+    def own_tokens(self, b: int):
+        """Cached tokens that sequence b alone owns: (positions, k, v)."""
+        s = self.spec
+        P = s.shared_prefix_tokens
+        L = int(self.seq_lens[b])
+        lo, hi = min(P, L - 1), L - 1
+        n = max(hi - lo, 0)
+        g = self._stream(1 + b)
+        shp = (n, s.num_kv_heads, s.head_dim)
+        k = to_bf16_bits(g.standard_normal(shp, np.float32))
+        v = to_bf16_bits(g.standard_normal(shp, np.float32))
+        return np.arange(lo, hi, dtype=np.int32), k, v
+
+    def fill_chunks(self, seqs: Optional[Sequence[int]] = None) -> Iterator[FillChunk]:
+        """Chunks of cached tokens to append before the step (the shared
+        prefix once, through sequence 0's table, then each sequence's own)."""
+        s = self.spec
+        seqs = range(s.batch) if seqs is None else seqs
+        P = s.shared_prefix_tokens
+        if P:
+            pk, pv = self._prefix_kv()
+            first = 0 if seqs is None else min(seqs)
+            yield FillChunk(np.full(P, first, np.int32), np.arange(P, dtype=np.int32), pk, pv)
+        for b in seqs:
+            pos, k, v = self.own_tokens(b)
+            if pos.size:
+                yield FillChunk(np.full(pos.size, b, np.int32), pos, k, v)
+
+    # -- int8 scales -------------------------------------------------------
+    def scales(self, seqs: Optional[Sequence[int]] = None):
+        """fp32 k_scale, v_scale [NB, Hkv]: max |x| / 127 over the bf16 values
+        (cached plus new) that land in each (block, KV head); 1.0 elsewhere."""
+        s = self.spec
+        NB, H, bs = self.num_blocks, s.num_kv_heads, s.block_size
+        ks = np.ones((NB, H), np.float32)
+        vs = np.ones((NB, H), np.float32)
+        seqs = range(s.batch) if seqs is None else seqs
+        assert s.shared_prefix_tokens == 0, "int8 workloads have no shared prefix"
+        for b in seqs:
+            L = int(self.seq_lens[b])
+            pos, k, v = self.own_tokens(b)
+            kf = np.concatenate([bf16_bits_to_f32(k), bf16_bits_to_f32(self.new_k[b:b + 1])])
+            vf = np.concatenate([bf16_bits_to_f32(v), bf16_bits_to_f32(self.new_v[b:b + 1])])
+            nblk = (L + bs - 1) // bs
+            pad = nblk * bs - L
+            kf = np.abs(np.concatenate([kf, np.zeros((pad,) + kf.shape[1:], np.float32)]))
+            vf = np.abs(np.concatenate([vf, np.zeros((pad,) + vf.shape[1:], np.float32)]))
+            kmax = kf.reshape(nblk, bs, H, -1).max(axis=(1, 3))
+            vmax = vf.reshape(nblk, bs, H, -1).max(axis=(1, 3))
+            phys = self.block_tables[b, :nblk]
+            ks[phys] = np.where(kmax > 0, kmax / np.float32(127.0), np.float32(1.0))
+            vs[phys] = np.where(vmax > 0, vmax / np.float32(127.0), np.float32(1.0))
+        return ks, vs
+
+    # -- byte accounting -----------------------------------------------------
+    def kv_bytes_logical(self) -> int:
+        """K and V bytes the step reads, counting shared blocks per reader."""
+        s = self.spec
+        return int(self.seq_lens.astype(np.int64).sum()) * 2 * s.num_kv_heads * s.head_dim * self.kv_elem_bytes
+
+    def kv_bytes_unique(self) -> int:
+        """K and V bytes of distinct cached tokens (a shared prefix once)."""
+        s = self.spec
+        P = s.shared_prefix_tokens
+        toks = int(self.seq_lens.astype(np.int64).sum()) - P * max(s.batch - 1, 0)
+        return toks * 2 * s.num_kv_heads * s.head_dim * self.kv_elem_bytes
+
+
+def make(config: int, seed: Optional[int] = None, seq_lens=None) -> Workload:
+    spec = CONFIGS[config]
+    return Workload(spec, SEED_BASE + config if seed is None else seed, seq_lens)
+
+
+def custom(*, batch, num_q_heads, num_kv_heads, head_dim, block_size, seq_lens,
+           kv_dtype="bf16", num_blocks=None, max_blocks_per_seq=None,
+           shared_prefix_tokens=0, seed=1234) -> Workload:
+    """A small workload with explicit lengths (tests: edge cases)."""
+    spec = Spec("custom", batch, num_q_heads, num_kv_heads, head_dim, block_size,
+                kv_dtype, ("fixed",), num_blocks=num_blocks,
+                max_blocks_per_seq=max_blocks_per_seq,
+                shared_prefix_tokens=shared_prefix_tokens)
+    return Workload(spec, seed, seq_lens=seq_lens)
