@@ -1,0 +1,389 @@
+#!/usr/bin/env python3
+"""Decode-step benchmark of paged attention on GB300.
+
+One step = the whole hot path over one synthetic decode batch: slot mapping
+of each sequence's new token, the append (reshape_and_cache), and the paged
+attention (per-partition decode kernel + log-sum-exp merge when a sequence
+spans several partitions).  The default workload is the Llama-3.1-8B-like
+decode layer (B 64, 32/8 heads, d 128, 16-token blocks, lengths U{512..4096}).
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+the same workload instead (the reference arm: a plain fp64 program, not a
+target).  Timing: CUDA events on the launching stream, W warm-up steps, K
+timed steps, barrier + synchronize on both sides, max over ranks.  The KV
+read per step (~600 MB) is larger than the 129 MB L2, so no flush is needed.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "paged decode attention: KV-read GB/s & % of GB300 HBM peak; µs per decode step"
+UNIT = "GB/s"
+DEFAULT_CONFIG = 2
+FALLBACK_HBM_GBS = 6800.0
+DECODE_SOURCE = os.path.join(ROOT, "paged_kv_cache_97_gb300", "csrc", "pagedkv_decode.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
+
+
+# ---------------------------------------------------------------------------
+# Byte accounting (algorithmic bytes per step)
+# ---------------------------------------------------------------------------
+
+def algorithmic_bytes(wl) -> dict:
+    """Bytes the step must move at minimum: K/V of every attended token (a
+    shared prefix counted once: it is read once from HBM and then hits L2),
+    int8 scales, the block-table entries in use, q and out, and the append's
+    reads and writes."""
+    s = wl.spec
+    elem = wl.kv_elem_bytes
+    B, hq, hkv, d, bs = s.batch, s.num_q_heads, s.num_kv_heads, s.head_dim, s.block_size
+    L = wl.seq_lens.astype(np.int64)
+    blocks = int(((L + bs - 1) // bs).sum())
+    kv_unique = wl.kv_bytes_unique()
+    scales = blocks * 2 * hkv * 4 if s.kv_dtype == "int8" else 0
+    qo = 2 * B * hq * d * 2
+    table = blocks * 4 + B * 4
+    append = B * hkv * d * 2 * 2 + B * hkv * d * elem * 2 + B * 8 * 2
+    attn = kv_unique + scales + qo + table
+    return {"kv_logical": wl.kv_bytes_logical(), "kv_unique": kv_unique, "attention": attn,
+            "step": attn + append}
+
+
+# ---------------------------------------------------------------------------
+# Clocks during the timed region (NVML through ctypes; reading only)
+# ---------------------------------------------------------------------------
+
+REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+           0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+           0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+           0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    def __init__(self, uuid: str, period_s: float = 0.02):
+        self.samples, self.max_mhz, self.reasons = [], None, set()
+        self.period, self._stop, self._t, self.error = period_s, threading.Event(), None, None
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            assert self.nvml.nvmlInit_v2() == 0
+            self.h = ctypes.c_void_p()
+            u = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            assert self.nvml.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(self.h)) == 0
+            m = ctypes.c_uint()
+            assert self.nvml.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(m)) == 0
+            self.max_mhz = m.value
+        except Exception as e:  # noqa: BLE001 - clocks are reported, not required
+            self.error = f"nvml unavailable: {e!r}"
+
+    def _run(self):
+        c, r = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c)) == 0:
+                self.samples.append(c.value)
+            fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+            if fn(self.h, ctypes.byref(r)) == 0:
+                for bit, name in REASONS.items():
+                    if r.value & bit and bit != 0x1:
+                        self.reasons.add(name)
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.error is None:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self._t:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if self.error:
+            return {"error": self.error}
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------------------
+# Ranks (replicas: every rank runs its own batch; no collective on the data path)
+# ---------------------------------------------------------------------------
+
+def rank_info():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def aggregate(elapsed_s: float, units_per_rank: float, world: int, dist=None):
+    """Max time over ranks; whole-job throughput = units all ranks processed
+    / that time."""
+    if world > 1:
+        import torch
+        t = torch.tensor([elapsed_s], dtype=torch.float64)
+        if dist.get_backend() == "nccl":
+            t = t.cuda()
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_s = float(t.item())
+    return elapsed_s, units_per_rank * world / elapsed_s
+
+
+# ---------------------------------------------------------------------------
+# Oracle (CPU baseline / reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_pools(wl):
+    """The oracle's own pools for the whole batch (setup, not timed)."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle
+    from oracle_helpers import oracle_pool
+    oracle.build()
+    return oracle_pool(wl)
+
+
+def oracle_time(wl, pools, seqs, threads):
+    """Time the oracle's attention over every query head of ``seqs``.
+    Returns (seconds, KV bytes attended)."""
+    import oracle
+    kc, vc, ks, vs = pools
+    rows = np.array([(b, h) for b in seqs for h in range(wl.spec.num_q_heads)], np.int32)
+    t0 = time.perf_counter()
+    _, rc = oracle.paged_attention(wl.q, kc, vc, wl.block_tables, wl.seq_lens, wl.spec.scale,
+                                   k_scale=ks, v_scale=vs, rows=rows, threads=threads)
+    dt = time.perf_counter() - t0
+    assert rc == 0
+    s = wl.spec
+    kv = int(wl.seq_lens[list(seqs)].astype(np.int64).sum()) * 2 * s.num_kv_heads * s.head_dim * wl.kv_elem_bytes
+    return dt, kv
+
+
+def oracle_sample(wl, threads, target_s=10.0, max_s=30.0):
+    """Time the oracle on growing prefixes of the batch until ~target_s of
+    work (bounded by max_s): returns a cpu_baseline dict."""
+    pools = oracle_pools(wl)
+    n = 2
+    while True:
+        seqs = list(range(min(n, wl.spec.batch)))
+        dt, kv = oracle_time(wl, pools, seqs, threads)
+        if dt >= target_s or len(seqs) == wl.spec.batch or dt * 2 > max_s:
+            break
+        n = min(wl.spec.batch, max(n + 1, int(n * target_s / max(dt, 1e-3))))
+    return {"value": round(kv / dt / 1e9, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{len(seqs)} of {wl.spec.batch} sequences, all {wl.spec.num_q_heads} query heads "
+                      f"({kv / 1e6:.1f} MB of KV), fp64 three-pass oracle, {dt:.2f} s"}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def source_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def stored_traffic(workload_name):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken
+    on the current decode kernel source and this workload; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if t.get("source_sha256_16") != source_hash(DECODE_SOURCE) or t.get("workload") != workload_name:
+        return None
+    return t.get("dram_bytes_per_launch")
+
+
+def measured_peak_gbs():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def gpu_arm(args, rank, world, local_rank, dist):
+    import torch
+
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import paged_kv_cache_97_gb300 as pkv
+    from gpu_helpers import GpuStep
+    pkv.load()
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = workloads.make(args.config)
+    g = GpuStep(wl, dev=dev)
+    s = wl.spec
+    stream = torch.cuda.current_stream(dev)
+    nbytes = algorithmic_bytes(wl)
+    part = pkv.partition_tokens(s.batch, s.num_kv_heads, g.max_seq_len, s.block_size)
+    merge = g.max_seq_len > part
+    launches_per_step = 3 + (1 if merge else 0)
+
+    for _ in range(args.warmup):
+        g.step()
+    torch.cuda.synchronize(dev)
+    st, flags = pkv.get_status()
+    assert st == 0, f"device status 0x{flags:x}"
+
+    # ---- device-resident timed region ---------------------------------
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(torch.cuda.get_device_properties(dev).uuid.__str__())
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with sampler:
+        for i in range(K):
+            ev[i][0].record(stream)
+            g.append()
+            ev[i][1].record(stream)
+            g.attend()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    total_ms = ev[0][0].elapsed_time(ev[-1][2])
+    attn_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    ms_step = total_ms / K
+    elapsed, agg_bytes_per_s = aggregate(total_ms / 1e3, nbytes["kv_logical"] * K, world, dist)
+    value = agg_bytes_per_s / 1e9
+    st, flags = pkv.get_status()
+    assert st == 0, f"device status 0x{flags:x}"
+
+    # ---- end to end through the public API, host buffers -----------------
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    h_q = pin(wl.q.view(np.int16)).view(torch.bfloat16)
+    h_k = pin(wl.new_k.view(np.int16)).view(torch.bfloat16)
+    h_v = pin(wl.new_v.view(np.int16)).view(torch.bfloat16)
+    h_bt = pin(wl.block_tables)
+    h_sl = pin(wl.seq_lens)
+    h_out = torch.empty(g.out.shape, dtype=torch.bfloat16).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_bt, h_sl))
+    d2h = h_out.numel() * h_out.element_size()
+    K2 = max(args.steps // 4, 10)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(K2):
+        g.q.copy_(h_q, non_blocking=True)
+        g.new_k.copy_(h_k, non_blocking=True)
+        g.new_v.copy_(h_v, non_blocking=True)
+        g.block_tables.copy_(h_bt, non_blocking=True)
+        g.seq_lens.copy_(h_sl, non_blocking=True)
+        g.step()
+        h_out.copy_(g.out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / K2
+    _, e2e_agg = aggregate(e2e_ms / 1e3, nbytes["kv_logical"], world, dist)
+
+    peak, peak_kind = measured_peak_gbs()
+    attn_mean_ms = statistics.fmean(attn_ms)
+    achieved = nbytes["attention"] / (attn_mean_ms / 1e3) / 1e9
+    traffic = stored_traffic(s.name)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "us_per_step": round(ms_step * 1e3, 2),
+        "pct_of_hbm_peak": round(100 * value / world / peak, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if s.kv_dtype == "bf16" else "int8 KV, bf16 q/out, fp32 accumulate",
+        "data": "synthetic",
+        "config": {"workload": s.name, "batch": s.batch, "num_q_heads": s.num_q_heads,
+                   "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim,
+                   "block_size": s.block_size, "kv_dtype": s.kv_dtype,
+                   "seq_lens": f"seed {wl.seed}: min {int(wl.seq_lens.min())}, "
+                               f"mean {float(wl.seq_lens.mean()):.0f}, max {int(wl.seq_lens.max())}",
+                   "kv_bytes_per_step": nbytes["kv_logical"], "partition_tokens": part,
+                   "l2": "inputs larger than L2 (KV read per step > 129 MB), no flush",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "paged_attention_decode (decode + merge launches)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": nbytes["attention"],
+                     "us_per_launch": round(attn_mean_ms * 1e3, 2), "traffic": traffic},
+        "e2e": {"value": round(e2e_agg / 1e9, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
+        "gpu_launches": launches_per_step * K,
+        "clocks": sampler.summary(),
+    }
+    return line, wl
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=sorted(workloads.CONFIGS),
+                    help="workload (default 2: the Llama-3.1-8B-like decode layer)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local_rank = rank_info()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        wl = workloads.make(args.config)
+        threads = os.cpu_count() or 1
+        pools = oracle_pools(wl)
+        per_step = []
+        for i in range(args.warmup + args.steps):
+            # each step is a bounded sample: one sequence (cycling), all its query heads
+            dt, kv = oracle_time(wl, pools, [i % wl.spec.batch], threads)
+            if i >= args.warmup:
+                per_step.append((dt, kv))
+        t = sum(d for d, _ in per_step)
+        kv = sum(k for _, k in per_step)
+        v = kv / t / 1e9
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": wl.spec.name},
+            "cpu_baseline": {"value": round(v, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": "per step: one sequence of the batch (cycling), all query heads, "
+                                       "fp64 three-pass oracle"},
+            "e2e": {"value": round(v, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }), flush=True)
+        return 0
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    line, wl = gpu_arm(args, rank, world, local_rank, dist)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_sample(wl, os.cpu_count() or 1)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

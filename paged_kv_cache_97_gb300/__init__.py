@@ -1,0 +1,271 @@
+"""paged_kv_cache_97_gb300 -- decode-phase paged attention on one GB300 GPU.
+
+A thin ctypes binding over ``libpagedkv.so`` (C ABI in ``include/pagedkv.h``):
+argument marshalling only.  Every step runs in the library's CUDA kernels;
+PyTorch provides device memory and streams.  There is no CPU fallback: if the
+library is not built, the first call raises.
+
+    import paged_kv_cache_97_gb300 as pkv
+    pkv.slot_mapping(block_tables, seq_lens, num_blocks, block_size, out=slots)
+    pkv.reshape_and_cache(k, v, k_cache, v_cache, slots)
+    pkv.paged_attention_decode(out, q, k_cache, v_cache, block_tables, seq_lens,
+                               max_seq_len, scale, workspace=ws)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+LIB_PATH = _build.LIB_PATH
+
+KV_OK, KV_ERR_INVALID_ARG, KV_ERR_OUT_OF_BLOCKS, KV_ERR_CUDA, KV_ERR_DEVICE_INDEX, \
+    KV_ERR_NOT_IMPLEMENTED = range(6)
+DTYPE_BF16, DTYPE_INT8 = 0, 1
+FLAG_BAD_SLOT, FLAG_BAD_BLOCK, FLAG_BAD_SEQ_LEN, FLAG_WAIT_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+
+# Every symbol include/pagedkv.h declares, with its ctypes signature.
+_P, _I, _SZ, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+SIGNATURES = {
+    "kv_pool_create": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_P)]),
+    "kv_pool_destroy": (None, [_P]),
+    "kv_pool_block_bytes": (_SZ, [_P]),
+    "kv_pool_alloc": (_I, [_P, _I, _P]),
+    "kv_pool_free": (_I, [_P, _P, _I]),
+    "kv_pool_stats": (_I, [_P, _P, _P]),
+    "pagedkv_pool_tensor_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "pagedkv_slot_mapping": (_I, [_P, _I, _P, _I, _I, _I, _P, _P]),
+    "pagedkv_token_slot_mapping": (_I, [_P, _I, _P, _P, _I, _I, _I, _P, _P]),
+    "reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "pagedkv_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "paged_attention_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I,
+                                    _I, _F, _I, _P, _SZ, _P]),
+    "pagedkv_get_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
+    "pagedkv_last_error": (ctypes.c_char_p, []),
+    "pagedkv_partition_tokens": (_I, [_I, _I, _I, _I]),
+}
+
+_lib = None
+
+
+class KVError(RuntimeError):
+    """A libpagedkv call returned a status other than KV_OK."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"libpagedkv status {status}: {message}")
+        self.status = status
+
+
+def load(path: str = LIB_PATH):
+    """Load libpagedkv.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path == LIB_PATH:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with "
+                          "`python -c 'import __graft_entry__ as g; g.build()'` (needs nvcc)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path == LIB_PATH:
+        _lib = lib
+    return lib
+
+
+def _check(st: int):
+    if st != KV_OK:
+        raise KVError(st, load().pagedkv_last_error().decode(errors="replace"))
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, dtype, name, ndim=None):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got {tuple(t.shape)}")
+
+
+def _pool_dtype(k_cache):
+    import torch
+    if k_cache.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    if k_cache.dtype == torch.int8:
+        return DTYPE_INT8
+    raise TypeError("pools must be torch.bfloat16 or torch.int8")
+
+
+# --------------------------------------------------------------------------
+# Block pool
+# --------------------------------------------------------------------------
+
+class KVPool:
+    """Host bookkeeping of a block pool (free list, FIFO, all-or-nothing)."""
+
+    def __init__(self, num_blocks: int, block_size: int, num_kv_heads: int, head_dim: int,
+                 dtype: int = DTYPE_BF16):
+        self._lib = load()
+        h = ctypes.c_void_p()
+        _check(self._lib.kv_pool_create(num_blocks, block_size, num_kv_heads, head_dim, dtype,
+                                        ctypes.byref(h)))
+        self._h = h
+
+    def close(self):
+        if self._h:
+            self._lib.kv_pool_destroy(self._h)
+            self._h = None
+
+    __del__ = close
+
+    def block_bytes(self) -> int:
+        return self._lib.kv_pool_block_bytes(self._h)
+
+    def alloc(self, n: int) -> list:
+        ids = (ctypes.c_int32 * max(n, 1))()
+        _check(self._lib.kv_pool_alloc(self._h, n, ids))
+        return list(ids[:n])
+
+    def free(self, ids) -> None:
+        ids = list(ids)
+        arr = (ctypes.c_int32 * max(len(ids), 1))(*ids)
+        _check(self._lib.kv_pool_free(self._h, arr, len(ids)))
+
+    def stats(self):
+        used, free = ctypes.c_int(), ctypes.c_int()
+        _check(self._lib.kv_pool_stats(self._h, ctypes.byref(used), ctypes.byref(free)))
+        return used.value, free.value
+
+
+def pool_tensor_bytes(num_blocks, block_size, num_kv_heads, head_dim, dtype=DTYPE_BF16) -> int:
+    return load().pagedkv_pool_tensor_bytes(num_blocks, block_size, num_kv_heads, head_dim, dtype)
+
+
+# --------------------------------------------------------------------------
+# Kernels
+# --------------------------------------------------------------------------
+
+def slot_mapping(block_tables, seq_lens, num_blocks, block_size, out, stream=None):
+    """Slots of each sequence's new token (position seq_lens[b] - 1) into ``out``."""
+    import torch
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _need(out, torch.int64, "out", 1)
+    B = seq_lens.shape[0]
+    if block_tables.shape[0] != B or out.shape[0] != B:
+        raise ValueError("block_tables, seq_lens and out disagree on the batch size")
+    _check(load().pagedkv_slot_mapping(_ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B,
+                                       block_size, num_blocks, _ptr(out), _stream(stream)))
+    return out
+
+
+def token_slot_mapping(block_tables, positions, num_blocks, block_size, out, seq_idx=None,
+                       stream=None):
+    """Slots of tokens (seq_idx[i], positions[i]) into ``out``."""
+    import torch
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(positions, torch.int32, "positions", 1)
+    _need(out, torch.int64, "out", 1)
+    n = positions.shape[0]
+    if seq_idx is not None:
+        _need(seq_idx, torch.int32, "seq_idx", 1)
+        if seq_idx.shape[0] != n:
+            raise ValueError("seq_idx and positions disagree")
+    if out.shape[0] != n:
+        raise ValueError("out and positions disagree")
+    _check(load().pagedkv_token_slot_mapping(_ptr(block_tables), block_tables.shape[1], _ptr(seq_idx),
+                                             _ptr(positions), n, block_size, num_blocks, _ptr(out),
+                                             _stream(stream)))
+    return out
+
+
+def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, k_scale=None, v_scale=None,
+                      stream=None):
+    """Append bf16 k, v [n, Hkv, d] into pools [NB, bs, Hkv, d] at the slots."""
+    import torch
+    _need(k, torch.bfloat16, "k", 3)
+    _need(v, torch.bfloat16, "v", 3)
+    dt = _pool_dtype(k_cache)
+    _need(k_cache, k_cache.dtype, "k_cache", 4)
+    _need(v_cache, k_cache.dtype, "v_cache", 4)
+    _need(slot_mapping, torch.int64, "slot_mapping", 1)
+    nb, bs, hkv, d = k_cache.shape
+    if v_cache.shape != k_cache.shape or k.shape != v.shape or k.shape[1:] != (hkv, d):
+        raise ValueError("k, v and the pools disagree on (num_kv_heads, head_dim)")
+    if slot_mapping.shape[0] != k.shape[0]:
+        raise ValueError("slot_mapping must have one entry per token")
+    for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+        if t is not None:
+            _need(t, torch.float32, name, 2)
+    _check(load().reshape_and_cache(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                    _ptr(v_scale), _ptr(slot_mapping), k.shape[0], nb, bs, hkv, d, dt,
+                                    _stream(stream)))
+
+
+def workspace_bytes(batch, num_q_heads, head_dim, max_seq_len, block_size) -> int:
+    return load().pagedkv_workspace_bytes(batch, num_q_heads, head_dim, max_seq_len, block_size)
+
+
+def partition_tokens(batch, num_kv_heads, max_seq_len, block_size) -> int:
+    return load().pagedkv_partition_tokens(batch, num_kv_heads, max_seq_len, block_size)
+
+
+def paged_attention_decode(out, q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, scale,
+                           workspace=None, k_scale=None, v_scale=None, stream=None):
+    """out[b, h] = softmax(scale q[b, h] . K) V over sequence b's paged tokens."""
+    import torch
+    _need(out, torch.bfloat16, "out", 3)
+    _need(q, torch.bfloat16, "q", 3)
+    dt = _pool_dtype(k_cache)
+    _need(k_cache, k_cache.dtype, "k_cache", 4)
+    _need(v_cache, k_cache.dtype, "v_cache", 4)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    B, hq, d = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    if out.shape != q.shape or d2 != d or v_cache.shape != k_cache.shape:
+        raise ValueError("q, out and the pools disagree")
+    if block_tables.shape[0] != B or seq_lens.shape[0] != B:
+        raise ValueError("block_tables / seq_lens must have one row per sequence")
+    for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+        if t is not None:
+            _need(t, torch.float32, name, 2)
+    wbytes = 0
+    if workspace is not None:
+        if not workspace.is_cuda or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        wbytes = workspace.numel() * workspace.element_size()
+    _check(load().paged_attention_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                         _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
+                                         block_tables.shape[1], _ptr(seq_lens), B, hq, hkv, d, nb, bs,
+                                         int(max_seq_len), float(scale), dt, _ptr(workspace), wbytes,
+                                         _stream(stream)))
+    return out
+
+
+def get_status(stream=None):
+    """(status, flags): waits for the stream, then reads and clears the
+    device status word (FLAG_* bits)."""
+    flags = ctypes.c_uint()
+    st = load().pagedkv_get_status(_stream(stream), ctypes.byref(flags))
+    return st, flags.value

@@ -1,0 +1,521 @@
+// pagedkv_api.cu -- the C ABI of libpagedkv: block pool bookkeeping, argument
+// checks, slot mapping and append kernels, the split-K merge kernel, and the
+// device status word.  The decode kernel itself is in pagedkv_decode.cu.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <deque>
+#include <mutex>
+#include <vector>
+
+#include "pagedkv_common.cuh"
+
+namespace pagedkv {
+
+static thread_local char g_last_error[512] = "";
+
+kv_status fail(kv_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+kv_status cuda_check(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return KV_OK;
+  return fail(KV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// One status word per device; kernels atomicOr PAGEDKV_FLAG_* bits into it.
+__device__ unsigned int g_status_word;
+
+kv_status device_info(DeviceInfo* out) {
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  int dev = 0;
+  kv_status st = cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
+  if (st != KV_OK) return st;
+  if (dev < 0 || dev >= 64) return fail(KV_ERR_CUDA, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  DeviceInfo& d = cache[dev];
+  if (d.device != dev) {
+    int sms = 0;
+    st = cuda_check(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev),
+                    "cudaDeviceGetAttribute(MultiProcessorCount)");
+    if (st != KV_OK) return st;
+    void* p = nullptr;
+    st = cuda_check(cudaGetSymbolAddress(&p, g_status_word), "cudaGetSymbolAddress(status word)");
+    if (st != KV_OK) return st;
+    d.num_sms = sms;
+    d.flags = static_cast<unsigned int*>(p);
+    d.device = dev;
+  }
+  *out = d;
+  return KV_OK;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int dtype_size(kv_dtype t) { return t == KV_DTYPE_INT8 ? 1 : 2; }
+
+static bool valid_dtype(kv_dtype t) { return t == KV_DTYPE_BF16 || t == KV_DTYPE_INT8; }
+
+// ---------------------------------------------------------------------------
+// Slot mapping
+// ---------------------------------------------------------------------------
+
+// Slot of position p of sequence s: block_tables[s][p / bs] * bs + p % bs.
+__device__ __forceinline__ int64_t slot_of(const int32_t* __restrict__ block_tables,
+                                           int max_blocks, int s, int p, int bs,
+                                           int num_blocks, unsigned int* flags) {
+  int logical = p / bs;
+  if (logical >= max_blocks) {
+    atomicOr(flags, PAGEDKV_FLAG_BAD_SEQ_LEN);
+    return -1;
+  }
+  int32_t phys = block_tables[(int64_t)s * max_blocks + logical];
+  if (phys < 0 || phys >= num_blocks) {
+    atomicOr(flags, PAGEDKV_FLAG_BAD_BLOCK);
+    return -1;
+  }
+  return (int64_t)phys * bs + (p % bs);
+}
+
+__global__ void decode_slots_kernel(const int32_t* __restrict__ block_tables, int max_blocks,
+                                    const int32_t* __restrict__ seq_lens, int batch, int bs,
+                                    int num_blocks, int64_t* __restrict__ slots,
+                                    unsigned int* flags) {
+  int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= batch) return;
+  int L = seq_lens[b];
+  if (L <= 0) {
+    atomicOr(flags, PAGEDKV_FLAG_BAD_SEQ_LEN);
+    slots[b] = -1;
+    return;
+  }
+  slots[b] = slot_of(block_tables, max_blocks, b, L - 1, bs, num_blocks, flags);
+}
+
+__global__ void token_slots_kernel(const int32_t* __restrict__ block_tables, int max_blocks,
+                                   const int32_t* __restrict__ seq_idx,
+                                   const int32_t* __restrict__ positions, int n, int bs,
+                                   int num_blocks, int64_t* __restrict__ slots,
+                                   unsigned int* flags) {
+  int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  int p = positions[i];
+  int s = seq_idx ? seq_idx[i] : i;
+  slots[i] = p < 0 ? -1 : slot_of(block_tables, max_blocks, s, p, bs, num_blocks, flags);
+}
+
+// ---------------------------------------------------------------------------
+// Append: one thread moves 8 elements (16 bytes of bf16 input).
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ int8_t quantize(float x, float s) {
+  // clamp(round_half_even(x / s), -127, 127) with an IEEE fp32 divide.
+  if (s == 0.0f) s = 1.0f;
+  int c = __float2int_rn(__fdiv_rn(x, s));  // NaN -> 0, +-inf saturate
+  c = c > 127 ? 127 : (c < -127 ? -127 : c);
+  return (int8_t)c;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ uint2 quantize8(uint4 x, float s) {
+  uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  uint32_t o[2] = {0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t lo = (uint8_t)quantize(bf16_lo(w[i]), s);
+    uint32_t hi = (uint8_t)quantize(bf16_hi(w[i]), s);
+    o[i / 2] |= (lo | (hi << 8)) << (16 * (i % 2));
+  }
+  return make_uint2(o[0], o[1]);
+}
+
+template <bool kInt8>
+__global__ void append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                              void* __restrict__ k_cache, void* __restrict__ v_cache,
+                              const float* __restrict__ k_scale,
+                              const float* __restrict__ v_scale,
+                              const int64_t* __restrict__ slots, int num_tokens,
+                              int num_blocks, int bs, int num_kv_heads, int head_dim,
+                              unsigned int* flags) {
+  const int chunks_per_head = head_dim / 8;
+  const int chunks_per_token = num_kv_heads * chunks_per_head;
+  int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (int64_t)num_tokens * chunks_per_token) return;
+  int token = (int)(idx / chunks_per_token);
+  int c = (int)(idx % chunks_per_token);
+  int h = c / chunks_per_head;
+  int64_t slot = slots[token];
+  if (slot < 0) return;
+  if (slot >= (int64_t)num_blocks * bs) {
+    atomicOr(flags, PAGEDKV_FLAG_BAD_SLOT);
+    return;
+  }
+  // Destination chunk: element ((slot * Hkv + h) * D + e0) of the pool.
+  int64_t dst = (slot * num_kv_heads + h) * chunks_per_head + (c % chunks_per_head);
+  uint4 kx = k[idx], vx = v[idx];
+  if (kInt8) {
+    int64_t sidx = (slot / bs) * num_kv_heads + h;
+    reinterpret_cast<uint2*>(k_cache)[dst] = quantize8(kx, k_scale[sidx]);
+    reinterpret_cast<uint2*>(v_cache)[dst] = quantize8(vx, v_scale[sidx]);
+  } else {
+    reinterpret_cast<uint4*>(k_cache)[dst] = kx;
+    reinterpret_cast<uint4*>(v_cache)[dst] = vx;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Split-K merge: one CTA per (sequence, query head), one thread per element.
+//   M = max_i m_i, w_i = 2^(m_i - M), out = sum_i w_i acc_i / sum_i w_i l_i
+// A partition whose l is negative marks a bad block: the row becomes zeros.
+// ---------------------------------------------------------------------------
+
+__global__ void merge_kernel(__nv_bfloat16* __restrict__ out, const float* __restrict__ ws_ml,
+                             const float* __restrict__ ws_acc,
+                             const int32_t* __restrict__ seq_lens, int num_q_heads,
+                             int head_dim, int part_tokens, int max_parts, int max_len) {
+  const int b = blockIdx.x / num_q_heads, h = blockIdx.x % num_q_heads;
+  const int L = seq_lens[b];
+  if (L <= 0 || L > max_len) return;  // invalid length: the decode kernel zeroed the row
+  const int np = (L + part_tokens - 1) / part_tokens;
+  if (np <= 1) return;                // single partition: written by the decode kernel
+  const int64_t row = (int64_t)b * num_q_heads + h;
+  const float* ml = ws_ml + row * max_parts * 2;
+  const float* acc = ws_acc + row * max_parts * head_dim;
+  float M = -INFINITY;
+  bool bad = false;
+  for (int i = 0; i < np; ++i) {
+    M = fmaxf(M, ml[2 * i]);
+    bad |= ml[2 * i + 1] < 0.0f;
+  }
+  for (int e = threadIdx.x; e < head_dim; e += blockDim.x) {
+    float num = 0.0f, den = 0.0f;
+    if (!bad) {
+      for (int i = 0; i < np; ++i) {
+        float w = exp2f(ml[2 * i] - M);
+        num += w * acc[(int64_t)i * head_dim + e];
+        den += w * ml[2 * i + 1];
+      }
+    }
+    out[row * head_dim + e] = __float2bfloat16_rn(bad ? 0.0f : num / den);
+  }
+}
+
+// Longest valid sequence: bounded by the host hint and by the table.
+static int valid_len_limit(const DecodeArgs& a) {
+  const int64_t table = (int64_t)a.max_blocks_per_seq * a.block_size;
+  return (int)(table < a.max_seq_len ? table : a.max_seq_len);
+}
+
+kv_status launch_merge(const DecodeArgs& a, cudaStream_t stream) {
+  if (a.max_parts <= 1) return KV_OK;
+  merge_kernel<<<a.batch * a.num_q_heads, a.head_dim, 0, stream>>>(
+      static_cast<__nv_bfloat16*>(a.out), a.ws_ml, a.ws_acc, a.seq_lens, a.num_q_heads,
+      a.head_dim, a.part_tokens, a.max_parts, valid_len_limit(a));
+  return cuda_check(cudaGetLastError(), "merge_kernel launch");
+}
+
+// ---------------------------------------------------------------------------
+// Partition size
+// ---------------------------------------------------------------------------
+
+static const int kMinPartTokens = 256;
+static const int kMaxPartTokens = 8192;
+
+// Largest power-of-two partition in [256, 8192] that still gives at least
+// 8 CTAs per SM over (sequence, KV head, partition).  The environment
+// variable PAGEDKV_PARTITION_TOKENS (a multiple of 256, read on every call)
+// overrides it.
+static int choose_part_tokens(int batch, int num_kv_heads, int max_seq_len, int num_sms) {
+  const char* s = getenv("PAGEDKV_PARTITION_TOKENS");
+  const int env = s ? atoi(s) : 0;
+  if (env >= kMinPartTokens && env % kMinPartTokens == 0) return env;
+  const int64_t target = 8LL * num_sms;
+  int pt = kMaxPartTokens;
+  while (pt > kMinPartTokens &&
+         (int64_t)batch * num_kv_heads * ((max_seq_len + pt - 1) / pt) < target)
+    pt /= 2;
+  return pt;
+}
+
+}  // namespace pagedkv
+
+using namespace pagedkv;
+
+// ===========================================================================
+// C ABI
+// ===========================================================================
+
+struct kv_pool {
+  int num_blocks, block_size, num_kv_heads, head_dim;
+  kv_dtype dtype;
+  std::deque<int32_t> free_list;   // front = next to hand out
+  std::vector<uint8_t> allocated;  // 1 = handed out
+  int used = 0;
+};
+
+extern "C" {
+
+const char* pagedkv_last_error(void) { return g_last_error; }
+
+kv_status kv_pool_create(int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                         kv_dtype dtype, kv_pool** out) {
+  if (!out) return fail(KV_ERR_INVALID_ARG, "kv_pool_create: out is NULL");
+  *out = nullptr;
+  if (num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      !valid_dtype(dtype))
+    return fail(KV_ERR_INVALID_ARG, "kv_pool_create: sizes must be positive and dtype valid");
+  kv_pool* p = new kv_pool;
+  p->num_blocks = num_blocks;
+  p->block_size = block_size;
+  p->num_kv_heads = num_kv_heads;
+  p->head_dim = head_dim;
+  p->dtype = dtype;
+  for (int i = 0; i < num_blocks; ++i) p->free_list.push_back(i);
+  p->allocated.assign(num_blocks, 0);
+  *out = p;
+  return KV_OK;
+}
+
+void kv_pool_destroy(kv_pool* pool) { delete pool; }
+
+size_t kv_pool_block_bytes(const kv_pool* p) {
+  if (!p) return 0;
+  return 2ull * p->block_size * p->num_kv_heads * p->head_dim * dtype_size(p->dtype);
+}
+
+kv_status kv_pool_alloc(kv_pool* p, int n, int32_t* out_ids) {
+  if (!p || n < 0 || (n > 0 && !out_ids))
+    return fail(KV_ERR_INVALID_ARG, "kv_pool_alloc: bad arguments");
+  if ((size_t)n > p->free_list.size())
+    return fail(KV_ERR_OUT_OF_BLOCKS, "kv_pool_alloc: %d blocks requested, %zu free", n,
+                p->free_list.size());
+  for (int i = 0; i < n; ++i) {
+    int32_t id = p->free_list.front();
+    p->free_list.pop_front();
+    p->allocated[id] = 1;
+    out_ids[i] = id;
+  }
+  p->used += n;
+  return KV_OK;
+}
+
+kv_status kv_pool_free(kv_pool* p, const int32_t* ids, int n) {
+  if (!p || n < 0 || (n > 0 && !ids)) return fail(KV_ERR_INVALID_ARG, "kv_pool_free: bad arguments");
+  std::vector<uint8_t> seen(p->num_blocks, 0);
+  for (int i = 0; i < n; ++i) {
+    int32_t id = ids[i];
+    if (id < 0 || id >= p->num_blocks || !p->allocated[id] || seen[id])
+      return fail(KV_ERR_INVALID_ARG, "kv_pool_free: block %d is not allocated (or repeated)", id);
+    seen[id] = 1;
+  }
+  for (int i = 0; i < n; ++i) {
+    p->allocated[ids[i]] = 0;
+    p->free_list.push_back(ids[i]);
+  }
+  p->used -= n;
+  return KV_OK;
+}
+
+kv_status kv_pool_stats(const kv_pool* p, int* used, int* free_blocks) {
+  if (!p) return fail(KV_ERR_INVALID_ARG, "kv_pool_stats: pool is NULL");
+  if (used) *used = p->used;
+  if (free_blocks) *free_blocks = (int)p->free_list.size();
+  return KV_OK;
+}
+
+size_t pagedkv_pool_tensor_bytes(int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                                 kv_dtype dtype) {
+  if (num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      !valid_dtype(dtype))
+    return 0;
+  return (size_t)num_blocks * block_size * num_kv_heads * head_dim * dtype_size(dtype);
+}
+
+kv_status pagedkv_slot_mapping(const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* seq_lens, int batch, int block_size,
+                               int num_blocks, int64_t* slot_mapping, void* stream) {
+  if (batch < 0 || max_blocks_per_seq <= 0 || block_size <= 0 || num_blocks <= 0)
+    return fail(KV_ERR_INVALID_ARG, "pagedkv_slot_mapping: bad sizes");
+  if (batch == 0) return KV_OK;
+  if (!block_tables || !seq_lens || !slot_mapping)
+    return fail(KV_ERR_INVALID_ARG, "pagedkv_slot_mapping: NULL pointer");
+  DeviceInfo di;
+  kv_status st = device_info(&di);
+  if (st != KV_OK) return st;
+  decode_slots_kernel<<<(batch + 255) / 256, 256, 0, (cudaStream_t)stream>>>(
+      block_tables, max_blocks_per_seq, seq_lens, batch, block_size, num_blocks, slot_mapping,
+      di.flags);
+  return cuda_check(cudaGetLastError(), "decode_slots_kernel launch");
+}
+
+kv_status pagedkv_token_slot_mapping(const int32_t* block_tables, int max_blocks_per_seq,
+                                     const int32_t* seq_idx, const int32_t* positions,
+                                     int num_tokens, int block_size, int num_blocks,
+                                     int64_t* slot_mapping, void* stream) {
+  if (num_tokens < 0 || max_blocks_per_seq <= 0 || block_size <= 0 || num_blocks <= 0)
+    return fail(KV_ERR_INVALID_ARG, "pagedkv_token_slot_mapping: bad sizes");
+  if (num_tokens == 0) return KV_OK;
+  if (!block_tables || !positions || !slot_mapping)
+    return fail(KV_ERR_INVALID_ARG, "pagedkv_token_slot_mapping: NULL pointer");
+  DeviceInfo di;
+  kv_status st = device_info(&di);
+  if (st != KV_OK) return st;
+  token_slots_kernel<<<(num_tokens + 255) / 256, 256, 0, (cudaStream_t)stream>>>(
+      block_tables, max_blocks_per_seq, seq_idx, positions, num_tokens, block_size, num_blocks,
+      slot_mapping, di.flags);
+  return cuda_check(cudaGetLastError(), "token_slots_kernel launch");
+}
+
+kv_status reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
+                            const float* k_scale, const float* v_scale,
+                            const int64_t* slot_mapping, int num_tokens, int num_blocks,
+                            int block_size, int num_kv_heads, int head_dim, kv_dtype dtype,
+                            void* stream) {
+  if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 ||
+      (head_dim != 64 && head_dim != 128) || !valid_dtype(dtype))
+    return fail(KV_ERR_INVALID_ARG,
+                "reshape_and_cache: bad geometry (head_dim must be 64 or 128, sizes positive)");
+  if (num_tokens == 0) return KV_OK;
+  if (!k || !v || !k_cache || !v_cache || !slot_mapping)
+    return fail(KV_ERR_INVALID_ARG, "reshape_and_cache: NULL pointer");
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(KV_ERR_INVALID_ARG, "reshape_and_cache: k, v and the pools must be 16-byte aligned");
+  const bool int8 = dtype == KV_DTYPE_INT8;
+  if (int8 != (k_scale != nullptr) || int8 != (v_scale != nullptr))
+    return fail(KV_ERR_INVALID_ARG,
+                "reshape_and_cache: int8 pools need k_scale and v_scale; bf16 pools take NULL");
+  DeviceInfo di;
+  kv_status st = device_info(&di);
+  if (st != KV_OK) return st;
+  const int64_t threads = (int64_t)num_tokens * num_kv_heads * (head_dim / 8);
+  const int block = 256;
+  const int64_t grid = (threads + block - 1) / block;
+  if (grid > 0x7fffffffLL) return fail(KV_ERR_INVALID_ARG, "reshape_and_cache: too many tokens");
+  cudaStream_t s = (cudaStream_t)stream;
+  if (int8)
+    append_kernel<true><<<(unsigned)grid, block, 0, s>>>(
+        (const uint4*)k, (const uint4*)v, k_cache, v_cache, k_scale, v_scale, slot_mapping,
+        num_tokens, num_blocks, block_size, num_kv_heads, head_dim, di.flags);
+  else
+    append_kernel<false><<<(unsigned)grid, block, 0, s>>>(
+        (const uint4*)k, (const uint4*)v, k_cache, v_cache, nullptr, nullptr, slot_mapping,
+        num_tokens, num_blocks, block_size, num_kv_heads, head_dim, di.flags);
+  return cuda_check(cudaGetLastError(), "append_kernel launch");
+}
+
+size_t pagedkv_workspace_bytes(int batch, int num_q_heads, int head_dim, int max_seq_len,
+                               int block_size) {
+  (void)block_size;
+  if (batch <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_seq_len <= kMinPartTokens) return 0;
+  const size_t parts = (size_t)(max_seq_len + kMinPartTokens - 1) / kMinPartTokens;
+  return (size_t)batch * num_q_heads * parts * (head_dim + 2) * sizeof(float);
+}
+
+int pagedkv_partition_tokens(int batch, int num_kv_heads, int max_seq_len, int block_size) {
+  (void)block_size;
+  DeviceInfo di;
+  if (batch <= 0 || num_kv_heads <= 0 || max_seq_len <= 0 || device_info(&di) != KV_OK) return 0;
+  return choose_part_tokens(batch, num_kv_heads, max_seq_len, di.num_sms);
+}
+
+kv_status paged_attention_decode(void* out, const void* q, const void* k_cache,
+                                 const void* v_cache, const float* k_scale, const float* v_scale,
+                                 const int32_t* block_tables, int max_blocks_per_seq,
+                                 const int32_t* seq_lens, int batch, int num_q_heads,
+                                 int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                                 int max_seq_len, float scale, kv_dtype dtype, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads ||
+      max_blocks_per_seq <= 0 || num_blocks <= 0 || max_seq_len <= 0 || !valid_dtype(dtype))
+    return fail(KV_ERR_INVALID_ARG, "paged_attention_decode: bad sizes");
+  const int G = num_q_heads / num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8)
+    return fail(KV_ERR_INVALID_ARG,
+                "paged_attention_decode: query heads per KV head must be 1, 2, 4 or 8 (got %d)", G);
+  if (head_dim != 64 && head_dim != 128)
+    return fail(KV_ERR_INVALID_ARG, "paged_attention_decode: head_dim must be 64 or 128");
+  if (block_size != 16 && block_size != 32)
+    return fail(KV_ERR_INVALID_ARG, "paged_attention_decode: block_size must be 16 or 32");
+  if (batch == 0) return KV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens)
+    return fail(KV_ERR_INVALID_ARG, "paged_attention_decode: NULL pointer");
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(KV_ERR_INVALID_ARG, "paged_attention_decode: out, q and the pools must be 16-byte aligned");
+  const bool int8 = dtype == KV_DTYPE_INT8;
+  if (int8 != (k_scale != nullptr) || int8 != (v_scale != nullptr))
+    return fail(KV_ERR_INVALID_ARG,
+                "paged_attention_decode: int8 pools need k_scale and v_scale; bf16 pools take NULL");
+  DeviceInfo di;
+  kv_status st = device_info(&di);
+  if (st != KV_OK) return st;
+
+  DecodeArgs a;
+  a.out = out;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.block_tables = block_tables;
+  a.seq_lens = seq_lens;
+  a.flags = di.flags;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.batch = batch;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.num_blocks = num_blocks;
+  a.block_size = block_size;
+  a.max_seq_len = max_seq_len;
+  a.part_tokens = choose_part_tokens(batch, num_kv_heads, max_seq_len, di.num_sms);
+  a.max_parts = (max_seq_len + a.part_tokens - 1) / a.part_tokens;
+  a.scale_log2 = scale * kLog2e;
+  a.dtype = dtype;
+  a.ws_ml = nullptr;
+  a.ws_acc = nullptr;
+  if (a.max_parts > 1) {
+    const size_t ml_bytes = (size_t)batch * num_q_heads * a.max_parts * 2 * sizeof(float);
+    const size_t need = ml_bytes + (size_t)batch * num_q_heads * a.max_parts * head_dim * sizeof(float);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace))
+      return fail(KV_ERR_INVALID_ARG,
+                  "paged_attention_decode: workspace must be 16-byte aligned and hold %zu bytes "
+                  "(pagedkv_workspace_bytes gives a safe size)", need);
+    a.ws_ml = static_cast<float*>(workspace);
+    a.ws_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + ml_bytes);
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  st = launch_decode(a, s);
+  if (st != KV_OK) return st;
+  return launch_merge(a, s);
+}
+
+kv_status pagedkv_get_status(void* stream, unsigned int* device_flags) {
+  DeviceInfo di;
+  kv_status st = device_info(&di);
+  if (st != KV_OK) return st;
+  unsigned int h = 0;
+  cudaStream_t s = (cudaStream_t)stream;
+  st = cuda_check(cudaMemcpyAsync(&h, di.flags, sizeof h, cudaMemcpyDeviceToHost, s),
+                  "pagedkv_get_status: read");
+  if (st == KV_OK) st = cuda_check(cudaStreamSynchronize(s), "pagedkv_get_status: sync");
+  if (st == KV_OK && h)
+    st = cuda_check(cudaMemsetAsync(di.flags, 0, sizeof h, s), "pagedkv_get_status: clear");
+  if (st == KV_OK) st = cuda_check(cudaStreamSynchronize(s), "pagedkv_get_status: sync");
+  if (device_flags) *device_flags = h;
+  if (st != KV_OK) return st;
+  if (h) return fail(KV_ERR_DEVICE_INDEX, "device status word 0x%x", h);
+  return KV_OK;
+}
+
+}  // extern "C"

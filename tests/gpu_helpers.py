@@ -1,0 +1,85 @@
+"""GPU-side helpers for the parity tests: every kernel runs through the C ABI
+(via the package's ctypes binding); inputs come from the seeded generator."""
+import numpy as np
+import torch
+
+import paged_kv_cache_97_gb300 as pkv
+
+
+def to_dev_bf16(bits: np.ndarray, dev="cuda"):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+
+def bits_of(t: torch.Tensor) -> np.ndarray:
+    """Raw bits of a device tensor (bf16 -> uint16, int8 -> int8)."""
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.cpu().numpy()
+
+
+class GpuStep:
+    """A workload's pools and step inputs on the device, filled by the
+    library's own slot mapping and append."""
+
+    def __init__(self, wl, dev="cuda", fill=True, seqs=None):
+        s = wl.spec
+        self.wl, self.dev = wl, dev
+        self.int8 = s.kv_dtype == "int8"
+        poison = wl.poisoned_pool()
+        if self.int8:
+            self.k_cache = torch.from_numpy(poison).to(dev)
+            self.v_cache = self.k_cache.clone()
+            ks, vs = wl.scales(seqs)
+            self.k_scale = torch.from_numpy(ks).to(dev)
+            self.v_scale = torch.from_numpy(vs).to(dev)
+        else:
+            self.k_cache = to_dev_bf16(poison, dev)
+            self.v_cache = self.k_cache.clone()
+            self.k_scale = self.v_scale = None
+        del poison
+        self.block_tables = torch.from_numpy(wl.block_tables).to(dev)
+        self.seq_lens = torch.from_numpy(wl.seq_lens).to(dev)
+        self.q = to_dev_bf16(wl.q, dev)
+        self.new_k = to_dev_bf16(wl.new_k, dev)
+        self.new_v = to_dev_bf16(wl.new_v, dev)
+        B = s.batch
+        self.slots = torch.empty(B, dtype=torch.int64, device=dev)
+        self.out = torch.empty((B, s.num_q_heads, s.head_dim), dtype=torch.bfloat16, device=dev)
+        self.max_seq_len = int(wl.seq_lens.max())
+        ws = pkv.workspace_bytes(B, s.num_q_heads, s.head_dim, self.max_seq_len, s.block_size)
+        self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+        if fill:
+            self.fill(seqs)
+
+    def fill(self, seqs=None):
+        wl, s = self.wl, self.wl.spec
+        for ch in wl.fill_chunks(seqs):
+            n = ch.positions.shape[0]
+            pos = torch.from_numpy(ch.positions).to(self.dev)
+            sid = torch.from_numpy(ch.seq_idx).to(self.dev)
+            slots = torch.empty(n, dtype=torch.int64, device=self.dev)
+            pkv.token_slot_mapping(self.block_tables, pos, wl.num_blocks, s.block_size, slots, seq_idx=sid)
+            pkv.reshape_and_cache(to_dev_bf16(ch.k, self.dev), to_dev_bf16(ch.v, self.dev),
+                                  self.k_cache, self.v_cache, slots, self.k_scale, self.v_scale)
+        torch.cuda.synchronize()
+
+    def append(self):
+        s = self.wl.spec
+        pkv.slot_mapping(self.block_tables, self.seq_lens, self.wl.num_blocks, s.block_size, self.slots)
+        pkv.reshape_and_cache(self.new_k, self.new_v, self.k_cache, self.v_cache, self.slots,
+                              self.k_scale, self.v_scale)
+
+    def attend(self, max_seq_len=None):
+        s = self.wl.spec
+        pkv.paged_attention_decode(self.out, self.q, self.k_cache, self.v_cache, self.block_tables,
+                                   self.seq_lens, max_seq_len or self.max_seq_len, s.scale,
+                                   workspace=self.workspace, k_scale=self.k_scale, v_scale=self.v_scale)
+        return self.out
+
+    def step(self):
+        self.append()
+        return self.attend()
+
+
+def out_f64(t: torch.Tensor) -> np.ndarray:
+    return t.float().cpu().numpy().astype(np.float64)

@@ -1,0 +1,288 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs.
+
+Bars: slot mapping and appends bit-exact (whole pools compared bit for bit,
+poison included); attention max-abs <= 1e-2 and mean-abs <= 1e-3 for bf16
+pools, max-abs <= 3e-2 and mean-abs <= 1e-3 for int8 pools (the oracle runs
+on the dequantised stored codes, so quantisation error is not counted).
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_97_gb300 as pkv
+import workloads
+from gpu_helpers import GpuStep, bits_of, out_f64
+from oracle_helpers import decode_slots, oracle_pool
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": (1e-2, 1e-3), "int8": (3e-2, 1e-3)}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from paged_kv_cache_97_gb300 import _build
+    _build.build()
+    oracle.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    torch.cuda.set_device(0)
+    pkv.get_status()
+
+
+def check_status(expect_flags=0):
+    st, flags = pkv.get_status()
+    assert flags == expect_flags, f"device status flags 0x{flags:x}, expected 0x{expect_flags:x}"
+
+
+def assert_close(got, ref, kv_dtype, what=""):
+    max_tol, mean_tol = TOL[kv_dtype]
+    err = np.abs(got - ref)
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    assert err.max() <= max_tol, f"{what}: max-abs {err.max():.3e} > {max_tol}"
+    assert err.mean() <= mean_tol, f"{what}: mean-abs {err.mean():.3e} > {mean_tol}"
+    return err.max(), err.mean()
+
+
+def small(lens, hq=8, hkv=2, d=64, bs=16, kv="bf16", nb=None, seed=7, prefix=0, mb=None):
+    return workloads.custom(batch=len(lens), num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                            block_size=bs, seq_lens=lens, kv_dtype=kv, num_blocks=nb,
+                            max_blocks_per_seq=mb, shared_prefix_tokens=prefix, seed=seed)
+
+
+CASES = {
+    "cfg1": lambda: workloads.make(1),
+    "ragged_g4_d128": lambda: small([1, 2, 15, 16, 17, 255, 256, 257, 1000, 3001], hq=32, hkv=8, d=128, seed=1),
+    "g8_int8_bs32": lambda: small([1, 31, 32, 33, 511, 700, 2049], hq=64, hkv=8, d=128, bs=32, kv="int8", seed=2),
+    "g1_mha_d64": lambda: small([5, 77, 300, 1290], hq=4, hkv=4, d=64, seed=3),
+    "g2_bs32_d64": lambda: small([3, 64, 500, 999], hq=4, hkv=2, d=64, bs=32, seed=4),
+    "g8_bf16_d128": lambda: small([17, 600, 1500], hq=16, hkv=2, d=128, seed=5),
+    "int8_d64_bs16": lambda: small([1, 90, 300, 777], hq=8, hkv=2, d=64, bs=16, kv="int8", seed=6),
+    "shared_prefix": lambda: small([33, 48, 300, 700], hq=32, hkv=8, d=128, prefix=32, seed=8),
+}
+
+
+# ---------------------------------------------------------------------------
+# Slot mapping and append: bit-exact
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("case", ["cfg1", "g8_int8_bs32", "int8_d64_bs16", "shared_prefix", "g2_bs32_d64"])
+def test_append_and_slots_bit_exact(case):
+    wl = CASES[case]()
+    g = GpuStep(wl)
+    g.append()
+    torch.cuda.synchronize()
+    check_status()
+    want_slots, rc = decode_slots(wl)
+    assert rc == 0
+    np.testing.assert_array_equal(g.slots.cpu().numpy(), want_slots)
+    kc, vc, _, _ = oracle_pool(wl)
+    np.testing.assert_array_equal(bits_of(g.k_cache), kc)
+    np.testing.assert_array_equal(bits_of(g.v_cache), vc)
+
+
+def test_int8_append_rounding_is_the_oracles():
+    """Values at and near rounding ties: device codes equal the oracle's."""
+    rng = np.random.default_rng(0)
+    n, H, d, bs, NB = 64, 2, 128, 32, 4
+    scale = np.float32(0.0234375)
+    ties = (np.arange(-128, 128) + 0.5).astype(np.float32) * scale  # exact ties in fp32
+    x = np.concatenate([ties, rng.standard_normal(n * H * d - ties.size).astype(np.float32) * 3])
+    bits = workloads.to_bf16_bits(x).reshape(n, H, d)
+    ks = np.full((NB, H), scale, np.float32)
+    ks[1, 0] = 0.0                                                    # zero scale reads as 1
+    slots = rng.permutation(NB * bs)[:n].astype(np.int64)
+    kc = np.zeros((NB, bs, H, d), np.int8)
+    vc = np.zeros_like(kc)
+    assert oracle.append_int8(bits, bits, kc, vc, ks, ks, slots) == 0
+    from gpu_helpers import to_dev_bf16
+    dk = torch.zeros((NB, bs, H, d), dtype=torch.int8, device="cuda")
+    dv = torch.zeros_like(dk)
+    t = to_dev_bf16(bits)
+    s = torch.from_numpy(ks).cuda()
+    pkv.reshape_and_cache(t, t, dk, dv, torch.from_numpy(slots).cuda(), s, s)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(dk.cpu().numpy(), kc)
+    np.testing.assert_array_equal(dv.cpu().numpy(), vc)
+
+
+# ---------------------------------------------------------------------------
+# Attention against the oracle (small, every row)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_attention_matches_oracle(case):
+    wl = CASES[case]()
+    g = GpuStep(wl)
+    got = out_f64(g.step())
+    torch.cuda.synchronize()
+    check_status()
+    kc, vc, ks, vs = oracle_pool(wl)
+    ref, rc = oracle.paged_attention(wl.q, kc, vc, wl.block_tables, wl.seq_lens, wl.spec.scale,
+                                     k_scale=ks, v_scale=vs, threads=os.cpu_count())
+    assert rc == 0
+    assert_close(got, ref, wl.spec.kv_dtype, case)
+
+
+def test_repeated_steps_are_deterministic():
+    wl = CASES["ragged_g4_d128"]()
+    g = GpuStep(wl)
+    a = bits_of(g.step()).copy()
+    b = bits_of(g.step())
+    np.testing.assert_array_equal(a, b)
+
+
+@pytest.mark.parametrize("part", ["256", "512", "8192"])
+def test_partition_size_does_not_change_the_answer(monkeypatch, part):
+    wl = CASES["ragged_g4_d128"]()
+    kc, vc, ks, vs = oracle_pool(wl)
+    ref, _ = oracle.paged_attention(wl.q, kc, vc, wl.block_tables, wl.seq_lens, wl.spec.scale,
+                                    threads=os.cpu_count())
+    monkeypatch.setenv("PAGEDKV_PARTITION_TOKENS", part)
+    g = GpuStep(wl)
+    assert pkv.partition_tokens(wl.spec.batch, wl.spec.num_kv_heads, g.max_seq_len, 16) == int(part)
+    assert_close(out_f64(g.step()), ref, "bf16", f"partition {part}")
+    check_status()
+
+
+# ---------------------------------------------------------------------------
+# Invariants
+# ---------------------------------------------------------------------------
+
+def test_single_token_returns_v_bit_exact():
+    for kv in ("bf16",):
+        wl = small([1] * 6, hq=32, hkv=8, d=128, kv=kv, seed=10)
+        g = GpuStep(wl)
+        out = bits_of(g.step())
+        want = np.repeat(wl.new_v, 4, axis=1)
+        np.testing.assert_array_equal(out, want)
+
+
+def test_permuted_placement_is_bit_identical():
+    wl = small([40, 257, 1000, 2222], hq=32, hkv=8, d=128, seed=12)
+    a = bits_of(GpuStep(wl).step()).copy()
+    perm = np.random.default_rng(1).permutation(wl.num_blocks).astype(np.int32)
+    bt = wl.block_tables.copy()
+    used = bt >= 0
+    bt[used] = perm[bt[used]]
+    wl.block_tables = bt
+    b = bits_of(GpuStep(wl).step())
+    np.testing.assert_array_equal(a, b)
+
+
+def test_shared_prefix_equals_private_copies_bit_exact():
+    wl = small([40, 64, 300, 1000], hq=32, hkv=8, d=128, prefix=32, seed=13)
+    a = bits_of(GpuStep(wl).step()).copy()
+    g = GpuStep(wl)
+    # private copies of the 2 prefix blocks for every sequence but the first
+    extra = 2 * (wl.spec.batch - 1)
+    nb = wl.num_blocks
+    k2 = torch.cat([g.k_cache, g.k_cache[:extra].clone()])
+    v2 = torch.cat([g.v_cache, g.v_cache[:extra].clone()])
+    bt = wl.block_tables.copy()
+    nxt = nb
+    for b in range(1, wl.spec.batch):
+        for j in range(2):
+            k2[nxt], v2[nxt] = g.k_cache[bt[b, j]], g.v_cache[bt[b, j]]
+            bt[b, j] = nxt
+            nxt += 1
+    wl.block_tables, wl.num_blocks = bt, nxt
+    g.k_cache, g.v_cache = k2.contiguous(), v2.contiguous()
+    g.block_tables = torch.from_numpy(bt).cuda()
+    b2 = bits_of(g.step())
+    np.testing.assert_array_equal(a, b2)
+
+
+def test_table_padding_and_poison_are_never_read():
+    wl = small([1, 17, 300, 900], hq=32, hkv=8, d=128, seed=14, mb=64)
+    g = GpuStep(wl)
+    a = bits_of(g.step()).copy()
+    bt = wl.block_tables.copy()
+    pad = bt < 0
+    bt[pad] = np.random.default_rng(2).integers(-5000, 5000, size=int(pad.sum()))
+    g.block_tables = torch.from_numpy(bt).cuda()
+    b = bits_of(g.attend())
+    np.testing.assert_array_equal(a, b)
+    check_status()
+
+
+# ---------------------------------------------------------------------------
+# Device-side index faults: flagged, zeroed, never a GPU fault
+# ---------------------------------------------------------------------------
+
+def test_bad_block_id_and_length_zero_the_row_and_flag():
+    wl = small([100, 600, 700, 50], hq=8, hkv=2, d=64, seed=15)
+    g = GpuStep(wl)
+    good = bits_of(g.step()).copy()
+    bt = wl.block_tables.copy()
+    bt[1, 3] = wl.num_blocks + 7            # inside sequence 1's range
+    sl = wl.seq_lens.copy()
+    sl[2] = 0
+    g.block_tables = torch.from_numpy(bt).cuda()
+    g.seq_lens = torch.from_numpy(sl).cuda()
+    out = bits_of(g.attend(max_seq_len=700))
+    st, flags = pkv.get_status()
+    assert st == pkv.KV_ERR_DEVICE_INDEX
+    assert flags == pkv.FLAG_BAD_BLOCK | pkv.FLAG_BAD_SEQ_LEN
+    assert not out[1].any() and not out[2].any()
+    np.testing.assert_array_equal(out[0], good[0])
+    np.testing.assert_array_equal(out[3], good[3])
+
+
+def test_length_past_the_hint_is_flagged():
+    wl = small([100, 600], hq=8, hkv=2, d=64, seed=16)
+    g = GpuStep(wl)
+    g.step()
+    out = bits_of(g.attend(max_seq_len=300))
+    st, flags = pkv.get_status()
+    assert flags == pkv.FLAG_BAD_SEQ_LEN and not out[1].any()
+
+
+def test_bad_slot_is_flagged_and_skipped():
+    wl = small([10, 20], hq=8, hkv=2, d=64, seed=17)
+    g = GpuStep(wl)
+    before = bits_of(g.k_cache).copy()
+    bad = torch.tensor([wl.num_blocks * 16, -1], dtype=torch.int64, device="cuda")
+    pkv.reshape_and_cache(g.new_k, g.new_v, g.k_cache, g.v_cache, bad)
+    st, flags = pkv.get_status()
+    assert flags == pkv.FLAG_BAD_SLOT
+    np.testing.assert_array_equal(bits_of(g.k_cache), before)
+
+
+# ---------------------------------------------------------------------------
+# Full-size workloads: sampled rows against the oracle
+# ---------------------------------------------------------------------------
+
+def sample_rows(wl, n_seqs=3, rng_seed=0):
+    """The longest and shortest sequences plus a random one; all query heads
+    of each (covers every KV head and both ends of the length range)."""
+    L = wl.seq_lens
+    rng = np.random.default_rng(rng_seed)
+    seqs = sorted({int(np.argmax(L)), int(np.argmin(L)), int(rng.integers(len(L)))})[:n_seqs]
+    rows = np.array([(b, h) for b in seqs for h in range(wl.spec.num_q_heads)], np.int32)
+    return seqs, rows
+
+
+@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
+def test_full_size_config_sampled_rows(cfg):
+    wl = workloads.make(cfg)
+    g = GpuStep(wl)
+    got = out_f64(g.step())
+    torch.cuda.synchronize()
+    check_status()
+    assert np.isfinite(got).all()
+    seqs, rows = sample_rows(wl)
+    kc, vc, ks, vs = oracle_pool(wl, seqs=seqs)
+    ref, rc = oracle.paged_attention(wl.q, kc, vc, wl.block_tables, wl.seq_lens, wl.spec.scale,
+                                     k_scale=ks, v_scale=vs, rows=rows, threads=os.cpu_count())
+    assert rc == 0
+    assert_close(got[rows[:, 0], rows[:, 1]], ref, wl.spec.kv_dtype, f"config {cfg}")
+    # the appended rows of the sampled sequences are the oracle's, bit for bit
+    slots, _ = decode_slots(wl)
+    for b in seqs:
+        blk, row = divmod(int(slots[b]), wl.spec.block_size)
+        np.testing.assert_array_equal(bits_of(g.k_cache[blk, row]), kc[blk, row])
+        np.testing.assert_array_equal(bits_of(g.v_cache[blk, row]), vc[blk, row])
