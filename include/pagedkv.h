@@ -205,6 +205,46 @@ kv_status paged_attention_decode(void *out, const void *q, const void *k_cache,
                                  void *workspace, size_t workspace_bytes,
                                  void *stream);
 
+/* Size of the fixed device scratch paged_attention_decode_noalloc uses. */
+#define PAGEDKV_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* paged_attention_decode without a workspace argument, for callers that
+ * cannot allocate device memory: a plain C host program that links only this
+ * library and the CUDA runtime and has no device allocator of its own, or a
+ * serving engine that reserves all of HBM for its KV pool at start-up and
+ * forbids allocation afterwards.  The pages describe no such entry point; it
+ * is this library's own addition.
+ *
+ * Arguments, layouts, results and errors are those of paged_attention_decode
+ * (minus workspace / workspace_bytes).  The split-K partials go to a scratch
+ * array of PAGEDKV_NOALLOC_SCRATCH_BYTES (32 MiB) compiled into the library:
+ * every GPU that loads the library holds it until the process exits, and the
+ * call itself allocates nothing (no cudaMalloc, cudaFree or allocating
+ * library routine).  A shape whose partials need more than that returns
+ * KV_ERR_INVALID_ARG with a message naming both sizes.
+ *
+ * The first call on each device looks up that device's scratch address
+ * (cudaGetSymbolAddress) with the device current; make that first call before
+ * any stream capture.  All calls on a device share the one scratch array,
+ * which keeps the last call's contents; nothing in it needs clearing, since
+ * each call writes every partial it later reads.  Calls whose work overlaps
+ * on the GPU (different streams, or several host threads) race on the
+ * scratch: serialise them, or use paged_attention_decode with one workspace
+ * per stream. */
+kv_status paged_attention_decode_noalloc(void *out, const void *q,
+                                         const void *k_cache,
+                                         const void *v_cache,
+                                         const float *k_scale,
+                                         const float *v_scale,
+                                         const int32_t *block_tables,
+                                         int max_blocks_per_seq,
+                                         const int32_t *seq_lens, int batch,
+                                         int num_q_heads, int num_kv_heads,
+                                         int head_dim, int num_blocks,
+                                         int block_size, int max_seq_len,
+                                         float scale, kv_dtype dtype,
+                                         void *stream);
+
 /* ------------------------------------------------------------------------ */
 /* Status                                                                   */
 /* ------------------------------------------------------------------------ */

@@ -41,6 +41,8 @@ SIGNATURES = {
     "pagedkv_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "paged_attention_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I,
                                     _I, _F, _I, _P, _SZ, _P]),
+    "paged_attention_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I,
+                                            _I, _I, _I, _F, _I, _P]),
     "pagedkv_get_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
     "pagedkv_last_error": (ctypes.c_char_p, []),
     "pagedkv_partition_tokens": (_I, [_I, _I, _I, _I]),
@@ -260,6 +262,41 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, seq_lens, max
                                          block_tables.shape[1], _ptr(seq_lens), B, hq, hkv, d, nb, bs,
                                          int(max_seq_len), float(scale), dt, _ptr(workspace), wbytes,
                                          _stream(stream)))
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def paged_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, seq_lens, max_seq_len,
+                                   scale, k_scale=None, v_scale=None, stream=None):
+    """paged_attention_decode for callers that cannot allocate device memory:
+    the split-K partials go to the library's fixed 32 MiB device scratch
+    instead of a caller workspace.  Calls that overlap on the GPU race on
+    that scratch; the first call on a device should come before any stream
+    capture."""
+    import torch
+    _need(out, torch.bfloat16, "out", 3)
+    _need(q, torch.bfloat16, "q", 3)
+    dt = _pool_dtype(k_cache)
+    _need(k_cache, k_cache.dtype, "k_cache", 4)
+    _need(v_cache, k_cache.dtype, "v_cache", 4)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    B, hq, d = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    if out.shape != q.shape or d2 != d or v_cache.shape != k_cache.shape:
+        raise ValueError("q, out and the pools disagree")
+    if block_tables.shape[0] != B or seq_lens.shape[0] != B:
+        raise ValueError("block_tables / seq_lens must have one row per sequence")
+    for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+        if t is not None:
+            _need(t, torch.float32, name, 2)
+    _check(load().paged_attention_decode_noalloc(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                                 _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
+                                                 block_tables.shape[1], _ptr(seq_lens), B, hq, hkv, d,
+                                                 nb, bs, int(max_seq_len), float(scale), dt,
+                                                 _stream(stream)))
     return out
 
 

@@ -1,0 +1,82 @@
+// pagedkv_noalloc.cu -- paged_attention_decode for callers that cannot hand
+// the library any scratch memory.
+//
+// paged_attention_decode needs a caller-provided workspace when a sequence is
+// split into several token partitions (the per-partition (m, l, acc) partials
+// live there until the merge kernel combines them).  Some callers cannot
+// provide one: a plain C host program that links only this library and the
+// CUDA runtime may have no device allocator of its own, and a serving engine
+// that reserves all of HBM for its KV pool at start-up forbids allocation
+// afterwards (a later cudaMalloc would fail or fragment its arena).  This
+// entry point serves them from a fixed scratch array that is part of the
+// library's device image: the library never calls cudaMalloc, cudaFree or any
+// allocating routine here.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "pagedkv_common.cuh"
+
+namespace pagedkv {
+namespace {
+
+// The scratch: PAGEDKV_NOALLOC_SCRATCH_BYTES of device memory, resident on
+// every GPU that loads the library, from load until process exit.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[PAGEDKV_NOALLOC_SCRATCH_BYTES];
+
+// Device address of this device's copy of the scratch, looked up once per
+// device with that device current.  (In host code the array's name is only a
+// host-side stand-in; the kernels must get this address instead.)
+kv_status scratch_address(void** out) {
+  static std::mutex mu;
+  static void* cache[64] = {};
+  int dev = 0;
+  kv_status st = cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
+  if (st != KV_OK) return st;
+  if (dev < 0 || dev >= 64) return fail(KV_ERR_CUDA, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* p = nullptr;
+    st = cuda_check(cudaGetSymbolAddress(&p, g_noalloc_scratch),
+                    "cudaGetSymbolAddress(no-alloc scratch)");
+    if (st != KV_OK) return st;
+    cache[dev] = p;
+  }
+  *out = cache[dev];
+  return KV_OK;
+}
+
+}  // namespace
+}  // namespace pagedkv
+
+using namespace pagedkv;
+
+extern "C" kv_status paged_attention_decode_noalloc(
+    void* out, const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+    const float* v_scale, const int32_t* block_tables, int max_blocks_per_seq,
+    const int32_t* seq_lens, int batch, int num_q_heads, int num_kv_heads, int head_dim,
+    int num_blocks, int block_size, int max_seq_len, float scale, kv_dtype dtype, void* stream) {
+  if (batch > 0 && num_q_heads > 0 && num_kv_heads > 0 && head_dim > 0 && max_seq_len > 0) {
+    // Scratch this call needs: the partials of every (sequence, query head,
+    // partition) when the sequences split into more than one partition.
+    const int part = pagedkv_partition_tokens(batch, num_kv_heads, max_seq_len, block_size);
+    if (part <= 0) return fail(KV_ERR_CUDA, "paged_attention_decode_noalloc: no device");
+    const size_t parts = (size_t)(max_seq_len + part - 1) / part;
+    const size_t need =
+        parts > 1 ? (size_t)batch * num_q_heads * parts * (head_dim + 2) * sizeof(float) : 0;
+    if (need > PAGEDKV_NOALLOC_SCRATCH_BYTES)
+      return fail(KV_ERR_INVALID_ARG,
+                  "paged_attention_decode_noalloc: this shape needs %zu bytes of scratch, more "
+                  "than the fixed %u bytes; use paged_attention_decode with a workspace",
+                  need, (unsigned)PAGEDKV_NOALLOC_SCRATCH_BYTES);
+  }
+  void* scratch = nullptr;
+  kv_status st = scratch_address(&scratch);
+  if (st != KV_OK) return st;
+  // Nothing in the scratch needs clearing: every partial the merge kernel
+  // reads is written earlier in the same call.
+  return paged_attention_decode(out, q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                                max_blocks_per_seq, seq_lens, batch, num_q_heads, num_kv_heads,
+                                head_dim, num_blocks, block_size, max_seq_len, scale, dtype,
+                                scratch, PAGEDKV_NOALLOC_SCRATCH_BYTES, stream);
+}
