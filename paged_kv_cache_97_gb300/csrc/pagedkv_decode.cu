@@ -1,70 +1,255 @@
 // pagedkv_decode.cu -- per-partition decode attention over a paged KV pool.
 //
-// One CTA serves one (token partition, KV head, sequence) and all G query
-// heads grouped on that KV head.  It walks the partition's logical tokens
-// through the block table, keeps the online-softmax state (m, l) and an
-// unnormalised accumulator per query head, and either writes the normalised
-// output (one partition) or its partial (m, l, acc) for the merge kernel.
+// One CTA serves one (token partition, KV head, sequence) and all G <= 8 query
+// heads grouped on that KV head, so every K/V byte of the step is read from
+// HBM once.  The CTA is a small producer/consumer pipeline:
+//
+//   * warp 4 (producer): one lane walks the partition's blocks in logical
+//     order and issues TMA tensor loads (cp.async.bulk.tensor) of each block's
+//     K and V rows for this KV head into a ring of shared-memory stages,
+//     completing on per-stage mbarriers;
+//   * warps 0..3 (consumers): consumer w takes block w of every stage and
+//     runs the online-softmax recurrence (“LLM 推理优化技术全景”, 在线 Softmax:
+//     m' = max(m, max S), l' = l e^(m-m') + sum e^(S-m'), O rescaled) on
+//     tensor cores, in base 2 and with the division deferred to the end
+//     (“Flash Attention v2 的改进”);
+//   * finally the four consumers' (m, l, acc) are combined through shared
+//     memory and the CTA writes either the normalised output (the sequence
+//     has one partition) or its partial for the log-sum-exp merge kernel.
+//
+// Tensor-core formulation (mma.sync m16n8k16, fp32 accumulate), per 16-token
+// tile of a block:
+//   S^T[16 tokens x 8 heads] = K[16 x d] . Q^T[d x 8]      (A = K from smem)
+//   O^T[d x 8 heads]        += V^T[d x 16] . P^T[16 x 8]   (A = V^T from smem)
+// Heads sit on the N = 8 side, so G <= 8 grouped query heads cost one MMA
+// column block; the padded heads carry q = 0 and are never written out.
+// Lane l = 4g + t of a warp holds S^T rows (tokens) g, g+8 and columns
+// (heads) 2t, 2t+1 -- the same heads as its O^T accumulator columns -- so the
+// softmax state (m, l) of heads 2t and 2t+1 lives in the lane that rescales
+// their accumulators.
+//
+// bf16 pools: K and V tiles come straight from the swizzled stage with
+// ldmatrix (V transposed by ldmatrix.trans).  int8 pools: codes are read with
+// 16-byte shared loads and widened to fp16 exactly (c + 128 placed in the
+// mantissa of 1024.0, minus 1152); q is fp16 (scaled by a power of two when
+// its magnitude needs it), the block's K scale multiplies the fp32 score and
+// its V scale (relative to the CTA's largest) multiplies p.  Every pairing
+// of d (or token) indices between the two MMA operands is the same on both
+// sides, so each dot product sums the same terms as the plain definition.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
+
+#include <mutex>
 
 #include "pagedkv_common.cuh"
 
 namespace pagedkv {
 namespace {
 
-constexpr int kWarps = 4;
+constexpr int kConsumers = 4;                        // consumer warps per CTA
+constexpr int kThreads = (kConsumers + 1) * 32;      // + one producer warp
+constexpr int kMaxStages = 8;
+constexpr int kMaxBlocks = 8192 / 16;                // blocks per partition (max)
+constexpr int kStageBudget = 96 * 1024;              // shared memory for stages
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+template <int D, int BS, bool kInt8>
+struct Geo {
+  static constexpr int kElem = kInt8 ? 1 : 2;
+  static constexpr int kRowBytes = D * kElem;                          // 256, 128, 64
+  static constexpr int kBoxRow = kRowBytes > 128 ? 128 : kRowBytes;    // bytes per box row
+  static constexpr int kBoxes = kRowBytes / kBoxRow;                   // 2 for bf16 d128
+  static constexpr int kBoxElems = kBoxRow / kElem;
+  static constexpr bool kSwizzle = kBoxRow == 128;                     // SWIZZLE_128B
+  static constexpr int kBoxBytes = BS * kBoxRow;
+  static constexpr int kTensorBytes = kBoxes * kBoxBytes;              // K (or V) of a block
+  static constexpr int kBlockBytes = 2 * kTensorBytes;                 // K + V
+  static constexpr int kStageBytes = kConsumers * kBlockBytes;
+  static constexpr int kStages0 = kStageBudget / kStageBytes;
+  static constexpr int kStages = kStages0 < 2 ? 2 : (kStages0 > kMaxStages ? kMaxStages : kStages0);
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024;      // + alignment slack
+  static constexpr int kTiles = BS / 16;                               // 16-token MMA tiles
+  static constexpr int kKSteps = D / 16;                               // MMA k-steps over d
+  static constexpr int kMTiles = D / 16;                               // O^T m-tiles over d
+};
 
-// Elements [lane * E, lane * E + E) of one K or V row, widened to fp32 and,
-// for int8 pools, multiplied by the block's scale.
-template <int E, bool kInt8>
-__device__ __forceinline__ void load_row(const void* base, int64_t row, int lane, float scale,
-                                         float (&x)[E]) {
-  if constexpr (kInt8) {
-    const int8_t* p = static_cast<const int8_t*>(base) + row + lane * E;
-    if constexpr (E == 4) {
-      const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) x[i] = (float)(int8_t)(w >> (8 * i)) * scale;
-    } else {
-      const uint16_t w = *reinterpret_cast<const uint16_t*>(p);
-      x[0] = (float)(int8_t)(w & 0xff) * scale;
-      x[1] = (float)(int8_t)(w >> 8) * scale;
-    }
+// ---------------------------------------------------------------------------
+// PTX helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Waits for the phase of `bar` with the given parity, giving up after
+// kWaitLimitNs; returns false on time-out (the caller reports it).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  return true;
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+// D += A . B for one m16n8k16 tile, fp32 accumulate; A, B bf16 or fp16.
+template <bool kF16>
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  if constexpr (kF16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
   } else {
-    const uint16_t* p = static_cast<const uint16_t*>(base) + row + lane * E;
-    if constexpr (E == 4) {
-      const uint2 w = *reinterpret_cast<const uint2*>(p);
-      x[0] = bf16_lo(w.x);
-      x[1] = bf16_hi(w.x);
-      x[2] = bf16_lo(w.y);
-      x[3] = bf16_hi(w.y);
-    } else {
-      const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
-      x[0] = bf16_lo(w);
-      x[1] = bf16_hi(w);
-    }
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
   }
 }
 
-template <int D, int G, bool kInt8>
-__global__ void __launch_bounds__(kWarps * 32) decode_kernel(DecodeArgs a) {
-  constexpr int E = D / 32;  // elements per lane
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+// Two fp32 -> packed pair, lower index in the low half.
+template <bool kF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  uint32_t r;
+  if constexpr (kF16)
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  else
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// int8 codes (two's complement) at bytes b0, b1 of w, already XORed with
+// 0x80 (so each byte is c + 128): fp16 pair of (1024 + c + 128) - 1152 = c,
+// exact.  sel 0x4140 takes bytes 0,1; 0x4342 bytes 2,3.
+__device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t w_biased, uint32_t sel) {
+  const uint32_t h = prmt(w_biased, 0x64646464u, sel);
+  __half2 x = *reinterpret_cast<const __half2*>(&h);
+  x = __hsub2(x, __half2half2(__ushort_as_half((unsigned short)0x6480)));  // 1152.0
+  return *reinterpret_cast<const uint32_t*>(&x);
+}
+
+// Byte offset of 16-byte chunk `c` of row `r` inside one K or V block of a
+// stage.  Rows of a box are kBoxRow bytes; with SWIZZLE_128B the chunk index
+// inside each 128-byte row is XORed with (row mod 8), the pattern TMA writes
+// (box starts are 1024-byte aligned).
+template <class G>
+__device__ __forceinline__ uint32_t chunk_off(int r, int c) {
+  constexpr int kChunksPerBox = G::kBoxRow / 16;
+  const int box = c / kChunksPerBox, cc = c % kChunksPerBox;
+  const int phys = G::kSwizzle ? (cc ^ (r & 7)) : cc;
+  return box * G::kBoxBytes + r * G::kBoxRow + phys * 16;
+}
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+
+template <int D, int BS, bool kInt8>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap k_map,
+                  const __grid_constant__ CUtensorMap v_map, const DecodeArgs a) {
+  using G = Geo<D, BS, kInt8>;
+  constexpr int S = G::kStages;
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
+  __shared__ int32_t blk_id[kMaxBlocks];
+  __shared__ float blk_ks[kInt8 ? kMaxBlocks : 1], blk_vr[kInt8 ? kMaxBlocks : 1];
+  __shared__ int cta_bad, cta_timeout;
+  __shared__ float v_max_scale;
+
   const int part = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int Hq = a.num_q_heads, Hkv = a.num_kv_heads, bs = a.block_size;
-  const int64_t head0 = (int64_t)b * Hq + (int64_t)hk * G;  // first query row of the group
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;                 // MMA fragment coordinates
+  const int Hq = a.num_q_heads, Hkv = a.num_kv_heads;
+  const int GQ = Hq / Hkv;                               // grouped query heads (1..8)
+  const int64_t head0 = (int64_t)b * Hq + (int64_t)hk * GQ;
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
 
+  // ---- sequence checks (uniform over the CTA) -----------------------------
   const int L = a.seq_lens[b];
-  const int64_t table_tokens = (int64_t)a.max_blocks_per_seq * bs;
+  const int64_t table_tokens = (int64_t)a.max_blocks_per_seq * BS;
   if (L <= 0 || L > a.max_seq_len || L > table_tokens) {
     if (part == 0) {
       if (threadIdx.x == 0) atomicOr(a.flags, PAGEDKV_FLAG_BAD_SEQ_LEN);
-      for (int i = threadIdx.x; i < G * D; i += blockDim.x)
+      for (int i = threadIdx.x; i < GQ * D; i += blockDim.x)
         out[head0 * D + i] = __float2bfloat16_rn(0.0f);
     }
     return;
@@ -73,32 +258,362 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(DecodeArgs a) {
   if (t0 >= L) return;
   const int t1 = min(t0 + a.part_tokens, L);
   const int nparts = (L + a.part_tokens - 1) / a.part_tokens;
+  const int first_blk = t0 / BS;
+  const int nblk = (t1 - 1) / BS - first_blk + 1;        // >= 1, <= kMaxBlocks
 
-  __shared__ float qs[G][D];
-  __shared__ float red_m[kWarps][G], red_l[kWarps][G];
-  __shared__ float red_acc[kWarps][G][D];
-  __shared__ int bad;
+  const uint32_t stages = (smem_addr(smem_raw) + 1023u) & ~1023u;
 
-  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q) + head0 * D;
-  for (int i = threadIdx.x; i < G * D; i += blockDim.x)
-    qs[i / D][i % D] = __bfloat162float(q[i]) * a.scale_log2;
-  if (threadIdx.x == 0) bad = 0;
-  __syncthreads();
-
-  const int32_t* bt = a.block_tables + (int64_t)b * a.max_blocks_per_seq;
-  for (int j = t0 / bs + threadIdx.x; j <= (t1 - 1) / bs; j += blockDim.x) {
-    const int32_t p = bt[j];
-    if (p < 0 || p >= a.num_blocks) bad = 1;
+  // ---- set-up: barriers, the partition's block ids (and int8 scales) ------
+  if (threadIdx.x == 0) {
+    cta_bad = 0;
+    cta_timeout = 0;
+    v_max_scale = 0.0f;
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_addr(&full_bar[s]), 1);
+      mbar_init(smem_addr(&empty_bar[s]), kConsumers);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  if (bad) {
-    if (threadIdx.x == 0) atomicOr(a.flags, PAGEDKV_FLAG_BAD_BLOCK);
-    for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-      const int g = i / D, e = i % D;
+  const int32_t* bt = a.block_tables + (int64_t)b * a.max_blocks_per_seq + first_blk;
+  for (int j = threadIdx.x; j < nblk; j += blockDim.x) {
+    const int32_t p = bt[j];
+    const bool ok = p >= 0 && p < a.num_blocks;
+    blk_id[j] = ok ? p : 0;
+    if (!ok) cta_bad = 1;
+    if constexpr (kInt8) {
+      if (ok) {
+        blk_ks[j] = a.k_scale[(int64_t)p * Hkv + hk];
+        const float vs = a.v_scale[(int64_t)p * Hkv + hk];
+        blk_vr[j] = vs;
+        atomicMax(reinterpret_cast<int*>(&v_max_scale), __float_as_int(fabsf(vs)));
+      }
+    }
+  }
+  __syncthreads();
+  if constexpr (kInt8) {
+    // p is multiplied by (V scale / the CTA's largest V scale) so that it stays
+    // in fp16 range; the output is multiplied back by the largest scale.
+    const float vmax = v_max_scale > 0.0f ? v_max_scale : 1.0f;
+    for (int j = threadIdx.x; j < nblk; j += blockDim.x) blk_vr[j] = blk_vr[j] / vmax;
+    __syncthreads();
+  }
+
+  const bool bad = cta_bad != 0;
+  const int n_iter = (nblk + kConsumers - 1) / kConsumers;
+
+  // Per-consumer softmax state for heads 2t, 2t+1 and the O^T accumulator.
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
+  float o[G::kMTiles][4];
+#pragma unroll
+  for (int i = 0; i < G::kMTiles; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
+
+  if (!bad && warp == kConsumers) {
+    // ======================= producer =======================================
+    if (lane == 0) {
+      int issued = 0;
+      bool ok = true;
+      for (int it = 0; it < n_iter; ++it) {
+        const int s = it % S;
+        if (it >= S && !mbar_wait(smem_addr(&empty_bar[s]), ((it / S) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        const int j0 = it * kConsumers;
+        const int cnt = min(kConsumers, nblk - j0);
+        const uint32_t fb = smem_addr(&full_bar[s]);
+        mbar_expect_tx(fb, (uint32_t)(cnt * G::kBlockBytes));
+        for (int c = 0; c < cnt; ++c) {
+          const int p = blk_id[j0 + c];
+          const uint32_t kdst = stages + (uint32_t)((s * kConsumers + c) * G::kBlockBytes);
+          const uint32_t vdst = kdst + G::kTensorBytes;
+#pragma unroll
+          for (int x = 0; x < G::kBoxes; ++x) {
+            tma_load_4d(kdst + x * G::kBoxBytes, &k_map, fb, x * G::kBoxElems, hk, 0, p);
+            tma_load_4d(vdst + x * G::kBoxBytes, &v_map, fb, x * G::kBoxElems, hk, 0, p);
+          }
+        }
+        issued = it + 1;
+      }
+      // Wait for every fill this thread issued before the CTA may reuse or
+      // release the stages (bounded; normally already complete).
+      for (int s = 0; s < S && s < issued; ++s) {
+        const int last = s + S * ((issued - 1 - s) / S);
+        if (!mbar_wait(smem_addr(&full_bar[s]), (last / S) & 1)) ok = false;
+      }
+      if (!ok) cta_timeout = 1;
+    }
+  } else if (!bad) {
+    // ======================= consumers =====================================
+    const int w = warp;
+    constexpr bool kF16 = kInt8;
+    // Q^T fragments (B operand of S^T = K . Q^T): b0 = (k = 2t, 2t+1; n = g),
+    // b1 = (k = 2t+8, 2t+9; n = g).  k indexes d: for bf16 the natural order
+    // 16ks + k; for int8 the order in which each lane reads its own 16-byte
+    // chunks of a K row (see the int8 K loads below).
+    uint32_t qf[G::kKSteps][2];
+    float qscale = 1.0f;
+    {
+      const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q) + (head0 + g) * D;
+      const bool live = g < GQ;
+      float amax = 0.0f;
+      float qv[G::kKSteps][4];
+#pragma unroll
+      for (int ks = 0; ks < G::kKSteps; ++ks) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          int d0;
+          if constexpr (kInt8) {
+            // lane t reads chunks t*NC .. t*NC+NC-1 (16 d each, NC = D/64)
+            // of a row; k-step ks uses 4 consecutive d of chunk ks/4.
+            constexpr int NC = D / 64;
+            d0 = 16 * (t * NC + ks / 4) + 4 * (ks % 4) + 2 * r;
+          } else {
+            d0 = 16 * ks + 2 * t + 8 * r;
+          }
+          const float x0 = live ? __bfloat162float(q[d0]) : 0.0f;
+          const float x1 = live ? __bfloat162float(q[d0 + 1]) : 0.0f;
+          qv[ks][2 * r] = x0;
+          qv[ks][2 * r + 1] = x1;
+          amax = fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1)));
+        }
+      }
+      if constexpr (kInt8) {
+        // fp16 holds |q| < 65504; scale by a power of two when needed and
+        // fold the inverse into the score scale (exact either way).
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        int e = 0;
+        if (amax >= 16384.0f) frexpf(amax, &e), e -= 14;
+        qscale = ldexpf(1.0f, -e);
+      }
+#pragma unroll
+      for (int ks = 0; ks < G::kKSteps; ++ks) {
+        qf[ks][0] = pack2<kF16>(qv[ks][0] * qscale, qv[ks][1] * qscale);
+        qf[ks][1] = pack2<kF16>(qv[ks][2] * qscale, qv[ks][3] * qscale);
+      }
+    }
+    const float score_scale = a.scale_log2 / qscale;
+    // P^T transpose sources: token 2t (and 2t+8) of head g sits in lane
+    // (2t)*4 + g/2, token 2t+1 (2t+9) in the lane 4 higher.
+    const int src_a = (2 * t) * 4 + (g >> 1), src_b = src_a + 4;
+    const uint32_t half_sel = (g & 1) ? 0x7632u : 0x5410u;
+
+    bool ok = true;
+    for (int it = 0; it < n_iter; ++it) {
+      const int s = it % S;
+      if (!mbar_wait(smem_addr(&full_bar[s]), (it / S) & 1)) {
+        ok = false;
+        break;
+      }
+      const int j = it * kConsumers + w;
+      if (j < nblk) {
+        const uint32_t kb = stages + (uint32_t)((s * kConsumers + w) * G::kBlockBytes);
+        const uint32_t vb = kb + G::kTensorBytes;
+        const int valid = min(BS, L - (first_blk + j) * BS);
+        const float kfac = kInt8 ? score_scale * blk_ks[j] : score_scale;
+
+        // ---- scores S^T for every 16-token tile ---------------------------
+        float sc[G::kTiles][4];
+#pragma unroll
+        for (int tile = 0; tile < G::kTiles; ++tile) {
+          float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+          if constexpr (!kInt8) {
+            // ldmatrix.x4: matrix q = lane/8 covers rows (tokens) 8*(q&1)..+7
+            // and d-chunk 2ks + (q>>1): registers = A fragment a0..a3.
+            const int row = tile * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+#pragma unroll
+            for (int ks = 0; ks < G::kKSteps; ++ks) {
+              uint32_t fa[4];
+              ldsm_x4(fa, kb + chunk_off<G>(row, 2 * ks + (lane >> 4)));
+              if (ks & 1) mma16816<false>(c1, fa, qf[ks][0], qf[ks][1]);
+              else        mma16816<false>(c0, fa, qf[ks][0], qf[ks][1]);
+            }
+          } else {
+            // Rows g and g+8 of the tile; lane t reads its NC chunks of each.
+            constexpr int NC = D / 64;
+            uint32_t kw[2][NC][4];
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+              const int row = tile * 16 + g + 8 * rr;
+#pragma unroll
+              for (int ci = 0; ci < NC; ++ci) {
+                const uint4 v = lds128(kb + chunk_off<G>(row, t * NC + ci));
+                kw[rr][ci][0] = v.x ^ 0x80808080u;
+                kw[rr][ci][1] = v.y ^ 0x80808080u;
+                kw[rr][ci][2] = v.z ^ 0x80808080u;
+                kw[rr][ci][3] = v.w ^ 0x80808080u;
+              }
+            }
+#pragma unroll
+            for (int ks = 0; ks < G::kKSteps; ++ks) {
+              const uint32_t w0 = kw[0][ks / 4][ks % 4], w1 = kw[1][ks / 4][ks % 4];
+              const uint32_t fa[4] = {codes_to_f16x2(w0, 0x4140u), codes_to_f16x2(w1, 0x4140u),
+                                      codes_to_f16x2(w0, 0x4342u), codes_to_f16x2(w1, 0x4342u)};
+              if (ks & 1) mma16816<true>(c1, fa, qf[ks][0], qf[ks][1]);
+              else        mma16816<true>(c0, fa, qf[ks][0], qf[ks][1]);
+            }
+          }
+          // rows (tokens) g and g+8 of this tile; masked rows -> -inf
+          const int tok_lo = tile * 16 + g, tok_hi = tok_lo + 8;
+          sc[tile][0] = tok_lo < valid ? (c0[0] + c1[0]) * kfac : -INFINITY;
+          sc[tile][1] = tok_lo < valid ? (c0[1] + c1[1]) * kfac : -INFINITY;
+          sc[tile][2] = tok_hi < valid ? (c0[2] + c1[2]) * kfac : -INFINITY;
+          sc[tile][3] = tok_hi < valid ? (c0[3] + c1[3]) * kfac : -INFINITY;
+        }
+
+        // ---- online softmax update for heads 2t (index 0) and 2t+1 (1) ----
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int tile = 0; tile < G::kTiles; ++tile) {
+          mx0 = fmaxf(mx0, fmaxf(sc[tile][0], sc[tile][2]));
+          mx1 = fmaxf(mx1, fmaxf(sc[tile][1], sc[tile][3]));
+        }
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+        const float al0 = exp2f(m_run[0] - mn0), al1 = exp2f(m_run[1] - mn1);
+        m_run[0] = mn0;
+        m_run[1] = mn1;
+        l_run[0] *= al0;
+        l_run[1] *= al1;
+#pragma unroll
+        for (int i = 0; i < G::kMTiles; ++i) {
+          o[i][0] *= al0;
+          o[i][1] *= al1;
+          o[i][2] *= al0;
+          o[i][3] *= al1;
+        }
+        const float vr = kInt8 ? blk_vr[j] : 1.0f;
+
+#pragma unroll
+        for (int tile = 0; tile < G::kTiles; ++tile) {
+          if (tile * 16 >= valid) break;                    // whole tile masked
+          const float p0 = exp2f(sc[tile][0] - mn0), p1 = exp2f(sc[tile][1] - mn1);
+          const float p2 = exp2f(sc[tile][2] - mn0), p3 = exp2f(sc[tile][3] - mn1);
+          l_run[0] += p0 + p2;
+          l_run[1] += p1 + p3;
+          // P^T as the B operand: b0 = (tokens 2t, 2t+1; head g),
+          // b1 = (tokens 2t+8, 2t+9; head g), gathered from the lanes that
+          // hold those tokens' scores.
+          const uint32_t r0 = pack2<kF16>(p0 * vr, p1 * vr), r1 = pack2<kF16>(p2 * vr, p3 * vr);
+          const uint32_t x0 = __shfl_sync(0xffffffffu, r0, src_a);
+          const uint32_t x1 = __shfl_sync(0xffffffffu, r0, src_b);
+          const uint32_t y0 = __shfl_sync(0xffffffffu, r1, src_a);
+          const uint32_t y1 = __shfl_sync(0xffffffffu, r1, src_b);
+          const uint32_t pb0 = prmt(x0, x1, half_sel), pb1 = prmt(y0, y1, half_sel);
+
+          if constexpr (!kInt8) {
+            // V^T tiles by ldmatrix.trans: matrix q = lane/8 covers tokens
+            // 8*(q>>1)..+7 of the tile and d-chunk 2i + (q&1).
+            const int row = tile * 16 + (lane >> 4) * 8 + (lane & 7);
+            uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;  // rows past `valid` -> 0
+            if (valid < BS) {
+              const int k0 = tile * 16 + 2 * t;
+              mlo = (k0 < valid ? 0x0000ffffu : 0u) | (k0 + 1 < valid ? 0xffff0000u : 0u);
+              mhi = (k0 + 8 < valid ? 0x0000ffffu : 0u) | (k0 + 9 < valid ? 0xffff0000u : 0u);
+            }
+#pragma unroll
+            for (int i = 0; i < G::kMTiles; ++i) {
+              uint32_t fa[4];
+              ldsm_x4_t(fa, vb + chunk_off<G>(row, 2 * i + ((lane >> 3) & 1)));
+              fa[0] &= mlo;
+              fa[1] &= mlo;
+              fa[2] &= mhi;
+              fa[3] &= mhi;
+              mma16816<false>(o[i], fa, pb0, pb1);
+            }
+          } else {
+            // Lane (g, t) reads tokens 2t, 2t+1, 2t+8, 2t+9 of the tile, the
+            // D/8 bytes of d in [g*D/8, (g+1)*D/8); m-tile i pairs d rows
+            // g <-> g*D/8 + 2i and g+8 <-> g*D/8 + 2i + 1.  int8 codes are
+            // finite, and p = 0 for masked tokens, so no masking is needed.
+            constexpr int NB = D / 8;                 // bytes per lane per token
+            constexpr int NW = NB / 4;
+            uint32_t vw[4][NW];
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+              const int row = tile * 16 + 2 * t + (rr & 1) + 8 * (rr >> 1);
+              if constexpr (NB == 16) {
+                const uint4 v = lds128(vb + chunk_off<G>(row, g));
+                vw[rr][0] = v.x ^ 0x80808080u;
+                vw[rr][1] = v.y ^ 0x80808080u;
+                vw[rr][2] = v.z ^ 0x80808080u;
+                vw[rr][3] = v.w ^ 0x80808080u;
+              } else {
+                const uint2 v = lds64(vb + chunk_off<G>(row, g / 2) + (g & 1) * 8);
+                vw[rr][0] = v.x ^ 0x80808080u;
+                vw[rr][1] = v.y ^ 0x80808080u;
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < G::kMTiles; ++i) {
+              const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;  // bytes 2,3 or 0,1
+              const uint32_t ulo = prmt(vw[0][i / 2], vw[1][i / 2], sel);  // tokens 2t, 2t+1
+              const uint32_t uhi = prmt(vw[2][i / 2], vw[3][i / 2], sel);  // tokens 2t+8, 2t+9
+              const uint32_t fa[4] = {codes_to_f16x2(ulo, 0x4140u), codes_to_f16x2(ulo, 0x4342u),
+                                      codes_to_f16x2(uhi, 0x4140u), codes_to_f16x2(uhi, 0x4342u)};
+              mma16816<true>(o[i], fa, pb0, pb1);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&empty_bar[s]));
+    }
+    if (!ok) cta_timeout = 1;
+  }
+
+  // ---- combine the consumer warps -----------------------------------------
+  __syncthreads();  // all fills landed and all stage reads done
+  const bool failed = bad || cta_timeout != 0;
+  float* red = reinterpret_cast<float*>(smem_raw + (stages - smem_addr(smem_raw)));
+  float* red_m = red;                              // [kConsumers][8]
+  float* red_l = red + kConsumers * 8;             // [kConsumers][8]
+  float* red_acc = red + 2 * kConsumers * 8;       // [kConsumers][8][D]
+  if (!failed && warp < kConsumers) {
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], off);
+      l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], off);
+    }
+    if (g == 0) {
+      red_m[warp * 8 + 2 * t] = m_run[0];
+      red_m[warp * 8 + 2 * t + 1] = m_run[1];
+      red_l[warp * 8 + 2 * t] = l_run[0];
+      red_l[warp * 8 + 2 * t + 1] = l_run[1];
+    }
+    float* acc = red_acc + warp * 8 * D;
+#pragma unroll
+    for (int i = 0; i < G::kMTiles; ++i) {
+      int d_lo, d_hi;                              // d rows g and g+8 of m-tile i
+      if constexpr (kInt8) {
+        d_lo = g * (D / 8) + 2 * i;
+        d_hi = d_lo + 1;
+      } else {
+        d_lo = 16 * i + g;
+        d_hi = d_lo + 8;
+      }
+      acc[(2 * t) * D + d_lo] = o[i][0];
+      acc[(2 * t + 1) * D + d_lo] = o[i][1];
+      acc[(2 * t) * D + d_hi] = o[i][2];
+      acc[(2 * t + 1) * D + d_hi] = o[i][3];
+    }
+  }
+  __syncthreads();
+
+  if (failed) {
+    if (threadIdx.x == 0)
+      atomicOr(a.flags, bad ? PAGEDKV_FLAG_BAD_BLOCK : PAGEDKV_FLAG_WAIT_TIMEOUT);
+    for (int i = threadIdx.x; i < GQ * D; i += blockDim.x) {
+      const int hh = i / D, e = i % D;
       if (nparts == 1) {
         out[head0 * D + i] = __float2bfloat16_rn(0.0f);
       } else {
-        const int64_t r = (head0 + g) * a.max_parts + part;
+        const int64_t r = (head0 + hh) * a.max_parts + part;
         a.ws_acc[r * D + e] = 0.0f;
         if (e == 0) {
           a.ws_ml[2 * r] = 0.0f;
@@ -109,80 +624,24 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(DecodeArgs a) {
     return;
   }
 
-  float qr[G][E];
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int i = 0; i < E; ++i) qr[g][i] = qs[g][lane * E + i];
-
-  float m[G], l[G], acc[G][E];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    m[g] = -INFINITY;
-    l[g] = 0.0f;
-#pragma unroll
-    for (int i = 0; i < E; ++i) acc[g][i] = 0.0f;
-  }
-
-  for (int t = t0 + warp; t < t1; t += kWarps) {
-    const int32_t blk = bt[t / bs];
-    const int64_t row = (((int64_t)blk * bs + t % bs) * Hkv + hk) * D;
-    const float ks = kInt8 ? a.k_scale[(int64_t)blk * Hkv + hk] : 1.0f;
-    const float vs = kInt8 ? a.v_scale[(int64_t)blk * Hkv + hk] : 1.0f;
-    float k[E], v[E];
-    load_row<E, kInt8>(a.k_cache, row, lane, ks, k);
-    load_row<E, kInt8>(a.v_cache, row, lane, vs, v);
-    float s[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float x = 0.0f;
-#pragma unroll
-      for (int i = 0; i < E; ++i) x = fmaf(qr[g][i], k[i], x);
-      s[g] = x;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-      for (int g = 0; g < G; ++g) s[g] += __shfl_xor_sync(0xffffffffu, s[g], off);
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float m_new = fmaxf(m[g], s[g]);
-      const float alpha = exp2f(m[g] - m_new);
-      const float p = exp2f(s[g] - m_new);
-      l[g] = l[g] * alpha + p;
-#pragma unroll
-      for (int i = 0; i < E; ++i) acc[g][i] = fmaf(p, v[i], acc[g][i] * alpha);
-      m[g] = m_new;
-    }
-  }
-
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    if (lane == 0) {
-      red_m[warp][g] = m[g];
-      red_l[warp][g] = l[g];
-    }
-#pragma unroll
-    for (int i = 0; i < E; ++i) red_acc[warp][g][lane * E + i] = acc[g][i];
-  }
-  __syncthreads();
-
-  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-    const int g = i / D, e = i % D;
+  const float out_scale = kInt8 ? (v_max_scale > 0.0f ? v_max_scale : 1.0f) : 1.0f;
+  for (int i = threadIdx.x; i < GQ * D; i += blockDim.x) {
+    const int hh = i / D, e = i % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w][g]);
+    for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, red_m[w * 8 + hh]);
     float num = 0.0f, den = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const float c = exp2f(red_m[w][g] - M);  // 0 for a warp that saw no token
-      num = fmaf(c, red_acc[w][g][e], num);
-      den = fmaf(c, red_l[w][g], den);
+    for (int w = 0; w < kConsumers; ++w) {
+      const float c = exp2f(red_m[w * 8 + hh] - M);  // 0 for a warp that saw no token
+      num = fmaf(c, red_acc[(w * 8 + hh) * D + e], num);
+      den = fmaf(c, red_l[w * 8 + hh], den);
     }
+    num *= out_scale;
     if (nparts == 1) {
       out[head0 * D + i] = __float2bfloat16_rn(num / den);
     } else {
-      const int64_t r = (head0 + g) * a.max_parts + part;
+      const int64_t r = (head0 + hh) * a.max_parts + part;
       a.ws_acc[r * D + e] = num;
       if (e == 0) {
         a.ws_ml[2 * r] = M;
@@ -192,17 +651,77 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(DecodeArgs a) {
   }
 }
 
-template <int D, bool kInt8>
-kv_status launch_d(const DecodeArgs& a, dim3 grid, cudaStream_t s) {
-  const int G = a.num_q_heads / a.num_kv_heads;
-  switch (G) {
-    case 1: decode_kernel<D, 1, kInt8><<<grid, kWarps * 32, 0, s>>>(a); break;
-    case 2: decode_kernel<D, 2, kInt8><<<grid, kWarps * 32, 0, s>>>(a); break;
-    case 4: decode_kernel<D, 4, kInt8><<<grid, kWarps * 32, 0, s>>>(a); break;
-    case 8: decode_kernel<D, 8, kInt8><<<grid, kWarps * 32, 0, s>>>(a); break;
-    default: return fail(KV_ERR_INVALID_ARG, "unsupported query group %d", G);
+// ---------------------------------------------------------------------------
+// Host side: tensor maps and launch
+// ---------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 4-D map over a pool [NB, bs, Hkv, d] (innermost first: d, head, row, block)
+// whose box is one block's rows of one head: [1, bs, 1, box elements].
+template <int D, int BS, bool kInt8>
+kv_status make_map(CUtensorMap* map, const void* pool, const DecodeArgs& a) {
+  using G = Geo<D, BS, kInt8>;
+  auto fn = encode_fn();
+  if (!fn) return fail(KV_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)a.num_kv_heads, (cuuint64_t)BS,
+                              (cuuint64_t)a.num_blocks};
+  const cuuint64_t strides[3] = {(cuuint64_t)D * G::kElem,
+                                 (cuuint64_t)a.num_kv_heads * D * G::kElem,
+                                 (cuuint64_t)BS * a.num_kv_heads * D * G::kElem};
+  const cuuint32_t box[4] = {(cuuint32_t)G::kBoxElems, 1, (cuuint32_t)BS, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(map, kInt8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        4, const_cast<void*>(pool), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        G::kSwizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(KV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return KV_OK;
+}
+
+template <int D, int BS, bool kInt8>
+kv_status launch_t(const DecodeArgs& a, cudaStream_t s) {
+  using G = Geo<D, BS, kInt8>;
+  static std::mutex mu;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  kv_status st = cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
+  if (st != KV_OK) return st;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+      st = cuda_check(cudaFuncSetAttribute(decode_kernel<D, BS, kInt8>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           G::kSmemBytes),
+                      "cudaFuncSetAttribute(decode_kernel)");
+      if (st != KV_OK) return st;
+      attr_set[dev] = true;
+    }
   }
+  alignas(64) CUtensorMap km, vm;
+  if ((st = make_map<D, BS, kInt8>(&km, a.k_cache, a)) != KV_OK) return st;
+  if ((st = make_map<D, BS, kInt8>(&vm, a.v_cache, a)) != KV_OK) return st;
+  const dim3 grid(a.max_parts, a.num_kv_heads, a.batch);
+  decode_kernel<D, BS, kInt8><<<grid, kThreads, G::kSmemBytes, s>>>(km, vm, a);
   return cuda_check(cudaGetLastError(), "decode_kernel launch");
+}
+
+template <int D, bool kInt8>
+kv_status launch_bs(const DecodeArgs& a, cudaStream_t s) {
+  return a.block_size == 32 ? launch_t<D, 32, kInt8>(a, s) : launch_t<D, 16, kInt8>(a, s);
 }
 
 }  // namespace
@@ -210,10 +729,14 @@ kv_status launch_d(const DecodeArgs& a, dim3 grid, cudaStream_t s) {
 kv_status launch_decode(const DecodeArgs& a, cudaStream_t s) {
   if (a.batch > 65535 || a.num_kv_heads > 65535)
     return fail(KV_ERR_INVALID_ARG, "batch and num_kv_heads must be at most 65535");
-  const dim3 grid(a.max_parts, a.num_kv_heads, a.batch);
+  if (a.num_q_heads / a.num_kv_heads > 8)
+    return fail(KV_ERR_INVALID_ARG, "at most 8 query heads per KV head");
+  if (a.part_tokens / a.block_size > kMaxBlocks || a.part_tokens % a.block_size)
+    return fail(KV_ERR_INVALID_ARG, "partition must be a multiple of block_size, at most %d blocks",
+                kMaxBlocks);
   const bool int8 = a.dtype == KV_DTYPE_INT8;
-  if (a.head_dim == 128) return int8 ? launch_d<128, true>(a, grid, s) : launch_d<128, false>(a, grid, s);
-  return int8 ? launch_d<64, true>(a, grid, s) : launch_d<64, false>(a, grid, s);
+  if (a.head_dim == 128) return int8 ? launch_bs<128, true>(a, s) : launch_bs<128, false>(a, s);
+  return int8 ? launch_bs<64, true>(a, s) : launch_bs<64, false>(a, s);
 }
 
 }  // namespace pagedkv
