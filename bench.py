@@ -1,11 +1,14 @@
 #!/usr/bin/env python3
 """Decode-step benchmark of paged attention on GB300.
 
-One step = the whole hot path over one synthetic decode batch: slot mapping
-of each sequence's new token, the append (reshape_and_cache), and the paged
-attention (per-partition decode kernel + log-sum-exp merge when a sequence
-spans several partitions).  The default workload is the Llama-3.1-8B-like
-decode layer (B 64, 32/8 heads, d 128, 16-token blocks, lengths U{512..4096}).
+One step = the whole hot path over one synthetic decode batch through
+pagedkv_decode_step: the slot of each sequence's new token, its append into
+the pool, and the paged attention (the per-partition decode kernel, with the
+append fused in, plus the log-sum-exp merge of sequences that span several
+partitions).  The same step as three calls (slot mapping, reshape_and_cache,
+paged_attention_decode) is timed beside it.  The default workload is the
+Llama-3.1-8B-like decode layer (B 64, 32/8 heads, d 128, 16-token blocks,
+lengths U{512..4096}).
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
 the same workload instead (the reference arm: a plain fp64 program, not a
@@ -236,10 +239,10 @@ def gpu_arm(args, rank, world, local_rank, dist):
     stream = torch.cuda.current_stream(dev)
     nbytes = algorithmic_bytes(wl)
     part = pkv.partition_tokens(s.batch, s.num_kv_heads, g.max_seq_len, s.block_size)
-    merge = g.max_seq_len > part
-    launches_per_step = 3 + (1 if merge else 0)
+    launches_per_step = 1 + (1 if g.max_seq_len > part else 0)   # decode (append fused) + merge
 
     for _ in range(args.warmup):
+        g.fused_step()
         g.step()
     torch.cuda.synchronize(dev)
     st, flags = pkv.get_status()
@@ -247,7 +250,7 @@ def gpu_arm(args, rank, world, local_rank, dist):
 
     # ---- device-resident timed region ---------------------------------
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     sampler = ClockSampler(torch.cuda.get_device_properties(dev).uuid.__str__())
     if dist is not None:
         dist.barrier()
@@ -255,16 +258,28 @@ def gpu_arm(args, rank, world, local_rank, dist):
     with sampler:
         for i in range(K):
             ev[i][0].record(stream)
-            g.append()
+            g.fused_step()
             ev[i][1].record(stream)
-            g.attend()
-            ev[i][2].record(stream)
         torch.cuda.synchronize(dev)
     if dist is not None:
         dist.barrier()
-    total_ms = ev[0][0].elapsed_time(ev[-1][2])
-    attn_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    total_ms = ev[0][0].elapsed_time(ev[-1][1])
+    step_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     ms_step = total_ms / K
+
+    # the same step as three calls (slot mapping, append, attention), for reference
+    K3 = max(K // 4, 10)
+    ev3 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K3)]
+    torch.cuda.synchronize(dev)
+    for i in range(K3):
+        ev3[i][0].record(stream)
+        g.append()
+        ev3[i][1].record(stream)
+        g.attend()
+        ev3[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    unfused_ms = ev3[0][0].elapsed_time(ev3[-1][2]) / K3
+    attn_only_ms = statistics.fmean(ev3[i][1].elapsed_time(ev3[i][2]) for i in range(K3))
     elapsed, agg_bytes_per_s = aggregate(total_ms / 1e3, nbytes["kv_logical"] * K, world, dist)
     value = agg_bytes_per_s / 1e9
     st, flags = pkv.get_status()
@@ -290,7 +305,7 @@ def gpu_arm(args, rank, world, local_rank, dist):
         g.new_v.copy_(h_v, non_blocking=True)
         g.block_tables.copy_(h_bt, non_blocking=True)
         g.seq_lens.copy_(h_sl, non_blocking=True)
-        g.step()
+        g.fused_step()
         h_out.copy_(g.out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize(dev)
@@ -298,8 +313,8 @@ def gpu_arm(args, rank, world, local_rank, dist):
     _, e2e_agg = aggregate(e2e_ms / 1e3, nbytes["kv_logical"], world, dist)
 
     peak, peak_kind = measured_peak_gbs()
-    attn_mean_ms = statistics.fmean(attn_ms)
-    achieved = nbytes["attention"] / (attn_mean_ms / 1e3) / 1e9
+    step_mean_ms = statistics.fmean(step_ms)
+    achieved = nbytes["step"] / (step_mean_ms / 1e3) / 1e9
     traffic = stored_traffic(s.name)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
@@ -317,11 +332,15 @@ def gpu_arm(args, rank, world, local_rank, dist):
                    "kv_bytes_per_step": nbytes["kv_logical"], "partition_tokens": part,
                    "l2": "inputs larger than L2 (KV read per step > 129 MB), no flush",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "kernel": "paged_attention_decode (decode + merge launches)",
+        "roofline": {"bound": "hbm",
+                     "kernel": "decode_kernel (append fused) + merge_kernel, one pagedkv_decode_step",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                     "algorithmic_bytes_per_launch": nbytes["attention"],
-                     "us_per_launch": round(attn_mean_ms * 1e3, 2), "traffic": traffic},
+                     "algorithmic_bytes_per_launch": nbytes["step"],
+                     "us_per_launch": round(step_mean_ms * 1e3, 2), "traffic": traffic},
+        "unfused": {"us_per_step": round(unfused_ms * 1e3, 2),
+                    "attention_us": round(attn_only_ms * 1e3, 2),
+                    "note": "slot mapping + reshape_and_cache + paged_attention_decode as three calls"},
         "e2e": {"value": round(e2e_agg / 1e9, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
         "gpu_launches": launches_per_step * K,

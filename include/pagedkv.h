@@ -170,8 +170,9 @@ kv_status reshape_and_cache(const void *k, const void *v, void *k_cache,
 /* Attention                                                                */
 /* ------------------------------------------------------------------------ */
 
-/* Workspace bytes paged_attention_decode may need for the split-K partials of
- * this shape (an upper bound over every partition size the library picks). */
+/* Workspace bytes paged_attention_decode / pagedkv_decode_step may need for
+ * the split-K partials of this shape (an upper bound over every partition
+ * size the library picks; 0 when every sequence fits one partition). */
 size_t pagedkv_workspace_bytes(int batch, int num_q_heads, int head_dim,
                                int max_seq_len, int block_size);
 
@@ -179,8 +180,10 @@ size_t pagedkv_workspace_bytes(int batch, int num_q_heads, int head_dim,
  * t < seq_lens[b] tokens of sequence b (“LLM 推理优化技术全景”: 在线 Softmax,
  * computed with the recurrence m' = max(m, max s), l' = l e^(m-m') + sum
  * e^(s-m'), and the rescale deferred to the end as in “Flash Attention v2 的
- * 改进”; long sequences are split into token partitions whose partials
- * (m, l, unnormalised acc) are merged by log-sum-exp in a second kernel).
+ * 改进”).  Each (sequence, KV head) is cut into token partitions; one CTA
+ * serves a partition for all query heads of the KV head, and a sequence with
+ * several partitions has their partials (m, l, unnormalised acc) merged by
+ * log-sum-exp in a second kernel launched behind the first.
  *   out           device bf16 [batch, num_q_heads, head_dim] (output)
  *   q             device bf16 [batch, num_q_heads, head_dim]
  *   k_cache, v_cache, k_scale, v_scale   as for reshape_and_cache
@@ -190,7 +193,8 @@ size_t pagedkv_workspace_bytes(int batch, int num_q_heads, int head_dim,
  *   max_seq_len   host bound on every seq_lens[b] (sizes the partitions)
  *   scale         softmax scale (1/sqrt(head_dim) for the usual attention)
  *   workspace     device memory of at least pagedkv_workspace_bytes(...)
- *                 bytes, 16-byte aligned; may be NULL when that size is 0
+ *                 bytes, 16-byte aligned; may be NULL when that size is 0.
+ *                 Calls that overlap on the GPU need separate workspaces.
  * Rows past seq_lens[b] inside the last block and blocks not in the table
  * are never used, whatever they hold. */
 kv_status paged_attention_decode(void *out, const void *q, const void *k_cache,
@@ -204,6 +208,28 @@ kv_status paged_attention_decode(void *out, const void *q, const void *k_cache,
                                  int max_seq_len, float scale, kv_dtype dtype,
                                  void *workspace, size_t workspace_bytes,
                                  void *stream);
+
+/* One decode step in two launches: append each sequence's new token (k[b],
+ * v[b] at position seq_lens[b] - 1, exactly as pagedkv_slot_mapping +
+ * reshape_and_cache would) and then attend as paged_attention_decode.  The
+ * append runs inside the attention kernel: the CTA that streams a (b, h)'s
+ * last block writes the new row first and orders that write before its own
+ * read of the block (“让 Agent 跑得快”, §五 共享前缀: only the current token
+ * writes, so no other reader of the step can see the row).
+ *   k, v  device bf16 [batch, num_kv_heads, head_dim]
+ * Other arguments as paged_attention_decode (the pools are written).  The new
+ * token's block must not be read by another sequence in the same step (shared
+ * prefix blocks are full, so appends land in private blocks). */
+kv_status pagedkv_decode_step(void *out, const void *q, const void *k,
+                              const void *v, void *k_cache, void *v_cache,
+                              const float *k_scale, const float *v_scale,
+                              const int32_t *block_tables,
+                              int max_blocks_per_seq, const int32_t *seq_lens,
+                              int batch, int num_q_heads, int num_kv_heads,
+                              int head_dim, int num_blocks, int block_size,
+                              int max_seq_len, float scale, kv_dtype dtype,
+                              void *workspace, size_t workspace_bytes,
+                              void *stream);
 
 /* Size of the fixed device scratch paged_attention_decode_noalloc uses. */
 #define PAGEDKV_NOALLOC_SCRATCH_BYTES (32u << 20)
@@ -258,8 +284,10 @@ kv_status pagedkv_get_status(void *stream, unsigned int *device_flags);
 const char *pagedkv_last_error(void);
 
 /* Token partition size paged_attention_decode would use for this shape on
- * the current device (0 on error); partitions of more than one per sequence
- * go through the merge kernel. */
+ * the current device (0 on error): the largest power of two in [256, 8192]
+ * that still gives at least 8 CTAs per SM.  Sequences longer than one
+ * partition go through the merge kernel.  The environment variable
+ * PAGEDKV_PARTITION_TOKENS (a multiple of 256) overrides it. */
 int pagedkv_partition_tokens(int batch, int num_kv_heads, int max_seq_len,
                              int block_size);
 

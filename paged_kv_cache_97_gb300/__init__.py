@@ -46,6 +46,8 @@ SIGNATURES = {
     "pagedkv_get_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
     "pagedkv_last_error": (ctypes.c_char_p, []),
     "pagedkv_partition_tokens": (_I, [_I, _I, _I, _I]),
+    "pagedkv_decode_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
+                                 _I, _I, _F, _I, _P, _SZ, _P]),
 }
 
 _lib = None
@@ -229,34 +231,64 @@ def workspace_bytes(batch, num_q_heads, head_dim, max_seq_len, block_size) -> in
 
 
 def partition_tokens(batch, num_kv_heads, max_seq_len, block_size) -> int:
+    """Token partition size the decode kernel uses for this shape."""
     return load().pagedkv_partition_tokens(batch, num_kv_heads, max_seq_len, block_size)
 
 
-def paged_attention_decode(out, q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, scale,
-                           workspace=None, k_scale=None, v_scale=None, stream=None):
-    """out[b, h] = softmax(scale q[b, h] . K) V over sequence b's paged tokens."""
+def _check_decode(out, q, k_cache, v_cache, block_tables, seq_lens, k_scale, v_scale, workspace):
     import torch
     _need(out, torch.bfloat16, "out", 3)
     _need(q, torch.bfloat16, "q", 3)
-    dt = _pool_dtype(k_cache)
+    _pool_dtype(k_cache)
     _need(k_cache, k_cache.dtype, "k_cache", 4)
     _need(v_cache, k_cache.dtype, "v_cache", 4)
     _need(block_tables, torch.int32, "block_tables", 2)
     _need(seq_lens, torch.int32, "seq_lens", 1)
     B, hq, d = q.shape
-    nb, bs, hkv, d2 = k_cache.shape
-    if out.shape != q.shape or d2 != d or v_cache.shape != k_cache.shape:
+    if out.shape != q.shape or k_cache.shape[3] != d or v_cache.shape != k_cache.shape:
         raise ValueError("q, out and the pools disagree")
     if block_tables.shape[0] != B or seq_lens.shape[0] != B:
         raise ValueError("block_tables / seq_lens must have one row per sequence")
     for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
         if t is not None:
             _need(t, torch.float32, name, 2)
-    wbytes = 0
-    if workspace is not None:
-        if not workspace.is_cuda or not workspace.is_contiguous():
-            raise ValueError("workspace must be a contiguous CUDA tensor")
-        wbytes = workspace.numel() * workspace.element_size()
+    if workspace is None:
+        return 0
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    return workspace.numel() * workspace.element_size()
+
+
+def decode_step(out, q, k, v, k_cache, v_cache, block_tables, seq_lens, max_seq_len, scale,
+                workspace, k_scale=None, v_scale=None, stream=None):
+    """Append k[b], v[b] (bf16 [B, Hkv, d]) at position seq_lens[b] - 1 and
+    attend, in two launches (the append runs inside the attention kernel)."""
+    import torch
+    wbytes = _check_decode(out, q, k_cache, v_cache, block_tables, seq_lens, k_scale, v_scale,
+                           workspace)
+    _need(k, torch.bfloat16, "k", 3)
+    _need(v, torch.bfloat16, "v", 3)
+    B, hq, d = q.shape
+    nb, bs, hkv, _ = k_cache.shape
+    if k.shape != (B, hkv, d) or v.shape != k.shape:
+        raise ValueError("k, v must be [batch, num_kv_heads, head_dim]")
+    _check(load().pagedkv_decode_step(_ptr(out), _ptr(q), _ptr(k), _ptr(v), _ptr(k_cache),
+                                      _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                      _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B,
+                                      hq, hkv, d, nb, bs, int(max_seq_len), float(scale),
+                                      _pool_dtype(k_cache), _ptr(workspace), wbytes,
+                                      _stream(stream)))
+    return out
+
+
+def paged_attention_decode(out, q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, scale,
+                           workspace=None, k_scale=None, v_scale=None, stream=None):
+    """out[b, h] = softmax(scale q[b, h] . K) V over sequence b's paged tokens."""
+    wbytes = _check_decode(out, q, k_cache, v_cache, block_tables, seq_lens, k_scale, v_scale,
+                           workspace)
+    B, hq, d = q.shape
+    nb, bs, hkv, _ = k_cache.shape
+    dt = _pool_dtype(k_cache)
     _check(load().paged_attention_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                          _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
                                          block_tables.shape[1], _ptr(seq_lens), B, hq, hkv, d, nb, bs,

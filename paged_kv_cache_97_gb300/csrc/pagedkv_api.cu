@@ -59,7 +59,7 @@ kv_status device_info(DeviceInfo* out) {
   return KV_OK;
 }
 
-static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }  // NULL passes
 
 static int dtype_size(kv_dtype t) { return t == KV_DTYPE_INT8 ? 1 : 2; }
 
@@ -185,6 +185,9 @@ __global__ void merge_kernel(__nv_bfloat16* __restrict__ out, const float* __res
                              const int32_t* __restrict__ seq_lens, int num_q_heads,
                              int head_dim, int part_tokens, int max_parts, int max_len) {
   const int b = blockIdx.x / num_q_heads, h = blockIdx.x % num_q_heads;
+  // Launched as a programmatic dependent of the decode kernel: wait until
+  // that grid has completed and its partials are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int L = seq_lens[b];
   if (L <= 0 || L > max_len) return;  // invalid length: the decode kernel zeroed the row
   const int np = (L + part_tokens - 1) / part_tokens;
@@ -219,10 +222,21 @@ static int valid_len_limit(const DecodeArgs& a) {
 
 kv_status launch_merge(const DecodeArgs& a, cudaStream_t stream) {
   if (a.max_parts <= 1) return KV_OK;
-  merge_kernel<<<a.batch * a.num_q_heads, a.head_dim, 0, stream>>>(
-      static_cast<__nv_bfloat16*>(a.out), a.ws_ml, a.ws_acc, a.seq_lens, a.num_q_heads,
-      a.head_dim, a.part_tokens, a.max_parts, valid_len_limit(a));
-  return cuda_check(cudaGetLastError(), "merge_kernel launch");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(a.batch * a.num_q_heads));
+  cfg.blockDim = dim3((unsigned)a.head_dim);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_check(cudaLaunchKernelEx(&cfg, merge_kernel, static_cast<__nv_bfloat16*>(a.out),
+                                       (const float*)a.ws_ml, (const float*)a.ws_acc, a.seq_lens,
+                                       a.num_q_heads, a.head_dim, a.part_tokens, a.max_parts,
+                                       valid_len_limit(a)),
+                    "merge_kernel launch");
 }
 
 // ---------------------------------------------------------------------------
@@ -429,38 +443,40 @@ int pagedkv_partition_tokens(int batch, int num_kv_heads, int max_seq_len, int b
   return choose_part_tokens(batch, num_kv_heads, max_seq_len, di.num_sms);
 }
 
-kv_status paged_attention_decode(void* out, const void* q, const void* k_cache,
-                                 const void* v_cache, const float* k_scale, const float* v_scale,
-                                 const int32_t* block_tables, int max_blocks_per_seq,
-                                 const int32_t* seq_lens, int batch, int num_q_heads,
-                                 int num_kv_heads, int head_dim, int num_blocks, int block_size,
-                                 int max_seq_len, float scale, kv_dtype dtype, void* workspace,
-                                 size_t workspace_bytes, void* stream) {
+// Shared body of paged_attention_decode and pagedkv_decode_step.
+static kv_status decode_common(void* out, const void* q, const void* new_k, const void* new_v,
+                               const void* k_cache, const void* v_cache, const float* k_scale,
+                               const float* v_scale, const int32_t* block_tables,
+                               int max_blocks_per_seq, const int32_t* seq_lens, int batch,
+                               int num_q_heads, int num_kv_heads, int head_dim, int num_blocks,
+                               int block_size, int max_seq_len, float scale, kv_dtype dtype,
+                               void* workspace, size_t workspace_bytes, void* stream,
+                               const char* who) {
   if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads ||
       max_blocks_per_seq <= 0 || num_blocks <= 0 || max_seq_len <= 0 || !valid_dtype(dtype))
-    return fail(KV_ERR_INVALID_ARG, "paged_attention_decode: bad sizes");
+    return fail(KV_ERR_INVALID_ARG, "%s: bad sizes", who);
   const int G = num_q_heads / num_kv_heads;
   if (G > 8)
-    return fail(KV_ERR_INVALID_ARG,
-                "paged_attention_decode: at most 8 query heads per KV head (got %d)", G);
+    return fail(KV_ERR_INVALID_ARG, "%s: at most 8 query heads per KV head (got %d)", who, G);
   if (head_dim != 64 && head_dim != 128)
-    return fail(KV_ERR_INVALID_ARG, "paged_attention_decode: head_dim must be 64 or 128");
+    return fail(KV_ERR_INVALID_ARG, "%s: head_dim must be 64 or 128", who);
   if (block_size != 16 && block_size != 32)
-    return fail(KV_ERR_INVALID_ARG, "paged_attention_decode: block_size must be 16 or 32");
+    return fail(KV_ERR_INVALID_ARG, "%s: block_size must be 16 or 32", who);
   if (batch == 0) return KV_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens)
-    return fail(KV_ERR_INVALID_ARG, "paged_attention_decode: NULL pointer");
-  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
-    return fail(KV_ERR_INVALID_ARG, "paged_attention_decode: out, q and the pools must be 16-byte aligned");
+    return fail(KV_ERR_INVALID_ARG, "%s: NULL pointer", who);
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(new_k) || !aligned16(new_v))
+    return fail(KV_ERR_INVALID_ARG, "%s: out, q, k, v and the pools must be 16-byte aligned", who);
   const bool int8 = dtype == KV_DTYPE_INT8;
   if (int8 != (k_scale != nullptr) || int8 != (v_scale != nullptr))
     return fail(KV_ERR_INVALID_ARG,
-                "paged_attention_decode: int8 pools need k_scale and v_scale; bf16 pools take NULL");
+                "%s: int8 pools need k_scale and v_scale; bf16 pools take NULL", who);
   DeviceInfo di;
   kv_status st = device_info(&di);
   if (st != KV_OK) return st;
 
-  DecodeArgs a;
+  DecodeArgs a = {};
   a.out = out;
   a.q = q;
   a.k_cache = k_cache;
@@ -469,6 +485,8 @@ kv_status paged_attention_decode(void* out, const void* q, const void* k_cache,
   a.v_scale = v_scale;
   a.block_tables = block_tables;
   a.seq_lens = seq_lens;
+  a.new_k = new_k;
+  a.new_v = new_v;
   a.flags = di.flags;
   a.max_blocks_per_seq = max_blocks_per_seq;
   a.batch = batch;
@@ -489,8 +507,8 @@ kv_status paged_attention_decode(void* out, const void* q, const void* k_cache,
     const size_t need = ml_bytes + (size_t)batch * num_q_heads * a.max_parts * head_dim * sizeof(float);
     if (!workspace || workspace_bytes < need || !aligned16(workspace))
       return fail(KV_ERR_INVALID_ARG,
-                  "paged_attention_decode: workspace must be 16-byte aligned and hold %zu bytes "
-                  "(pagedkv_workspace_bytes gives a safe size)", need);
+                  "%s: workspace must be 16-byte aligned and hold %zu bytes "
+                  "(pagedkv_workspace_bytes gives a safe size)", who, need);
     a.ws_ml = static_cast<float*>(workspace);
     a.ws_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + ml_bytes);
   }
@@ -498,6 +516,34 @@ kv_status paged_attention_decode(void* out, const void* q, const void* k_cache,
   st = launch_decode(a, s);
   if (st != KV_OK) return st;
   return launch_merge(a, s);
+}
+
+kv_status paged_attention_decode(void* out, const void* q, const void* k_cache,
+                                 const void* v_cache, const float* k_scale, const float* v_scale,
+                                 const int32_t* block_tables, int max_blocks_per_seq,
+                                 const int32_t* seq_lens, int batch, int num_q_heads,
+                                 int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                                 int max_seq_len, float scale, kv_dtype dtype, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  return decode_common(out, q, nullptr, nullptr, k_cache, v_cache, k_scale, v_scale,
+                       block_tables, max_blocks_per_seq, seq_lens, batch, num_q_heads,
+                       num_kv_heads, head_dim, num_blocks, block_size, max_seq_len, scale, dtype,
+                       workspace, workspace_bytes, stream, "paged_attention_decode");
+}
+
+kv_status pagedkv_decode_step(void* out, const void* q, const void* k, const void* v,
+                              void* k_cache, void* v_cache, const float* k_scale,
+                              const float* v_scale, const int32_t* block_tables,
+                              int max_blocks_per_seq, const int32_t* seq_lens, int batch,
+                              int num_q_heads, int num_kv_heads, int head_dim, int num_blocks,
+                              int block_size, int max_seq_len, float scale, kv_dtype dtype,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  if (batch > 0 && (!k || !v))
+    return fail(KV_ERR_INVALID_ARG, "pagedkv_decode_step: NULL k or v");
+  return decode_common(out, q, k, v, k_cache, v_cache, k_scale, v_scale, block_tables,
+                       max_blocks_per_seq, seq_lens, batch, num_q_heads, num_kv_heads, head_dim,
+                       num_blocks, block_size, max_seq_len, scale, dtype, workspace,
+                       workspace_bytes, stream, "pagedkv_decode_step");
 }
 
 kv_status pagedkv_get_status(void* stream, unsigned int* device_flags) {

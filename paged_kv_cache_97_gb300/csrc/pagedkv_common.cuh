@@ -35,6 +35,8 @@ struct DecodeArgs {
   const float* v_scale;
   const int32_t* block_tables; // [B, MB]
   const int32_t* seq_lens;     // [B]
+  const void* new_k;           // bf16 [B, Hkv, D] appended in the same launch, or null
+  const void* new_v;
   float* ws_ml;                // [B, Hq, max_parts, 2]   (m, l) per partition
   float* ws_acc;               // [B, Hq, max_parts, D]   unnormalised acc
   unsigned int* flags;
@@ -45,9 +47,11 @@ struct DecodeArgs {
   kv_dtype dtype;
 };
 
-// Launches the per-partition decode kernel (and nothing else).
+// Launches the per-partition decode kernel (with the append fused in when
+// new_k is set).
 kv_status launch_decode(const DecodeArgs& a, cudaStream_t stream);
-// Launches the log-sum-exp merge of the partitions (only when max_parts > 1).
+// Launches the log-sum-exp merge of the partitions (only when max_parts > 1),
+// as a programmatic dependent of the decode kernel.
 kv_status launch_merge(const DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace pagedkv

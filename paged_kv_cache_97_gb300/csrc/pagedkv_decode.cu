@@ -206,6 +206,14 @@ __device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t w_biased, uint32_t s
   return *reinterpret_cast<const uint32_t*>(&x);
 }
 
+__device__ __forceinline__ int8_t quantize(float x, float s) {
+  // clamp(round_half_even(x / s), -127, 127) with an IEEE fp32 divide.
+  if (s == 0.0f) s = 1.0f;
+  int c = __float2int_rn(__fdiv_rn(x, s));
+  c = c > 127 ? 127 : (c < -127 ? -127 : c);
+  return (int8_t)c;
+}
+
 // Byte offset of 16-byte chunk `c` of row `r` inside one K or V block of a
 // stage.  Rows of a box are kBoxRow bytes; with SWIZZLE_128B the chunk index
 // inside each 128-byte row is XORed with (row mod 8), the pattern TMA writes
@@ -274,7 +282,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  __syncthreads();
+  // Consumers start their q loads now, so they overlap the block-id loads.
+  // Q^T fragments (B operand of S^T = K . Q^T): b0 = (k = 2t, 2t+1; n = g),
+  // b1 = (k = 2t+8, 2t+9; n = g).  k indexes d: for bf16 the natural order
+  // 16ks + k; for int8 the order in which each lane reads its own 16-byte
+  // chunks of a K row (see the int8 K loads below).
+  uint32_t qraw[G::kKSteps][2];
+  if (warp < kConsumers) {
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q) + (head0 + g) * D;
+#pragma unroll
+    for (int ks = 0; ks < G::kKSteps; ++ks) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        int d0;
+        if constexpr (kInt8) {
+          // lane t reads chunks t*NC .. t*NC+NC-1 (16 d each, NC = D/64)
+          // of a row; k-step ks uses 4 consecutive d of chunk ks/4.
+          constexpr int NC = D / 64;
+          d0 = 16 * (t * NC + ks / 4) + 4 * (ks % 4) + 2 * r;
+        } else {
+          d0 = 16 * ks + 2 * t + 8 * r;
+        }
+        qraw[ks][r] = g < GQ ? *reinterpret_cast<const uint32_t*>(q + d0) : 0u;
+      }
+    }
+  }
+  __syncthreads();  // barriers and flags initialised
   const int32_t* bt = a.block_tables + (int64_t)b * a.max_blocks_per_seq + first_blk;
   for (int j = threadIdx.x; j < nblk; j += blockDim.x) {
     const int32_t p = bt[j];
@@ -310,17 +343,52 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (!bad && warp == kConsumers) {
     // ======================= producer =======================================
-    if (lane == 0) {
-      int issued = 0;
-      bool ok = true;
-      for (int it = 0; it < n_iter; ++it) {
-        const int s = it % S;
-        if (it >= S && !mbar_wait(smem_addr(&empty_bar[s]), ((it / S) - 1) & 1)) {
-          ok = false;
-          break;
+    // The whole warp walks the stages (lane 0 issues the loads).  When this
+    // partition ends the sequence and a new token is given, the warp first
+    // writes that token's K/V row into the last block and orders the write
+    // before the TMA read of the block (the append, fused into this launch).
+    const bool append = a.new_k != nullptr && t1 == L;
+    int issued = 0;
+    bool ok = true;
+    for (int it = 0; it < n_iter; ++it) {
+      const int s = it % S;
+      if (it >= S && !mbar_wait(smem_addr(&empty_bar[s]), ((it / S) - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      const int j0 = it * kConsumers;
+      const int cnt = min(kConsumers, nblk - j0);
+      if (append && j0 + cnt == nblk) {
+        constexpr int kChunks = D / 8;                 // 8 elements per lane
+        const int p = blk_id[nblk - 1];
+        const int row = (L - 1) % BS;
+        const int64_t dst = (((int64_t)p * BS + row) * Hkv + hk) * D;
+        const int64_t src = ((int64_t)b * Hkv + hk) * D;
+        if (lane < 2 * kChunks) {
+          const bool is_v = lane >= kChunks;
+          const int e0 = (is_v ? lane - kChunks : lane) * 8;
+          const uint4 x = *reinterpret_cast<const uint4*>(
+              static_cast<const __nv_bfloat16*>(is_v ? a.new_v : a.new_k) + src + e0);
+          void* pool = const_cast<void*>(is_v ? a.v_cache : a.k_cache);
+          if constexpr (kInt8) {
+            const float sc = is_v ? a.v_scale[(int64_t)p * Hkv + hk] : blk_ks[nblk - 1];
+            const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+            uint32_t o2[2] = {0u, 0u};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t lo = (uint8_t)quantize(__uint_as_float(w4[i] << 16), sc);
+              const uint32_t hi = (uint8_t)quantize(__uint_as_float(w4[i] & 0xffff0000u), sc);
+              o2[i / 2] |= (lo | (hi << 8)) << (16 * (i % 2));
+            }
+            *reinterpret_cast<uint2*>(static_cast<int8_t*>(pool) + dst + e0) = make_uint2(o2[0], o2[1]);
+          } else {
+            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(pool) + dst + e0) = x;
+          }
         }
-        const int j0 = it * kConsumers;
-        const int cnt = min(kConsumers, nblk - j0);
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        __syncwarp();
+      }
+      if (lane == 0) {
         const uint32_t fb = smem_addr(&full_bar[s]);
         mbar_expect_tx(fb, (uint32_t)(cnt * G::kBlockBytes));
         for (int c = 0; c < cnt; ++c) {
@@ -333,46 +401,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_4d(vdst + x * G::kBoxBytes, &v_map, fb, x * G::kBoxElems, hk, 0, p);
           }
         }
-        issued = it + 1;
       }
-      // Wait for every fill this thread issued before the CTA may reuse or
-      // release the stages (bounded; normally already complete).
-      for (int s = 0; s < S && s < issued; ++s) {
-        const int last = s + S * ((issued - 1 - s) / S);
-        if (!mbar_wait(smem_addr(&full_bar[s]), (last / S) & 1)) ok = false;
-      }
-      if (!ok) cta_timeout = 1;
+      __syncwarp();
+      issued = it + 1;
     }
+    // Wait for every fill this warp issued before the CTA may reuse or
+    // release the stages (bounded; normally already complete).
+    for (int s = 0; s < S && s < issued; ++s) {
+      const int last = s + S * ((issued - 1 - s) / S);
+      if (!mbar_wait(smem_addr(&full_bar[s]), (last / S) & 1)) ok = false;
+    }
+    if (!ok && lane == 0) cta_timeout = 1;
   } else if (!bad) {
     // ======================= consumers =====================================
     const int w = warp;
     constexpr bool kF16 = kInt8;
-    // Q^T fragments (B operand of S^T = K . Q^T): b0 = (k = 2t, 2t+1; n = g),
-    // b1 = (k = 2t+8, 2t+9; n = g).  k indexes d: for bf16 the natural order
-    // 16ks + k; for int8 the order in which each lane reads its own 16-byte
-    // chunks of a K row (see the int8 K loads below).
     uint32_t qf[G::kKSteps][2];
     float qscale = 1.0f;
     {
-      const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q) + (head0 + g) * D;
-      const bool live = g < GQ;
-      float amax = 0.0f;
       float qv[G::kKSteps][4];
+      float amax = 0.0f;
 #pragma unroll
       for (int ks = 0; ks < G::kKSteps; ++ks) {
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-          int d0;
-          if constexpr (kInt8) {
-            // lane t reads chunks t*NC .. t*NC+NC-1 (16 d each, NC = D/64)
-            // of a row; k-step ks uses 4 consecutive d of chunk ks/4.
-            constexpr int NC = D / 64;
-            d0 = 16 * (t * NC + ks / 4) + 4 * (ks % 4) + 2 * r;
-          } else {
-            d0 = 16 * ks + 2 * t + 8 * r;
-          }
-          const float x0 = live ? __bfloat162float(q[d0]) : 0.0f;
-          const float x1 = live ? __bfloat162float(q[d0 + 1]) : 0.0f;
+          const float x0 = __uint_as_float(qraw[ks][r] << 16);
+          const float x1 = __uint_as_float(qraw[ks][r] & 0xffff0000u);
           qv[ks][2 * r] = x0;
           qv[ks][2 * r + 1] = x1;
           amax = fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1)));
@@ -384,7 +438,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
         int e = 0;
-        if (amax >= 16384.0f) frexpf(amax, &e), e -= 14;
+        if (amax >= 16384.0f) {
+          frexpf(amax, &e);
+          e -= 14;
+        }
         qscale = ldexpf(1.0f, -e);
       }
 #pragma unroll
@@ -649,6 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -687,7 +745,9 @@ kv_status make_map(CUtensorMap* map, const void* pool, const DecodeArgs& a) {
                         4, const_cast<void*>(pool), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE,
                         G::kSwizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        G::kRowBytes >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                            : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(KV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   return KV_OK;
 }

@@ -80,6 +80,13 @@ class GpuStep:
         self.append()
         return self.attend()
 
+    def fused_step(self):
+        s = self.wl.spec
+        pkv.decode_step(self.out, self.q, self.new_k, self.new_v, self.k_cache, self.v_cache,
+                        self.block_tables, self.seq_lens, self.max_seq_len, s.scale, self.workspace,
+                        k_scale=self.k_scale, v_scale=self.v_scale)
+        return self.out
+
 
 def out_f64(t: torch.Tensor) -> np.ndarray:
     return t.float().cpu().numpy().astype(np.float64)

@@ -112,6 +112,9 @@ def test_host_checks_fail_before_touching_the_gpu(pkv):
     st = lib.paged_attention_decode(P, P, P, P, None, None, P, 4, P, 2, 24, 2, 64, 10, 16, 100,
                                     0.1, 0, None, 0, None)
     assert st == pkv.KV_ERR_INVALID_ARG and b"at most 8" in lib.pagedkv_last_error()
+    st = lib.pagedkv_decode_step(P, P, None, None, P, P, None, None, P, 4, P, 2, 8, 2, 64, 10, 16,
+                                 100, 0.1, 0, P, 1 << 20, None)
+    assert st == pkv.KV_ERR_INVALID_ARG and b"NULL k or v" in lib.pagedkv_last_error()
     st = lib.paged_attention_decode(P, P, P, P, P, P, P, 4, P, 2, 8, 2, 64, 10, 16, 100,
                                     0.1, 0, None, 0, None)
     assert st == pkv.KV_ERR_INVALID_ARG and b"NULL" in lib.pagedkv_last_error()   # bf16 + scales

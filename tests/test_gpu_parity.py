@@ -145,7 +145,24 @@ def test_partition_size_does_not_change_the_answer(monkeypatch, part):
     g = GpuStep(wl)
     assert pkv.partition_tokens(wl.spec.batch, wl.spec.num_kv_heads, g.max_seq_len, 16) == int(part)
     assert_close(out_f64(g.step()), ref, "bf16", f"partition {part}")
+    assert_close(out_f64(g.fused_step()), ref, "bf16", f"partition {part}, fused")
     check_status()
+
+
+@pytest.mark.parametrize("case", ["cfg1", "ragged_g4_d128", "g8_int8_bs32", "shared_prefix", "int8_d64_bs16"])
+def test_fused_step_equals_separate_calls(case):
+    """pagedkv_decode_step (append inside the attention kernel) leaves the same
+    pools, bit for bit, and the same output as slot mapping + append +
+    attention as three calls."""
+    wl = CASES[case]()
+    a = GpuStep(wl)
+    out_a = bits_of(a.step()).copy()
+    b = GpuStep(wl)
+    out_b = bits_of(b.fused_step())
+    check_status()
+    np.testing.assert_array_equal(bits_of(b.k_cache), bits_of(a.k_cache))
+    np.testing.assert_array_equal(bits_of(b.v_cache), bits_of(a.v_cache))
+    np.testing.assert_array_equal(out_b, out_a)
 
 
 # ---------------------------------------------------------------------------
@@ -228,8 +245,12 @@ def test_bad_block_id_and_length_zero_the_row_and_flag():
     assert st == pkv.KV_ERR_DEVICE_INDEX
     assert flags == pkv.FLAG_BAD_BLOCK | pkv.FLAG_BAD_SEQ_LEN
     assert not out[1].any() and not out[2].any()
-    np.testing.assert_array_equal(out[0], good[0])
-    np.testing.assert_array_equal(out[3], good[3])
+    # Other rows keep their values; not their exact bits, since a changed
+    # batch moves the balanced split between workers (and so the order in
+    # which a sequence's partials combine).
+    from workloads import bf16_bits_to_f32
+    for b in (0, 3):
+        np.testing.assert_allclose(bf16_bits_to_f32(out[b]), bf16_bits_to_f32(good[b]), rtol=0, atol=1e-2)
 
 
 def test_length_past_the_hint_is_flagged():
