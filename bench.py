@@ -40,6 +40,7 @@ METRIC = "paged decode attention: KV-read GB/s & % of GB300 HBM peak; µs per de
 UNIT = "GB/s"
 DEFAULT_CONFIG = 2
 FALLBACK_HBM_GBS = 6800.0
+GRAPH_STEPS = 20
 DECODE_SOURCE = os.path.join(ROOT, "paged_kv_cache_97_gb300", "csrc", "pagedkv_decode.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
 
@@ -245,30 +246,51 @@ def gpu_arm(args, rank, world, local_rank, dist):
         g.fused_step()
         g.step()
     torch.cuda.synchronize(dev)
+    # GRAPH_STEPS consecutive steps captured once in a CUDA graph (each a
+    # decode + merge pair), the graph replayed: the GPU work of the steps
+    # without Python's per-call overhead or a gap between graph launches.
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(GRAPH_STEPS):
+            g.fused_step()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize(dev)
     st, flags = pkv.get_status()
     assert st == 0, f"device status 0x{flags:x}"
 
     # ---- device-resident timed region ---------------------------------
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    R = max(1, K // GRAPH_STEPS)                        # graph replays in the timed region
+    K = R * GRAPH_STEPS
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(R)]
     sampler = ClockSampler(torch.cuda.get_device_properties(dev).uuid.__str__())
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
     with sampler:
-        for i in range(K):
+        for i in range(R):
             ev[i][0].record(stream)
-            g.fused_step()
+            graph.replay()
             ev[i][1].record(stream)
         torch.cuda.synchronize(dev)
     if dist is not None:
         dist.barrier()
     total_ms = ev[0][0].elapsed_time(ev[-1][1])
-    step_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    step_ms = [ev[i][0].elapsed_time(ev[i][1]) / GRAPH_STEPS for i in range(R)]
     ms_step = total_ms / K
 
-    # the same step as three calls (slot mapping, append, attention), for reference
+    # the same step through eager calls: the fused step, and the three calls
+    # (slot mapping, append, attention)
     K3 = max(K // 4, 10)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for i in range(K3):
+        g.fused_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    eager_ms = e0.elapsed_time(e1) / K3
     ev3 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K3)]
     torch.cuda.synchronize(dev)
     for i in range(K3):
@@ -338,6 +360,8 @@ def gpu_arm(args, rank, world, local_rank, dist):
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": nbytes["step"],
                      "us_per_launch": round(step_mean_ms * 1e3, 2), "traffic": traffic},
+        "timing": f"value and ms_per_step: {GRAPH_STEPS} steps captured in one CUDA graph, replayed",
+        "eager_us_per_step": round(eager_ms * 1e3, 2),
         "unfused": {"us_per_step": round(unfused_ms * 1e3, 2),
                     "attention_us": round(attn_only_ms * 1e3, 2),
                     "note": "slot mapping + reshape_and_cache + paged_attention_decode as three calls"},

@@ -284,7 +284,7 @@ kv_status pagedkv_get_status(void *stream, unsigned int *device_flags);
 const char *pagedkv_last_error(void);
 
 /* Token partition size paged_attention_decode would use for this shape on
- * the current device (0 on error): the largest power of two in [256, 8192]
+ * the current device (0 on error): the largest power of two in [256, 2048]
  * that still gives at least 8 CTAs per SM.  Sequences longer than one
  * partition go through the merge kernel.  The environment variable
  * PAGEDKV_PARTITION_TOKENS (a multiple of 256) overrides it. */

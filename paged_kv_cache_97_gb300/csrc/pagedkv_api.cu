@@ -244,10 +244,11 @@ kv_status launch_merge(const DecodeArgs& a, cudaStream_t stream) {
 // ---------------------------------------------------------------------------
 
 static const int kMinPartTokens = 256;
-static const int kMaxPartTokens = 8192;
+static const int kMaxPartTokens = 2048;
 
-// Largest power-of-two partition in [256, 8192] that still gives at least
-// 8 CTAs per SM over (sequence, KV head, partition).  The environment
+// Largest power-of-two partition in [256, 2048] that still gives at least
+// 8 CTAs per SM over (sequence, KV head, partition).  Longer partitions
+// measured slower on GB300 (fewer, longer CTAs leave a longer tail).  The environment
 // variable PAGEDKV_PARTITION_TOKENS (a multiple of 256, read on every call)
 // overrides it.
 static int choose_part_tokens(int batch, int num_kv_heads, int max_seq_len, int num_sms) {

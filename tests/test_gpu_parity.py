@@ -165,6 +165,31 @@ def test_fused_step_equals_separate_calls(case):
     np.testing.assert_array_equal(out_b, out_a)
 
 
+@pytest.mark.parametrize("case", ["cfg1", "ragged_g4_d128", "g8_int8_bs32"])
+def test_decode_step_replays_from_a_cuda_graph(case):
+    """The fused step captured once in a CUDA graph (decode + PDL merge) and
+    replayed gives the eager step's output bit for bit; replaying re-appends
+    the same token, so the pools stay bit-identical too."""
+    wl = CASES[case]()
+    eager = GpuStep(wl)
+    want = bits_of(eager.fused_step()).copy()
+    g = GpuStep(wl)
+    g.fused_step()                       # warm-up outside capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    g.out.zero_()
+    with torch.cuda.graph(graph):
+        g.fused_step()
+    for _ in range(2):
+        g.out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(bits_of(g.out), want)
+    np.testing.assert_array_equal(bits_of(g.k_cache), bits_of(eager.k_cache))
+    np.testing.assert_array_equal(bits_of(g.v_cache), bits_of(eager.v_cache))
+    check_status()
+
+
 # ---------------------------------------------------------------------------
 # Invariants
 # ---------------------------------------------------------------------------
