@@ -236,14 +236,17 @@ def gpu_arm(args, rank, world, local_rank, dist):
     dev = torch.device("cuda", local_rank)
     wl = workloads.make(args.config)
     g = GpuStep(wl, dev=dev)
+    use_prefix = wl.spec.shared_prefix_tokens > 0 and not args.no_shared_prefix
+    step_fn = g.prefix_step if use_prefix else g.fused_step
     s = wl.spec
     stream = torch.cuda.current_stream(dev)
     nbytes = algorithmic_bytes(wl)
     part = pkv.partition_tokens(s.batch, s.num_kv_heads, g.max_seq_len, s.block_size)
-    launches_per_step = 1 + (1 if g.max_seq_len > part else 0)   # decode (append fused) + merge
+    # decode (append fused) + merge, + the prefix kernel on the shared-prefix path
+    launches_per_step = (3 if use_prefix else 1 + (1 if g.max_seq_len > part else 0))
 
     for _ in range(args.warmup):
-        g.fused_step()
+        step_fn()
         g.step()
     torch.cuda.synchronize(dev)
     # GRAPH_STEPS consecutive steps captured once in a CUDA graph (each a
@@ -252,7 +255,7 @@ def gpu_arm(args, rank, world, local_rank, dist):
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         for _ in range(GRAPH_STEPS):
-            g.fused_step()
+            step_fn()
     for _ in range(args.warmup):
         graph.replay()
     torch.cuda.synchronize(dev)
@@ -287,7 +290,7 @@ def gpu_arm(args, rank, world, local_rank, dist):
     torch.cuda.synchronize(dev)
     e0.record(stream)
     for i in range(K3):
-        g.fused_step()
+        step_fn()
     e1.record(stream)
     torch.cuda.synchronize(dev)
     eager_ms = e0.elapsed_time(e1) / K3
@@ -327,7 +330,7 @@ def gpu_arm(args, rank, world, local_rank, dist):
         g.new_v.copy_(h_v, non_blocking=True)
         g.block_tables.copy_(h_bt, non_blocking=True)
         g.seq_lens.copy_(h_sl, non_blocking=True)
-        g.fused_step()
+        step_fn()
         h_out.copy_(g.out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize(dev)
@@ -355,7 +358,9 @@ def gpu_arm(args, rank, world, local_rank, dist):
                    "l2": "inputs larger than L2 (KV read per step > 129 MB), no flush",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm",
-                     "kernel": "decode_kernel (append fused) + merge_kernel, one pagedkv_decode_step",
+                     "kernel": ("prefix_kernel + decode_kernel (append fused) + merge_kernel, one "
+                   "pagedkv_decode_step_prefix" if use_prefix else
+                   "decode_kernel (append fused) + merge_kernel, one pagedkv_decode_step"),
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": nbytes["step"],
@@ -382,6 +387,9 @@ def main():
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=sorted(workloads.CONFIGS),
                     help="workload (default 2: the Llama-3.1-8B-like decode layer)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-shared-prefix", action="store_true",
+                    help="for workloads with a shared prefix, time the plain step instead of "
+                         "pagedkv_decode_step_prefix")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -231,6 +231,44 @@ kv_status pagedkv_decode_step(void *out, const void *q, const void *k,
                               void *workspace, size_t workspace_bytes,
                               void *stream);
 
+/* pagedkv_decode_step for a batch whose sequences all begin with the same
+ * num_prefix_blocks physical blocks (a shared system prompt: “让 Agent
+ * 跑得快”, §五 共享前缀 -- several block tables map to the same read-only
+ * blocks).  The prefix part of attention is computed once per KV head for
+ * every query row of the batch (a dense product on tensor cores) instead of
+ * once per sequence; tokens past the prefix go through the decode kernel and
+ * the two are merged by log-sum-exp.  Results equal pagedkv_decode_step up
+ * to rounding.
+ *   prefix_blocks      device int32 [num_prefix_blocks]: the shared physical
+ *                      blocks, which must also be entries 0..P-1 of every
+ *                      row of block_tables (a mismatch zeroes that sequence's
+ *                      rows and sets PAGEDKV_FLAG_BAD_BLOCK)
+ *   num_prefix_blocks  P >= 1; every seq_lens[b] must exceed P * block_size
+ *                      (shorter sequences are flagged and zeroed)
+ *   k, v               as pagedkv_decode_step, or both NULL to attend
+ *                      without appending
+ *   workspace          at least pagedkv_prefix_workspace_bytes(...) bytes
+ * bf16 pools only (int8 returns KV_ERR_NOT_IMPLEMENTED). */
+kv_status pagedkv_decode_step_prefix(void *out, const void *q, const void *k,
+                                     const void *v, void *k_cache,
+                                     void *v_cache, const float *k_scale,
+                                     const float *v_scale,
+                                     const int32_t *block_tables,
+                                     int max_blocks_per_seq,
+                                     const int32_t *seq_lens, int batch,
+                                     int num_q_heads, int num_kv_heads,
+                                     int head_dim, int num_blocks,
+                                     int block_size, int max_seq_len,
+                                     float scale, kv_dtype dtype,
+                                     const int32_t *prefix_blocks,
+                                     int num_prefix_blocks, void *workspace,
+                                     size_t workspace_bytes, void *stream);
+
+/* Workspace bytes pagedkv_decode_step_prefix may need for this shape. */
+size_t pagedkv_prefix_workspace_bytes(int batch, int num_q_heads, int head_dim,
+                                      int max_seq_len, int block_size,
+                                      int num_prefix_blocks);
+
 /* Size of the fixed device scratch paged_attention_decode_noalloc uses. */
 #define PAGEDKV_NOALLOC_SCRATCH_BYTES (32u << 20)
 

@@ -46,6 +46,9 @@ SIGNATURES = {
     "pagedkv_get_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
     "pagedkv_last_error": (ctypes.c_char_p, []),
     "pagedkv_partition_tokens": (_I, [_I, _I, _I, _I]),
+    "pagedkv_decode_step_prefix": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I,
+                                        _I, _I, _I, _F, _I, _P, _I, _P, _SZ, _P]),
+    "pagedkv_prefix_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "pagedkv_decode_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
                                  _I, _I, _F, _I, _P, _SZ, _P]),
 }
@@ -278,6 +281,36 @@ def decode_step(out, q, k, v, k_cache, v_cache, block_tables, seq_lens, max_seq_
                                       hq, hkv, d, nb, bs, int(max_seq_len), float(scale),
                                       _pool_dtype(k_cache), _ptr(workspace), wbytes,
                                       _stream(stream)))
+    return out
+
+
+def prefix_workspace_bytes(batch, num_q_heads, head_dim, max_seq_len, block_size,
+                           num_prefix_blocks) -> int:
+    return load().pagedkv_prefix_workspace_bytes(batch, num_q_heads, head_dim, max_seq_len,
+                                                 block_size, num_prefix_blocks)
+
+
+def decode_step_prefix(out, q, k, v, k_cache, v_cache, block_tables, seq_lens, max_seq_len, scale,
+                       prefix_blocks, workspace, k_scale=None, v_scale=None, stream=None):
+    """decode_step for a batch whose sequences all start with the physical
+    blocks ``prefix_blocks`` (int32 [P]): the prefix is attended once per KV
+    head for all query rows.  k, v may both be None (attend only)."""
+    import torch
+    wbytes = _check_decode(out, q, k_cache, v_cache, block_tables, seq_lens, k_scale, v_scale,
+                           workspace)
+    _need(prefix_blocks, torch.int32, "prefix_blocks", 1)
+    B, hq, d = q.shape
+    nb, bs, hkv, _ = k_cache.shape
+    if k is not None:
+        _need(k, torch.bfloat16, "k", 3)
+        _need(v, torch.bfloat16, "v", 3)
+        if k.shape != (B, hkv, d) or v.shape != k.shape:
+            raise ValueError("k, v must be [batch, num_kv_heads, head_dim]")
+    _check(load().pagedkv_decode_step_prefix(
+        _ptr(out), _ptr(q), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+        _ptr(v_scale), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B, hq, hkv, d,
+        nb, bs, int(max_seq_len), float(scale), _pool_dtype(k_cache), _ptr(prefix_blocks),
+        prefix_blocks.shape[0], _ptr(workspace), wbytes, _stream(stream)))
     return out
 
 

@@ -175,43 +175,76 @@ __global__ void append_kernel(const uint4* __restrict__ k, const uint4* __restri
 }
 
 // ---------------------------------------------------------------------------
-// Split-K merge: one CTA per (sequence, query head), one thread per element.
+// Log-sum-exp merge.  One CTA per (sequence, KV head), one warp per query
+// head; a row's partials are its partitions of tokens [skip, L) (slots
+// 0 .. np-1) and, with a shared prefix, the prefix kernel's chunks (slots
+// max_parts .. slots-1):
 //   M = max_i m_i, w_i = 2^(m_i - M), out = sum_i w_i acc_i / sum_i w_i l_i
-// A partition whose l is negative marks a bad block: the row becomes zeros.
+// A partial whose l is negative marks a bad block: the row becomes zeros.
+// Launched as a programmatic dependent of the kernel before it: the wait
+// returns once that grid has completed and its partials are visible.
 // ---------------------------------------------------------------------------
 
 __global__ void merge_kernel(__nv_bfloat16* __restrict__ out, const float* __restrict__ ws_ml,
                              const float* __restrict__ ws_acc,
                              const int32_t* __restrict__ seq_lens, int num_q_heads,
-                             int head_dim, int part_tokens, int max_parts, int max_len) {
-  const int b = blockIdx.x / num_q_heads, h = blockIdx.x % num_q_heads;
-  // Launched as a programmatic dependent of the decode kernel: wait until
-  // that grid has completed and its partials are visible.
+                             int num_kv_heads, int head_dim, int part_tokens, int max_parts,
+                             int slots, int skip, int prefix_chunks, int max_len) {
+  const int b = blockIdx.x / num_kv_heads, hk = blockIdx.x % num_kv_heads;
+  const int G = num_q_heads / num_kv_heads;
+  const int g = threadIdx.x >> 5, lane = threadIdx.x & 31;
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int L = seq_lens[b];
-  if (L <= 0 || L > max_len) return;  // invalid length: the decode kernel zeroed the row
-  const int np = (L + part_tokens - 1) / part_tokens;
-  if (np <= 1) return;                // single partition: written by the decode kernel
-  const int64_t row = (int64_t)b * num_q_heads + h;
-  const float* ml = ws_ml + row * max_parts * 2;
-  const float* acc = ws_acc + row * max_parts * head_dim;
+  if (g >= G || L <= skip || L > max_len) return;  // invalid rows were zeroed by the decode kernel
+  const int np = (L - skip + part_tokens - 1) / part_tokens;
+  const int total = np + (skip > 0 ? prefix_chunks : 0);
+  if (total <= 1) return;                           // written whole by the decode kernel
+  const int64_t row = (int64_t)b * num_q_heads + (int64_t)hk * G + g;
+  const float* ml = ws_ml + row * slots * 2;
+  const float* acc = ws_acc + row * slots * head_dim;
+  // pass 1: the largest m and any bad partial, 32 partials per round
   float M = -INFINITY;
   bool bad = false;
-  for (int i = 0; i < np; ++i) {
-    M = fmaxf(M, ml[2 * i]);
-    bad |= ml[2 * i + 1] < 0.0f;
+  for (int i = lane; i < total; i += 32) {
+    const int s = i < np ? i : max_parts + (i - np);
+    M = fmaxf(M, ml[2 * s]);
+    bad |= ml[2 * s + 1] < 0.0f;
   }
-  for (int e = threadIdx.x; e < head_dim; e += blockDim.x) {
-    float num = 0.0f, den = 0.0f;
-    if (!bad) {
-      for (int i = 0; i < np; ++i) {
-        float w = exp2f(ml[2 * i] - M);
-        num += w * acc[(int64_t)i * head_dim + e];
-        den += w * ml[2 * i + 1];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  bad = __any_sync(0xffffffffu, bad);
+  // pass 2: each lane owns 4 consecutive elements
+  float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+  float den = 0.0f;
+  const int e0 = lane * 4;
+  if (!bad) {
+#pragma unroll 4
+    for (int i = 0; i < total; ++i) {
+      const int s = i < np ? i : max_parts + (i - np);
+      const float w = exp2f(ml[2 * s] - M);
+      den = fmaf(w, ml[2 * s + 1], den);
+      if (e0 < head_dim) {
+        const float4 x = *reinterpret_cast<const float4*>(acc + (int64_t)s * head_dim + e0);
+        num.x = fmaf(w, x.x, num.x);
+        num.y = fmaf(w, x.y, num.y);
+        num.z = fmaf(w, x.z, num.z);
+        num.w = fmaf(w, x.w, num.w);
       }
     }
-    out[row * head_dim + e] = __float2bfloat16_rn(bad ? 0.0f : num / den);
   }
+  if (e0 < head_dim) {
+    const float r = bad ? 0.0f : 1.0f / den;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(bad ? 0.0f : num.x * r, bad ? 0.0f : num.y * r);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(bad ? 0.0f : num.z * r, bad ? 0.0f : num.w * r);
+    uint2 v;
+    v.x = *reinterpret_cast<uint32_t*>(&lo);
+    v.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(out + row * head_dim + e0) = v;
+  }
+}
+
+size_t decode_workspace_need(int batch, int num_q_heads, int head_dim, int slots) {
+  return slots > 1 ? (size_t)batch * num_q_heads * slots * (head_dim + 2) * sizeof(float) : 0;
 }
 
 // Longest valid sequence: bounded by the host hint and by the table.
@@ -221,20 +254,24 @@ static int valid_len_limit(const DecodeArgs& a) {
 }
 
 kv_status launch_merge(const DecodeArgs& a, cudaStream_t stream) {
-  if (a.max_parts <= 1) return KV_OK;
+  if (a.max_parts <= 1 && a.skip_tokens == 0) return KV_OK;
+  // With a shared prefix the partials come from two kernels: a plain launch
+  // waits for both; otherwise launch behind the decode kernel (PDL).
+  const int G = a.num_q_heads / a.num_kv_heads;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(a.batch * a.num_q_heads));
-  cfg.blockDim = dim3((unsigned)a.head_dim);
+  cfg.gridDim = dim3((unsigned)(a.batch * a.num_kv_heads));
+  cfg.blockDim = dim3((unsigned)(32 * G));
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = a.prefix_chunks > 0 ? 0 : 1;
   return cuda_check(cudaLaunchKernelEx(&cfg, merge_kernel, static_cast<__nv_bfloat16*>(a.out),
                                        (const float*)a.ws_ml, (const float*)a.ws_acc, a.seq_lens,
-                                       a.num_q_heads, a.head_dim, a.part_tokens, a.max_parts,
+                                       a.num_q_heads, a.num_kv_heads, a.head_dim, a.part_tokens,
+                                       a.max_parts, a.slots, a.skip_tokens, a.prefix_chunks,
                                        valid_len_limit(a)),
                     "merge_kernel launch");
 }
@@ -254,7 +291,7 @@ static const int kMaxPartTokens = 2048;
 static int choose_part_tokens(int batch, int num_kv_heads, int max_seq_len, int num_sms) {
   const char* s = getenv("PAGEDKV_PARTITION_TOKENS");
   const int env = s ? atoi(s) : 0;
-  if (env >= kMinPartTokens && env % kMinPartTokens == 0) return env;
+  if (env >= kMinPartTokens && env <= kMaxPartTokens && env % kMinPartTokens == 0) return env;
   const int64_t target = 8LL * num_sms;
   int pt = kMaxPartTokens;
   while (pt > kMinPartTokens &&
@@ -432,9 +469,9 @@ kv_status reshape_and_cache(const void* k, const void* v, void* k_cache, void* v
 size_t pagedkv_workspace_bytes(int batch, int num_q_heads, int head_dim, int max_seq_len,
                                int block_size) {
   (void)block_size;
-  if (batch <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_seq_len <= kMinPartTokens) return 0;
-  const size_t parts = (size_t)(max_seq_len + kMinPartTokens - 1) / kMinPartTokens;
-  return (size_t)batch * num_q_heads * parts * (head_dim + 2) * sizeof(float);
+  if (batch <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_seq_len <= 0) return 0;
+  const int parts = (max_seq_len + kMinPartTokens - 1) / kMinPartTokens;
+  return decode_workspace_need(batch, num_q_heads, head_dim, parts);
 }
 
 int pagedkv_partition_tokens(int batch, int num_kv_heads, int max_seq_len, int block_size) {
@@ -444,13 +481,31 @@ int pagedkv_partition_tokens(int batch, int num_kv_heads, int max_seq_len, int b
   return choose_part_tokens(batch, num_kv_heads, max_seq_len, di.num_sms);
 }
 
-// Shared body of paged_attention_decode and pagedkv_decode_step.
+static const int kMaxPrefixChunks = 16;
+
+
+
+// Prefix chunks per row: enough (row tile, KV head, chunk) CTAs to cover the
+// SMs twice, at most one per prefix block and kMaxPrefixChunks.
+static int choose_prefix_chunks(int batch, int num_q_heads, int num_kv_heads,
+                                int num_prefix_blocks, int num_sms) {
+  const int G = num_q_heads / num_kv_heads;
+  const int64_t base = (int64_t)((batch * G + 63) / 64) * num_kv_heads;
+  int64_t nc = (2LL * num_sms + base - 1) / base;
+  if (nc > num_prefix_blocks) nc = num_prefix_blocks;
+  if (nc > kMaxPrefixChunks) nc = kMaxPrefixChunks;
+  return (int)(nc < 1 ? 1 : nc);
+}
+
+// Shared body of paged_attention_decode, pagedkv_decode_step and
+// pagedkv_decode_step_prefix.
 static kv_status decode_common(void* out, const void* q, const void* new_k, const void* new_v,
                                const void* k_cache, const void* v_cache, const float* k_scale,
                                const float* v_scale, const int32_t* block_tables,
                                int max_blocks_per_seq, const int32_t* seq_lens, int batch,
                                int num_q_heads, int num_kv_heads, int head_dim, int num_blocks,
                                int block_size, int max_seq_len, float scale, kv_dtype dtype,
+                               const int32_t* prefix_blocks, int num_prefix_blocks,
                                void* workspace, size_t workspace_bytes, void* stream,
                                const char* who) {
   if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads ||
@@ -473,6 +528,14 @@ static kv_status decode_common(void* out, const void* q, const void* new_k, cons
   if (int8 != (k_scale != nullptr) || int8 != (v_scale != nullptr))
     return fail(KV_ERR_INVALID_ARG,
                 "%s: int8 pools need k_scale and v_scale; bf16 pools take NULL", who);
+  const int skip = num_prefix_blocks * block_size;
+  if (num_prefix_blocks < 0 || (num_prefix_blocks > 0 && !prefix_blocks) ||
+      num_prefix_blocks > max_blocks_per_seq || (num_prefix_blocks > 0 && max_seq_len <= skip))
+    return fail(KV_ERR_INVALID_ARG,
+                "%s: the shared prefix needs 1..max_blocks_per_seq block ids and sequences "
+                "longer than it", who);
+  if (num_prefix_blocks > 0 && int8)
+    return fail(KV_ERR_NOT_IMPLEMENTED, "%s: the shared-prefix path supports bf16 pools only", who);
   DeviceInfo di;
   kv_status st = device_info(&di);
   if (st != KV_OK) return st;
@@ -497,23 +560,31 @@ static kv_status decode_common(void* out, const void* q, const void* new_k, cons
   a.num_blocks = num_blocks;
   a.block_size = block_size;
   a.max_seq_len = max_seq_len;
-  a.part_tokens = choose_part_tokens(batch, num_kv_heads, max_seq_len, di.num_sms);
-  a.max_parts = (max_seq_len + a.part_tokens - 1) / a.part_tokens;
+  a.part_tokens = choose_part_tokens(batch, num_kv_heads, max_seq_len - skip, di.num_sms);
+  a.max_parts = (max_seq_len - skip + a.part_tokens - 1) / a.part_tokens;
+  a.skip_tokens = skip;
+  a.num_prefix_blocks = num_prefix_blocks;
+  a.prefix_chunks = num_prefix_blocks > 0
+                        ? choose_prefix_chunks(batch, num_q_heads, num_kv_heads,
+                                               num_prefix_blocks, di.num_sms)
+                        : 0;
+  a.slots = a.max_parts + a.prefix_chunks;
+  a.prefix_blocks = prefix_blocks;
   a.scale_log2 = scale * kLog2e;
   a.dtype = dtype;
   a.ws_ml = nullptr;
   a.ws_acc = nullptr;
-  if (a.max_parts > 1) {
-    const size_t ml_bytes = (size_t)batch * num_q_heads * a.max_parts * 2 * sizeof(float);
-    const size_t need = ml_bytes + (size_t)batch * num_q_heads * a.max_parts * head_dim * sizeof(float);
+  const size_t need = decode_workspace_need(batch, num_q_heads, head_dim, a.slots);
+  if (need > 0) {
     if (!workspace || workspace_bytes < need || !aligned16(workspace))
       return fail(KV_ERR_INVALID_ARG,
                   "%s: workspace must be 16-byte aligned and hold %zu bytes "
                   "(pagedkv_workspace_bytes gives a safe size)", who, need);
     a.ws_ml = static_cast<float*>(workspace);
-    a.ws_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + ml_bytes);
+    a.ws_acc = a.ws_ml + (size_t)batch * num_q_heads * a.slots * 2;
   }
   cudaStream_t s = (cudaStream_t)stream;
+  if (num_prefix_blocks > 0 && (st = launch_prefix(a, s)) != KV_OK) return st;
   st = launch_decode(a, s);
   if (st != KV_OK) return st;
   return launch_merge(a, s);
@@ -529,7 +600,7 @@ kv_status paged_attention_decode(void* out, const void* q, const void* k_cache,
   return decode_common(out, q, nullptr, nullptr, k_cache, v_cache, k_scale, v_scale,
                        block_tables, max_blocks_per_seq, seq_lens, batch, num_q_heads,
                        num_kv_heads, head_dim, num_blocks, block_size, max_seq_len, scale, dtype,
-                       workspace, workspace_bytes, stream, "paged_attention_decode");
+                       nullptr, 0, workspace, workspace_bytes, stream, "paged_attention_decode");
 }
 
 kv_status pagedkv_decode_step(void* out, const void* q, const void* k, const void* v,
@@ -543,8 +614,40 @@ kv_status pagedkv_decode_step(void* out, const void* q, const void* k, const voi
     return fail(KV_ERR_INVALID_ARG, "pagedkv_decode_step: NULL k or v");
   return decode_common(out, q, k, v, k_cache, v_cache, k_scale, v_scale, block_tables,
                        max_blocks_per_seq, seq_lens, batch, num_q_heads, num_kv_heads, head_dim,
-                       num_blocks, block_size, max_seq_len, scale, dtype, workspace,
+                       num_blocks, block_size, max_seq_len, scale, dtype, nullptr, 0, workspace,
                        workspace_bytes, stream, "pagedkv_decode_step");
+}
+
+kv_status pagedkv_decode_step_prefix(void* out, const void* q, const void* k, const void* v,
+                                     void* k_cache, void* v_cache, const float* k_scale,
+                                     const float* v_scale, const int32_t* block_tables,
+                                     int max_blocks_per_seq, const int32_t* seq_lens, int batch,
+                                     int num_q_heads, int num_kv_heads, int head_dim,
+                                     int num_blocks, int block_size, int max_seq_len,
+                                     float scale, kv_dtype dtype, const int32_t* prefix_blocks,
+                                     int num_prefix_blocks, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  if (batch > 0 && ((k == nullptr) != (v == nullptr)))
+    return fail(KV_ERR_INVALID_ARG, "pagedkv_decode_step_prefix: give both k and v, or neither");
+  if (batch > 0 && num_prefix_blocks <= 0)
+    return fail(KV_ERR_INVALID_ARG, "pagedkv_decode_step_prefix: num_prefix_blocks must be >= 1");
+  return decode_common(out, q, k, v, k_cache, v_cache, k_scale, v_scale, block_tables,
+                       max_blocks_per_seq, seq_lens, batch, num_q_heads, num_kv_heads, head_dim,
+                       num_blocks, block_size, max_seq_len, scale, dtype, prefix_blocks,
+                       num_prefix_blocks, workspace, workspace_bytes, stream,
+                       "pagedkv_decode_step_prefix");
+}
+
+size_t pagedkv_prefix_workspace_bytes(int batch, int num_q_heads, int head_dim, int max_seq_len,
+                                      int block_size, int num_prefix_blocks) {
+  if (batch <= 0 || num_q_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+      num_prefix_blocks <= 0)
+    return 0;
+  const int rest = max_seq_len - num_prefix_blocks * block_size;
+  if (rest <= 0) return 0;
+  const int parts = (rest + kMinPartTokens - 1) / kMinPartTokens;
+  const int chunks = num_prefix_blocks < kMaxPrefixChunks ? num_prefix_blocks : kMaxPrefixChunks;
+  return decode_workspace_need(batch, num_q_heads, head_dim, parts + chunks);
 }
 
 kv_status pagedkv_get_status(void* stream, unsigned int* device_flags) {

@@ -2,6 +2,7 @@
 // translation units (never installed, never seen by callers).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -22,6 +23,9 @@ struct DeviceInfo {
 };
 kv_status device_info(DeviceInfo* out);
 
+// Query heads per KV head the kernels serve (the MMA's N = 8 columns).
+constexpr int kMaxGroup = 8;
+
 // log2(e): scores are kept in the base-2 domain so exp() becomes exp2().
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -37,21 +41,37 @@ struct DecodeArgs {
   const int32_t* seq_lens;     // [B]
   const void* new_k;           // bf16 [B, Hkv, D] appended in the same launch, or null
   const void* new_v;
-  float* ws_ml;                // [B, Hq, max_parts, 2]   (m, l) per partition
-  float* ws_acc;               // [B, Hq, max_parts, D]   unnormalised acc
+  const int32_t* prefix_blocks; // [num_prefix_blocks] shared first blocks of every sequence, or null
+  float* ws_ml;                // [B, Hq, slots, 2]   (m, l) per partial
+  float* ws_acc;               // [B, Hq, slots, D]   unnormalised acc
   unsigned int* flags;
   int max_blocks_per_seq, batch, num_q_heads, num_kv_heads, head_dim;
   int num_blocks, block_size, max_seq_len;
-  int part_tokens, max_parts;
+  int part_tokens, max_parts;  // partitions of tokens [skip_tokens, L)
+  int skip_tokens;             // leading tokens attended elsewhere (the shared prefix)
+  int num_prefix_blocks;       // = skip_tokens / block_size
+  int prefix_chunks;           // prefix partials per row, in slots [max_parts, slots)
+  int slots;                   // max_parts + prefix_chunks
   float scale_log2;            // scale * log2(e)
   kv_dtype dtype;
 };
 
+// Workspace of one decode call: (m, l) and acc of `slots` partials per query
+// row, or nothing when every row has a single partial.
+size_t decode_workspace_need(int batch, int num_q_heads, int head_dim, int slots);
+
+// Tensor maps over the K and V pools for this launch's geometry: 4-D
+// [NB, bs, Hkv, d], box = one block's rows of one head (128-byte swizzle).
+kv_status make_kv_maps(const DecodeArgs& a, CUtensorMap* k_map, CUtensorMap* v_map);
+
 // Launches the per-partition decode kernel (with the append fused in when
 // new_k is set).
 kv_status launch_decode(const DecodeArgs& a, cudaStream_t stream);
-// Launches the log-sum-exp merge of the partitions (only when max_parts > 1),
-// as a programmatic dependent of the decode kernel.
+// Launches the log-sum-exp merge of the partials (when any row can have more
+// than one), as a programmatic dependent of the kernel before it.
 kv_status launch_merge(const DecodeArgs& a, cudaStream_t stream);
+// Launches the shared-prefix kernel: every sequence's query rows against the
+// prefix blocks, one partial per row and prefix chunk.
+kv_status launch_prefix(const DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace pagedkv

@@ -45,195 +45,16 @@
 #include <mutex>
 
 #include "pagedkv_common.cuh"
+#include "pagedkv_device.cuh"
 
 namespace pagedkv {
 namespace {
 
-#ifndef PAGEDKV_CONSUMERS
-#define PAGEDKV_CONSUMERS 3
-#endif
-constexpr int kConsumers = PAGEDKV_CONSUMERS;        // consumer warps per CTA
+using namespace dev;
+
 constexpr int kThreads = (kConsumers + 1) * 32;      // + one producer warp
-constexpr int kMaxStages = 8;
 constexpr int kMaxBlocks = 8192 / 16;                // blocks per partition (max)
-// Stage memory and consumer warps per CTA: 48 KB and 3 consumers (about 4
-// CTAs per SM) measured best across the bench workloads on GB300 against
-// 64-128 KB with 4 consumers and 32-48 KB with 2.
-#ifndef PAGEDKV_STAGE_BUDGET
-#define PAGEDKV_STAGE_BUDGET (48 * 1024)
-#endif
-constexpr int kStageBudget = PAGEDKV_STAGE_BUDGET;    // shared memory for stages
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
-
-template <int D, int BS, bool kInt8>
-struct Geo {
-  static constexpr int kElem = kInt8 ? 1 : 2;
-  static constexpr int kRowBytes = D * kElem;                          // 256, 128, 64
-  static constexpr int kBoxRow = kRowBytes > 128 ? 128 : kRowBytes;    // bytes per box row
-  static constexpr int kBoxes = kRowBytes / kBoxRow;                   // 2 for bf16 d128
-  static constexpr int kBoxElems = kBoxRow / kElem;
-  static constexpr bool kSwizzle = kBoxRow == 128;                     // SWIZZLE_128B
-  static constexpr int kBoxBytes = BS * kBoxRow;
-  static constexpr int kTensorBytes = kBoxes * kBoxBytes;              // K (or V) of a block
-  static constexpr int kBlockBytes = 2 * kTensorBytes;                 // K + V
-  static constexpr int kStageBytes = kConsumers * kBlockBytes;
-  static constexpr int kStages0 = kStageBudget / kStageBytes;
-  static constexpr int kStages = kStages0 < 2 ? 2 : (kStages0 > kMaxStages ? kMaxStages : kStages0);
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024;      // + alignment slack
-  static constexpr int kTiles = BS / 16;                               // 16-token MMA tiles
-  static constexpr int kKSteps = D / 16;                               // MMA k-steps over d
-  static constexpr int kMTiles = D / 16;                               // O^T m-tiles over d
-};
-
-// ---------------------------------------------------------------------------
-// PTX helpers
-// ---------------------------------------------------------------------------
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Waits for the phase of `bar` with the given parity, giving up after
-// kWaitLimitNs; returns false on time-out (the caller reports it).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (global_ns() - t0 > kWaitLimitNs) return false;
-  return true;
-}
-
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int c0, int c1, int c2, int c3) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr));
-  return v;
-}
-
-__device__ __forceinline__ uint2 lds64(uint32_t addr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-  return v;
-}
-
-// D += A . B for one m16n8k16 tile, fp32 accumulate; A, B bf16 or fp16.
-template <bool kF16>
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  if constexpr (kF16) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
-        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-  } else {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
-        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-  }
-}
-
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t r;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-  return r;
-}
-
-// Two fp32 -> packed pair, lower index in the low half.
-template <bool kF16>
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-  uint32_t r;
-  if constexpr (kF16)
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  else
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-// int8 codes (two's complement) at bytes b0, b1 of w, already XORed with
-// 0x80 (so each byte is c + 128): fp16 pair of (1024 + c + 128) - 1152 = c,
-// exact.  sel 0x4140 takes bytes 0,1; 0x4342 bytes 2,3.
-__device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t w_biased, uint32_t sel) {
-  const uint32_t h = prmt(w_biased, 0x64646464u, sel);
-  __half2 x = *reinterpret_cast<const __half2*>(&h);
-  x = __hsub2(x, __half2half2(__ushort_as_half((unsigned short)0x6480)));  // 1152.0
-  return *reinterpret_cast<const uint32_t*>(&x);
-}
-
-__device__ __forceinline__ int8_t quantize(float x, float s) {
-  // clamp(round_half_even(x / s), -127, 127) with an IEEE fp32 divide.
-  if (s == 0.0f) s = 1.0f;
-  int c = __float2int_rn(__fdiv_rn(x, s));
-  c = c > 127 ? 127 : (c < -127 ? -127 : c);
-  return (int8_t)c;
-}
-
-// Byte offset of 16-byte chunk `c` of row `r` inside one K or V block of a
-// stage.  Rows of a box are kBoxRow bytes; with SWIZZLE_128B the chunk index
-// inside each 128-byte row is XORed with (row mod 8), the pattern TMA writes
-// (box starts are 1024-byte aligned).
-template <class G>
-__device__ __forceinline__ uint32_t chunk_off(int r, int c) {
-  constexpr int kChunksPerBox = G::kBoxRow / 16;
-  const int box = c / kChunksPerBox, cc = c % kChunksPerBox;
-  const int phys = G::kSwizzle ? (cc ^ (r & 7)) : cc;
-  return box * G::kBoxBytes + r * G::kBoxRow + phys * 16;
-}
+constexpr int kSpec = (kMaxBlocks + kThreads - 1) / kThreads;  // table entries per thread
 
 // ---------------------------------------------------------------------------
 // The kernel
@@ -264,38 +85,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t head0 = (int64_t)b * Hq + (int64_t)hk * GQ;
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
 
-  // ---- sequence checks (uniform over the CTA) -----------------------------
-  const int L = a.seq_lens[b];
-  const int64_t table_tokens = (int64_t)a.max_blocks_per_seq * BS;
-  if (L <= 0 || L > a.max_seq_len || L > table_tokens) {
-    if (part == 0) {
-      if (threadIdx.x == 0) atomicOr(a.flags, PAGEDKV_FLAG_BAD_SEQ_LEN);
-      for (int i = threadIdx.x; i < GQ * D; i += blockDim.x)
-        out[head0 * D + i] = __float2bfloat16_rn(0.0f);
-    }
-    return;
-  }
-  const int t0 = part * a.part_tokens;
-  if (t0 >= L) return;
-  const int t1 = min(t0 + a.part_tokens, L);
-  const int nparts = (L + a.part_tokens - 1) / a.part_tokens;
+  // This partition's block-table entries and the consumers' q fragments are
+  // loaded before the sequence length arrives (neither depends on it), so
+  // the start-up costs one round trip to memory instead of two.
+  const int skip = a.skip_tokens;
+  const int t0 = skip + part * a.part_tokens;
   const int first_blk = t0 / BS;
-  const int nblk = (t1 - 1) / BS - first_blk + 1;        // >= 1, <= kMaxBlocks
-
-  const uint32_t stages = (smem_addr(smem_raw) + 1023u) & ~1023u;
-
-  // ---- set-up: barriers, the partition's block ids (and int8 scales) ------
-  if (threadIdx.x == 0) {
-    cta_bad = 0;
-    cta_timeout = 0;
-    v_max_scale = 0.0f;
-    for (int s = 0; s < S; ++s) {
-      mbar_init(smem_addr(&full_bar[s]), 1);
-      mbar_init(smem_addr(&empty_bar[s]), kConsumers);
-    }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  const int spec_blk = min(a.part_tokens / BS, a.max_blocks_per_seq - first_blk);
+  const int32_t* bt = a.block_tables + (int64_t)b * a.max_blocks_per_seq + first_blk;
+  int32_t spec_id[kSpec];
+#pragma unroll
+  for (int r = 0; r < kSpec; ++r) {
+    const int j = threadIdx.x + r * kThreads;
+    spec_id[r] = j < spec_blk ? bt[j] : -1;
   }
-  // Consumers start their q loads now, so they overlap the block-id loads.
   // Q^T fragments (B operand of S^T = K . Q^T): b0 = (k = 2t, 2t+1; n = g),
   // b1 = (k = 2t+8, 2t+9; n = g).  k indexes d: for bf16 the natural order
   // 16ks + k; for int8 the order in which each lane reads its own 16-byte
@@ -320,10 +123,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
+
+  // ---- sequence checks (uniform over the CTA) -----------------------------
+  const int L = a.seq_lens[b];
+  const int64_t table_tokens = (int64_t)a.max_blocks_per_seq * BS;
+  if (L <= a.skip_tokens || L > a.max_seq_len || L > table_tokens) {
+    if (part == 0) {
+      if (threadIdx.x == 0) atomicOr(a.flags, PAGEDKV_FLAG_BAD_SEQ_LEN);
+      for (int i = threadIdx.x; i < GQ * D; i += blockDim.x)
+        out[head0 * D + i] = __float2bfloat16_rn(0.0f);
+    }
+    return;
+  }
+  // Tokens [skip, L) are split into partitions here; a shared prefix
+  // (skip > 0) is attended by the prefix kernel and merged afterwards, so
+  // with one every row writes a partial.
+  if (t0 >= L) return;
+  const int t1 = min(t0 + a.part_tokens, L);
+  const int nparts = (L - skip + a.part_tokens - 1) / a.part_tokens + (skip > 0 ? a.prefix_chunks : 0);
+  const int nblk = (t1 - 1) / BS - first_blk + 1;        // >= 1, <= spec_blk
+
+  const uint32_t stages = (smem_addr(smem_raw) + 1023u) & ~1023u;
+
+  // ---- set-up: barriers, the partition's block ids (and int8 scales) ------
+  if (threadIdx.x == 0) {
+    cta_bad = 0;
+    cta_timeout = 0;
+    v_max_scale = 0.0f;
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_addr(&full_bar[s]), 1);
+      mbar_init(smem_addr(&empty_bar[s]), kConsumers);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
   __syncthreads();  // barriers and flags initialised
-  const int32_t* bt = a.block_tables + (int64_t)b * a.max_blocks_per_seq + first_blk;
-  for (int j = threadIdx.x; j < nblk; j += blockDim.x) {
-    const int32_t p = bt[j];
+  if (part == 0 && a.prefix_blocks != nullptr) {
+    // The sequence's first blocks must be the shared prefix blocks.
+    const int32_t* bt0 = a.block_tables + (int64_t)b * a.max_blocks_per_seq;
+    for (int j = threadIdx.x; j < a.num_prefix_blocks; j += blockDim.x)
+      if (bt0[j] != a.prefix_blocks[j]) cta_bad = 1;
+  }
+#pragma unroll
+  for (int r = 0; r < kSpec; ++r) {
+    const int j = threadIdx.x + r * kThreads;
+    if (j >= nblk) continue;
+    const int32_t p = spec_id[r];
     const bool ok = p >= 0 && p < a.num_blocks;
     blk_id[j] = ok ? p : 0;
     if (!ok) cta_bad = 1;
@@ -683,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (nparts == 1) {
         out[head0 * D + i] = __float2bfloat16_rn(0.0f);
       } else {
-        const int64_t r = (head0 + hh) * a.max_parts + part;
+        const int64_t r = (head0 + hh) * a.slots + part;
         a.ws_acc[r * D + e] = 0.0f;
         if (e == 0) {
           a.ws_ml[2 * r] = 0.0f;
@@ -711,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (nparts == 1) {
       out[head0 * D + i] = __float2bfloat16_rn(num / den);
     } else {
-      const int64_t r = (head0 + hh) * a.max_parts + part;
+      const int64_t r = (head0 + hh) * a.slots + part;
       a.ws_acc[r * D + e] = num;
       if (e == 0) {
         a.ws_ml[2 * r] = M;
@@ -788,8 +632,25 @@ kv_status launch_t(const DecodeArgs& a, cudaStream_t s) {
   if ((st = make_map<D, BS, kInt8>(&km, a.k_cache, a)) != KV_OK) return st;
   if ((st = make_map<D, BS, kInt8>(&vm, a.v_cache, a)) != KV_OK) return st;
   const dim3 grid(a.num_kv_heads, a.batch, a.max_parts);
-  decode_kernel<D, BS, kInt8><<<grid, kThreads, G::kSmemBytes, s>>>(km, vm, a);
-  return cuda_check(cudaGetLastError(), "decode_kernel launch");
+  if (a.prefix_chunks == 0) {
+    decode_kernel<D, BS, kInt8><<<grid, kThreads, G::kSmemBytes, s>>>(km, vm, a);
+    return cuda_check(cudaGetLastError(), "decode_kernel launch");
+  }
+  // Behind the prefix kernel: launched as its programmatic dependent so the
+  // two run side by side (this kernel never reads the prefix results; the
+  // merge, a plain launch, waits for both).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = G::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_check(cudaLaunchKernelEx(&cfg, decode_kernel<D, BS, kInt8>, km, vm, a),
+                    "decode_kernel launch");
 }
 
 template <int D, bool kInt8>
@@ -797,7 +658,23 @@ kv_status launch_bs(const DecodeArgs& a, cudaStream_t s) {
   return a.block_size == 32 ? launch_t<D, 32, kInt8>(a, s) : launch_t<D, 16, kInt8>(a, s);
 }
 
+template <int D, int BS, bool kInt8>
+kv_status maps_t(const DecodeArgs& a, CUtensorMap* km, CUtensorMap* vm) {
+  kv_status st = make_map<D, BS, kInt8>(km, a.k_cache, a);
+  return st != KV_OK ? st : make_map<D, BS, kInt8>(vm, a.v_cache, a);
+}
+
 }  // namespace
+
+kv_status make_kv_maps(const DecodeArgs& a, CUtensorMap* km, CUtensorMap* vm) {
+  const bool int8 = a.dtype == KV_DTYPE_INT8, b32 = a.block_size == 32;
+  if (a.head_dim == 128) {
+    if (int8) return b32 ? maps_t<128, 32, true>(a, km, vm) : maps_t<128, 16, true>(a, km, vm);
+    return b32 ? maps_t<128, 32, false>(a, km, vm) : maps_t<128, 16, false>(a, km, vm);
+  }
+  if (int8) return b32 ? maps_t<64, 32, true>(a, km, vm) : maps_t<64, 16, true>(a, km, vm);
+  return b32 ? maps_t<64, 32, false>(a, km, vm) : maps_t<64, 16, false>(a, km, vm);
+}
 
 kv_status launch_decode(const DecodeArgs& a, cudaStream_t s) {
   if (a.batch > 65535 || a.max_parts > 65535)

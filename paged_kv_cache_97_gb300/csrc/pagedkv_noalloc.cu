@@ -58,12 +58,11 @@ extern "C" kv_status paged_attention_decode_noalloc(
     int num_blocks, int block_size, int max_seq_len, float scale, kv_dtype dtype, void* stream) {
   if (batch > 0 && num_q_heads > 0 && num_kv_heads > 0 && head_dim > 0 && max_seq_len > 0) {
     // Scratch this call needs: the partials of every (sequence, query head,
-    // partition) when the sequences split into more than one partition.
+    // partition) when a sequence spans several partitions.
     const int part = pagedkv_partition_tokens(batch, num_kv_heads, max_seq_len, block_size);
     if (part <= 0) return fail(KV_ERR_CUDA, "paged_attention_decode_noalloc: no device");
-    const size_t parts = (size_t)(max_seq_len + part - 1) / part;
-    const size_t need =
-        parts > 1 ? (size_t)batch * num_q_heads * parts * (head_dim + 2) * sizeof(float) : 0;
+    const int parts = (max_seq_len + part - 1) / part;
+    const size_t need = decode_workspace_need(batch, num_q_heads, head_dim, parts);
     if (need > PAGEDKV_NOALLOC_SCRATCH_BYTES)
       return fail(KV_ERR_INVALID_ARG,
                   "paged_attention_decode_noalloc: this shape needs %zu bytes of scratch, more "

@@ -80,6 +80,22 @@ class GpuStep:
         self.append()
         return self.attend()
 
+    def prefix_step(self, append=True):
+        """pagedkv_decode_step_prefix with the workload's shared prefix."""
+        s = self.wl.spec
+        P = s.shared_prefix_tokens // s.block_size
+        if not hasattr(self, "prefix_blocks"):
+            self.prefix_blocks = self.block_tables[0, :P].contiguous()
+            ws = pkv.prefix_workspace_bytes(s.batch, s.num_q_heads, s.head_dim, self.max_seq_len,
+                                            s.block_size, P)
+            self.prefix_ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=self.dev)
+        pkv.decode_step_prefix(self.out, self.q, self.new_k if append else None,
+                               self.new_v if append else None, self.k_cache, self.v_cache,
+                               self.block_tables, self.seq_lens, self.max_seq_len, s.scale,
+                               self.prefix_blocks, self.prefix_ws, k_scale=self.k_scale,
+                               v_scale=self.v_scale)
+        return self.out
+
     def fused_step(self):
         s = self.wl.spec
         pkv.decode_step(self.out, self.q, self.new_k, self.new_v, self.k_cache, self.v_cache,

@@ -135,7 +135,7 @@ def test_repeated_steps_are_deterministic():
     np.testing.assert_array_equal(a, b)
 
 
-@pytest.mark.parametrize("part", ["256", "512", "8192"])
+@pytest.mark.parametrize("part", ["256", "512", "2048"])
 def test_partition_size_does_not_change_the_answer(monkeypatch, part):
     wl = CASES["ragged_g4_d128"]()
     kc, vc, ks, vs = oracle_pool(wl)
@@ -188,6 +188,85 @@ def test_decode_step_replays_from_a_cuda_graph(case):
     np.testing.assert_array_equal(bits_of(g.k_cache), bits_of(eager.k_cache))
     np.testing.assert_array_equal(bits_of(g.v_cache), bits_of(eager.v_cache))
     check_status()
+
+
+# ---------------------------------------------------------------------------
+# Shared prefix (one dense pass per KV head over the shared blocks)
+# ---------------------------------------------------------------------------
+
+PREFIX_CASES = {
+    "g4_d128_bs16": lambda: small([33, 48, 49, 300, 1000, 2100], hq=32, hkv=8, d=128, prefix=32, seed=31),
+    "g8_d128_bs32": lambda: small([65, 90, 700, 1500], hq=64, hkv=8, d=128, bs=32, prefix=64, seed=32),
+    "g4_d64_bs16_long_prefix": lambda: small([600, 601, 640, 1200, 700, 900, 650, 3000, 610, 800,
+                                              999, 1001, 608, 2048, 1800, 777, 650],
+                                             hq=8, hkv=2, d=64, prefix=592, seed=33),
+    "g1_d128": lambda: small([17, 40, 333], hq=4, hkv=4, d=128, prefix=16, seed=34),
+}
+
+
+@pytest.mark.parametrize("case", sorted(PREFIX_CASES))
+def test_prefix_step_matches_oracle(case):
+    wl = PREFIX_CASES[case]()
+    g = GpuStep(wl)
+    got = out_f64(g.prefix_step())
+    torch.cuda.synchronize()
+    check_status()
+    kc, vc, ks, vs = oracle_pool(wl)
+    np.testing.assert_array_equal(bits_of(g.k_cache), kc)          # the append, bit for bit
+    np.testing.assert_array_equal(bits_of(g.v_cache), vc)
+    ref, rc = oracle.paged_attention(wl.q, kc, vc, wl.block_tables, wl.seq_lens, wl.spec.scale,
+                                     threads=os.cpu_count())
+    assert rc == 0
+    assert_close(got, ref, "bf16", case)
+    plain = out_f64(GpuStep(wl).fused_step())
+    assert_close(got, plain, "bf16", case + " vs plain step")
+
+
+def test_prefix_attend_only_and_repeat():
+    wl = PREFIX_CASES["g4_d128_bs16"]()
+    g = GpuStep(wl)
+    first = bits_of(g.prefix_step()).copy()
+    again = bits_of(g.prefix_step(append=False))        # token already appended: same answer
+    np.testing.assert_array_equal(first, again)
+
+
+def test_prefix_mismatch_is_flagged_and_zeroed():
+    wl = PREFIX_CASES["g4_d128_bs16"]()
+    g = GpuStep(wl)
+    g.prefix_step()
+    bt = wl.block_tables.copy()
+    bt[2, 1] = bt[2, 5] if bt[2, 5] >= 0 else wl.num_blocks - 1   # sequence 2 leaves the prefix
+    g.block_tables = torch.from_numpy(bt).cuda()
+    out = bits_of(g.prefix_step(append=False))
+    st, flags = pkv.get_status()
+    assert flags == pkv.FLAG_BAD_BLOCK
+    assert not out[2].any() and out[0].any() and out[3].any()
+
+
+def test_prefix_rejects_int8_pools():
+    wl = small([65, 90], hq=64, hkv=8, d=128, bs=32, kv="int8", seed=35)
+    g = GpuStep(wl)
+    pb = g.block_tables[0, :1].contiguous()
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pkv.KVError) as e:
+        pkv.decode_step_prefix(g.out, g.q, None, None, g.k_cache, g.v_cache, g.block_tables,
+                               g.seq_lens, g.max_seq_len, wl.spec.scale, pb, ws, k_scale=g.k_scale,
+                               v_scale=g.v_scale)
+    assert e.value.status == pkv.KV_ERR_NOT_IMPLEMENTED
+
+
+def test_full_size_shared_prefix_workload_sampled_rows():
+    wl = workloads.make(4)
+    g = GpuStep(wl)
+    got = out_f64(g.prefix_step())
+    torch.cuda.synchronize()
+    check_status()
+    seqs, rows = sample_rows(wl)
+    kc, vc, ks, vs = oracle_pool(wl, seqs=seqs)
+    ref, rc = oracle.paged_attention(wl.q, kc, vc, wl.block_tables, wl.seq_lens, wl.spec.scale,
+                                     rows=rows, threads=os.cpu_count())
+    assert rc == 0
+    assert_close(got[rows[:, 0], rows[:, 1]], ref, "bf16", "config 4, shared-prefix path")
 
 
 # ---------------------------------------------------------------------------
