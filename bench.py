@@ -224,6 +224,118 @@ def measured_peak_gbs():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# ---------------------------------------------------------------------------
+# The rows beyond the decode step: copy-on-write
+# ---------------------------------------------------------------------------
+
+def measure_cow(pkv, dev, stream, peak):
+    """Copy-on-write (block copy + beam-search decode steps), timed with CUDA
+    events on the launching stream."""
+    import torch
+    from gpu_helpers import to_dev_bf16
+
+    # (1) pagedkv_copy_blocks: 2048 block pairs of the 8B-like geometry
+    # (16 x 8 x 128 bf16 = 32 KB per block and pool); two disjoint pair sets
+    # alternate so each launch reads and writes 256 MB that are not in L2.
+    nb, bs, hkv, d, npairs = 8192, 16, 8, 128, 2048
+    kc = torch.zeros((nb, bs, hkv, d), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    perm = torch.randperm(nb, generator=torch.Generator().manual_seed(7)).to(torch.int32)
+    sets = [torch.stack([perm[i * 2 * npairs: i * 2 * npairs + npairs],
+                         perm[i * 2 * npairs + npairs: (i + 1) * 2 * npairs]], 1).contiguous().to(dev)
+            for i in range(2)]
+    for i in range(6):
+        pkv.copy_blocks(kc, vc, sets[i % 2])
+    reps = 40
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * reps)]
+    torch.cuda.synchronize(dev)
+    for i in range(reps):
+        ev[2 * i].record(stream)
+        pkv.copy_blocks(kc, vc, sets[i % 2])
+        ev[2 * i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    us = statistics.fmean(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(reps)) * 1e3
+    copy_bytes = npairs * 2 * bs * hkv * d * 2 * 2          # K and V, read + write
+    del kc, vc
+    copy_row = {"kernel": "copy_blocks_kernel", "pairs": npairs, "bytes_per_launch": copy_bytes,
+                "us_per_launch": round(us, 2), "achieved_gbs": round(copy_bytes / us / 1e3, 1),
+                "frac": round(copy_bytes / us / 1e3 / peak, 4)}
+
+    # (2) beam search: 16 prompts x 4 beams; per step the pool's copy-on-write
+    # bookkeeping (host), the block copies and the fused decode step
+    w = workloads.beam_search_8b()
+    pool = pkv.KVPool(w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
+    kc = torch.zeros((w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim), dtype=torch.bfloat16,
+                     device=dev)
+    vc = torch.zeros_like(kc)
+    tables = np.full((w.num_seqs, w.max_blocks_per_seq), -1, np.int32)
+    for p, L in enumerate(w.parent_lens):
+        L = int(L)
+        ids = pool.alloc((L + w.block_size - 1) // w.block_size)
+        tables[p * w.beams, :len(ids)] = ids
+        slots = torch.empty(L, dtype=torch.int64, device=dev)
+        pkv.token_slot_mapping(torch.from_numpy(tables[p * w.beams:p * w.beams + 1].copy()).to(dev),
+                               torch.arange(L, dtype=torch.int32, device=dev), w.num_blocks,
+                               w.block_size, slots, seq_idx=torch.zeros(L, dtype=torch.int32, device=dev))
+        pkv.reshape_and_cache(to_dev_bf16(w.parent_k[p], dev), to_dev_bf16(w.parent_v[p], dev), kc, vc,
+                              slots)
+        for j in range(1, w.beams):
+            pool.fork(ids)
+            tables[p * w.beams + j] = tables[p * w.beams]
+    q = to_dev_bf16(w.step_q, dev)
+    nk, nv = to_dev_bf16(w.step_k, dev), to_dev_bf16(w.step_v, dev)
+    n = w.num_seqs
+    out = torch.empty((n, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
+    max_len = int(w.seq_lens_at(w.steps - 1).max())
+    ws = torch.empty(max(pkv.workspace_bytes(n, w.num_q_heads, w.head_dim, max_len, w.block_size), 16),
+                     dtype=torch.uint8, device=dev)
+    bt_dev = torch.empty(tables.shape, dtype=torch.int32, device=dev)
+    sl_dev = torch.empty(n, dtype=torch.int32, device=dev)
+    pairs_dev = torch.empty((n, 2), dtype=torch.int32, device=dev)
+    h_bt = torch.empty(tables.shape, dtype=torch.int32).pin_memory()
+    h_sl = torch.empty(n, dtype=torch.int32).pin_memory()
+    h_pairs = torch.empty((n, 2), dtype=torch.int32).pin_memory()
+    copies, kv_read = 0, 0
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record(stream)
+    for step in range(w.steps):
+        lens = w.seq_lens_at(step)
+        pairs = pool.prepare_append(tables, lens)
+        copies += len(pairs)
+        kv_read += int(lens.sum()) * 2 * w.num_kv_heads * w.head_dim * 2
+        torch.cuda.current_stream(dev).synchronize()      # pinned staging is reused next step
+        h_bt.numpy()[:] = tables
+        h_sl.numpy()[:] = lens
+        bt_dev.copy_(h_bt, non_blocking=True)
+        sl_dev.copy_(h_sl, non_blocking=True)
+        if len(pairs):
+            h_pairs.numpy()[:len(pairs)] = pairs
+            pairs_dev[:len(pairs)].copy_(h_pairs[:len(pairs)], non_blocking=True)
+            pkv.copy_blocks(kc, vc, pairs_dev[:len(pairs)])
+        pkv.decode_step(out, q[step], nk[step], nv[step], kc, vc, bt_dev, sl_dev, int(lens.max()),
+                        w.scale, ws)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall_us = (time.perf_counter() - t0) / w.steps * 1e6
+    gpu_us = e0.elapsed_time(e1) / w.steps * 1e3
+    st, flags = pkv.get_status()
+    assert st == 0 and flags == 0, f"device status 0x{flags:x}"
+    used, _ = pool.stats()
+    unshared = sum((int(L) + w.block_size - 1) // w.block_size for L in w.seq_lens_at(w.steps - 1))
+    beam_row = {"workload": f"beam search, 16 prompts U{{512..4096}} x 4 beams, 32/8 heads, d 128, "
+                            f"bs 16, {w.steps} steps",
+                "us_per_step": round(gpu_us, 2), "wall_us_per_step": round(wall_us, 2),
+                "kv_read_gbs": round(kv_read / w.steps / gpu_us / 1e3, 1),
+                "block_copies": copies,
+                "blocks_used": used, "blocks_unshared": unshared,
+                "memory_saved": round(1 - used / unshared, 4),
+                "note": "per step: host copy-on-write bookkeeping, table/length upload, block "
+                        "copies, fused decode step; synchronised once per step for the host tables"}
+    return {"copy_blocks": copy_row, "beam_search": beam_row}
+
+
 def gpu_arm(args, rank, world, local_rank, dist):
     import torch
 
@@ -375,6 +487,8 @@ def gpu_arm(args, rank, world, local_rank, dist):
         "gpu_launches": launches_per_step * K,
         "clocks": sampler.summary(),
     }
+    if not args.no_rows:
+        line["rows"] = {"cow": measure_cow(pkv, dev, stream, peak)}
     return line, wl
 
 
@@ -390,6 +504,8 @@ def main():
     ap.add_argument("--no-shared-prefix", action="store_true",
                     help="for workloads with a shared prefix, time the plain step instead of "
                          "pagedkv_decode_step_prefix")
+    ap.add_argument("--no-rows", action="store_true",
+                    help="skip the extra measurements (copy-on-write) reported under 'rows'")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -73,9 +73,10 @@ typedef enum { KV_DTYPE_BF16 = 0, KV_DTYPE_INT8 = 1 } kv_dtype;
 /* Block pool (host bookkeeping)                                            */
 /* ------------------------------------------------------------------------ */
 
-/* Opaque host object: pool geometry plus the free list.  It owns no device
- * memory: the caller allocates the K/V pool tensors (pagedkv_pool_tensor_bytes
- * each) and the scales. */
+/* Opaque host object: pool geometry, the free list and a reference count per
+ * block.  It owns no device memory: the caller allocates the K/V pool tensors
+ * (pagedkv_pool_tensor_bytes each) and the scales.  Not thread-safe: one
+ * scheduler thread owns a pool. */
 typedef struct kv_pool kv_pool;
 
 /* Create a pool of num_blocks blocks.  Every id is free, in ascending order
@@ -93,24 +94,86 @@ void kv_pool_destroy(kv_pool *pool);
 size_t kv_pool_block_bytes(const kv_pool *pool);
 
 /* Allocate n blocks, all or none, from the front of the free list, writing
- * their ids to host array out_ids[n] (“LLM 推理引擎深度解析”, §2.1: allocation
- * takes ids in free-list order and fails when too few are free).
- * KV_ERR_OUT_OF_BLOCKS leaves the pool unchanged. */
+ * their ids to host array out_ids[n]; each starts with one reference
+ * (“LLM 推理引擎深度解析”, §2.1: allocation takes ids in free-list order and
+ * fails when too few are free).  KV_ERR_OUT_OF_BLOCKS leaves the pool
+ * unchanged. */
 kv_status kv_pool_alloc(kv_pool *pool, int n, int32_t *out_ids);
 
-/* Return n block ids (host array) to the back of the free list (same page:
- * finishing a request returns all its blocks).  Ids that are not currently
- * allocated, or repeated, make the whole call fail with KV_ERR_INVALID_ARG
- * and change nothing. */
+/* Add one reference to each of n allocated blocks (host array): a forked
+ * sequence (a beam, a parallel sample) now maps them too (“让 Agent 跑得快：
+ * LLM 推理服务”, §二 Copy-on-Write: candidates forked from one prefix share
+ * its physical blocks, reference count above one).  An id that is not
+ * allocated fails the whole call with KV_ERR_INVALID_ARG, changing nothing. */
+kv_status kv_pool_fork(kv_pool *pool, const int32_t *ids, int n);
+
+/* Drop one reference from each of n block ids (host array); a block left
+ * with none goes to the back of the free list, in the order of `ids` (same
+ * §二: a block whose count reaches zero returns to the pool; “LLM 推理引擎
+ * 深度解析”, §2.1: finishing a request returns its blocks).  An id that is
+ * not allocated, or listed more often than it is referenced, fails the whole
+ * call with KV_ERR_INVALID_ARG and changes nothing. */
 kv_status kv_pool_free(kv_pool *pool, const int32_t *ids, int n);
+
+/* References held on block `id`: 0 when free, -1 for an id outside the
+ * pool or a NULL pool. */
+int kv_pool_refcount(const kv_pool *pool, int32_t id);
 
 /* Number of allocated and free blocks (either pointer may be NULL). */
 kv_status kv_pool_stats(const kv_pool *pool, int *used, int *free_blocks);
+
+/* Makes every sequence's decode append target writable before the step
+ * (host arrays; sequences in order b = 0..batch-1):
+ *   - the new token sits at position p = seq_lens[b] - 1 (seq_lens counts
+ *     it), in logical block j = p / block_size;
+ *   - p % block_size == 0 (the token opens a block): a block is taken from
+ *     the free list and written to block_tables[b][j], whose old value is
+ *     ignored (“让 Agent 跑得快”, §五: a new block every block_size tokens);
+ *   - otherwise, when block_tables[b][j] is shared (reference count above
+ *     one), a free block d is taken, the old block loses one reference,
+ *     block_tables[b][j] becomes d and the pair (old, d) is appended to
+ *     copy_pairs (§二 Copy-on-Write: copy the block and repoint the table
+ *     before writing).  A block shared by k sequences of the batch is copied
+ *     for the first k - 1 and written in place by the last.
+ * The caller copies the pairs with pagedkv_copy_blocks and uploads the
+ * tables before the append.
+ *   block_tables  host int32 [batch, max_blocks_per_seq], updated in place
+ *   seq_lens      host int32 [batch]
+ *   copy_pairs    host int32 [batch][2] (output: src, dst)
+ *   num_copies    output: pairs written
+ * All or nothing: KV_ERR_OUT_OF_BLOCKS when the free list is too short,
+ * KV_ERR_INVALID_ARG for a length outside (0, max_blocks_per_seq *
+ * block_size] or a write into a block that is not allocated; either leaves
+ * the pool and the tables unchanged. */
+kv_status kv_pool_prepare_append(kv_pool *pool, int32_t *block_tables,
+                                 int max_blocks_per_seq, const int32_t *seq_lens,
+                                 int batch, int32_t *copy_pairs, int *num_copies);
 
 /* Bytes of one pool tensor (K or V): num_blocks * block_size * num_kv_heads
  * * head_dim * dtype_size. */
 size_t pagedkv_pool_tensor_bytes(int num_blocks, int block_size,
                                  int num_kv_heads, int head_dim, kv_dtype dtype);
+
+/* Copies whole physical blocks of both pools, bit for bit: for every pair i,
+ * block block_pairs[i][1] of k_cache and v_cache (and its row of k_scale and
+ * v_scale for 8-bit pools) becomes a copy of block block_pairs[i][0] (“让
+ * Agent 跑得快”, §二 Copy-on-Write: the block is copied before a shared
+ * sequence writes into it).
+ *   k_cache, v_cache  device [num_blocks, block_size, num_kv_heads, head_dim],
+ *                     16-byte aligned
+ *   k_scale, v_scale  device fp32 [num_blocks, num_kv_heads] for INT8, NULL
+ *                     for BF16
+ *   block_pairs       device int32 [num_pairs][2] (src, dst)
+ * A destination must not be the source or destination of another pair of
+ * the same call (pairs from kv_pool_prepare_append never are).  A pair with
+ * an id outside [0, num_blocks) is skipped and sets PAGEDKV_FLAG_BAD_BLOCK;
+ * src == dst is a no-op.  At most 65535 pairs per call.  Asynchronous on
+ * `stream`. */
+kv_status pagedkv_copy_blocks(void *k_cache, void *v_cache, float *k_scale,
+                              float *v_scale, const int32_t *block_pairs,
+                              int num_pairs, int num_blocks, int block_size,
+                              int num_kv_heads, int head_dim, kv_dtype dtype,
+                              void *stream);
 
 /* ------------------------------------------------------------------------ */
 /* Slot mapping                                                             */

@@ -13,7 +13,9 @@ Contents, each citing the passage it follows (page titles as printed):
   PagedKVCache.allocate; “让 Agent 跑得快”, §五: waste only in the last block);
 * ``BlockPoolModel`` -- the block pool's allocation rules (“LLM 推理引擎深度解析”,
   §2.1: FIFO free list, all-or-nothing allocation that fails when short,
-  free returns every block);
+  free returns every block) and its sharing rules (“让 Agent 跑得快”, §二
+  Copy-on-Write: reference counts, copy before writing a shared block);
+* ``copy_blocks`` -- the block copy of copy-on-write (plain numpy);
 * ``token_slots``, ``append_bf16``, ``append_int8``, ``quantize_int8``,
   ``paged_attention`` (three-pass or online), ``attention_partials``,
   ``lse_merge`` -- thin ctypes wrappers over ``pagedkv_oracle.c`` (plain C,
@@ -25,6 +27,7 @@ brute force and a library routine; none is "parity unpinned".
 """
 from __future__ import annotations
 
+import copy
 import ctypes
 import os
 import subprocess
@@ -143,17 +146,31 @@ def internal_waste_tokens(seq_len: int, block_size: int) -> int:
 
 @dataclass
 class BlockPoolModel:
-    """Allocation rules of the physical block pool.
+    """Allocation, sharing and copy-on-write rules of the physical block pool.
 
     “LLM 推理引擎深度解析”, §2.1 (PagedKVCache): the pool starts with every
     block id free in ascending order; allocation takes ids from the front of
     the free list, all or none, and fails when too few are free; freeing
-    appends the ids to the back.  Freeing an id that is not allocated is an
-    error here (the page's sketch frees per sequence and never sees it).
+    appends the ids to the back.
+
+    “让 Agent 跑得快：LLM 推理服务”, §二 (Copy-on-Write：Beam Search 的内存优化):
+    sequences forked from one prefix map the same physical blocks, each
+    holding a reference; a sequence that must write a token into a block
+    held more than once first copies the block and points its table at the
+    copy; a block whose count reaches zero goes back to the pool.  §五 (共享
+    前缀): only the current decode token writes, and a new block is taken each
+    time a sequence fills its last one.
+
+    Readings of this library where the pages are silent: freeing drops one
+    reference per listed id (an id listed more often than it is held, or not
+    held at all, is an error and nothing changes); blocks whose count reaches
+    zero join the free list in the order listed; ``prepare_append`` handles
+    the sequences of a step in order, each copy or new block taking the front
+    of the free list, and changes nothing when the list runs short.
     """
     num_blocks: int
     free_list: list = field(default_factory=list)
-    allocated: set = field(default_factory=set)
+    refs: dict = field(default_factory=dict)      # block id -> references (> 0)
 
     def __post_init__(self):
         self.free_list = list(range(self.num_blocks))
@@ -164,22 +181,78 @@ class BlockPoolModel:
         if len(self.free_list) < n:
             raise MemoryError("block pool exhausted")
         ids, self.free_list = self.free_list[:n], self.free_list[n:]
-        self.allocated.update(ids)
+        for i in ids:
+            self.refs[i] = 1
         return ids
 
     def alloc_sequence(self, seq_len: int, block_size: int) -> list:
         return self.alloc(blocks_needed(seq_len, block_size))
 
+    def fork(self, ids) -> None:
+        ids = list(ids)
+        if any(i not in self.refs for i in ids):
+            raise ValueError("forking a block that is not allocated")
+        for i in ids:
+            self.refs[i] += 1
+
     def free(self, ids) -> None:
         ids = list(ids)
-        if len(set(ids)) != len(ids) or any(i not in self.allocated for i in ids):
-            raise ValueError("freeing a block that is not allocated")
+        for i in set(ids):
+            if ids.count(i) > self.refs.get(i, 0):
+                raise ValueError("freeing a block that is not allocated")
         for i in ids:
-            self.allocated.discard(i)
-        self.free_list.extend(ids)
+            self.refs[i] -= 1
+            if self.refs[i] == 0:
+                del self.refs[i]
+                self.free_list.append(i)
+
+    def refcount(self, i: int) -> int:
+        return self.refs.get(i, 0) if 0 <= i < self.num_blocks else -1
 
     def stats(self):
-        return len(self.allocated), len(self.free_list)
+        return len(self.refs), len(self.free_list)
+
+    def prepare_append(self, tables, seq_lens, block_size):
+        """Make each sequence's append target writable; ``tables`` is a list
+        of per-sequence block-id lists (updated in place, grown when the token
+        opens a block).  Returns the (src, dst) block copies in order."""
+        trial = copy.deepcopy(self)
+        new_tables = [list(t) for t in tables]
+        copies = []
+        for t, L in zip(new_tables, seq_lens):
+            if L <= 0:
+                raise ValueError("sequence length must be positive")
+            j, row = (L - 1) // block_size, (L - 1) % block_size
+            if row == 0:                                  # the token opens a block
+                new = trial.alloc(1)[0]
+                if j < len(t):
+                    t[j] = new
+                else:
+                    t.extend([-1] * (j - len(t)) + [new])
+                continue
+            if j >= len(t) or t[j] not in trial.refs:
+                raise ValueError("writing into a block that is not allocated")
+            old = t[j]
+            if trial.refs[old] > 1:                       # shared: copy, then write
+                new = trial.alloc(1)[0]
+                trial.free([old])
+                t[j] = new
+                copies.append((old, new))
+        self.free_list, self.refs = trial.free_list, trial.refs
+        for t, nt in zip(tables, new_tables):
+            t[:] = nt
+        return copies
+
+
+def copy_blocks(k_cache, v_cache, pairs, k_scale=None, v_scale=None) -> None:
+    """Block copy of copy-on-write (“让 Agent 跑得快”, §二): for each (src, dst)
+    in order, block dst of both pools (and its scale rows) becomes block src."""
+    for src, dst in pairs:
+        k_cache[dst] = k_cache[src]
+        v_cache[dst] = v_cache[src]
+        if k_scale is not None:
+            k_scale[dst] = k_scale[src]
+            v_scale[dst] = v_scale[src]
 
 
 # --------------------------------------------------------------------------

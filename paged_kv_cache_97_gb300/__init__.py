@@ -34,6 +34,10 @@ SIGNATURES = {
     "kv_pool_alloc": (_I, [_P, _I, _P]),
     "kv_pool_free": (_I, [_P, _P, _I]),
     "kv_pool_stats": (_I, [_P, _P, _P]),
+    "kv_pool_fork": (_I, [_P, _P, _I]),
+    "kv_pool_refcount": (_I, [_P, ctypes.c_int32]),
+    "kv_pool_prepare_append": (_I, [_P, _P, _I, _P, _I, _P, _P]),
+    "pagedkv_copy_blocks": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "pagedkv_pool_tensor_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "pagedkv_slot_mapping": (_I, [_P, _I, _P, _I, _I, _I, _P, _P]),
     "pagedkv_token_slot_mapping": (_I, [_P, _I, _P, _P, _I, _I, _I, _P, _P]),
@@ -128,7 +132,9 @@ def _pool_dtype(k_cache):
 # --------------------------------------------------------------------------
 
 class KVPool:
-    """Host bookkeeping of a block pool (free list, FIFO, all-or-nothing)."""
+    """Host bookkeeping of a block pool: FIFO free list, all-or-nothing
+    allocation, a reference count per block and copy-on-write before a
+    decode append."""
 
     def __init__(self, num_blocks: int, block_size: int, num_kv_heads: int, head_dim: int,
                  dtype: int = DTYPE_BF16):
@@ -162,6 +168,31 @@ class KVPool:
         used, free = ctypes.c_int(), ctypes.c_int()
         _check(self._lib.kv_pool_stats(self._h, ctypes.byref(used), ctypes.byref(free)))
         return used.value, free.value
+
+    def fork(self, ids) -> None:
+        """One more reference on each block (a forked sequence maps them)."""
+        ids = list(ids)
+        arr = (ctypes.c_int32 * max(len(ids), 1))(*ids)
+        _check(self._lib.kv_pool_fork(self._h, arr, len(ids)))
+
+    def refcount(self, block_id: int) -> int:
+        return self._lib.kv_pool_refcount(self._h, block_id)
+
+    def prepare_append(self, block_tables, seq_lens):
+        """Blocks for this step's appends (host int32 numpy arrays; the table
+        is updated in place).  Returns the (src, dst) copy pairs as an int32
+        array [n, 2] for copy_blocks."""
+        import numpy as np
+        bt, sl = block_tables, np.ascontiguousarray(seq_lens, dtype=np.int32)
+        if bt.dtype != np.int32 or not bt.flags.c_contiguous or bt.ndim != 2:
+            raise TypeError("block_tables must be a C-contiguous int32 [batch, max_blocks] array")
+        if sl.shape != (bt.shape[0],):
+            raise ValueError("seq_lens must have one entry per table row")
+        pairs = np.zeros((max(bt.shape[0], 1), 2), np.int32)
+        n = ctypes.c_int()
+        _check(self._lib.kv_pool_prepare_append(self._h, bt.ctypes.data, bt.shape[1], sl.ctypes.data,
+                                                bt.shape[0], pairs.ctypes.data, ctypes.byref(n)))
+        return pairs[:n.value].copy()
 
 
 def pool_tensor_bytes(num_blocks, block_size, num_kv_heads, head_dim, dtype=DTYPE_BF16) -> int:
@@ -227,6 +258,25 @@ def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, k_scale=None, v_scal
     _check(load().reshape_and_cache(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
                                     _ptr(v_scale), _ptr(slot_mapping), k.shape[0], nb, bs, hkv, d, dt,
                                     _stream(stream)))
+
+
+def copy_blocks(k_cache, v_cache, block_pairs, k_scale=None, v_scale=None, stream=None):
+    """Copy whole blocks src -> dst of both pools (and 8-bit scales), for
+    the device int32 pairs [n, 2]."""
+    import torch
+    dt = _pool_dtype(k_cache)
+    _need(k_cache, k_cache.dtype, "k_cache", 4)
+    _need(v_cache, k_cache.dtype, "v_cache", 4)
+    _need(block_pairs, torch.int32, "block_pairs", 2)
+    if v_cache.shape != k_cache.shape or block_pairs.shape[1] != 2:
+        raise ValueError("pools must match and block_pairs must be [n, 2]")
+    for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+        if t is not None:
+            _need(t, torch.float32, name, 2)
+    nb, bs, hkv, d = k_cache.shape
+    _check(load().pagedkv_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                      _ptr(block_pairs), block_pairs.shape[0], nb, bs, hkv, d, dt,
+                                      _stream(stream)))
 
 
 def workspace_bytes(batch, num_q_heads, head_dim, max_seq_len, block_size) -> int:

@@ -1,6 +1,7 @@
-// pagedkv_api.cu -- the C ABI of libpagedkv: block pool bookkeeping, argument
-// checks, slot mapping and append kernels, the split-K merge kernel, and the
-// device status word.  The decode kernel itself is in pagedkv_decode.cu.
+// pagedkv_api.cu -- the C ABI of libpagedkv: argument checks, slot mapping
+// and append kernels, the split-K merge kernel, and the device status word.
+// The block pool is in pagedkv_pool.cu, the decode kernel in
+// pagedkv_decode.cu, the shared-prefix kernel in pagedkv_prefix.cu.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -58,12 +59,6 @@ kv_status device_info(DeviceInfo* out) {
   *out = d;
   return KV_OK;
 }
-
-static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }  // NULL passes
-
-static int dtype_size(kv_dtype t) { return t == KV_DTYPE_INT8 ? 1 : 2; }
-
-static bool valid_dtype(kv_dtype t) { return t == KV_DTYPE_BF16 || t == KV_DTYPE_INT8; }
 
 // ---------------------------------------------------------------------------
 // Slot mapping
@@ -308,91 +303,9 @@ using namespace pagedkv;
 // C ABI
 // ===========================================================================
 
-struct kv_pool {
-  int num_blocks, block_size, num_kv_heads, head_dim;
-  kv_dtype dtype;
-  std::deque<int32_t> free_list;   // front = next to hand out
-  std::vector<uint8_t> allocated;  // 1 = handed out
-  int used = 0;
-};
-
 extern "C" {
 
 const char* pagedkv_last_error(void) { return g_last_error; }
-
-kv_status kv_pool_create(int num_blocks, int block_size, int num_kv_heads, int head_dim,
-                         kv_dtype dtype, kv_pool** out) {
-  if (!out) return fail(KV_ERR_INVALID_ARG, "kv_pool_create: out is NULL");
-  *out = nullptr;
-  if (num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
-      !valid_dtype(dtype))
-    return fail(KV_ERR_INVALID_ARG, "kv_pool_create: sizes must be positive and dtype valid");
-  kv_pool* p = new kv_pool;
-  p->num_blocks = num_blocks;
-  p->block_size = block_size;
-  p->num_kv_heads = num_kv_heads;
-  p->head_dim = head_dim;
-  p->dtype = dtype;
-  for (int i = 0; i < num_blocks; ++i) p->free_list.push_back(i);
-  p->allocated.assign(num_blocks, 0);
-  *out = p;
-  return KV_OK;
-}
-
-void kv_pool_destroy(kv_pool* pool) { delete pool; }
-
-size_t kv_pool_block_bytes(const kv_pool* p) {
-  if (!p) return 0;
-  return 2ull * p->block_size * p->num_kv_heads * p->head_dim * dtype_size(p->dtype);
-}
-
-kv_status kv_pool_alloc(kv_pool* p, int n, int32_t* out_ids) {
-  if (!p || n < 0 || (n > 0 && !out_ids))
-    return fail(KV_ERR_INVALID_ARG, "kv_pool_alloc: bad arguments");
-  if ((size_t)n > p->free_list.size())
-    return fail(KV_ERR_OUT_OF_BLOCKS, "kv_pool_alloc: %d blocks requested, %zu free", n,
-                p->free_list.size());
-  for (int i = 0; i < n; ++i) {
-    int32_t id = p->free_list.front();
-    p->free_list.pop_front();
-    p->allocated[id] = 1;
-    out_ids[i] = id;
-  }
-  p->used += n;
-  return KV_OK;
-}
-
-kv_status kv_pool_free(kv_pool* p, const int32_t* ids, int n) {
-  if (!p || n < 0 || (n > 0 && !ids)) return fail(KV_ERR_INVALID_ARG, "kv_pool_free: bad arguments");
-  std::vector<uint8_t> seen(p->num_blocks, 0);
-  for (int i = 0; i < n; ++i) {
-    int32_t id = ids[i];
-    if (id < 0 || id >= p->num_blocks || !p->allocated[id] || seen[id])
-      return fail(KV_ERR_INVALID_ARG, "kv_pool_free: block %d is not allocated (or repeated)", id);
-    seen[id] = 1;
-  }
-  for (int i = 0; i < n; ++i) {
-    p->allocated[ids[i]] = 0;
-    p->free_list.push_back(ids[i]);
-  }
-  p->used -= n;
-  return KV_OK;
-}
-
-kv_status kv_pool_stats(const kv_pool* p, int* used, int* free_blocks) {
-  if (!p) return fail(KV_ERR_INVALID_ARG, "kv_pool_stats: pool is NULL");
-  if (used) *used = p->used;
-  if (free_blocks) *free_blocks = (int)p->free_list.size();
-  return KV_OK;
-}
-
-size_t pagedkv_pool_tensor_bytes(int num_blocks, int block_size, int num_kv_heads, int head_dim,
-                                 kv_dtype dtype) {
-  if (num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
-      !valid_dtype(dtype))
-    return 0;
-  return (size_t)num_blocks * block_size * num_kv_heads * head_dim * dtype_size(dtype);
-}
 
 kv_status pagedkv_slot_mapping(const int32_t* block_tables, int max_blocks_per_seq,
                                const int32_t* seq_lens, int batch, int block_size,

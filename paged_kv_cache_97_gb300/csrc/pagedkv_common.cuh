@@ -23,6 +23,12 @@ struct DeviceInfo {
 };
 kv_status device_info(DeviceInfo* out);
 
+// Bytes of one stored K/V element.
+inline int dtype_size(kv_dtype t) { return t == KV_DTYPE_BF16 ? 2 : 1; }
+inline bool valid_dtype(kv_dtype t) { return t == KV_DTYPE_BF16 || t == KV_DTYPE_INT8; }
+// 16-byte alignment (NULL passes).
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
 // Query heads per KV head the kernels serve (the MMA's N = 8 columns).
 constexpr int kMaxGroup = 8;
 

@@ -265,3 +265,81 @@ def custom(*, batch, num_q_heads, num_kv_heads, head_dim, block_size, seq_lens,
                 max_blocks_per_seq=max_blocks_per_seq,
                 shared_prefix_tokens=shared_prefix_tokens)
     return Workload(spec, seed, seq_lens=seq_lens)
+
+
+class BeamWorkload:
+    """Seeded inputs of a beam-search (parallel-sampling) decode run over a
+    shared pool: ``num_parents`` prompts of ``parent_lens`` tokens, each
+    forked into ``beams`` sequences (beam 0 is the parent itself) that then
+    decode ``steps`` tokens each, every beam its own k, v and q per step.
+
+    Inputs only, like ``Workload``: which blocks are shared, copied or taken
+    is decided by the pool under test.  Recipe: ``SeedSequence(seed)`` spawns
+    stream 0 (the prompts' k and v), stream 1 (per-step q), stream 2 (per-step
+    k and v) and stream 3 (int8 scales of every physical block: U(3.5, 4.5) /
+    127 per (block, KV head), fixed up front because a block's scale outlives
+    the sequence that first fills it).  Values are N(0, 1) rounded to bf16.
+    Sequence ``p * beams + j`` is beam j of parent p."""
+
+    def __init__(self, *, num_parents, beams, parent_lens, steps, num_q_heads, num_kv_heads,
+                 head_dim, block_size, num_blocks, max_blocks_per_seq, kv_dtype="bf16",
+                 seed=SEED_BASE + 97):
+        self.num_parents, self.beams, self.steps = num_parents, beams, steps
+        self.parent_lens = np.asarray(parent_lens, np.int32)
+        assert self.parent_lens.shape == (num_parents,)
+        self.num_q_heads, self.num_kv_heads, self.head_dim = num_q_heads, num_kv_heads, head_dim
+        self.block_size, self.num_blocks = block_size, num_blocks
+        self.max_blocks_per_seq, self.kv_dtype = max_blocks_per_seq, kv_dtype
+        self.scale = 1.0 / math.sqrt(head_dim)
+        st = [np.random.Generator(np.random.PCG64(c)) for c in np.random.SeedSequence(seed).spawn(4)]
+        kv = (num_kv_heads, head_dim)
+        self.parent_k = [to_bf16_bits(st[0].standard_normal((int(L),) + kv, np.float32))
+                         for L in self.parent_lens]
+        self.parent_v = [to_bf16_bits(st[0].standard_normal((int(L),) + kv, np.float32))
+                         for L in self.parent_lens]
+        n = num_parents * beams
+        self.step_q = to_bf16_bits(st[1].standard_normal((steps, n, num_q_heads, head_dim),
+                                                         np.float32))
+        self.step_k = to_bf16_bits(st[2].standard_normal((steps, n) + kv, np.float32))
+        self.step_v = to_bf16_bits(st[2].standard_normal((steps, n) + kv, np.float32))
+        sc = st[3].uniform(3.5, 4.5, size=(2, num_blocks, num_kv_heads)).astype(np.float32)
+        self.k_scale, self.v_scale = sc[0] / np.float32(127), sc[1] / np.float32(127)
+
+    @property
+    def num_seqs(self) -> int:
+        return self.num_parents * self.beams
+
+    def seq_lens_at(self, step: int) -> np.ndarray:
+        """Lengths of every sequence in decode step ``step`` (counting the
+        token that step appends)."""
+        return np.repeat(self.parent_lens, self.beams).astype(np.int32) + np.int32(step + 1)
+
+    def poisoned_pool(self) -> np.ndarray:
+        shape = (self.num_blocks, self.block_size, self.num_kv_heads, self.head_dim)
+        if self.kv_dtype == "int8":
+            return np.full(shape, INT8_POISON, np.int8)
+        return np.full(shape, BF16_NAN, np.uint16)
+
+    def dense_tokens(self, seq: int, step: int):
+        """bf16 bits of K, V [L, Hkv, d] of sequence ``seq`` after decode step
+        ``step`` in logical order: the parent's prompt, then the beam's own
+        step tokens (the un-paged, unshared view)."""
+        p = seq // self.beams
+        k = np.concatenate([self.parent_k[p], self.step_k[:step + 1, seq]])
+        v = np.concatenate([self.parent_v[p], self.step_v[:step + 1, seq]])
+        return k, v
+
+
+def beam_search_8b(seed: int = SEED_BASE + 98, steps: int = 64) -> BeamWorkload:
+    """Beam search over the Llama-3.1-8B-like decode layer: 16 prompts of
+    U{512..4096} tokens, 4 beams each (B 64, 32/8 heads, d 128, 16-token
+    blocks); the pool holds ceil(1.25 x) the blocks the prompts and every
+    beam's own decoded tokens (plus one copied block per beam) need."""
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed).spawn(5)[4]))
+    parents, beams, bs = 16, 4, 16
+    lens = g.integers(512, 4096, size=parents, endpoint=True)
+    need = sum((int(L) + bs - 1) // bs for L in lens) + parents * beams * ((steps + bs - 1) // bs + 1)
+    mb = (int(lens.max()) + steps + bs - 1) // bs
+    return BeamWorkload(num_parents=parents, beams=beams, parent_lens=lens, steps=steps,
+                        num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=bs,
+                        num_blocks=int(math.ceil(1.25 * need)), max_blocks_per_seq=mb, seed=seed)
