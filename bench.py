@@ -52,7 +52,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
 def algorithmic_bytes(wl) -> dict:
     """Bytes the step must move at minimum: K/V of every attended token (a
     shared prefix counted once: it is read once from HBM and then hits L2),
-    int8 scales, the block-table entries in use, q and out, and the append's
+    8-bit scales, the block-table entries in use, q and out, and the append's
     reads and writes."""
     s = wl.spec
     elem = wl.kv_elem_bytes
@@ -60,7 +60,7 @@ def algorithmic_bytes(wl) -> dict:
     L = wl.seq_lens.astype(np.int64)
     blocks = int(((L + bs - 1) // bs).sum())
     kv_unique = wl.kv_bytes_unique()
-    scales = blocks * 2 * hkv * 4 if s.kv_dtype == "int8" else 0
+    scales = blocks * 2 * hkv * 4 if s.kv_dtype != "bf16" else 0
     qo = 2 * B * hq * d * 2
     table = blocks * 4 + B * 4
     append = B * hkv * d * 2 * 2 + B * hkv * d * elem * 2 + B * 8 * 2
@@ -336,6 +336,40 @@ def measure_cow(pkv, dev, stream, peak):
     return {"copy_blocks": copy_row, "beam_search": beam_row}
 
 
+def measure_config_step(config, pkv, dev, stream, peak, replays=40):
+    """One workload's fused decode step (pagedkv_decode_step), timed like the
+    headline: GRAPH_STEPS steps captured in one CUDA graph, replayed."""
+    import torch
+    from gpu_helpers import GpuStep
+    wl = workloads.make(config)
+    g = GpuStep(wl, dev=dev)
+    for _ in range(5):
+        g.fused_step()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(GRAPH_STEPS):
+            g.fused_step()
+    for _ in range(3):
+        graph.replay()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * replays)]
+    torch.cuda.synchronize(dev)
+    for i in range(replays):
+        ev[2 * i].record(stream)
+        graph.replay()
+        ev[2 * i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    st, flags = pkv.get_status()
+    assert st == 0 and flags == 0, f"device status 0x{flags:x}"
+    us = statistics.fmean(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(replays)) * 1e3 / GRAPH_STEPS
+    nbytes = algorithmic_bytes(wl)
+    achieved = nbytes["step"] / us / 1e3
+    return {"workload": wl.spec.name, "us_per_step": round(us, 2),
+            "kv_read_gbs": round(nbytes["kv_logical"] / us / 1e3, 1),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4),
+                         "algorithmic_bytes_per_step": nbytes["step"]}}
+
+
 def gpu_arm(args, rank, world, local_rank, dist):
     import torch
 
@@ -459,7 +493,7 @@ def gpu_arm(args, rank, world, local_rank, dist):
         "us_per_step": round(ms_step * 1e3, 2),
         "pct_of_hbm_peak": round(100 * value / world / peak, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if s.kv_dtype == "bf16" else "int8 KV, bf16 q/out, fp32 accumulate",
+        "dtype": "bf16" if s.kv_dtype == "bf16" else f"{s.kv_dtype} KV, bf16 q/out, fp32 accumulate",
         "data": "synthetic",
         "config": {"workload": s.name, "batch": s.batch, "num_q_heads": s.num_q_heads,
                    "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim,
@@ -488,7 +522,8 @@ def gpu_arm(args, rank, world, local_rank, dist):
         "clocks": sampler.summary(),
     }
     if not args.no_rows:
-        line["rows"] = {"cow": measure_cow(pkv, dev, stream, peak)}
+        line["rows"] = {"cow": measure_cow(pkv, dev, stream, peak),
+                        "fp8_kv": measure_config_step(6, pkv, dev, stream, peak)}
     return line, wl
 
 

@@ -12,11 +12,12 @@
  * Conventions shared by every call
  * --------------------------------
  *  - Pool tensors (K and V, separate): [num_blocks, block_size, num_kv_heads,
- *    head_dim], row-major, elements bf16 or int8 (“LLM 推理引擎深度解析”,
+ *    head_dim], row-major, elements bf16, int8 or FP8 E4M3 (“LLM 推理引擎深度解析”,
  *    §2.1: key_cache / value_cache of that shape).  The base of each pool must
  *    be 16-byte aligned.
- *  - int8 pools carry fp32 scales [num_blocks, num_kv_heads] for K and for V;
- *    the stored value of element x is code * scale.
+ *  - 8-bit pools (int8, E4M3; see kv_dtype) carry fp32 scales [num_blocks,
+ *    num_kv_heads] for K and for V; the stored value of element x is
+ *    code * scale.
  *  - Token slot: slot = physical_block * block_size + row.
  *  - GQA: query head h reads KV head h / (num_q_heads / num_kv_heads).
  *  - seq_lens[b] counts every cached token of sequence b INCLUDING the one
@@ -61,7 +62,20 @@ typedef enum {
     KV_ERR_NOT_IMPLEMENTED = 5
 } kv_status;
 
-typedef enum { KV_DTYPE_BF16 = 0, KV_DTYPE_INT8 = 1 } kv_dtype;
+/* Element type of the K/V pools.  The two 8-bit types store codes under an
+ * fp32 scale per (block, KV head), k_scale / v_scale [num_blocks,
+ * num_kv_heads]: the value of a code c is c * scale.
+ *   KV_DTYPE_INT8       c = clamp(round_half_even(fp32(x) / scale), -127, 127)
+ *                       (“The engineering behind LLM inference” notes, §3.2:
+ *                       INT8 KV halves the cache)
+ *   KV_DTYPE_FP8_E4M3   c = the E4M3 value nearest fp32(x) / scale, ties to
+ *                       the even code, magnitudes above 448 saturating to
+ *                       448 (“让 Agent 跑得快”, §四 FP8 量化: a 1-byte FP8 KV
+ *                       cache; “LLM 推理优化技术全景”, Flash Attention v3:
+ *                       E4M3 with block-wise scales).  E4M3: sign, 4
+ *                       exponent bits (bias 7), 3 mantissa bits, no
+ *                       infinities, 0x7F / 0xFF NaN. */
+typedef enum { KV_DTYPE_BF16 = 0, KV_DTYPE_INT8 = 1, KV_DTYPE_FP8_E4M3 = 2 } kv_dtype;
 
 /* Bits of the device status word (pagedkv_get_status). */
 #define PAGEDKV_FLAG_BAD_SLOT 0x1u     /* slot >= num_blocks * block_size     */
@@ -161,8 +175,8 @@ size_t pagedkv_pool_tensor_bytes(int num_blocks, int block_size,
  * sequence writes into it).
  *   k_cache, v_cache  device [num_blocks, block_size, num_kv_heads, head_dim],
  *                     16-byte aligned
- *   k_scale, v_scale  device fp32 [num_blocks, num_kv_heads] for INT8, NULL
- *                     for BF16
+ *   k_scale, v_scale  device fp32 [num_blocks, num_kv_heads] for 8-bit pools,
+ *                     NULL for BF16
  *   block_pairs       device int32 [num_pairs][2] (src, dst)
  * A destination must not be the source or destination of another pair of
  * the same call (pairs from kv_pool_prepare_append never are).  A pair with
@@ -213,14 +227,15 @@ kv_status pagedkv_token_slot_mapping(const int32_t *block_tables,
  * decode appends the new token's K/V; §五 “共享前缀”: only the current token
  * writes).
  *   k, v          device bf16 [num_tokens, num_kv_heads, head_dim]
- *   k_cache, v_cache  device pool tensors (bf16 or int8, see above)
- *   k_scale, v_scale  device fp32 [num_blocks, num_kv_heads] for int8 pools;
+ *   k_cache, v_cache  device pool tensors (bf16, int8 or E4M3, see above)
+ *   k_scale, v_scale  device fp32 [num_blocks, num_kv_heads] for 8-bit pools;
  *                     must be NULL for bf16 pools
  *   slot_mapping  device int64 [num_tokens]; slot < 0 skips the token
  * bf16 pools receive the bits unchanged.  int8 pools receive
  * clamp(round_half_even(fp32(x) / scale), -127, 127) computed with an IEEE
  * fp32 divide (scale 0 is read as 1, NaN gives 0), with the scale of the
- * slot's block and head.  A slot >= num_blocks * block_size is skipped and
+ * slot's block and head.  E4M3 pools receive the E4M3 code of the same fp32
+ * quotient (nearest, ties to even, saturating at 448; NaN gives 0x7F).  A slot >= num_blocks * block_size is skipped and
  * sets PAGEDKV_FLAG_BAD_SLOT. */
 kv_status reshape_and_cache(const void *k, const void *v, void *k_cache,
                             void *v_cache, const float *k_scale,
@@ -311,7 +326,7 @@ kv_status pagedkv_decode_step(void *out, const void *q, const void *k,
  *   k, v               as pagedkv_decode_step, or both NULL to attend
  *                      without appending
  *   workspace          at least pagedkv_prefix_workspace_bytes(...) bytes
- * bf16 pools only (int8 returns KV_ERR_NOT_IMPLEMENTED). */
+ * bf16 pools only (8-bit pools return KV_ERR_NOT_IMPLEMENTED). */
 kv_status pagedkv_decode_step_prefix(void *out, const void *q, const void *k,
                                      const void *v, void *k_cache,
                                      void *v_cache, const float *k_scale,

@@ -17,6 +17,7 @@ Contents, each citing the passage it follows (page titles as printed):
   Copy-on-Write: reference counts, copy before writing a shared block);
 * ``copy_blocks`` -- the block copy of copy-on-write (plain numpy);
 * ``token_slots``, ``append_bf16``, ``append_int8``, ``quantize_int8``,
+  ``append_fp8``, ``quantize_fp8``, ``fp8_value``,
   ``paged_attention`` (three-pass or online), ``attention_partials``,
   ``lse_merge`` -- thin ctypes wrappers over ``pagedkv_oracle.c`` (plain C,
   fp64), whose header cites the passages it follows.
@@ -78,6 +79,10 @@ def _bind(lib):
     lib.oracle_append_bf16.argtypes = [P, P, P, P, P, I, I, I, I, I]
     lib.oracle_append_int8.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I]
     lib.oracle_quantize_int8.argtypes = [ctypes.c_float, ctypes.c_float]
+    lib.oracle_append_fp8.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I]
+    lib.oracle_quantize_fp8.argtypes = [ctypes.c_float, ctypes.c_float]
+    lib.oracle_fp8_value.argtypes = [I]
+    lib.oracle_fp8_value.restype = D
     lib.oracle_paged_attention.argtypes = [P, P, P, P, P, P, I, P, I, P, I, I,
                                            I, I, I, I, D, P, I, I, I]
     lib.oracle_attention_partials.argtypes = [P, P, P, P, P, P, P, I, P, I, P,
@@ -299,6 +304,38 @@ def quantize_int8(x: float, s: float) -> int:
     return _load().oracle_quantize_int8(float(x), float(s))
 
 
+def append_fp8(k, v, k_cache, v_cache, k_scale, v_scale, slots):
+    """Store E4M3 codes (uint8 pools) of bf16 k, v under the slot's block
+    scales."""
+    lib = _load()
+    k, v, s = _c(k, np.uint16), _c(v, np.uint16), _c(slots, np.int64)
+    ks, vs = _c(k_scale, np.float32), _c(v_scale, np.float32)
+    nb, bs, hkv, d = k_cache.shape
+    assert k_cache.dtype == np.uint8 and v_cache.dtype == np.uint8
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    return lib.oracle_append_fp8(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
+                                 _ptr(ks), _ptr(vs), _ptr(s), k.shape[0], nb,
+                                 bs, hkv, d)
+
+
+def quantize_fp8(x: float, s: float) -> int:
+    """E4M3 code of the fp32 quotient x / s: nearest finite value, ties to
+    the even code, |.| > 448 -> 448, NaN -> 0x7F, s = 0 -> 1."""
+    return _load().oracle_quantize_fp8(float(x), float(s))
+
+
+def fp8_value(code: int) -> float:
+    """Value of an E4M3 code (NaN for 0x7F / 0xFF)."""
+    return _load().oracle_fp8_value(int(code))
+
+
+def _kv_kind(k_cache):
+    """0 bf16 bits (uint16), 1 int8 codes, 2 E4M3 codes (uint8)."""
+    kinds = {np.dtype(np.uint16): 0, np.dtype(np.int8): 1, np.dtype(np.uint8): 2}
+    assert k_cache.dtype in kinds, k_cache.dtype
+    return kinds[k_cache.dtype]
+
+
 # --------------------------------------------------------------------------
 # Attention
 # --------------------------------------------------------------------------
@@ -308,8 +345,9 @@ def paged_attention(q, k_cache, v_cache, block_tables, seq_lens, scale, *,
                     mode="three_pass", threads=1):
     """fp64 decode attention through the block table.
 
-    q: bf16 bits [B, Hq, d]; k_cache / v_cache: bf16 bits (uint16) or int8
-    [NB, bs, Hkv, d]; block_tables int32 [B, MB]; seq_lens int32 [B].
+    q: bf16 bits [B, Hq, d]; k_cache / v_cache: bf16 bits (uint16), int8 or
+    E4M3 codes (uint8) [NB, bs, Hkv, d]; block_tables int32 [B, MB]; seq_lens
+    int32 [B].
     rows: optional int array [n, 2] of (b, h) to compute; default all, in
     b-major order.  Returns (out fp64 [n, d] or [B, Hq, d], status).
     """
@@ -318,11 +356,9 @@ def paged_attention(q, k_cache, v_cache, block_tables, seq_lens, scale, *,
     B, Hq, d = q.shape
     nb, bs, hkv, d2 = k_cache.shape
     assert d2 == d and v_cache.shape == k_cache.shape
-    kv_int8 = k_cache.dtype == np.int8
-    if kv_int8:
+    kind = _kv_kind(k_cache)
+    if kind:
         k_scale, v_scale = _c(k_scale, np.float32), _c(v_scale, np.float32)
-    else:
-        assert k_cache.dtype == np.uint16
     kc, vc = np.ascontiguousarray(k_cache), np.ascontiguousarray(v_cache)
     bt, sl = _c(block_tables, np.int32), _c(seq_lens, np.int32)
     r = None if rows is None else _c(rows, np.int32).reshape(-1, 2)
@@ -331,8 +367,8 @@ def paged_attention(q, k_cache, v_cache, block_tables, seq_lens, scale, *,
     m = {"three_pass": 0, "online": 1}[mode]
     rc = lib.oracle_paged_attention(
         _ptr(out), _ptr(q), _ptr(kc), _ptr(vc),
-        _ptr(k_scale) if kv_int8 else None, _ptr(v_scale) if kv_int8 else None,
-        int(kv_int8), _ptr(bt), bt.shape[1], _ptr(sl), B, Hq, hkv, d, nb, bs,
+        _ptr(k_scale) if kind else None, _ptr(v_scale) if kind else None,
+        kind, _ptr(bt), bt.shape[1], _ptr(sl), B, Hq, hkv, d, nb, bs,
         float(scale), _ptr(r), n, m, int(threads))
     if r is None:
         out = out.reshape(B, Hq, d)
@@ -347,8 +383,8 @@ def attention_partials(q, k_cache, v_cache, block_tables, seq_lens, scale, b, h,
     q = _c(q, np.uint16)
     B, Hq, d = q.shape
     nb, bs, hkv, _ = k_cache.shape
-    kv_int8 = k_cache.dtype == np.int8
-    if kv_int8:
+    kind = _kv_kind(k_cache)
+    if kind:
         k_scale, v_scale = _c(k_scale, np.float32), _c(v_scale, np.float32)
     kc, vc = np.ascontiguousarray(k_cache), np.ascontiguousarray(v_cache)
     bt, sl = _c(block_tables, np.int32), _c(seq_lens, np.int32)
@@ -357,8 +393,8 @@ def attention_partials(q, k_cache, v_cache, block_tables, seq_lens, scale, b, h,
     acc = np.zeros((max(npart, 1), d), np.float64)
     rc = lib.oracle_attention_partials(
         _ptr(ml), _ptr(acc), _ptr(q), _ptr(kc), _ptr(vc),
-        _ptr(k_scale) if kv_int8 else None, _ptr(v_scale) if kv_int8 else None,
-        int(kv_int8), _ptr(bt), bt.shape[1], _ptr(sl), B, Hq, hkv, d, nb, bs,
+        _ptr(k_scale) if kind else None, _ptr(v_scale) if kind else None,
+        kind, _ptr(bt), bt.shape[1], _ptr(sl), B, Hq, hkv, d, nb, bs,
         float(scale), int(b), int(h), int(part))
     if rc < 0:
         raise ValueError(f"oracle_attention_partials failed ({-rc})")

@@ -15,7 +15,7 @@
  *        table maps each request's logical blocks to physical blocks of a
  *        shared pool; §二: blocks hold 16 tokens by default)
  *   - appending the new token's K/V into its slot (bf16 bit copy, or an int8
- *       code under a per-(block, KV head) scale)
+ *       or FP8 E4M3 code under a per-(block, KV head) scale)
  *       (same page, §一 “KV Cache”: decode computes the new token's Q, attends
  *        over cached K/V and appends the new K/V; §五 “共享前缀”: only the
  *        current decode token writes; pool layout [num_blocks, block_size,
@@ -157,13 +157,63 @@ static int8_t quantize_int8(float x, float s)
 
 int oracle_quantize_int8(float x, float s) { return (int)quantize_int8(x, s); }
 
-/* As oracle_append_bf16, but stores int8 codes under k_scale / v_scale, which
- * are fp32 [num_blocks, num_kv_heads]: the scale of the slot's block. */
-int oracle_append_int8(const uint16_t *k, const uint16_t *v, int8_t *k_cache,
-                       int8_t *v_cache, const float *k_scale,
-                       const float *v_scale, const int64_t *slots,
-                       int num_tokens, int num_blocks, int block_size,
-                       int num_kv_heads, int head_dim)
+/* FP8 E4M3 (the 8-bit float named beside E5M2 in “LLM 推理优化技术全景”,
+ * Flash Attention v3, and used for the KV cache in “让 Agent 跑得快”, §四
+ * “FP8 量化”): bit 7 sign, bits 6..3 exponent field E (bias 7), bits 2..0
+ * mantissa M.  E = 0: subnormal, M/8 * 2^-6.  Otherwise (1 + M/8) * 2^(E-7).
+ * The one pattern with E = 15 and M = 7 is NaN; there is no infinity, so the
+ * largest finite value is (1 + 6/8) * 2^8 = 448. */
+double oracle_fp8_value(int code)
+{
+    int c = code & 0xFF;
+    int e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7)
+        return NAN;
+    double mag = e == 0 ? ldexp(m / 8.0, -6) : ldexp(1.0 + m / 8.0, e - 7);
+    return (c & 0x80) ? -mag : mag;
+}
+
+/* The E4M3 code of value x under scale s: the fp32 quotient x / s (as for
+ * int8; s == 0 -> 1), rounded to the nearest finite E4M3 value with ties to
+ * the even code (even mantissa), magnitudes above 448 saturating to 448 (the
+ * reading this library takes, as int8 clamps to 127), NaN -> 0x7F.  The sign
+ * is kept, so negative values that round to zero give 0x80.  Found by
+ * comparing the quotient with every finite non-negative code. */
+static uint8_t quantize_fp8(float x, float s)
+{
+    if (s == 0.0f)
+        s = 1.0f;
+    float r = x / s;
+    if (r != r)
+        return 0x7F;
+    uint8_t sign = signbit(r) ? 0x80 : 0x00;
+    double a = fabs((double)r);
+    if (a >= 448.0)
+        return sign | 0x7E;
+    int best = 0;
+    double best_d = a;
+    for (int c = 1; c <= 0x7E; ++c) {
+        double d = fabs(oracle_fp8_value(c) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return sign | (uint8_t)best;
+}
+
+int oracle_quantize_fp8(float x, float s) { return (int)quantize_fp8(x, s); }
+
+/* int8 codes as bytes, for the shared 8-bit append below. */
+static uint8_t quantize_int8_byte(float x, float s) { return (uint8_t)quantize_int8(x, s); }
+
+/* As oracle_append_bf16, but stores 8-bit codes under k_scale / v_scale,
+ * which are fp32 [num_blocks, num_kv_heads]: the scale of the slot's block. */
+static int append_codes(const uint16_t *k, const uint16_t *v, uint8_t *k_cache,
+                        uint8_t *v_cache, const float *k_scale, const float *v_scale,
+                        const int64_t *slots, int num_tokens, int num_blocks,
+                        int block_size, int num_kv_heads, int head_dim,
+                        uint8_t (*code)(float, float))
 {
     if (!k || !v || !k_cache || !v_cache || !k_scale || !v_scale || !slots)
         return OR_INVALID;
@@ -184,12 +234,33 @@ int oracle_append_int8(const uint16_t *k, const uint16_t *v, int8_t *k_cache,
             for (int e = 0; e < head_dim; ++e) {
                 int64_t src = ((int64_t)i * num_kv_heads + h) * head_dim + e;
                 int64_t dst = pool_index(slot, block_size, num_kv_heads, head_dim, h, e);
-                k_cache[dst] = quantize_int8(bf16_to_float(k[src]), ks);
-                v_cache[dst] = quantize_int8(bf16_to_float(v[src]), vs);
+                k_cache[dst] = code(bf16_to_float(k[src]), ks);
+                v_cache[dst] = code(bf16_to_float(v[src]), vs);
             }
         }
     }
     return rc;
+}
+
+int oracle_append_int8(const uint16_t *k, const uint16_t *v, int8_t *k_cache,
+                       int8_t *v_cache, const float *k_scale,
+                       const float *v_scale, const int64_t *slots,
+                       int num_tokens, int num_blocks, int block_size,
+                       int num_kv_heads, int head_dim)
+{
+    return append_codes(k, v, (uint8_t *)k_cache, (uint8_t *)v_cache, k_scale, v_scale, slots,
+                        num_tokens, num_blocks, block_size, num_kv_heads, head_dim,
+                        quantize_int8_byte);
+}
+
+int oracle_append_fp8(const uint16_t *k, const uint16_t *v, uint8_t *k_cache,
+                      uint8_t *v_cache, const float *k_scale,
+                      const float *v_scale, const int64_t *slots,
+                      int num_tokens, int num_blocks, int block_size,
+                      int num_kv_heads, int head_dim)
+{
+    return append_codes(k, v, k_cache, v_cache, k_scale, v_scale, slots, num_tokens,
+                        num_blocks, block_size, num_kv_heads, head_dim, quantize_fp8);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -198,11 +269,11 @@ int oracle_append_int8(const uint16_t *k, const uint16_t *v, int8_t *k_cache,
 
 typedef struct {
     const uint16_t *q;       /* bf16 [batch, num_q_heads, head_dim] */
-    const void *k_cache;     /* bf16 bits or int8 [num_blocks, bs, Hkv, d] */
+    const void *k_cache;     /* bf16 bits, int8 or E4M3 [num_blocks, bs, Hkv, d] */
     const void *v_cache;
-    const float *k_scale;    /* [num_blocks, Hkv] when kv_int8 */
+    const float *k_scale;    /* [num_blocks, Hkv] for 8-bit pools */
     const float *v_scale;
-    int kv_int8;
+    int kv_kind;             /* 0 bf16, 1 int8, 2 E4M3 */
     const int32_t *block_tables; /* [batch, max_blocks] */
     int max_blocks;
     const int32_t *seq_lens;     /* [batch], including the appended token */
@@ -212,16 +283,21 @@ typedef struct {
 
 /* Value of element e of the token at logical position t of sequence b, KV
  * head hk, from the K (which = 0) or V (which = 1) pool, widened to fp64.
- * int8 codes are multiplied by their block's scale in fp64. */
+ * int8 and E4M3 codes are multiplied by their block's scale in fp64. */
 static double pool_value(const attn_problem *P, int which, int32_t block,
                          int row, int hk, int e)
 {
     int64_t idx = (((int64_t)block * P->block_size + row) * P->num_kv_heads + hk) *
                       P->head_dim + e;
-    if (P->kv_int8) {
-        const int8_t *c = (const int8_t *)(which ? P->v_cache : P->k_cache);
+    if (P->kv_kind != 0) {
         const float *s = which ? P->v_scale : P->k_scale;
-        return (double)c[idx] * (double)s[(int64_t)block * P->num_kv_heads + hk];
+        double sc = (double)s[(int64_t)block * P->num_kv_heads + hk];
+        if (P->kv_kind == 2) {
+            const uint8_t *c = (const uint8_t *)(which ? P->v_cache : P->k_cache);
+            return oracle_fp8_value(c[idx]) * sc;
+        }
+        const int8_t *c = (const int8_t *)(which ? P->v_cache : P->k_cache);
+        return (double)c[idx] * sc;
     }
     const uint16_t *c = (const uint16_t *)(which ? P->v_cache : P->k_cache);
     return (double)bf16_to_float(c[idx]);
@@ -441,7 +517,7 @@ static int valid_problem(const attn_problem *P)
 {
     if (!P->q || !P->k_cache || !P->v_cache || !P->block_tables || !P->seq_lens)
         return 0;
-    if (P->kv_int8 && (!P->k_scale || !P->v_scale))
+    if (P->kv_kind != 0 && (!P->k_scale || !P->v_scale))
         return 0;
     if (P->batch < 0 || P->num_q_heads <= 0 || P->num_kv_heads <= 0 ||
         P->num_q_heads % P->num_kv_heads || P->head_dim <= 0 ||
@@ -481,14 +557,14 @@ static int run_rows(attn_problem *P, const int32_t *rows, int n_rows, int mode,
  * mode 0 = three-pass softmax (the oracle), 1 = online recurrence. */
 int oracle_paged_attention(double *out, const uint16_t *q, const void *k_cache,
                            const void *v_cache, const float *k_scale,
-                           const float *v_scale, int kv_int8,
+                           const float *v_scale, int kv_kind,
                            const int32_t *block_tables, int max_blocks_per_seq,
                            const int32_t *seq_lens, int batch, int num_q_heads,
                            int num_kv_heads, int head_dim, int num_blocks,
                            int block_size, double scale, const int32_t *rows,
                            int n_rows, int mode, int num_threads)
 {
-    attn_problem P = {q, k_cache, v_cache, k_scale, v_scale, kv_int8,
+    attn_problem P = {q, k_cache, v_cache, k_scale, v_scale, kv_kind,
                       block_tables, max_blocks_per_seq, seq_lens, batch,
                       num_q_heads, num_kv_heads, head_dim, num_blocks,
                       block_size, scale};
@@ -501,13 +577,13 @@ int oracle_paged_attention(double *out, const uint16_t *q, const void *k_cache,
 int oracle_attention_partials(double *ml, double *acc, const uint16_t *q,
                               const void *k_cache, const void *v_cache,
                               const float *k_scale, const float *v_scale,
-                              int kv_int8, const int32_t *block_tables,
+                              int kv_kind, const int32_t *block_tables,
                               int max_blocks_per_seq, const int32_t *seq_lens,
                               int batch, int num_q_heads, int num_kv_heads,
                               int head_dim, int num_blocks, int block_size,
                               double scale, int b, int h, int part)
 {
-    attn_problem P = {q, k_cache, v_cache, k_scale, v_scale, kv_int8,
+    attn_problem P = {q, k_cache, v_cache, k_scale, v_scale, kv_kind,
                       block_tables, max_blocks_per_seq, seq_lens, batch,
                       num_q_heads, num_kv_heads, head_dim, num_blocks,
                       block_size, scale};

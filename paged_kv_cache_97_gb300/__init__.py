@@ -22,7 +22,7 @@ LIB_PATH = _build.LIB_PATH
 
 KV_OK, KV_ERR_INVALID_ARG, KV_ERR_OUT_OF_BLOCKS, KV_ERR_CUDA, KV_ERR_DEVICE_INDEX, \
     KV_ERR_NOT_IMPLEMENTED = range(6)
-DTYPE_BF16, DTYPE_INT8 = 0, 1
+DTYPE_BF16, DTYPE_INT8, DTYPE_FP8_E4M3 = 0, 1, 2
 FLAG_BAD_SLOT, FLAG_BAD_BLOCK, FLAG_BAD_SEQ_LEN, FLAG_WAIT_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 
 # Every symbol include/pagedkv.h declares, with its ctypes signature.
@@ -124,7 +124,9 @@ def _pool_dtype(k_cache):
         return DTYPE_BF16
     if k_cache.dtype == torch.int8:
         return DTYPE_INT8
-    raise TypeError("pools must be torch.bfloat16 or torch.int8")
+    if k_cache.dtype == torch.float8_e4m3fn:
+        return DTYPE_FP8_E4M3
+    raise TypeError("pools must be torch.bfloat16, torch.int8 or torch.float8_e4m3fn")
 
 
 # --------------------------------------------------------------------------

@@ -14,6 +14,7 @@
 #include <vector>
 
 #include "pagedkv_common.cuh"
+#include "pagedkv_device.cuh"
 
 namespace pagedkv {
 
@@ -112,30 +113,25 @@ __global__ void token_slots_kernel(const int32_t* __restrict__ block_tables, int
 // Append: one thread moves 8 elements (16 bytes of bf16 input).
 // ---------------------------------------------------------------------------
 
-__device__ __forceinline__ int8_t quantize(float x, float s) {
-  // clamp(round_half_even(x / s), -127, 127) with an IEEE fp32 divide.
-  if (s == 0.0f) s = 1.0f;
-  int c = __float2int_rn(__fdiv_rn(x, s));  // NaN -> 0, +-inf saturate
-  c = c > 127 ? 127 : (c < -127 ? -127 : c);
-  return (int8_t)c;
-}
-
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// Eight bf16 values as eight 8-bit codes (int8, or E4M3 when kFp8).
+template <bool kFp8>
 __device__ __forceinline__ uint2 quantize8(uint4 x, float s) {
   uint32_t w[4] = {x.x, x.y, x.z, x.w};
   uint32_t o[2] = {0u, 0u};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    uint32_t lo = (uint8_t)quantize(bf16_lo(w[i]), s);
-    uint32_t hi = (uint8_t)quantize(bf16_hi(w[i]), s);
+    uint32_t lo = dev::code8<kFp8>(bf16_lo(w[i]), s);
+    uint32_t hi = dev::code8<kFp8>(bf16_hi(w[i]), s);
     o[i / 2] |= (lo | (hi << 8)) << (16 * (i % 2));
   }
   return make_uint2(o[0], o[1]);
 }
 
-template <bool kInt8>
+// kKind: the pool dtype (KV_DTYPE_BF16, KV_DTYPE_INT8, KV_DTYPE_FP8_E4M3).
+template <int kKind>
 __global__ void append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
                               void* __restrict__ k_cache, void* __restrict__ v_cache,
                               const float* __restrict__ k_scale,
@@ -159,10 +155,11 @@ __global__ void append_kernel(const uint4* __restrict__ k, const uint4* __restri
   // Destination chunk: element ((slot * Hkv + h) * D + e0) of the pool.
   int64_t dst = (slot * num_kv_heads + h) * chunks_per_head + (c % chunks_per_head);
   uint4 kx = k[idx], vx = v[idx];
-  if (kInt8) {
+  if (kKind != KV_DTYPE_BF16) {
     int64_t sidx = (slot / bs) * num_kv_heads + h;
-    reinterpret_cast<uint2*>(k_cache)[dst] = quantize8(kx, k_scale[sidx]);
-    reinterpret_cast<uint2*>(v_cache)[dst] = quantize8(vx, v_scale[sidx]);
+    constexpr bool kFp8 = kKind == KV_DTYPE_FP8_E4M3;
+    reinterpret_cast<uint2*>(k_cache)[dst] = quantize8<kFp8>(kx, k_scale[sidx]);
+    reinterpret_cast<uint2*>(v_cache)[dst] = quantize8<kFp8>(vx, v_scale[sidx]);
   } else {
     reinterpret_cast<uint4*>(k_cache)[dst] = kx;
     reinterpret_cast<uint4*>(v_cache)[dst] = vx;
@@ -356,10 +353,10 @@ kv_status reshape_and_cache(const void* k, const void* v, void* k_cache, void* v
     return fail(KV_ERR_INVALID_ARG, "reshape_and_cache: NULL pointer");
   if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
     return fail(KV_ERR_INVALID_ARG, "reshape_and_cache: k, v and the pools must be 16-byte aligned");
-  const bool int8 = dtype == KV_DTYPE_INT8;
-  if (int8 != (k_scale != nullptr) || int8 != (v_scale != nullptr))
+  const bool q8 = dtype != KV_DTYPE_BF16;
+  if (q8 != (k_scale != nullptr) || q8 != (v_scale != nullptr))
     return fail(KV_ERR_INVALID_ARG,
-                "reshape_and_cache: int8 pools need k_scale and v_scale; bf16 pools take NULL");
+                "reshape_and_cache: 8-bit pools need k_scale and v_scale; bf16 pools take NULL");
   DeviceInfo di;
   kv_status st = device_info(&di);
   if (st != KV_OK) return st;
@@ -368,12 +365,16 @@ kv_status reshape_and_cache(const void* k, const void* v, void* k_cache, void* v
   const int64_t grid = (threads + block - 1) / block;
   if (grid > 0x7fffffffLL) return fail(KV_ERR_INVALID_ARG, "reshape_and_cache: too many tokens");
   cudaStream_t s = (cudaStream_t)stream;
-  if (int8)
-    append_kernel<true><<<(unsigned)grid, block, 0, s>>>(
+  if (dtype == KV_DTYPE_INT8)
+    append_kernel<KV_DTYPE_INT8><<<(unsigned)grid, block, 0, s>>>(
+        (const uint4*)k, (const uint4*)v, k_cache, v_cache, k_scale, v_scale, slot_mapping,
+        num_tokens, num_blocks, block_size, num_kv_heads, head_dim, di.flags);
+  else if (dtype == KV_DTYPE_FP8_E4M3)
+    append_kernel<KV_DTYPE_FP8_E4M3><<<(unsigned)grid, block, 0, s>>>(
         (const uint4*)k, (const uint4*)v, k_cache, v_cache, k_scale, v_scale, slot_mapping,
         num_tokens, num_blocks, block_size, num_kv_heads, head_dim, di.flags);
   else
-    append_kernel<false><<<(unsigned)grid, block, 0, s>>>(
+    append_kernel<KV_DTYPE_BF16><<<(unsigned)grid, block, 0, s>>>(
         (const uint4*)k, (const uint4*)v, k_cache, v_cache, nullptr, nullptr, slot_mapping,
         num_tokens, num_blocks, block_size, num_kv_heads, head_dim, di.flags);
   return cuda_check(cudaGetLastError(), "append_kernel launch");
@@ -437,17 +438,17 @@ static kv_status decode_common(void* out, const void* q, const void* new_k, cons
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
       !aligned16(new_k) || !aligned16(new_v))
     return fail(KV_ERR_INVALID_ARG, "%s: out, q, k, v and the pools must be 16-byte aligned", who);
-  const bool int8 = dtype == KV_DTYPE_INT8;
-  if (int8 != (k_scale != nullptr) || int8 != (v_scale != nullptr))
+  const bool q8 = dtype != KV_DTYPE_BF16;
+  if (q8 != (k_scale != nullptr) || q8 != (v_scale != nullptr))
     return fail(KV_ERR_INVALID_ARG,
-                "%s: int8 pools need k_scale and v_scale; bf16 pools take NULL", who);
+                "%s: 8-bit pools need k_scale and v_scale; bf16 pools take NULL", who);
   const int skip = num_prefix_blocks * block_size;
   if (num_prefix_blocks < 0 || (num_prefix_blocks > 0 && !prefix_blocks) ||
       num_prefix_blocks > max_blocks_per_seq || (num_prefix_blocks > 0 && max_seq_len <= skip))
     return fail(KV_ERR_INVALID_ARG,
                 "%s: the shared prefix needs 1..max_blocks_per_seq block ids and sequences "
                 "longer than it", who);
-  if (num_prefix_blocks > 0 && int8)
+  if (num_prefix_blocks > 0 && q8)
     return fail(KV_ERR_NOT_IMPLEMENTED, "%s: the shared-prefix path supports bf16 pools only", who);
   DeviceInfo di;
   kv_status st = device_info(&di);

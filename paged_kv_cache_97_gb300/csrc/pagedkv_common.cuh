@@ -25,7 +25,9 @@ kv_status device_info(DeviceInfo* out);
 
 // Bytes of one stored K/V element.
 inline int dtype_size(kv_dtype t) { return t == KV_DTYPE_BF16 ? 2 : 1; }
-inline bool valid_dtype(kv_dtype t) { return t == KV_DTYPE_BF16 || t == KV_DTYPE_INT8; }
+inline bool valid_dtype(kv_dtype t) {
+  return t == KV_DTYPE_BF16 || t == KV_DTYPE_INT8 || t == KV_DTYPE_FP8_E4M3;
+}
 // 16-byte alignment (NULL passes).
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

@@ -60,16 +60,23 @@ constexpr int kSpec = (kMaxBlocks + kThreads - 1) / kThreads;  // table entries 
 // The kernel
 // ---------------------------------------------------------------------------
 
-template <int D, int BS, bool kInt8>
-__global__ void __launch_bounds__(kThreads, 1)
+// kQ8: the pools hold 8-bit codes under per-(block, KV head) scales, int8
+// or (kFp8) E4M3; otherwise bf16.
+// 8-bit instances may be held to 128 registers (4 CTAs of 4 warps per SM,
+// the residency their shared memory allows).
+#ifndef PAGEDKV_Q8_MIN_BLOCKS
+#define PAGEDKV_Q8_MIN_BLOCKS 4
+#endif
+template <int D, int BS, bool kQ8, bool kFp8>
+__global__ void __launch_bounds__(kThreads, kQ8 ? PAGEDKV_Q8_MIN_BLOCKS : 1)
     decode_kernel(const __grid_constant__ CUtensorMap k_map,
                   const __grid_constant__ CUtensorMap v_map, const DecodeArgs a) {
-  using G = Geo<D, BS, kInt8>;
+  using G = Geo<D, BS, kQ8>;
   constexpr int S = G::kStages;
   extern __shared__ unsigned char smem_raw[];
   __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
   __shared__ int32_t blk_id[kMaxBlocks];
-  __shared__ float blk_ks[kInt8 ? kMaxBlocks : 1], blk_vr[kInt8 ? kMaxBlocks : 1];
+  __shared__ float blk_ks[kQ8 ? kMaxBlocks : 1], blk_vr[kQ8 ? kMaxBlocks : 1];
   __shared__ int cta_bad, cta_timeout;
   __shared__ float v_max_scale;
 
@@ -111,7 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         int d0;
-        if constexpr (kInt8) {
+        if constexpr (kQ8) {
           // lane t reads chunks t*NC .. t*NC+NC-1 (16 d each, NC = D/64)
           // of a row; k-step ks uses 4 consecutive d of chunk ks/4.
           constexpr int NC = D / 64;
@@ -171,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool ok = p >= 0 && p < a.num_blocks;
     blk_id[j] = ok ? p : 0;
     if (!ok) cta_bad = 1;
-    if constexpr (kInt8) {
+    if constexpr (kQ8) {
       if (ok) {
         blk_ks[j] = a.k_scale[(int64_t)p * Hkv + hk];
         const float vs = a.v_scale[(int64_t)p * Hkv + hk];
@@ -181,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
-  if constexpr (kInt8) {
+  if constexpr (kQ8) {
     // p is multiplied by (V scale / the CTA's largest V scale) so that it stays
     // in fp16 range; the output is multiplied back by the largest scale.
     const float vmax = v_max_scale > 0.0f ? v_max_scale : 1.0f;
@@ -227,14 +234,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint4 x = *reinterpret_cast<const uint4*>(
               static_cast<const __nv_bfloat16*>(is_v ? a.new_v : a.new_k) + src + e0);
           void* pool = const_cast<void*>(is_v ? a.v_cache : a.k_cache);
-          if constexpr (kInt8) {
+          if constexpr (kQ8) {
             const float sc = is_v ? a.v_scale[(int64_t)p * Hkv + hk] : blk_ks[nblk - 1];
             const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
             uint32_t o2[2] = {0u, 0u};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const uint32_t lo = (uint8_t)quantize(__uint_as_float(w4[i] << 16), sc);
-              const uint32_t hi = (uint8_t)quantize(__uint_as_float(w4[i] & 0xffff0000u), sc);
+              const uint32_t lo = code8<kFp8>(__uint_as_float(w4[i] << 16), sc);
+              const uint32_t hi = code8<kFp8>(__uint_as_float(w4[i] & 0xffff0000u), sc);
               o2[i / 2] |= (lo | (hi << 8)) << (16 * (i % 2));
             }
             *reinterpret_cast<uint2*>(static_cast<int8_t*>(pool) + dst + e0) = make_uint2(o2[0], o2[1]);
@@ -272,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (!bad) {
     // ======================= consumers =====================================
     const int w = warp;
-    constexpr bool kF16 = kInt8;
+    constexpr bool kF16 = kQ8;
     uint32_t qf[G::kKSteps][2];
     float qscale = 1.0f;
     {
@@ -289,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           amax = fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1)));
         }
       }
-      if constexpr (kInt8) {
+      if constexpr (kQ8) {
         // fp16 holds |q| < 65504; scale by a power of two when needed and
         // fold the inverse into the score scale (exact either way).
 #pragma unroll
@@ -325,14 +332,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t kb = stages + (uint32_t)((s * kConsumers + w) * G::kBlockBytes);
         const uint32_t vb = kb + G::kTensorBytes;
         const int valid = min(BS, L - (first_blk + j) * BS);
-        const float kfac = kInt8 ? score_scale * blk_ks[j] : score_scale;
+        const float kfac = kQ8 ? score_scale * blk_ks[j] : score_scale;
 
         // ---- scores S^T for every 16-token tile ---------------------------
         float sc[G::kTiles][4];
 #pragma unroll
         for (int tile = 0; tile < G::kTiles; ++tile) {
           float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-          if constexpr (!kInt8) {
+          if constexpr (!kQ8) {
             // ldmatrix.x4: matrix q = lane/8 covers rows (tokens) 8*(q&1)..+7
             // and d-chunk 2ks + (q>>1): registers = A fragment a0..a3.
             const int row = tile * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
@@ -353,17 +360,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int ci = 0; ci < NC; ++ci) {
                 const uint4 v = lds128(kb + chunk_off<G>(row, t * NC + ci));
-                kw[rr][ci][0] = v.x ^ 0x80808080u;
-                kw[rr][ci][1] = v.y ^ 0x80808080u;
-                kw[rr][ci][2] = v.z ^ 0x80808080u;
-                kw[rr][ci][3] = v.w ^ 0x80808080u;
+                kw[rr][ci][0] = v.x ^ kCodeBias<kFp8>;
+                kw[rr][ci][1] = v.y ^ kCodeBias<kFp8>;
+                kw[rr][ci][2] = v.z ^ kCodeBias<kFp8>;
+                kw[rr][ci][3] = v.w ^ kCodeBias<kFp8>;
               }
             }
 #pragma unroll
             for (int ks = 0; ks < G::kKSteps; ++ks) {
               const uint32_t w0 = kw[0][ks / 4][ks % 4], w1 = kw[1][ks / 4][ks % 4];
-              const uint32_t fa[4] = {codes_to_f16x2(w0, 0x4140u), codes_to_f16x2(w1, 0x4140u),
-                                      codes_to_f16x2(w0, 0x4342u), codes_to_f16x2(w1, 0x4342u)};
+              const uint32_t fa[4] = {codes_to_f16x2<kFp8>(w0, 0x4140u), codes_to_f16x2<kFp8>(w1, 0x4140u),
+                                      codes_to_f16x2<kFp8>(w0, 0x4342u), codes_to_f16x2<kFp8>(w1, 0x4342u)};
               if (ks & 1) mma16816<true>(c1, fa, qf[ks][0], qf[ks][1]);
               else        mma16816<true>(c0, fa, qf[ks][0], qf[ks][1]);
             }
@@ -401,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           o[i][2] *= al0;
           o[i][3] *= al1;
         }
-        const float vr = kInt8 ? blk_vr[j] : 1.0f;
+        const float vr = kQ8 ? blk_vr[j] : 1.0f;
 
 #pragma unroll
         for (int tile = 0; tile < G::kTiles; ++tile) {
@@ -420,16 +427,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t y1 = __shfl_sync(0xffffffffu, r1, src_b);
           const uint32_t pb0 = prmt(x0, x1, half_sel), pb1 = prmt(y0, y1, half_sel);
 
-          if constexpr (!kInt8) {
+          // V rows past `valid` are zeroed in the A fragments (tokens 2t, 2t+1
+          // in fa[0..1], 2t+8, 2t+9 in fa[2..3]): p is 0 there, but the pool
+          // may hold NaN (bf16 or E4M3 patterns) and 0 * NaN is NaN.  int8
+          // codes are always finite and skip it.
+          uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+          if ((!kQ8 || kFp8) && valid < BS) {
+            const int k0 = tile * 16 + 2 * t;
+            mlo = (k0 < valid ? 0x0000ffffu : 0u) | (k0 + 1 < valid ? 0xffff0000u : 0u);
+            mhi = (k0 + 8 < valid ? 0x0000ffffu : 0u) | (k0 + 9 < valid ? 0xffff0000u : 0u);
+          }
+          if constexpr (!kQ8) {
             // V^T tiles by ldmatrix.trans: matrix q = lane/8 covers tokens
             // 8*(q>>1)..+7 of the tile and d-chunk 2i + (q&1).
             const int row = tile * 16 + (lane >> 4) * 8 + (lane & 7);
-            uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;  // rows past `valid` -> 0
-            if (valid < BS) {
-              const int k0 = tile * 16 + 2 * t;
-              mlo = (k0 < valid ? 0x0000ffffu : 0u) | (k0 + 1 < valid ? 0xffff0000u : 0u);
-              mhi = (k0 + 8 < valid ? 0x0000ffffu : 0u) | (k0 + 9 < valid ? 0xffff0000u : 0u);
-            }
 #pragma unroll
             for (int i = 0; i < G::kMTiles; ++i) {
               uint32_t fa[4];
@@ -443,8 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             // Lane (g, t) reads tokens 2t, 2t+1, 2t+8, 2t+9 of the tile, the
             // D/8 bytes of d in [g*D/8, (g+1)*D/8); m-tile i pairs d rows
-            // g <-> g*D/8 + 2i and g+8 <-> g*D/8 + 2i + 1.  int8 codes are
-            // finite, and p = 0 for masked tokens, so no masking is needed.
+            // g <-> g*D/8 + 2i and g+8 <-> g*D/8 + 2i + 1.
             constexpr int NB = D / 8;                 // bytes per lane per token
             constexpr int NW = NB / 4;
             uint32_t vw[4][NW];
@@ -453,14 +463,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int row = tile * 16 + 2 * t + (rr & 1) + 8 * (rr >> 1);
               if constexpr (NB == 16) {
                 const uint4 v = lds128(vb + chunk_off<G>(row, g));
-                vw[rr][0] = v.x ^ 0x80808080u;
-                vw[rr][1] = v.y ^ 0x80808080u;
-                vw[rr][2] = v.z ^ 0x80808080u;
-                vw[rr][3] = v.w ^ 0x80808080u;
+                vw[rr][0] = v.x ^ kCodeBias<kFp8>;
+                vw[rr][1] = v.y ^ kCodeBias<kFp8>;
+                vw[rr][2] = v.z ^ kCodeBias<kFp8>;
+                vw[rr][3] = v.w ^ kCodeBias<kFp8>;
               } else {
                 const uint2 v = lds64(vb + chunk_off<G>(row, g / 2) + (g & 1) * 8);
-                vw[rr][0] = v.x ^ 0x80808080u;
-                vw[rr][1] = v.y ^ 0x80808080u;
+                vw[rr][0] = v.x ^ kCodeBias<kFp8>;
+                vw[rr][1] = v.y ^ kCodeBias<kFp8>;
               }
             }
 #pragma unroll
@@ -468,8 +478,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;  // bytes 2,3 or 0,1
               const uint32_t ulo = prmt(vw[0][i / 2], vw[1][i / 2], sel);  // tokens 2t, 2t+1
               const uint32_t uhi = prmt(vw[2][i / 2], vw[3][i / 2], sel);  // tokens 2t+8, 2t+9
-              const uint32_t fa[4] = {codes_to_f16x2(ulo, 0x4140u), codes_to_f16x2(ulo, 0x4342u),
-                                      codes_to_f16x2(uhi, 0x4140u), codes_to_f16x2(uhi, 0x4342u)};
+              uint32_t fa[4] = {codes_to_f16x2<kFp8>(ulo, 0x4140u), codes_to_f16x2<kFp8>(ulo, 0x4342u),
+                                codes_to_f16x2<kFp8>(uhi, 0x4140u), codes_to_f16x2<kFp8>(uhi, 0x4342u)};
+              if constexpr (kFp8) {
+                fa[0] &= mlo;
+                fa[1] &= mlo;
+                fa[2] &= mhi;
+                fa[3] &= mhi;
+              }
               mma16816<true>(o[i], fa, pb0, pb1);
             }
           }
@@ -504,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int i = 0; i < G::kMTiles; ++i) {
       int d_lo, d_hi;                              // d rows g and g+8 of m-tile i
-      if constexpr (kInt8) {
+      if constexpr (kQ8) {
         d_lo = g * (D / 8) + 2 * i;
         d_hi = d_lo + 1;
       } else {
@@ -538,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
 
-  const float out_scale = kInt8 ? (v_max_scale > 0.0f ? v_max_scale : 1.0f) : 1.0f;
+  const float out_scale = kQ8 ? (v_max_scale > 0.0f ? v_max_scale : 1.0f) : 1.0f;
   for (int i = threadIdx.x; i < GQ * D; i += blockDim.x) {
     const int hh = i / D, e = i % D;
     float M = -INFINITY;
@@ -586,9 +602,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 4-D map over a pool [NB, bs, Hkv, d] (innermost first: d, head, row, block)
 // whose box is one block's rows of one head: [1, bs, 1, box elements].
-template <int D, int BS, bool kInt8>
+template <int D, int BS, bool kQ8>
 kv_status make_map(CUtensorMap* map, const void* pool, const DecodeArgs& a) {
-  using G = Geo<D, BS, kInt8>;
+  using G = Geo<D, BS, kQ8>;
   auto fn = encode_fn();
   if (!fn) return fail(KV_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
   const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)a.num_kv_heads, (cuuint64_t)BS,
@@ -598,7 +614,7 @@ kv_status make_map(CUtensorMap* map, const void* pool, const DecodeArgs& a) {
                                  (cuuint64_t)BS * a.num_kv_heads * D * G::kElem};
   const cuuint32_t box[4] = {(cuuint32_t)G::kBoxElems, 1, (cuuint32_t)BS, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
-  const CUresult r = fn(map, kInt8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+  const CUresult r = fn(map, kQ8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                         4, const_cast<void*>(pool), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE,
                         G::kSwizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -609,9 +625,9 @@ kv_status make_map(CUtensorMap* map, const void* pool, const DecodeArgs& a) {
   return KV_OK;
 }
 
-template <int D, int BS, bool kInt8>
+template <int D, int BS, bool kQ8, bool kFp8>
 kv_status launch_t(const DecodeArgs& a, cudaStream_t s) {
-  using G = Geo<D, BS, kInt8>;
+  using G = Geo<D, BS, kQ8>;
   static std::mutex mu;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -620,7 +636,7 @@ kv_status launch_t(const DecodeArgs& a, cudaStream_t s) {
   {
     std::lock_guard<std::mutex> lock(mu);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-      st = cuda_check(cudaFuncSetAttribute(decode_kernel<D, BS, kInt8>,
+      st = cuda_check(cudaFuncSetAttribute(decode_kernel<D, BS, kQ8, kFp8>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            G::kSmemBytes),
                       "cudaFuncSetAttribute(decode_kernel)");
@@ -629,11 +645,11 @@ kv_status launch_t(const DecodeArgs& a, cudaStream_t s) {
     }
   }
   alignas(64) CUtensorMap km, vm;
-  if ((st = make_map<D, BS, kInt8>(&km, a.k_cache, a)) != KV_OK) return st;
-  if ((st = make_map<D, BS, kInt8>(&vm, a.v_cache, a)) != KV_OK) return st;
+  if ((st = make_map<D, BS, kQ8>(&km, a.k_cache, a)) != KV_OK) return st;
+  if ((st = make_map<D, BS, kQ8>(&vm, a.v_cache, a)) != KV_OK) return st;
   const dim3 grid(a.num_kv_heads, a.batch, a.max_parts);
   if (a.prefix_chunks == 0) {
-    decode_kernel<D, BS, kInt8><<<grid, kThreads, G::kSmemBytes, s>>>(km, vm, a);
+    decode_kernel<D, BS, kQ8, kFp8><<<grid, kThreads, G::kSmemBytes, s>>>(km, vm, a);
     return cuda_check(cudaGetLastError(), "decode_kernel launch");
   }
   // Behind the prefix kernel: launched as its programmatic dependent so the
@@ -649,30 +665,30 @@ kv_status launch_t(const DecodeArgs& a, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cuda_check(cudaLaunchKernelEx(&cfg, decode_kernel<D, BS, kInt8>, km, vm, a),
+  return cuda_check(cudaLaunchKernelEx(&cfg, decode_kernel<D, BS, kQ8, kFp8>, km, vm, a),
                     "decode_kernel launch");
 }
 
-template <int D, bool kInt8>
+template <int D, bool kQ8, bool kFp8>
 kv_status launch_bs(const DecodeArgs& a, cudaStream_t s) {
-  return a.block_size == 32 ? launch_t<D, 32, kInt8>(a, s) : launch_t<D, 16, kInt8>(a, s);
+  return a.block_size == 32 ? launch_t<D, 32, kQ8, kFp8>(a, s) : launch_t<D, 16, kQ8, kFp8>(a, s);
 }
 
-template <int D, int BS, bool kInt8>
+template <int D, int BS, bool kQ8>
 kv_status maps_t(const DecodeArgs& a, CUtensorMap* km, CUtensorMap* vm) {
-  kv_status st = make_map<D, BS, kInt8>(km, a.k_cache, a);
-  return st != KV_OK ? st : make_map<D, BS, kInt8>(vm, a.v_cache, a);
+  kv_status st = make_map<D, BS, kQ8>(km, a.k_cache, a);
+  return st != KV_OK ? st : make_map<D, BS, kQ8>(vm, a.v_cache, a);
 }
 
 }  // namespace
 
 kv_status make_kv_maps(const DecodeArgs& a, CUtensorMap* km, CUtensorMap* vm) {
-  const bool int8 = a.dtype == KV_DTYPE_INT8, b32 = a.block_size == 32;
+  const bool q8 = a.dtype != KV_DTYPE_BF16, b32 = a.block_size == 32;
   if (a.head_dim == 128) {
-    if (int8) return b32 ? maps_t<128, 32, true>(a, km, vm) : maps_t<128, 16, true>(a, km, vm);
+    if (q8) return b32 ? maps_t<128, 32, true>(a, km, vm) : maps_t<128, 16, true>(a, km, vm);
     return b32 ? maps_t<128, 32, false>(a, km, vm) : maps_t<128, 16, false>(a, km, vm);
   }
-  if (int8) return b32 ? maps_t<64, 32, true>(a, km, vm) : maps_t<64, 16, true>(a, km, vm);
+  if (q8) return b32 ? maps_t<64, 32, true>(a, km, vm) : maps_t<64, 16, true>(a, km, vm);
   return b32 ? maps_t<64, 32, false>(a, km, vm) : maps_t<64, 16, false>(a, km, vm);
 }
 
@@ -684,9 +700,13 @@ kv_status launch_decode(const DecodeArgs& a, cudaStream_t s) {
   if (a.part_tokens / a.block_size > kMaxBlocks || a.part_tokens % a.block_size)
     return fail(KV_ERR_INVALID_ARG, "partition must be a multiple of block_size, at most %d blocks",
                 kMaxBlocks);
-  const bool int8 = a.dtype == KV_DTYPE_INT8;
-  if (a.head_dim == 128) return int8 ? launch_bs<128, true>(a, s) : launch_bs<128, false>(a, s);
-  return int8 ? launch_bs<64, true>(a, s) : launch_bs<64, false>(a, s);
+  if (a.head_dim == 128) {
+    if (a.dtype == KV_DTYPE_FP8_E4M3) return launch_bs<128, true, true>(a, s);
+    return a.dtype == KV_DTYPE_INT8 ? launch_bs<128, true, false>(a, s)
+                                    : launch_bs<128, false, false>(a, s);
+  }
+  if (a.dtype == KV_DTYPE_FP8_E4M3) return launch_bs<64, true, true>(a, s);
+  return a.dtype == KV_DTYPE_INT8 ? launch_bs<64, true, false>(a, s) : launch_bs<64, false, false>(a, s);
 }
 
 }  // namespace pagedkv

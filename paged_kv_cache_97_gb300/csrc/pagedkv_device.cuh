@@ -26,9 +26,9 @@ constexpr int kMaxStages = 8;
 constexpr int kStageBudget = PAGEDKV_STAGE_BUDGET;    // shared memory for decode stages
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
-template <int D, int BS, bool kInt8>
+template <int D, int BS, bool kQ8>
 struct Geo {
-  static constexpr int kElem = kInt8 ? 1 : 2;
+  static constexpr int kElem = kQ8 ? 1 : 2;
   static constexpr int kRowBytes = D * kElem;                          // 256, 128, 64
   static constexpr int kBoxRow = kRowBytes > 128 ? 128 : kRowBytes;    // bytes per box row
   static constexpr int kBoxes = kRowBytes / kBoxRow;                   // 2 for bf16 d128
@@ -166,14 +166,32 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return r;
 }
 
-// int8 codes (two's complement) at bytes b0, b1 of w, already XORed with
-// 0x80 (so each byte is c + 128): fp16 pair of (1024 + c + 128) - 1152 = c,
-// exact.  sel 0x4140 takes bytes 0,1; 0x4342 bytes 2,3.
-__device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t w_biased, uint32_t sel) {
-  const uint32_t h = prmt(w_biased, 0x64646464u, sel);
-  __half2 x = *reinterpret_cast<const __half2*>(&h);
-  x = __hsub2(x, __half2half2(__ushort_as_half((unsigned short)0x6480)));  // 1152.0
-  return *reinterpret_cast<const uint32_t*>(&x);
+// XOR applied to each 32-bit word of codes before codes_to_f16x2: int8
+// codes are biased by 128 (below); E4M3 codes are converted as they are.
+template <bool kFp8>
+constexpr uint32_t kCodeBias = kFp8 ? 0u : 0x80808080u;
+
+// Two 8-bit codes of w as an fp16 pair (low half = the lower byte), exact
+// either way; sel 0x4140 takes bytes 0,1 and 0x4342 bytes 2,3.
+//   int8: w already XORed with kCodeBias, so each byte is c + 128; the
+//         bytes are placed under 0x64 (fp16 1024 + byte) and 1152 is
+//         subtracted: c.
+//   E4M3: the hardware conversion of an e4m3 pair to f16x2 (every E4M3
+//         value, subnormals included, is an fp16 value).
+template <bool kFp8>
+__device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t w, uint32_t sel) {
+  if constexpr (kFp8) {
+    const unsigned short pair = sel == 0x4140u ? (unsigned short)(w & 0xffffu)
+                                               : (unsigned short)(w >> 16);
+    uint32_t h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(pair));
+    return h;
+  } else {
+    const uint32_t h = prmt(w, 0x64646464u, sel);
+    __half2 x = *reinterpret_cast<const __half2*>(&h);
+    x = __hsub2(x, __half2half2(__ushort_as_half((unsigned short)0x6480)));  // 1152.0
+    return *reinterpret_cast<const uint32_t*>(&x);
+  }
 }
 
 __device__ __forceinline__ int8_t quantize(float x, float s) {
@@ -182,6 +200,25 @@ __device__ __forceinline__ int8_t quantize(float x, float s) {
   int c = __float2int_rn(__fdiv_rn(x, s));
   c = c > 127 ? 127 : (c < -127 ? -127 : c);
   return (int8_t)c;
+}
+
+// E4M3 code of x / s (IEEE fp32 divide; s == 0 -> 1): round to nearest even,
+// magnitudes above 448 saturate to 448, NaN gives the NaN pattern.  The
+// conversion packs its first operand in the upper byte, its second in the
+// lower one.
+__device__ __forceinline__ uint8_t quantize_e4m3(float x, float s) {
+  if (s == 0.0f) s = 1.0f;
+  const float r = __fdiv_rn(x, s);
+  unsigned short h;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(0.0f), "f"(r));
+  return (uint8_t)(h & 0xffu);
+}
+
+// The byte an 8-bit pool stores for x under scale s.
+template <bool kFp8>
+__device__ __forceinline__ uint8_t code8(float x, float s) {
+  if constexpr (kFp8) return quantize_e4m3(x, s);
+  else return (uint8_t)quantize(x, s);
 }
 
 // Byte offset of 16-byte chunk `c` of row `r` inside one K or V block of a

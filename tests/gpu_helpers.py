@@ -11,10 +11,23 @@ def to_dev_bf16(bits: np.ndarray, dev="cuda"):
 
 
 def bits_of(t: torch.Tensor) -> np.ndarray:
-    """Raw bits of a device tensor (bf16 -> uint16, int8 -> int8)."""
+    """Raw bits of a device tensor (bf16 -> uint16, int8 -> int8, E4M3 ->
+    uint8), the oracle's pool dtypes."""
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    if t.dtype == torch.float8_e4m3fn:
+        return t.view(torch.uint8).cpu().numpy()
     return t.cpu().numpy()
+
+
+def dev_pool(host: np.ndarray, dev="cuda") -> torch.Tensor:
+    """A device pool from the oracle's host layout (uint16 bf16 bits, int8
+    codes or uint8 E4M3 codes)."""
+    if host.dtype == np.uint16:
+        return to_dev_bf16(host, dev)
+    if host.dtype == np.uint8:
+        return torch.from_numpy(np.ascontiguousarray(host)).to(dev).view(torch.float8_e4m3fn)
+    return torch.from_numpy(np.ascontiguousarray(host)).to(dev)
 
 
 class GpuStep:
@@ -24,10 +37,10 @@ class GpuStep:
     def __init__(self, wl, dev="cuda", fill=True, seqs=None):
         s = wl.spec
         self.wl, self.dev = wl, dev
-        self.int8 = s.kv_dtype == "int8"
+        self.q8 = s.kv_dtype != "bf16"
         poison = wl.poisoned_pool()
-        if self.int8:
-            self.k_cache = torch.from_numpy(poison).to(dev)
+        if self.q8:
+            self.k_cache = dev_pool(poison, dev)
             self.v_cache = self.k_cache.clone()
             ks, vs = wl.scales(seqs)
             self.k_scale = torch.from_numpy(ks).to(dev)

@@ -16,18 +16,15 @@ def oracle_pool(wl, seqs=None, with_new_token=True):
     position L_b - 1.  Returns (k_cache, v_cache, k_scale, v_scale)."""
     s = wl.spec
     kc, vc = wl.poisoned_pool(), wl.poisoned_pool()
-    int8 = s.kv_dtype == "int8"
+    q8 = s.kv_dtype != "bf16"
     ks = vs = None
-    if int8:
+    if q8:
         ks, vs = wl.scales(seqs)
     for ch in wl.fill_chunks(seqs):
         slots, rc = oracle.token_slots(wl.block_tables, ch.positions, s.block_size,
                                        wl.num_blocks, seq_idx=ch.seq_idx)
         assert rc == 0
-        if int8:
-            rc = oracle.append_int8(ch.k, ch.v, kc, vc, ks, vs, slots)
-        else:
-            rc = oracle.append_bf16(ch.k, ch.v, kc, vc, slots)
+        rc = append_any(ch.k, ch.v, kc, vc, ks, vs, slots)
         assert rc == 0
     if with_new_token:
         b_all = np.arange(s.batch) if seqs is None else np.asarray(list(seqs))
@@ -35,12 +32,19 @@ def oracle_pool(wl, seqs=None, with_new_token=True):
         assert rc == 0
         sel = np.full(s.batch, -1, np.int64)
         sel[b_all] = slots[b_all]
-        if int8:
-            rc = oracle.append_int8(wl.new_k, wl.new_v, kc, vc, ks, vs, sel)
-        else:
-            rc = oracle.append_bf16(wl.new_k, wl.new_v, kc, vc, sel)
+        rc = append_any(wl.new_k, wl.new_v, kc, vc, ks, vs, sel)
         assert rc == 0
     return kc, vc, ks, vs
+
+
+def append_any(k, v, kc, vc, ks, vs, slots):
+    """The oracle's append for the pool's dtype (uint16 bf16 bits, int8
+    codes, uint8 E4M3 codes)."""
+    if kc.dtype == np.int8:
+        return oracle.append_int8(k, v, kc, vc, ks, vs, slots)
+    if kc.dtype == np.uint8:
+        return oracle.append_fp8(k, v, kc, vc, ks, vs, slots)
+    return oracle.append_bf16(k, v, kc, vc, slots)
 
 
 def decode_slots(wl):
@@ -76,10 +80,10 @@ class OracleBeamRun:
     def __init__(self, w, pool=None):
         self.w = w
         self.pool = pool if pool is not None else oracle.BlockPoolModel(w.num_blocks)
-        self.int8 = w.kv_dtype == "int8"
+        self.q8 = w.kv_dtype != "bf16"
         self.kc, self.vc = w.poisoned_pool(), w.poisoned_pool()
-        self.ks = w.k_scale.copy() if self.int8 else None
-        self.vs = w.v_scale.copy() if self.int8 else None
+        self.ks = w.k_scale.copy() if self.q8 else None
+        self.vs = w.v_scale.copy() if self.q8 else None
         MB, bs = w.max_blocks_per_seq, w.block_size
         self.tables = []
         for p, L in enumerate(w.parent_lens):
@@ -98,11 +102,7 @@ class OracleBeamRun:
         self.step = -1
 
     def _append(self, k, v, slots):
-        if self.int8:
-            rc = oracle.append_int8(k, v, self.kc, self.vc, self.ks, self.vs, slots)
-        else:
-            rc = oracle.append_bf16(k, v, self.kc, self.vc, slots)
-        assert rc == 0
+        assert append_any(k, v, self.kc, self.vc, self.ks, self.vs, slots) == 0
 
     def table_array(self):
         return np.stack(self.tables).astype(np.int32)

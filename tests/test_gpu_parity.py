@@ -3,8 +3,9 @@ same seeded inputs.
 
 Bars: slot mapping and appends bit-exact (whole pools compared bit for bit,
 poison included); attention max-abs <= 1e-2 and mean-abs <= 1e-3 for bf16
-pools, max-abs <= 3e-2 and mean-abs <= 1e-3 for int8 pools (the oracle runs
-on the dequantised stored codes, so quantisation error is not counted).
+pools, max-abs <= 3e-2 and mean-abs <= 1e-3 for int8 and FP8 E4M3 pools (the
+oracle runs on the dequantised stored codes, so quantisation error is not
+counted).
 """
 import os
 
@@ -20,7 +21,7 @@ from oracle_helpers import decode_slots, oracle_pool
 
 pytestmark = pytest.mark.gpu
 
-TOL = {"bf16": (1e-2, 1e-3), "int8": (3e-2, 1e-3)}
+TOL = {"bf16": (1e-2, 1e-3), "int8": (3e-2, 1e-3), "fp8": (3e-2, 1e-3)}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -62,6 +63,9 @@ CASES = {
     "g8_bf16_d128": lambda: small([17, 600, 1500], hq=16, hkv=2, d=128, seed=5),
     "int8_d64_bs16": lambda: small([1, 90, 300, 777], hq=8, hkv=2, d=64, bs=16, kv="int8", seed=6),
     "shared_prefix": lambda: small([33, 48, 300, 700], hq=32, hkv=8, d=128, prefix=32, seed=8),
+    "g8_fp8_bs32": lambda: small([1, 31, 32, 33, 511, 700, 2049], hq=64, hkv=8, d=128, bs=32, kv="fp8", seed=12),
+    "fp8_d64_bs16": lambda: small([1, 90, 300, 777], hq=8, hkv=2, d=64, bs=16, kv="fp8", seed=13),
+    "fp8_g4_d128_bs16": lambda: small([2, 17, 1000, 2500], hq=32, hkv=8, d=128, bs=16, kv="fp8", seed=14),
 }
 
 
@@ -69,7 +73,8 @@ CASES = {
 # Slot mapping and append: bit-exact
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("case", ["cfg1", "g8_int8_bs32", "int8_d64_bs16", "shared_prefix", "g2_bs32_d64"])
+@pytest.mark.parametrize("case", ["cfg1", "g8_int8_bs32", "int8_d64_bs16", "shared_prefix", "g2_bs32_d64",
+                                  "g8_fp8_bs32", "fp8_d64_bs16"])
 def test_append_and_slots_bit_exact(case):
     wl = CASES[case]()
     g = GpuStep(wl)
@@ -107,6 +112,40 @@ def test_int8_append_rounding_is_the_oracles():
     torch.cuda.synchronize()
     np.testing.assert_array_equal(dk.cpu().numpy(), kc)
     np.testing.assert_array_equal(dv.cpu().numpy(), vc)
+
+
+def test_fp8_append_rounding_is_the_oracles():
+    """E4M3 codes at and near every rounding tie, in the subnormal range and
+    past the saturation point: device codes equal the oracle's; NaN inputs
+    give the NaN pattern on both sides."""
+    rng = np.random.default_rng(1)
+    n, H, d, bs, NB = 64, 2, 128, 32, 4
+    scale = np.float32(2.0 ** -5)                                     # x / scale exact
+    vals = np.array([oracle.fp8_value(c) for c in range(0x7F)])
+    mids = ((vals[:-1] + vals[1:]) / 2).astype(np.float32)            # ties, bf16-exact
+    special = np.array([448.0, 460.0, 464.0, 500.0, 1e4, 2.0 ** -10, 3 * 2.0 ** -11, 0.0],
+                       np.float32)
+    x = np.concatenate([mids, -mids, special, -special]) * scale
+    x = np.concatenate([x, rng.standard_normal(n * H * d - x.size - 2).astype(np.float32) * 0.1,
+                        np.array([np.nan, -np.nan], np.float32)])
+    bits = workloads.to_bf16_bits(x).reshape(n, H, d)
+    ks = np.full((NB, H), scale, np.float32)
+    ks[1, 0] = 0.0                                                    # zero scale reads as 1
+    slots = rng.permutation(NB * bs)[:n].astype(np.int64)
+    kc = np.zeros((NB, bs, H, d), np.uint8)
+    vc = np.zeros_like(kc)
+    assert oracle.append_fp8(bits, bits, kc, vc, ks, ks, slots) == 0
+    from gpu_helpers import dev_pool, to_dev_bf16
+    dk, dv = dev_pool(np.zeros_like(kc)), dev_pool(np.zeros_like(kc))
+    t = to_dev_bf16(bits)
+    s = torch.from_numpy(ks).cuda()
+    pkv.reshape_and_cache(t, t, dk, dv, torch.from_numpy(slots).cuda(), s, s)
+    torch.cuda.synchronize()
+    got_k, got_v = bits_of(dk), bits_of(dv)
+    nan = (kc & 0x7F) == 0x7F
+    assert nan.sum() == 2 and ((got_k[nan] & 0x7F) == 0x7F).all()
+    np.testing.assert_array_equal(got_k[~nan], kc[~nan])
+    np.testing.assert_array_equal(got_v[~nan], vc[~nan])
 
 
 # ---------------------------------------------------------------------------
@@ -149,7 +188,8 @@ def test_partition_size_does_not_change_the_answer(monkeypatch, part):
     check_status()
 
 
-@pytest.mark.parametrize("case", ["cfg1", "ragged_g4_d128", "g8_int8_bs32", "shared_prefix", "int8_d64_bs16"])
+@pytest.mark.parametrize("case", ["cfg1", "ragged_g4_d128", "g8_int8_bs32", "shared_prefix", "int8_d64_bs16",
+                                  "g8_fp8_bs32"])
 def test_fused_step_equals_separate_calls(case):
     """pagedkv_decode_step (append inside the attention kernel) leaves the same
     pools, bit for bit, and the same output as slot mapping + append +
@@ -165,7 +205,7 @@ def test_fused_step_equals_separate_calls(case):
     np.testing.assert_array_equal(out_b, out_a)
 
 
-@pytest.mark.parametrize("case", ["cfg1", "ragged_g4_d128", "g8_int8_bs32"])
+@pytest.mark.parametrize("case", ["cfg1", "ragged_g4_d128", "g8_int8_bs32", "fp8_d64_bs16"])
 def test_decode_step_replays_from_a_cuda_graph(case):
     """The fused step captured once in a CUDA graph (decode + PDL merge) and
     replayed gives the eager step's output bit for bit; replaying re-appends
@@ -243,8 +283,9 @@ def test_prefix_mismatch_is_flagged_and_zeroed():
     assert not out[2].any() and out[0].any() and out[3].any()
 
 
-def test_prefix_rejects_int8_pools():
-    wl = small([65, 90], hq=64, hkv=8, d=128, bs=32, kv="int8", seed=35)
+@pytest.mark.parametrize("kv", ["int8", "fp8"])
+def test_prefix_rejects_8bit_pools(kv):
+    wl = small([65, 90], hq=64, hkv=8, d=128, bs=32, kv=kv, seed=35)
     g = GpuStep(wl)
     pb = g.block_tables[0, :1].contiguous()
     ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
@@ -391,7 +432,7 @@ def sample_rows(wl, n_seqs=3, rng_seed=0):
     return seqs, rows
 
 
-@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
+@pytest.mark.parametrize("cfg", [2, 3, 4, 5, 6])
 def test_full_size_config_sampled_rows(cfg):
     wl = workloads.make(cfg)
     g = GpuStep(wl)

@@ -10,6 +10,7 @@ import pytest
 import oracle
 from test_oracle_append import check_fp32_decision, check_rounding
 from test_oracle_attention import check_against_sdpa, check_int8_against_sdpa, small
+from test_oracle_fp8 import check_decode, check_encode, check_fp8_against_sdpa, check_saturation
 
 
 def _sdpa():
@@ -18,6 +19,16 @@ def _sdpa():
 
 def _sdpa_int8():
     check_int8_against_sdpa(small([1, 5, 32, 33, 70, 200], hq=16, hkv=2, d=128, bs=32, kv="int8", seed=3))
+
+
+def _sdpa_fp8():
+    check_fp8_against_sdpa(small([1, 5, 32, 33, 70, 200], hq=16, hkv=2, d=128, bs=32, kv="fp8", seed=3))
+
+
+def _fp8_codes():
+    check_decode(oracle.fp8_value)
+    check_encode(oracle.quantize_fp8)
+    check_saturation(oracle.quantize_fp8)
 
 
 def _rounding():
@@ -43,8 +54,14 @@ MUTANTS = {
     "slot_row_wrong": ("slots[i] = (int64_t)physical * block_size + (p % block_size);",
                        "slots[i] = (int64_t)physical * block_size + (p / block_size);", _sdpa),
     "sum_sign_flipped": ("Z += exp(s[t] - m);", "Z += exp(m - s[t]);", _sdpa),
-    "dequant_scale_dropped": ("return (double)c[idx] * (double)s[(int64_t)block * P->num_kv_heads + hk];",
-                              "return (double)c[idx];", _sdpa_int8),
+    "dequant_scale_dropped": ("return (double)c[idx] * sc;", "return (double)c[idx];", _sdpa_int8),
+    "fp8_dequant_scale_dropped": ("return oracle_fp8_value(c[idx]) * sc;",
+                                  "return oracle_fp8_value(c[idx]);", _sdpa_fp8),
+    "fp8_ties_to_odd": ("(d == best_d && (c & 1) == 0)", "(d == best_d && (c & 1) == 1)", _fp8_codes),
+    "fp8_exponent_bias_8": ("ldexp(1.0 + m / 8.0, e - 7)", "ldexp(1.0 + m / 8.0, e - 8)", _fp8_codes),
+    "fp8_subnormal_exponent": ("ldexp(m / 8.0, -6)", "ldexp(m / 8.0, -7)", _fp8_codes),
+    "fp8_no_saturation": ("        return sign | 0x7E;", "        return 0x7F;", _fp8_codes),
+    "fp8_sign_dropped": ("    return sign | (uint8_t)best;", "    return (uint8_t)best;", _fp8_codes),
     "round_half_away": ("float r = nearbyintf(x / s);", "float r = roundf(x / s);", _rounding),
     "fp64_decision": ("float r = nearbyintf(x / s);",
                       "float r = (float)nearbyint((double)x / (double)s);", _fp32),

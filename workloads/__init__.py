@@ -19,6 +19,7 @@ shared 800-token system prompt; 16-token blocks, 32 for the int8 case):
                    lognormal(6, 1)), 16, 2048); blocks 0..49 shared by all
   5 70B-like INT8  B 128, 64/8 heads, d 128, bs 32, L ~ U{1024..8192},
                    int8 pool, scale = max|x| / 127 per (block, KV head)
+  6 70B-like FP8   as 5 with an FP8 E4M3 pool, scale = max|x| / 448
 
 Recipe: ``numpy.random.Generator(PCG64)`` streams spawned from
 ``SeedSequence(20260000 + config)``: stream 0 draws lengths then placement,
@@ -28,7 +29,7 @@ regenerated alone).  Values are N(0, 1) in fp32 rounded to the nearest-even
 bf16.  The pool holds ceil(1.25 x needed blocks) unless the config fixes it;
 placement is a seeded random permutation of the pool, each sequence taking
 the next ``ceil(L_b / bs)`` entries.  Unused pool memory starts poisoned
-(bf16 NaN, int8 127) and table padding is -1.  ``L_b`` counts the token
+(bf16 NaN, int8 127, E4M3 NaN 0x7F) and table padding is -1.  ``L_b`` counts the token
 appended in this step; cached tokens are positions ``0 .. L_b - 2``.
 """
 from __future__ import annotations
@@ -41,6 +42,9 @@ import numpy as np
 
 BF16_NAN = np.uint16(0x7FC0)
 INT8_POISON = np.int8(127)
+FP8_NAN = np.uint8(0x7F)            # the E4M3 NaN pattern
+# largest code magnitude of each 8-bit KV format: scale = max |x| / this
+CODE_MAX = {"int8": 127.0, "fp8": 448.0}
 SEED_BASE = 20260000
 
 
@@ -63,7 +67,7 @@ class Spec:
     num_kv_heads: int
     head_dim: int
     block_size: int
-    kv_dtype: str                      # "bf16" | "int8"
+    kv_dtype: str                      # "bf16" | "int8" | "fp8" (E4M3)
     lens: tuple                        # ("uniform", lo, hi) | ("prefix_lognormal", ...) | ("fixed", [..])
     num_blocks: Optional[int] = None   # None: ceil(1.25 * needed)
     max_blocks_per_seq: Optional[int] = None
@@ -89,6 +93,9 @@ CONFIGS = {
             max_blocks_per_seq=(800 + 2048 + 15) // 16, shared_prefix_tokens=800),
     5: Spec("Llama-2-70B-like INT8 KV (B128, 64/8 heads, d128, bs32, L 1024..8192)",
             128, 64, 8, 128, 32, "int8", ("uniform", 1024, 8192),
+            max_blocks_per_seq=256),
+    6: Spec("Llama-2-70B-like FP8 E4M3 KV (B128, 64/8 heads, d128, bs32, L 1024..8192)",
+            128, 64, 8, 128, 32, "fp8", ("uniform", 1024, 8192),
             max_blocks_per_seq=256),
 }
 
@@ -162,11 +169,13 @@ class Workload:
 
     @property
     def kv_elem_bytes(self) -> int:
-        return 1 if self.spec.kv_dtype == "int8" else 2
+        return 2 if self.spec.kv_dtype == "bf16" else 1
 
     def poisoned_pool(self) -> np.ndarray:
         if self.spec.kv_dtype == "int8":
             return np.full(self.pool_shape, INT8_POISON, np.int8)
+        if self.spec.kv_dtype == "fp8":
+            return np.full(self.pool_shape, FP8_NAN, np.uint8)
         return np.full(self.pool_shape, BF16_NAN, np.uint16)
 
     # -- cached token values ---------------------------------------------
@@ -211,16 +220,18 @@ class Workload:
             if pos.size:
                 yield FillChunk(np.full(pos.size, b, np.int32), pos, k, v)
 
-    # -- int8 scales -------------------------------------------------------
+    # -- 8-bit scales ------------------------------------------------------
     def scales(self, seqs: Optional[Sequence[int]] = None):
-        """fp32 k_scale, v_scale [NB, Hkv]: max |x| / 127 over the bf16 values
-        (cached plus new) that land in each (block, KV head); 1.0 elsewhere."""
+        """fp32 k_scale, v_scale [NB, Hkv]: max |x| / 127 (int8) or / 448
+        (E4M3) over the bf16 values (cached plus new) that land in each
+        (block, KV head); 1.0 elsewhere."""
         s = self.spec
         NB, H, bs = self.num_blocks, s.num_kv_heads, s.block_size
         ks = np.ones((NB, H), np.float32)
         vs = np.ones((NB, H), np.float32)
         seqs = range(s.batch) if seqs is None else seqs
-        assert s.shared_prefix_tokens == 0, "int8 workloads have no shared prefix"
+        assert s.shared_prefix_tokens == 0, "8-bit workloads have no shared prefix"
+        top = np.float32(CODE_MAX[s.kv_dtype])
         for b in seqs:
             L = int(self.seq_lens[b])
             pos, k, v = self.own_tokens(b)
@@ -233,8 +244,8 @@ class Workload:
             kmax = kf.reshape(nblk, bs, H, -1).max(axis=(1, 3))
             vmax = vf.reshape(nblk, bs, H, -1).max(axis=(1, 3))
             phys = self.block_tables[b, :nblk]
-            ks[phys] = np.where(kmax > 0, kmax / np.float32(127.0), np.float32(1.0))
-            vs[phys] = np.where(vmax > 0, vmax / np.float32(127.0), np.float32(1.0))
+            ks[phys] = np.where(kmax > 0, kmax / top, np.float32(1.0))
+            vs[phys] = np.where(vmax > 0, vmax / top, np.float32(1.0))
         return ks, vs
 
     # -- byte accounting -----------------------------------------------------
@@ -276,8 +287,8 @@ class BeamWorkload:
     Inputs only, like ``Workload``: which blocks are shared, copied or taken
     is decided by the pool under test.  Recipe: ``SeedSequence(seed)`` spawns
     stream 0 (the prompts' k and v), stream 1 (per-step q), stream 2 (per-step
-    k and v) and stream 3 (int8 scales of every physical block: U(3.5, 4.5) /
-    127 per (block, KV head), fixed up front because a block's scale outlives
+    k and v) and stream 3 (8-bit scales of every physical block: U(3.5, 4.5) /
+    127 (int8) or / 448 (E4M3) per (block, KV head), fixed up front because a block's scale outlives
     the sequence that first fills it).  Values are N(0, 1) rounded to bf16.
     Sequence ``p * beams + j`` is beam j of parent p."""
 
@@ -303,7 +314,8 @@ class BeamWorkload:
         self.step_k = to_bf16_bits(st[2].standard_normal((steps, n) + kv, np.float32))
         self.step_v = to_bf16_bits(st[2].standard_normal((steps, n) + kv, np.float32))
         sc = st[3].uniform(3.5, 4.5, size=(2, num_blocks, num_kv_heads)).astype(np.float32)
-        self.k_scale, self.v_scale = sc[0] / np.float32(127), sc[1] / np.float32(127)
+        top = np.float32(CODE_MAX.get(kv_dtype, 127.0))
+        self.k_scale, self.v_scale = sc[0] / top, sc[1] / top
 
     @property
     def num_seqs(self) -> int:
@@ -318,6 +330,8 @@ class BeamWorkload:
         shape = (self.num_blocks, self.block_size, self.num_kv_heads, self.head_dim)
         if self.kv_dtype == "int8":
             return np.full(shape, INT8_POISON, np.int8)
+        if self.kv_dtype == "fp8":
+            return np.full(shape, FP8_NAN, np.uint8)
         return np.full(shape, BF16_NAN, np.uint16)
 
     def dense_tokens(self, seq: int, step: int):
