@@ -17,7 +17,8 @@ Contents, each citing the passage it follows (page titles as printed):
   Copy-on-Write: reference counts, copy before writing a shared block);
 * ``copy_blocks`` -- the block copy of copy-on-write (plain numpy);
 * ``token_slots``, ``append_bf16``, ``append_int8``, ``quantize_int8``,
-  ``append_fp8``, ``quantize_fp8``, ``fp8_value``,
+  ``append_fp8``, ``quantize_fp8``, ``fp8_value``, ``paged_attention_multi``
+  (multi-token causal queries),
   ``paged_attention`` (three-pass or online), ``attention_partials``,
   ``lse_merge`` -- thin ctypes wrappers over ``pagedkv_oracle.c`` (plain C,
   fp64), whose header cites the passages it follows.
@@ -87,6 +88,8 @@ def _bind(lib):
                                            I, I, I, I, D, P, I, I, I]
     lib.oracle_attention_partials.argtypes = [P, P, P, P, P, P, P, I, P, I, P,
                                               I, I, I, I, I, I, D, I, I, I]
+    lib.oracle_paged_attention_multi.argtypes = [P, P, P, P, P, P, I, P, I, P, P, I, I, I, I,
+                                                 I, I, I, D, I, I]
     lib.oracle_lse_merge.argtypes = [P, P, I, I, P]
     lib.oracle_lse_merge.restype = None
     return lib
@@ -372,6 +375,35 @@ def paged_attention(q, k_cache, v_cache, block_tables, seq_lens, scale, *,
         float(scale), _ptr(r), n, m, int(threads))
     if r is None:
         out = out.reshape(B, Hq, d)
+    return out, rc
+
+
+def paged_attention_multi(q, k_cache, v_cache, block_tables, seq_lens, query_start, scale, *,
+                          k_scale=None, v_scale=None, mode="three_pass", threads=1):
+    """fp64 attention of multi-token queries: q bf16 bits [T, Hq, d], the
+    query tokens of sequence b being rows query_start[b] .. query_start[b+1]-1,
+    the last of its seq_lens[b] tokens, each attending causally up to its own
+    position.  Returns (out fp64 [T, Hq, d], status)."""
+    lib = _load()
+    q = _c(q, np.uint16)
+    T, Hq, d = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    assert d2 == d and v_cache.shape == k_cache.shape
+    kind = _kv_kind(k_cache)
+    if kind:
+        k_scale, v_scale = _c(k_scale, np.float32), _c(v_scale, np.float32)
+    kc, vc = np.ascontiguousarray(k_cache), np.ascontiguousarray(v_cache)
+    bt, sl = _c(block_tables, np.int32), _c(seq_lens, np.int32)
+    qs = _c(query_start, np.int32)
+    B = sl.shape[0]
+    assert qs.shape == (B + 1,)
+    out = np.zeros((T, Hq, d), np.float64)
+    m = {"three_pass": 0, "online": 1}[mode]
+    rc = lib.oracle_paged_attention_multi(
+        _ptr(out), _ptr(q), _ptr(kc), _ptr(vc),
+        _ptr(k_scale) if kind else None, _ptr(v_scale) if kind else None,
+        kind, _ptr(bt), bt.shape[1], _ptr(sl), _ptr(qs), B, T, Hq, hkv, d, nb, bs,
+        float(scale), m, int(threads))
     return out, rc
 
 

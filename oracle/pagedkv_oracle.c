@@ -279,6 +279,12 @@ typedef struct {
     const int32_t *seq_lens;     /* [batch], including the appended token */
     int batch, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size;
     double scale;
+    /* Multi-token queries (NULL for one query token per sequence): the
+     * query tokens of sequence b are q rows query_start[b] ..
+     * query_start[b + 1] - 1, the last n_b = query_start[b + 1] -
+     * query_start[b] tokens of the sequence, in order. */
+    const int32_t *query_start;  /* [batch + 1] */
+    int num_tokens;
 } attn_problem;
 
 /* Value of element e of the token at logical position t of sequence b, KV
@@ -319,12 +325,12 @@ static int check_sequence(const attn_problem *P, int b)
     return OR_OK;
 }
 
-/* Gather the L tokens of sequence b, KV head hk, into contiguous fp64
+/* Gather the first L tokens of sequence b, KV head hk, into contiguous fp64
  * K[L][d] and V[L][d]: token t lives in physical block
  * block_tables[b][t / bs], row t % bs. */
-static void gather_kv(const attn_problem *P, int b, int hk, double *K, double *V)
+static void gather_kv(const attn_problem *P, int b, int hk, int L, double *K, double *V)
 {
-    int L = P->seq_lens[b], d = P->head_dim, bs = P->block_size;
+    int d = P->head_dim, bs = P->block_size;
     for (int t = 0; t < L; ++t) {
         int32_t block = P->block_tables[(int64_t)b * P->max_blocks + t / bs];
         for (int e = 0; e < d; ++e) {
@@ -334,11 +340,12 @@ static void gather_kv(const attn_problem *P, int b, int hk, double *K, double *V
     }
 }
 
-/* s_t = scale * sum_e q_e K_t,e for every gathered token. */
-static void scores(const attn_problem *P, int b, int h, const double *K, double *s)
+/* s_t = scale * sum_e q_e K_t,e for the first L gathered tokens, q being
+ * row qrow of the query tensor [rows, d]. */
+static void scores(const attn_problem *P, int64_t qrow, int L, const double *K, double *s)
 {
-    int L = P->seq_lens[b], d = P->head_dim;
-    const uint16_t *q = P->q + ((int64_t)b * P->num_q_heads + h) * d;
+    int d = P->head_dim;
+    const uint16_t *q = P->q + qrow * d;
     for (int t = 0; t < L; ++t) {
         double acc = 0.0;
         for (int e = 0; e < d; ++e)
@@ -347,15 +354,16 @@ static void scores(const attn_problem *P, int b, int h, const double *K, double 
     }
 }
 
-/* Three-pass safe softmax attention for query row (b, h):
+/* Three-pass safe softmax attention for query row qrow over the first L
+ * tokens:
  *   pass 1: m = max_t s_t
  *   pass 2: Z = sum_t exp(s_t - m)
  *   pass 3: o = sum_t exp(s_t - m) / Z * V_t                           */
-static void three_pass_row(const attn_problem *P, int b, int h, const double *K,
+static void three_pass_row(const attn_problem *P, int64_t qrow, int L, const double *K,
                            const double *V, double *s, double *o)
 {
-    int L = P->seq_lens[b], d = P->head_dim;
-    scores(P, b, h, K, s);
+    int d = P->head_dim;
+    scores(P, qrow, L, K, s);
     double m = -INFINITY;
     for (int t = 0; t < L; ++t)
         if (s[t] > m)
@@ -380,11 +388,11 @@ static void three_pass_row(const attn_problem *P, int b, int h, const double *K,
  *           + sum exp(S_j - m_new) V_j / l_new
  * with m = -inf, l = 0, O = 0 before the first block, and the chunk S_j being
  * one block of block_size tokens (the last one ragged). */
-static void online_row(const attn_problem *P, int b, int h, const double *K,
+static void online_row(const attn_problem *P, int64_t qrow, int L, const double *K,
                        const double *V, double *s, double *o)
 {
-    int L = P->seq_lens[b], d = P->head_dim, bs = P->block_size;
-    scores(P, b, h, K, s);
+    int d = P->head_dim, bs = P->block_size;
+    scores(P, qrow, L, K, s);
     double m_old = -INFINITY, l_old = 0.0;
     for (int e = 0; e < d; ++e)
         o[e] = 0.0;
@@ -424,7 +432,7 @@ static void partial_row(const attn_problem *P, int b, int h, const double *K,
                         double *acc)
 {
     int L = P->seq_lens[b], d = P->head_dim;
-    scores(P, b, h, K, s);
+    scores(P, (int64_t)b * P->num_q_heads + h, L, K, s);
     int np = (L + part - 1) / part;
     for (int i = 0; i < np; ++i) {
         int t0 = i * part, t1 = (i + 1) * part < L ? (i + 1) * part : L;
@@ -464,6 +472,32 @@ typedef struct {
     pthread_mutex_t lock;
 } row_job;
 
+/* Multi-token queries: the sequence b of query token j (query_start[b] <= j <
+ * query_start[b + 1]) and the number of tokens it attends: with n_b query
+ * tokens, token i = j - query_start[b] sits at position L_b - n_b + i and
+ * attends positions 0 .. L_b - n_b + i (causal: its own and the earlier ones).
+ * OR_INDEX when the offsets are not non-decreasing from 0 to num_tokens or
+ * n_b exceeds L_b. */
+static int multi_token_row(const attn_problem *P, int j, int *b_out, int *L_out)
+{
+    const int32_t *qs = P->query_start;
+    if (qs[0] != 0 || qs[P->batch] != P->num_tokens || j < 0 || j >= P->num_tokens)
+        return OR_INDEX;
+    for (int b = 0; b < P->batch; ++b) {
+        if (qs[b + 1] < qs[b])
+            return OR_INDEX;
+        if (j < qs[b + 1]) {
+            int n = qs[b + 1] - qs[b], L = P->seq_lens[b];
+            if (n > L)
+                return OR_INDEX;
+            *b_out = b;
+            *L_out = L - n + (j - qs[b]) + 1;
+            return OR_OK;
+        }
+    }
+    return OR_INDEX;
+}
+
 static int take_row(row_job *J)
 {
     pthread_mutex_lock(&J->lock);
@@ -482,13 +516,33 @@ static void *row_worker(void *arg)
     double *V = (double *)malloc((size_t)cap * d * sizeof(double));
     double *s = (double *)malloc((size_t)cap * sizeof(double));
     for (int r; (r = take_row(J)) >= 0;) {
-        int b, h;
-        if (J->rows) {
-            b = J->rows[2 * r];
-            h = J->rows[2 * r + 1];
-        } else {
-            b = r / P->num_q_heads;
+        /* The row's sequence b, query head h, query-tensor row and the
+         * number of tokens it attends (L_b, or pos + 1 for a multi-token
+         * query at position pos). */
+        int b = -1, h, L = 0;
+        int64_t qrow = 0;
+        if (P->query_start) {
+            int j = r / P->num_q_heads;
             h = r % P->num_q_heads;
+            int ok = 0;
+            if (multi_token_row(P, j, &b, &L) == OR_OK) {
+                qrow = (int64_t)j * P->num_q_heads + h;
+                ok = 1;
+            }
+            if (!ok)
+                b = -1;
+        } else {
+            if (J->rows) {
+                b = J->rows[2 * r];
+                h = J->rows[2 * r + 1];
+            } else {
+                b = r / P->num_q_heads;
+                h = r % P->num_q_heads;
+            }
+            if (b >= 0 && b < P->batch) {
+                L = P->seq_lens[b];
+                qrow = (int64_t)b * P->num_q_heads + h;
+            }
         }
         double *o = J->out + (int64_t)r * d;
         if (b < 0 || b >= P->batch || h < 0 || h >= P->num_q_heads ||
@@ -501,16 +555,32 @@ static void *row_worker(void *arg)
             continue;
         }
         int hk = h / (P->num_q_heads / P->num_kv_heads);
-        gather_kv(P, b, hk, K, V);
+        gather_kv(P, b, hk, L, K, V);
         if (J->mode == MODE_ONLINE)
-            online_row(P, b, h, K, V, s, o);
+            online_row(P, qrow, L, K, V, s, o);
         else
-            three_pass_row(P, b, h, K, V, s, o);
+            three_pass_row(P, qrow, L, K, V, s, o);
     }
     free(K);
     free(V);
     free(s);
     return NULL;
+}
+
+static int run_job(attn_problem *P, const int32_t *rows, int n_rows, int mode,
+                   double *out, int num_threads);
+
+/* Listed rows (pairs (b, h)), or every (b, h) when rows is NULL. */
+static int run_rows(attn_problem *P, const int32_t *rows, int n_rows, int mode,
+                    double *out, int num_threads)
+{
+    return run_job(P, rows, rows ? n_rows : P->batch * P->num_q_heads, mode, out, num_threads);
+}
+
+/* Every (query token, head) row of a multi-token problem. */
+static int run_rows_n(attn_problem *P, int n_rows, int mode, double *out, int num_threads)
+{
+    return run_job(P, NULL, n_rows, mode, out, num_threads);
 }
 
 static int valid_problem(const attn_problem *P)
@@ -526,15 +596,15 @@ static int valid_problem(const attn_problem *P)
     return 1;
 }
 
-static int run_rows(attn_problem *P, const int32_t *rows, int n_rows, int mode,
-                    double *out, int num_threads)
+static int run_job(attn_problem *P, const int32_t *rows, int n_rows, int mode,
+                   double *out, int num_threads)
 {
     if (!valid_problem(P) || !out)
         return OR_INVALID;
     row_job J;
     J.P = P;
     J.rows = rows;
-    J.n_rows = rows ? n_rows : P->batch * P->num_q_heads;
+    J.n_rows = n_rows;
     J.mode = mode;
     J.out = out;
     J.next = 0;
@@ -567,7 +637,7 @@ int oracle_paged_attention(double *out, const uint16_t *q, const void *k_cache,
     attn_problem P = {q, k_cache, v_cache, k_scale, v_scale, kv_kind,
                       block_tables, max_blocks_per_seq, seq_lens, batch,
                       num_q_heads, num_kv_heads, head_dim, num_blocks,
-                      block_size, scale};
+                      block_size, scale, NULL, 0};
     return run_rows(&P, rows, n_rows, mode, out, num_threads);
 }
 
@@ -586,7 +656,7 @@ int oracle_attention_partials(double *ml, double *acc, const uint16_t *q,
     attn_problem P = {q, k_cache, v_cache, k_scale, v_scale, kv_kind,
                       block_tables, max_blocks_per_seq, seq_lens, batch,
                       num_q_heads, num_kv_heads, head_dim, num_blocks,
-                      block_size, scale};
+                      block_size, scale, NULL, 0};
     if (!valid_problem(&P) || part <= 0 || b < 0 || b >= batch || h < 0 ||
         h >= num_q_heads)
         return -OR_INVALID;
@@ -596,7 +666,7 @@ int oracle_attention_partials(double *ml, double *acc, const uint16_t *q,
     double *K = (double *)malloc((size_t)L * d * sizeof(double));
     double *V = (double *)malloc((size_t)L * d * sizeof(double));
     double *s = (double *)malloc((size_t)L * sizeof(double));
-    gather_kv(&P, b, h / (num_q_heads / num_kv_heads), K, V);
+    gather_kv(&P, b, h / (num_q_heads / num_kv_heads), seq_lens[b], K, V);
     partial_row(&P, b, h, K, V, s, part, ml, acc);
     free(K);
     free(V);
@@ -624,4 +694,31 @@ void oracle_lse_merge(const double *ml, const double *acc, int np, int head_dim,
     }
     for (int e = 0; e < head_dim; ++e)
         out[e] /= den;
+}
+
+/* Attention of multi-token queries (speculative verification, chunked
+ * prefill: “让 Agent 跑得快”, §六 投机解码 -- the target model scores the
+ * gamma draft tokens in one parallel pass instead of gamma decode steps).
+ * Sequence b has n_b = query_start[b + 1] - query_start[b] query tokens,
+ * already appended, the last n_b of its seq_lens[b] tokens; query token i
+ * (q row query_start[b] + i) at position L_b - n_b + i attends, causally,
+ * positions 0 .. L_b - n_b + i.  q: bf16 [num_tokens, Hq, d]; out fp64
+ * [num_tokens, Hq, d], rows of bad sequences (length, table, offsets)
+ * zeroed with return value OR_INDEX.  mode as for oracle_paged_attention. */
+int oracle_paged_attention_multi(double *out, const uint16_t *q, const void *k_cache,
+                                 const void *v_cache, const float *k_scale,
+                                 const float *v_scale, int kv_kind,
+                                 const int32_t *block_tables, int max_blocks_per_seq,
+                                 const int32_t *seq_lens, const int32_t *query_start,
+                                 int batch, int num_tokens, int num_q_heads,
+                                 int num_kv_heads, int head_dim, int num_blocks,
+                                 int block_size, double scale, int mode, int num_threads)
+{
+    if (!query_start || num_tokens < 0)
+        return OR_INVALID;
+    attn_problem P = {q, k_cache, v_cache, k_scale, v_scale, kv_kind,
+                      block_tables, max_blocks_per_seq, seq_lens, batch,
+                      num_q_heads, num_kv_heads, head_dim, num_blocks,
+                      block_size, scale, query_start, num_tokens};
+    return run_rows_n(&P, num_tokens * num_q_heads, mode, out, num_threads);
 }

@@ -27,12 +27,13 @@ def oracle_pool(wl, seqs=None, with_new_token=True):
         rc = append_any(ch.k, ch.v, kc, vc, ks, vs, slots)
         assert rc == 0
     if with_new_token:
-        b_all = np.arange(s.batch) if seqs is None else np.asarray(list(seqs))
-        slots, rc = decode_slots(wl)
+        seq, pos = wl.new_positions()
+        slots, rc = oracle.token_slots(wl.block_tables, pos, s.block_size, wl.num_blocks,
+                                       seq_idx=seq)
         assert rc == 0
-        sel = np.full(s.batch, -1, np.int64)
-        sel[b_all] = slots[b_all]
-        rc = append_any(wl.new_k, wl.new_v, kc, vc, ks, vs, sel)
+        if seqs is not None:
+            slots[~np.isin(seq, np.asarray(list(seqs)))] = -1
+        rc = append_any(wl.new_k, wl.new_v, kc, vc, ks, vs, slots)
         assert rc == 0
     return kc, vc, ks, vs
 
@@ -64,8 +65,9 @@ def contiguous_kv(wl, b):
         parts_k.append(bf16_bits_to_f32(pk))
         parts_v.append(bf16_bits_to_f32(pv))
     _, k, v = wl.own_tokens(b)
-    parts_k += [bf16_bits_to_f32(k), bf16_bits_to_f32(wl.new_k[b:b + 1])]
-    parts_v += [bf16_bits_to_f32(v), bf16_bits_to_f32(wl.new_v[b:b + 1])]
+    nk, nv = wl.new_kv_of(b)
+    parts_k += [bf16_bits_to_f32(k), bf16_bits_to_f32(nk)]
+    parts_v += [bf16_bits_to_f32(v), bf16_bits_to_f32(nv)]
     return (np.concatenate(parts_k).astype(np.float64),
             np.concatenate(parts_v).astype(np.float64))
 

@@ -11,6 +11,7 @@ import oracle
 from test_oracle_append import check_fp32_decision, check_rounding
 from test_oracle_attention import check_against_sdpa, check_int8_against_sdpa, small
 from test_oracle_fp8 import check_decode, check_encode, check_fp8_against_sdpa, check_saturation
+from test_oracle_multi import check_multi_against_sdpa, multi
 
 
 def _sdpa():
@@ -29,6 +30,10 @@ def _fp8_codes():
     check_decode(oracle.fp8_value)
     check_encode(oracle.quantize_fp8)
     check_saturation(oracle.quantize_fp8)
+
+
+def _multi():
+    check_multi_against_sdpa(multi([1, 5, 17, 40, 100, 250], [1, 5, 3, 40, 7, 64], hq=8, hkv=2, d=64))
 
 
 def _rounding():
@@ -62,6 +67,12 @@ MUTANTS = {
     "fp8_subnormal_exponent": ("ldexp(m / 8.0, -6)", "ldexp(m / 8.0, -7)", _fp8_codes),
     "fp8_no_saturation": ("        return sign | 0x7E;", "        return 0x7F;", _fp8_codes),
     "fp8_sign_dropped": ("    return sign | (uint8_t)best;", "    return (uint8_t)best;", _fp8_codes),
+    "multi_excludes_own_token": ("*L_out = L - n + (j - qs[b]) + 1;", "*L_out = L - n + (j - qs[b]);",
+                                 _multi),
+    "multi_sees_one_more": ("*L_out = L - n + (j - qs[b]) + 1;",
+                            "*L_out = L - n + (j - qs[b]) + 1 + (j - qs[b] + 1 < n);", _multi),
+    "multi_query_row_of_sequence": ("qrow = (int64_t)j * P->num_q_heads + h;",
+                                    "qrow = (int64_t)b * P->num_q_heads + h;", _multi),
     "round_half_away": ("float r = nearbyintf(x / s);", "float r = roundf(x / s);", _rounding),
     "fp64_decision": ("float r = nearbyintf(x / s);",
                       "float r = (float)nearbyint((double)x / (double)s);", _fp32),

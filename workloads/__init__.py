@@ -20,6 +20,10 @@ shared 800-token system prompt; 16-token blocks, 32 for the int8 case):
   5 70B-like INT8  B 128, 64/8 heads, d 128, bs 32, L ~ U{1024..8192},
                    int8 pool, scale = max|x| / 127 per (block, KV head)
   6 70B-like FP8   as 5 with an FP8 E4M3 pool, scale = max|x| / 448
+  7 spec. verify   as 2, the last 5 tokens of each sequence are queries
+                   (the gamma = 5 draft tokens scored in one pass)
+  8 decode-max     as 2, sequence 0's last 512 tokens are a prefill chunk,
+                   the other 63 sequences decode one token
 
 Recipe: ``numpy.random.Generator(PCG64)`` streams spawned from
 ``SeedSequence(20260000 + config)``: stream 0 draws lengths then placement,
@@ -28,7 +32,10 @@ and stream 4 + b the cached tokens of sequence b (so one sequence can be
 regenerated alone).  Values are N(0, 1) in fp32 rounded to the nearest-even
 bf16.  The pool holds ceil(1.25 x needed blocks) unless the config fixes it;
 placement is a seeded random permutation of the pool, each sequence taking
-the next ``ceil(L_b / bs)`` entries.  Unused pool memory starts poisoned
+the next ``ceil(L_b / bs)`` entries.  With query_len n_b > 1 the last n_b
+tokens of sequence b are this step's queries and appended tokens (q and the
+new k, v have one row per query token, sequences in order); its cached
+tokens are positions ``0 .. L_b - n_b - 1``.  Unused pool memory starts poisoned
 (bf16 NaN, int8 127, E4M3 NaN 0x7F) and table padding is -1.  ``L_b`` counts the token
 appended in this step; cached tokens are positions ``0 .. L_b - 2``.
 """
@@ -72,6 +79,8 @@ class Spec:
     num_blocks: Optional[int] = None   # None: ceil(1.25 * needed)
     max_blocks_per_seq: Optional[int] = None
     shared_prefix_tokens: int = 0
+    query_len: object = 1              # query tokens per sequence: an int, or
+                                       # ("chunk_first", n): sequence 0 has n, the rest 1
 
     @property
     def scale(self) -> float:
@@ -97,6 +106,14 @@ CONFIGS = {
     6: Spec("Llama-2-70B-like FP8 E4M3 KV (B128, 64/8 heads, d128, bs32, L 1024..8192)",
             128, 64, 8, 128, 32, "fp8", ("uniform", 1024, 8192),
             max_blocks_per_seq=256),
+    7: Spec("speculative verification, 5 draft tokens per sequence (B64, 32/8 heads, d128, "
+            "bs16, L 512..4096)",
+            64, 32, 8, 128, 16, "bf16", ("uniform", 512, 4096),
+            max_blocks_per_seq=256, query_len=5),
+    8: Spec("decode-maximal batch: one 512-token prefill chunk + 63 decodes (B64, 32/8 heads, "
+            "d128, bs16, L 512..4096)",
+            64, 32, 8, 128, 16, "bf16", ("uniform", 512, 4096),
+            max_blocks_per_seq=256, query_len=("chunk_first", 512)),
 }
 
 
@@ -113,7 +130,8 @@ class FillChunk:
 class Workload:
     """One synthetic decode step."""
 
-    def __init__(self, spec: Spec, seed: int, seq_lens: Optional[Sequence[int]] = None):
+    def __init__(self, spec: Spec, seed: int, seq_lens: Optional[Sequence[int]] = None,
+                 query_lens: Optional[Sequence[int]] = None):
         self.spec = spec
         self.seed = seed
         ss = np.random.SeedSequence(seed)
@@ -152,10 +170,23 @@ class Workload:
             nxt += own
         assert nxt <= NB
         self.block_tables = bt
+        # query tokens: the last n_b tokens of sequence b (n_b = 1: decode)
+        if query_lens is not None:
+            n = np.asarray(query_lens, np.int64)
+        elif isinstance(spec.query_len, tuple):
+            assert spec.query_len[0] == "chunk_first"
+            n = np.ones(B, np.int64)
+            n[0] = spec.query_len[1]
+        else:
+            n = np.full(B, spec.query_len, np.int64)
+        assert n.shape == (B,) and (n >= 1).all() and (n <= self.seq_lens).all()
+        self.query_lens = n.astype(np.int32)
+        self.query_start = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+        T = int(self.query_start[-1])
         s1 = np.random.Generator(np.random.PCG64(self._children[1]))
-        self.q = to_bf16_bits(s1.standard_normal((B, spec.num_q_heads, spec.head_dim), np.float32))
+        self.q = to_bf16_bits(s1.standard_normal((T, spec.num_q_heads, spec.head_dim), np.float32))
         s2 = np.random.Generator(np.random.PCG64(self._children[2]))
-        shp = (B, spec.num_kv_heads, spec.head_dim)
+        shp = (T, spec.num_kv_heads, spec.head_dim)
         self.new_k = to_bf16_bits(s2.standard_normal(shp, np.float32))
         self.new_v = to_bf16_bits(s2.standard_normal(shp, np.float32))
         self._prefix = None
@@ -192,12 +223,31 @@ class Workload:
                             to_bf16_bits(g.standard_normal(shp, np.float32)))
         return self._prefix
 
+    @property
+    def num_tokens(self) -> int:
+        """Query tokens of the step (= batch for one-token decode)."""
+        return int(self.query_start[-1])
+
+    def new_kv_of(self, b: int):
+        """bf16 bits of the K, V rows sequence b appends this step."""
+        a, e = int(self.query_start[b]), int(self.query_start[b + 1])
+        return self.new_k[a:e], self.new_v[a:e]
+
+    def new_positions(self):
+        """(sequence, position) int32 [T] of every token appended this step:
+        the last n_b positions of sequence b."""
+        seq = np.repeat(np.arange(self.spec.batch, dtype=np.int32), self.query_lens)
+        first = np.repeat(self.seq_lens - self.query_lens, self.query_lens)
+        off = np.arange(self.num_tokens, dtype=np.int32) - np.repeat(self.query_start[:-1], self.query_lens)
+        return seq, (first + off).astype(np.int32)
+
     def own_tokens(self, b: int):
         """Cached tokens that sequence b alone owns: (positions, k, v)."""
         s = self.spec
         P = s.shared_prefix_tokens
         L = int(self.seq_lens[b])
-        lo, hi = min(P, L - 1), L - 1
+        hi = L - int(self.query_lens[b])
+        lo = min(P, hi)
         n = max(hi - lo, 0)
         g = self._stream(1 + b)
         shp = (n, s.num_kv_heads, s.head_dim)
@@ -235,8 +285,9 @@ class Workload:
         for b in seqs:
             L = int(self.seq_lens[b])
             pos, k, v = self.own_tokens(b)
-            kf = np.concatenate([bf16_bits_to_f32(k), bf16_bits_to_f32(self.new_k[b:b + 1])])
-            vf = np.concatenate([bf16_bits_to_f32(v), bf16_bits_to_f32(self.new_v[b:b + 1])])
+            nk, nv = self.new_kv_of(b)
+            kf = np.concatenate([bf16_bits_to_f32(k), bf16_bits_to_f32(nk)])
+            vf = np.concatenate([bf16_bits_to_f32(v), bf16_bits_to_f32(nv)])
             nblk = (L + bs - 1) // bs
             pad = nblk * bs - L
             kf = np.abs(np.concatenate([kf, np.zeros((pad,) + kf.shape[1:], np.float32)]))
@@ -269,13 +320,14 @@ def make(config: int, seed: Optional[int] = None, seq_lens=None) -> Workload:
 
 def custom(*, batch, num_q_heads, num_kv_heads, head_dim, block_size, seq_lens,
            kv_dtype="bf16", num_blocks=None, max_blocks_per_seq=None,
-           shared_prefix_tokens=0, seed=1234) -> Workload:
-    """A small workload with explicit lengths (tests: edge cases)."""
+           shared_prefix_tokens=0, seed=1234, query_lens=None) -> Workload:
+    """A small workload with explicit lengths (tests: edge cases); with
+    query_lens, each sequence's last query_lens[b] tokens are its queries."""
     spec = Spec("custom", batch, num_q_heads, num_kv_heads, head_dim, block_size,
                 kv_dtype, ("fixed",), num_blocks=num_blocks,
                 max_blocks_per_seq=max_blocks_per_seq,
                 shared_prefix_tokens=shared_prefix_tokens)
-    return Workload(spec, seed, seq_lens=seq_lens)
+    return Workload(spec, seed, seq_lens=seq_lens, query_lens=query_lens)
 
 
 class BeamWorkload:
