@@ -388,6 +388,55 @@ kv_status paged_attention_decode_noalloc(void *out, const void *q,
                                          void *stream);
 
 /* ------------------------------------------------------------------------ */
+/* Multi-token queries                                                      */
+/* ------------------------------------------------------------------------ */
+
+/* Workspace bytes paged_attention_multi may need (an upper bound over every
+ * partition size the library picks; 0 when every query fits one). */
+size_t pagedkv_multi_workspace_bytes(int num_tokens, int num_q_heads,
+                                     int head_dim, int max_seq_len,
+                                     int block_size);
+
+/* Attention of several query tokens per sequence over the paged pool, causal
+ * within each sequence: speculative verification (“让 Agent 跑得快”, §六 投机
+ * 解码: the target model scores the gamma draft tokens in one parallel pass)
+ * and chunked prefill batched with decodes (“LLM 推理优化技术全景”, SARATHI:
+ * 512-token prefill chunks plus decodes in one batch).  Sequence b has n_b =
+ * query_start[b + 1] - query_start[b] query tokens, q rows query_start[b] ..
+ * query_start[b + 1] - 1, which are its LAST n_b tokens and are already in
+ * the pool (append them first with pagedkv_token_slot_mapping +
+ * reshape_and_cache).  Query token i of sequence b sits at position
+ * seq_lens[b] - n_b + i and attends positions 0 .. seq_lens[b] - n_b + i:
+ *   out[j, h, :] = softmax_t(scale * q[j, h, :] . K_t) . V_t.
+ *   out           device bf16 [num_tokens, num_q_heads, head_dim]
+ *   q             device bf16 [num_tokens, num_q_heads, head_dim]
+ *   k_cache, v_cache   bf16 pools as for paged_attention_decode
+ *                 (8-bit pools return KV_ERR_NOT_IMPLEMENTED; scales NULL)
+ *   block_tables, max_blocks_per_seq, seq_lens, batch  as for
+ *                 paged_attention_decode (seq_lens counts the query tokens)
+ *   query_start   device int32 [batch + 1], non-decreasing from 0 to
+ *                 num_tokens (n_b = 0 is allowed: no queries)
+ *   max_seq_len   host bound on every seq_lens[b]
+ *   workspace     at least pagedkv_multi_workspace_bytes(...) bytes,
+ *                 16-byte aligned (may be NULL when that size is 0)
+ * A sequence with a bad length (n_b > seq_lens[b], beyond the table or the
+ * hint) or a bad table entry has its rows zeroed and sets
+ * PAGEDKV_FLAG_BAD_SEQ_LEN or PAGEDKV_FLAG_BAD_BLOCK; offsets outside
+ * [0, num_tokens] leave that sequence's rows unwritten and set
+ * PAGEDKV_FLAG_BAD_SEQ_LEN.  Asynchronous on `stream`: one attention launch,
+ * plus a log-sum-exp merge launch when the keys are split into partitions. */
+kv_status paged_attention_multi(void *out, const void *q, const void *k_cache,
+                                const void *v_cache, const float *k_scale,
+                                const float *v_scale, const int32_t *block_tables,
+                                int max_blocks_per_seq, const int32_t *seq_lens,
+                                const int32_t *query_start, int batch,
+                                int num_tokens, int num_q_heads, int num_kv_heads,
+                                int head_dim, int num_blocks, int block_size,
+                                int max_seq_len, float scale, kv_dtype dtype,
+                                void *workspace, size_t workspace_bytes,
+                                void *stream);
+
+/* ------------------------------------------------------------------------ */
 /* Status                                                                   */
 /* ------------------------------------------------------------------------ */
 

@@ -38,6 +38,9 @@ SIGNATURES = {
     "kv_pool_refcount": (_I, [_P, ctypes.c_int32]),
     "kv_pool_prepare_append": (_I, [_P, _P, _I, _P, _I, _P, _P]),
     "pagedkv_copy_blocks": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "pagedkv_multi_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "paged_attention_multi": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I,
+                                   _I, _I, _F, _I, _P, _SZ, _P]),
     "pagedkv_pool_tensor_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "pagedkv_slot_mapping": (_I, [_P, _I, _P, _I, _I, _I, _P, _P]),
     "pagedkv_token_slot_mapping": (_I, [_P, _I, _P, _P, _I, _I, _I, _P, _P]),
@@ -279,6 +282,39 @@ def copy_blocks(k_cache, v_cache, block_pairs, k_scale=None, v_scale=None, strea
     _check(load().pagedkv_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
                                       _ptr(block_pairs), block_pairs.shape[0], nb, bs, hkv, d, dt,
                                       _stream(stream)))
+
+
+def multi_workspace_bytes(num_tokens, num_q_heads, head_dim, max_seq_len, block_size) -> int:
+    return load().pagedkv_multi_workspace_bytes(num_tokens, num_q_heads, head_dim, max_seq_len,
+                                                block_size)
+
+
+def paged_attention_multi(out, q, k_cache, v_cache, block_tables, seq_lens, query_start,
+                          max_seq_len, scale, workspace=None, k_scale=None, v_scale=None,
+                          stream=None):
+    """Causal attention of several query tokens per sequence (the last
+    query_start[b+1] - query_start[b] tokens of sequence b, already
+    appended): q, out bf16 [T, Hq, d]."""
+    import torch
+    dt = _pool_dtype(k_cache)
+    _need(out, torch.bfloat16, "out", 3)
+    _need(q, torch.bfloat16, "q", 3)
+    _need(k_cache, k_cache.dtype, "k_cache", 4)
+    _need(v_cache, k_cache.dtype, "v_cache", 4)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _need(query_start, torch.int32, "query_start", 1)
+    nb, bs, hkv, d = k_cache.shape
+    T, hq, d2 = q.shape
+    B = seq_lens.shape[0]
+    if out.shape != q.shape or d2 != d or query_start.shape[0] != B + 1 or block_tables.shape[0] != B:
+        raise ValueError("shapes of out, q, the pools, the table, seq_lens and query_start disagree")
+    ws_ptr, ws_n = (None, 0) if workspace is None else (_ptr(workspace), workspace.numel() * workspace.element_size())
+    _check(load().paged_attention_multi(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                        _ptr(v_scale), _ptr(block_tables), block_tables.shape[1],
+                                        _ptr(seq_lens), _ptr(query_start), B, T, hq, hkv, d, nb, bs,
+                                        int(max_seq_len), float(scale), dt, ws_ptr, ws_n,
+                                        _stream(stream)))
 
 
 def workspace_bytes(batch, num_q_heads, head_dim, max_seq_len, block_size) -> int:

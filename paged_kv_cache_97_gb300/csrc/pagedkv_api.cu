@@ -280,7 +280,7 @@ static const int kMaxPartTokens = 2048;
 // measured slower on GB300 (fewer, longer CTAs leave a longer tail).  The environment
 // variable PAGEDKV_PARTITION_TOKENS (a multiple of 256, read on every call)
 // overrides it.
-static int choose_part_tokens(int batch, int num_kv_heads, int max_seq_len, int num_sms) {
+int choose_part_tokens(int batch, int num_kv_heads, int max_seq_len, int num_sms) {
   const char* s = getenv("PAGEDKV_PARTITION_TOKENS");
   const int env = s ? atoi(s) : 0;
   if (env >= kMinPartTokens && env <= kMaxPartTokens && env % kMinPartTokens == 0) return env;

@@ -62,6 +62,10 @@ struct DecodeArgs {
   int slots;                   // max_parts + prefix_chunks
   float scale_log2;            // scale * log2(e)
   kv_dtype dtype;
+  // multi-token queries: sequence b's query tokens are q rows
+  // query_start[b] .. query_start[b + 1] - 1 (its last tokens); null otherwise
+  const int32_t* query_start;  // [batch + 1]
+  int num_tokens;
 };
 
 // Workspace of one decode call: (m, l) and acc of `slots` partials per query
@@ -81,5 +85,9 @@ kv_status launch_merge(const DecodeArgs& a, cudaStream_t stream);
 // Launches the shared-prefix kernel: every sequence's query rows against the
 // prefix blocks, one partial per row and prefix chunk.
 kv_status launch_prefix(const DecodeArgs& a, cudaStream_t stream);
+
+// Token partition length for `work` independent (row group, KV head) units
+// over sequences of up to max_seq_len tokens (power of two in [256, 2048]).
+int choose_part_tokens(int work, int num_kv_heads, int max_seq_len, int num_sms);
 
 }  // namespace pagedkv

@@ -109,6 +109,40 @@ class GpuStep:
                                v_scale=self.v_scale)
         return self.out
 
+    def append_tokens(self):
+        """Append every new token of the step (several per sequence for
+        multi-token workloads) through the general slot mapping."""
+        s = self.wl.spec
+        seq, pos = self.wl.new_positions()
+        if not hasattr(self, "tok_slots"):
+            self.tok_seq = torch.from_numpy(seq).to(self.dev)
+            self.tok_pos = torch.from_numpy(pos).to(self.dev)
+            self.tok_slots = torch.empty(len(seq), dtype=torch.int64, device=self.dev)
+        pkv.token_slot_mapping(self.block_tables, self.tok_pos, self.wl.num_blocks, s.block_size,
+                               self.tok_slots, seq_idx=self.tok_seq)
+        pkv.reshape_and_cache(self.new_k, self.new_v, self.k_cache, self.v_cache, self.tok_slots,
+                              self.k_scale, self.v_scale)
+
+    def attend_multi(self):
+        """paged_attention_multi over the step's query tokens."""
+        s = self.wl.spec
+        if not hasattr(self, "query_start"):
+            self.query_start = torch.from_numpy(self.wl.query_start).to(self.dev)
+            self.out_multi = torch.empty((self.wl.num_tokens, s.num_q_heads, s.head_dim),
+                                         dtype=torch.bfloat16, device=self.dev)
+            ws = pkv.multi_workspace_bytes(self.wl.num_tokens, s.num_q_heads, s.head_dim,
+                                           self.max_seq_len, s.block_size)
+            self.ws_multi = torch.empty(max(ws, 16), dtype=torch.uint8, device=self.dev)
+        pkv.paged_attention_multi(self.out_multi, self.q, self.k_cache, self.v_cache,
+                                  self.block_tables, self.seq_lens, self.query_start,
+                                  self.max_seq_len, s.scale, self.ws_multi, self.k_scale,
+                                  self.v_scale)
+        return self.out_multi
+
+    def multi_step(self):
+        self.append_tokens()
+        return self.attend_multi()
+
     def fused_step(self):
         s = self.wl.spec
         pkv.decode_step(self.out, self.q, self.new_k, self.new_v, self.k_cache, self.v_cache,

@@ -179,7 +179,7 @@ class Workload:
             n[0] = spec.query_len[1]
         else:
             n = np.full(B, spec.query_len, np.int64)
-        assert n.shape == (B,) and (n >= 1).all() and (n <= self.seq_lens).all()
+        assert n.shape == (B,) and (n >= 0).all() and (n <= self.seq_lens).all()
         self.query_lens = n.astype(np.int32)
         self.query_start = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
         T = int(self.query_start[-1])
