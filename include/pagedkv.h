@@ -163,6 +163,44 @@ kv_status kv_pool_prepare_append(kv_pool *pool, int32_t *block_tables,
                                  int max_blocks_per_seq, const int32_t *seq_lens,
                                  int batch, int32_t *copy_pairs, int *num_copies);
 
+/* Prefix cache (“让 Agent 跑得快”, §七 前缀缓存: each full block is hashed from
+ * its parent block's hash, its tokens and optional extra keys such as a LoRA
+ * id or a cache salt; a new request looks its prompt's blocks up in order,
+ * takes a reference on each hit and prefills from the first miss; blocks a
+ * finished request frees stay findable in the free queue until reused).
+ *
+ * Hash of one full block: FNV-1a 64 (offset basis 0xcbf29ce484222325, prime
+ * 0x100000001b3; per byte h ^= byte, h *= prime) over parent_hash (8 bytes),
+ * extra_key (8 bytes) and the block_size token ids (4 bytes each, two's
+ * complement), all little-endian.  The first block's parent hash is 0. */
+uint64_t pagedkv_block_hash(uint64_t parent_hash, const int32_t *tokens,
+                            int block_size, uint64_t extra_key);
+
+/* Looks the full blocks of a prompt (host int32 tokens[num_tokens]) up in
+ * the cache, in order, stopping at the first block whose hash chain has no
+ * registered block with exactly these tokens, parent and key (so a hit
+ * implies every earlier block hit too).  Every hit block gains a reference
+ * (a cached block waiting in the free queue leaves it); their ids go to
+ * out_ids[0 .. *num_hit) (capacity num_tokens / block_size).  The caller
+ * allocates the rest and prefills from token *num_hit * block_size. */
+kv_status kv_pool_match_prefix(kv_pool *pool, const int32_t *tokens,
+                               int num_tokens, uint64_t extra_key,
+                               int32_t *out_ids, int *num_hit);
+
+/* Registers the full blocks of a sequence whose K/V are now in the pool:
+ * block_ids[j] holds tokens [j * block_size, (j + 1) * block_size) of
+ * tokens[num_tokens] (a partial last block is not registered).  A block
+ * whose content is already registered under another id stays unregistered.
+ * Registered blocks leave the cache when allocation takes them again.
+ * KV_ERR_INVALID_ARG (nothing registered) for an id that is not allocated
+ * or one already registered with a different content. */
+kv_status kv_pool_register_prefix(kv_pool *pool, const int32_t *block_ids,
+                                  const int32_t *tokens, int num_tokens,
+                                  uint64_t extra_key);
+
+/* Number of blocks the prefix cache holds (in use or free); -1 for NULL. */
+int kv_pool_cached_blocks(const kv_pool *pool);
+
 /* Bytes of one pool tensor (K or V): num_blocks * block_size * num_kv_heads
  * * head_dim * dtype_size. */
 size_t pagedkv_pool_tensor_bytes(int num_blocks, int block_size,

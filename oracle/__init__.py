@@ -16,6 +16,8 @@ Contents, each citing the passage it follows (page titles as printed):
   free returns every block) and its sharing rules (“让 Agent 跑得快”, §二
   Copy-on-Write: reference counts, copy before writing a shared block);
 * ``copy_blocks`` -- the block copy of copy-on-write (plain numpy);
+* ``fnv1a64``, ``block_hash`` -- the prefix cache's block hash chain
+  (“让 Agent 跑得快”, §七; FNV-1a from its published definition);
 * ``token_slots``, ``append_bf16``, ``append_int8``, ``quantize_int8``,
   ``append_fp8``, ``quantize_fp8``, ``fp8_value``, ``paged_attention_multi``
   (multi-token causal queries),
@@ -175,10 +177,21 @@ class BlockPoolModel:
     zero join the free list in the order listed; ``prepare_append`` handles
     the sequences of a step in order, each copy or new block taking the front
     of the free list, and changes nothing when the list runs short.
+
+    Prefix cache, “让 Agent 跑得快”, §七 (前缀缓存): a full block's hash
+    chains its parent's hash, its tokens and extra keys (``block_hash``); a
+    request looks its prompt's full blocks up in order, stopping at the first
+    miss, and takes a reference on every hit (a cached free block leaves the
+    free list); a finished request's blocks stay findable in the free list
+    until allocation takes them again, which evicts them.  Readings: a hit
+    also requires the stored tokens, parent hash and key to match; a block
+    whose content is already registered elsewhere is not registered again.
     """
     num_blocks: int
     free_list: list = field(default_factory=list)
     refs: dict = field(default_factory=dict)      # block id -> references (> 0)
+    cache: dict = field(default_factory=dict)     # block id -> (hash, parent, key, tokens)
+    by_hash: dict = field(default_factory=dict)   # hash -> block id
 
     def __post_init__(self):
         self.free_list = list(range(self.num_blocks))
@@ -191,7 +204,46 @@ class BlockPoolModel:
         ids, self.free_list = self.free_list[:n], self.free_list[n:]
         for i in ids:
             self.refs[i] = 1
+            if i in self.cache:                       # reused: its cached content goes
+                del self.by_hash[self.cache.pop(i)[0]]
         return ids
+
+    def match_prefix(self, tokens, block_size, extra_key=0) -> list:
+        hits, parent = [], 0
+        for j in range(len(tokens) // block_size):
+            blk = tuple(int(x) for x in tokens[j * block_size:(j + 1) * block_size])
+            h = block_hash(parent, blk, extra_key)
+            i = self.by_hash.get(h)
+            if i is None or self.cache[i] != (h, parent, extra_key, blk):
+                break
+            if i not in self.refs:                    # cached but free
+                self.free_list.remove(i)
+                self.refs[i] = 0
+            self.refs[i] += 1
+            hits.append(i)
+            parent = h
+        return hits
+
+    def register_prefix(self, ids, tokens, block_size, extra_key=0) -> None:
+        n = len(tokens) // block_size
+        ids = list(ids)[:n]
+        if any(i not in self.refs for i in ids):
+            raise ValueError("registering a block that is not allocated")
+        parent, plan = 0, []
+        for j, i in enumerate(ids):
+            blk = tuple(int(x) for x in tokens[j * block_size:(j + 1) * block_size])
+            h = block_hash(parent, blk, extra_key)
+            if i in self.cache and self.cache[i][0] != h:
+                raise ValueError("block already holds another prefix")
+            plan.append((i, (h, parent, extra_key, blk)))
+            parent = h
+        for i, entry in plan:
+            if i not in self.cache and entry[0] not in self.by_hash:
+                self.cache[i] = entry
+                self.by_hash[entry[0]] = i
+
+    def cached_blocks(self) -> int:
+        return len(self.by_hash)
 
     def alloc_sequence(self, seq_len: int, block_size: int) -> list:
         return self.alloc(blocks_needed(seq_len, block_size))
@@ -246,10 +298,30 @@ class BlockPoolModel:
                 trial.free([old])
                 t[j] = new
                 copies.append((old, new))
-        self.free_list, self.refs = trial.free_list, trial.refs
+        self.__dict__.update(trial.__dict__)
         for t, nt in zip(tables, new_tables):
             t[:] = nt
         return copies
+
+
+def fnv1a64(data: bytes) -> int:
+    """FNV-1a, 64-bit: start at the offset basis 0xcbf29ce484222325; for
+    every byte, xor it in, then multiply by the prime 0x100000001b3 mod 2^64."""
+    h = 0xcbf29ce484222325
+    for byte in data:
+        h ^= byte
+        h = (h * 0x100000001b3) & 0xFFFFFFFFFFFFFFFF
+    return h
+
+
+def block_hash(parent: int, tokens, extra_key: int = 0) -> int:
+    """Hash of one full block (“让 Agent 跑得快”, §七: parent block's hash +
+    the block's tokens + extra keys): FNV-1a 64 over the parent hash and the
+    key (8 bytes each) and the token ids (4 bytes each, two's complement),
+    little-endian."""
+    data = parent.to_bytes(8, "little") + extra_key.to_bytes(8, "little")
+    data += b"".join(int(t).to_bytes(4, "little", signed=True) for t in tokens)
+    return fnv1a64(data)
 
 
 def copy_blocks(k_cache, v_cache, pairs, k_scale=None, v_scale=None) -> None:

@@ -39,6 +39,10 @@ SIGNATURES = {
     "kv_pool_prepare_append": (_I, [_P, _P, _I, _P, _I, _P, _P]),
     "pagedkv_copy_blocks": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "pagedkv_multi_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "pagedkv_block_hash": (ctypes.c_uint64, [ctypes.c_uint64, _P, _I, ctypes.c_uint64]),
+    "kv_pool_match_prefix": (_I, [_P, _P, _I, ctypes.c_uint64, _P, _P]),
+    "kv_pool_register_prefix": (_I, [_P, _P, _P, _I, ctypes.c_uint64]),
+    "kv_pool_cached_blocks": (_I, [_P]),
     "paged_attention_multi": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I,
                                    _I, _I, _F, _I, _P, _SZ, _P]),
     "pagedkv_pool_tensor_bytes": (_SZ, [_I, _I, _I, _I, _I]),
@@ -148,6 +152,7 @@ class KVPool:
         _check(self._lib.kv_pool_create(num_blocks, block_size, num_kv_heads, head_dim, dtype,
                                         ctypes.byref(h)))
         self._h = h
+        self.block_size_ = block_size
 
     def close(self):
         if self._h:
@@ -183,6 +188,31 @@ class KVPool:
     def refcount(self, block_id: int) -> int:
         return self._lib.kv_pool_refcount(self._h, block_id)
 
+    def match_prefix(self, tokens, extra_key: int = 0) -> list:
+        """Ids of the cached blocks that hold the prompt's leading full
+        blocks (each gains a reference)."""
+        import numpy as np
+        tk = np.ascontiguousarray(tokens, dtype=np.int32)
+        out = np.zeros(max(len(tk) // self.block_size_, 1), np.int32)
+        n = ctypes.c_int()
+        _check(self._lib.kv_pool_match_prefix(self._h, tk.ctypes.data, len(tk), extra_key,
+                                              out.ctypes.data, ctypes.byref(n)))
+        return out[:n.value].tolist()
+
+    def register_prefix(self, block_ids, tokens, extra_key: int = 0) -> None:
+        """Register the sequence's full blocks for later prefix matches."""
+        import numpy as np
+        tk = np.ascontiguousarray(tokens, dtype=np.int32)
+        ids = np.ascontiguousarray(block_ids, dtype=np.int32)
+        if len(ids) < len(tk) // self.block_size_:
+            raise ValueError("one block id per full block of tokens is needed")
+        _check(self._lib.kv_pool_register_prefix(self._h, ids.ctypes.data if len(ids) else None,
+                                                 tk.ctypes.data if len(tk) else None, len(tk),
+                                                 extra_key))
+
+    def cached_blocks(self) -> int:
+        return self._lib.kv_pool_cached_blocks(self._h)
+
     def prepare_append(self, block_tables, seq_lens):
         """Blocks for this step's appends (host int32 numpy arrays; the table
         is updated in place).  Returns the (src, dst) copy pairs as an int32
@@ -198,6 +228,14 @@ class KVPool:
         _check(self._lib.kv_pool_prepare_append(self._h, bt.ctypes.data, bt.shape[1], sl.ctypes.data,
                                                 bt.shape[0], pairs.ctypes.data, ctypes.byref(n)))
         return pairs[:n.value].copy()
+
+
+def block_hash(parent_hash: int, tokens, extra_key: int = 0) -> int:
+    """The prefix cache's hash of one full block (FNV-1a 64 over parent,
+    key and token ids)."""
+    import numpy as np
+    tk = np.ascontiguousarray(tokens, dtype=np.int32)
+    return load().pagedkv_block_hash(parent_hash, tk.ctypes.data, len(tk), extra_key)
 
 
 def pool_tensor_bytes(num_blocks, block_size, num_kv_heads, head_dim, dtype=DTYPE_BF16) -> int:

@@ -5,6 +5,11 @@
 // “LLM 推理引擎深度解析”, §2.1 (PagedKVCache): the free list starts as every
 // block id in order, allocation takes ids from its front (all or none) and
 // finished sequences return theirs to its back.
+// “让 Agent 跑得快”, §七 (前缀缓存): a full block's hash chains its parent
+// block's hash, its tokens and optional extra keys; a new request looks its
+// prompt's blocks up in order and takes a reference on every hit (prefill
+// resumes at the first miss); freed blocks stay findable in the free queue
+// until allocation reuses them (least recently freed first).
 // “让 Agent 跑得快：LLM 推理服务”, §二 (Copy-on-Write：Beam Search 的内存优化):
 // candidate sequences forked from one prefix map the same physical blocks,
 // each holding a reference; a sequence about to write a token into a block
@@ -13,33 +18,116 @@
 // the current decode token writes, so that write is the only trigger.
 #include <cuda_runtime.h>
 
-#include <deque>
+#include <unordered_map>
 #include <vector>
 
 #include "pagedkv_common.cuh"
 
 using namespace pagedkv;
 
+namespace {
+
+// The free blocks in queue order, as an intrusive doubly linked list so that
+// a cached block can leave from the middle in O(1) when a request hits it.
+struct FreeQueue {
+  std::vector<int32_t> prev, next;  // -1 = none
+  int32_t head = -1, tail = -1;
+  size_t count = 0;
+
+  void init(int n) {
+    prev.assign(n, -1);
+    next.assign(n, -1);
+    for (int i = 0; i < n; ++i) push_back(i);
+  }
+  size_t size() const { return count; }
+  void push_back(int32_t id) {
+    prev[id] = tail;
+    next[id] = -1;
+    if (tail >= 0) next[tail] = id;
+    else head = id;
+    tail = id;
+    ++count;
+  }
+  void remove(int32_t id) {
+    if (prev[id] >= 0) next[prev[id]] = next[id];
+    else head = next[id];
+    if (next[id] >= 0) prev[next[id]] = prev[id];
+    else tail = prev[id];
+    prev[id] = next[id] = -1;
+    --count;
+  }
+  int32_t pop_front() {
+    const int32_t id = head;
+    remove(id);
+    return id;
+  }
+};
+
+// What the prefix cache knows of a registered full block.
+struct CachedBlock {
+  bool registered = false;
+  uint64_t hash = 0, parent = 0, extra_key = 0;
+  std::vector<int32_t> tokens;
+};
+
+// FNV-1a, 64-bit (offset basis 0xcbf29ce484222325, prime 0x100000001b3):
+// for every input byte, h ^= byte, then h *= prime (mod 2^64).
+constexpr uint64_t kFnvBasis = 0xcbf29ce484222325ull;
+constexpr uint64_t kFnvPrime = 0x100000001b3ull;
+
+inline uint64_t fnv_bytes(uint64_t h, uint64_t v, int nbytes) {
+  for (int i = 0; i < nbytes; ++i) {
+    h ^= (v >> (8 * i)) & 0xffu;
+    h *= kFnvPrime;
+  }
+  return h;
+}
+
+// Hash of one full block: FNV-1a over the parent hash (8 bytes), the extra
+// key (8 bytes) and the block's token ids (4 bytes each), little-endian.
+uint64_t block_hash(uint64_t parent, const int32_t* tokens, int bs, uint64_t extra_key) {
+  uint64_t h = kFnvBasis;
+  h = fnv_bytes(h, parent, 8);
+  h = fnv_bytes(h, extra_key, 8);
+  for (int i = 0; i < bs; ++i) h = fnv_bytes(h, (uint32_t)tokens[i], 4);
+  return h;
+}
+
+}  // namespace
+
 struct kv_pool {
   int num_blocks, block_size, num_kv_heads, head_dim;
   kv_dtype dtype;
-  std::deque<int32_t> free_list;  // front = next to hand out
+  FreeQueue free_list;            // front = next to hand out
   std::vector<int32_t> refs;      // references per block; 0 = free
   int used = 0;                   // blocks with refs > 0
+  std::vector<CachedBlock> cache;                    // per block
+  std::unordered_map<uint64_t, int32_t> by_hash;     // registered blocks
 };
 
 namespace {
 
-// Takes the front of the free list with one reference.
+// Drops a block's prefix-cache entry (its contents are about to change).
+void evict(kv_pool* p, int32_t id) {
+  CachedBlock& c = p->cache[id];
+  if (!c.registered) return;
+  auto it = p->by_hash.find(c.hash);
+  if (it != p->by_hash.end() && it->second == id) p->by_hash.erase(it);
+  c = CachedBlock();
+}
+
+// Takes the front of the free list with one reference (evicting whatever
+// the prefix cache still kept in that block).
 int32_t take_block(kv_pool* p) {
-  const int32_t id = p->free_list.front();
-  p->free_list.pop_front();
+  const int32_t id = p->free_list.pop_front();
+  evict(p, id);
   p->refs[id] = 1;
   ++p->used;
   return id;
 }
 
-// Drops one reference; a block left with none goes to the back of the list.
+// Drops one reference; a block left with none goes to the back of the list
+// (a registered block stays findable there until it is taken again).
 void drop_ref(kv_pool* p, int32_t id) {
   if (--p->refs[id] == 0) {
     p->free_list.push_back(id);
@@ -110,8 +198,9 @@ kv_status kv_pool_create(int num_blocks, int block_size, int num_kv_heads, int h
   p->num_kv_heads = num_kv_heads;
   p->head_dim = head_dim;
   p->dtype = dtype;
-  for (int i = 0; i < num_blocks; ++i) p->free_list.push_back(i);
+  p->free_list.init(num_blocks);
   p->refs.assign(num_blocks, 0);
+  p->cache.assign(num_blocks, CachedBlock());
   *out = p;
   return KV_OK;
 }
@@ -227,6 +316,79 @@ kv_status kv_pool_prepare_append(kv_pool* p, int32_t* block_tables, int max_bloc
   *num_copies = n;
   return KV_OK;
 }
+
+uint64_t pagedkv_block_hash(uint64_t parent_hash, const int32_t* tokens, int block_size,
+                            uint64_t extra_key) {
+  if (!tokens || block_size <= 0) return 0;
+  return block_hash(parent_hash, tokens, block_size, extra_key);
+}
+
+kv_status kv_pool_match_prefix(kv_pool* p, const int32_t* tokens, int num_tokens,
+                               uint64_t extra_key, int32_t* out_ids, int* num_hit) {
+  if (!p || num_tokens < 0 || (num_tokens > 0 && (!tokens || !out_ids)) || !num_hit)
+    return fail(KV_ERR_INVALID_ARG, "kv_pool_match_prefix: bad arguments");
+  const int bs = p->block_size;
+  int n = 0;
+  uint64_t parent = 0;
+  for (int j = 0; j < num_tokens / bs; ++j) {
+    const int32_t* tk = tokens + (int64_t)j * bs;
+    const uint64_t h = block_hash(parent, tk, bs, extra_key);
+    auto it = p->by_hash.find(h);
+    if (it == p->by_hash.end()) break;
+    const int32_t id = it->second;
+    const CachedBlock& c = p->cache[id];
+    // the stored block must really hold this content (a hash collision is a miss)
+    bool same = c.registered && c.hash == h && c.parent == parent && c.extra_key == extra_key;
+    for (int i = 0; same && i < bs; ++i) same = c.tokens[i] == tk[i];
+    if (!same) break;
+    if (p->refs[id] == 0) {          // cached but free: leave the free queue
+      p->free_list.remove(id);
+      ++p->used;
+    }
+    ++p->refs[id];
+    out_ids[n++] = id;
+    parent = h;
+  }
+  *num_hit = n;
+  return KV_OK;
+}
+
+kv_status kv_pool_register_prefix(kv_pool* p, const int32_t* block_ids, const int32_t* tokens,
+                                  int num_tokens, uint64_t extra_key) {
+  if (!p || num_tokens < 0 || (num_tokens > 0 && (!tokens || !block_ids)))
+    return fail(KV_ERR_INVALID_ARG, "kv_pool_register_prefix: bad arguments");
+  const int bs = p->block_size, nfull = num_tokens / bs;
+  for (int j = 0; j < nfull; ++j) {
+    const int32_t id = block_ids[j];
+    if (id < 0 || id >= p->num_blocks || p->refs[id] == 0)
+      return fail(KV_ERR_INVALID_ARG, "kv_pool_register_prefix: block %d is not allocated", id);
+  }
+  uint64_t parent = 0;
+  for (int j = 0; j < nfull; ++j) {
+    const int32_t id = block_ids[j];
+    const int32_t* tk = tokens + (int64_t)j * bs;
+    const uint64_t h = block_hash(parent, tk, bs, extra_key);
+    CachedBlock& c = p->cache[id];
+    if (c.registered) {
+      if (c.hash != h)
+        return fail(KV_ERR_INVALID_ARG,
+                    "kv_pool_register_prefix: block %d already holds another prefix", id);
+    } else if (p->by_hash.find(h) == p->by_hash.end()) {
+      // first block with this content: it becomes the cached copy (a later
+      // duplicate keeps its contents but is not registered)
+      c.registered = true;
+      c.hash = h;
+      c.parent = parent;
+      c.extra_key = extra_key;
+      c.tokens.assign(tk, tk + bs);
+      p->by_hash.emplace(h, id);
+    }
+    parent = h;
+  }
+  return KV_OK;
+}
+
+int kv_pool_cached_blocks(const kv_pool* p) { return p ? (int)p->by_hash.size() : -1; }
 
 size_t pagedkv_pool_tensor_bytes(int num_blocks, int block_size, int num_kv_heads, int head_dim,
                                  kv_dtype dtype) {
