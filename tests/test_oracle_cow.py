@@ -310,7 +310,8 @@ MODEL_MUTANTS = {
     "copies_private_blocks": ("if trial.refs[old] > 1:", "if trial.refs[old] >= 1:"),
     "never_copies": ("if trial.refs[old] > 1:", "if trial.refs[old] > 10 ** 6:"),
     "keeps_old_reference": ("                trial.free([old])\n", ""),
-    "fork_without_reference": ("            self.refs[i] += 1\n", "            pass\n"),
+    "fork_without_reference": ("        for i in ids:\n            self.refs[i] += 1\n",
+                               "        for i in ids:\n            pass\n"),
     "free_returns_shared_block": ("            if self.refs[i] == 0:", "            if self.refs[i] <= 1:"),
 }
 
