@@ -57,13 +57,14 @@ def algorithmic_bytes(wl) -> dict:
     s = wl.spec
     elem = wl.kv_elem_bytes
     B, hq, hkv, d, bs = s.batch, s.num_q_heads, s.num_kv_heads, s.head_dim, s.block_size
+    T = wl.num_tokens                                    # query tokens (= B for decode)
     L = wl.seq_lens.astype(np.int64)
     blocks = int(((L + bs - 1) // bs).sum())
     kv_unique = wl.kv_bytes_unique()
     scales = blocks * 2 * hkv * 4 if s.kv_dtype != "bf16" else 0
-    qo = 2 * B * hq * d * 2
+    qo = 2 * T * hq * d * 2
     table = blocks * 4 + B * 4
-    append = B * hkv * d * 2 * 2 + B * hkv * d * elem * 2 + B * 8 * 2
+    append = T * hkv * d * 2 * 2 + T * hkv * d * elem * 2 + T * 8 * 2
     attn = kv_unique + scales + qo + table
     return {"kv_logical": wl.kv_bytes_logical(), "kv_unique": kv_unique, "attention": attn,
             "step": attn + append}
@@ -370,6 +371,65 @@ def measure_config_step(config, pkv, dev, stream, peak, replays=40):
                          "algorithmic_bytes_per_step": nbytes["step"]}}
 
 
+def multi_flops(wl) -> int:
+    """Multiply-adds x 2 of S = Q.K^T and O = P.V over the attended (causal)
+    tokens: 4 * d per (query row, attended token), Hq rows per query token."""
+    s = wl.spec
+    total = 0
+    for b in range(s.batch):
+        L, n = int(wl.seq_lens[b]), int(wl.query_lens[b])
+        # query i attends L - n + i + 1 tokens
+        total += n * (L - n + 1) + n * (n - 1) // 2
+    return 4 * s.head_dim * s.num_q_heads * total
+
+
+def measure_multi(config, pkv, dev, stream, peak, replays=40):
+    """A multi-token workload's step (append of every query token through
+    the general slot mapping + paged_attention_multi), timed like the
+    headline: GRAPH_STEPS steps captured in one CUDA graph, replayed."""
+    import torch
+    from gpu_helpers import GpuStep
+    wl = workloads.make(config)
+    g = GpuStep(wl, dev=dev)
+    for _ in range(5):
+        g.multi_step()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(GRAPH_STEPS):
+            g.multi_step()
+    for _ in range(3):
+        graph.replay()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * replays)]
+    torch.cuda.synchronize(dev)
+    for i in range(replays):
+        ev[2 * i].record(stream)
+        graph.replay()
+        ev[2 * i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    st, flags = pkv.get_status()
+    assert st == 0 and flags == 0, f"device status 0x{flags:x}"
+    us = statistics.fmean(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(replays)) * 1e3 / GRAPH_STEPS
+    s = wl.spec
+    T = wl.num_tokens
+    kv = wl.kv_bytes_logical()
+    step_bytes = (kv + 2 * T * s.num_q_heads * s.head_dim * 2 + T * s.num_kv_heads * s.head_dim * 2 * 2 * 2
+                  + int(((wl.seq_lens + s.block_size - 1) // s.block_size).sum()) * 4)
+    fl = multi_flops(wl)
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tpeak = float(json.load(f)["bf16_tflops"])
+    except (OSError, ValueError, KeyError):
+        tpeak = 1900.0
+    return {"workload": s.name, "query_tokens": T, "us_per_step": round(us, 2),
+            "kv_read_gbs": round(kv / us / 1e3, 1),
+            "roofline": {"bound": "hbm", "achieved": round(step_bytes / us / 1e3, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(step_bytes / us / 1e3 / peak, 4),
+                         "algorithmic_bytes_per_step": step_bytes},
+            "tensor": {"achieved_tflops": round(fl / us / 1e6, 2), "peak_tflops": tpeak,
+                       "frac": round(fl / us / 1e6 / tpeak, 4), "flops_per_step": fl,
+                       "note": "mma.sync m16n8k16 bf16; peak = measured cuBLAS bf16 (burst)"}}
+
+
 def gpu_arm(args, rank, world, local_rank, dist):
     import torch
 
@@ -382,18 +442,22 @@ def gpu_arm(args, rank, world, local_rank, dist):
     dev = torch.device("cuda", local_rank)
     wl = workloads.make(args.config)
     g = GpuStep(wl, dev=dev)
-    use_prefix = wl.spec.shared_prefix_tokens > 0 and not args.no_shared_prefix
-    step_fn = g.prefix_step if use_prefix else g.fused_step
     s = wl.spec
+    multi = bool((wl.query_lens != 1).any())             # several query tokens per sequence
+    use_prefix = s.shared_prefix_tokens > 0 and not args.no_shared_prefix and not multi
+    step_fn = g.multi_step if multi else (g.prefix_step if use_prefix else g.fused_step)
     stream = torch.cuda.current_stream(dev)
     nbytes = algorithmic_bytes(wl)
     part = pkv.partition_tokens(s.batch, s.num_kv_heads, g.max_seq_len, s.block_size)
-    # decode (append fused) + merge, + the prefix kernel on the shared-prefix path
-    launches_per_step = (3 if use_prefix else 1 + (1 if g.max_seq_len > part else 0))
+    # decode (append fused) + merge, + the prefix kernel on the shared-prefix
+    # path; multi-token: slot mapping + append + attention (+ merge when the
+    # keys are split, counted as launched)
+    launches_per_step = (4 if multi else 3 if use_prefix else 1 + (1 if g.max_seq_len > part else 0))
 
     for _ in range(args.warmup):
         step_fn()
-        g.step()
+        if not multi:
+            g.step()
     torch.cuda.synchronize(dev)
     # GRAPH_STEPS consecutive steps captured once in a CUDA graph (each a
     # decode + merge pair), the graph replayed: the GPU work of the steps
@@ -444,9 +508,9 @@ def gpu_arm(args, rank, world, local_rank, dist):
     torch.cuda.synchronize(dev)
     for i in range(K3):
         ev3[i][0].record(stream)
-        g.append()
+        g.append_tokens() if multi else g.append()
         ev3[i][1].record(stream)
-        g.attend()
+        g.attend_multi() if multi else g.attend()
         ev3[i][2].record(stream)
     torch.cuda.synchronize(dev)
     unfused_ms = ev3[0][0].elapsed_time(ev3[-1][2]) / K3
@@ -463,8 +527,10 @@ def gpu_arm(args, rank, world, local_rank, dist):
     h_v = pin(wl.new_v.view(np.int16)).view(torch.bfloat16)
     h_bt = pin(wl.block_tables)
     h_sl = pin(wl.seq_lens)
-    h_out = torch.empty(g.out.shape, dtype=torch.bfloat16).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_bt, h_sl))
+    h_qs = pin(wl.query_start)
+    out_dev = g.out_multi if multi else g.out
+    h_out = torch.empty(out_dev.shape, dtype=torch.bfloat16).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_bt, h_sl) + ((h_qs,) if multi else ()))
     d2h = h_out.numel() * h_out.element_size()
     K2 = max(args.steps // 4, 10)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -476,8 +542,10 @@ def gpu_arm(args, rank, world, local_rank, dist):
         g.new_v.copy_(h_v, non_blocking=True)
         g.block_tables.copy_(h_bt, non_blocking=True)
         g.seq_lens.copy_(h_sl, non_blocking=True)
+        if multi:
+            g.query_start.copy_(h_qs, non_blocking=True)
         step_fn()
-        h_out.copy_(g.out, non_blocking=True)
+        h_out.copy_(out_dev, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / K2
@@ -504,9 +572,11 @@ def gpu_arm(args, rank, world, local_rank, dist):
                    "l2": "inputs larger than L2 (KV read per step > 129 MB), no flush",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm",
-                     "kernel": ("prefix_kernel + decode_kernel (append fused) + merge_kernel, one "
-                   "pagedkv_decode_step_prefix" if use_prefix else
-                   "decode_kernel (append fused) + merge_kernel, one pagedkv_decode_step"),
+                     "kernel": ("token slot mapping + append + multi_kernel (+ multi_merge_kernel), "
+                                "paged_attention_multi" if multi else
+                                "prefix_kernel + decode_kernel (append fused) + merge_kernel, one "
+                                "pagedkv_decode_step_prefix" if use_prefix else
+                                "decode_kernel (append fused) + merge_kernel, one pagedkv_decode_step"),
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": nbytes["step"],
@@ -515,7 +585,8 @@ def gpu_arm(args, rank, world, local_rank, dist):
         "eager_us_per_step": round(eager_ms * 1e3, 2),
         "unfused": {"us_per_step": round(unfused_ms * 1e3, 2),
                     "attention_us": round(attn_only_ms * 1e3, 2),
-                    "note": "slot mapping + reshape_and_cache + paged_attention_decode as three calls"},
+                    "note": ("token slot mapping + reshape_and_cache, then paged_attention_multi" if multi
+                             else "slot mapping + reshape_and_cache + paged_attention_decode as three calls")},
         "e2e": {"value": round(e2e_agg / 1e9, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
         "gpu_launches": launches_per_step * K,
@@ -523,7 +594,9 @@ def gpu_arm(args, rank, world, local_rank, dist):
     }
     if not args.no_rows:
         line["rows"] = {"cow": measure_cow(pkv, dev, stream, peak),
-                        "fp8_kv": measure_config_step(6, pkv, dev, stream, peak)}
+                        "fp8_kv": measure_config_step(6, pkv, dev, stream, peak),
+                        "multi_token": {"speculative_verification": measure_multi(7, pkv, dev, stream, peak),
+                                        "decode_maximal_batch": measure_multi(8, pkv, dev, stream, peak)}}
     return line, wl
 
 

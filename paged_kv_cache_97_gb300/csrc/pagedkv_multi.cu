@@ -10,14 +10,18 @@
 //
 // Tiling (rows on the MMA's M, as in Flash Attention v2): rows of one
 // (sequence, KV head) are (query token, grouped head) pairs, token-major; a
-// CTA of 4 warps takes 64 of them (16 per warp) and one token partition of
-// the sequence, and streams that range's blocks through a 4-stage ring of TMA
-// tensor loads, stopping at the tile's last query position.  Per 16-token
-// tile a warp computes S = Q . K^T, masks tokens past each row's position,
-// updates the online softmax, and reuses the S accumulators as the A operand
-// of O += P . V.  One partition writes the output; several write per-row
-// (m, l, acc) partials that a merge kernel combines (“LLM 推理优化技术全景”,
-// 在线 Softmax; “Flash Attention v2 的改进”).  bf16 pools.
+// CTA of 4 warps takes up to 64 of them and one token partition of the
+// sequence, and streams that range's blocks through a 4-stage ring of TMA
+// tensor loads, stopping at the tile's last query position.  The tile's
+// 16-row groups (1, 2 or 4) share the warps: with fewer than four groups,
+// the warps of a group take alternate blocks and combine their (m, l, O)
+// through shared memory at the end (speculative verification has 5 tokens x
+// 4 heads = 20 rows).  Per 16-token tile a warp computes S = Q . K^T, masks
+// tokens past each row's position, updates the online softmax, and reuses
+// the S accumulators as the A operand of O += P . V.  One partition writes
+// the output; several write per-row (m, l, acc) partials that a merge kernel
+// combines (“LLM 推理优化技术全景”, 在线 Softmax; “Flash Attention v2 的改进”).
+// bf16 pools.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -35,21 +39,36 @@ using namespace dev;
 constexpr int kMWarps = 4;
 constexpr int kMThreads = kMWarps * 32;
 constexpr int kMRows = kMWarps * 16;     // query rows per CTA
-constexpr int kMStages = 4;
+// Shared memory for the ring of stages (one block of K and V each): as many
+// stages as fit, 4 to 8, so that several blocks per CTA are in flight.
+#ifndef PAGEDKV_MULTI_STAGE_BUDGET
+#define PAGEDKV_MULTI_STAGE_BUDGET (32 * 1024)
+#endif
+template <class G>
+__host__ __device__ constexpr int multi_stages() {
+  return PAGEDKV_MULTI_STAGE_BUDGET / G::kBlockBytes > 8 ? 8
+         : PAGEDKV_MULTI_STAGE_BUDGET / G::kBlockBytes < 4 ? 4
+         : PAGEDKV_MULTI_STAGE_BUDGET / G::kBlockBytes;
+}
 
 // Row tiles of a sequence with n query tokens and GQ grouped heads.
 __device__ __forceinline__ int row_tiles(int n, int GQ) { return n > 0 ? (n * GQ + kMRows - 1) / kMRows : 0; }
 
+#ifndef PAGEDKV_MULTI_MIN_BLOCKS
+#define PAGEDKV_MULTI_MIN_BLOCKS 3
+#endif
 template <int D, int BS>
-__global__ void __launch_bounds__(kMThreads)
+__global__ void __launch_bounds__(kMThreads, PAGEDKV_MULTI_MIN_BLOCKS)
     multi_kernel(const __grid_constant__ CUtensorMap k_map,
                  const __grid_constant__ CUtensorMap v_map, const DecodeArgs a) {
   using G = Geo<D, BS, false>;
-  constexpr int S = kMStages;
+  constexpr int S = multi_stages<G>();
+  // the warps' combine parks up to 3 x (O[16][D], m[16], l[16]) in the stages
+  static_assert(3 * (16 * D + 32) * 4 <= S * G::kBlockBytes, "stage memory too small to combine");
   extern __shared__ unsigned char smem_raw[];
   __shared__ uint64_t full_bar[S], empty_bar[S];
   __shared__ int scan[kMThreads];
-  __shared__ int sh_b, sh_rt, sh_bad;
+  __shared__ int sh_b, sh_rt, sh_bad, sh_fail;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -62,6 +81,7 @@ __global__ void __launch_bounds__(kMThreads)
   if (tid == 0) {
     sh_b = -1;
     sh_bad = 0;
+    sh_fail = 0;
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_addr(&full_bar[s]), 1);
       mbar_init(smem_addr(&empty_bar[s]), kMWarps);
@@ -117,8 +137,14 @@ __global__ void __launch_bounds__(kMThreads)
   const bool len_ok = rows_ok && L > 0 && n <= L && L <= a.max_seq_len &&
                       (int64_t)L <= (int64_t)a.max_blocks_per_seq * BS;
 
-  // This warp's rows ra = r0 + g and rb = ra + 8 of the sequence's rows.
-  const int r0 = rt * kMRows + warp * 16;
+  // The tile's 16-row groups (RG of them, 1, 2 or 4) and the warps per
+  // group (W = 4 / RG), which take the blocks k with k % W == lane_i.  This
+  // warp's rows ra = r0 + g and rb = ra + 8 of the sequence's rows.
+  const int groups = (min(kMRows, rows_b - rt * kMRows) + 15) / 16;
+  const int RG = groups <= 1 ? 1 : (groups <= 2 ? 2 : 4);
+  const int W = kMWarps / RG;
+  const int grp = warp % RG, lane_i = warp / RG;
+  const int r0 = rt * kMRows + grp * 16;
   const int ra = r0 + g, rb = ra + 8;
   const bool va = len_ok && ra < rows_b, vb = len_ok && rb < rows_b;
   const int64_t qrow_a = va ? (int64_t)(q0 + ra / GQ) * Hq + hk * GQ + ra % GQ : 0;
@@ -130,6 +156,7 @@ __global__ void __launch_bounds__(kMThreads)
   const int first_blk = t0 / BS;
   const int nblk = (len_ok && t_end > t0) ? (t_end - 1) / BS - first_blk + 1 : 0;
   const bool warp_live = r0 < rows_b;
+  const int wpos_min = L - n + r0 / GQ;                    // the warp's first row's position
 
   uint32_t qa[G::kKSteps][4];
   {
@@ -189,7 +216,7 @@ __global__ void __launch_bounds__(kMThreads)
       const uint32_t kb = stages + (uint32_t)(s * G::kBlockBytes), vb_ = kb + G::kTensorBytes;
       const int tb = (first_blk + k) * BS;                  // the block's first token
       const int valid = L - tb;                             // rows holding tokens (may exceed BS)
-      if (warp_live) {
+      if (warp_live && k % W == lane_i) {
 #pragma unroll
         for (int tile = 0; tile < G::kTiles; ++tile) {
           const int tt = tb + tile * 16;
@@ -205,15 +232,24 @@ __global__ void __launch_bounds__(kMThreads)
             mma16816<false>(c[1], qa[ks], fb4[2], fb4[3]);
           }
           // ---- causal mask and scale: token tt + 8nt + 2t + (e&1), row a
-          // for e < 2 and row b for e >= 2
+          // for e < 2 and row b for e >= 2.  A tile wholly at or before the
+          // warp's first position and before t_end needs no mask (rows past
+          // the sequence's queries are never written, whatever they hold).
+          if (tt + 15 <= wpos_min && tt + 16 <= t_end) {
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
+            for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int tok = tt + 8 * nt + 2 * t + (e & 1);
-              const int pos = e < 2 ? pos_a : pos_b;
-              c[nt][e] = (tok <= pos && tok < t_end) ? c[nt][e] * a.scale_log2 : -INFINITY;
-            }
+              for (int e = 0; e < 4; ++e) c[nt][e] *= a.scale_log2;
+          } else {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int tok = tt + 8 * nt + 2 * t + (e & 1);
+                const int pos = e < 2 ? pos_a : pos_b;
+                c[nt][e] = (tok <= pos && tok < t_end) ? c[nt][e] * a.scale_log2 : -INFINITY;
+              }
+          }
           float mx_a = fmaxf(fmaxf(c[0][0], c[0][1]), fmaxf(c[1][0], c[1][1]));
           float mx_b = fmaxf(fmaxf(c[0][2], c[0][3]), fmaxf(c[1][2], c[1][3]));
 #pragma unroll
@@ -239,12 +275,16 @@ __global__ void __launch_bounds__(kMThreads)
           }
           l_a = l_a * al_a + p[0][0] + p[0][1] + p[1][0] + p[1][1];
           l_b = l_b * al_b + p[0][2] + p[0][3] + p[1][2] + p[1][3];
+          // the accumulator is rescaled only when some row's maximum moved
+          // (the factor is exactly 1 otherwise)
+          if (__any_sync(0xffffffffu, al_a != 1.0f || al_b != 1.0f)) {
 #pragma unroll
-          for (int i = 0; i < D / 8; ++i) {
-            o[i][0] *= al_a;
-            o[i][1] *= al_a;
-            o[i][2] *= al_b;
-            o[i][3] *= al_b;
+            for (int i = 0; i < D / 8; ++i) {
+              o[i][0] *= al_a;
+              o[i][1] *= al_a;
+              o[i][2] *= al_b;
+              o[i][3] *= al_b;
+            }
           }
           // ---- O += P . V.  Rows at or past L in the sequence's last block
           // are zeroed in the V fragments (tokens 2t, 2t+1 of each half in
@@ -282,18 +322,68 @@ __global__ void __launch_bounds__(kMThreads)
       }
     }
   }
-  if (!ok) atomicOr(a.flags, PAGEDKV_FLAG_WAIT_TIMEOUT);
+  if (!ok) {
+    atomicOr(a.flags, PAGEDKV_FLAG_WAIT_TIMEOUT);
+    sh_fail = 1;
+  }
   if (bad && tid == 0) atomicOr(a.flags, PAGEDKV_FLAG_BAD_BLOCK);
   if (!len_ok && tid == 0 && rt == 0 && hk == 0 && part == 0) atomicOr(a.flags, PAGEDKV_FLAG_BAD_SEQ_LEN);
-  if (!rows_ok) return;                                    // no rows to write
+  if (!rows_ok) return;                                    // no rows to write (CTA-uniform)
 
-  // ---- epilogue: rows of this tile (invalid sequences: zeros)
 #pragma unroll
   for (int off = 1; off < 4; off <<= 1) {
     l_a += __shfl_xor_sync(0xffffffffu, l_a, off);
     l_b += __shfl_xor_sync(0xffffffffu, l_b, off);
   }
-  const bool failed = bad || !ok || !len_ok;
+  // ---- the warps of a row group combine: lane_i > 0 park (m, l, O) in the
+  // stage memory (every fill has landed and every warp is past its reads),
+  // lane_i == 0 folds them in and writes the rows.
+  __syncthreads();
+  const bool failed = bad || sh_fail != 0 || !len_ok;
+  if (W > 1) {
+    float* park = reinterpret_cast<float*>(smem_raw + (stages - smem_addr(smem_raw)));
+    constexpr int kSlot = 16 * D + 32;                     // O[16][D], m[16], l[16]
+    if (lane_i > 0) {
+      float* base = park + ((lane_i - 1) * RG + grp) * kSlot;
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) {
+        *reinterpret_cast<float2*>(base + g * D + 8 * i + 2 * t) = make_float2(o[i][0], o[i][1]);
+        *reinterpret_cast<float2*>(base + (g + 8) * D + 8 * i + 2 * t) = make_float2(o[i][2], o[i][3]);
+      }
+      if (t == 0) {
+        base[16 * D + g] = m_a;
+        base[16 * D + g + 8] = m_b;
+        base[16 * D + 16 + g] = l_a;
+        base[16 * D + 16 + g + 8] = l_b;
+      }
+    }
+    __syncthreads();
+    if (lane_i > 0) return;
+    for (int w2 = 1; w2 < W; ++w2) {
+      const float* base = park + ((w2 - 1) * RG + grp) * kSlot;
+      const float m2a = base[16 * D + g], m2b = base[16 * D + g + 8];
+      const float l2a = base[16 * D + 16 + g], l2b = base[16 * D + 16 + g + 8];
+      const float mna = fmaxf(m_a, m2a), mnb = fmaxf(m_b, m2b);
+      const float za = mna == -INFINITY ? 0.0f : mna, zb = mnb == -INFINITY ? 0.0f : mnb;
+      const float sa = exp2f(m_a - za), s2a = exp2f(m2a - za);
+      const float sb = exp2f(m_b - zb), s2b = exp2f(m2b - zb);
+      l_a = l_a * sa + l2a * s2a;
+      l_b = l_b * sb + l2b * s2b;
+      m_a = mna;
+      m_b = mnb;
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) {
+        const float2 xa = *reinterpret_cast<const float2*>(base + g * D + 8 * i + 2 * t);
+        const float2 xb = *reinterpret_cast<const float2*>(base + (g + 8) * D + 8 * i + 2 * t);
+        o[i][0] = o[i][0] * sa + xa.x * s2a;
+        o[i][1] = o[i][1] * sa + xa.y * s2a;
+        o[i][2] = o[i][2] * sb + xb.x * s2b;
+        o[i][3] = o[i][3] * sb + xb.y * s2b;
+      }
+    }
+  }
+
+  // ---- epilogue: rows of this tile (invalid sequences: zeros)
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     const int r = half ? rb : ra;
@@ -383,7 +473,7 @@ __global__ void __launch_bounds__(128) multi_merge_kernel(const DecodeArgs a) {
 template <int D, int BS>
 kv_status launch_m(const DecodeArgs& a, int tiles, cudaStream_t s) {
   using G = Geo<D, BS, false>;
-  constexpr int kSmem = kMStages * G::kBlockBytes + 1024;
+  constexpr int kSmem = multi_stages<G>() * G::kBlockBytes + 1024;
   static std::mutex mu;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -485,8 +575,7 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
   a.num_blocks = num_blocks;
   a.block_size = block_size;
   a.max_seq_len = max_seq_len;
-  a.part_tokens = choose_part_tokens((int)((num_tokens * (int64_t)GQ + kMRows - 1) / kMRows),
-                                     num_kv_heads, max_seq_len, di.num_sms);
+  a.part_tokens = choose_part_tokens((int)tiles, num_kv_heads, max_seq_len, di.num_sms);
   a.max_parts = (max_seq_len + a.part_tokens - 1) / a.part_tokens;
   if (a.max_parts > 65535) return fail(KV_ERR_INVALID_ARG, "%s: too many partitions", who);
   a.slots = a.max_parts;
