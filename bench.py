@@ -180,8 +180,9 @@ def oracle_time(wl, pools, seqs, threads):
 
 
 def oracle_sample(wl, threads, target_s=10.0, max_s=30.0):
-    """Time the oracle on growing prefixes of the batch until ~target_s of
-    work (bounded by max_s): returns a cpu_baseline dict."""
+    """Time the oracle for about target_s of work (bounded by max_s): growing
+    prefixes of the batch, and when the whole batch takes less than
+    target_s, repeated passes over it.  Returns a cpu_baseline dict."""
     pools = oracle_pools(wl)
     n = 2
     while True:
@@ -190,9 +191,14 @@ def oracle_sample(wl, threads, target_s=10.0, max_s=30.0):
         if dt >= target_s or len(seqs) == wl.spec.batch or dt * 2 > max_s:
             break
         n = min(wl.spec.batch, max(n + 1, int(n * target_s / max(dt, 1e-3))))
+    passes = 1
+    while len(seqs) == wl.spec.batch and dt < target_s and dt * (passes + 1) / passes <= max_s:
+        d2, k2 = oracle_time(wl, pools, seqs, threads)
+        dt, kv, passes = dt + d2, kv + k2, passes + 1
     return {"value": round(kv / dt / 1e9, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{len(seqs)} of {wl.spec.batch} sequences, all {wl.spec.num_q_heads} query heads "
-                      f"({kv / 1e6:.1f} MB of KV), fp64 three-pass oracle, {dt:.2f} s"}
+            "sample": f"{passes} pass(es) over {len(seqs)} of {wl.spec.batch} sequences, all "
+                      f"{wl.spec.num_q_heads} query heads ({kv / 1e6:.1f} MB of KV in all), fp64 "
+                      f"three-pass oracle, {dt:.2f} s"}
 
 
 # ---------------------------------------------------------------------------
