@@ -448,27 +448,33 @@ size_t pagedkv_multi_workspace_bytes(int num_tokens, int num_q_heads,
  *   out[j, h, :] = softmax_t(scale * q[j, h, :] . K_t) . V_t.
  *   out           device bf16 [num_tokens, num_q_heads, head_dim]
  *   q             device bf16 [num_tokens, num_q_heads, head_dim]
- *   k_cache, v_cache   bf16 pools as for paged_attention_decode
- *                 (8-bit pools return KV_ERR_NOT_IMPLEMENTED; scales NULL)
+ *   k_cache, v_cache, k_scale, v_scale   as for paged_attention_decode;
+ *                 8-bit pools (int8, E4M3) take up to 4 * (8 / G) query tokens
+ *                 per sequence (8 for G = 4), else KV_ERR_NOT_IMPLEMENTED
  *   block_tables, max_blocks_per_seq, seq_lens, batch  as for
  *                 paged_attention_decode (seq_lens counts the query tokens)
  *   query_start   device int32 [batch + 1], non-decreasing from 0 to
  *                 num_tokens (n_b = 0 is allowed: no queries)
+ *   max_query_len host bound on every n_b (sizes the launch)
  *   max_seq_len   host bound on every seq_lens[b]
  *   workspace     at least pagedkv_multi_workspace_bytes(...) bytes,
  *                 16-byte aligned (may be NULL when that size is 0)
- * A sequence with a bad length (n_b > seq_lens[b], beyond the table or the
- * hint) or a bad table entry has its rows zeroed and sets
+ * A sequence with a bad length (n_b > seq_lens[b] or > max_query_len, beyond
+ * the table or the hint) or a bad table entry has its rows zeroed and sets
  * PAGEDKV_FLAG_BAD_SEQ_LEN or PAGEDKV_FLAG_BAD_BLOCK; offsets outside
  * [0, num_tokens] leave that sequence's rows unwritten and set
- * PAGEDKV_FLAG_BAD_SEQ_LEN.  Asynchronous on `stream`: one attention launch,
- * plus a log-sum-exp merge launch when the keys are split into partitions. */
+ * PAGEDKV_FLAG_BAD_SEQ_LEN (rows past max_query_len are not written).
+ * Asynchronous on `stream`: one attention launch, plus a log-sum-exp merge
+ * launch when the keys are split into partitions.  With at most 4 * (8 / G)
+ * query tokens per sequence the decode kernel serves them (8 (token, head)
+ * columns per CTA); longer queries go to a row-tiled kernel. */
 kv_status paged_attention_multi(void *out, const void *q, const void *k_cache,
                                 const void *v_cache, const float *k_scale,
                                 const float *v_scale, const int32_t *block_tables,
                                 int max_blocks_per_seq, const int32_t *seq_lens,
                                 const int32_t *query_start, int batch,
-                                int num_tokens, int num_q_heads, int num_kv_heads,
+                                int num_tokens, int max_query_len,
+                                int num_q_heads, int num_kv_heads,
                                 int head_dim, int num_blocks, int block_size,
                                 int max_seq_len, float scale, kv_dtype dtype,
                                 void *workspace, size_t workspace_bytes,

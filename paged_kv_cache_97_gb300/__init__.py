@@ -44,7 +44,7 @@ SIGNATURES = {
     "kv_pool_register_prefix": (_I, [_P, _P, _P, _I, ctypes.c_uint64]),
     "kv_pool_cached_blocks": (_I, [_P]),
     "paged_attention_multi": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I,
-                                   _I, _I, _F, _I, _P, _SZ, _P]),
+                                   _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "pagedkv_pool_tensor_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "pagedkv_slot_mapping": (_I, [_P, _I, _P, _I, _I, _I, _P, _P]),
     "pagedkv_token_slot_mapping": (_I, [_P, _I, _P, _P, _I, _I, _I, _P, _P]),
@@ -328,8 +328,8 @@ def multi_workspace_bytes(num_tokens, num_q_heads, head_dim, max_seq_len, block_
 
 
 def paged_attention_multi(out, q, k_cache, v_cache, block_tables, seq_lens, query_start,
-                          max_seq_len, scale, workspace=None, k_scale=None, v_scale=None,
-                          stream=None):
+                          max_seq_len, max_query_len, scale, workspace=None, k_scale=None,
+                          v_scale=None, stream=None):
     """Causal attention of several query tokens per sequence (the last
     query_start[b+1] - query_start[b] tokens of sequence b, already
     appended): q, out bf16 [T, Hq, d]."""
@@ -350,8 +350,9 @@ def paged_attention_multi(out, q, k_cache, v_cache, block_tables, seq_lens, quer
     ws_ptr, ws_n = (None, 0) if workspace is None else (_ptr(workspace), workspace.numel() * workspace.element_size())
     _check(load().paged_attention_multi(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
                                         _ptr(v_scale), _ptr(block_tables), block_tables.shape[1],
-                                        _ptr(seq_lens), _ptr(query_start), B, T, hq, hkv, d, nb, bs,
-                                        int(max_seq_len), float(scale), dt, ws_ptr, ws_n,
+                                        _ptr(seq_lens), _ptr(query_start), B, T, int(max_query_len),
+                                        hq, hkv, d, nb, bs, int(max_seq_len), float(scale), dt,
+                                        ws_ptr, ws_n,
                                         _stream(stream)))
 
 

@@ -66,6 +66,8 @@ struct DecodeArgs {
   // query_start[b] .. query_start[b + 1] - 1 (its last tokens); null otherwise
   const int32_t* query_start;  // [batch + 1]
   int num_tokens;
+  int max_query_len;           // host bound on query tokens per sequence
+  int vgroups;                 // column groups per sequence (decode kernel, multi-token)
 };
 
 // Workspace of one decode call: (m, l) and acc of `slots` partials per query

@@ -28,6 +28,14 @@
 // softmax state (m, l) of heads 2t and 2t+1 lives in the lane that rescales
 // their accumulators.
 //
+// Multi-token queries (kMulti, paged_attention_multi with few query tokens
+// per sequence: speculative verification, “让 Agent 跑得快”, §六): the 8 MMA
+// columns of a CTA become (query token, grouped head) pairs -- 8 / G tokens
+// of one sequence times its G heads, a "column group" -- each with its own
+// causal limit (query i of n sits at position L - n + i and sees positions up
+// to it).  The column groups of one (sequence, KV head, partition) are
+// neighbouring CTAs, so their reads of the same blocks meet in L2.
+//
 // bf16 pools: K and V tiles come straight from the swizzled stage with
 // ldmatrix (V transposed by ldmatrix.trans).  int8 pools: codes are read with
 // 16-byte shared loads and widened to fp16 exactly (c + 128 placed in the
@@ -67,7 +75,7 @@ constexpr int kSpec = (kMaxBlocks + kThreads - 1) / kThreads;  // table entries 
 #ifndef PAGEDKV_Q8_MIN_BLOCKS
 #define PAGEDKV_Q8_MIN_BLOCKS 4
 #endif
-template <int D, int BS, bool kQ8, bool kFp8>
+template <int D, int BS, bool kQ8, bool kFp8, bool kMulti>
 __global__ void __launch_bounds__(kThreads, kQ8 ? PAGEDKV_Q8_MIN_BLOCKS : 1)
     decode_kernel(const __grid_constant__ CUtensorMap k_map,
                   const __grid_constant__ CUtensorMap v_map, const DecodeArgs a) {
@@ -84,13 +92,37 @@ __global__ void __launch_bounds__(kThreads, kQ8 ? PAGEDKV_Q8_MIN_BLOCKS : 1)
   // first partitions launch first and the short last partitions of long
   // sequences launch last, which trims the tail; neighbouring heads of one
   // block run side by side.
-  const int hk = blockIdx.x, b = blockIdx.y, part = blockIdx.z;
+  // (kMulti: blockIdx.y = sequence * vgroups + column group.)
+  const int hk = blockIdx.x, part = blockIdx.z;
+  const int b = kMulti ? (int)(blockIdx.y / a.vgroups) : (int)blockIdx.y;
+  const int vg = kMulti ? (int)(blockIdx.y % a.vgroups) : 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;                 // MMA fragment coordinates
   const int Hq = a.num_q_heads, Hkv = a.num_kv_heads;
   const int GQ = Hq / Hkv;                               // grouped query heads (1..8)
   const int64_t head0 = (int64_t)b * Hq + (int64_t)hk * GQ;
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+  // Multi-token queries: the sequence's q rows [q0, q0 + nq), TPG tokens per
+  // column group.
+  int q0 = 0, nq = 1;
+  if constexpr (kMulti) {
+    q0 = a.query_start[b];
+    nq = a.query_start[b + 1] - q0;
+  }
+  const int TPG = kMulti ? kMaxGroup / GQ : 1;
+  const bool rows_ok = !kMulti || (q0 >= 0 && nq >= 0 && q0 + nq <= a.num_tokens);
+  // Row of the q / out tensors that column c serves (-1: a padding column):
+  // head c of the group, or (kMulti) token vg * TPG + c / GQ, head c % GQ.
+  auto col_row = [&](int c) -> int64_t {
+    if constexpr (kMulti) {
+      const int i = vg * TPG + c / GQ;
+      return (rows_ok && c < TPG * GQ && i < nq) ? (int64_t)(q0 + i) * Hq + (int64_t)hk * GQ + c % GQ
+                                                   : -1;
+    } else {
+      return c < GQ ? head0 + c : -1;
+    }
+  };
+  const int ncols = kMulti ? kMaxGroup : GQ;             // columns that may be written
 
   // This partition's block-table entries and the consumers' q fragments are
   // loaded before the sequence length arrives (neither depends on it), so
@@ -112,7 +144,8 @@ __global__ void __launch_bounds__(kThreads, kQ8 ? PAGEDKV_Q8_MIN_BLOCKS : 1)
   // chunks of a K row (see the int8 K loads below).
   uint32_t qraw[G::kKSteps][2];
   if (warp < kConsumers) {
-    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q) + (head0 + g) * D;
+    const int64_t qrow = col_row(g);
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q) + (qrow < 0 ? 0 : qrow) * D;
 #pragma unroll
     for (int ks = 0; ks < G::kKSteps; ++ks) {
 #pragma unroll
@@ -126,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, kQ8 ? PAGEDKV_Q8_MIN_BLOCKS : 1)
         } else {
           d0 = 16 * ks + 2 * t + 8 * r;
         }
-        qraw[ks][r] = g < GQ ? *reinterpret_cast<const uint32_t*>(q + d0) : 0u;
+        qraw[ks][r] = qrow >= 0 ? *reinterpret_cast<const uint32_t*>(q + d0) : 0u;
       }
     }
   }
@@ -134,20 +167,45 @@ __global__ void __launch_bounds__(kThreads, kQ8 ? PAGEDKV_Q8_MIN_BLOCKS : 1)
   // ---- sequence checks (uniform over the CTA) -----------------------------
   const int L = a.seq_lens[b];
   const int64_t table_tokens = (int64_t)a.max_blocks_per_seq * BS;
-  if (L <= a.skip_tokens || L > a.max_seq_len || L > table_tokens) {
+  const bool len_bad = L <= a.skip_tokens || L > a.max_seq_len || L > table_tokens ||
+                       (kMulti && (!rows_ok || nq > L || nq > a.max_query_len));
+  if (len_bad) {
     if (part == 0) {
-      if (threadIdx.x == 0) atomicOr(a.flags, PAGEDKV_FLAG_BAD_SEQ_LEN);
-      for (int i = threadIdx.x; i < GQ * D; i += blockDim.x)
-        out[head0 * D + i] = __float2bfloat16_rn(0.0f);
+      if (threadIdx.x == 0 && vg == 0) atomicOr(a.flags, PAGEDKV_FLAG_BAD_SEQ_LEN);
+      // (with several partitions, the multi-token merge zeroes these rows)
+      if (!kMulti || a.max_parts == 1)
+        for (int i = threadIdx.x; i < ncols * D; i += blockDim.x) {
+          const int64_t r = col_row(i / D);
+          if (r >= 0) out[r * D + i % D] = __float2bfloat16_rn(0.0f);
+        }
     }
     return;
   }
+  if (kMulti && vg * TPG >= nq) return;                  // a column group with no queries
   // Tokens [skip, L) are split into partitions here; a shared prefix
   // (skip > 0) is attended by the prefix kernel and merged afterwards, so
-  // with one every row writes a partial.
+  // with one every row writes a partial.  A column group of multi-token
+  // queries needs keys only up to its last query's position.
   if (t0 >= L) return;
-  const int t1 = min(t0 + a.part_tokens, L);
+  int t1 = min(t0 + a.part_tokens, L);
+  if constexpr (kMulti) t1 = min(t1, L - nq + min(nq - 1, vg * TPG + TPG - 1) + 1);
   const int nparts = (L - skip + a.part_tokens - 1) / a.part_tokens + (skip > 0 ? a.prefix_chunks : 0);
+  // direct output (one partial per row) or a partial for the merge
+  const bool direct = kMulti ? a.max_parts == 1 : nparts == 1;
+  if (kMulti && t1 <= t0) {
+    // every query of this group precedes the partition: empty partials
+    for (int i = threadIdx.x; i < ncols * D; i += blockDim.x) {
+      const int64_t r = col_row(i / D);
+      if (r < 0) continue;
+      const int64_t sl = r * a.slots + part;
+      a.ws_acc[sl * D + i % D] = 0.0f;
+      if (i % D == 0) {
+        a.ws_ml[2 * sl] = -INFINITY;
+        a.ws_ml[2 * sl + 1] = 0.0f;
+      }
+    }
+    return;
+  }
   const int nblk = (t1 - 1) / BS - first_blk + 1;        // >= 1, <= spec_blk
 
   const uint32_t stages = (smem_addr(smem_raw) + 1023u) & ~1023u;
@@ -315,6 +373,12 @@ __global__ void __launch_bounds__(kThreads, kQ8 ? PAGEDKV_Q8_MIN_BLOCKS : 1)
       }
     }
     const float score_scale = a.scale_log2 / qscale;
+    // causal limits of this lane's columns 2t and 2t+1 (multi-token queries)
+    int cpos0 = 0x7fffffff, cpos1 = 0x7fffffff;
+    if constexpr (kMulti) {
+      if (2 * t < TPG * GQ) cpos0 = L - nq + vg * TPG + (2 * t) / GQ;
+      if (2 * t + 1 < TPG * GQ) cpos1 = L - nq + vg * TPG + (2 * t + 1) / GQ;
+    }
     // P^T transpose sources: token 2t (and 2t+8) of head g sits in lane
     // (2t)*4 + g/2, token 2t+1 (2t+9) in the lane 4 higher.
     const int src_a = (2 * t) * 4 + (g >> 1), src_b = src_a + 4;
@@ -375,12 +439,21 @@ __global__ void __launch_bounds__(kThreads, kQ8 ? PAGEDKV_Q8_MIN_BLOCKS : 1)
               else        mma16816<true>(c0, fa, qf[ks][0], qf[ks][1]);
             }
           }
-          // rows (tokens) g and g+8 of this tile; masked rows -> -inf
+          // rows (tokens) g and g+8 of this tile; masked rows -> -inf (and,
+          // for multi-token queries, tokens past a column's position)
           const int tok_lo = tile * 16 + g, tok_hi = tok_lo + 8;
-          sc[tile][0] = tok_lo < valid ? (c0[0] + c1[0]) * kfac : -INFINITY;
-          sc[tile][1] = tok_lo < valid ? (c0[1] + c1[1]) * kfac : -INFINITY;
-          sc[tile][2] = tok_hi < valid ? (c0[2] + c1[2]) * kfac : -INFINITY;
-          sc[tile][3] = tok_hi < valid ? (c0[3] + c1[3]) * kfac : -INFINITY;
+          if constexpr (kMulti) {
+            const int abs_lo = (first_blk + j) * BS + tok_lo, abs_hi = abs_lo + 8;
+            sc[tile][0] = (tok_lo < valid && abs_lo <= cpos0) ? (c0[0] + c1[0]) * kfac : -INFINITY;
+            sc[tile][1] = (tok_lo < valid && abs_lo <= cpos1) ? (c0[1] + c1[1]) * kfac : -INFINITY;
+            sc[tile][2] = (tok_hi < valid && abs_hi <= cpos0) ? (c0[2] + c1[2]) * kfac : -INFINITY;
+            sc[tile][3] = (tok_hi < valid && abs_hi <= cpos1) ? (c0[3] + c1[3]) * kfac : -INFINITY;
+          } else {
+            sc[tile][0] = tok_lo < valid ? (c0[0] + c1[0]) * kfac : -INFINITY;
+            sc[tile][1] = tok_lo < valid ? (c0[1] + c1[1]) * kfac : -INFINITY;
+            sc[tile][2] = tok_hi < valid ? (c0[2] + c1[2]) * kfac : -INFINITY;
+            sc[tile][3] = tok_hi < valid ? (c0[3] + c1[3]) * kfac : -INFINITY;
+          }
         }
 
         // ---- online softmax update for heads 2t (index 0) and 2t+1 (1) ----
@@ -395,10 +468,14 @@ __global__ void __launch_bounds__(kThreads, kQ8 ? PAGEDKV_Q8_MIN_BLOCKS : 1)
           mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
           mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
         }
-        const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+        const float mx0n = fmaxf(m_run[0], mx0), mx1n = fmaxf(m_run[1], mx1);
+        // a column with no key yet keeps m = -inf: subtract 0 then (multi-
+        // token queries; a decode column always has a key)
+        const float mn0 = (kMulti && mx0n == -INFINITY) ? 0.0f : mx0n;
+        const float mn1 = (kMulti && mx1n == -INFINITY) ? 0.0f : mx1n;
         const float al0 = exp2f(m_run[0] - mn0), al1 = exp2f(m_run[1] - mn1);
-        m_run[0] = mn0;
-        m_run[1] = mn1;
+        m_run[0] = mx0n;
+        m_run[1] = mx1n;
         l_run[0] *= al0;
         l_run[1] *= al1;
 #pragma unroll
@@ -538,12 +615,14 @@ __global__ void __launch_bounds__(kThreads, kQ8 ? PAGEDKV_Q8_MIN_BLOCKS : 1)
   if (failed) {
     if (threadIdx.x == 0)
       atomicOr(a.flags, bad ? PAGEDKV_FLAG_BAD_BLOCK : PAGEDKV_FLAG_WAIT_TIMEOUT);
-    for (int i = threadIdx.x; i < GQ * D; i += blockDim.x) {
+    for (int i = threadIdx.x; i < ncols * D; i += blockDim.x) {
       const int hh = i / D, e = i % D;
-      if (nparts == 1) {
-        out[head0 * D + i] = __float2bfloat16_rn(0.0f);
+      const int64_t row = col_row(hh);
+      if (row < 0) continue;
+      if (direct) {
+        out[row * D + e] = __float2bfloat16_rn(0.0f);
       } else {
-        const int64_t r = (head0 + hh) * a.slots + part;
+        const int64_t r = row * a.slots + part;
         a.ws_acc[r * D + e] = 0.0f;
         if (e == 0) {
           a.ws_ml[2 * r] = 0.0f;
@@ -555,23 +634,26 @@ __global__ void __launch_bounds__(kThreads, kQ8 ? PAGEDKV_Q8_MIN_BLOCKS : 1)
   }
 
   const float out_scale = kQ8 ? (v_max_scale > 0.0f ? v_max_scale : 1.0f) : 1.0f;
-  for (int i = threadIdx.x; i < GQ * D; i += blockDim.x) {
+  for (int i = threadIdx.x; i < ncols * D; i += blockDim.x) {
     const int hh = i / D, e = i % D;
+    const int64_t row = col_row(hh);
+    if (row < 0) continue;
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, red_m[w * 8 + hh]);
+    const float Mz = (kMulti && M == -INFINITY) ? 0.0f : M;  // a column with no key here
     float num = 0.0f, den = 0.0f;
 #pragma unroll
     for (int w = 0; w < kConsumers; ++w) {
-      const float c = exp2f(red_m[w * 8 + hh] - M);  // 0 for a warp that saw no token
+      const float c = exp2f(red_m[w * 8 + hh] - Mz);  // 0 for a warp that saw no token
       num = fmaf(c, red_acc[(w * 8 + hh) * D + e], num);
       den = fmaf(c, red_l[w * 8 + hh], den);
     }
     num *= out_scale;
-    if (nparts == 1) {
-      out[head0 * D + i] = __float2bfloat16_rn(num / den);
+    if (direct) {
+      out[row * D + e] = __float2bfloat16_rn(num / den);
     } else {
-      const int64_t r = (head0 + hh) * a.slots + part;
+      const int64_t r = row * a.slots + part;
       a.ws_acc[r * D + e] = num;
       if (e == 0) {
         a.ws_ml[2 * r] = M;
@@ -625,7 +707,7 @@ kv_status make_map(CUtensorMap* map, const void* pool, const DecodeArgs& a) {
   return KV_OK;
 }
 
-template <int D, int BS, bool kQ8, bool kFp8>
+template <int D, int BS, bool kQ8, bool kFp8, bool kMulti>
 kv_status launch_t(const DecodeArgs& a, cudaStream_t s) {
   using G = Geo<D, BS, kQ8>;
   static std::mutex mu;
@@ -636,7 +718,7 @@ kv_status launch_t(const DecodeArgs& a, cudaStream_t s) {
   {
     std::lock_guard<std::mutex> lock(mu);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-      st = cuda_check(cudaFuncSetAttribute(decode_kernel<D, BS, kQ8, kFp8>,
+      st = cuda_check(cudaFuncSetAttribute(decode_kernel<D, BS, kQ8, kFp8, kMulti>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            G::kSmemBytes),
                       "cudaFuncSetAttribute(decode_kernel)");
@@ -647,9 +729,9 @@ kv_status launch_t(const DecodeArgs& a, cudaStream_t s) {
   alignas(64) CUtensorMap km, vm;
   if ((st = make_map<D, BS, kQ8>(&km, a.k_cache, a)) != KV_OK) return st;
   if ((st = make_map<D, BS, kQ8>(&vm, a.v_cache, a)) != KV_OK) return st;
-  const dim3 grid(a.num_kv_heads, a.batch, a.max_parts);
+  const dim3 grid(a.num_kv_heads, kMulti ? a.batch * a.vgroups : a.batch, a.max_parts);
   if (a.prefix_chunks == 0) {
-    decode_kernel<D, BS, kQ8, kFp8><<<grid, kThreads, G::kSmemBytes, s>>>(km, vm, a);
+    decode_kernel<D, BS, kQ8, kFp8, kMulti><<<grid, kThreads, G::kSmemBytes, s>>>(km, vm, a);
     return cuda_check(cudaGetLastError(), "decode_kernel launch");
   }
   // Behind the prefix kernel: launched as its programmatic dependent so the
@@ -665,13 +747,15 @@ kv_status launch_t(const DecodeArgs& a, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cuda_check(cudaLaunchKernelEx(&cfg, decode_kernel<D, BS, kQ8, kFp8>, km, vm, a),
+  return cuda_check(cudaLaunchKernelEx(&cfg, decode_kernel<D, BS, kQ8, kFp8, kMulti>, km, vm, a),
                     "decode_kernel launch");
 }
 
 template <int D, bool kQ8, bool kFp8>
 kv_status launch_bs(const DecodeArgs& a, cudaStream_t s) {
-  return a.block_size == 32 ? launch_t<D, 32, kQ8, kFp8>(a, s) : launch_t<D, 16, kQ8, kFp8>(a, s);
+  if (a.query_start != nullptr)
+    return a.block_size == 32 ? launch_t<D, 32, kQ8, kFp8, true>(a, s) : launch_t<D, 16, kQ8, kFp8, true>(a, s);
+  return a.block_size == 32 ? launch_t<D, 32, kQ8, kFp8, false>(a, s) : launch_t<D, 16, kQ8, kFp8, false>(a, s);
 }
 
 template <int D, int BS, bool kQ8>
@@ -693,8 +777,9 @@ kv_status make_kv_maps(const DecodeArgs& a, CUtensorMap* km, CUtensorMap* vm) {
 }
 
 kv_status launch_decode(const DecodeArgs& a, cudaStream_t s) {
-  if (a.batch > 65535 || a.max_parts > 65535)
-    return fail(KV_ERR_INVALID_ARG, "batch and the partition count must be at most 65535");
+  const int64_t rows = (int64_t)a.batch * (a.query_start ? a.vgroups : 1);
+  if (rows > 65535 || a.max_parts > 65535)
+    return fail(KV_ERR_INVALID_ARG, "batch (x column groups) and the partition count must be at most 65535");
   if (a.num_q_heads / a.num_kv_heads > 8)
     return fail(KV_ERR_INVALID_ARG, "at most 8 query heads per KV head");
   if (a.part_tokens / a.block_size > kMaxBlocks || a.part_tokens % a.block_size)

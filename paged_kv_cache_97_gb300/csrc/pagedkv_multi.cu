@@ -21,7 +21,9 @@
 // the S accumulators as the A operand of O += P . V.  One partition writes
 // the output; several write per-row (m, l, acc) partials that a merge kernel
 // combines (“LLM 推理优化技术全景”, 在线 Softmax; “Flash Attention v2 的改进”).
-// bf16 pools.
+// bf16 pools.  Sequences with few query tokens (at most 4 x 8 / G) go to the
+// decode kernel instead, whose 8 MMA columns per CTA then hold (token, head)
+// pairs (pagedkv_decode.cu); both paths share the per-row merge below.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -50,6 +52,10 @@ __host__ __device__ constexpr int multi_stages() {
          : PAGEDKV_MULTI_STAGE_BUDGET / G::kBlockBytes < 4 ? 4
          : PAGEDKV_MULTI_STAGE_BUDGET / G::kBlockBytes;
 }
+
+// Column groups the decode kernel may serve per sequence (8 columns each):
+// beyond this, the row-tiled kernel below takes the queries.
+constexpr int kMaxVGroups = 4;
 
 // Row tiles of a sequence with n query tokens and GQ grouped heads.
 __device__ __forceinline__ int row_tiles(int n, int GQ) { return n > 0 ? (n * GQ + kMRows - 1) / kMRows : 0; }
@@ -134,7 +140,7 @@ __global__ void __launch_bounds__(kMThreads, PAGEDKV_MULTI_MIN_BLOCKS)
   const int t0 = part * a.part_tokens;
   if (t0 >= L && L > 0) return;                            // no such partition for this sequence
   const bool rows_ok = q0 >= 0 && q0 + n <= a.num_tokens;
-  const bool len_ok = rows_ok && L > 0 && n <= L && L <= a.max_seq_len &&
+  const bool len_ok = rows_ok && L > 0 && n <= L && n <= a.max_query_len && L <= a.max_seq_len &&
                       (int64_t)L <= (int64_t)a.max_blocks_per_seq * BS;
 
   // The tile's 16-row groups (RG of them, 1, 2 or 4) and the warps per
@@ -435,6 +441,7 @@ __global__ void __launch_bounds__(128) multi_merge_kernel(const DecodeArgs a) {
   const int L = a.seq_lens[b], n = qs[b + 1] - qs[b];
   // the sequence checks of the attention kernel: a bad sequence's rows are 0
   const bool seq_ok = qs[b] >= 0 && qs[b + 1] <= a.num_tokens && L > 0 && n <= L &&
+                      n <= a.max_query_len &&
                       L <= a.max_seq_len &&
                       (int64_t)L <= (int64_t)a.max_blocks_per_seq * a.block_size;
   const int np = seq_ok ? min((L + a.part_tokens - 1) / a.part_tokens, a.max_parts) : 0;
@@ -493,10 +500,14 @@ kv_status launch_m(const DecodeArgs& a, int tiles, cudaStream_t s) {
   if ((st = make_kv_maps(a, &km, &vm)) != KV_OK) return st;
   const dim3 grid((unsigned)tiles, (unsigned)a.num_kv_heads, (unsigned)a.max_parts);
   multi_kernel<D, BS><<<grid, kMThreads, kSmem, s>>>(km, vm, a);
-  st = cuda_check(cudaGetLastError(), "multi_kernel launch");
-  if (st != KV_OK || a.max_parts == 1) return st;
+  return cuda_check(cudaGetLastError(), "multi_kernel launch");
+}
+
+kv_status launch_multi_merge(const DecodeArgs& a, cudaStream_t s) {
+  if (a.max_parts == 1) return KV_OK;
   const dim3 mgrid((unsigned)a.num_tokens, (unsigned)((a.num_q_heads + 3) / 4));
-  multi_merge_kernel<D><<<mgrid, 128, 0, s>>>(a);
+  if (a.head_dim == 128) multi_merge_kernel<128><<<mgrid, 128, 0, s>>>(a);
+  else multi_merge_kernel<64><<<mgrid, 128, 0, s>>>(a);
   return cuda_check(cudaGetLastError(), "multi_merge_kernel launch");
 }
 
@@ -526,22 +537,33 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
                                 const void* v_cache, const float* k_scale, const float* v_scale,
                                 const int32_t* block_tables, int max_blocks_per_seq,
                                 const int32_t* seq_lens, const int32_t* query_start, int batch,
-                                int num_tokens, int num_q_heads, int num_kv_heads, int head_dim,
-                                int num_blocks, int block_size, int max_seq_len, float scale,
-                                kv_dtype dtype, void* workspace, size_t workspace_bytes,
-                                void* stream) {
+                                int num_tokens, int max_query_len, int num_q_heads,
+                                int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                                int max_seq_len, float scale, kv_dtype dtype, void* workspace,
+                                size_t workspace_bytes, void* stream) {
   const char* who = "paged_attention_multi";
   if (batch < 0 || num_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
       num_q_heads % num_kv_heads || max_blocks_per_seq <= 0 || num_blocks <= 0 ||
-      max_seq_len <= 0 || !valid_dtype(dtype))
+      max_seq_len <= 0 || max_query_len <= 0 || !valid_dtype(dtype))
     return fail(KV_ERR_INVALID_ARG, "%s: bad sizes", who);
   if (head_dim != 64 && head_dim != 128)
     return fail(KV_ERR_INVALID_ARG, "%s: head_dim must be 64 or 128", who);
   if (block_size != 16 && block_size != 32)
     return fail(KV_ERR_INVALID_ARG, "%s: block_size must be 16 or 32", who);
-  if (dtype != KV_DTYPE_BF16)
-    return fail(KV_ERR_NOT_IMPLEMENTED, "%s: multi-token queries support bf16 pools only", who);
-  if (k_scale || v_scale) return fail(KV_ERR_INVALID_ARG, "%s: bf16 pools take no scales", who);
+  const bool q8 = dtype != KV_DTYPE_BF16;
+  if (q8 != (k_scale != nullptr) || q8 != (v_scale != nullptr))
+    return fail(KV_ERR_INVALID_ARG, "%s: 8-bit pools need k_scale and v_scale; bf16 pools take NULL", who);
+  const int GQ = num_q_heads / num_kv_heads;
+  // Few query tokens per sequence: the decode kernel's 8 columns per CTA
+  // hold (token, head) pairs, 8 / G tokens per column group.  Otherwise the
+  // row-tiled kernel (bf16 pools).
+  const int tpg = GQ <= kMaxGroup ? kMaxGroup / GQ : 0;
+  const int vgroups = tpg > 0 ? (max_query_len + tpg - 1) / tpg : 0;
+  const bool column_path = tpg > 0 && vgroups <= kMaxVGroups;
+  if (!column_path && q8)
+    return fail(KV_ERR_NOT_IMPLEMENTED,
+                "%s: 8-bit pools support up to %d query tokens per sequence here", who,
+                tpg * kMaxVGroups);
   if (batch == 0 || num_tokens == 0) return KV_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !query_start)
     return fail(KV_ERR_INVALID_ARG, "%s: NULL pointer", who);
@@ -551,7 +573,6 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
   DeviceInfo di;
   kv_status st = device_info(&di);
   if (st != KV_OK) return st;
-  const int GQ = num_q_heads / num_kv_heads;
   // Upper bound of the row tiles over all sequences: sum ceil(n_b GQ / 64)
   // <= T GQ / 64 + batch (tiles past the real count exit at once).
   const int64_t tiles = ((int64_t)num_tokens * GQ + kMRows - 1) / kMRows + batch;
@@ -564,8 +585,12 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
   a.v_cache = v_cache;
   a.block_tables = block_tables;
   a.seq_lens = seq_lens;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
   a.query_start = query_start;
   a.num_tokens = num_tokens;
+  a.max_query_len = max_query_len;
+  a.vgroups = column_path ? vgroups : 1;
   a.flags = di.flags;
   a.max_blocks_per_seq = max_blocks_per_seq;
   a.batch = batch;
@@ -575,7 +600,8 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
   a.num_blocks = num_blocks;
   a.block_size = block_size;
   a.max_seq_len = max_seq_len;
-  a.part_tokens = choose_part_tokens((int)tiles, num_kv_heads, max_seq_len, di.num_sms);
+  a.part_tokens = choose_part_tokens(column_path ? batch * vgroups : (int)tiles, num_kv_heads,
+                                     max_seq_len, di.num_sms);
   a.max_parts = (max_seq_len + a.part_tokens - 1) / a.part_tokens;
   if (a.max_parts > 65535) return fail(KV_ERR_INVALID_ARG, "%s: too many partitions", who);
   a.slots = a.max_parts;
@@ -591,9 +617,15 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
     a.ws_acc = a.ws_ml + (size_t)num_tokens * num_q_heads * a.max_parts * 2;
   }
   cudaStream_t s = (cudaStream_t)stream;
-  if (head_dim == 128)
-    return block_size == 32 ? launch_m<128, 32>(a, (int)tiles, s) : launch_m<128, 16>(a, (int)tiles, s);
-  return block_size == 32 ? launch_m<64, 32>(a, (int)tiles, s) : launch_m<64, 16>(a, (int)tiles, s);
+  if (column_path) {
+    st = launch_decode(a, s);
+  } else if (head_dim == 128) {
+    st = block_size == 32 ? launch_m<128, 32>(a, (int)tiles, s) : launch_m<128, 16>(a, (int)tiles, s);
+  } else {
+    st = block_size == 32 ? launch_m<64, 32>(a, (int)tiles, s) : launch_m<64, 16>(a, (int)tiles, s);
+  }
+  if (st != KV_OK) return st;
+  return launch_multi_merge(a, s);
 }
 
 }  // extern "C"

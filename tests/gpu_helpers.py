@@ -135,8 +135,8 @@ class GpuStep:
             self.ws_multi = torch.empty(max(ws, 16), dtype=torch.uint8, device=self.dev)
         pkv.paged_attention_multi(self.out_multi, self.q, self.k_cache, self.v_cache,
                                   self.block_tables, self.seq_lens, self.query_start,
-                                  self.max_seq_len, s.scale, self.ws_multi, self.k_scale,
-                                  self.v_scale)
+                                  self.max_seq_len, max(int(self.wl.query_lens.max()), 1), s.scale,
+                                  self.ws_multi, self.k_scale, self.v_scale)
         return self.out_multi
 
     def multi_step(self):
