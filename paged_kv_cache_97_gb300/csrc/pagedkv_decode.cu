@@ -70,13 +70,13 @@ constexpr int kSpec = (kMaxBlocks + kThreads - 1) / kThreads;  // table entries 
 
 // kQ8: the pools hold 8-bit codes under per-(block, KV head) scales, int8
 // or (kFp8) E4M3; otherwise bf16.
-// 8-bit instances may be held to 128 registers (4 CTAs of 4 warps per SM,
-// the residency their shared memory allows).
+// 8-bit and multi-token instances may be held to 128 registers (4 CTAs of
+// 4 warps per SM, the residency their shared memory allows).
 #ifndef PAGEDKV_Q8_MIN_BLOCKS
 #define PAGEDKV_Q8_MIN_BLOCKS 4
 #endif
 template <int D, int BS, bool kQ8, bool kFp8, bool kMulti>
-__global__ void __launch_bounds__(kThreads, kQ8 ? PAGEDKV_Q8_MIN_BLOCKS : 1)
+__global__ void __launch_bounds__(kThreads, (kQ8 || kMulti) ? PAGEDKV_Q8_MIN_BLOCKS : 1)
     decode_kernel(const __grid_constant__ CUtensorMap k_map,
                   const __grid_constant__ CUtensorMap v_map, const DecodeArgs a) {
   using G = Geo<D, BS, kQ8>;
