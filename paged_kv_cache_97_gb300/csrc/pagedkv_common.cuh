@@ -68,6 +68,8 @@ struct DecodeArgs {
   int num_tokens;
   int max_query_len;           // host bound on query tokens per sequence
   int vgroups;                 // column groups per sequence (decode kernel, multi-token)
+  int col_max_n;               // sequences with at most this many queries use the
+                               // decode kernel's column groups, longer ones the row tiles
 };
 
 // Workspace of one decode call: (m, l) and acc of `slots` partials per query

@@ -57,8 +57,11 @@ __host__ __device__ constexpr int multi_stages() {
 // beyond this, the row-tiled kernel below takes the queries.
 constexpr int kMaxVGroups = 4;
 
-// Row tiles of a sequence with n query tokens and GQ grouped heads.
-__device__ __forceinline__ int row_tiles(int n, int GQ) { return n > 0 ? (n * GQ + kMRows - 1) / kMRows : 0; }
+// Row tiles of a sequence with n query tokens and GQ grouped heads (none for
+// a sequence the decode kernel's column groups serve: n <= col_max_n).
+__device__ __forceinline__ int row_tiles(int n, int GQ, int col_max_n) {
+  return n > col_max_n ? (n * GQ + kMRows - 1) / kMRows : 0;
+}
 
 #ifndef PAGEDKV_MULTI_MIN_BLOCKS
 #define PAGEDKV_MULTI_MIN_BLOCKS 3
@@ -104,7 +107,7 @@ __global__ void __launch_bounds__(kMThreads, PAGEDKV_MULTI_MIN_BLOCKS)
     if (b < B) {
       const int n = qs[b + 1] - qs[b];
       if (n < 0 && blockIdx.x == 0 && hk == 0 && part == 0) atomicOr(a.flags, PAGEDKV_FLAG_BAD_SEQ_LEN);
-      mine += row_tiles(n, GQ);
+      mine += row_tiles(n, GQ, a.col_max_n);
     }
   }
   scan[tid] = mine;
@@ -121,7 +124,7 @@ __global__ void __launch_bounds__(kMThreads, PAGEDKV_MULTI_MIN_BLOCKS)
     for (int i = 0; i < per; ++i) {
       const int b = tid * per + i;
       if (b >= B) break;
-      const int tl = row_tiles(qs[b + 1] - qs[b], GQ);
+      const int tl = row_tiles(qs[b + 1] - qs[b], GQ, a.col_max_n);
       if (x < acc + tl) {
         sh_b = b;
         sh_rt = x - acc;
@@ -499,8 +502,23 @@ kv_status launch_m(const DecodeArgs& a, int tiles, cudaStream_t s) {
   alignas(64) CUtensorMap km, vm;
   if ((st = make_kv_maps(a, &km, &vm)) != KV_OK) return st;
   const dim3 grid((unsigned)tiles, (unsigned)a.num_kv_heads, (unsigned)a.max_parts);
-  multi_kernel<D, BS><<<grid, kMThreads, kSmem, s>>>(km, vm, a);
-  return cuda_check(cudaGetLastError(), "multi_kernel launch");
+  if (a.col_max_n == 0) {
+    multi_kernel<D, BS><<<grid, kMThreads, kSmem, s>>>(km, vm, a);
+    return cuda_check(cudaGetLastError(), "multi_kernel launch");
+  }
+  // behind the decode kernel's column groups (it needs nothing from them):
+  // a programmatic dependent, so it starts during their tail
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kMThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_check(cudaLaunchKernelEx(&cfg, multi_kernel<D, BS>, km, vm, a), "multi_kernel launch");
 }
 
 kv_status launch_multi_merge(const DecodeArgs& a, cudaStream_t s) {
@@ -554,13 +572,16 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
   if (q8 != (k_scale != nullptr) || q8 != (v_scale != nullptr))
     return fail(KV_ERR_INVALID_ARG, "%s: 8-bit pools need k_scale and v_scale; bf16 pools take NULL", who);
   const int GQ = num_q_heads / num_kv_heads;
-  // Few query tokens per sequence: the decode kernel's 8 columns per CTA
-  // hold (token, head) pairs, 8 / G tokens per column group.  Otherwise the
-  // row-tiled kernel (bf16 pools).
+  // Sequences with few query tokens (at most 4 x 8 / G): the decode
+  // kernel's 8 columns per CTA hold (token, head) pairs, 8 / G tokens per
+  // column group.  Longer queries: the row-tiled kernel (bf16 pools), in the
+  // same call when both kinds occur.
   const int tpg = GQ <= kMaxGroup ? kMaxGroup / GQ : 0;
-  const int vgroups = tpg > 0 ? (max_query_len + tpg - 1) / tpg : 0;
-  const bool column_path = tpg > 0 && vgroups <= kMaxVGroups;
-  if (!column_path && q8)
+  const int col_max_n = tpg * kMaxVGroups;               // 0 when G > 8
+  const int vgroups = tpg > 0 ? (min(max_query_len, col_max_n) + tpg - 1) / tpg : 0;
+  const bool column_path = tpg > 0;                       // some sequences may use it
+  const bool row_path = max_query_len > col_max_n;        // some sequences may need it
+  if (row_path && q8)
     return fail(KV_ERR_NOT_IMPLEMENTED,
                 "%s: 8-bit pools support up to %d query tokens per sequence here", who,
                 tpg * kMaxVGroups);
@@ -591,6 +612,7 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
   a.num_tokens = num_tokens;
   a.max_query_len = max_query_len;
   a.vgroups = column_path ? vgroups : 1;
+  a.col_max_n = col_max_n;
   a.flags = di.flags;
   a.max_blocks_per_seq = max_blocks_per_seq;
   a.batch = batch;
@@ -600,8 +622,8 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
   a.num_blocks = num_blocks;
   a.block_size = block_size;
   a.max_seq_len = max_seq_len;
-  a.part_tokens = choose_part_tokens(column_path ? batch * vgroups : (int)tiles, num_kv_heads,
-                                     max_seq_len, di.num_sms);
+  a.part_tokens = choose_part_tokens((column_path ? batch * vgroups : 0) + (row_path ? (int)tiles : 0),
+                                     num_kv_heads, max_seq_len, di.num_sms);
   a.max_parts = (max_seq_len + a.part_tokens - 1) / a.part_tokens;
   if (a.max_parts > 65535) return fail(KV_ERR_INVALID_ARG, "%s: too many partitions", who);
   a.slots = a.max_parts;
@@ -617,14 +639,14 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
     a.ws_acc = a.ws_ml + (size_t)num_tokens * num_q_heads * a.max_parts * 2;
   }
   cudaStream_t s = (cudaStream_t)stream;
-  if (column_path) {
-    st = launch_decode(a, s);
-  } else if (head_dim == 128) {
-    st = block_size == 32 ? launch_m<128, 32>(a, (int)tiles, s) : launch_m<128, 16>(a, (int)tiles, s);
-  } else {
-    st = block_size == 32 ? launch_m<64, 32>(a, (int)tiles, s) : launch_m<64, 16>(a, (int)tiles, s);
+  if (column_path && (st = launch_decode(a, s)) != KV_OK) return st;
+  if (row_path) {
+    if (head_dim == 128)
+      st = block_size == 32 ? launch_m<128, 32>(a, (int)tiles, s) : launch_m<128, 16>(a, (int)tiles, s);
+    else
+      st = block_size == 32 ? launch_m<64, 32>(a, (int)tiles, s) : launch_m<64, 16>(a, (int)tiles, s);
+    if (st != KV_OK) return st;
   }
-  if (st != KV_OK) return st;
   return launch_multi_merge(a, s);
 }
 
