@@ -90,6 +90,12 @@ kv_status launch_merge(const DecodeArgs& a, cudaStream_t stream);
 // prefix blocks, one partial per row and prefix chunk.
 kv_status launch_prefix(const DecodeArgs& a, cudaStream_t stream);
 
+// Long multi-token queries on the tensor cores with TMEM accumulators
+// (pagedkv_multi_tc.cu): an upper bound of the 128-row tiles over all
+// sequences, and the launch over `tiles` of them.
+int multi_tc_tiles_upper(int num_tokens, int num_q_heads, int num_kv_heads, int batch);
+kv_status launch_multi_tc(const DecodeArgs& a, int tiles, cudaStream_t stream);
+
 // Token partition length for `work` independent (row group, KV head) units
 // over sequences of up to max_seq_len tokens (power of two in [256, 2048]).
 int choose_part_tokens(int work, int num_kv_heads, int max_seq_len, int num_sms);

@@ -640,13 +640,10 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
   }
   cudaStream_t s = (cudaStream_t)stream;
   if (column_path && (st = launch_decode(a, s)) != KV_OK) return st;
-  if (row_path) {
-    if (head_dim == 128)
-      st = block_size == 32 ? launch_m<128, 32>(a, (int)tiles, s) : launch_m<128, 16>(a, (int)tiles, s);
-    else
-      st = block_size == 32 ? launch_m<64, 32>(a, (int)tiles, s) : launch_m<64, 16>(a, (int)tiles, s);
-    if (st != KV_OK) return st;
-  }
+  if (row_path &&
+      (st = launch_multi_tc(a, multi_tc_tiles_upper(num_tokens, num_q_heads, num_kv_heads, batch), s)) !=
+          KV_OK)
+    return st;
   return launch_multi_merge(a, s);
 }
 

@@ -1,0 +1,562 @@
+// pagedkv_multi_tc.cu -- attention of long multi-token queries (prefill
+// chunks: “LLM 推理优化技术全景”, SARATHI -- 512-token chunks batched with
+// decodes) on the fifth-generation tensor cores, accumulators in TMEM.
+//
+// Sequence b's query token i (of n_b, its last tokens) at position
+// L_b - n_b + i attends positions 0 .. L_b - n_b + i.  A CTA takes 128 rows
+// (query token, grouped head) of one sequence and KV head -- the MMA's M --
+// and one token partition, in chunks of 64 keys:
+//
+//   * warp 4 (one lane issues): TMA tensor loads of each chunk's K and V
+//     blocks into a stage laid out as 64 contiguous 128-byte-swizzled rows per
+//     64-element column band (so one descriptor covers the chunk), then
+//       S[128 x 64]  = Q[128 x d] . K^T          (tcgen05.mma, A and B from smem)
+//       O[128 x d]  += P[128 x 64] . V[64 x d]   (tcgen05.mma, A = P from TMEM)
+//     committing each to an mbarrier;
+//   * warps 0-3 (one row per thread): read S from TMEM, apply the causal mask
+//     and the scale, update the row's running maximum and sum (“LLM 推理优化
+//     技术全景”, 在线 Softmax; “Flash Attention v2 的改进”: deferred
+//     normalisation), write P (bf16) back over its S in TMEM, and at the end
+//     normalise O.  The maximum used for P moves only when a row's scores pass
+//     it by more than 2^8 (then O is rescaled in TMEM): P <= 2^8 stays exact
+//     in the sums, and O and l always share the same reference, so the result
+//     is the softmax's.
+//
+// TMEM: O (d columns) + two 64-column S/P buffers (S of chunk c+1 is computed
+// while chunk c's softmax runs) = 256 columns, two CTAs per SM.  V rows past
+// the sequence end are zeroed in shared memory before P . V (p is 0 there but
+// the pool may hold NaN).  Every wait is bounded; a CTA that gives up flags
+// PAGEDKV_FLAG_WAIT_TIMEOUT, drains its copies and tensor-core work, frees its
+// TMEM and marks its rows bad.  bf16 pools.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "pagedkv_common.cuh"
+#include "pagedkv_device.cuh"
+
+namespace pagedkv {
+namespace {
+
+using namespace dev;
+
+constexpr int kTRows = 128;               // query rows per CTA (the MMA's M)
+constexpr int kChunk = 64;                // keys per chunk (the S MMA's N)
+constexpr int kTStages = 2;               // chunk stages in shared memory
+constexpr int kTThreads = 5 * 32;         // 4 softmax warps + the issuing warp
+constexpr int kTmemCols = 256;
+constexpr float kRescaleLog2 = 8.0f;      // move the reference max past 2^8
+
+template <int D>
+struct TcGeo {
+  static constexpr int kAtoms = D / 64;                  // 64-element (128-byte) column bands
+  static constexpr int kQBytes = kTRows * D * 2;         // Q image
+  static constexpr int kKBytes = kChunk * D * 2;         // K (or V) of a chunk
+  static constexpr int kStageBytes = 2 * kKBytes;
+  static constexpr int kSmemBytes = kQBytes + kTStages * kStageBytes + 1024;
+  static constexpr int kOCol = 0;                        // O in TMEM columns [0, D)
+  static constexpr int kSCol = 128;                      // S/P buffers at 128 and 192
+};
+
+// 128-byte-swizzled K-major / MN-major shared-memory matrix descriptor.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((addr & 0x3FFFF) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;                                // descriptor version
+  d |= (uint64_t)2 << 61;                                // 128-byte swizzle
+  return d;
+}
+
+// kind::f16 instruction descriptor: fp32 D, bf16 A and B, A/B major, N, M.
+__host__ __device__ constexpr uint32_t mma_idesc(int M, int N, int b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn_major << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t acc) {
+  asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+               " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
+               ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                       uint32_t acc) {
+  asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+               " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}"
+               ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 consecutive TMEM columns of this warp's 32 lanes (one row per thread).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+        "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]),
+        "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]),
+        "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+        "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};"
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+        "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]),
+        "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// A bounded mbarrier wait whose outcome the whole warp agrees on (the
+// warp's later tcgen05 loads and stores are collective).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Byte offset of 16-byte chunk `c` (0..7) of row `r` in a 128-byte-swizzled
+// band (the pattern TMA writes; bands start 1024-byte aligned).
+__device__ __forceinline__ uint32_t sw128(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
+
+// Row tiles of a sequence with n query tokens served here (n > col_max_n).
+__device__ __forceinline__ int tc_tiles(int n, int GQ, int col_max_n) {
+  return n > col_max_n ? (n * GQ + kTRows - 1) / kTRows : 0;
+}
+
+template <int D, int BS>
+__global__ void __launch_bounds__(kTThreads, 1)
+    multi_tc_kernel(const __grid_constant__ CUtensorMap k_map,
+                    const __grid_constant__ CUtensorMap v_map, const DecodeArgs a) {
+  using T = TcGeo<D>;
+  using Gm = Geo<D, BS, false>;                          // TMA box geometry of one block
+  constexpr int kBlocksPerChunk = kChunk / BS;
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ uint64_t full_bar[kTStages], empty_bar[kTStages], s_bar[2], p_bar, o_bar, drain_bar;
+  __shared__ uint32_t tmem_base;
+  __shared__ int scan[kTThreads];
+  __shared__ int sh_b, sh_rt, sh_bad, sh_fail;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int Hq = a.num_q_heads, Hkv = a.num_kv_heads, GQ = Hq / Hkv;
+  const int hk = blockIdx.y, part = blockIdx.z, B = a.batch;
+  const int32_t* qs = a.query_start;
+  const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
+  unsigned char* gbase = smem_raw + (base - smem_addr(smem_raw));
+  const uint32_t q_img = base;                           // Q: kAtoms bands of [128 x 64]
+  auto k_img = [&](int s) { return base + T::kQBytes + s * T::kStageBytes; };
+  auto v_img = [&](int s) { return k_img(s) + T::kKBytes; };
+
+  if (tid == 0) {
+    sh_b = -1;
+    sh_bad = 0;
+    sh_fail = 0;
+  }
+  // ---- which (sequence, row tile) CTA x serves (sequences past the column
+  // groups' limit, in order; as in the row-tiled kernel)
+  const int per = (B + kTThreads - 1) / kTThreads;
+  int mine = 0;
+  for (int i = 0; i < per; ++i) {
+    const int b = tid * per + i;
+    if (b < B) mine += tc_tiles(qs[b + 1] - qs[b], GQ, a.col_max_n);
+  }
+  scan[tid] = mine;
+  __syncthreads();
+  for (int off = 1; off < kTThreads; off <<= 1) {
+    const int v = tid >= off ? scan[tid - off] : 0;
+    __syncthreads();
+    scan[tid] += v;
+    __syncthreads();
+  }
+  const int x = blockIdx.x;
+  if (x >= scan[tid] - mine && x < scan[tid]) {
+    int acc = scan[tid] - mine;
+    for (int i = 0; i < per; ++i) {
+      const int b = tid * per + i;
+      if (b >= B) break;
+      const int tl = tc_tiles(qs[b + 1] - qs[b], GQ, a.col_max_n);
+      if (x < acc + tl) {
+        sh_b = b;
+        sh_rt = x - acc;
+        break;
+      }
+      acc += tl;
+    }
+  }
+  __syncthreads();
+  if (sh_b < 0) return;                                  // past the last tile (CTA-uniform)
+  const int b = sh_b, rt = sh_rt;
+  const int q0 = qs[b], n = qs[b + 1] - q0;
+  const int L = a.seq_lens[b];
+  const int t0 = part * a.part_tokens;
+  if (t0 >= L && L > 0) return;                          // no such partition for this sequence
+  const bool rows_ok = q0 >= 0 && q0 + n <= a.num_tokens;
+  const bool len_ok = rows_ok && L > 0 && n <= L && n <= a.max_query_len && L <= a.max_seq_len &&
+                      (int64_t)L <= (int64_t)a.max_blocks_per_seq * BS;
+  const int rows_b = n * GQ;
+  const int row0 = rt * kTRows;
+  const int last_row = min(row0 + kTRows, rows_b) - 1;
+  const int pos_max = L - n + last_row / GQ;
+  const int t_end = min(min(t0 + a.part_tokens, L), pos_max + 1);
+  const int nch = (len_ok && t_end > t0) ? (t_end - t0 + kChunk - 1) / kChunk : 0;
+  const int first_blk = t0 / BS;
+  const int last_blk = nch > 0 ? (t_end - 1) / BS : first_blk - 1;
+  const int32_t* bt = a.block_tables + (int64_t)b * a.max_blocks_per_seq;
+  for (int j = first_blk + tid; j <= last_blk; j += kTThreads) {
+    const int32_t p = bt[j];
+    if (p < 0 || p >= a.num_blocks) sh_bad = 1;
+  }
+  // This thread's row (softmax warps): (query token, grouped head)
+  const int r = row0 + tid;                              // meaningful for tid < 128
+  const bool row_valid = tid < kTRows && len_ok && r < rows_b;
+  const int pos = row_valid ? L - n + r / GQ : -1;
+  const int64_t qrow = row_valid ? (int64_t)(q0 + r / GQ) * Hq + (int64_t)hk * GQ + r % GQ : 0;
+  // Q row into its swizzled bands (zeros for rows past the sequence's queries)
+  if (tid < kTRows) {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) + qrow * D);
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) {
+      const uint4 v = row_valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(gbase + (c / 8) * (kTRows * 128) + sw128(tid, c % 8)) = v;
+    }
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kTStages; ++s) {
+      mbar_init(smem_addr(&full_bar[s]), 1);
+      mbar_init(smem_addr(&empty_bar[s]), 1);
+    }
+    mbar_init(smem_addr(&s_bar[0]), 1);
+    mbar_init(smem_addr(&s_bar[1]), 1);
+    mbar_init(smem_addr(&p_bar), kTRows);
+    mbar_init(smem_addr(&o_bar), 1);
+    mbar_init(smem_addr(&drain_bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  const bool work = nch > 0;
+  if (work && warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_addr(&tmem_base)), "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // Q image -> tensor core
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const bool bad = sh_bad != 0;
+  const uint32_t tm = tmem_base;
+  float m_ref = -INFINITY, l = 0.0f;
+
+  if (work && !bad) {
+    if (warp == 4) {
+      // ======================= loads and tensor-core issue ==================
+      bool ok = true;
+      int issued = 0;
+      auto load = [&](int c) {                           // lane 0 only; stage free
+        const int s = c % kTStages;
+        const int blk0 = first_blk + c * kBlocksPerChunk;
+        const int nb = min(kBlocksPerChunk, last_blk - blk0 + 1);
+        const uint32_t fb = smem_addr(&full_bar[s]);
+        mbar_expect_tx(fb, (uint32_t)(nb * Gm::kBlockBytes));
+        for (int j = 0; j < nb; ++j) {
+          const int p = bt[blk0 + j];
+#pragma unroll
+          for (int xx = 0; xx < Gm::kBoxes; ++xx) {
+            // band xx of the chunk image, rows j*BS .. j*BS + BS - 1
+            const uint32_t off = xx * (kChunk * 128) + j * (BS * 128);
+            tma_load_4d(k_img(s) + off, &k_map, fb, xx * Gm::kBoxElems, hk, 0, p);
+            tma_load_4d(v_img(s) + off, &v_map, fb, xx * Gm::kBoxElems, hk, 0, p);
+          }
+        }
+      };
+      if (lane == 0)
+        for (int c = 0; c < kTStages && c < nch; ++c) load(c);
+      issued = min(kTStages, nch);
+      const uint32_t id_s = mma_idesc(kTRows, kChunk, 0);
+      const uint32_t id_o = mma_idesc(kTRows, D, 1);
+      for (int c = 0; c <= nch && ok; ++c) {
+        if (c < nch) {
+          const int s = c % kTStages;
+          if (!warp_wait(smem_addr(&full_bar[s]), (c / kTStages) & 1)) { ok = false; break; }
+          // V rows at or past the sequence end in this chunk -> 0 (both bands)
+          const int cstart = t0 + c * kChunk;
+          if (L < cstart + kChunk && L > cstart && (L % BS) != 0) {
+            const int row_lo = L - cstart, row_hi = min(kChunk, ((L + BS - 1) / BS) * BS - cstart);
+            const int nrow = row_hi - row_lo;
+            for (int i = lane; i < nrow * 8 * T::kAtoms; i += 32) {
+              const int rr = row_lo + i / (8 * T::kAtoms), rest = i % (8 * T::kAtoms);
+              const int band = rest / 8, cc = rest % 8;
+              *reinterpret_cast<uint4*>(gbase + (v_img(s) - base) + band * (kChunk * 128) + sw128(rr, cc)) =
+                  make_uint4(0u, 0u, 0u, 0u);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          }
+          __syncwarp();
+          // S(c) reuses the TMEM buffer of chunk c-2: its P must be consumed
+          if (c >= 2 && !warp_wait(smem_addr(&o_bar), (c - 2) & 1)) { ok = false; break; }
+          if (lane == 0) {
+            tc_fence_after();
+            const uint32_t s_tmem = tm + T::kSCol + (c & 1) * kChunk;
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const uint64_t ad = smem_desc(q_img + (ks / 4) * (kTRows * 128) + (ks % 4) * 32, 16, 1024);
+              const uint64_t bd = smem_desc(k_img(s) + (ks / 4) * (kChunk * 128) + (ks % 4) * 32, 16, 1024);
+              mma_ss(s_tmem, ad, bd, id_s, ks > 0);
+            }
+            mma_commit(smem_addr(&s_bar[c & 1]));
+          }
+          __syncwarp();
+        }
+        if (c >= 1) {
+          const int cp = c - 1, s = cp % kTStages;
+          if (!warp_wait(smem_addr(&p_bar), cp & 1)) { ok = false; break; }
+          const int cstart = t0 + cp * kChunk;
+          const int nsub = (min(t_end, cstart + kChunk) - cstart + 15) / 16;
+          if (lane == 0) {
+            tc_fence_after();
+            const uint32_t p_tmem = tm + T::kSCol + (cp & 1) * kChunk;
+            for (int kk = 0; kk < nsub; ++kk) {
+              const uint64_t bd = smem_desc(v_img(s) + kk * (16 * 128), kChunk * 128, 1024);
+              mma_ts(tm + T::kOCol, p_tmem + kk * 8, bd, id_o, (cp > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(smem_addr(&o_bar));
+            mma_commit(smem_addr(&empty_bar[s]));
+          }
+          __syncwarp();
+          // refill the stage with chunk cp + kTStages once P . V has read it
+          if (cp + kTStages < nch) {
+            if (!warp_wait(smem_addr(&empty_bar[s]), (cp / kTStages) & 1)) { ok = false; break; }
+            if (lane == 0) load(cp + kTStages);
+            issued = cp + kTStages + 1;
+          }
+        }
+      }
+      if (!ok && lane == 0) sh_fail = 1;
+      // every load issued has landed before the CTA may exit (bounded)
+      if (lane == 0)
+        for (int s = 0; s < kTStages && s < issued; ++s) {
+          const int last = s + kTStages * ((issued - 1 - s) / kTStages);
+          mbar_wait(smem_addr(&full_bar[s]), (last / kTStages) & 1);
+        }
+    } else {
+      // ======================= softmax: one row per thread ==================
+      const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+      bool ok = true;
+      for (int c = 0; c < nch; ++c) {
+        if (__shfl_sync(0xffffffffu, sh_fail, 0)) { ok = false; break; }
+        if (!warp_wait(smem_addr(&s_bar[c & 1]), (c >> 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t s_tmem = tm + lane_base + T::kSCol + (c & 1) * kChunk;
+        uint32_t raw[2][32];
+        tmem_ld32(s_tmem, raw[0]);
+        tmem_ld32(s_tmem + 32, raw[1]);
+        tmem_wait_ld();
+        const int cstart = t0 + c * kChunk;
+        const int lim = min(pos, t_end - 1);             // last key this row may see
+        float mx = -INFINITY;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int tok = cstart + 32 * h + j;
+            const float v = tok <= lim ? __uint_as_float(raw[h][j]) * a.scale_log2 : -INFINITY;
+            raw[h][j] = __float_as_uint(v);
+            mx = fmaxf(mx, v);
+          }
+        // move the reference maximum only when it is passed by > 2^8
+        const bool need = m_ref == -INFINITY ? mx > -INFINITY : mx > m_ref + kRescaleLog2;
+        const float m_new = need ? mx : m_ref;
+        const float zero_ref = m_new == -INFINITY ? 0.0f : m_new;
+        uint32_t pw[2][16];
+        float lsum = 0.0f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float p0 = exp2f(__uint_as_float(raw[h][2 * j]) - zero_ref);
+            const float p1 = exp2f(__uint_as_float(raw[h][2 * j + 1]) - zero_ref);
+            lsum += p0 + p1;
+            __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
+            pw[h][j] = *reinterpret_cast<uint32_t*>(&pp);
+          }
+        // P . V of chunk c-1 has finished (O is stable, and the issuing
+        // thread has taken chunk c-1's P before this chunk's arrives)
+        if (c > 0) {
+          if (!warp_wait(smem_addr(&o_bar), (c - 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, need)) {             // rescale O in TMEM
+            const float alpha = need ? (m_ref == -INFINITY ? 0.0f : exp2f(m_ref - m_new)) : 1.0f;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t ov[32];
+              tmem_ld32(tm + lane_base + T::kOCol + c0, ov);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
+              tmem_st32(tm + lane_base + T::kOCol + c0, ov);
+            }
+            tmem_wait_st();
+            l *= alpha;
+          }
+        }
+        m_ref = m_new;
+        l += lsum;
+        // P (bf16 pairs, 32 columns) over this chunk's S
+        tmem_st16(s_tmem, pw[0]);
+        tmem_st16(s_tmem + 16, pw[1]);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(smem_addr(&p_bar));
+      }
+      if (ok && !warp_wait(smem_addr(&o_bar), (nch - 1) & 1)) ok = false;
+      if (!ok) sh_fail = 1;
+      tc_fence_after();
+    }
+  }
+  __syncthreads();
+  const bool failed = bad || sh_fail != 0 || !len_ok;
+  if (work && !bad && warp == 4 && lane == 0) {
+    // all tensor-core work of this CTA completes before TMEM is read or freed
+    tc_fence_after();
+    mma_commit(smem_addr(&drain_bar));
+    if (!mbar_wait(smem_addr(&drain_bar), 0)) sh_fail = 1;
+  }
+  __syncthreads();
+  if (bad && tid == 0) atomicOr(a.flags, PAGEDKV_FLAG_BAD_BLOCK);
+  if (sh_fail && tid == 0) atomicOr(a.flags, PAGEDKV_FLAG_WAIT_TIMEOUT);
+  if (!len_ok && tid == 0 && rt == 0 && hk == 0 && part == 0) atomicOr(a.flags, PAGEDKV_FLAG_BAD_SEQ_LEN);
+
+  // ---- epilogue: this thread's row (TMEM read by whole warps)
+  if (warp < 4 && rows_ok) {
+    const bool mine_row = r < rows_b;
+    const int64_t orow = mine_row ? (int64_t)(q0 + r / GQ) * Hq + (int64_t)hk * GQ + r % GQ : 0;
+    const bool split = a.max_parts > 1;
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    const bool have = work && !failed;                   // CTA-uniform
+    const float inv = (have && l > 0.0f) ? 1.0f / l : 0.0f;
+    const int64_t slot = orow * a.max_parts + part;
+    if (split && mine_row) {
+      a.ws_ml[2 * slot] = m_ref;
+      a.ws_ml[2 * slot + 1] = failed ? -1.0f : (have ? l : 0.0f);
+    }
+#pragma unroll
+    for (int c0 = 0; c0 < D; c0 += 32) {
+      uint32_t ov[32];
+      if (have) {
+        tmem_ld32(tm + lane_base + T::kOCol + c0, ov);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) ov[j] = 0u;
+      }
+      if (!mine_row) continue;
+      if (!split) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + orow * D + c0;
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(ov[j + 2 * e]) * inv,
+                                                     __uint_as_float(ov[j + 2 * e + 1]) * inv);
+            w[e] = *reinterpret_cast<uint32_t*>(&h);
+          }
+          *reinterpret_cast<uint4*>(out + j) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      } else {
+        float* acc = a.ws_acc + slot * D + c0;
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          *reinterpret_cast<float4*>(acc + j) =
+              make_float4(__uint_as_float(ov[j]), __uint_as_float(ov[j + 1]),
+                          __uint_as_float(ov[j + 2]), __uint_as_float(ov[j + 3]));
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (work && warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tm), "r"(kTmemCols)
+                 : "memory");
+}
+
+template <int D, int BS>
+kv_status launch_tc(const DecodeArgs& a, int tiles, cudaStream_t s) {
+  using T = TcGeo<D>;
+  static std::mutex mu;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  kv_status st = cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
+  if (st != KV_OK) return st;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+      st = cuda_check(cudaFuncSetAttribute(multi_tc_kernel<D, BS>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmemBytes),
+                      "cudaFuncSetAttribute(multi_tc_kernel)");
+      if (st != KV_OK) return st;
+      attr_set[dev] = true;
+    }
+  }
+  alignas(64) CUtensorMap km, vm;
+  if ((st = make_kv_maps(a, &km, &vm)) != KV_OK) return st;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)tiles, (unsigned)a.num_kv_heads, (unsigned)a.max_parts);
+  cfg.blockDim = dim3(kTThreads);
+  cfg.dynamicSmemBytes = T::kSmemBytes;
+  cfg.stream = s;
+  // behind the decode kernel's column groups (nothing read from them): a
+  // programmatic dependent, started while they run
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.col_max_n > 0 ? 1 : 0;
+  return cuda_check(cudaLaunchKernelEx(&cfg, multi_tc_kernel<D, BS>, km, vm, a),
+                    "multi_tc_kernel launch");
+}
+
+}  // namespace
+
+int multi_tc_tiles_upper(int num_tokens, int num_q_heads, int num_kv_heads, int batch) {
+  const int GQ = num_q_heads / num_kv_heads;
+  return (int)(((int64_t)num_tokens * GQ + kTRows - 1) / kTRows) + batch;
+}
+
+kv_status launch_multi_tc(const DecodeArgs& a, int tiles, cudaStream_t s) {
+  if (a.head_dim == 128)
+    return a.block_size == 32 ? launch_tc<128, 32>(a, tiles, s) : launch_tc<128, 16>(a, tiles, s);
+  return a.block_size == 32 ? launch_tc<64, 32>(a, tiles, s) : launch_tc<64, 16>(a, tiles, s);
+}
+
+}  // namespace pagedkv
