@@ -433,7 +433,8 @@ def measure_multi(config, pkv, dev, stream, peak, replays=40):
                          "algorithmic_bytes_per_step": step_bytes},
             "tensor": {"achieved_tflops": round(fl / us / 1e6, 2), "peak_tflops": tpeak,
                        "frac": round(fl / us / 1e6 / tpeak, 4), "flops_per_step": fl,
-                       "note": "mma.sync m16n8k16 bf16; peak = measured cuBLAS bf16 (burst)"}}
+                       "note": "long queries on tcgen05 (TMEM accumulators), few on mma.sync "
+                               "m16n8k16; peak = measured cuBLAS bf16 (burst)"}}
 
 
 def gpu_arm(args, rank, world, local_rank, dist):
@@ -603,7 +604,8 @@ def gpu_arm(args, rank, world, local_rank, dist):
                    "l2": "inputs larger than L2 (KV read per step > 129 MB), no flush",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm",
-                     "kernel": ("token slot mapping + append + multi_kernel (+ multi_merge_kernel), "
+                     "kernel": ("token slot mapping + append + decode_kernel column groups / "
+                                "multi_tc_kernel (+ multi_merge_kernel), "
                                 "paged_attention_multi" if multi else
                                 "prefix_kernel + decode_kernel (append fused) + merge_kernel, one "
                                 "pagedkv_decode_step_prefix" if use_prefix else

@@ -467,7 +467,8 @@ size_t pagedkv_multi_workspace_bytes(int num_tokens, int num_q_heads,
  * Asynchronous on `stream`: one attention launch, plus a log-sum-exp merge
  * launch when the keys are split into partitions.  With at most 4 * (8 / G)
  * query tokens per sequence the decode kernel serves them (8 (token, head)
- * columns per CTA); longer queries go to a row-tiled kernel. */
+ * columns per CTA); longer queries go to a tensor-core kernel with TMEM
+ * accumulators (128 query rows per CTA). */
 kv_status paged_attention_multi(void *out, const void *q, const void *k_cache,
                                 const void *v_cache, const float *k_scale,
                                 const float *v_scale, const int32_t *block_tables,

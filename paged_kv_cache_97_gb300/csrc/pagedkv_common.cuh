@@ -91,9 +91,8 @@ kv_status launch_merge(const DecodeArgs& a, cudaStream_t stream);
 kv_status launch_prefix(const DecodeArgs& a, cudaStream_t stream);
 
 // Long multi-token queries on the tensor cores with TMEM accumulators
-// (pagedkv_multi_tc.cu): an upper bound of the 128-row tiles over all
-// sequences, and the launch over `tiles` of them.
-int multi_tc_tiles_upper(int num_tokens, int num_q_heads, int num_kv_heads, int batch);
+// (pagedkv_multi_tc.cu), over `tiles` CTAs (an upper bound of the 128-row
+// tiles of all sequences; the extra ones exit at once).
 kv_status launch_multi_tc(const DecodeArgs& a, int tiles, cudaStream_t stream);
 
 // Token partition length for `work` independent (row group, KV head) units

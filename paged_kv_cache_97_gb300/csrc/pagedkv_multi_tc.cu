@@ -548,11 +548,6 @@ kv_status launch_tc(const DecodeArgs& a, int tiles, cudaStream_t s) {
 
 }  // namespace
 
-int multi_tc_tiles_upper(int num_tokens, int num_q_heads, int num_kv_heads, int batch) {
-  const int GQ = num_q_heads / num_kv_heads;
-  return (int)(((int64_t)num_tokens * GQ + kTRows - 1) / kTRows) + batch;
-}
-
 kv_status launch_multi_tc(const DecodeArgs& a, int tiles, cudaStream_t s) {
   if (a.head_dim == 128)
     return a.block_size == 32 ? launch_tc<128, 32>(a, tiles, s) : launch_tc<128, 16>(a, tiles, s);

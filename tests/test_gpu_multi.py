@@ -6,8 +6,8 @@ The step's tokens are appended with the general slot mapping and
 reshape_and_cache (pools compared bit for bit with the oracle's), then
 attended causally; outputs within max-abs 1e-2 / mean-abs 1e-3 of the fp64
 oracle (3e-2 / 1e-3 for 8-bit pools), on small cases covering both kernels
-(decode-kernel column groups for few query tokens, the row-tiled kernel for
-many), the one-partition path and the split path with its merge, and on
+(decode-kernel column groups for few query tokens, the tcgen05 tensor-core
+kernel for many), the one-partition path and the split path with its merge, and on
 sampled sequences of the full-size workloads.
 """
 import os
