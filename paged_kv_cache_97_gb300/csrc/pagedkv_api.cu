@@ -272,9 +272,6 @@ kv_status launch_merge(const DecodeArgs& a, cudaStream_t stream) {
 // Partition size
 // ---------------------------------------------------------------------------
 
-static const int kMinPartTokens = 256;
-static const int kMaxPartTokens = 2048;
-
 // Largest power-of-two partition in [256, 2048] that still gives at least
 // 8 CTAs per SM over (sequence, KV head, partition).  Longer partitions
 // measured slower on GB300 (fewer, longer CTAs leave a longer tail).  The environment

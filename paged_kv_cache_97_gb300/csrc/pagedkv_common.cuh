@@ -34,6 +34,10 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // Query heads per KV head the kernels serve (the MMA's N = 8 columns).
 constexpr int kMaxGroup = 8;
 
+// Token partitions of the split-K path: powers of two in [256, 2048].
+constexpr int kMinPartTokens = 256;
+constexpr int kMaxPartTokens = 2048;
+
 // log2(e): scores are kept in the base-2 domain so exp() becomes exp2().
 constexpr float kLog2e = 1.4426950408889634f;
 

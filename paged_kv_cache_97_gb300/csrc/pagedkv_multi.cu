@@ -194,6 +194,8 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
                                      num_kv_heads, max_seq_len, di.num_sms);
   a.max_parts = (max_seq_len + a.part_tokens - 1) / a.part_tokens;
   if (a.max_parts > 65535) return fail(KV_ERR_INVALID_ARG, "%s: too many partitions", who);
+  if (row_path && tiles * num_kv_heads * a.max_parts > 0x7fffffffLL)
+    return fail(KV_ERR_INVALID_ARG, "%s: too many query tokens", who);
   a.slots = a.max_parts;
   a.scale_log2 = scale * kLog2e;
   a.dtype = dtype;

@@ -7,25 +7,32 @@
 // (query token, grouped head) of one sequence and KV head -- the MMA's M --
 // and one token partition, in chunks of 64 keys:
 //
-//   * warp 4 (one lane issues): TMA tensor loads of each chunk's K and V
-//     blocks into a stage laid out as 64 contiguous 128-byte-swizzled rows per
-//     64-element column band (so one descriptor covers the chunk), then
+//   * warp 5 (one lane issues): TMA tensor loads of each chunk's K and V
+//     blocks (ids staged in shared memory) into stages laid out as 64
+//     contiguous 128-byte-swizzled rows per 64-element column band, so one
+//     descriptor covers the chunk; K's stage is refilled once S of its chunk
+//     is done, V's once P . V of its chunk is;
+//   * warp 4 (one lane issues):
 //       S[128 x 64]  = Q[128 x d] . K^T          (tcgen05.mma, A and B from smem)
 //       O[128 x d]  += P[128 x 64] . V[64 x d]   (tcgen05.mma, A = P from TMEM)
-//     committing each to an mbarrier;
+//     in the order S(0), S(1), P.V(0), S(2), P.V(1), ..., committing each to
+//     mbarriers;
 //   * warps 0-3 (one row per thread): read S from TMEM, apply the causal mask
-//     and the scale, update the row's running maximum and sum (“LLM 推理优化
-//     技术全景”, 在线 Softmax; “Flash Attention v2 的改进”: deferred
-//     normalisation), write P (bf16) back over its S in TMEM, and at the end
-//     normalise O.  The maximum used for P moves only when a row's scores pass
-//     it by more than 2^8 (then O is rescaled in TMEM): P <= 2^8 stays exact
-//     in the sums, and O and l always share the same reference, so the result
-//     is the softmax's.
+//     (only in chunks that cross a row's last key) and the scale, update the
+//     row's running maximum and sum (“LLM 推理优化技术全景”, 在线 Softmax;
+//     “Flash Attention v2 的改进”: deferred normalisation), write P (bf16)
+//     back over its S in TMEM, and at the end normalise O.  The maximum used
+//     for P moves only when a row's scores pass it by more than 2^8 (then O is
+//     rescaled in TMEM): P <= 2^8 stays exact in the sums, and O and l always
+//     share the same reference, so the result is the softmax's.  A negative
+//     scale flips Q's signs instead (exact), so maxima are taken on raw scores.
 //
 // TMEM: O (d columns) + two 64-column S/P buffers (S of chunk c+1 is computed
-// while chunk c's softmax runs) = 256 columns, two CTAs per SM.  V rows past
-// the sequence end are zeroed in shared memory before P . V (p is 0 there but
-// the pool may hold NaN).  Every wait is bounded; a CTA that gives up flags
+// while chunk c's softmax runs) = 256 columns, two CTAs per SM.  CTAs are
+// numbered KV head fastest, then partition, then row tile, so the real tiles
+// are dispatched before the bound's surplus.  V rows past the sequence end
+// are zeroed in shared memory before P . V (p is 0 there but the pool may
+// hold NaN).  Every wait is bounded; a CTA that gives up flags
 // PAGEDKV_FLAG_WAIT_TIMEOUT, drains its copies and tensor-core work, frees its
 // TMEM and marks its rows bad.  bf16 pools.
 #include <cuda.h>
@@ -44,8 +51,9 @@ using namespace dev;
 
 constexpr int kTRows = 128;               // query rows per CTA (the MMA's M)
 constexpr int kChunk = 64;                // keys per chunk (the S MMA's N)
-constexpr int kTStages = 2;               // chunk stages in shared memory
-constexpr int kTThreads = 5 * 32;         // 4 softmax warps + the issuing warp
+constexpr int kKStages = 2;               // K of a chunk: free once S of the chunk is done
+constexpr int kVStages = 2;               // V of a chunk: free once P . V of the chunk is done
+constexpr int kTThreads = 6 * 32;         // 4 softmax warps, the MMA warp, the load warp
 constexpr int kTmemCols = 256;
 constexpr float kRescaleLog2 = 8.0f;      // move the reference max past 2^8
 
@@ -54,8 +62,7 @@ struct TcGeo {
   static constexpr int kAtoms = D / 64;                  // 64-element (128-byte) column bands
   static constexpr int kQBytes = kTRows * D * 2;         // Q image
   static constexpr int kKBytes = kChunk * D * 2;         // K (or V) of a chunk
-  static constexpr int kStageBytes = 2 * kKBytes;
-  static constexpr int kSmemBytes = kQBytes + kTStages * kStageBytes + 1024;
+  static constexpr int kSmemBytes = kQBytes + (kKStages + kVStages) * kKBytes + 1024;
   static constexpr int kOCol = 0;                        // O in TMEM columns [0, D)
   static constexpr int kSCol = 128;                      // S/P buffers at 128 and 192
 };
@@ -150,33 +157,87 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 // band (the pattern TMA writes; bands start 1024-byte aligned).
 __device__ __forceinline__ uint32_t sw128(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
 
+// 2^x on the special-function unit (PTX ex2.approx.ftz.f32: relative error
+// about 2^-22, results below 2^-126 flushed to 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Largest raw score of a chunk row (keys past `lim` left out when kMask),
+// four independent partial maxima.
+template <bool kMask, int kH>
+__device__ __forceinline__ float chunk_max(const uint32_t (&raw)[kH][32], int first_tok, int lim) {
+  float mr[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int h = 0; h < kH; ++h)
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      float v = __uint_as_float(raw[h][j]);
+      if (kMask && first_tok + 32 * h + j > lim) v = -INFINITY;
+      mr[j & 3] = fmaxf(mr[j & 3], v);
+    }
+  return fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3]));
+}
+
+// p = 2^(s * sl2 - ref) of a chunk row as bf16 pairs (0 for keys past `lim`
+// when kMask); returns the fp32 sum of the p.
+template <bool kMask, int kH>
+__device__ __forceinline__ float chunk_exp(const uint32_t (&raw)[kH][32], uint32_t (&pw)[kH][16],
+                                           int first_tok, int lim, float sl2, float ref) {
+  float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+  for (int h = 0; h < kH; ++h)
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      float p0 = ex2(fmaf(__uint_as_float(raw[h][2 * j]), sl2, -ref));
+      float p1 = ex2(fmaf(__uint_as_float(raw[h][2 * j + 1]), sl2, -ref));
+      if (kMask) {
+        const int tok = first_tok + 32 * h + 2 * j;
+        p0 = tok <= lim ? p0 : 0.0f;
+        p1 = tok + 1 <= lim ? p1 : 0.0f;
+      }
+      ls[(2 * j) & 3] += p0;
+      ls[(2 * j + 1) & 3] += p1;
+      __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
+      pw[h][j] = *reinterpret_cast<uint32_t*>(&pp);
+    }
+  return (ls[0] + ls[1]) + (ls[2] + ls[3]);
+}
+
 // Row tiles of a sequence with n query tokens served here (n > col_max_n).
 __device__ __forceinline__ int tc_tiles(int n, int GQ, int col_max_n) {
   return n > col_max_n ? (n * GQ + kTRows - 1) / kTRows : 0;
 }
 
 template <int D, int BS>
-__global__ void __launch_bounds__(kTThreads, 1)
+__global__ void __launch_bounds__(kTThreads, 2)
     multi_tc_kernel(const __grid_constant__ CUtensorMap k_map,
                     const __grid_constant__ CUtensorMap v_map, const DecodeArgs a) {
   using T = TcGeo<D>;
   using Gm = Geo<D, BS, false>;                          // TMA box geometry of one block
   constexpr int kBlocksPerChunk = kChunk / BS;
   extern __shared__ unsigned char smem_raw[];
-  __shared__ uint64_t full_bar[kTStages], empty_bar[kTStages], s_bar[2], p_bar, o_bar, drain_bar;
+  __shared__ uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
+  __shared__ uint64_t s_bar[2], p_bar[2], o_bar, drain_bar;
   __shared__ uint32_t tmem_base;
   __shared__ int scan[kTThreads];
   __shared__ int sh_b, sh_rt, sh_bad, sh_fail;
+  __shared__ int32_t blk_ids[kMaxPartTokens / 16];       // this partition's physical blocks
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hq = a.num_q_heads, Hkv = a.num_kv_heads, GQ = Hq / Hkv;
-  const int hk = blockIdx.y, part = blockIdx.z, B = a.batch;
+  // CTA x: KV head fastest, then partition, then row tile, so that the real
+  // tiles (the first ones) are dispatched before the bound's surplus.
+  const int hk = blockIdx.x % Hkv, part = (blockIdx.x / Hkv) % a.max_parts;
+  const int B = a.batch;
   const int32_t* qs = a.query_start;
   const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
   unsigned char* gbase = smem_raw + (base - smem_addr(smem_raw));
   const uint32_t q_img = base;                           // Q: kAtoms bands of [128 x 64]
-  auto k_img = [&](int s) { return base + T::kQBytes + s * T::kStageBytes; };
-  auto v_img = [&](int s) { return k_img(s) + T::kKBytes; };
+  auto k_img = [&](int s) { return base + T::kQBytes + s * T::kKBytes; };
+  auto v_img = [&](int s) { return base + T::kQBytes + (kKStages + s) * T::kKBytes; };
 
   if (tid == 0) {
     sh_b = -1;
@@ -199,7 +260,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
     scan[tid] += v;
     __syncthreads();
   }
-  const int x = blockIdx.x;
+  const int x = blockIdx.x / (Hkv * a.max_parts);        // row tile over all sequences
   if (x >= scan[tid] - mine && x < scan[tid]) {
     int acc = scan[tid] - mine;
     for (int i = 0; i < per; ++i) {
@@ -233,32 +294,48 @@ __global__ void __launch_bounds__(kTThreads, 1)
   const int first_blk = t0 / BS;
   const int last_blk = nch > 0 ? (t_end - 1) / BS : first_blk - 1;
   const int32_t* bt = a.block_tables + (int64_t)b * a.max_blocks_per_seq;
+  // the partition's block ids, checked and kept in shared memory (the host
+  // holds partitions to kMaxPartTokens tokens)
   for (int j = first_blk + tid; j <= last_blk; j += kTThreads) {
     const int32_t p = bt[j];
     if (p < 0 || p >= a.num_blocks) sh_bad = 1;
+    blk_ids[j - first_blk] = p;
   }
   // This thread's row (softmax warps): (query token, grouped head)
   const int r = row0 + tid;                              // meaningful for tid < 128
   const bool row_valid = tid < kTRows && len_ok && r < rows_b;
   const int pos = row_valid ? L - n + r / GQ : -1;
   const int64_t qrow = row_valid ? (int64_t)(q0 + r / GQ) * Hq + (int64_t)hk * GQ + r % GQ : 0;
-  // Q row into its swizzled bands (zeros for rows past the sequence's queries)
+  // Q row into its swizzled bands (zeros for rows past the sequence's
+  // queries).  A negative scale flips Q's signs instead (exact), so that the
+  // softmax below scales S by |scale| and may take maxima of raw scores.
+  const float sl2 = fabsf(a.scale_log2);
   if (tid < kTRows) {
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) + qrow * D);
+    const uint32_t flip = a.scale_log2 < 0.0f ? 0x80008000u : 0u;
 #pragma unroll
     for (int c = 0; c < D / 8; ++c) {
-      const uint4 v = row_valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+      uint4 v = row_valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+      v.x ^= flip;
+      v.y ^= flip;
+      v.z ^= flip;
+      v.w ^= flip;
       *reinterpret_cast<uint4*>(gbase + (c / 8) * (kTRows * 128) + sw128(tid, c % 8)) = v;
     }
   }
   if (tid == 0) {
-    for (int s = 0; s < kTStages; ++s) {
-      mbar_init(smem_addr(&full_bar[s]), 1);
-      mbar_init(smem_addr(&empty_bar[s]), 1);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(smem_addr(&k_full[s]), 1);
+      mbar_init(smem_addr(&k_empty[s]), 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(smem_addr(&v_full[s]), 1);
+      mbar_init(smem_addr(&v_empty[s]), 1);
     }
     mbar_init(smem_addr(&s_bar[0]), 1);
     mbar_init(smem_addr(&s_bar[1]), 1);
-    mbar_init(smem_addr(&p_bar), kTRows);
+    mbar_init(smem_addr(&p_bar[0]), kTRows);
+    mbar_init(smem_addr(&p_bar[1]), kTRows);
     mbar_init(smem_addr(&o_bar), 1);
     mbar_init(smem_addr(&drain_bar), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -279,37 +356,37 @@ __global__ void __launch_bounds__(kTThreads, 1)
 
   if (work && !bad) {
     if (warp == 4) {
-      // ======================= loads and tensor-core issue ==================
+      // ======================= tensor-core issue ===========================
+      // Order S(0), S(1), P.V(0), S(2), P.V(1), ...; the load warp refills K's
+      // stage once S of its chunk is done, V's once P . V of its chunk is.
       bool ok = true;
-      int issued = 0;
-      auto load = [&](int c) {                           // lane 0 only; stage free
-        const int s = c % kTStages;
-        const int blk0 = first_blk + c * kBlocksPerChunk;
-        const int nb = min(kBlocksPerChunk, last_blk - blk0 + 1);
-        const uint32_t fb = smem_addr(&full_bar[s]);
-        mbar_expect_tx(fb, (uint32_t)(nb * Gm::kBlockBytes));
-        for (int j = 0; j < nb; ++j) {
-          const int p = bt[blk0 + j];
-#pragma unroll
-          for (int xx = 0; xx < Gm::kBoxes; ++xx) {
-            // band xx of the chunk image, rows j*BS .. j*BS + BS - 1
-            const uint32_t off = xx * (kChunk * 128) + j * (BS * 128);
-            tma_load_4d(k_img(s) + off, &k_map, fb, xx * Gm::kBoxElems, hk, 0, p);
-            tma_load_4d(v_img(s) + off, &v_map, fb, xx * Gm::kBoxElems, hk, 0, p);
-          }
-        }
-      };
-      if (lane == 0)
-        for (int c = 0; c < kTStages && c < nch; ++c) load(c);
-      issued = min(kTStages, nch);
       const uint32_t id_s = mma_idesc(kTRows, kChunk, 0);
       const uint32_t id_o = mma_idesc(kTRows, D, 1);
       for (int c = 0; c <= nch && ok; ++c) {
         if (c < nch) {
-          const int s = c % kTStages;
-          if (!warp_wait(smem_addr(&full_bar[s]), (c / kTStages) & 1)) { ok = false; break; }
+          const int s = c % kKStages;
+          if (!warp_wait(smem_addr(&k_full[s]), (c / kKStages) & 1)) { ok = false; break; }
+          // S(c) reuses the TMEM buffer of chunk c-2: P . V(c-2) must be done
+          if (c >= 2 && !warp_wait(smem_addr(&o_bar), (c - 2) & 1)) { ok = false; break; }
+          if (lane == 0) {
+            tc_fence_after();
+            const uint32_t s_tmem = tm + T::kSCol + (c & 1) * kChunk;
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const uint64_t ad = smem_desc(q_img + (ks / 4) * (kTRows * 128) + (ks % 4) * 32, 16, 1024);
+              const uint64_t bd = smem_desc(k_img(s) + (ks / 4) * (kChunk * 128) + (ks % 4) * 32, 16, 1024);
+              mma_ss(s_tmem, ad, bd, id_s, ks > 0);
+            }
+            mma_commit(smem_addr(&s_bar[c & 1]));
+            mma_commit(smem_addr(&k_empty[s]));
+          }
+          __syncwarp();
+        }
+        if (c >= 1) {
+          const int cp = c - 1, s = cp % kVStages;
+          if (!warp_wait(smem_addr(&v_full[s]), (cp / kVStages) & 1)) { ok = false; break; }
           // V rows at or past the sequence end in this chunk -> 0 (both bands)
-          const int cstart = t0 + c * kChunk;
+          const int cstart = t0 + cp * kChunk;
           if (L < cstart + kChunk && L > cstart && (L % BS) != 0) {
             const int row_lo = L - cstart, row_hi = min(kChunk, ((L + BS - 1) / BS) * BS - cstart);
             const int nrow = row_hi - row_lo;
@@ -322,25 +399,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           }
           __syncwarp();
-          // S(c) reuses the TMEM buffer of chunk c-2: its P must be consumed
-          if (c >= 2 && !warp_wait(smem_addr(&o_bar), (c - 2) & 1)) { ok = false; break; }
-          if (lane == 0) {
-            tc_fence_after();
-            const uint32_t s_tmem = tm + T::kSCol + (c & 1) * kChunk;
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-              const uint64_t ad = smem_desc(q_img + (ks / 4) * (kTRows * 128) + (ks % 4) * 32, 16, 1024);
-              const uint64_t bd = smem_desc(k_img(s) + (ks / 4) * (kChunk * 128) + (ks % 4) * 32, 16, 1024);
-              mma_ss(s_tmem, ad, bd, id_s, ks > 0);
-            }
-            mma_commit(smem_addr(&s_bar[c & 1]));
-          }
-          __syncwarp();
-        }
-        if (c >= 1) {
-          const int cp = c - 1, s = cp % kTStages;
-          if (!warp_wait(smem_addr(&p_bar), cp & 1)) { ok = false; break; }
-          const int cstart = t0 + cp * kChunk;
+          if (!warp_wait(smem_addr(&p_bar[cp & 1]), (cp >> 1) & 1)) { ok = false; break; }
           const int nsub = (min(t_end, cstart + kChunk) - cstart + 15) / 16;
           if (lane == 0) {
             tc_fence_after();
@@ -350,26 +409,54 @@ __global__ void __launch_bounds__(kTThreads, 1)
               mma_ts(tm + T::kOCol, p_tmem + kk * 8, bd, id_o, (cp > 0 || kk > 0) ? 1u : 0u);
             }
             mma_commit(smem_addr(&o_bar));
-            mma_commit(smem_addr(&empty_bar[s]));
+            mma_commit(smem_addr(&v_empty[s]));
           }
           __syncwarp();
-          // refill the stage with chunk cp + kTStages once P . V has read it
-          if (cp + kTStages < nch) {
-            if (!warp_wait(smem_addr(&empty_bar[s]), (cp / kTStages) & 1)) { ok = false; break; }
-            if (lane == 0) load(cp + kTStages);
-            issued = cp + kTStages + 1;
-          }
         }
       }
       if (!ok && lane == 0) sh_fail = 1;
-      // every load issued has landed before the CTA may exit (bounded)
-      if (lane == 0)
-        for (int s = 0; s < kTStages && s < issued; ++s) {
-          const int last = s + kTStages * ((issued - 1 - s) / kTStages);
-          mbar_wait(smem_addr(&full_bar[s]), (last / kTStages) & 1);
+    } else if (warp == 5) {
+      // ======================= loads (TMA) ==================================
+      // K(c) once S(c - 2) has read its stage, V(c) once P . V(c - 2) has.
+      bool ok = true;
+      int k_issued = 0, v_issued = 0;
+      auto load = [&](const CUtensorMap* map, uint32_t img, uint32_t bar, int c) {   // lane 0
+        const int blk0 = first_blk + c * kBlocksPerChunk;
+        const int nb = min(kBlocksPerChunk, last_blk - blk0 + 1);
+        mbar_expect_tx(bar, (uint32_t)(nb * Gm::kTensorBytes));
+        for (int j = 0; j < nb; ++j) {
+          const int p = blk_ids[blk0 - first_blk + j];
+#pragma unroll
+          for (int xx = 0; xx < Gm::kBoxes; ++xx)
+            // band xx of the chunk image, rows j*BS .. j*BS + BS - 1
+            tma_load_4d(img + xx * (kChunk * 128) + j * (BS * 128), map, bar, xx * Gm::kBoxElems, hk, 0, p);
         }
+      };
+      for (int c = 0; c < nch; ++c) {
+        const int sk = c % kKStages, sv = c % kVStages;
+        if (c >= kKStages &&
+            !warp_wait(smem_addr(&k_empty[sk]), ((c - kKStages) / kKStages) & 1)) { ok = false; break; }
+        if (lane == 0) load(&k_map, k_img(sk), smem_addr(&k_full[sk]), c);
+        k_issued = c + 1;
+        if (c >= kVStages &&
+            !warp_wait(smem_addr(&v_empty[sv]), ((c - kVStages) / kVStages) & 1)) { ok = false; break; }
+        if (lane == 0) load(&v_map, v_img(sv), smem_addr(&v_full[sv]), c);
+        v_issued = c + 1;
+      }
+      if (!ok && lane == 0) sh_fail = 1;
+      // every load issued has landed before the CTA may exit (bounded)
+      if (lane == 0) {
+        for (int s = 0; s < kKStages && s < k_issued; ++s) {
+          const int last = s + kKStages * ((k_issued - 1 - s) / kKStages);
+          mbar_wait(smem_addr(&k_full[s]), (last / kKStages) & 1);
+        }
+        for (int s = 0; s < kVStages && s < v_issued; ++s) {
+          const int last = s + kVStages * ((v_issued - 1 - s) / kVStages);
+          mbar_wait(smem_addr(&v_full[s]), (last / kVStages) & 1);
+        }
+      }
     } else {
-      // ======================= softmax: one row per thread ==================
+      // ======================= softmax: one row per thread (warps 0-3) ======
       const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
       bool ok = true;
       for (int c = 0; c < nch; ++c) {
@@ -377,44 +464,32 @@ __global__ void __launch_bounds__(kTThreads, 1)
         if (!warp_wait(smem_addr(&s_bar[c & 1]), (c >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
         const uint32_t s_tmem = tm + lane_base + T::kSCol + (c & 1) * kChunk;
-        uint32_t raw[2][32];
-        tmem_ld32(s_tmem, raw[0]);
-        tmem_ld32(s_tmem + 32, raw[1]);
+        constexpr int kH = kChunk / 32;                  // 32-key halves of the chunk
+        uint32_t raw[kH][32];
+#pragma unroll
+        for (int h = 0; h < kH; ++h) tmem_ld32(s_tmem + 32 * h, raw[h]);
         tmem_wait_ld();
         const int cstart = t0 + c * kChunk;
         const int lim = min(pos, t_end - 1);             // last key this row may see
-        float mx = -INFINITY;
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int tok = cstart + 32 * h + j;
-            const float v = tok <= lim ? __uint_as_float(raw[h][j]) * a.scale_log2 : -INFINITY;
-            raw[h][j] = __float_as_uint(v);
-            mx = fmaxf(mx, v);
-          }
+        // only chunks that cross some row's last visible key need the mask
+        const bool masked = __any_sync(0xffffffffu, cstart + kChunk - 1 > lim);
+        const float mx_raw = masked ? chunk_max<true>(raw, cstart, lim) : chunk_max<false>(raw, cstart, lim);
+        const float mx = mx_raw == -INFINITY ? -INFINITY : mx_raw * sl2;
         // move the reference maximum only when it is passed by > 2^8
         const bool need = m_ref == -INFINITY ? mx > -INFINITY : mx > m_ref + kRescaleLog2;
         const float m_new = need ? mx : m_ref;
         const float zero_ref = m_new == -INFINITY ? 0.0f : m_new;
-        uint32_t pw[2][16];
-        float lsum = 0.0f;
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float p0 = exp2f(__uint_as_float(raw[h][2 * j]) - zero_ref);
-            const float p1 = exp2f(__uint_as_float(raw[h][2 * j + 1]) - zero_ref);
-            lsum += p0 + p1;
-            __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
-            pw[h][j] = *reinterpret_cast<uint32_t*>(&pp);
-          }
-        // P . V of chunk c-1 has finished (O is stable, and the issuing
-        // thread has taken chunk c-1's P before this chunk's arrives)
-        if (c > 0) {
+        uint32_t pw[kH][16];
+        const float lsum = masked ? chunk_exp<true>(raw, pw, cstart, lim, sl2, zero_ref)
+                                  : chunk_exp<false>(raw, pw, cstart, lim, sl2, zero_ref);
+        // A moved reference maximum: rescale O in TMEM once P . V of chunk
+        // c-1 has finished.  (P of chunk c goes to the other P barrier than
+        // chunk c-1's; chunk c+2's cannot arrive before S(c+2), which the
+        // issuing thread computes only after P . V of chunk c.)
+        if (c > 0 && __any_sync(0xffffffffu, need)) {
           if (!warp_wait(smem_addr(&o_bar), (c - 1) & 1)) { ok = false; break; }
           tc_fence_after();
-          if (__any_sync(0xffffffffu, need)) {             // rescale O in TMEM
+          {
             const float alpha = need ? (m_ref == -INFINITY ? 0.0f : exp2f(m_ref - m_new)) : 1.0f;
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
@@ -431,12 +506,12 @@ __global__ void __launch_bounds__(kTThreads, 1)
         }
         m_ref = m_new;
         l += lsum;
-        // P (bf16 pairs, 32 columns) over this chunk's S
-        tmem_st16(s_tmem, pw[0]);
-        tmem_st16(s_tmem + 16, pw[1]);
+        // P (bf16 pairs, kChunk / 2 columns) over this chunk's S
+#pragma unroll
+        for (int h = 0; h < kH; ++h) tmem_st16(s_tmem + 16 * h, pw[h]);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(smem_addr(&p_bar));
+        mbar_arrive(smem_addr(&p_bar[c & 1]));
       }
       if (ok && !warp_wait(smem_addr(&o_bar), (nch - 1) & 1)) ok = false;
       if (!ok) sh_fail = 1;
@@ -531,7 +606,7 @@ kv_status launch_tc(const DecodeArgs& a, int tiles, cudaStream_t s) {
   alignas(64) CUtensorMap km, vm;
   if ((st = make_kv_maps(a, &km, &vm)) != KV_OK) return st;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)tiles, (unsigned)a.num_kv_heads, (unsigned)a.max_parts);
+  cfg.gridDim = dim3((unsigned)((int64_t)tiles * a.num_kv_heads * a.max_parts));
   cfg.blockDim = dim3(kTThreads);
   cfg.dynamicSmemBytes = T::kSmemBytes;
   cfg.stream = s;
@@ -549,6 +624,9 @@ kv_status launch_tc(const DecodeArgs& a, int tiles, cudaStream_t s) {
 }  // namespace
 
 kv_status launch_multi_tc(const DecodeArgs& a, int tiles, cudaStream_t s) {
+  if (a.part_tokens > kMaxPartTokens || a.part_tokens % 16 ||
+      (int64_t)tiles * a.num_kv_heads * a.max_parts > 0x7fffffffLL)
+    return fail(KV_ERR_INVALID_ARG, "paged_attention_multi: too many row tiles or partition too long");
   if (a.head_dim == 128)
     return a.block_size == 32 ? launch_tc<128, 32>(a, tiles, s) : launch_tc<128, 16>(a, tiles, s);
   return a.block_size == 32 ? launch_tc<64, 32>(a, tiles, s) : launch_tc<64, 16>(a, tiles, s);

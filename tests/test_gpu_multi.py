@@ -164,3 +164,33 @@ def test_full_size_multi_workload_sampled_sequences(cfg):
     ref, rc = oracle.paged_attention_multi(q, kc, vc, bt, sl, qs, wl.spec.scale, threads=os.cpu_count())
     assert rc == 0
     check(got[rows], ref, f"workload {cfg}")
+
+
+@pytest.mark.parametrize("scale", [-0.125, 0.0, 1.0], ids=["negative", "zero", "sharp"])
+def test_multi_softmax_scale_values(scale):
+    """Scales other than 1/sqrt(d), on both kernels (sequence 0 takes the
+    tensor-core kernel, the others the column groups): a negative scale, a zero
+    scale (equal weights over the visible keys) and a sharp one whose running
+    maximum moves by more than 2^8 mid-row, so that O is rescaled in TMEM.
+    Near-one-hot rows put outputs near a single V row (|v| up to about 4.5),
+    where rounding P and the output to bf16 each cost up to 2^-9 relative: the
+    bound is 1e-2 + 2^-8 |ref| there."""
+    wl = multi([3000, 40, 700], [300, 1, 5], hq=8, hkv=2, d=64, seed=47)
+    g = GpuStep(wl)
+    g.multi_step()
+    out = torch.empty_like(g.out_multi)
+    pkv.paged_attention_multi(out, g.q, g.k_cache, g.v_cache, g.block_tables, g.seq_lens,
+                              g.query_start, g.max_seq_len, int(wl.query_lens.max()), scale,
+                              g.ws_multi)
+    torch.cuda.synchronize()
+    st, flags = pkv.get_status()
+    assert flags == 0, hex(flags)
+    got = out_f64(out)
+    kc, vc, _, _ = oracle_pool(wl)
+    ref, rc = oracle.paged_attention_multi(wl.q, kc, vc, wl.block_tables, wl.seq_lens,
+                                           wl.query_start, scale, threads=os.cpu_count())
+    assert rc == 0
+    assert np.isfinite(got).all()
+    err = np.abs(got - ref)
+    assert (err <= 1e-2 + 2.0 ** -8 * np.abs(ref)).all(), (scale, err.max())
+    assert err.mean() <= 1e-3, (scale, err.mean())
