@@ -236,7 +236,9 @@ __global__ void merge_kernel(__nv_bfloat16* __restrict__ out, const float* __res
 }
 
 size_t decode_workspace_need(int batch, int num_q_heads, int head_dim, int slots) {
-  return slots > 1 ? (size_t)batch * num_q_heads * slots * (head_dim + 2) * sizeof(float) : 0;
+  if (slots <= 1) return 0;
+  const size_t rows = (size_t)batch * num_q_heads;
+  return (ml_region_floats(rows, slots) + rows * slots * head_dim) * sizeof(float);
 }
 
 // Longest valid sequence: bounded by the host hint and by the table.
@@ -492,7 +494,7 @@ static kv_status decode_common(void* out, const void* q, const void* new_k, cons
                   "%s: workspace must be 16-byte aligned and hold %zu bytes "
                   "(pagedkv_workspace_bytes gives a safe size)", who, need);
     a.ws_ml = static_cast<float*>(workspace);
-    a.ws_acc = a.ws_ml + (size_t)batch * num_q_heads * a.slots * 2;
+    a.ws_acc = a.ws_ml + ml_region_floats((size_t)batch * num_q_heads, a.slots);
   }
   cudaStream_t s = (cudaStream_t)stream;
   if (num_prefix_blocks > 0 && (st = launch_prefix(a, s)) != KV_OK) return st;

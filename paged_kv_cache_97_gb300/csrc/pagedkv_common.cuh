@@ -80,6 +80,13 @@ struct DecodeArgs {
 // row, or nothing when every row has a single partial.
 size_t decode_workspace_need(int batch, int num_q_heads, int head_dim, int slots);
 
+// Floats of the (m, l) region of a workspace holding `rows` x `slots`
+// partials, rounded up to 16 bytes so that the acc region after it takes
+// 16-byte vector loads and stores.
+inline size_t ml_region_floats(size_t rows, int slots) {
+  return (rows * (size_t)slots * 2 + 3) & ~(size_t)3;
+}
+
 // Tensor maps over the K and V pools for this launch's geometry: 4-D
 // [NB, bs, Hkv, d], box = one block's rows of one head (128-byte swizzle).
 kv_status make_kv_maps(const DecodeArgs& a, CUtensorMap* k_map, CUtensorMap* v_map);
@@ -95,9 +102,9 @@ kv_status launch_merge(const DecodeArgs& a, cudaStream_t stream);
 kv_status launch_prefix(const DecodeArgs& a, cudaStream_t stream);
 
 // Long multi-token queries on the tensor cores with TMEM accumulators
-// (pagedkv_multi_tc.cu), over `tiles` CTAs (an upper bound of the 128-row
-// tiles of all sequences; the extra ones exit at once).
-kv_status launch_multi_tc(const DecodeArgs& a, int tiles, cudaStream_t stream);
+// (pagedkv_multi_tc.cu): `ctas` persistent CTAs over all (KV head,
+// partition, 128-row tile) units.
+kv_status launch_multi_tc(const DecodeArgs& a, int ctas, cudaStream_t stream);
 
 // Token partition length for `work` independent (row group, KV head) units
 // over sequences of up to max_seq_len tokens (power of two in [256, 2048]).

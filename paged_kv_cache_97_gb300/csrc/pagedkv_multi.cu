@@ -18,6 +18,8 @@
 // 在线 Softmax; “Flash Attention v2 的改进”).
 #include <cuda.h>
 #include <cuda_bf16.h>
+
+#include <algorithm>
 #include <cuda_runtime.h>
 
 #include "pagedkv_common.cuh"
@@ -31,62 +33,90 @@ namespace {
 constexpr int kMaxVGroups = 4;
 
 // Log-sum-exp merge of the partition partials of every (query token, head)
-// row: one warp per row.  Partials of partitions wholly past a row's position
-// hold l = 0 and are skipped; a partial marked l < 0 (bad sequence or a wait
-// that gave up) zeroes the row.
+// row: one warp per row, four heads per CTA.  Partials of partitions wholly
+// past a row's position hold l = 0 and are skipped (their acc is never read
+// into the sum); a partial marked l < 0 (bad sequence or a wait that gave up)
+// zeroes the row.
 template <int D>
 __global__ void __launch_bounds__(128) multi_merge_kernel(const DecodeArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j = blockIdx.x, h = blockIdx.y * 4 + warp;
-  if (h >= a.num_q_heads) return;
   const int32_t* qs = a.query_start;
-  // sequence of token j: the last b with query_start[b] <= j (offsets checked
-  // by the attention kernel; a row it did not serve is left untouched)
-  int lo = 0, hi = a.batch - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (qs[mid] <= j) lo = mid;
-    else hi = mid - 1;
+  // sequence of token j: the last b with query_start[b] <= j, found by the
+  // whole CTA in rounds of 128 samples of query_start (one round for up to
+  // 128 sequences).  Offsets are checked by the attention kernels; a row they
+  // did not serve is left untouched.
+  int lo = 0, hi = a.batch;                              // b in [lo, hi)
+  while (hi - lo > 1) {
+    const int step = (hi - lo + 127) / 128;
+    const int idx = lo + (int)threadIdx.x * step;
+    const int cnt = __syncthreads_count(idx < hi && qs[idx] <= j);
+    if (cnt == 0) return;                                // before every sequence (CTA-uniform)
+    lo += (cnt - 1) * step;
+    hi = min(lo + step, hi);
   }
   const int b = lo;
-  if (j < qs[b] || j >= qs[b + 1]) return;
+  if (h >= a.num_q_heads || j < qs[b] || j >= qs[b + 1]) return;
   const int L = a.seq_lens[b], n = qs[b + 1] - qs[b];
-  // the sequence checks of the attention kernel: a bad sequence's rows are 0
+  // the sequence checks of the attention kernels: a bad sequence's rows are 0
   const bool seq_ok = qs[b] >= 0 && qs[b + 1] <= a.num_tokens && L > 0 && n <= L &&
-                      n <= a.max_query_len &&
-                      L <= a.max_seq_len &&
+                      n <= a.max_query_len && L <= a.max_seq_len &&
                       (int64_t)L <= (int64_t)a.max_blocks_per_seq * a.block_size;
   const int np = seq_ok ? min((L + a.part_tokens - 1) / a.part_tokens, a.max_parts) : 0;
   const int64_t row = (int64_t)j * a.num_q_heads + h;
   const float* ml = a.ws_ml + row * a.max_parts * 2;
+  // pass 1 (32 partials per round): the largest m among l > 0, any bad partial
   float M = -INFINITY;
   bool bad = np == 0;
-  for (int i = 0; i < np; ++i) {
+  for (int i = lane; i < np; i += 32) {
     const float l = ml[2 * i + 1];
-    if (l < 0.0f) bad = true;
+    bad |= l < 0.0f;
     if (l > 0.0f) M = fmaxf(M, ml[2 * i]);
   }
-  constexpr int E = D / 32;                                // elements per lane
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  bad = __any_sync(0xffffffffu, bad);
+  // pass 2: each lane owns D / 32 consecutive elements
+  constexpr int E = D / 32;
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.0f;
   float den = 0.0f;
   if (!bad) {
+#pragma unroll 4
     for (int i = 0; i < np; ++i) {
-      const float l = ml[2 * i + 1];
-      if (!(l > 0.0f)) continue;
-      const float w = exp2f(ml[2 * i] - M);
-      den += w * l;
+      const float m = ml[2 * i], l = ml[2 * i + 1];
       const float* src = a.ws_acc + (row * a.max_parts + i) * D + lane * E;
+      float x[E];
+      if constexpr (E == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        x[0] = v.x;
+        x[1] = v.y;
+        x[2] = v.z;
+        x[3] = v.w;
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        x[0] = v.x;
+        x[1] = v.y;
+      }
+      if (l > 0.0f) {
+        const float w = exp2f(m - M);
+        den = fmaf(w, l, den);
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] += w * src[e];
+        for (int e = 0; e < E; ++e) acc[e] = fmaf(w, x[e], acc[e]);
+      }
     }
   }
   const float inv = (bad || !(den > 0.0f)) ? 0.0f : 1.0f / den;
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + row * D + lane * E;
+  uint32_t w2[E / 2];
 #pragma unroll
-  for (int e = 0; e < E; e += 2)
-    *reinterpret_cast<__nv_bfloat162*>(out + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+  for (int e = 0; e < E; e += 2) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+    w2[e / 2] = *reinterpret_cast<uint32_t*>(&v);
+  }
+  if constexpr (E == 4) *reinterpret_cast<uint2*>(out) = make_uint2(w2[0], w2[1]);
+  else *reinterpret_cast<uint32_t*>(out) = w2[0];
 }
 
 kv_status launch_multi_merge(const DecodeArgs& a, cudaStream_t s) {
@@ -97,6 +127,36 @@ kv_status launch_multi_merge(const DecodeArgs& a, cudaStream_t s) {
   return cuda_check(cudaGetLastError(), "multi_merge_kernel launch");
 }
 
+// A side stream and two events per (host thread, device): the tensor-core
+// kernel runs there, concurrently with the decode kernel's column groups on
+// the caller's stream (fork from it, join before the merge; the same pattern
+// records as two parallel branches under graph capture).  Thread-local, so
+// callers on different host threads never share an event.
+struct SideLane {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  ~SideLane() {
+    if (fork) cudaEventDestroy(fork);
+    if (join) cudaEventDestroy(join);
+    if (stream) cudaStreamDestroy(stream);
+  }
+};
+
+kv_status side_lane(int dev, SideLane** out) {
+  static thread_local SideLane lanes[64];
+  SideLane& l = lanes[dev];
+  if (!l.stream) {
+    kv_status st;
+    if ((st = cuda_check(cudaEventCreateWithFlags(&l.fork, cudaEventDisableTiming), "cudaEventCreate")) != KV_OK ||
+        (st = cuda_check(cudaEventCreateWithFlags(&l.join, cudaEventDisableTiming), "cudaEventCreate")) != KV_OK ||
+        (st = cuda_check(cudaStreamCreateWithFlags(&l.stream, cudaStreamNonBlocking), "cudaStreamCreate")) != KV_OK)
+      return st;
+  }
+  *out = &l;
+  return KV_OK;
+}
+
+
 }  // namespace
 }  // namespace pagedkv
 
@@ -105,7 +165,9 @@ using namespace pagedkv;
 namespace {
 
 size_t multi_need(int num_tokens, int num_q_heads, int head_dim, int parts) {
-  return parts > 1 ? (size_t)num_tokens * num_q_heads * parts * (head_dim + 2) * sizeof(float) : 0;
+  if (parts <= 1) return 0;
+  const size_t rows = (size_t)num_tokens * num_q_heads;
+  return (ml_region_floats(rows, parts) + rows * parts * head_dim) * sizeof(float);
 }
 
 }  // namespace
@@ -163,7 +225,7 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
   kv_status st = device_info(&di);
   if (st != KV_OK) return st;
   // Upper bound of the tensor-core kernel's 128-row tiles over all sequences
-  // (tiles past the real count exit at once).
+  // (it sizes the persistent grid; the kernel counts the real tiles).
   const int64_t tiles = ((int64_t)num_tokens * GQ + 127) / 128 + batch;
   if (tiles > 0x7fffffffLL) return fail(KV_ERR_INVALID_ARG, "%s: too many query tokens", who);
 
@@ -206,11 +268,32 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
                   "%s: workspace must be 16-byte aligned and hold %zu bytes "
                   "(pagedkv_multi_workspace_bytes gives a safe size)", who, need);
     a.ws_ml = static_cast<float*>(workspace);
-    a.ws_acc = a.ws_ml + (size_t)num_tokens * num_q_heads * a.max_parts * 2;
+    a.ws_acc = a.ws_ml + ml_region_floats((size_t)num_tokens * num_q_heads, a.max_parts);
   }
   cudaStream_t s = (cudaStream_t)stream;
-  if (column_path && (st = launch_decode(a, s)) != KV_OK) return st;
-  if (row_path && (st = launch_multi_tc(a, (int)tiles, s)) != KV_OK) return st;
+  // Persistent tensor-core CTAs, two per SM (measured best both beside the
+  // column groups and alone), never more than the units.
+  auto tc_ctas = [&](int per_sm) {
+    return (int)std::min<int64_t>(tiles * num_kv_heads * a.max_parts, (int64_t)di.num_sms * per_sm);
+  };
+  if (row_path && column_path) {
+    // the tensor-core kernel (tensor-bound) beside the column groups (HBM-bound)
+    SideLane* lane = nullptr;
+    if ((st = side_lane(di.device, &lane)) != KV_OK ||
+        (st = cuda_check(cudaEventRecord(lane->fork, s), "cudaEventRecord")) != KV_OK ||
+        (st = cuda_check(cudaStreamWaitEvent(lane->stream, lane->fork, 0), "cudaStreamWaitEvent")) != KV_OK ||
+        (st = launch_multi_tc(a, tc_ctas(2), lane->stream)) != KV_OK ||
+        (st = cuda_check(cudaEventRecord(lane->join, lane->stream), "cudaEventRecord")) != KV_OK)
+      return st;
+    st = launch_decode(a, s);
+    const kv_status sj = cuda_check(cudaStreamWaitEvent(s, lane->join, 0), "cudaStreamWaitEvent");
+    if (st != KV_OK) return st;
+    if (sj != KV_OK) return sj;
+  } else if (column_path) {
+    if ((st = launch_decode(a, s)) != KV_OK) return st;
+  } else if (row_path) {
+    if ((st = launch_multi_tc(a, tc_ctas(2), s)) != KV_OK) return st;
+  }
   return launch_multi_merge(a, s);
 }
 

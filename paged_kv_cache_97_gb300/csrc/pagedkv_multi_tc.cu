@@ -28,9 +28,12 @@
 //     scale flips Q's signs instead (exact), so maxima are taken on raw scores.
 //
 // TMEM: O (d columns) + two 64-column S/P buffers (S of chunk c+1 is computed
-// while chunk c's softmax runs) = 256 columns, two CTAs per SM.  CTAs are
-// numbered KV head fastest, then partition, then row tile, so the real tiles
-// are dispatched before the bound's surplus.  V rows past the sequence end
+// while chunk c's softmax runs) = 256 columns, at most two CTAs per SM.  The
+// CTAs are persistent: each takes units (KV head fastest, then partition,
+// then row tile) gridDim apart, over the real tiles only, with TMEM held
+// throughout and the barriers invalidated and set up again per unit; the
+// host launches two per SM (beside the decode kernel's column groups, on a
+// side stream, or alone).  V rows past the sequence end
 // are zeroed in shared memory before P . V (p is 0 there but the pool may
 // hold NaN).  Every wait is bounded; a CTA that gives up flags
 // PAGEDKV_FLAG_WAIT_TIMEOUT, drains its copies and tensor-core work, frees its
@@ -107,6 +110,10 @@ __device__ __forceinline__ void tc_fence_before() {
 }
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_inval(uint32_t bar) {
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 // 32 consecutive TMEM columns of this warp's 32 lanes (one row per thread).
@@ -228,9 +235,6 @@ __global__ void __launch_bounds__(kTThreads, 2)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hq = a.num_q_heads, Hkv = a.num_kv_heads, GQ = Hq / Hkv;
-  // CTA x: KV head fastest, then partition, then row tile, so that the real
-  // tiles (the first ones) are dispatched before the bound's surplus.
-  const int hk = blockIdx.x % Hkv, part = (blockIdx.x / Hkv) % a.max_parts;
   const int B = a.batch;
   const int32_t* qs = a.query_start;
   const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
@@ -239,13 +243,9 @@ __global__ void __launch_bounds__(kTThreads, 2)
   auto k_img = [&](int s) { return base + T::kQBytes + s * T::kKBytes; };
   auto v_img = [&](int s) { return base + T::kQBytes + (kKStages + s) * T::kKBytes; };
 
-  if (tid == 0) {
-    sh_b = -1;
-    sh_bad = 0;
-    sh_fail = 0;
-  }
-  // ---- which (sequence, row tile) CTA x serves (sequences past the column
-  // groups' limit, in order; as in the row-tiled kernel)
+  // ---- row tiles per sequence (sequences past the column groups' limit, in
+  // order), prefix-summed once: scan[tid] ends the tiles of sequences
+  // tid*per .. tid*per + per - 1
   const int per = (B + kTThreads - 1) / kTThreads;
   int mine = 0;
   for (int i = 0; i < per; ++i) {
@@ -260,7 +260,22 @@ __global__ void __launch_bounds__(kTThreads, 2)
     scan[tid] += v;
     __syncthreads();
   }
-  const int x = blockIdx.x / (Hkv * a.max_parts);        // row tile over all sequences
+  const int64_t units = (int64_t)scan[kTThreads - 1] * Hkv * a.max_parts;
+  bool tm_held = false;                                  // TMEM allocated (CTA-uniform)
+  uint32_t tm = 0;
+
+  // ---- persistent loop over (KV head, partition, row tile) units, KV head
+  // fastest
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+  const int hk = (int)(u % Hkv), part = (int)((u / Hkv) % a.max_parts);
+  const int x = (int)(u / ((int64_t)Hkv * a.max_parts));   // row tile over all sequences
+  __syncthreads();                                       // the last unit's readers are done
+  if (tid == 0) {
+    sh_b = -1;
+    sh_bad = 0;
+    sh_fail = 0;
+  }
+  __syncthreads();
   if (x >= scan[tid] - mine && x < scan[tid]) {
     int acc = scan[tid] - mine;
     for (int i = 0; i < per; ++i) {
@@ -276,12 +291,11 @@ __global__ void __launch_bounds__(kTThreads, 2)
     }
   }
   __syncthreads();
-  if (sh_b < 0) return;                                  // past the last tile (CTA-uniform)
-  const int b = sh_b, rt = sh_rt;
+  const int b = sh_b, rt = sh_rt;                        // x < the tile count: found
   const int q0 = qs[b], n = qs[b + 1] - q0;
   const int L = a.seq_lens[b];
   const int t0 = part * a.part_tokens;
-  if (t0 >= L && L > 0) return;                          // no such partition for this sequence
+  if (t0 >= L && L > 0) continue;                        // no such partition (CTA-uniform)
   const bool rows_ok = q0 >= 0 && q0 + n <= a.num_tokens;
   const bool len_ok = rows_ok && L > 0 && n <= L && n <= a.max_query_len && L <= a.max_seq_len &&
                       (int64_t)L <= (int64_t)a.max_blocks_per_seq * BS;
@@ -341,7 +355,8 @@ __global__ void __launch_bounds__(kTThreads, 2)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   const bool work = nch > 0;
-  if (work && warp == 0) {
+  const bool alloc_now = work && !tm_held;
+  if (alloc_now && warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                  ::"r"(smem_addr(&tmem_base)), "r"(kTmemCols) : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -350,8 +365,11 @@ __global__ void __launch_bounds__(kTThreads, 2)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (alloc_now) {
+    tm_held = true;
+    tm = tmem_base;
+  }
   const bool bad = sh_bad != 0;
-  const uint32_t tm = tmem_base;
   float m_ref = -INFINITY, l = 0.0f;
 
   if (work && !bad) {
@@ -580,13 +598,35 @@ __global__ void __launch_bounds__(kTThreads, 2)
   }
   tc_fence_before();
   __syncthreads();
-  if (work && warp == 0)
+  tc_fence_after();
+  // every copy, MMA and arrival of this unit is done: the barriers start over
+  if (tid == 0) {
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_inval(smem_addr(&k_full[s]));
+      mbar_inval(smem_addr(&k_empty[s]));
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_inval(smem_addr(&v_full[s]));
+      mbar_inval(smem_addr(&v_empty[s]));
+    }
+    mbar_inval(smem_addr(&s_bar[0]));
+    mbar_inval(smem_addr(&s_bar[1]));
+    mbar_inval(smem_addr(&p_bar[0]));
+    mbar_inval(smem_addr(&p_bar[1]));
+    mbar_inval(smem_addr(&o_bar));
+    mbar_inval(smem_addr(&drain_bar));
+  }
+  }  // units
+  tc_fence_before();
+  __syncthreads();
+  if (tm_held && warp == 0)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tm), "r"(kTmemCols)
                  : "memory");
 }
 
+
 template <int D, int BS>
-kv_status launch_tc(const DecodeArgs& a, int tiles, cudaStream_t s) {
+kv_status launch_tc(const DecodeArgs& a, int ctas, cudaStream_t s) {
   using T = TcGeo<D>;
   static std::mutex mu;
   static bool attr_set[64] = {};
@@ -606,30 +646,22 @@ kv_status launch_tc(const DecodeArgs& a, int tiles, cudaStream_t s) {
   alignas(64) CUtensorMap km, vm;
   if ((st = make_kv_maps(a, &km, &vm)) != KV_OK) return st;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((int64_t)tiles * a.num_kv_heads * a.max_parts));
+  cfg.gridDim = dim3((unsigned)ctas);
   cfg.blockDim = dim3(kTThreads);
   cfg.dynamicSmemBytes = T::kSmemBytes;
   cfg.stream = s;
-  // behind the decode kernel's column groups (nothing read from them): a
-  // programmatic dependent, started while they run
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = a.col_max_n > 0 ? 1 : 0;
   return cuda_check(cudaLaunchKernelEx(&cfg, multi_tc_kernel<D, BS>, km, vm, a),
                     "multi_tc_kernel launch");
 }
 
 }  // namespace
 
-kv_status launch_multi_tc(const DecodeArgs& a, int tiles, cudaStream_t s) {
-  if (a.part_tokens > kMaxPartTokens || a.part_tokens % 16 ||
-      (int64_t)tiles * a.num_kv_heads * a.max_parts > 0x7fffffffLL)
-    return fail(KV_ERR_INVALID_ARG, "paged_attention_multi: too many row tiles or partition too long");
+kv_status launch_multi_tc(const DecodeArgs& a, int ctas, cudaStream_t s) {
+  if (a.part_tokens > kMaxPartTokens || a.part_tokens % 16 || ctas <= 0)
+    return fail(KV_ERR_INVALID_ARG, "paged_attention_multi: bad tensor-core launch");
   if (a.head_dim == 128)
-    return a.block_size == 32 ? launch_tc<128, 32>(a, tiles, s) : launch_tc<128, 16>(a, tiles, s);
-  return a.block_size == 32 ? launch_tc<64, 32>(a, tiles, s) : launch_tc<64, 16>(a, tiles, s);
+    return a.block_size == 32 ? launch_tc<128, 32>(a, ctas, s) : launch_tc<128, 16>(a, ctas, s);
+  return a.block_size == 32 ? launch_tc<64, 32>(a, ctas, s) : launch_tc<64, 16>(a, ctas, s);
 }
 
 }  // namespace pagedkv

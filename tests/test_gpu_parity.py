@@ -188,6 +188,23 @@ def test_partition_size_does_not_change_the_answer(monkeypatch, part):
     check_status()
 
 
+def test_odd_partial_count_keeps_the_workspace_aligned(monkeypatch):
+    """3 sequences x 1 query head x 3 partitions: 18 floats of (m, l), so the
+    acc region after it is 16-byte aligned only because the (m, l) region is
+    rounded up; the merge reads it with 16-byte loads."""
+    wl = small([300, 700, 37], hq=1, hkv=1, d=64, seed=15)
+    monkeypatch.setenv("PAGEDKV_PARTITION_TOKENS", "256")
+    g = GpuStep(wl)
+    got = out_f64(g.step())
+    torch.cuda.synchronize()
+    check_status()
+    kc, vc, _, _ = oracle_pool(wl)
+    ref, rc = oracle.paged_attention(wl.q, kc, vc, wl.block_tables, wl.seq_lens, wl.spec.scale,
+                                     threads=os.cpu_count())
+    assert rc == 0
+    assert_close(got, ref, "bf16", "odd partial count")
+
+
 @pytest.mark.parametrize("case", ["cfg1", "ragged_g4_d128", "g8_int8_bs32", "shared_prefix", "int8_d64_bs16",
                                   "g8_fp8_bs32"])
 def test_fused_step_equals_separate_calls(case):
