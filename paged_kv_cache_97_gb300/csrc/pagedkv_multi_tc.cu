@@ -5,18 +5,18 @@
 // Sequence b's query token i (of n_b, its last tokens) at position
 // L_b - n_b + i attends positions 0 .. L_b - n_b + i.  A CTA takes 128 rows
 // (query token, grouped head) of one sequence and KV head -- the MMA's M --
-// and one token partition, in chunks of 64 keys:
+// and one token partition, in chunks of 128 keys:
 //
 //   * warp 5 (one lane issues): TMA tensor loads of each chunk's K and V
-//     blocks (ids staged in shared memory) into stages laid out as 64
-//     contiguous 128-byte-swizzled rows per 64-element column band, so one
-//     descriptor covers the chunk; K's stage is refilled once S of its chunk
-//     is done, V's once P . V of its chunk is;
+//     blocks (ids staged in shared memory) into one stage each, laid out as
+//     128 contiguous 128-byte-swizzled rows per 64-element column band, so
+//     one descriptor covers the chunk; K's stage is refilled once S of its
+//     chunk is done (it lands during the softmax), V's once P . V is;
 //   * warp 4 (one lane issues):
-//       S[128 x 64]  = Q[128 x d] . K^T          (tcgen05.mma, A and B from smem)
-//       O[128 x d]  += P[128 x 64] . V[64 x d]   (tcgen05.mma, A = P from TMEM)
-//     in the order S(0), S(1), P.V(0), S(2), P.V(1), ..., committing each to
-//     mbarriers;
+//       S[128 x 128] = Q[128 x d] . K^T          (tcgen05.mma, A and B from smem)
+//       O[128 x d]  += P[128 x 128] . V[128 x d] (tcgen05.mma, A = P from TMEM)
+//     per chunk in turn, committing each to mbarriers (an N = 64 MMA takes as
+//     long to issue as an N = 128 one, so wide chunks halve S's issue time);
 //   * warps 0-3 (one row per thread): read S from TMEM, apply the causal mask
 //     (only in chunks that cross a row's last key) and the scale, update the
 //     row's running maximum and sum (“LLM 推理优化技术全景”, 在线 Softmax;
@@ -27,8 +27,8 @@
 //     share the same reference, so the result is the softmax's.  A negative
 //     scale flips Q's signs instead (exact), so maxima are taken on raw scores.
 //
-// TMEM: O (d columns) + two 64-column S/P buffers (S of chunk c+1 is computed
-// while chunk c's softmax runs) = 256 columns, at most two CTAs per SM.  The
+// TMEM: O (d columns) + one 128-column S/P buffer = 256 columns, two CTAs
+// per SM, so one CTA's MMAs run while the other's softmax does.  The
 // CTAs are persistent: each takes units (KV head fastest, then partition,
 // then row tile) gridDim apart, over the real tiles only, with TMEM held
 // throughout and the barriers invalidated and set up again per unit; the
@@ -53,9 +53,7 @@ namespace {
 using namespace dev;
 
 constexpr int kTRows = 128;               // query rows per CTA (the MMA's M)
-constexpr int kChunk = 64;                // keys per chunk (the S MMA's N)
-constexpr int kKStages = 2;               // K of a chunk: free once S of the chunk is done
-constexpr int kVStages = 2;               // V of a chunk: free once P . V of the chunk is done
+constexpr int kChunk = 128;               // keys per chunk (the S MMA's N)
 constexpr int kTThreads = 6 * 32;         // 4 softmax warps, the MMA warp, the load warp
 constexpr int kTmemCols = 256;
 constexpr float kRescaleLog2 = 8.0f;      // move the reference max past 2^8
@@ -65,9 +63,9 @@ struct TcGeo {
   static constexpr int kAtoms = D / 64;                  // 64-element (128-byte) column bands
   static constexpr int kQBytes = kTRows * D * 2;         // Q image
   static constexpr int kKBytes = kChunk * D * 2;         // K (or V) of a chunk
-  static constexpr int kSmemBytes = kQBytes + (kKStages + kVStages) * kKBytes + 1024;
+  static constexpr int kSmemBytes = kQBytes + 2 * kKBytes + 1024;   // Q, K, V (+ alignment)
   static constexpr int kOCol = 0;                        // O in TMEM columns [0, D)
-  static constexpr int kSCol = 128;                      // S/P buffers at 128 and 192
+  static constexpr int kSCol = 128;                      // S (and P over it): [128, 256)
 };
 
 // 128-byte-swizzled K-major / MN-major shared-memory matrix descriptor.
@@ -226,8 +224,7 @@ __global__ void __launch_bounds__(kTThreads, 2)
   using Gm = Geo<D, BS, false>;                          // TMA box geometry of one block
   constexpr int kBlocksPerChunk = kChunk / BS;
   extern __shared__ unsigned char smem_raw[];
-  __shared__ uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
-  __shared__ uint64_t s_bar[2], p_bar[2], o_bar, drain_bar;
+  __shared__ uint64_t k_full, k_empty, v_full, v_empty, s_bar, p_bar, o_bar, drain_bar;
   __shared__ uint32_t tmem_base;
   __shared__ int scan[kTThreads];
   __shared__ int sh_b, sh_rt, sh_bad, sh_fail;
@@ -240,8 +237,7 @@ __global__ void __launch_bounds__(kTThreads, 2)
   const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
   unsigned char* gbase = smem_raw + (base - smem_addr(smem_raw));
   const uint32_t q_img = base;                           // Q: kAtoms bands of [128 x 64]
-  auto k_img = [&](int s) { return base + T::kQBytes + s * T::kKBytes; };
-  auto v_img = [&](int s) { return base + T::kQBytes + (kKStages + s) * T::kKBytes; };
+  const uint32_t k_img = base + T::kQBytes, v_img = k_img + T::kKBytes;
 
   // ---- row tiles per sequence (sequences past the column groups' limit, in
   // order), prefix-summed once: scan[tid] ends the tiles of sequences
@@ -338,18 +334,12 @@ __global__ void __launch_bounds__(kTThreads, 2)
     }
   }
   if (tid == 0) {
-    for (int s = 0; s < kKStages; ++s) {
-      mbar_init(smem_addr(&k_full[s]), 1);
-      mbar_init(smem_addr(&k_empty[s]), 1);
-    }
-    for (int s = 0; s < kVStages; ++s) {
-      mbar_init(smem_addr(&v_full[s]), 1);
-      mbar_init(smem_addr(&v_empty[s]), 1);
-    }
-    mbar_init(smem_addr(&s_bar[0]), 1);
-    mbar_init(smem_addr(&s_bar[1]), 1);
-    mbar_init(smem_addr(&p_bar[0]), kTRows);
-    mbar_init(smem_addr(&p_bar[1]), kTRows);
+    mbar_init(smem_addr(&k_full), 1);
+    mbar_init(smem_addr(&k_empty), 1);
+    mbar_init(smem_addr(&v_full), 1);
+    mbar_init(smem_addr(&v_empty), 1);
+    mbar_init(smem_addr(&s_bar), 1);
+    mbar_init(smem_addr(&p_bar), kTRows);
     mbar_init(smem_addr(&o_bar), 1);
     mbar_init(smem_addr(&drain_bar), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -375,67 +365,61 @@ __global__ void __launch_bounds__(kTThreads, 2)
   if (work && !bad) {
     if (warp == 4) {
       // ======================= tensor-core issue ===========================
-      // Order S(0), S(1), P.V(0), S(2), P.V(1), ...; the load warp refills K's
-      // stage once S of its chunk is done, V's once P . V of its chunk is.
+      // Per chunk: S(c) once K(c) has landed and P . V(c-1) has read the
+      // S/P buffer; then P . V(c) once P(c) is written.  (The second CTA on
+      // the SM keeps the tensor core busy while this one runs its softmax.)
       bool ok = true;
       const uint32_t id_s = mma_idesc(kTRows, kChunk, 0);
       const uint32_t id_o = mma_idesc(kTRows, D, 1);
-      for (int c = 0; c <= nch && ok; ++c) {
-        if (c < nch) {
-          const int s = c % kKStages;
-          if (!warp_wait(smem_addr(&k_full[s]), (c / kKStages) & 1)) { ok = false; break; }
-          // S(c) reuses the TMEM buffer of chunk c-2: P . V(c-2) must be done
-          if (c >= 2 && !warp_wait(smem_addr(&o_bar), (c - 2) & 1)) { ok = false; break; }
-          if (lane == 0) {
-            tc_fence_after();
-            const uint32_t s_tmem = tm + T::kSCol + (c & 1) * kChunk;
+      const uint32_t s_tmem = tm + T::kSCol;
+      for (int c = 0; c < nch && ok; ++c) {
+        if (!warp_wait(smem_addr(&k_full), c & 1)) { ok = false; break; }
+        if (c >= 1 && !warp_wait(smem_addr(&o_bar), (c - 1) & 1)) { ok = false; break; }
+        if (lane == 0) {
+          tc_fence_after();
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-              const uint64_t ad = smem_desc(q_img + (ks / 4) * (kTRows * 128) + (ks % 4) * 32, 16, 1024);
-              const uint64_t bd = smem_desc(k_img(s) + (ks / 4) * (kChunk * 128) + (ks % 4) * 32, 16, 1024);
-              mma_ss(s_tmem, ad, bd, id_s, ks > 0);
-            }
-            mma_commit(smem_addr(&s_bar[c & 1]));
-            mma_commit(smem_addr(&k_empty[s]));
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint64_t ad = smem_desc(q_img + (ks / 4) * (kTRows * 128) + (ks % 4) * 32, 16, 1024);
+            const uint64_t bd = smem_desc(k_img + (ks / 4) * (kChunk * 128) + (ks % 4) * 32, 16, 1024);
+            mma_ss(s_tmem, ad, bd, id_s, ks > 0);
           }
-          __syncwarp();
+          mma_commit(smem_addr(&s_bar));
+          mma_commit(smem_addr(&k_empty));
         }
-        if (c >= 1) {
-          const int cp = c - 1, s = cp % kVStages;
-          if (!warp_wait(smem_addr(&v_full[s]), (cp / kVStages) & 1)) { ok = false; break; }
-          // V rows at or past the sequence end in this chunk -> 0 (both bands)
-          const int cstart = t0 + cp * kChunk;
-          if (L < cstart + kChunk && L > cstart && (L % BS) != 0) {
-            const int row_lo = L - cstart, row_hi = min(kChunk, ((L + BS - 1) / BS) * BS - cstart);
-            const int nrow = row_hi - row_lo;
-            for (int i = lane; i < nrow * 8 * T::kAtoms; i += 32) {
-              const int rr = row_lo + i / (8 * T::kAtoms), rest = i % (8 * T::kAtoms);
-              const int band = rest / 8, cc = rest % 8;
-              *reinterpret_cast<uint4*>(gbase + (v_img(s) - base) + band * (kChunk * 128) + sw128(rr, cc)) =
-                  make_uint4(0u, 0u, 0u, 0u);
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (!warp_wait(smem_addr(&v_full), c & 1)) { ok = false; break; }
+        // V rows at or past the sequence end in this chunk -> 0 (every band)
+        const int cstart = t0 + c * kChunk;
+        if (L < cstart + kChunk && L > cstart && (L % BS) != 0) {
+          const int row_lo = L - cstart, row_hi = min(kChunk, ((L + BS - 1) / BS) * BS - cstart);
+          const int nrow = row_hi - row_lo;
+          for (int i = lane; i < nrow * 8 * T::kAtoms; i += 32) {
+            const int rr = row_lo + i / (8 * T::kAtoms), rest = i % (8 * T::kAtoms);
+            const int band = rest / 8, cc = rest % 8;
+            *reinterpret_cast<uint4*>(gbase + (v_img - base) + band * (kChunk * 128) + sw128(rr, cc)) =
+                make_uint4(0u, 0u, 0u, 0u);
           }
-          __syncwarp();
-          if (!warp_wait(smem_addr(&p_bar[cp & 1]), (cp >> 1) & 1)) { ok = false; break; }
-          const int nsub = (min(t_end, cstart + kChunk) - cstart + 15) / 16;
-          if (lane == 0) {
-            tc_fence_after();
-            const uint32_t p_tmem = tm + T::kSCol + (cp & 1) * kChunk;
-            for (int kk = 0; kk < nsub; ++kk) {
-              const uint64_t bd = smem_desc(v_img(s) + kk * (16 * 128), kChunk * 128, 1024);
-              mma_ts(tm + T::kOCol, p_tmem + kk * 8, bd, id_o, (cp > 0 || kk > 0) ? 1u : 0u);
-            }
-            mma_commit(smem_addr(&o_bar));
-            mma_commit(smem_addr(&v_empty[s]));
-          }
-          __syncwarp();
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
+        __syncwarp();
+        if (!warp_wait(smem_addr(&p_bar), c & 1)) { ok = false; break; }
+        const int nsub = (min(t_end, cstart + kChunk) - cstart + 15) / 16;
+        if (lane == 0) {
+          tc_fence_after();
+          for (int kk = 0; kk < nsub; ++kk) {
+            const uint64_t bd = smem_desc(v_img + kk * (16 * 128), kChunk * 128, 1024);
+            mma_ts(tm + T::kOCol, s_tmem + kk * 8, bd, id_o, (c > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(smem_addr(&o_bar));
+          mma_commit(smem_addr(&v_empty));
+        }
+        __syncwarp();
       }
       if (!ok && lane == 0) sh_fail = 1;
     } else if (warp == 5) {
       // ======================= loads (TMA) ==================================
-      // K(c) once S(c - 2) has read its stage, V(c) once P . V(c - 2) has.
+      // K(c) once S(c - 1) has read the K stage, V(c) once P . V(c - 1) has
+      // read the V stage: each lands during the softmax before its use.
       bool ok = true;
       int k_issued = 0, v_issued = 0;
       auto load = [&](const CUtensorMap* map, uint32_t img, uint32_t bar, int c) {   // lane 0
@@ -451,87 +435,92 @@ __global__ void __launch_bounds__(kTThreads, 2)
         }
       };
       for (int c = 0; c < nch; ++c) {
-        const int sk = c % kKStages, sv = c % kVStages;
-        if (c >= kKStages &&
-            !warp_wait(smem_addr(&k_empty[sk]), ((c - kKStages) / kKStages) & 1)) { ok = false; break; }
-        if (lane == 0) load(&k_map, k_img(sk), smem_addr(&k_full[sk]), c);
+        if (c >= 1 && !warp_wait(smem_addr(&k_empty), (c - 1) & 1)) { ok = false; break; }
+        if (lane == 0) load(&k_map, k_img, smem_addr(&k_full), c);
         k_issued = c + 1;
-        if (c >= kVStages &&
-            !warp_wait(smem_addr(&v_empty[sv]), ((c - kVStages) / kVStages) & 1)) { ok = false; break; }
-        if (lane == 0) load(&v_map, v_img(sv), smem_addr(&v_full[sv]), c);
+        if (c >= 1 && !warp_wait(smem_addr(&v_empty), (c - 1) & 1)) { ok = false; break; }
+        if (lane == 0) load(&v_map, v_img, smem_addr(&v_full), c);
         v_issued = c + 1;
       }
       if (!ok && lane == 0) sh_fail = 1;
-      // every load issued has landed before the CTA may exit (bounded)
+      // every load issued has landed before the CTA moves on (bounded)
       if (lane == 0) {
-        for (int s = 0; s < kKStages && s < k_issued; ++s) {
-          const int last = s + kKStages * ((k_issued - 1 - s) / kKStages);
-          mbar_wait(smem_addr(&k_full[s]), (last / kKStages) & 1);
-        }
-        for (int s = 0; s < kVStages && s < v_issued; ++s) {
-          const int last = s + kVStages * ((v_issued - 1 - s) / kVStages);
-          mbar_wait(smem_addr(&v_full[s]), (last / kVStages) & 1);
-        }
+        if (k_issued > 0) mbar_wait(smem_addr(&k_full), (k_issued - 1) & 1);
+        if (v_issued > 0) mbar_wait(smem_addr(&v_full), (v_issued - 1) & 1);
       }
     } else {
       // ======================= softmax: one row per thread (warps 0-3) ======
+      // The 128 scores of a chunk row in two passes of 64 (TMEM is read
+      // twice rather than holding 128 values): the maximum, then P.  P of
+      // columns [64h, 64h + 64) lands in packed columns [32h, 32h + 32),
+      // which the first pass has already read.
       const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+      const uint32_t s_tmem = tm + lane_base + T::kSCol;
+      constexpr int kH = 2;                              // 32-key groups per pass
+      constexpr int kPasses = kChunk / (32 * kH);
       bool ok = true;
       for (int c = 0; c < nch; ++c) {
         if (__shfl_sync(0xffffffffu, sh_fail, 0)) { ok = false; break; }
-        if (!warp_wait(smem_addr(&s_bar[c & 1]), (c >> 1) & 1)) { ok = false; break; }
+        if (!warp_wait(smem_addr(&s_bar), c & 1)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t s_tmem = tm + lane_base + T::kSCol + (c & 1) * kChunk;
-        constexpr int kH = kChunk / 32;                  // 32-key halves of the chunk
-        uint32_t raw[kH][32];
-#pragma unroll
-        for (int h = 0; h < kH; ++h) tmem_ld32(s_tmem + 32 * h, raw[h]);
-        tmem_wait_ld();
         const int cstart = t0 + c * kChunk;
         const int lim = min(pos, t_end - 1);             // last key this row may see
         // only chunks that cross some row's last visible key need the mask
         const bool masked = __any_sync(0xffffffffu, cstart + kChunk - 1 > lim);
-        const float mx_raw = masked ? chunk_max<true>(raw, cstart, lim) : chunk_max<false>(raw, cstart, lim);
+        uint32_t raw[kH][32];
+        float mx_raw = -INFINITY;
+#pragma unroll
+        for (int ps = 0; ps < kPasses; ++ps) {
+#pragma unroll
+          for (int h = 0; h < kH; ++h) tmem_ld32(s_tmem + 64 * ps + 32 * h, raw[h]);
+          tmem_wait_ld();
+          const int first = cstart + 64 * ps;
+          mx_raw = fmaxf(mx_raw, masked ? chunk_max<true>(raw, first, lim) : chunk_max<false>(raw, first, lim));
+        }
         const float mx = mx_raw == -INFINITY ? -INFINITY : mx_raw * sl2;
         // move the reference maximum only when it is passed by > 2^8
         const bool need = m_ref == -INFINITY ? mx > -INFINITY : mx > m_ref + kRescaleLog2;
         const float m_new = need ? mx : m_ref;
         const float zero_ref = m_new == -INFINITY ? 0.0f : m_new;
-        uint32_t pw[kH][16];
-        const float lsum = masked ? chunk_exp<true>(raw, pw, cstart, lim, sl2, zero_ref)
-                                  : chunk_exp<false>(raw, pw, cstart, lim, sl2, zero_ref);
-        // A moved reference maximum: rescale O in TMEM once P . V of chunk
-        // c-1 has finished.  (P of chunk c goes to the other P barrier than
-        // chunk c-1's; chunk c+2's cannot arrive before S(c+2), which the
-        // issuing thread computes only after P . V of chunk c.)
+        // A moved reference maximum: rescale O in TMEM (P . V of chunk c-1
+        // finished before S(c) was issued).
         if (c > 0 && __any_sync(0xffffffffu, need)) {
           if (!warp_wait(smem_addr(&o_bar), (c - 1) & 1)) { ok = false; break; }
           tc_fence_after();
-          {
-            const float alpha = need ? (m_ref == -INFINITY ? 0.0f : exp2f(m_ref - m_new)) : 1.0f;
+          const float alpha = need ? (m_ref == -INFINITY ? 0.0f : exp2f(m_ref - m_new)) : 1.0f;
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
-              uint32_t ov[32];
-              tmem_ld32(tm + lane_base + T::kOCol + c0, ov);
-              tmem_wait_ld();
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t ov[32];
+            tmem_ld32(tm + lane_base + T::kOCol + c0, ov);
+            tmem_wait_ld();
 #pragma unroll
-              for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
-              tmem_st32(tm + lane_base + T::kOCol + c0, ov);
-            }
-            tmem_wait_st();
-            l *= alpha;
+            for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
+            tmem_st32(tm + lane_base + T::kOCol + c0, ov);
           }
+          tmem_wait_st();
+          l *= alpha;
         }
         m_ref = m_new;
-        l += lsum;
-        // P (bf16 pairs, kChunk / 2 columns) over this chunk's S
+        float lsum = 0.0f;
 #pragma unroll
-        for (int h = 0; h < kH; ++h) tmem_st16(s_tmem + 16 * h, pw[h]);
+        for (int ps = 0; ps < kPasses; ++ps) {
+#pragma unroll
+          for (int h = 0; h < kH; ++h) tmem_ld32(s_tmem + 64 * ps + 32 * h, raw[h]);
+          tmem_wait_ld();
+          const int first = cstart + 64 * ps;
+          uint32_t pw[kH][16];
+          lsum += masked ? chunk_exp<true>(raw, pw, first, lim, sl2, zero_ref)
+                         : chunk_exp<false>(raw, pw, first, lim, sl2, zero_ref);
+          // P (bf16 pairs) of these 64 keys: packed columns [32 ps, 32 ps + 32)
+#pragma unroll
+          for (int h = 0; h < kH; ++h) tmem_st16(s_tmem + 32 * ps + 16 * h, pw[h]);
+        }
         tmem_wait_st();
+        l += lsum;
         tc_fence_before();
-        mbar_arrive(smem_addr(&p_bar[c & 1]));
+        mbar_arrive(smem_addr(&p_bar));
       }
-      if (ok && !warp_wait(smem_addr(&o_bar), (nch - 1) & 1)) ok = false;
+      if (ok && nch > 0 && !warp_wait(smem_addr(&o_bar), (nch - 1) & 1)) ok = false;
       if (!ok) sh_fail = 1;
       tc_fence_after();
     }
@@ -601,18 +590,12 @@ __global__ void __launch_bounds__(kTThreads, 2)
   tc_fence_after();
   // every copy, MMA and arrival of this unit is done: the barriers start over
   if (tid == 0) {
-    for (int s = 0; s < kKStages; ++s) {
-      mbar_inval(smem_addr(&k_full[s]));
-      mbar_inval(smem_addr(&k_empty[s]));
-    }
-    for (int s = 0; s < kVStages; ++s) {
-      mbar_inval(smem_addr(&v_full[s]));
-      mbar_inval(smem_addr(&v_empty[s]));
-    }
-    mbar_inval(smem_addr(&s_bar[0]));
-    mbar_inval(smem_addr(&s_bar[1]));
-    mbar_inval(smem_addr(&p_bar[0]));
-    mbar_inval(smem_addr(&p_bar[1]));
+    mbar_inval(smem_addr(&k_full));
+    mbar_inval(smem_addr(&k_empty));
+    mbar_inval(smem_addr(&v_full));
+    mbar_inval(smem_addr(&v_empty));
+    mbar_inval(smem_addr(&s_bar));
+    mbar_inval(smem_addr(&p_bar));
     mbar_inval(smem_addr(&o_bar));
     mbar_inval(smem_addr(&drain_bar));
   }
@@ -657,7 +640,7 @@ kv_status launch_tc(const DecodeArgs& a, int ctas, cudaStream_t s) {
 }  // namespace
 
 kv_status launch_multi_tc(const DecodeArgs& a, int ctas, cudaStream_t s) {
-  if (a.part_tokens > kMaxPartTokens || a.part_tokens % 16 || ctas <= 0)
+  if (a.part_tokens > kMaxPartTokens || a.part_tokens % kChunk || ctas <= 0)
     return fail(KV_ERR_INVALID_ARG, "paged_attention_multi: bad tensor-core launch");
   if (a.head_dim == 128)
     return a.block_size == 32 ? launch_tc<128, 32>(a, ctas, s) : launch_tc<128, 16>(a, ctas, s);
