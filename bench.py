@@ -607,7 +607,7 @@ def gpu_arm(args, rank, world, local_rank, dist):
                      "kernel": ("token slot mapping + append + decode_kernel column groups / "
                                 "multi_tc_kernel (+ multi_merge_kernel), "
                                 "paged_attention_multi" if multi else
-                                "prefix_kernel + decode_kernel (append fused) + merge_kernel, one "
+                                "multi_tc_kernel (shared-prefix mode) + decode_kernel (append fused) + merge_kernel, one "
                                 "pagedkv_decode_step_prefix" if use_prefix else
                                 "decode_kernel (append fused) + merge_kernel, one pagedkv_decode_step"),
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",

@@ -1,7 +1,8 @@
 // pagedkv_api.cu -- the C ABI of libpagedkv: argument checks, slot mapping
 // and append kernels, the split-K merge kernel, and the device status word.
 // The block pool is in pagedkv_pool.cu, the decode kernel in
-// pagedkv_decode.cu, the shared-prefix kernel in pagedkv_prefix.cu.
+// pagedkv_decode.cu, the tensor-core kernel for long multi-token queries and
+// the shared prefix in pagedkv_multi_tc.cu.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -275,18 +276,24 @@ kv_status launch_merge(const DecodeArgs& a, cudaStream_t stream) {
 // ---------------------------------------------------------------------------
 
 // Largest power-of-two partition in [256, 2048] that still gives at least
-// 8 CTAs per SM over (sequence, KV head, partition).  Longer partitions
-// measured slower on GB300 (fewer, longer CTAs leave a longer tail).  The environment
-// variable PAGEDKV_PARTITION_TOKENS (a multiple of 256, read on every call)
-// overrides it.
-int choose_part_tokens(int batch, int num_kv_heads, int max_seq_len, int num_sms) {
+// 8 CTAs per SM over (sequence, KV head, partition) and, with split_longest,
+// splits a sequence of the longest length in two.  Longer partitions measured
+// slower on GB300 for one-token decode (fewer, longer CTAs leave a longer
+// tail; with lengths spread as widely as the lognormal suffixes of a
+// shared-prefix batch, the CTAs of the longest sequences alone set the step
+// time), but not for multi-token queries, whose column groups re-read each
+// block and whose partials cost more to merge.  The environment variable
+// PAGEDKV_PARTITION_TOKENS (a multiple of 256, read on every call) overrides it.
+int choose_part_tokens(int batch, int num_kv_heads, int max_seq_len, int num_sms,
+                       bool split_longest) {
   const char* s = getenv("PAGEDKV_PARTITION_TOKENS");
   const int env = s ? atoi(s) : 0;
   if (env >= kMinPartTokens && env <= kMaxPartTokens && env % kMinPartTokens == 0) return env;
   const int64_t target = 8LL * num_sms;
   int pt = kMaxPartTokens;
   while (pt > kMinPartTokens &&
-         (int64_t)batch * num_kv_heads * ((max_seq_len + pt - 1) / pt) < target)
+         ((int64_t)batch * num_kv_heads * ((max_seq_len + pt - 1) / pt) < target ||
+          (split_longest && 2 * pt > max_seq_len)))
     pt /= 2;
   return pt;
 }
@@ -391,23 +398,38 @@ int pagedkv_partition_tokens(int batch, int num_kv_heads, int max_seq_len, int b
   (void)block_size;
   DeviceInfo di;
   if (batch <= 0 || num_kv_heads <= 0 || max_seq_len <= 0 || device_info(&di) != KV_OK) return 0;
-  return choose_part_tokens(batch, num_kv_heads, max_seq_len, di.num_sms);
+  return choose_part_tokens(batch, num_kv_heads, max_seq_len, di.num_sms, true);
 }
 
 static const int kMaxPrefixChunks = 16;
 
 
 
-// Prefix chunks per row: enough (row tile, KV head, chunk) CTAs to cover the
-// SMs twice, at most one per prefix block and kMaxPrefixChunks.
-static int choose_prefix_chunks(int batch, int num_q_heads, int num_kv_heads,
-                                int num_prefix_blocks, int num_sms) {
+// Prefix partials per row.  The tensor-core prefix kernel takes units of
+// (128-row tile, KV head, prefix partial); a partial covers a multiple of 128
+// prefix tokens and at most kMaxPartTokens.  Enough partials that the units
+// cover the SMs once (the decode kernel runs beside them), within
+// [ceil(T / kMaxPartTokens), max(that, min(ceil(T / 128), kMaxPrefixChunks))]
+// for T prefix tokens -- the bound pagedkv_prefix_workspace_bytes sizes for.
+static int prefix_chunk_bound(int prefix_tokens) {
+  const int lo = (prefix_tokens + kMaxPartTokens - 1) / kMaxPartTokens;
+  const int fine = (prefix_tokens + 127) / 128;
+  const int hi = fine < kMaxPrefixChunks ? fine : kMaxPrefixChunks;
+  return hi > lo ? hi : lo;
+}
+
+static void choose_prefix_parts(int batch, int num_q_heads, int num_kv_heads, int prefix_tokens,
+                                int num_sms, int* part_tokens, int* chunks) {
   const int G = num_q_heads / num_kv_heads;
-  const int64_t base = (int64_t)((batch * G + 63) / 64) * num_kv_heads;
-  int64_t nc = (2LL * num_sms + base - 1) / base;
-  if (nc > num_prefix_blocks) nc = num_prefix_blocks;
-  if (nc > kMaxPrefixChunks) nc = kMaxPrefixChunks;
-  return (int)(nc < 1 ? 1 : nc);
+  const int64_t tiles = (int64_t)((batch * G + 127) / 128) * num_kv_heads;
+  const int lo = (prefix_tokens + kMaxPartTokens - 1) / kMaxPartTokens;
+  const int hi = prefix_chunk_bound(prefix_tokens);
+  int64_t nc = (num_sms + tiles - 1) / tiles;
+  if (nc < lo) nc = lo;
+  if (nc > hi) nc = hi;
+  const int per = (int)((prefix_tokens + nc - 1) / nc);
+  *part_tokens = (per + 127) / 128 * 128;
+  *chunks = (prefix_tokens + *part_tokens - 1) / *part_tokens;
 }
 
 // Shared body of paged_attention_decode, pagedkv_decode_step and
@@ -473,14 +495,20 @@ static kv_status decode_common(void* out, const void* q, const void* new_k, cons
   a.num_blocks = num_blocks;
   a.block_size = block_size;
   a.max_seq_len = max_seq_len;
-  a.part_tokens = choose_part_tokens(batch, num_kv_heads, max_seq_len - skip, di.num_sms);
+  a.part_tokens = choose_part_tokens(batch, num_kv_heads, max_seq_len - skip, di.num_sms, true);
   a.max_parts = (max_seq_len - skip + a.part_tokens - 1) / a.part_tokens;
+  // Few partitions per sequence: the last ones hold the ragged remainders of
+  // the sequences long enough to have them; dispatching those first leaves
+  // full partitions for the last wave (measured 4 % faster on B64 sequences
+  // of 512..4096 tokens, 2 % slower with 64 partitions per sequence).
+  a.reverse_parts = a.max_parts <= 8;
   a.skip_tokens = skip;
   a.num_prefix_blocks = num_prefix_blocks;
-  a.prefix_chunks = num_prefix_blocks > 0
-                        ? choose_prefix_chunks(batch, num_q_heads, num_kv_heads,
-                                               num_prefix_blocks, di.num_sms)
-                        : 0;
+  a.prefix_chunks = 0;
+  a.prefix_part_tokens = 0;
+  if (num_prefix_blocks > 0)
+    choose_prefix_parts(batch, num_q_heads, num_kv_heads, skip, di.num_sms, &a.prefix_part_tokens,
+                        &a.prefix_chunks);
   a.slots = a.max_parts + a.prefix_chunks;
   a.prefix_blocks = prefix_blocks;
   a.scale_log2 = scale * kLog2e;
@@ -497,7 +525,12 @@ static kv_status decode_common(void* out, const void* q, const void* new_k, cons
     a.ws_acc = a.ws_ml + ml_region_floats((size_t)batch * num_q_heads, a.slots);
   }
   cudaStream_t s = (cudaStream_t)stream;
-  if (num_prefix_blocks > 0 && (st = launch_prefix(a, s)) != KV_OK) return st;
+  if (num_prefix_blocks > 0) {
+    const int G = num_q_heads / num_kv_heads;
+    const int64_t units = (int64_t)((batch * G + 127) / 128) * num_kv_heads * a.prefix_chunks;
+    const int ctas = (int)(units < 2LL * di.num_sms ? units : 2LL * di.num_sms);
+    if ((st = launch_prefix_tc(a, ctas, s)) != KV_OK) return st;
+  }
   st = launch_decode(a, s);
   if (st != KV_OK) return st;
   return launch_merge(a, s);
@@ -559,8 +592,8 @@ size_t pagedkv_prefix_workspace_bytes(int batch, int num_q_heads, int head_dim, 
   const int rest = max_seq_len - num_prefix_blocks * block_size;
   if (rest <= 0) return 0;
   const int parts = (rest + kMinPartTokens - 1) / kMinPartTokens;
-  const int chunks = num_prefix_blocks < kMaxPrefixChunks ? num_prefix_blocks : kMaxPrefixChunks;
-  return decode_workspace_need(batch, num_q_heads, head_dim, parts + chunks);
+  return decode_workspace_need(batch, num_q_heads, head_dim,
+                               parts + prefix_chunk_bound(num_prefix_blocks * block_size));
 }
 
 kv_status pagedkv_get_status(void* stream, unsigned int* device_flags) {

@@ -63,7 +63,9 @@ struct DecodeArgs {
   int skip_tokens;             // leading tokens attended elsewhere (the shared prefix)
   int num_prefix_blocks;       // = skip_tokens / block_size
   int prefix_chunks;           // prefix partials per row, in slots [max_parts, slots)
+  int prefix_part_tokens;      // tokens per prefix partial (a multiple of 128)
   int slots;                   // max_parts + prefix_chunks
+  int reverse_parts;           // decode grid: partition max_parts-1-blockIdx.z (else blockIdx.z)
   float scale_log2;            // scale * log2(e)
   kv_dtype dtype;
   // multi-token queries: sequence b's query tokens are q rows
@@ -97,17 +99,20 @@ kv_status launch_decode(const DecodeArgs& a, cudaStream_t stream);
 // Launches the log-sum-exp merge of the partials (when any row can have more
 // than one), as a programmatic dependent of the kernel before it.
 kv_status launch_merge(const DecodeArgs& a, cudaStream_t stream);
-// Launches the shared-prefix kernel: every sequence's query rows against the
-// prefix blocks, one partial per row and prefix chunk.
-kv_status launch_prefix(const DecodeArgs& a, cudaStream_t stream);
 
 // Long multi-token queries on the tensor cores with TMEM accumulators
 // (pagedkv_multi_tc.cu): `ctas` persistent CTAs over all (KV head,
 // partition, 128-row tile) units.
 kv_status launch_multi_tc(const DecodeArgs& a, int ctas, cudaStream_t stream);
+// The same kernel in shared-prefix mode: every sequence's query rows against
+// the prefix blocks, one partial per row and prefix_part_tokens of prefix
+// (slots max_parts .. slots-1); releases the kernel queued behind it at once.
+kv_status launch_prefix_tc(const DecodeArgs& a, int ctas, cudaStream_t stream);
 
 // Token partition length for `work` independent (row group, KV head) units
 // over sequences of up to max_seq_len tokens (power of two in [256, 2048]).
-int choose_part_tokens(int work, int num_kv_heads, int max_seq_len, int num_sms);
+// With split_longest, also at most half of max_seq_len (one-token decode).
+int choose_part_tokens(int work, int num_kv_heads, int max_seq_len, int num_sms,
+                       bool split_longest);
 
 }  // namespace pagedkv

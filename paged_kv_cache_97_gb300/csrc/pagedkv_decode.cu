@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kThreads, (kQ8 || kMulti) ? PAGEDKV_Q8_MIN_BLO
   // sequences launch last, which trims the tail; neighbouring heads of one
   // block run side by side.
   // (kMulti: blockIdx.y = sequence * vgroups + column group.)
-  const int hk = blockIdx.x, part = blockIdx.z;
+  const int hk = blockIdx.x, part = a.reverse_parts ? (int)(gridDim.z - 1 - blockIdx.z) : (int)blockIdx.z;
   const int b = kMulti ? (int)(blockIdx.y / a.vgroups) : (int)blockIdx.y;
   const int vg = kMulti ? (int)(blockIdx.y % a.vgroups) : 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

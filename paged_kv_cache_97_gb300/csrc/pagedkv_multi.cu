@@ -253,7 +253,7 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
   a.block_size = block_size;
   a.max_seq_len = max_seq_len;
   a.part_tokens = choose_part_tokens((column_path ? batch * vgroups : 0) + (row_path ? (int)tiles : 0),
-                                     num_kv_heads, max_seq_len, di.num_sms);
+                                     num_kv_heads, max_seq_len, di.num_sms, false);
   a.max_parts = (max_seq_len + a.part_tokens - 1) / a.part_tokens;
   if (a.max_parts > 65535) return fail(KV_ERR_INVALID_ARG, "%s: too many partitions", who);
   if (row_path && tiles * num_kv_heads * a.max_parts > 0x7fffffffLL)

@@ -216,7 +216,7 @@ __device__ __forceinline__ int tc_tiles(int n, int GQ, int col_max_n) {
   return n > col_max_n ? (n * GQ + kTRows - 1) / kTRows : 0;
 }
 
-template <int D, int BS>
+template <int D, int BS, bool kPrefix>
 __global__ void __launch_bounds__(kTThreads, 2)
     multi_tc_kernel(const __grid_constant__ CUtensorMap k_map,
                     const __grid_constant__ CUtensorMap v_map, const DecodeArgs a) {
@@ -239,32 +239,42 @@ __global__ void __launch_bounds__(kTThreads, 2)
   const uint32_t q_img = base;                           // Q: kAtoms bands of [128 x 64]
   const uint32_t k_img = base + T::kQBytes, v_img = k_img + T::kKBytes;
 
-  // ---- row tiles per sequence (sequences past the column groups' limit, in
-  // order), prefix-summed once: scan[tid] ends the tiles of sequences
-  // tid*per .. tid*per + per - 1
+  // ---- work units.  Multi-token mode: row tiles per sequence (sequences past
+  // the column groups' limit, in order), prefix-summed once: scan[tid] ends
+  // the tiles of sequences tid*per .. tid*per + per - 1.  Shared-prefix mode:
+  // the batch's query tokens form one query block over the prefix blocks.
   const int per = (B + kTThreads - 1) / kTThreads;
   int mine = 0;
-  for (int i = 0; i < per; ++i) {
-    const int b = tid * per + i;
-    if (b < B) mine += tc_tiles(qs[b + 1] - qs[b], GQ, a.col_max_n);
-  }
-  scan[tid] = mine;
-  __syncthreads();
-  for (int off = 1; off < kTThreads; off <<= 1) {
-    const int v = tid >= off ? scan[tid - off] : 0;
+  int64_t units;
+  if constexpr (kPrefix) {
+    // the decode kernel queued behind this one reads nothing it writes
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    units = (int64_t)((B * GQ + kTRows - 1) / kTRows) * Hkv * a.prefix_chunks;
+  } else {
+    for (int i = 0; i < per; ++i) {
+      const int b = tid * per + i;
+      if (b < B) mine += tc_tiles(qs[b + 1] - qs[b], GQ, a.col_max_n);
+    }
+    scan[tid] = mine;
     __syncthreads();
-    scan[tid] += v;
-    __syncthreads();
+    for (int off = 1; off < kTThreads; off <<= 1) {
+      const int v = tid >= off ? scan[tid - off] : 0;
+      __syncthreads();
+      scan[tid] += v;
+      __syncthreads();
+    }
+    units = (int64_t)scan[kTThreads - 1] * Hkv * a.max_parts;
   }
-  const int64_t units = (int64_t)scan[kTThreads - 1] * Hkv * a.max_parts;
+  const int nparts = kPrefix ? a.prefix_chunks : a.max_parts;
+  const int ptok = kPrefix ? a.prefix_part_tokens : a.part_tokens;
   bool tm_held = false;                                  // TMEM allocated (CTA-uniform)
   uint32_t tm = 0;
 
   // ---- persistent loop over (KV head, partition, row tile) units, KV head
   // fastest
   for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
-  const int hk = (int)(u % Hkv), part = (int)((u / Hkv) % a.max_parts);
-  const int x = (int)(u / ((int64_t)Hkv * a.max_parts));   // row tile over all sequences
+  const int hk = (int)(u % Hkv), part = (int)((u / Hkv) % nparts);
+  const int x = (int)(u / ((int64_t)Hkv * nparts));      // row tile over all sequences
   __syncthreads();                                       // the last unit's readers are done
   if (tid == 0) {
     sh_b = -1;
@@ -272,7 +282,7 @@ __global__ void __launch_bounds__(kTThreads, 2)
     sh_fail = 0;
   }
   __syncthreads();
-  if (x >= scan[tid] - mine && x < scan[tid]) {
+  if (!kPrefix && x >= scan[tid] - mine && x < scan[tid]) {
     int acc = scan[tid] - mine;
     for (int i = 0; i < per; ++i) {
       const int b = tid * per + i;
@@ -287,23 +297,25 @@ __global__ void __launch_bounds__(kTThreads, 2)
     }
   }
   __syncthreads();
-  const int b = sh_b, rt = sh_rt;                        // x < the tile count: found
-  const int q0 = qs[b], n = qs[b + 1] - q0;
-  const int L = a.seq_lens[b];
-  const int t0 = part * a.part_tokens;
+  // Shared-prefix mode: row r is sequence r / GQ's one query token, which
+  // sees every prefix token.
+  const int b = kPrefix ? 0 : sh_b, rt = kPrefix ? x : sh_rt;   // x < the tile count: found
+  const int q0 = kPrefix ? 0 : qs[b], n = kPrefix ? B : qs[b + 1] - q0;
+  const int L = kPrefix ? a.num_prefix_blocks * BS : a.seq_lens[b];
+  const int t0 = part * ptok;
   if (t0 >= L && L > 0) continue;                        // no such partition (CTA-uniform)
-  const bool rows_ok = q0 >= 0 && q0 + n <= a.num_tokens;
-  const bool len_ok = rows_ok && L > 0 && n <= L && n <= a.max_query_len && L <= a.max_seq_len &&
-                      (int64_t)L <= (int64_t)a.max_blocks_per_seq * BS;
+  const bool rows_ok = kPrefix || (q0 >= 0 && q0 + n <= a.num_tokens);
+  const bool len_ok = kPrefix || (rows_ok && L > 0 && n <= L && n <= a.max_query_len &&
+                                  L <= a.max_seq_len && (int64_t)L <= (int64_t)a.max_blocks_per_seq * BS);
   const int rows_b = n * GQ;
   const int row0 = rt * kTRows;
   const int last_row = min(row0 + kTRows, rows_b) - 1;
-  const int pos_max = L - n + last_row / GQ;
-  const int t_end = min(min(t0 + a.part_tokens, L), pos_max + 1);
+  const int pos_max = kPrefix ? L - 1 : L - n + last_row / GQ;
+  const int t_end = min(min(t0 + ptok, L), pos_max + 1);
   const int nch = (len_ok && t_end > t0) ? (t_end - t0 + kChunk - 1) / kChunk : 0;
   const int first_blk = t0 / BS;
   const int last_blk = nch > 0 ? (t_end - 1) / BS : first_blk - 1;
-  const int32_t* bt = a.block_tables + (int64_t)b * a.max_blocks_per_seq;
+  const int32_t* bt = kPrefix ? a.prefix_blocks : a.block_tables + (int64_t)b * a.max_blocks_per_seq;
   // the partition's block ids, checked and kept in shared memory (the host
   // holds partitions to kMaxPartTokens tokens)
   for (int j = first_blk + tid; j <= last_blk; j += kTThreads) {
@@ -314,7 +326,7 @@ __global__ void __launch_bounds__(kTThreads, 2)
   // This thread's row (softmax warps): (query token, grouped head)
   const int r = row0 + tid;                              // meaningful for tid < 128
   const bool row_valid = tid < kTRows && len_ok && r < rows_b;
-  const int pos = row_valid ? L - n + r / GQ : -1;
+  const int pos = row_valid ? (kPrefix ? L - 1 : L - n + r / GQ) : -1;
   const int64_t qrow = row_valid ? (int64_t)(q0 + r / GQ) * Hq + (int64_t)hk * GQ + r % GQ : 0;
   // Q row into its swizzled bands (zeros for rows past the sequence's
   // queries).  A negative scale flips Q's signs instead (exact), so that the
@@ -542,11 +554,12 @@ __global__ void __launch_bounds__(kTThreads, 2)
   if (warp < 4 && rows_ok) {
     const bool mine_row = r < rows_b;
     const int64_t orow = mine_row ? (int64_t)(q0 + r / GQ) * Hq + (int64_t)hk * GQ + r % GQ : 0;
-    const bool split = a.max_parts > 1;
+    const bool split = kPrefix || a.max_parts > 1;
     const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
     const bool have = work && !failed;                   // CTA-uniform
     const float inv = (have && l > 0.0f) ? 1.0f / l : 0.0f;
-    const int64_t slot = orow * a.max_parts + part;
+    // prefix partials sit after the row's max_parts decode partitions
+    const int64_t slot = kPrefix ? orow * a.slots + a.max_parts + part : orow * a.max_parts + part;
     if (split && mine_row) {
       a.ws_ml[2 * slot] = m_ref;
       a.ws_ml[2 * slot + 1] = failed ? -1.0f : (have ? l : 0.0f);
@@ -608,7 +621,7 @@ __global__ void __launch_bounds__(kTThreads, 2)
 }
 
 
-template <int D, int BS>
+template <int D, int BS, bool kPrefix>
 kv_status launch_tc(const DecodeArgs& a, int ctas, cudaStream_t s) {
   using T = TcGeo<D>;
   static std::mutex mu;
@@ -619,7 +632,7 @@ kv_status launch_tc(const DecodeArgs& a, int ctas, cudaStream_t s) {
   {
     std::lock_guard<std::mutex> lock(mu);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-      st = cuda_check(cudaFuncSetAttribute(multi_tc_kernel<D, BS>,
+      st = cuda_check(cudaFuncSetAttribute(multi_tc_kernel<D, BS, kPrefix>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmemBytes),
                       "cudaFuncSetAttribute(multi_tc_kernel)");
       if (st != KV_OK) return st;
@@ -633,7 +646,7 @@ kv_status launch_tc(const DecodeArgs& a, int ctas, cudaStream_t s) {
   cfg.blockDim = dim3(kTThreads);
   cfg.dynamicSmemBytes = T::kSmemBytes;
   cfg.stream = s;
-  return cuda_check(cudaLaunchKernelEx(&cfg, multi_tc_kernel<D, BS>, km, vm, a),
+  return cuda_check(cudaLaunchKernelEx(&cfg, multi_tc_kernel<D, BS, kPrefix>, km, vm, a),
                     "multi_tc_kernel launch");
 }
 
@@ -643,8 +656,22 @@ kv_status launch_multi_tc(const DecodeArgs& a, int ctas, cudaStream_t s) {
   if (a.part_tokens > kMaxPartTokens || a.part_tokens % kChunk || ctas <= 0)
     return fail(KV_ERR_INVALID_ARG, "paged_attention_multi: bad tensor-core launch");
   if (a.head_dim == 128)
-    return a.block_size == 32 ? launch_tc<128, 32>(a, ctas, s) : launch_tc<128, 16>(a, ctas, s);
-  return a.block_size == 32 ? launch_tc<64, 32>(a, ctas, s) : launch_tc<64, 16>(a, ctas, s);
+    return a.block_size == 32 ? launch_tc<128, 32, false>(a, ctas, s) : launch_tc<128, 16, false>(a, ctas, s);
+  return a.block_size == 32 ? launch_tc<64, 32, false>(a, ctas, s) : launch_tc<64, 16, false>(a, ctas, s);
+}
+
+kv_status launch_prefix_tc(const DecodeArgs& a, int ctas, cudaStream_t s) {
+  if (a.dtype != KV_DTYPE_BF16)
+    return fail(KV_ERR_NOT_IMPLEMENTED, "the shared-prefix path supports bf16 pools only");
+  if (a.prefix_part_tokens <= 0 || a.prefix_part_tokens > kMaxPartTokens ||
+      a.prefix_part_tokens % kChunk || a.prefix_chunks < 1 ||
+      (int64_t)a.prefix_chunks * a.prefix_part_tokens < (int64_t)a.num_prefix_blocks * a.block_size ||
+      (int64_t)(a.prefix_chunks - 1) * a.prefix_part_tokens >= (int64_t)a.num_prefix_blocks * a.block_size ||
+      ctas <= 0)
+    return fail(KV_ERR_INVALID_ARG, "shared prefix: bad tensor-core launch");
+  if (a.head_dim == 128)
+    return a.block_size == 32 ? launch_tc<128, 32, true>(a, ctas, s) : launch_tc<128, 16, true>(a, ctas, s);
+  return a.block_size == 32 ? launch_tc<64, 32, true>(a, ctas, s) : launch_tc<64, 16, true>(a, ctas, s);
 }
 
 }  // namespace pagedkv
