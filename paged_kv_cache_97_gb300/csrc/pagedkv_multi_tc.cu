@@ -471,10 +471,19 @@ __global__ void __launch_bounds__(kTThreads, 2)
       constexpr int kH = 2;                              // 32-key groups per pass
       constexpr int kPasses = kChunk / (32 * kH);
       bool ok = true;
+      // A warp whose 32 rows are all padding (a tile's last rows) has nothing
+      // to compute: its P rows feed only O rows that are never written out,
+      // so it just keeps the barrier phases (S(c) done, then P(c) "written").
+      const bool warp_live = __any_sync(0xffffffffu, row_valid);
       for (int c = 0; c < nch; ++c) {
         if (__shfl_sync(0xffffffffu, sh_fail, 0)) { ok = false; break; }
         if (!warp_wait(smem_addr(&s_bar), c & 1)) { ok = false; break; }
         tc_fence_after();
+        if (!warp_live) {
+          tc_fence_before();
+          mbar_arrive(smem_addr(&p_bar));
+          continue;
+        }
         const int cstart = t0 + c * kChunk;
         const int lim = min(pos, t_end - 1);             // last key this row may see
         // only chunks that cross some row's last visible key need the mask
