@@ -168,34 +168,40 @@ __global__ void append_kernel(const uint4* __restrict__ k, const uint4* __restri
 }
 
 // ---------------------------------------------------------------------------
-// Log-sum-exp merge.  One CTA per (sequence, KV head), one warp per query
+// Log-sum-exp merge.  One CTA per (sequence, KV head), `wpr` warps per query
 // head; a row's partials are its partitions of tokens [skip, L) (slots
 // 0 .. np-1) and, with a shared prefix, the prefix kernel's chunks (slots
 // max_parts .. slots-1):
 //   M = max_i m_i, w_i = 2^(m_i - M), out = sum_i w_i acc_i / sum_i w_i l_i
-// A partial whose l is negative marks a bad block: the row becomes zeros.
-// Launched as a programmatic dependent of the kernel before it: the wait
-// returns once that grid has completed and its partials are visible.
+// The warps of a row take its partials in turn (a long context has dozens:
+// one warp walking them alone waits on memory once per few partials) and add
+// their sums through shared memory.  A partial whose l is negative marks a
+// bad block: the row becomes zeros.  Launched as a programmatic dependent of
+// the kernel before it: the wait returns once that grid has completed and
+// its partials are visible.
 // ---------------------------------------------------------------------------
 
-__global__ void merge_kernel(__nv_bfloat16* __restrict__ out, const float* __restrict__ ws_ml,
-                             const float* __restrict__ ws_acc,
-                             const int32_t* __restrict__ seq_lens, int num_q_heads,
-                             int num_kv_heads, int head_dim, int part_tokens, int max_parts,
-                             int slots, int skip, int prefix_chunks, int max_len) {
+__global__ void __launch_bounds__(1024)
+    merge_kernel(__nv_bfloat16* __restrict__ out, const float* __restrict__ ws_ml,
+                 const float* __restrict__ ws_acc, const int32_t* __restrict__ seq_lens,
+                 int num_q_heads, int num_kv_heads, int head_dim, int part_tokens, int max_parts,
+                 int slots, int skip, int prefix_chunks, int max_len, int wpr) {
+  extern __shared__ float red[];                   // [G][wpr][32][5] when wpr > 1
   const int b = blockIdx.x / num_kv_heads, hk = blockIdx.x % num_kv_heads;
   const int G = num_q_heads / num_kv_heads;
-  const int g = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = w / wpr, sub = w % wpr;
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int L = seq_lens[b];
-  if (g >= G || L <= skip || L > max_len) return;  // invalid rows were zeroed by the decode kernel
+  // (CTA-uniform exits, before the barrier below)
+  if (L <= skip || L > max_len) return;             // invalid rows were zeroed by the decode kernel
   const int np = (L - skip + part_tokens - 1) / part_tokens;
   const int total = np + (skip > 0 ? prefix_chunks : 0);
   if (total <= 1) return;                           // written whole by the decode kernel
   const int64_t row = (int64_t)b * num_q_heads + (int64_t)hk * G + g;
   const float* ml = ws_ml + row * slots * 2;
   const float* acc = ws_acc + row * slots * head_dim;
-  // pass 1: the largest m and any bad partial, 32 partials per round
+  // pass 1: the largest m and any bad partial (every warp of the row)
   float M = -INFINITY;
   bool bad = false;
   for (int i = lane; i < total; i += 32) {
@@ -206,26 +212,46 @@ __global__ void merge_kernel(__nv_bfloat16* __restrict__ out, const float* __res
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   bad = __any_sync(0xffffffffu, bad);
-  // pass 2: each lane owns 4 consecutive elements
+  // pass 2: this warp's partials sub, sub + wpr, ...; each lane owns 4
+  // consecutive elements
   float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
   float den = 0.0f;
   const int e0 = lane * 4;
   if (!bad) {
-#pragma unroll 4
-    for (int i = 0; i < total; ++i) {
+#pragma unroll 8
+    for (int i = sub; i < total; i += wpr) {
       const int s = i < np ? i : max_parts + (i - np);
-      const float w = exp2f(ml[2 * s] - M);
-      den = fmaf(w, ml[2 * s + 1], den);
+      const float wgt = exp2f(ml[2 * s] - M);
+      den = fmaf(wgt, ml[2 * s + 1], den);
       if (e0 < head_dim) {
         const float4 x = *reinterpret_cast<const float4*>(acc + (int64_t)s * head_dim + e0);
-        num.x = fmaf(w, x.x, num.x);
-        num.y = fmaf(w, x.y, num.y);
-        num.z = fmaf(w, x.z, num.z);
-        num.w = fmaf(w, x.w, num.w);
+        num.x = fmaf(wgt, x.x, num.x);
+        num.y = fmaf(wgt, x.y, num.y);
+        num.z = fmaf(wgt, x.z, num.z);
+        num.w = fmaf(wgt, x.w, num.w);
       }
     }
   }
-  if (e0 < head_dim) {
+  if (wpr > 1) {
+    float* r = red + ((g * wpr + sub) * 32 + lane) * 5;
+    r[0] = num.x;
+    r[1] = num.y;
+    r[2] = num.z;
+    r[3] = num.w;
+    r[4] = den;
+    __syncthreads();
+    if (sub == 0) {
+      for (int k = 1; k < wpr; ++k) {
+        const float* o = red + ((g * wpr + k) * 32 + lane) * 5;
+        num.x += o[0];
+        num.y += o[1];
+        num.z += o[2];
+        num.w += o[3];
+        den += o[4];
+      }
+    }
+  }
+  if (sub == 0 && e0 < head_dim) {
     const float r = bad ? 0.0f : 1.0f / den;
     __nv_bfloat162 lo = __floats2bfloat162_rn(bad ? 0.0f : num.x * r, bad ? 0.0f : num.y * r);
     __nv_bfloat162 hi = __floats2bfloat162_rn(bad ? 0.0f : num.z * r, bad ? 0.0f : num.w * r);
@@ -253,10 +279,15 @@ kv_status launch_merge(const DecodeArgs& a, cudaStream_t stream) {
   // With a shared prefix the partials come from two kernels: a plain launch
   // waits for both; otherwise launch behind the decode kernel (PDL).
   const int G = a.num_q_heads / a.num_kv_heads;
+  // warps per row: about 8 partials each, at most 1024 threads per CTA
+  const int most = a.max_parts + a.prefix_chunks;
+  int wpr = (most + 7) / 8;
+  if (wpr > 32 / G) wpr = 32 / G;
+  if (wpr < 1) wpr = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(a.batch * a.num_kv_heads));
-  cfg.blockDim = dim3((unsigned)(32 * G));
-  cfg.dynamicSmemBytes = 0;
+  cfg.blockDim = dim3((unsigned)(32 * G * wpr));
+  cfg.dynamicSmemBytes = wpr > 1 ? (size_t)G * wpr * 32 * 5 * sizeof(float) : 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -267,7 +298,7 @@ kv_status launch_merge(const DecodeArgs& a, cudaStream_t stream) {
                                        (const float*)a.ws_ml, (const float*)a.ws_acc, a.seq_lens,
                                        a.num_q_heads, a.num_kv_heads, a.head_dim, a.part_tokens,
                                        a.max_parts, a.slots, a.skip_tokens, a.prefix_chunks,
-                                       valid_len_limit(a)),
+                                       valid_len_limit(a), wpr),
                     "merge_kernel launch");
 }
 
