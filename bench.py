@@ -455,11 +455,21 @@ def gpu_arm(args, rank, world, local_rank, dist):
     step_fn = g.multi_step if multi else (g.prefix_step if use_prefix else g.fused_step)
     stream = torch.cuda.current_stream(dev)
     nbytes = algorithmic_bytes(wl)
-    part = pkv.partition_tokens(s.batch, s.num_kv_heads, g.max_seq_len, s.block_size)
+    # token partition of the decode kernel (the multi-token path chooses its
+    # own, not exported: not reported there)
+    part = None if multi else pkv.partition_tokens(s.batch, s.num_kv_heads,
+                                                   g.max_seq_len - s.shared_prefix_tokens * use_prefix,
+                                                   s.block_size)
     # decode (append fused) + merge, + the prefix kernel on the shared-prefix
-    # path; multi-token: slot mapping + append + attention (+ merge when the
-    # keys are split, counted as launched)
-    launches_per_step = (4 if multi else 3 if use_prefix else 1 + (1 if g.max_seq_len > part else 0))
+    # path; multi-token: slot mapping + append + merge + the column groups
+    # (sequences with few queries) and/or the tensor-core kernel (long ones)
+    if multi:
+        G = s.num_q_heads // s.num_kv_heads
+        col_max = (8 // G) * 4 if G <= 8 else 0
+        launches_per_step = (3 + int(bool((wl.query_lens <= col_max).any()))
+                             + int(bool((wl.query_lens > col_max).any())))
+    else:
+        launches_per_step = 3 if use_prefix else 1 + (1 if g.max_seq_len > part else 0)
 
     for _ in range(args.warmup):
         step_fn()
