@@ -438,10 +438,12 @@ static const int kMaxPrefixChunks = 16;
 
 // Prefix partials per row.  The tensor-core prefix kernel takes units of
 // (128-row tile, KV head, prefix partial); a partial covers a multiple of 128
-// prefix tokens and at most kMaxPartTokens.  Enough partials that the units
-// cover the SMs once (the decode kernel runs beside them), within
-// [ceil(T / kMaxPartTokens), max(that, min(ceil(T / 128), kMaxPrefixChunks))]
-// for T prefix tokens -- the bound pagedkv_prefix_workspace_bytes sizes for.
+// prefix tokens and at most kMaxPartTokens.  The product runs beside the
+// decode kernel and only has to finish before it, so rows get as few partials
+// as that allows: ceil(T / kMaxPartTokens) for T prefix tokens (fewer partials
+// to write and merge; workload 4: one 896-token partial 119.3 us per step,
+// two 122.0, three 123.9).  pagedkv_prefix_workspace_bytes sizes for
+// prefix_chunk_bound(T) >= that.
 static int prefix_chunk_bound(int prefix_tokens) {
   const int lo = (prefix_tokens + kMaxPartTokens - 1) / kMaxPartTokens;
   const int fine = (prefix_tokens + 127) / 128;
@@ -449,16 +451,9 @@ static int prefix_chunk_bound(int prefix_tokens) {
   return hi > lo ? hi : lo;
 }
 
-static void choose_prefix_parts(int batch, int num_q_heads, int num_kv_heads, int prefix_tokens,
-                                int num_sms, int* part_tokens, int* chunks) {
-  const int G = num_q_heads / num_kv_heads;
-  const int64_t tiles = (int64_t)((batch * G + 127) / 128) * num_kv_heads;
-  const int lo = (prefix_tokens + kMaxPartTokens - 1) / kMaxPartTokens;
-  const int hi = prefix_chunk_bound(prefix_tokens);
-  int64_t nc = (num_sms + tiles - 1) / tiles;
-  if (nc < lo) nc = lo;
-  if (nc > hi) nc = hi;
-  const int per = (int)((prefix_tokens + nc - 1) / nc);
+static void choose_prefix_parts(int prefix_tokens, int* part_tokens, int* chunks) {
+  const int nc = (prefix_tokens + kMaxPartTokens - 1) / kMaxPartTokens;
+  const int per = (prefix_tokens + nc - 1) / nc;
   *part_tokens = (per + 127) / 128 * 128;
   *chunks = (prefix_tokens + *part_tokens - 1) / *part_tokens;
 }
@@ -538,8 +533,7 @@ static kv_status decode_common(void* out, const void* q, const void* new_k, cons
   a.prefix_chunks = 0;
   a.prefix_part_tokens = 0;
   if (num_prefix_blocks > 0)
-    choose_prefix_parts(batch, num_q_heads, num_kv_heads, skip, di.num_sms, &a.prefix_part_tokens,
-                        &a.prefix_chunks);
+    choose_prefix_parts(skip, &a.prefix_part_tokens, &a.prefix_chunks);
   a.slots = a.max_parts + a.prefix_chunks;
   a.prefix_blocks = prefix_blocks;
   a.scale_log2 = scale * kLog2e;
@@ -558,14 +552,15 @@ static kv_status decode_common(void* out, const void* q, const void* new_k, cons
   cudaStream_t s = (cudaStream_t)stream;
   if (num_prefix_blocks > 0) {
     // The prefix product is small beside the decode's KV stream and only has
-    // to finish before it: at most 5 units per CTA but no more than a quarter
-    // of the SMs busy with it (then each of those SMs still holds two decode
+    // to finish before it: about 16 chunks of 128 keys per CTA but no fewer
+    // than a quarter of the SMs (each of those SMs still holds two decode
     // CTAs, enough loads in flight to keep its share of HBM bandwidth).
     // Workload of 256 sequences behind an 800-token prefix: 38 CTAs 123.4 us
-    // per step, 76 CTAs 123.8, 152 CTAs 128.5, 304 CTAs 130.3.
+    // per step, 76 CTAs 123.8, 152 CTAs 128.5, 304 CTAs 130.3 (three partials).
     const int G = num_q_heads / num_kv_heads;
     const int64_t units = (int64_t)((batch * G + 127) / 128) * num_kv_heads * a.prefix_chunks;
-    int64_t ctas = (units + 4) / 5;
+    const int64_t chunks = units * (a.prefix_part_tokens / 128);
+    int64_t ctas = (chunks + 15) / 16;
     const int64_t quarter = di.num_sms / 4 > 0 ? di.num_sms / 4 : 1;
     if (ctas < quarter) ctas = quarter;
     if (ctas > 2LL * di.num_sms) ctas = 2LL * di.num_sms;
