@@ -379,6 +379,28 @@ __global__ void __launch_bounds__(kThreads, (kQ8 || kMulti) ? PAGEDKV_Q8_MIN_BLO
       }
     }
     const float score_scale = a.scale_log2 / qscale;
+    // int8 K enters the MMA as fp16 w = c + 1152 (one byte permute per code
+    // pair, no subtraction): S = sum_d q_d w_d - 1152 sum_d q_d, so each
+    // score column (heads 2t, 2t+1 of this lane) subtracts 1152 times the
+    // sum of its fp16 q -- summed here from the B fragments lane (g, t)
+    // holds for head g (exact products; the cancellation costs about 2^-24
+    // of the biased sum, some 1e-6 of a score).
+    float kb0 = 0.0f, kb1 = 0.0f;
+    if constexpr (kQ8 && !kFp8) {
+      float sq = 0.0f;
+#pragma unroll
+      for (int ks = 0; ks < G::kKSteps; ++ks) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const __half2 h = *reinterpret_cast<const __half2*>(&qf[ks][r]);
+          sq += __low2float(h) + __high2float(h);
+        }
+      }
+      sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+      sq += __shfl_xor_sync(0xffffffffu, sq, 2);        // sum over head g (lanes 4g..4g+3)
+      kb0 = -1152.0f * __shfl_sync(0xffffffffu, sq, (2 * t) * 4);
+      kb1 = -1152.0f * __shfl_sync(0xffffffffu, sq, (2 * t + 1) * 4);
+    }
     // causal limits of this lane's columns 2t and 2t+1 (multi-token queries)
     int cpos0 = 0x7fffffff, cpos1 = 0x7fffffff;
     if constexpr (kMulti) {
@@ -439,8 +461,8 @@ __global__ void __launch_bounds__(kThreads, (kQ8 || kMulti) ? PAGEDKV_Q8_MIN_BLO
 #pragma unroll
             for (int ks = 0; ks < G::kKSteps; ++ks) {
               const uint32_t w0 = kw[0][ks / 4][ks % 4], w1 = kw[1][ks / 4][ks % 4];
-              const uint32_t fa[4] = {codes_to_f16x2<kFp8>(w0, 0x4140u), codes_to_f16x2<kFp8>(w1, 0x4140u),
-                                      codes_to_f16x2<kFp8>(w0, 0x4342u), codes_to_f16x2<kFp8>(w1, 0x4342u)};
+              const uint32_t fa[4] = {codes_to_f16x2<kFp8, true>(w0, 0x4140u), codes_to_f16x2<kFp8, true>(w1, 0x4140u),
+                                      codes_to_f16x2<kFp8, true>(w0, 0x4342u), codes_to_f16x2<kFp8, true>(w1, 0x4342u)};
               if (ks & 1) mma16816<true>(c1, fa, qf[ks][0], qf[ks][1]);
               else        mma16816<true>(c0, fa, qf[ks][0], qf[ks][1]);
             }
@@ -450,15 +472,15 @@ __global__ void __launch_bounds__(kThreads, (kQ8 || kMulti) ? PAGEDKV_Q8_MIN_BLO
           const int tok_lo = tile * 16 + g, tok_hi = tok_lo + 8;
           if constexpr (kMulti) {
             const int abs_lo = (first_blk + j) * BS + tok_lo, abs_hi = abs_lo + 8;
-            sc[tile][0] = (tok_lo < valid && abs_lo <= cpos0) ? (c0[0] + c1[0]) * kfac : -INFINITY;
-            sc[tile][1] = (tok_lo < valid && abs_lo <= cpos1) ? (c0[1] + c1[1]) * kfac : -INFINITY;
-            sc[tile][2] = (tok_hi < valid && abs_hi <= cpos0) ? (c0[2] + c1[2]) * kfac : -INFINITY;
-            sc[tile][3] = (tok_hi < valid && abs_hi <= cpos1) ? (c0[3] + c1[3]) * kfac : -INFINITY;
+            sc[tile][0] = (tok_lo < valid && abs_lo <= cpos0) ? (c0[0] + c1[0] + kb0) * kfac : -INFINITY;
+            sc[tile][1] = (tok_lo < valid && abs_lo <= cpos1) ? (c0[1] + c1[1] + kb1) * kfac : -INFINITY;
+            sc[tile][2] = (tok_hi < valid && abs_hi <= cpos0) ? (c0[2] + c1[2] + kb0) * kfac : -INFINITY;
+            sc[tile][3] = (tok_hi < valid && abs_hi <= cpos1) ? (c0[3] + c1[3] + kb1) * kfac : -INFINITY;
           } else {
-            sc[tile][0] = tok_lo < valid ? (c0[0] + c1[0]) * kfac : -INFINITY;
-            sc[tile][1] = tok_lo < valid ? (c0[1] + c1[1]) * kfac : -INFINITY;
-            sc[tile][2] = tok_hi < valid ? (c0[2] + c1[2]) * kfac : -INFINITY;
-            sc[tile][3] = tok_hi < valid ? (c0[3] + c1[3]) * kfac : -INFINITY;
+            sc[tile][0] = tok_lo < valid ? (c0[0] + c1[0] + kb0) * kfac : -INFINITY;
+            sc[tile][1] = tok_lo < valid ? (c0[1] + c1[1] + kb1) * kfac : -INFINITY;
+            sc[tile][2] = tok_hi < valid ? (c0[2] + c1[2] + kb0) * kfac : -INFINITY;
+            sc[tile][3] = tok_hi < valid ? (c0[3] + c1[3] + kb1) * kfac : -INFINITY;
           }
         }
 

@@ -175,10 +175,11 @@ constexpr uint32_t kCodeBias = kFp8 ? 0u : 0x80808080u;
 // either way; sel 0x4140 takes bytes 0,1 and 0x4342 bytes 2,3.
 //   int8: w already XORed with kCodeBias, so each byte is c + 128; the
 //         bytes are placed under 0x64 (fp16 1024 + byte) and 1152 is
-//         subtracted: c.
+//         subtracted: c.  kBiased leaves c + 1152 (the caller removes the
+//         1152 from its sums).
 //   E4M3: the hardware conversion of an e4m3 pair to f16x2 (every E4M3
 //         value, subnormals included, is an fp16 value).
-template <bool kFp8>
+template <bool kFp8, bool kBiased = false>
 __device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t w, uint32_t sel) {
   if constexpr (kFp8) {
     const unsigned short pair = sel == 0x4140u ? (unsigned short)(w & 0xffffu)
@@ -188,6 +189,7 @@ __device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t w, uint32_t sel) {
     return h;
   } else {
     const uint32_t h = prmt(w, 0x64646464u, sel);
+    if constexpr (kBiased) return h;
     __half2 x = *reinterpret_cast<const __half2*>(&h);
     x = __hsub2(x, __half2half2(__ushort_as_half((unsigned short)0x6480)));  // 1152.0
     return *reinterpret_cast<const uint32_t*>(&x);
