@@ -258,6 +258,13 @@ PREFIX_CASES = {
                                               999, 1001, 608, 2048, 1800, 777, 650],
                                              hq=8, hkv=2, d=64, prefix=592, seed=33),
     "g1_d128": lambda: small([17, 40, 333], hq=4, hkv=4, d=128, prefix=16, seed=34),
+    # prefixes past one 2048-token prefix partial: three partials of 1408
+    # tokens (and a 16-row tile: three of four softmax warps hold padding)
+    "g4_d128_bs16_prefix_4224": lambda: small([4225, 4300, 5000, 6500], hq=32, hkv=8, d=128,
+                                              prefix=4224, seed=35),
+    # two partials of 1152 tokens over 65 blocks of 32, G = 8
+    "g8_d64_bs32_prefix_2080": lambda: small([2081, 2100, 3000], hq=16, hkv=2, d=64, bs=32,
+                                             prefix=2080, seed=36),
 }
 
 
