@@ -432,30 +432,22 @@ int pagedkv_partition_tokens(int batch, int num_kv_heads, int max_seq_len, int b
   return choose_part_tokens(batch, num_kv_heads, max_seq_len, di.num_sms, true);
 }
 
-static const int kMaxPrefixChunks = 16;
-
-
-
 // Prefix partials per row.  The tensor-core prefix kernel takes units of
 // (128-row tile, KV head, prefix partial); a partial covers a multiple of 128
 // prefix tokens and at most kMaxPartTokens.  The product runs beside the
 // decode kernel and only has to finish before it, so rows get as few partials
 // as that allows: ceil(T / kMaxPartTokens) for T prefix tokens (fewer partials
 // to write and merge; workload 4: one 896-token partial 119.3 us per step,
-// two 122.0, three 123.9).  pagedkv_prefix_workspace_bytes sizes for
-// prefix_chunk_bound(T) >= that.
-static int prefix_chunk_bound(int prefix_tokens) {
-  const int lo = (prefix_tokens + kMaxPartTokens - 1) / kMaxPartTokens;
-  const int fine = (prefix_tokens + 127) / 128;
-  const int hi = fine < kMaxPrefixChunks ? fine : kMaxPrefixChunks;
-  return hi > lo ? hi : lo;
+// two 122.0, three 123.9).  pagedkv_prefix_workspace_bytes sizes for this.
+static int prefix_chunk_count(int prefix_tokens) {
+  return (prefix_tokens + kMaxPartTokens - 1) / kMaxPartTokens;
 }
 
 static void choose_prefix_parts(int prefix_tokens, int* part_tokens, int* chunks) {
-  const int nc = (prefix_tokens + kMaxPartTokens - 1) / kMaxPartTokens;
+  const int nc = prefix_chunk_count(prefix_tokens);
   const int per = (prefix_tokens + nc - 1) / nc;
   *part_tokens = (per + 127) / 128 * 128;
-  *chunks = (prefix_tokens + *part_tokens - 1) / *part_tokens;
+  *chunks = (prefix_tokens + *part_tokens - 1) / *part_tokens;   // <= nc
 }
 
 // Shared body of paged_attention_decode, pagedkv_decode_step and
@@ -629,7 +621,7 @@ size_t pagedkv_prefix_workspace_bytes(int batch, int num_q_heads, int head_dim, 
   if (rest <= 0) return 0;
   const int parts = (rest + kMinPartTokens - 1) / kMinPartTokens;
   return decode_workspace_need(batch, num_q_heads, head_dim,
-                               parts + prefix_chunk_bound(num_prefix_blocks * block_size));
+                               parts + prefix_chunk_count(num_prefix_blocks * block_size));
 }
 
 kv_status pagedkv_get_status(void* stream, unsigned int* device_flags) {
