@@ -179,11 +179,12 @@ def oracle_time(wl, pools, seqs, threads):
     return dt, kv
 
 
-def oracle_sample(wl, threads, target_s=10.0, max_s=30.0):
+def oracle_sample(wl, threads, target_s=10.0, max_s=30.0, pools=None):
     """Time the oracle for about target_s of work (bounded by max_s): growing
     prefixes of the batch, and when the whole batch takes less than
     target_s, repeated passes over it.  Returns a cpu_baseline dict."""
-    pools = oracle_pools(wl)
+    if pools is None:
+        pools = oracle_pools(wl)
     n = 2
     while True:
         seqs = list(range(min(n, wl.spec.batch)))
@@ -698,7 +699,13 @@ def main():
         dist.init_process_group("nccl")
     line, wl = gpu_arm(args, rank, world, local_rank, dist)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = oracle_sample(wl, os.cpu_count() or 1)
+        pools = oracle_pools(wl)
+        line["cpu_baseline"] = oracle_sample(wl, os.cpu_count() or 1, pools=pools)
+        if args.config in (1, 2):
+            # the same oracle on one core (a few seconds of work)
+            one = oracle_sample(wl, 1, target_s=3.0, max_s=8.0, pools=pools)
+            line["cpu_baseline"]["single_thread"] = {"value": one["value"], "unit": one["unit"],
+                                                     "cores": 1, "sample": one["sample"]}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
