@@ -110,12 +110,7 @@ __global__ void __launch_bounds__(kThreads, (kQ8 || kMulti) ? PAGEDKV_Q8_MIN_BLO
     nq = a.query_start[b + 1] - q0;
   }
   const int TPG = kMulti ? kMaxGroup / GQ : 1;
-  // Multi-token queries: the kernel queued behind this one (the row-tiled
-  // kernel for long queries) reads nothing this one writes -- let it start
-  // now so both fill the GPU.  (The decode path's merge waits for this grid
-  // with griddepcontrol.wait and is released at the end instead.)
-  if constexpr (kMulti) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (kMulti && nq > a.col_max_n) return;                // a long query: the row-tiled kernel's
+  if (kMulti && nq > a.col_max_n) return;                // a long query: the tensor-core kernel's
   const bool rows_ok = !kMulti || (q0 >= 0 && nq >= 0 && q0 + nq <= a.num_tokens);
   // Row of the q / out tensors that column c serves (-1: a padding column):
   // head c of the group, or (kMulti) token vg * TPG + c / GQ, head c % GQ.
@@ -689,6 +684,8 @@ __global__ void __launch_bounds__(kThreads, (kQ8 || kMulti) ? PAGEDKV_Q8_MIN_BLO
       }
     }
   }
+  // this CTA's partials are written: the merge launched behind this grid
+  // (programmatic dependent; it waits for the whole grid) may be scheduled
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
