@@ -98,22 +98,35 @@ def _check(st: int):
         raise KVError(st, load().pagedkv_last_error().decode(errors="replace"))
 
 
+_raw_stream = None          # torch's raw current-stream query, resolved once
+
+
 def _stream(stream):
+    """The cudaStream_t to launch on: `stream` (a torch stream or a raw
+    handle), else torch's current stream on the current device.  Pointer
+    arguments go to ctypes as plain ints (the signatures convert them)."""
+    global _raw_stream
     import torch
     if stream is None:
-        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        if _raw_stream is None:
+            # the raw query skips torch.cuda.current_stream's device-argument
+            # handling (a third of a small step's host time); same stream
+            _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", False)
+        if _raw_stream:
+            return _raw_stream(torch.cuda.current_device())
+        return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, int):
-        return ctypes.c_void_p(stream)
-    return ctypes.c_void_p(stream.cuda_stream)
+        return stream
+    return stream.cuda_stream
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
 def _need(t, dtype, name, ndim=None):
     import torch
-    if not isinstance(t, torch.Tensor):
+    if type(t) is not torch.Tensor and not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
