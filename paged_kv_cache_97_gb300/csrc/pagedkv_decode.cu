@@ -263,6 +263,10 @@ __global__ void __launch_bounds__(kThreads, (kQ8 || kMulti) ? PAGEDKV_Q8_MIN_BLO
   float o[G::kMTiles][4];
 #pragma unroll
   for (int i = 0; i < G::kMTiles; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
+  // int8 V enters P . V as c + 1152 (no subtraction per code pair); vb holds
+  // sum_t p_t per column (an all-ones A fragment times P^T, one MMA per tile)
+  // and O loses 1152 vsum before the warps combine.
+  float vsum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 
   if (!bad && warp == kConsumers) {
     // ======================= producer =======================================
@@ -508,6 +512,12 @@ __global__ void __launch_bounds__(kThreads, (kQ8 || kMulti) ? PAGEDKV_Q8_MIN_BLO
           o[i][2] *= al0;
           o[i][3] *= al1;
         }
+        if constexpr (kQ8 && !kFp8) {
+          vsum[0] *= al0;
+          vsum[1] *= al1;
+          vsum[2] *= al0;
+          vsum[3] *= al1;
+        }
         const float vr = kQ8 ? blk_vr[j] : 1.0f;
 
 #pragma unroll
@@ -573,13 +583,17 @@ __global__ void __launch_bounds__(kThreads, (kQ8 || kMulti) ? PAGEDKV_Q8_MIN_BLO
                 vw[rr][1] = v.y ^ kCodeBias<kFp8>;
               }
             }
+            if constexpr (!kFp8) {
+              const uint32_t ones[4] = {0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u};
+              mma16816<true>(vsum, ones, pb0, pb1);
+            }
 #pragma unroll
             for (int i = 0; i < G::kMTiles; ++i) {
               const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;  // bytes 2,3 or 0,1
               const uint32_t ulo = prmt(vw[0][i / 2], vw[1][i / 2], sel);  // tokens 2t, 2t+1
               const uint32_t uhi = prmt(vw[2][i / 2], vw[3][i / 2], sel);  // tokens 2t+8, 2t+9
-              uint32_t fa[4] = {codes_to_f16x2<kFp8>(ulo, 0x4140u), codes_to_f16x2<kFp8>(ulo, 0x4342u),
-                                codes_to_f16x2<kFp8>(uhi, 0x4140u), codes_to_f16x2<kFp8>(uhi, 0x4342u)};
+              uint32_t fa[4] = {codes_to_f16x2<kFp8, true>(ulo, 0x4140u), codes_to_f16x2<kFp8, true>(ulo, 0x4342u),
+                                codes_to_f16x2<kFp8, true>(uhi, 0x4140u), codes_to_f16x2<kFp8, true>(uhi, 0x4342u)};
               if constexpr (kFp8) {
                 fa[0] &= mlo;
                 fa[1] &= mlo;
@@ -615,6 +629,12 @@ __global__ void __launch_bounds__(kThreads, (kQ8 || kMulti) ? PAGEDKV_Q8_MIN_BLO
       red_m[warp * 8 + 2 * t + 1] = m_run[1];
       red_l[warp * 8 + 2 * t] = l_run[0];
       red_l[warp * 8 + 2 * t + 1] = l_run[1];
+    }
+    if constexpr (kQ8 && !kFp8) {
+#pragma unroll
+      for (int i = 0; i < G::kMTiles; ++i)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) o[i][k] = fmaf(-1152.0f, vsum[k], o[i][k]);
     }
     float* acc = red_acc + warp * 8 * D;
 #pragma unroll
