@@ -37,7 +37,16 @@
 // are zeroed in shared memory before P . V (p is 0 there but the pool may
 // hold NaN).  Every wait is bounded; a CTA that gives up flags
 // PAGEDKV_FLAG_WAIT_TIMEOUT, drains its copies and tensor-core work, frees its
-// TMEM and marks its rows bad.  bf16 pools.
+// TMEM and marks its rows bad.  A warp whose 32 rows are all padding only
+// keeps the barrier phases.  bf16 pools.
+//
+// Shared-prefix mode (kPrefix): when every sequence's first blocks are the
+// same physical blocks (“让 Agent 跑得快”, §五 共享前缀), the prefix part of
+// attention is one dense, unmasked product per KV head; the batch's query
+// tokens (one per sequence) form the query block, every row sees every prefix
+// token, the block ids come from the prefix list, and each row's partial goes
+// to its slots after the decode partitions for the merge.  The host runs it
+// on few CTAs ahead of the decode kernel, which it releases at once.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
