@@ -41,8 +41,24 @@ UNIT = "GB/s"
 DEFAULT_CONFIG = 2
 FALLBACK_HBM_GBS = 6800.0
 GRAPH_STEPS = 20
+L2_BYTES = 129e6                                         # GB300 L2
 DECODE_SOURCE = os.path.join(ROOT, "paged_kv_cache_97_gb300", "csrc", "pagedkv_decode.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
+
+
+def workload_config(wl, nbytes) -> dict:
+    """The workload as both arms report it in `config`: shapes, the seeded
+    length mix and the KV bytes one step reads."""
+    s = wl.spec
+    return {"workload": s.name, "batch": s.batch, "num_q_heads": s.num_q_heads,
+            "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim,
+            "block_size": s.block_size, "kv_dtype": s.kv_dtype,
+            "seq_lens": f"seed {wl.seed}: min {int(wl.seq_lens.min())}, "
+                        f"mean {float(wl.seq_lens.mean()):.0f}, max {int(wl.seq_lens.max())}",
+            "kv_bytes_per_step": nbytes["kv_logical"],
+            "l2": ("inputs larger than L2 (KV read per step > 129 MB), no flush"
+                   if nbytes["kv_logical"] > L2_BYTES else
+                   "inputs fit in L2 and are not flushed: an L2-resident, launch-latency figure")}
 
 
 # ---------------------------------------------------------------------------
@@ -606,14 +622,8 @@ def gpu_arm(args, rank, world, local_rank, dist):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if s.kv_dtype == "bf16" else f"{s.kv_dtype} KV, bf16 q/out, fp32 accumulate",
         "data": "synthetic",
-        "config": {"workload": s.name, "batch": s.batch, "num_q_heads": s.num_q_heads,
-                   "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim,
-                   "block_size": s.block_size, "kv_dtype": s.kv_dtype,
-                   "seq_lens": f"seed {wl.seed}: min {int(wl.seq_lens.min())}, "
-                               f"mean {float(wl.seq_lens.mean()):.0f}, max {int(wl.seq_lens.max())}",
-                   "kv_bytes_per_step": nbytes["kv_logical"], "partition_tokens": part,
-                   "l2": "inputs larger than L2 (KV read per step > 129 MB), no flush",
-                   "parallelism": f"replicas x{world}"},
+        "config": dict(workload_config(wl, nbytes), partition_tokens=part,
+                       parallelism=f"replicas x{world}"),
         "roofline": {"bound": "hbm",
                      "kernel": ("token slot mapping + append + decode_kernel column groups / "
                                 "multi_tc_kernel (+ multi_merge_kernel), "
@@ -685,7 +695,7 @@ def main():
             "impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": UNIT, "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": wl.spec.name},
+            "data": "synthetic", "config": dict(workload_config(wl, algorithmic_bytes(wl)), parallelism="oracle on host cores"),
             "cpu_baseline": {"value": round(v, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": "per step: one sequence of the batch (cycling), all query heads, "
                                        "fp64 three-pass oracle"},
