@@ -56,7 +56,14 @@ extern "C" kv_status paged_attention_decode_noalloc(
     const float* v_scale, const int32_t* block_tables, int max_blocks_per_seq,
     const int32_t* seq_lens, int batch, int num_q_heads, int num_kv_heads, int head_dim,
     int num_blocks, int block_size, int max_seq_len, float scale, kv_dtype dtype, void* stream) {
-  if (batch > 0 && num_q_heads > 0 && num_kv_heads > 0 && head_dim > 0 && max_seq_len > 0) {
+  // An empty batch (and any bad size) is settled by the argument checks of
+  // paged_attention_decode before it touches a device: no scratch is needed.
+  if (batch <= 0)
+    return paged_attention_decode(out, q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                                  max_blocks_per_seq, seq_lens, batch, num_q_heads,
+                                  num_kv_heads, head_dim, num_blocks, block_size, max_seq_len,
+                                  scale, dtype, nullptr, 0, stream);
+  if (num_q_heads > 0 && num_kv_heads > 0 && head_dim > 0 && max_seq_len > 0) {
     // Scratch this call needs: the partials of every (sequence, query head,
     // partition) when a sequence spans several partitions.
     const int part = pagedkv_partition_tokens(batch, num_kv_heads, max_seq_len, block_size);

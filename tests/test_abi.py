@@ -123,3 +123,38 @@ def test_host_checks_fail_before_touching_the_gpu(pkv):
     st = lib.reshape_and_cache(P + 8, P, P, P, None, None, P, 3, 10, 16, 2, 64, 0, None)
     assert st == pkv.KV_ERR_INVALID_ARG and b"aligned" in lib.pagedkv_last_error()
     assert lib.reshape_and_cache(None, None, None, None, None, None, None, 0, 10, 16, 2, 64, 0, None) == 0
+
+
+def test_empty_inputs_return_ok_without_a_device(pkv):
+    # Zero sequences, tokens or block pairs: every entry point checks its
+    # sizes, then returns KV_OK with no launch.  This runs on a machine with
+    # no GPU, where any CUDA call would fail, so it also shows that nothing
+    # reaches the device.
+    lib = pkv.load()
+    assert lib.pagedkv_slot_mapping(None, 4, None, 0, 16, 10, None, None) == pkv.KV_OK
+    assert lib.pagedkv_token_slot_mapping(None, 4, None, None, 0, 16, 10, None, None) == pkv.KV_OK
+    assert lib.reshape_and_cache(None, None, None, None, None, None, None, 0, 10, 16, 2, 64, 0,
+                                 None) == pkv.KV_OK
+    assert lib.paged_attention_decode(None, None, None, None, None, None, None, 4, None, 0, 8, 2,
+                                      64, 10, 16, 64, 0.125, 0, None, 0, None) == pkv.KV_OK
+    assert lib.paged_attention_decode_noalloc(None, None, None, None, None, None, None, 4, None,
+                                              0, 8, 2, 64, 10, 16, 64, 0.125, 0, None) == pkv.KV_OK
+    assert lib.pagedkv_decode_step(None, None, None, None, None, None, None, None, None, 4, None,
+                                   0, 8, 2, 64, 10, 16, 64, 0.125, 0, None, 0, None) == pkv.KV_OK
+    assert lib.pagedkv_decode_step_prefix(None, None, None, None, None, None, None, None, None, 4,
+                                          None, 0, 8, 2, 64, 10, 16, 64, 0.125, 0, None, 0, None,
+                                          0, None) == pkv.KV_OK
+    assert lib.paged_attention_multi(None, None, None, None, None, None, None, 4, None, None, 0, 0,
+                                     1, 8, 2, 64, 10, 16, 64, 0.125, 0, None, 0, None) == pkv.KV_OK
+    assert lib.pagedkv_copy_blocks(None, None, None, None, None, 0, 10, 16, 2, 64, 0,
+                                   None) == pkv.KV_OK
+    assert lib.pagedkv_workspace_bytes(0, 8, 64, 64, 16) == 0
+    assert lib.pagedkv_multi_workspace_bytes(0, 8, 64, 64, 16) == 0
+    assert lib.pagedkv_prefix_workspace_bytes(0, 8, 64, 64, 16, 2) == 0
+    # an empty batch still gets its sizes checked
+    assert lib.paged_attention_decode_noalloc(None, None, None, None, None, None, None, 4, None,
+                                              0, 8, 3, 64, 10, 16, 64, 0.125, 0,
+                                              None) == pkv.KV_ERR_INVALID_ARG
+    assert lib.paged_attention_decode_noalloc(None, None, None, None, None, None, None, 4, None,
+                                              -1, 8, 2, 64, 10, 16, 64, 0.125, 0,
+                                              None) == pkv.KV_ERR_INVALID_ARG
