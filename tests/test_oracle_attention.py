@@ -170,8 +170,7 @@ def test_identical_keys_give_mean_of_v(oracle_mod):
 # Online recurrence and split-K merge
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("bs", [16, 32])
-def test_online_equals_three_pass(oracle_mod, bs):
+def check_online(bs):
     wl = small([1, 16, 17, 100, 333, 1000], hq=8, hkv=2, d=64, bs=bs, seed=13)
     ref, rc = run(wl)
     got, rc2 = run(wl, mode="online")
@@ -179,8 +178,12 @@ def test_online_equals_three_pass(oracle_mod, bs):
     np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-14)
 
 
-@pytest.mark.parametrize("part", [16, 48, 64, 512, 4096])
-def test_partials_merge_equals_full(oracle_mod, part):
+@pytest.mark.parametrize("bs", [16, 32])
+def test_online_equals_three_pass(oracle_mod, bs):
+    check_online(bs)
+
+
+def check_partials_merge(part):
     wl = small([1, 17, 100, 700], hq=8, hkv=2, d=64, seed=17)
     kc, vc, ks, vs = oracle_pool(wl)
     ref, _ = run(wl, (kc, vc, ks, vs))
@@ -190,6 +193,11 @@ def test_partials_merge_equals_full(oracle_mod, part):
                                                 wl.spec.scale, b, h, part)
             assert ml.shape[0] == -(-int(wl.seq_lens[b]) // part)
             np.testing.assert_allclose(oracle.lse_merge(ml, acc), ref[b, h], rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("part", [16, 48, 64, 512, 4096])
+def test_partials_merge_equals_full(oracle_mod, part):
+    check_partials_merge(part)
 
 
 # ---------------------------------------------------------------------------

@@ -9,7 +9,8 @@ import pytest
 
 import oracle
 from test_oracle_append import check_fp32_decision, check_rounding
-from test_oracle_attention import check_against_sdpa, check_int8_against_sdpa, small
+from test_oracle_attention import (check_against_sdpa, check_int8_against_sdpa, check_online,
+                                   check_partials_merge, small)
 from test_oracle_fp8 import check_decode, check_encode, check_fp8_against_sdpa, check_saturation
 from test_oracle_multi import check_multi_against_sdpa, multi
 
@@ -34,6 +35,15 @@ def _fp8_codes():
 
 def _multi():
     check_multi_against_sdpa(multi([1, 5, 17, 40, 100, 250], [1, 5, 3, 40, 7, 64], hq=8, hkv=2, d=64))
+
+
+def _online():
+    check_online(16)
+
+
+def _merge():
+    for part in (16, 48, 512):
+        check_partials_merge(part)
 
 
 def _rounding():
@@ -73,6 +83,16 @@ MUTANTS = {
                             "*L_out = L - n + (j - qs[b]) + 1 + (j - qs[b] + 1 < n);", _multi),
     "multi_query_row_of_sequence": ("qrow = (int64_t)j * P->num_q_heads + h;",
                                     "qrow = (int64_t)b * P->num_q_heads + h;", _multi),
+    "online_carry_dropped": ("double l_new = l_old * carry + sum;", "double l_new = l_old + sum;",
+                             _online),
+    "online_output_not_rescaled": ("o[e] = o[e] * l_old * carry / l_new + num[e] / l_new;",
+                                   "o[e] = o[e] + num[e] / l_new;", _online),
+    "partition_end_off_by_one": ("t1 = (i + 1) * part < L ? (i + 1) * part : L;",
+                                 "t1 = (i + 1) * part < L ? (i + 1) * part - 1 : L;", _merge),
+    "partial_sum_of_scores": ("            l += p;\n", "            l += s[t];\n", _merge),
+    "merge_denominator_unweighted": ("den += w * ml[2 * i + 1];", "den += ml[2 * i + 1];", _merge),
+    "merge_weight_sign_flipped": ("double w = exp(ml[2 * i] - M);", "double w = exp(M - ml[2 * i]);",
+                                  _merge),
     "round_half_away": ("float r = nearbyintf(x / s);", "float r = roundf(x / s);", _rounding),
     "fp64_decision": ("float r = nearbyintf(x / s);",
                       "float r = (float)nearbyint((double)x / (double)s);", _fp32),
