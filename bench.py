@@ -549,6 +549,7 @@ def gpu_arm(args, rank, world, local_rank, dist):
     torch.cuda.synchronize(dev)
     unfused_ms = ev3[0][0].elapsed_time(ev3[-1][2]) / K3
     attn_only_ms = statistics.fmean(ev3[i][1].elapsed_time(ev3[i][2]) for i in range(K3))
+    append_only_ms = statistics.fmean(ev3[i][0].elapsed_time(ev3[i][1]) for i in range(K3))
     elapsed, agg_bytes_per_s = aggregate(total_ms / 1e3, nbytes["kv_logical"] * K, world, dist)
     value = agg_bytes_per_s / 1e9
     st, flags = pkv.get_status()
@@ -638,9 +639,11 @@ def gpu_arm(args, rank, world, local_rank, dist):
         "timing": f"value and ms_per_step: {GRAPH_STEPS} steps captured in one CUDA graph, replayed",
         "eager_us_per_step": round(eager_ms * 1e3, 2),
         "unfused": {"us_per_step": round(unfused_ms * 1e3, 2),
+                    "append_us": round(append_only_ms * 1e3, 2),
                     "attention_us": round(attn_only_ms * 1e3, 2),
                     "note": ("token slot mapping + reshape_and_cache, then paged_attention_multi" if multi
-                             else "slot mapping + reshape_and_cache + paged_attention_decode as three calls")},
+                             else "slot mapping + reshape_and_cache (append_us), then "
+                                  "paged_attention_decode (attention_us: decode + merge), as three calls")},
         "e2e": {"value": round(e2e_agg / 1e9, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5),
                 "note": "inputs of every step copied from pinned host memory and outputs read "
