@@ -472,19 +472,23 @@ def gpu_arm(args, rank, world, local_rank, dist):
     step_fn = g.multi_step if multi else (g.prefix_step if use_prefix else g.fused_step)
     stream = torch.cuda.current_stream(dev)
     nbytes = algorithmic_bytes(wl)
-    # token partition of the decode kernel (the multi-token path chooses its
-    # own, not exported: not reported there)
-    part = None if multi else pkv.partition_tokens(s.batch, s.num_kv_heads,
-                                                   g.max_seq_len - s.shared_prefix_tokens * use_prefix,
-                                                   s.block_size)
+    # token partition of the decode kernel, or of the multi-token call
+    if multi:
+        part = pkv.multi_partition_tokens(s.batch, wl.num_tokens, max(int(wl.query_lens.max()), 1),
+                                          s.num_q_heads, s.num_kv_heads, g.max_seq_len)
+    else:
+        part = pkv.partition_tokens(s.batch, s.num_kv_heads,
+                                    g.max_seq_len - s.shared_prefix_tokens * use_prefix, s.block_size)
     # decode (append fused) + merge, + the prefix kernel on the shared-prefix
-    # path; multi-token: slot mapping + append + merge + the column groups
-    # (sequences with few queries) and/or the tensor-core kernel (long ones)
+    # path; multi-token: slot mapping + append + the column groups (sequences
+    # with few queries) and/or the tensor-core kernel (long ones) + the merge
+    # when a sequence spans several partitions
     if multi:
         G = s.num_q_heads // s.num_kv_heads
         col_max = (8 // G) * 4 if G <= 8 else 0
-        launches_per_step = (3 + int(bool((wl.query_lens <= col_max).any()))
-                             + int(bool((wl.query_lens > col_max).any())))
+        launches_per_step = (2 + int(G <= 8)              # the column groups' launch
+                             + int(bool((wl.query_lens > col_max).any()))
+                             + int(g.max_seq_len > part))
     else:
         launches_per_step = 3 if use_prefix else 1 + (1 if g.max_seq_len > part else 0)
 

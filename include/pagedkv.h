@@ -501,6 +501,19 @@ const char *pagedkv_last_error(void);
 int pagedkv_partition_tokens(int batch, int num_kv_heads, int max_seq_len,
                              int block_size);
 
+/* Token partition size paged_attention_multi would use for this call on the
+ * current device (0 on error); arguments as for paged_attention_multi.  A
+ * power of two from 256 up to 8192 when every sequence's queries go to the
+ * decode kernel's column groups (max_query_len <= 4 * (8 / G)), up to 2048
+ * when the tensor-core kernel is in the call; the largest that still gives
+ * at least 8 CTAs per SM.  Sequences longer than one partition go through
+ * the merge kernel, which is launched only when max_seq_len exceeds it.
+ * PAGEDKV_PARTITION_TOKENS (a multiple of 256, within the same limits)
+ * overrides it. */
+int pagedkv_multi_partition_tokens(int batch, int num_tokens, int max_query_len,
+                                   int num_q_heads, int num_kv_heads,
+                                   int max_seq_len);
+
 #ifdef __cplusplus
 }
 #endif

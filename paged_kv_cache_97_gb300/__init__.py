@@ -57,6 +57,7 @@ SIGNATURES = {
     "pagedkv_get_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
     "pagedkv_last_error": (ctypes.c_char_p, []),
     "pagedkv_partition_tokens": (_I, [_I, _I, _I, _I]),
+    "pagedkv_multi_partition_tokens": (_I, [_I, _I, _I, _I, _I, _I]),
     "pagedkv_decode_step_prefix": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I,
                                         _I, _I, _I, _F, _I, _P, _I, _P, _SZ, _P]),
     "pagedkv_prefix_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
@@ -376,6 +377,13 @@ def workspace_bytes(batch, num_q_heads, head_dim, max_seq_len, block_size) -> in
 def partition_tokens(batch, num_kv_heads, max_seq_len, block_size) -> int:
     """Token partition size the decode kernel uses for this shape."""
     return load().pagedkv_partition_tokens(batch, num_kv_heads, max_seq_len, block_size)
+
+
+def multi_partition_tokens(batch, num_tokens, max_query_len, num_q_heads, num_kv_heads,
+                           max_seq_len) -> int:
+    """Token partition size paged_attention_multi uses for this call."""
+    return load().pagedkv_multi_partition_tokens(batch, num_tokens, max_query_len, num_q_heads,
+                                                 num_kv_heads, max_seq_len)
 
 
 def _check_decode(out, q, k_cache, v_cache, block_tables, seq_lens, k_scale, v_scale, workspace):

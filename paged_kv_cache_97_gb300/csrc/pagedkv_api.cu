@@ -316,12 +316,12 @@ kv_status launch_merge(const DecodeArgs& a, cudaStream_t stream) {
 // block and whose partials cost more to merge.  The environment variable
 // PAGEDKV_PARTITION_TOKENS (a multiple of 256, read on every call) overrides it.
 int choose_part_tokens(int batch, int num_kv_heads, int max_seq_len, int num_sms,
-                       bool split_longest) {
+                       bool split_longest, int max_tokens) {
   const char* s = getenv("PAGEDKV_PARTITION_TOKENS");
   const int env = s ? atoi(s) : 0;
-  if (env >= kMinPartTokens && env <= kMaxPartTokens && env % kMinPartTokens == 0) return env;
+  if (env >= kMinPartTokens && env <= max_tokens && env % kMinPartTokens == 0) return env;
   const int64_t target = 8LL * num_sms;
-  int pt = kMaxPartTokens;
+  int pt = max_tokens;
   while (pt > kMinPartTokens &&
          ((int64_t)batch * num_kv_heads * ((max_seq_len + pt - 1) / pt) < target ||
           (split_longest && 2 * pt > max_seq_len)))

@@ -37,6 +37,9 @@ constexpr int kMaxGroup = 8;
 // Token partitions of the split-K path: powers of two in [256, 2048].
 constexpr int kMinPartTokens = 256;
 constexpr int kMaxPartTokens = 2048;
+// Longest partition the decode kernel's column groups take (its block-id
+// table holds 512 blocks: 8192 tokens of 16-token blocks).
+constexpr int kMaxColumnPartTokens = 8192;
 
 // log2(e): scores are kept in the base-2 domain so exp() becomes exp2().
 constexpr float kLog2e = 1.4426950408889634f;
@@ -110,9 +113,10 @@ kv_status launch_multi_tc(const DecodeArgs& a, int ctas, cudaStream_t stream);
 kv_status launch_prefix_tc(const DecodeArgs& a, int ctas, cudaStream_t stream);
 
 // Token partition length for `work` independent (row group, KV head) units
-// over sequences of up to max_seq_len tokens (power of two in [256, 2048]).
-// With split_longest, also at most half of max_seq_len (one-token decode).
+// over sequences of up to max_seq_len tokens (power of two in [256,
+// max_tokens]).  With split_longest, also at most half of max_seq_len
+// (one-token decode).
 int choose_part_tokens(int work, int num_kv_heads, int max_seq_len, int num_sms,
-                       bool split_longest);
+                       bool split_longest, int max_tokens = kMaxPartTokens);
 
 }  // namespace pagedkv

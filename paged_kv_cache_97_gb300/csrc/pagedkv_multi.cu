@@ -181,6 +181,39 @@ size_t pagedkv_multi_workspace_bytes(int num_tokens, int num_q_heads, int head_d
   return multi_need(num_tokens, num_q_heads, head_dim, (max_seq_len + 255) / 256);
 }
 
+// Token partition of a multi-token call (the same choice for both kernels
+// of one call).  Column groups alone take partitions up to 8192 tokens:
+// their per-CTA start and the merge cost more than the tail of fewer, longer
+// CTAs (speculative verification, 64 sequences of 512..4096 tokens with 5
+// queries each: 512-token partitions 215.5 us per step, 1024 182.1, 2048
+// 166.1, one 8192-token partition 159.6).  With the tensor-core kernel in
+// the call, at most the 2048 tokens its block-id table holds.
+static int multi_part_tokens(int batch, int num_tokens, int max_query_len, int num_q_heads,
+                             int num_kv_heads, int max_seq_len, int num_sms) {
+  const int GQ = num_q_heads / num_kv_heads;
+  const int tpg = GQ <= kMaxGroup ? kMaxGroup / GQ : 0;
+  const int col_max_n = tpg * kMaxVGroups;
+  const int vgroups = tpg > 0 ? (min(max_query_len, col_max_n) + tpg - 1) / tpg : 0;
+  const bool column_path = tpg > 0;
+  const bool row_path = max_query_len > col_max_n;
+  const int64_t tiles = ((int64_t)num_tokens * GQ + 127) / 128 + batch;
+  return choose_part_tokens((column_path ? batch * vgroups : 0) + (row_path ? (int)tiles : 0),
+                            num_kv_heads, max_seq_len, num_sms, false,
+                            row_path ? kMaxPartTokens : kMaxColumnPartTokens);
+}
+
+int pagedkv_multi_partition_tokens(int batch, int num_tokens, int max_query_len, int num_q_heads,
+                                   int num_kv_heads, int max_seq_len) {
+  DeviceInfo di;
+  if (batch <= 0 || num_tokens <= 0 || max_query_len <= 0 || num_q_heads <= 0 ||
+      num_kv_heads <= 0 || num_q_heads % num_kv_heads || max_seq_len <= 0 ||
+      ((int64_t)num_tokens * (num_q_heads / num_kv_heads) + 127) / 128 + batch > 0x7fffffffLL ||
+      device_info(&di) != KV_OK)
+    return 0;
+  return multi_part_tokens(batch, num_tokens, max_query_len, num_q_heads, num_kv_heads,
+                           max_seq_len, di.num_sms);
+}
+
 kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
                                 const void* v_cache, const float* k_scale, const float* v_scale,
                                 const int32_t* block_tables, int max_blocks_per_seq,
@@ -252,8 +285,8 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
   a.num_blocks = num_blocks;
   a.block_size = block_size;
   a.max_seq_len = max_seq_len;
-  a.part_tokens = choose_part_tokens((column_path ? batch * vgroups : 0) + (row_path ? (int)tiles : 0),
-                                     num_kv_heads, max_seq_len, di.num_sms, false);
+  a.part_tokens = multi_part_tokens(batch, num_tokens, max_query_len, num_q_heads, num_kv_heads,
+                                    max_seq_len, di.num_sms);
   a.max_parts = (max_seq_len + a.part_tokens - 1) / a.part_tokens;
   if (a.max_parts > 65535) return fail(KV_ERR_INVALID_ARG, "%s: too many partitions", who);
   if (row_path && tiles * num_kv_heads * a.max_parts > 0x7fffffffLL)

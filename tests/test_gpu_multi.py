@@ -65,13 +65,16 @@ CASES = {
                                  seed=45),
     "col_fp8_g4": lambda: multi([20, 900, 1600], [8, 5, 1], hq=32, hkv=8, d=128, bs=16, kv="fp8",
                                 seed=46),
+    # column groups only, one sequence past 8192 tokens: two of the longest
+    # (8192-token) partitions and their merge
+    "col_long_g4": lambda: multi([9000, 300, 2], [5, 3, 1], hq=32, hkv=8, d=128, seed=49),
     # one query head, 43 tokens: with 3 partitions the (m, l) region holds 258
     # floats, so the acc region is 16-byte aligned only by its rounding
     "odd_rows_mha": lambda: multi([300, 700, 37], [41, 1, 1], hq=1, hkv=1, d=64, seed=48),
 }
 
 
-@pytest.mark.parametrize("part", ["", "256", "2048"])
+@pytest.mark.parametrize("part", ["", "256", "2048", "8192"])
 @pytest.mark.parametrize("case", sorted(CASES))
 def test_multi_matches_oracle(monkeypatch, case, part):
     if part:
@@ -197,3 +200,20 @@ def test_multi_softmax_scale_values(scale):
     err = np.abs(got - ref)
     assert (err <= 1e-2 + 2.0 ** -8 * np.abs(ref)).all(), (scale, err.max())
     assert err.mean() <= 1e-3, (scale, err.mean())
+
+
+def test_partition_choice_follows_the_kernels_in_the_call(monkeypatch):
+    """Column groups alone may take one partition of up to 8192 tokens (no
+    merge launch); with a long query in the call the tensor-core kernel caps
+    it at 2048; the override is honoured within those limits only."""
+    monkeypatch.delenv("PAGEDKV_PARTITION_TOKENS", raising=False)
+    # 64 sequences x 5 draft tokens, 32/8 heads, up to 4096 tokens: column groups only
+    assert pkv.multi_partition_tokens(64, 320, 5, 32, 8, 4096) == 8192
+    # the same batch with one 512-token prefill chunk: the tensor-core kernel joins
+    assert pkv.multi_partition_tokens(64, 575, 512, 32, 8, 4096) == 2048
+    monkeypatch.setenv("PAGEDKV_PARTITION_TOKENS", "4096")
+    assert pkv.multi_partition_tokens(64, 320, 5, 32, 8, 4096) == 4096
+    assert pkv.multi_partition_tokens(64, 575, 512, 32, 8, 4096) == 2048    # beyond its limit: ignored
+    monkeypatch.setenv("PAGEDKV_PARTITION_TOKENS", "512")
+    assert pkv.multi_partition_tokens(64, 575, 512, 32, 8, 4096) == 512
+    assert pkv.multi_partition_tokens(0, 0, 5, 32, 8, 4096) == 0             # nothing to size
