@@ -494,7 +494,9 @@ kv_status pagedkv_get_status(void *stream, unsigned int *device_flags);
 const char *pagedkv_last_error(void);
 
 /* Token partition size paged_attention_decode would use for this shape on
- * the current device (0 on error): the largest power of two in [256, 2048]
+ * the current device (0 on error).  The partitions split each sequence's
+ * tokens among CTAs, the parallelism along the sequence of “LLM 推理优化技术
+ * 全景”, Flash Attention v2 的改进.  The largest power of two in [256, 2048]
  * that still gives at least 8 CTAs per SM.  Sequences longer than one
  * partition go through the merge kernel.  The environment variable
  * PAGEDKV_PARTITION_TOKENS (a multiple of 256) overrides it. */
@@ -502,7 +504,9 @@ int pagedkv_partition_tokens(int batch, int num_kv_heads, int max_seq_len,
                              int block_size);
 
 /* Token partition size paged_attention_multi would use for this call on the
- * current device (0 on error); arguments as for paged_attention_multi.  A
+ * current device (0 on error); arguments as for paged_attention_multi.  The
+ * same split along the sequence (“LLM 推理优化技术全景”, Flash Attention v2
+ * 的改进) as for paged_attention_decode.  A
  * power of two from 256 up to 8192 when every sequence's queries go to the
  * decode kernel's column groups (max_query_len <= 4 * (8 / G)), up to 2048
  * when the tensor-core kernel is in the call; the largest that still gives
