@@ -497,7 +497,8 @@ const char *pagedkv_last_error(void);
  * the current device (0 on error).  The partitions split each sequence's
  * tokens among CTAs, the parallelism along the sequence of “LLM 推理优化技术
  * 全景”, Flash Attention v2 的改进.  The largest power of two in [256, 2048]
- * that still gives at least 8 CTAs per SM.  Sequences longer than one
+ * that still gives at least 8 CTAs per SM and is at most half of max_seq_len
+ * (256 when nothing larger qualifies).  Sequences longer than one
  * partition go through the merge kernel.  The environment variable
  * PAGEDKV_PARTITION_TOKENS (a multiple of 256) overrides it. */
 int pagedkv_partition_tokens(int batch, int num_kv_heads, int max_seq_len,
