@@ -437,8 +437,8 @@ int pagedkv_partition_tokens(int batch, int num_kv_heads, int max_seq_len, int b
 // prefix tokens and at most kMaxPartTokens.  The product runs beside the
 // decode kernel and only has to finish before it, so rows get as few partials
 // as that allows: ceil(T / kMaxPartTokens) for T prefix tokens (fewer partials
-// to write and merge; workload 4: one 896-token partial 119.3 us per step,
-// two 122.0, three 123.9).  pagedkv_prefix_workspace_bytes sizes for this.
+// to write and merge; 256 sequences behind an 800-token shared prefix: one
+// 896-token partial 119.3 us per step, two 122.0, three 123.9).  pagedkv_prefix_workspace_bytes sizes for this.
 static int prefix_chunk_count(int prefix_tokens) {
   return (prefix_tokens + kMaxPartTokens - 1) / kMaxPartTokens;
 }

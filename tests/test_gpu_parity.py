@@ -55,7 +55,7 @@ def small(lens, hq=8, hkv=2, d=64, bs=16, kv="bf16", nb=None, seed=7, prefix=0, 
 
 
 CASES = {
-    "cfg1": lambda: workloads.make(1),
+    "tiny_b4_g4_d64": lambda: workloads.make(1),
     "ragged_g4_d128": lambda: small([1, 2, 15, 16, 17, 255, 256, 257, 1000, 3001], hq=32, hkv=8, d=128, seed=1),
     "g8_int8_bs32": lambda: small([1, 31, 32, 33, 511, 700, 2049], hq=64, hkv=8, d=128, bs=32, kv="int8", seed=2),
     "g1_mha_d64": lambda: small([5, 77, 300, 1290], hq=4, hkv=4, d=64, seed=3),
@@ -73,7 +73,7 @@ CASES = {
 # Slot mapping and append: bit-exact
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("case", ["cfg1", "g8_int8_bs32", "int8_d64_bs16", "shared_prefix", "g2_bs32_d64",
+@pytest.mark.parametrize("case", ["tiny_b4_g4_d64", "g8_int8_bs32", "int8_d64_bs16", "shared_prefix", "g2_bs32_d64",
                                   "g8_fp8_bs32", "fp8_d64_bs16"])
 def test_append_and_slots_bit_exact(case):
     wl = CASES[case]()
@@ -205,7 +205,7 @@ def test_odd_partial_count_keeps_the_workspace_aligned(monkeypatch):
     assert_close(got, ref, "bf16", "odd partial count")
 
 
-@pytest.mark.parametrize("case", ["cfg1", "ragged_g4_d128", "g8_int8_bs32", "shared_prefix", "int8_d64_bs16",
+@pytest.mark.parametrize("case", ["tiny_b4_g4_d64", "ragged_g4_d128", "g8_int8_bs32", "shared_prefix", "int8_d64_bs16",
                                   "g8_fp8_bs32"])
 def test_fused_step_equals_separate_calls(case):
     """pagedkv_decode_step (append inside the attention kernel) leaves the same
@@ -222,7 +222,7 @@ def test_fused_step_equals_separate_calls(case):
     np.testing.assert_array_equal(out_b, out_a)
 
 
-@pytest.mark.parametrize("case", ["cfg1", "ragged_g4_d128", "g8_int8_bs32", "fp8_d64_bs16"])
+@pytest.mark.parametrize("case", ["tiny_b4_g4_d64", "ragged_g4_d128", "g8_int8_bs32", "fp8_d64_bs16"])
 def test_decode_step_replays_from_a_cuda_graph(case):
     """The fused step captured once in a CUDA graph (decode + PDL merge) and
     replayed gives the eager step's output bit for bit; replaying re-appends
@@ -331,7 +331,7 @@ def test_full_size_shared_prefix_workload_sampled_rows():
     ref, rc = oracle.paged_attention(wl.q, kc, vc, wl.block_tables, wl.seq_lens, wl.spec.scale,
                                      rows=rows, threads=os.cpu_count())
     assert rc == 0
-    assert_close(got[rows[:, 0], rows[:, 1]], ref, "bf16", "config 4, shared-prefix path")
+    assert_close(got[rows[:, 0], rows[:, 1]], ref, "bf16", "256 sequences behind an 800-token prefix, shared-prefix path")
 
 
 # ---------------------------------------------------------------------------
