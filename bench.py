@@ -7,14 +7,19 @@ the pool, and the paged attention (the per-partition decode kernel, with the
 append fused in, plus the log-sum-exp merge of sequences that span several
 partitions).  The same step as three calls (slot mapping, reshape_and_cache,
 paged_attention_decode) is timed beside it.  The default workload is the
-Llama-3.1-8B-like decode layer (B 64, 32/8 heads, d 128, 16-token blocks,
-lengths U{512..4096}).
+largest single-GPU one: long-context split-K decode (B 8, 32/8 heads, d 128,
+16-token blocks, lengths U{32768..131072}, 2.4 GB of KV per step).  Every
+other decode workload (tiny, Llama-3.1-8B-like, shared prefix, Llama-2-70B-like
+INT8) is measured the same way under ``rows.configs``, and the FP8,
+multi-token and copy-on-write rows beside them.
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
 the same workload instead (the reference arm: a plain fp64 program, not a
 target).  Timing: CUDA events on the launching stream, W warm-up steps, K
 timed steps, barrier + synchronize on both sides, max over ranks.  The KV
-read per step (~600 MB) is larger than the 129 MB L2, so no flush is needed.
+read per step of every bandwidth-bound workload is larger than the 129 MB L2,
+so no flush is needed (the tiny workload fits in L2 and is reported as a
+launch-latency figure).
 """
 from __future__ import annotations
 
@@ -38,12 +43,19 @@ import workloads  # noqa: E402
 
 METRIC = "paged decode attention: KV-read GB/s & % of GB300 HBM peak; µs per decode step"
 UNIT = "GB/s"
-DEFAULT_CONFIG = 2
+DEFAULT_CONFIG = 3
+ROW_CONFIGS = (1, 2, 3, 4, 5)                       # the decode workloads under rows.configs
+STEADY_S = 0.5                                        # length of the steady timed region
 FALLBACK_HBM_GBS = 6800.0
 GRAPH_STEPS = 20
 L2_BYTES = 129e6                                         # GB300 L2
-DECODE_SOURCE = os.path.join(ROOT, "paged_kv_cache_97_gb300", "csrc", "pagedkv_decode.cu")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
+CSRC = os.path.join(ROOT, "paged_kv_cache_97_gb300", "csrc")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+# sources whose hash a stored DRAM-traffic capture of each kernel must match
+KERNEL_SOURCES = {
+    "decode_kernel": ("pagedkv_decode.cu", "pagedkv_device.cuh", "pagedkv_common.cuh"),
+    "multi_tc_kernel": ("pagedkv_multi_tc.cu", "pagedkv_device.cuh", "pagedkv_common.cuh"),
+}
 
 
 def workload_config(wl, nbytes) -> dict:
@@ -172,11 +184,9 @@ def aggregate(elapsed_s: float, units_per_rank: float, world: int, dist=None):
 
 def oracle_pools(wl):
     """The oracle's own pools for the whole batch (setup, not timed)."""
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
     import oracle
-    from oracle_helpers import oracle_pool
     oracle.build()
-    return oracle_pool(wl)
+    return oracle.workload_pools(wl)
 
 
 def oracle_time(wl, pools, seqs, threads):
@@ -219,25 +229,37 @@ def oracle_sample(wl, threads, target_s=10.0, max_s=30.0, pools=None):
 
 
 # ---------------------------------------------------------------------------
-# GPU arm
+# GPU arm: helpers
 # ---------------------------------------------------------------------------
 
-def source_hash(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def source_hash(files):
+    h = hashlib.sha256()
+    for name in files:
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
-def stored_traffic(workload_name):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken
-    on the current decode kernel source and this workload; else None."""
+def kernel_hash(kernel):
+    return source_hash(KERNEL_SOURCES[kernel])
+
+
+def stored_traffic(workload_name, kernel="decode_kernel"):
+    """DRAM bytes per launch of `kernel` on this workload from a committed
+    ncu capture (read + write; scaled to a full launch where the capture ran
+    a smaller case), if it was taken on the kernel's current sources; else
+    None."""
     try:
         with open(TRAFFIC_FILE) as f:
-            t = json.load(f)
-    except (OSError, ValueError):
+            captures = json.load(f)["captures"]
+    except (OSError, ValueError, KeyError):
         return None
-    if t.get("source_sha256_16") != source_hash(DECODE_SOURCE) or t.get("workload") != workload_name:
-        return None
-    return t.get("dram_bytes_per_launch")
+    want = kernel_hash(kernel)
+    for t in captures:
+        if t.get("workload") == workload_name and t.get("kernel") == kernel and \
+                t.get("source_sha256_16") == want:
+            return t.get("dram_bytes_per_launch")
+    return None
 
 
 def measured_peak_gbs():
@@ -248,6 +270,167 @@ def measured_peak_gbs():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_peak_tflops():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return 1900.0, "fallback"
+
+
+class StepPlan:
+    """How one workload's step runs through the public API: the call, a
+    description of its kernels, the token partition and the launches of
+    this library's kernels per step."""
+
+    def __init__(self, wl, g, pkv, no_shared_prefix=False):
+        s = wl.spec
+        self.multi = bool((wl.query_lens != 1).any())      # several query tokens per sequence
+        self.prefix = s.shared_prefix_tokens > 0 and not no_shared_prefix and not self.multi
+        if self.multi:
+            self.fn = g.multi_step
+            self.part = pkv.multi_partition_tokens(s.batch, wl.num_tokens,
+                                                   max(int(wl.query_lens.max()), 1),
+                                                   s.num_q_heads, s.num_kv_heads, g.max_seq_len)
+            G = s.num_q_heads // s.num_kv_heads
+            col_max = (8 // G) * 4 if G <= 8 else 0
+            # token slot mapping + append + the column groups (few-query
+            # sequences) and/or the tensor-core kernel (long ones) + the merge
+            # when a sequence spans several partitions
+            self.launches = (2 + int(bool((wl.query_lens <= col_max).any()))
+                             + int(bool((wl.query_lens > col_max).any()))
+                             + int(g.max_seq_len > self.part))
+            self.kernels = ("token slot mapping + append + decode_kernel column groups / "
+                            "multi_tc_kernel (+ multi_merge_kernel), paged_attention_multi")
+        else:
+            skip = s.shared_prefix_tokens if self.prefix else 0
+            self.fn = g.prefix_step if self.prefix else g.fused_step
+            self.part = pkv.partition_tokens(s.batch, s.num_kv_heads, g.max_seq_len - skip,
+                                             s.block_size)
+            if self.prefix:
+                self.launches = 3
+                self.kernels = ("multi_tc_kernel (shared-prefix mode) + decode_kernel (append "
+                                "fused) + merge_kernel, one pagedkv_decode_step_prefix")
+            else:
+                self.launches = 1 + int(g.max_seq_len > self.part)
+                self.kernels = "decode_kernel (append fused) + merge_kernel, one pagedkv_decode_step"
+
+
+def capture(step_fn, dev, warm=5):
+    """GRAPH_STEPS consecutive steps captured once in a CUDA graph (the GPU
+    work of the steps without Python's per-call overhead or a gap between
+    launches), after `warm` eager steps, then replayed three times."""
+    import torch
+    for _ in range(warm):
+        step_fn()
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(GRAPH_STEPS):
+            step_fn()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    return graph
+
+
+def time_replays(graph, stream, dev, replays):
+    """Per-step ms of each of `replays` graph replays (CUDA events on the
+    launching stream) and the ms from the first event to the last."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(replays)]
+    torch.cuda.synchronize(dev)
+    for a, b in ev:
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    return [a.elapsed_time(b) / GRAPH_STEPS for a, b in ev], ev[0][0].elapsed_time(ev[-1][1])
+
+
+def steady_region(graph, stream, dev, seconds=STEADY_S):
+    """Replays for at least `seconds` with clocks sampled throughout: the
+    spread of the per-replay step time and the clocks under load."""
+    import torch
+    probe, _ = time_replays(graph, stream, dev, 3)
+    n = max(10, int(math.ceil(seconds * 1e3 / (statistics.fmean(probe) * GRAPH_STEPS))))
+    sampler = ClockSampler(str(torch.cuda.get_device_properties(dev).uuid))
+    with sampler:
+        ms, total = time_replays(graph, stream, dev, n)
+    us = sorted(x * 1e3 for x in ms)
+    q = lambda f: us[min(len(us) - 1, int(f * len(us)))]  # noqa: E731
+    return {"seconds": round(total / 1e3, 3), "replays": n, "steps": n * GRAPH_STEPS,
+            "us_per_step": round(statistics.fmean(us), 2), "us_per_step_p10": round(q(0.1), 2),
+            "us_per_step_p50": round(q(0.5), 2), "us_per_step_p90": round(q(0.9), 2),
+            "spread_p90_p10": round((q(0.9) - q(0.1)) / q(0.5), 4), "clocks": sampler.summary()}
+
+
+def roofline_of(wl, plan, us, peak, peak_kind):
+    """Roofline object of one step: algorithmic bytes (SURVEY's per-token
+    figure x the tokens one step attends, plus q/out, tables and the append)
+    over the measured step time, against the measured copy peak."""
+    nbytes = algorithmic_bytes(wl)
+    achieved = nbytes["step"] / us / 1e3
+    traffic = stored_traffic(wl.spec.name, "decode_kernel")
+    return {"bound": "hbm", "kernel": plan.kernels, "achieved": round(achieved, 1), "peak": peak,
+            "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+            "algorithmic_bytes_per_launch": nbytes["step"], "us_per_launch": round(us, 2),
+            "traffic": traffic,
+            "traffic_over_algorithmic": round(traffic / nbytes["step"], 4) if traffic else None}
+
+
+def check_status(pkv):
+    st, flags = pkv.get_status()
+    assert st == 0 and flags == 0, f"device status 0x{flags:x}"
+
+
+def eager_us(step_fn, stream, dev, n=50):
+    """Per-step device time of `n` steps called from Python one by one."""
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(n):
+        step_fn()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / n * 1e3
+
+
+def measure_config(config, pkv, dev, stream, peak, peak_kind, replays=40):
+    """One decode workload's step (the fused decode step; the shared-prefix
+    step where the workload has a shared prefix), timed like the headline:
+    GRAPH_STEPS steps captured in one CUDA graph, replayed."""
+    import torch
+    from paged_kv_cache_97_gb300.batch import DecodeBatch
+    wl = workloads.make(config)
+    g = DecodeBatch(wl, dev=dev)
+    plan = StepPlan(wl, g, pkv)
+    graph = capture(plan.fn, dev)
+    ms, _ = time_replays(graph, stream, dev, replays)
+    check_status(pkv)
+    us = statistics.fmean(ms) * 1e3
+    nbytes = algorithmic_bytes(wl)
+    row = {"workload": wl.spec.name, "kv_dtype": wl.spec.kv_dtype,
+           "us_per_step": round(us, 2),
+           "kv_read_gbs": round(nbytes["kv_logical"] / us / 1e3, 1),
+           "unique_kv_gbs": round(nbytes["kv_unique"] / us / 1e3, 1),
+           "partition_tokens": plan.part, "launches_per_step": plan.launches,
+           "eager_us_per_step": round(eager_us(plan.fn, stream, dev), 2),
+           "roofline": roofline_of(wl, plan, us, peak, peak_kind)}
+    if nbytes["kv_logical"] <= L2_BYTES:
+        row["note"] = ("launch-bound: the step reads %.2f MB of KV, which stays in L2; one "
+                       "launch of a few microseconds, so no bandwidth fraction is reachable"
+                       % (nbytes["kv_logical"] / 1e6))
+    if plan.prefix:
+        row["note"] = ("shared prefix counted once in the algorithmic bytes (read from HBM "
+                       "once, then L2); kv_read_gbs counts it per sequence")
+    del graph, g
+    torch.cuda.empty_cache()
+    return row
+
+
 # ---------------------------------------------------------------------------
 # The rows beyond the decode step: copy-on-write
 # ---------------------------------------------------------------------------
@@ -256,7 +439,7 @@ def measure_cow(pkv, dev, stream, peak):
     """Copy-on-write (block copy + beam-search decode steps), timed with CUDA
     events on the launching stream."""
     import torch
-    from gpu_helpers import to_dev_bf16
+    from paged_kv_cache_97_gb300.batch import to_dev_bf16
 
     # (1) pagedkv_copy_blocks: 2048 block pairs of the 8B-like geometry
     # (16 x 8 x 128 bf16 = 32 KB per block and pool); two disjoint pair sets
@@ -344,8 +527,7 @@ def measure_cow(pkv, dev, stream, peak):
     torch.cuda.synchronize(dev)
     wall_us = (time.perf_counter() - t0) / w.steps * 1e6
     gpu_us = e0.elapsed_time(e1) / w.steps * 1e3
-    st, flags = pkv.get_status()
-    assert st == 0 and flags == 0, f"device status 0x{flags:x}"
+    check_status(pkv)
     used, _ = pool.stats()
     unshared = sum((int(L) + w.block_size - 1) // w.block_size for L in w.seq_lens_at(w.steps - 1))
     beam_row = {"workload": f"beam search, 16 prompts U{{512..4096}} x 4 beams, 32/8 heads, d 128, "
@@ -357,41 +539,9 @@ def measure_cow(pkv, dev, stream, peak):
                 "memory_saved": round(1 - used / unshared, 4),
                 "note": "per step: host copy-on-write bookkeeping, table/length upload, block "
                         "copies, fused decode step; synchronised once per step for the host tables"}
+    del kc, vc
+    torch.cuda.empty_cache()
     return {"copy_blocks": copy_row, "beam_search": beam_row}
-
-
-def measure_config_step(config, pkv, dev, stream, peak, replays=40):
-    """One workload's fused decode step (pagedkv_decode_step), timed like the
-    headline: GRAPH_STEPS steps captured in one CUDA graph, replayed."""
-    import torch
-    from gpu_helpers import GpuStep
-    wl = workloads.make(config)
-    g = GpuStep(wl, dev=dev)
-    for _ in range(5):
-        g.fused_step()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        for _ in range(GRAPH_STEPS):
-            g.fused_step()
-    for _ in range(3):
-        graph.replay()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * replays)]
-    torch.cuda.synchronize(dev)
-    for i in range(replays):
-        ev[2 * i].record(stream)
-        graph.replay()
-        ev[2 * i + 1].record(stream)
-    torch.cuda.synchronize(dev)
-    st, flags = pkv.get_status()
-    assert st == 0 and flags == 0, f"device status 0x{flags:x}"
-    us = statistics.fmean(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(replays)) * 1e3 / GRAPH_STEPS
-    nbytes = algorithmic_bytes(wl)
-    achieved = nbytes["step"] / us / 1e3
-    return {"workload": wl.spec.name, "us_per_step": round(us, 2),
-            "kv_read_gbs": round(nbytes["kv_logical"] / us / 1e3, 1),
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4),
-                         "algorithmic_bytes_per_step": nbytes["step"]}}
 
 
 def multi_flops(wl) -> int:
@@ -406,104 +556,74 @@ def multi_flops(wl) -> int:
     return 4 * s.head_dim * s.num_q_heads * total
 
 
+def multi_step_bytes(wl) -> int:
+    s = wl.spec
+    T = wl.num_tokens
+    return (wl.kv_bytes_logical() + 2 * T * s.num_q_heads * s.head_dim * 2
+            + T * s.num_kv_heads * s.head_dim * 2 * 2 * 2
+            + int(((wl.seq_lens + s.block_size - 1) // s.block_size).sum()) * 4)
+
+
 def measure_multi(config, pkv, dev, stream, peak, replays=40):
     """A multi-token workload's step (append of every query token through
     the general slot mapping + paged_attention_multi), timed like the
     headline: GRAPH_STEPS steps captured in one CUDA graph, replayed."""
     import torch
-    from gpu_helpers import GpuStep
+    from paged_kv_cache_97_gb300.batch import DecodeBatch
     wl = workloads.make(config)
-    g = GpuStep(wl, dev=dev)
-    for _ in range(5):
-        g.multi_step()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        for _ in range(GRAPH_STEPS):
-            g.multi_step()
-    for _ in range(3):
-        graph.replay()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * replays)]
-    torch.cuda.synchronize(dev)
-    for i in range(replays):
-        ev[2 * i].record(stream)
-        graph.replay()
-        ev[2 * i + 1].record(stream)
-    torch.cuda.synchronize(dev)
-    st, flags = pkv.get_status()
-    assert st == 0 and flags == 0, f"device status 0x{flags:x}"
-    us = statistics.fmean(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(replays)) * 1e3 / GRAPH_STEPS
+    g = DecodeBatch(wl, dev=dev)
+    plan = StepPlan(wl, g, pkv)
+    graph = capture(plan.fn, dev)
+    ms, _ = time_replays(graph, stream, dev, replays)
+    check_status(pkv)
+    us = statistics.fmean(ms) * 1e3
     s = wl.spec
-    T = wl.num_tokens
-    kv = wl.kv_bytes_logical()
-    step_bytes = (kv + 2 * T * s.num_q_heads * s.head_dim * 2 + T * s.num_kv_heads * s.head_dim * 2 * 2 * 2
-                  + int(((wl.seq_lens + s.block_size - 1) // s.block_size).sum()) * 4)
+    step_bytes = multi_step_bytes(wl)
     fl = multi_flops(wl)
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            tpeak = float(json.load(f)["bf16_tflops"])
-    except (OSError, ValueError, KeyError):
-        tpeak = 1900.0
-    return {"workload": s.name, "query_tokens": T, "us_per_step": round(us, 2),
-            "kv_read_gbs": round(kv / us / 1e3, 1),
-            "roofline": {"bound": "hbm", "achieved": round(step_bytes / us / 1e3, 1), "peak": peak,
+    tpeak, _ = measured_peak_tflops()
+    del graph, g
+    torch.cuda.empty_cache()
+    return {"workload": s.name, "kv_dtype": s.kv_dtype, "query_tokens": wl.num_tokens,
+            "us_per_step": round(us, 2),
+            "kv_read_gbs": round(wl.kv_bytes_logical() / us / 1e3, 1),
+            "partition_tokens": plan.part, "launches_per_step": plan.launches,
+            "roofline": {"bound": "hbm", "kernel": plan.kernels,
+                         "achieved": round(step_bytes / us / 1e3, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(step_bytes / us / 1e3 / peak, 4),
-                         "algorithmic_bytes_per_step": step_bytes},
+                         "algorithmic_bytes_per_launch": step_bytes},
             "tensor": {"achieved_tflops": round(fl / us / 1e6, 2), "peak_tflops": tpeak,
                        "frac": round(fl / us / 1e6 / tpeak, 4), "flops_per_step": fl,
                        "note": "long queries on tcgen05 (TMEM accumulators), few on mma.sync "
                                "m16n8k16; peak = measured cuBLAS bf16 (burst)"}}
 
 
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
 def gpu_arm(args, rank, world, local_rank, dist):
     import torch
 
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
     import paged_kv_cache_97_gb300 as pkv
-    from gpu_helpers import GpuStep
+    from paged_kv_cache_97_gb300.batch import DecodeBatch
     pkv.load()
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     wl = workloads.make(args.config)
-    g = GpuStep(wl, dev=dev)
+    g = DecodeBatch(wl, dev=dev)
     s = wl.spec
-    multi = bool((wl.query_lens != 1).any())             # several query tokens per sequence
-    use_prefix = s.shared_prefix_tokens > 0 and not args.no_shared_prefix and not multi
-    step_fn = g.multi_step if multi else (g.prefix_step if use_prefix else g.fused_step)
+    plan = StepPlan(wl, g, pkv, no_shared_prefix=args.no_shared_prefix)
+    multi, step_fn = plan.multi, plan.fn
     stream = torch.cuda.current_stream(dev)
     nbytes = algorithmic_bytes(wl)
-    # token partition of the decode kernel, or of the multi-token call
-    if multi:
-        part = pkv.multi_partition_tokens(s.batch, wl.num_tokens, max(int(wl.query_lens.max()), 1),
-                                          s.num_q_heads, s.num_kv_heads, g.max_seq_len)
-    else:
-        part = pkv.partition_tokens(s.batch, s.num_kv_heads,
-                                    g.max_seq_len - s.shared_prefix_tokens * use_prefix, s.block_size)
-    # decode (append fused) + merge, + the prefix kernel on the shared-prefix
-    # path; multi-token: slot mapping + append + the column groups (sequences
-    # with few queries) and/or the tensor-core kernel (long ones) + the merge
-    # when a sequence spans several partitions
-    if multi:
-        G = s.num_q_heads // s.num_kv_heads
-        col_max = (8 // G) * 4 if G <= 8 else 0
-        launches_per_step = (2 + int(G <= 8)              # the column groups' launch
-                             + int(bool((wl.query_lens > col_max).any()))
-                             + int(g.max_seq_len > part))
-    else:
-        launches_per_step = 3 if use_prefix else 1 + (1 if g.max_seq_len > part else 0)
+    peak, peak_kind = measured_peak_gbs()
 
     for _ in range(args.warmup):
         step_fn()
         if not multi:
             g.step()
-    torch.cuda.synchronize(dev)
-    # GRAPH_STEPS consecutive steps captured once in a CUDA graph (each a
-    # decode + merge pair), the graph replayed: the GPU work of the steps
-    # without Python's per-call overhead or a gap between graph launches.
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        for _ in range(GRAPH_STEPS):
-            step_fn()
+    graph = capture(step_fn, dev, warm=args.warmup)
     for _ in range(args.warmup):
         graph.replay()
     torch.cuda.synchronize(dev)
@@ -515,7 +635,7 @@ def gpu_arm(args, rank, world, local_rank, dist):
     R = max(1, K // GRAPH_STEPS)                        # graph replays in the timed region
     K = R * GRAPH_STEPS
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(R)]
-    sampler = ClockSampler(torch.cuda.get_device_properties(dev).uuid.__str__())
+    sampler = ClockSampler(str(torch.cuda.get_device_properties(dev).uuid))
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -530,18 +650,16 @@ def gpu_arm(args, rank, world, local_rank, dist):
     total_ms = ev[0][0].elapsed_time(ev[-1][1])
     step_ms = [ev[i][0].elapsed_time(ev[i][1]) / GRAPH_STEPS for i in range(R)]
     ms_step = total_ms / K
+    elapsed, agg_bytes_per_s = aggregate(total_ms / 1e3, nbytes["kv_logical"] * K, world, dist)
+    value = agg_bytes_per_s / 1e9
+    # a longer steady region of the same replays: run-to-run spread and clocks
+    steady = steady_region(graph, stream, dev)
+    check_status(pkv)
 
     # the same step through eager calls: the fused step, and the three calls
     # (slot mapping, append, attention)
     K3 = max(K // 4, 10)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize(dev)
-    e0.record(stream)
-    for i in range(K3):
-        step_fn()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    eager_ms = e0.elapsed_time(e1) / K3
+    eager_ms = eager_us(step_fn, stream, dev, K3) / 1e3
     ev3 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K3)]
     torch.cuda.synchronize(dev)
     for i in range(K3):
@@ -554,8 +672,6 @@ def gpu_arm(args, rank, world, local_rank, dist):
     unfused_ms = ev3[0][0].elapsed_time(ev3[-1][2]) / K3
     attn_only_ms = statistics.fmean(ev3[i][1].elapsed_time(ev3[i][2]) for i in range(K3))
     append_only_ms = statistics.fmean(ev3[i][0].elapsed_time(ev3[i][1]) for i in range(K3))
-    elapsed, agg_bytes_per_s = aggregate(total_ms / 1e3, nbytes["kv_logical"] * K, world, dist)
-    value = agg_bytes_per_s / 1e9
     st, flags = pkv.get_status()
     assert st == 0, f"device status 0x{flags:x}"
 
@@ -615,10 +731,12 @@ def gpu_arm(args, rank, world, local_rank, dist):
     _, e2e_agg = aggregate(e2e_ms / 1e3, nbytes["kv_logical"], world, dist)
     assert np.isfinite(h_out[(K2 - 1) % 2].float().numpy()).all()
 
-    peak, peak_kind = measured_peak_gbs()
     step_mean_ms = statistics.fmean(step_ms)
-    achieved = nbytes["step"] / (step_mean_ms / 1e3) / 1e9
-    traffic = stored_traffic(s.name)
+    roofline = roofline_of(wl, plan, step_mean_ms * 1e3, peak, peak_kind)
+    if plan.multi:
+        roofline["algorithmic_bytes_per_launch"] = multi_step_bytes(wl)
+        roofline["achieved"] = round(multi_step_bytes(wl) / (step_mean_ms * 1e3) / 1e3, 1)
+        roofline["frac"] = round(roofline["achieved"] / peak, 4)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
@@ -627,20 +745,11 @@ def gpu_arm(args, rank, world, local_rank, dist):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if s.kv_dtype == "bf16" else f"{s.kv_dtype} KV, bf16 q/out, fp32 accumulate",
         "data": "synthetic",
-        "config": dict(workload_config(wl, nbytes), partition_tokens=part,
-                       parallelism=f"replicas x{world}"),
-        "roofline": {"bound": "hbm",
-                     "kernel": ("token slot mapping + append + decode_kernel column groups / "
-                                "multi_tc_kernel (+ multi_merge_kernel), "
-                                "paged_attention_multi" if multi else
-                                "multi_tc_kernel (shared-prefix mode) + decode_kernel (append fused) + merge_kernel, one "
-                                "pagedkv_decode_step_prefix" if use_prefix else
-                                "decode_kernel (append fused) + merge_kernel, one pagedkv_decode_step"),
-                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                     "algorithmic_bytes_per_launch": nbytes["step"],
-                     "us_per_launch": round(step_mean_ms * 1e3, 2), "traffic": traffic},
+        "config": dict(workload_config(wl, nbytes), parallelism=f"replicas x{world}"),
+        "partition_tokens": plan.part,
+        "roofline": roofline,
         "timing": f"value and ms_per_step: {GRAPH_STEPS} steps captured in one CUDA graph, replayed",
+        "steady": steady,
         "eager_us_per_step": round(eager_ms * 1e3, 2),
         "unfused": {"us_per_step": round(unfused_ms * 1e3, 2),
                     "append_us": round(append_only_ms * 1e3, 2),
@@ -653,31 +762,45 @@ def gpu_arm(args, rank, world, local_rank, dist):
                 "note": "inputs of every step copied from pinned host memory and outputs read "
                         "back inside the timed region; two buffer sets alternate so step i's "
                         "copies overlap step i-1's compute"},
-        "gpu_launches": launches_per_step * K,
+        "gpu_launches": plan.launches * K,
         "clocks": sampler.summary(),
     }
+    del graph, g, sets
+    torch.cuda.empty_cache()
     if not args.no_rows:
-        line["rows"] = {"cow": measure_cow(pkv, dev, stream, peak),
-                        "fp8_kv": measure_config_step(6, pkv, dev, stream, peak),
+        configs = {}
+        for c in ROW_CONFIGS:
+            if c == args.config:
+                configs[str(c)] = {"workload": s.name, "kv_dtype": s.kv_dtype,
+                                   "us_per_step": line["us_per_step"],
+                                   "kv_read_gbs": round(nbytes["kv_logical"] / (ms_step * 1e3) / 1e3, 1),
+                                   "partition_tokens": plan.part, "launches_per_step": plan.launches,
+                                   "eager_us_per_step": line["eager_us_per_step"],
+                                   "roofline": roofline, "note": "the headline workload (above)"}
+            else:
+                configs[str(c)] = measure_config(c, pkv, dev, stream, peak, peak_kind)
+        line["rows"] = {"configs": configs,
+                        "fp8_kv": measure_config(6, pkv, dev, stream, peak, peak_kind),
                         "multi_token": {"speculative_verification": measure_multi(7, pkv, dev, stream, peak),
-                                        "decode_maximal_batch": measure_multi(8, pkv, dev, stream, peak)}}
+                                        "decode_maximal_batch": measure_multi(8, pkv, dev, stream, peak)},
+                        "cow": measure_cow(pkv, dev, stream, peak)}
     return line, wl
 
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=sorted(workloads.CONFIGS),
-                    help="workload (default 2: the Llama-3.1-8B-like decode layer)")
+                    help="workload (default 3: long-context split-K decode, the largest single-GPU one)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-shared-prefix", action="store_true",
                     help="for workloads with a shared prefix, time the plain step instead of "
                          "pagedkv_decode_step_prefix")
     ap.add_argument("--no-rows", action="store_true",
-                    help="skip the extra measurements (copy-on-write) reported under 'rows'")
+                    help="skip the other workloads and the copy-on-write rows reported under 'rows'")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -699,13 +822,14 @@ def main():
         kv = sum(k for _, k in per_step)
         v = kv / t / 1e9
         print(json.dumps({
-            "impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": UNIT, "n_gpus": 1,
+            "impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": dict(workload_config(wl, algorithmic_bytes(wl)), parallelism="oracle on host cores"),
+            "data": "synthetic",
+            "config": dict(workload_config(wl, algorithmic_bytes(wl)), parallelism=f"replicas x{world}"),
             "cpu_baseline": {"value": round(v, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": "per step: one sequence of the batch (cycling), all query heads, "
-                                       "fp64 three-pass oracle"},
+                                       "fp64 three-pass oracle on the host cores (rank 0 only)"},
             "e2e": {"value": round(v, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         }), flush=True)
         return 0

@@ -216,8 +216,10 @@ size_t pagedkv_pool_tensor_bytes(int num_blocks, int block_size,
  *   k_scale, v_scale  device fp32 [num_blocks, num_kv_heads] for 8-bit pools,
  *                     NULL for BF16
  *   block_pairs       device int32 [num_pairs][2] (src, dst)
- * A destination must not be the source or destination of another pair of
- * the same call (pairs from kv_pool_prepare_append never are).  A pair with
+ * The pairs of one call run at the same time, so every destination must be
+ * distinct and no destination may be the source of any pair of the call
+ * (pagedkv_check_block_pairs tests this on the host; kv_pool_prepare_append
+ * checks its own output with it).  A pair with
  * an id outside [0, num_blocks) is skipped and sets PAGEDKV_FLAG_BAD_BLOCK;
  * src == dst is a no-op.  At most 65535 pairs per call.  Asynchronous on
  * `stream`. */
@@ -226,6 +228,14 @@ kv_status pagedkv_copy_blocks(void *k_cache, void *v_cache, float *k_scale,
                               int num_pairs, int num_blocks, int block_size,
                               int num_kv_heads, int head_dim, kv_dtype dtype,
                               void *stream);
+
+/* Host check of a copy list for pagedkv_copy_blocks: KV_OK when every id is in
+ * [0, num_blocks), every destination is distinct and no destination is the
+ * source of any pair; else KV_ERR_INVALID_ARG naming the first offending
+ * pair.  block_pairs is host int32 [num_pairs][2] (src, dst); pairs with
+ * src == dst are no-ops and are ignored.  Reads only its arguments. */
+kv_status pagedkv_check_block_pairs(const int32_t *block_pairs, int num_pairs,
+                                    int num_blocks);
 
 /* ------------------------------------------------------------------------ */
 /* Slot mapping                                                             */
@@ -424,6 +434,11 @@ kv_status paged_attention_decode_noalloc(void *out, const void *q,
                                          int block_size, int max_seq_len,
                                          float scale, kv_dtype dtype,
                                          void *stream);
+
+/* PAGEDKV_NOALLOC_SCRATCH_BYTES as compiled into this library: the largest
+ * split-K scratch paged_attention_decode_noalloc serves (a binding can read
+ * the limit here instead of repeating the macro). */
+size_t pagedkv_noalloc_scratch_bytes(void);
 
 /* ------------------------------------------------------------------------ */
 /* Multi-token queries                                                      */

@@ -18,6 +18,8 @@ Contents, each citing the passage it follows (page titles as printed):
 * ``copy_blocks`` -- the block copy of copy-on-write (plain numpy);
 * ``fnv1a64``, ``block_hash`` -- the prefix cache's block hash chain
   (“让 Agent 跑得快”, §七; FNV-1a from its published definition);
+* ``workload_pools`` -- the oracle's own pools for a seeded workload (its
+  slot mapping and append over the generator's token values);
 * ``token_slots``, ``append_bf16``, ``append_int8``, ``quantize_int8``,
   ``append_fp8``, ``quantize_fp8``, ``fp8_value``, ``paged_attention_multi``
   (multi-token causal queries),
@@ -402,6 +404,42 @@ def quantize_fp8(x: float, s: float) -> int:
 def fp8_value(code: int) -> float:
     """Value of an E4M3 code (NaN for 0x7F / 0xFF)."""
     return _load().oracle_fp8_value(int(code))
+
+
+def append_any(k, v, k_cache, v_cache, k_scale, v_scale, slots):
+    """The append for the pool's dtype (uint16 bf16 bits, int8 codes, uint8
+    E4M3 codes)."""
+    if k_cache.dtype == np.int8:
+        return append_int8(k, v, k_cache, v_cache, k_scale, v_scale, slots)
+    if k_cache.dtype == np.uint8:
+        return append_fp8(k, v, k_cache, v_cache, k_scale, v_scale, slots)
+    return append_bf16(k, v, k_cache, v_cache, slots)
+
+
+def workload_pools(wl, seqs=None, with_new_token=True):
+    """The oracle's own K/V pools for a seeded workload ``wl`` (optionally
+    only sequences ``seqs``): poisoned pools, the cached tokens appended
+    through this module's slot mapping and append, then (by default) the
+    step's new tokens at their positions.  Nothing comes from the CUDA path.
+    Returns (k_cache, v_cache, k_scale, v_scale)."""
+    s = wl.spec
+    kc, vc = wl.poisoned_pool(), wl.poisoned_pool()
+    ks = vs = None
+    if s.kv_dtype != "bf16":
+        ks, vs = wl.scales(seqs)
+    for ch in wl.fill_chunks(seqs):
+        slots, rc = token_slots(wl.block_tables, ch.positions, s.block_size, wl.num_blocks,
+                                seq_idx=ch.seq_idx)
+        assert rc == 0
+        assert append_any(ch.k, ch.v, kc, vc, ks, vs, slots) == 0
+    if with_new_token:
+        seq, pos = wl.new_positions()
+        slots, rc = token_slots(wl.block_tables, pos, s.block_size, wl.num_blocks, seq_idx=seq)
+        assert rc == 0
+        if seqs is not None:
+            slots[~np.isin(seq, np.asarray(list(seqs)))] = -1
+        assert append_any(wl.new_k, wl.new_v, kc, vc, ks, vs, slots) == 0
+    return kc, vc, ks, vs
 
 
 def _kv_kind(k_cache):

@@ -38,6 +38,7 @@ SIGNATURES = {
     "kv_pool_refcount": (_I, [_P, ctypes.c_int32]),
     "kv_pool_prepare_append": (_I, [_P, _P, _I, _P, _I, _P, _P]),
     "pagedkv_copy_blocks": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "pagedkv_check_block_pairs": (_I, [_P, _I, _I]),
     "pagedkv_multi_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "pagedkv_block_hash": (ctypes.c_uint64, [ctypes.c_uint64, _P, _I, ctypes.c_uint64]),
     "kv_pool_match_prefix": (_I, [_P, _P, _I, ctypes.c_uint64, _P, _P]),
@@ -54,6 +55,7 @@ SIGNATURES = {
                                     _I, _F, _I, _P, _SZ, _P]),
     "paged_attention_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I,
                                             _I, _I, _I, _F, _I, _P]),
+    "pagedkv_noalloc_scratch_bytes": (_SZ, []),
     "pagedkv_get_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
     "pagedkv_last_error": (ctypes.c_char_p, []),
     "pagedkv_partition_tokens": (_I, [_I, _I, _I, _I]),
@@ -336,6 +338,16 @@ def copy_blocks(k_cache, v_cache, block_pairs, k_scale=None, v_scale=None, strea
                                       _stream(stream)))
 
 
+def check_block_pairs(block_pairs, num_blocks):
+    """Host check of a copy list for copy_blocks (a host int32 array [n, 2] of
+    (src, dst)): every id in range, destinations distinct and none of them a
+    source.  Raises KVError otherwise."""
+    import numpy as np
+    pairs = np.ascontiguousarray(block_pairs, np.int32).reshape(-1, 2)
+    _check(load().pagedkv_check_block_pairs(pairs.ctypes.data if len(pairs) else None, len(pairs),
+                                            int(num_blocks)))
+
+
 def multi_workspace_bytes(num_tokens, num_q_heads, head_dim, max_seq_len, block_size) -> int:
     return load().pagedkv_multi_workspace_bytes(num_tokens, num_q_heads, head_dim, max_seq_len,
                                                 block_size)
@@ -478,14 +490,17 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, seq_lens, max
     return out
 
 
-NOALLOC_SCRATCH_BYTES = 32 << 20
+def noalloc_scratch_bytes() -> int:
+    """Size of the fixed device scratch paged_attention_decode_noalloc uses,
+    as compiled into the library."""
+    return load().pagedkv_noalloc_scratch_bytes()
 
 
 def paged_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, seq_lens, max_seq_len,
                                    scale, k_scale=None, v_scale=None, stream=None):
     """paged_attention_decode for callers that cannot allocate device memory:
-    the split-K partials go to the library's fixed 32 MiB device scratch
-    instead of a caller workspace.  Calls that overlap on the GPU race on
+    the split-K partials go to the library's fixed device scratch
+    (``noalloc_scratch_bytes()``, 32 MiB) instead of a caller workspace.  Calls that overlap on the GPU race on
     that scratch; the first call on a device should come before any stream
     capture."""
     import torch

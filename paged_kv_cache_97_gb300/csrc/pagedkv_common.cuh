@@ -94,6 +94,8 @@ inline size_t ml_region_floats(size_t rows, int slots) {
 
 // Tensor maps over the K and V pools for this launch's geometry: 4-D
 // [NB, bs, Hkv, d], box = one block's rows of one head (128-byte swizzle).
+// Encoded once per (device, pool addresses, geometry) and then served from
+// a small cache.
 kv_status make_kv_maps(const DecodeArgs& a, CUtensorMap* k_map, CUtensorMap* v_map);
 
 // Launches the per-partition decode kernel (with the append fused in when

@@ -772,8 +772,7 @@ kv_status launch_t(const DecodeArgs& a, cudaStream_t s) {
     }
   }
   alignas(64) CUtensorMap km, vm;
-  if ((st = make_map<D, BS, kQ8>(&km, a.k_cache, a)) != KV_OK) return st;
-  if ((st = make_map<D, BS, kQ8>(&vm, a.v_cache, a)) != KV_OK) return st;
+  if ((st = make_kv_maps(a, &km, &vm)) != KV_OK) return st;
   const dim3 grid(a.num_kv_heads, kMulti ? a.batch * a.vgroups : a.batch, a.max_parts);
   if (a.prefix_chunks == 0) {
     decode_kernel<D, BS, kQ8, kFp8, kMulti><<<grid, kThreads, G::kSmemBytes, s>>>(km, vm, a);
@@ -809,9 +808,7 @@ kv_status maps_t(const DecodeArgs& a, CUtensorMap* km, CUtensorMap* vm) {
   return st != KV_OK ? st : make_map<D, BS, kQ8>(vm, a.v_cache, a);
 }
 
-}  // namespace
-
-kv_status make_kv_maps(const DecodeArgs& a, CUtensorMap* km, CUtensorMap* vm) {
+kv_status encode_kv_maps(const DecodeArgs& a, CUtensorMap* km, CUtensorMap* vm) {
   const bool q8 = a.dtype != KV_DTYPE_BF16, b32 = a.block_size == 32;
   if (a.head_dim == 128) {
     if (q8) return b32 ? maps_t<128, 32, true>(a, km, vm) : maps_t<128, 16, true>(a, km, vm);
@@ -819,6 +816,59 @@ kv_status make_kv_maps(const DecodeArgs& a, CUtensorMap* km, CUtensorMap* vm) {
   }
   if (q8) return b32 ? maps_t<64, 32, true>(a, km, vm) : maps_t<64, 16, true>(a, km, vm);
   return b32 ? maps_t<64, 32, false>(a, km, vm) : maps_t<64, 16, false>(a, km, vm);
+}
+
+// The K and V tensor maps of recently used pools.  A map holds only the
+// pool's address and geometry, so an entry whose key matches is the map
+// that encoding would produce again (a pool freed and re-allocated at the
+// same address with the same geometry gets the same map).  Looking one up
+// costs a mutex and a short scan instead of two driver encodings per call.
+struct MapEntry {
+  const void* k = nullptr;
+  const void* v = nullptr;
+  int64_t num_blocks = 0;
+  int device = -1, kv8 = 0, head_dim = 0, block_size = 0, num_kv_heads = 0;
+  CUtensorMap km, vm;                 // (CUtensorMap carries its own alignment)
+};
+constexpr int kMapCache = 16;
+
+}  // namespace
+
+kv_status make_kv_maps(const DecodeArgs& a, CUtensorMap* km, CUtensorMap* vm) {
+  static std::mutex mu;
+  static MapEntry cache[kMapCache];
+  static int next = 0;
+  int dev = 0;
+  kv_status st = cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
+  if (st != KV_OK) return st;
+  const int kv8 = a.dtype != KV_DTYPE_BF16;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const MapEntry& e : cache) {
+    if (e.device == dev && e.k == a.k_cache && e.v == a.v_cache && e.kv8 == kv8 &&
+        e.head_dim == a.head_dim && e.block_size == a.block_size &&
+        e.num_kv_heads == a.num_kv_heads && e.num_blocks == a.num_blocks) {
+      *km = e.km;
+      *vm = e.vm;
+      return KV_OK;
+    }
+  }
+  MapEntry& e = cache[next];
+  if ((st = encode_kv_maps(a, &e.km, &e.vm)) != KV_OK) {
+    e.device = -1;
+    return st;
+  }
+  e.device = dev;
+  e.k = a.k_cache;
+  e.v = a.v_cache;
+  e.kv8 = kv8;
+  e.head_dim = a.head_dim;
+  e.block_size = a.block_size;
+  e.num_kv_heads = a.num_kv_heads;
+  e.num_blocks = a.num_blocks;
+  next = (next + 1) % kMapCache;
+  *km = e.km;
+  *vm = e.vm;
+  return KV_OK;
 }
 
 kv_status launch_decode(const DecodeArgs& a, cudaStream_t s) {

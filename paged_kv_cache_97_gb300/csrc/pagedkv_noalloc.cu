@@ -51,33 +51,42 @@ kv_status scratch_address(void** out) {
 
 using namespace pagedkv;
 
+extern "C" size_t pagedkv_noalloc_scratch_bytes(void) { return PAGEDKV_NOALLOC_SCRATCH_BYTES; }
+
 extern "C" kv_status paged_attention_decode_noalloc(
     void* out, const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
     const float* v_scale, const int32_t* block_tables, int max_blocks_per_seq,
     const int32_t* seq_lens, int batch, int num_q_heads, int num_kv_heads, int head_dim,
     int num_blocks, int block_size, int max_seq_len, float scale, kv_dtype dtype, void* stream) {
-  // An empty batch (and any bad size) is settled by the argument checks of
-  // paged_attention_decode before it touches a device: no scratch is needed.
-  if (batch <= 0)
+  // An empty batch and every shape paged_attention_decode rejects are left to
+  // its own argument checks (they return before it touches a device or reads
+  // the workspace), so those callers get its messages.
+  const bool shape_ok = batch > 0 && num_q_heads > 0 && num_kv_heads > 0 &&
+                        num_q_heads % num_kv_heads == 0 && num_q_heads / num_kv_heads <= kMaxGroup &&
+                        (head_dim == 64 || head_dim == 128) && (block_size == 16 || block_size == 32) &&
+                        max_blocks_per_seq > 0 && num_blocks > 0 && max_seq_len > 0 &&
+                        valid_dtype(dtype);
+  if (!shape_ok)
     return paged_attention_decode(out, q, k_cache, v_cache, k_scale, v_scale, block_tables,
                                   max_blocks_per_seq, seq_lens, batch, num_q_heads,
                                   num_kv_heads, head_dim, num_blocks, block_size, max_seq_len,
                                   scale, dtype, nullptr, 0, stream);
-  if (num_q_heads > 0 && num_kv_heads > 0 && head_dim > 0 && max_seq_len > 0) {
-    // Scratch this call needs: the partials of every (sequence, query head,
-    // partition) when a sequence spans several partitions.
-    const int part = pagedkv_partition_tokens(batch, num_kv_heads, max_seq_len, block_size);
-    if (part <= 0) return fail(KV_ERR_CUDA, "paged_attention_decode_noalloc: no device");
-    const int parts = (max_seq_len + part - 1) / part;
-    const size_t need = decode_workspace_need(batch, num_q_heads, head_dim, parts);
-    if (need > PAGEDKV_NOALLOC_SCRATCH_BYTES)
-      return fail(KV_ERR_INVALID_ARG,
-                  "paged_attention_decode_noalloc: this shape needs %zu bytes of scratch, more "
-                  "than the fixed %u bytes; use paged_attention_decode with a workspace",
-                  need, (unsigned)PAGEDKV_NOALLOC_SCRATCH_BYTES);
-  }
+  // Scratch this call needs: the partials of every (sequence, query head,
+  // partition) when a sequence spans several partitions, with the partition
+  // paged_attention_decode will choose on this device.
+  DeviceInfo di;
+  kv_status st = device_info(&di);
+  if (st != KV_OK) return st;
+  const int part = choose_part_tokens(batch, num_kv_heads, max_seq_len, di.num_sms, true);
+  const int parts = (max_seq_len + part - 1) / part;
+  const size_t need = decode_workspace_need(batch, num_q_heads, head_dim, parts);
+  if (need > PAGEDKV_NOALLOC_SCRATCH_BYTES)
+    return fail(KV_ERR_INVALID_ARG,
+                "paged_attention_decode_noalloc: this shape needs %zu bytes of scratch, more "
+                "than the fixed %u bytes; use paged_attention_decode with a workspace",
+                need, (unsigned)PAGEDKV_NOALLOC_SCRATCH_BYTES);
   void* scratch = nullptr;
-  kv_status st = scratch_address(&scratch);
+  st = scratch_address(&scratch);
   if (st != KV_OK) return st;
   // Nothing in the scratch needs clearing: every partial the merge kernel
   // reads is written earlier in the same call.

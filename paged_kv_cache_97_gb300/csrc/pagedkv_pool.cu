@@ -314,6 +314,33 @@ kv_status kv_pool_prepare_append(kv_pool* p, int32_t* block_tables, int max_bloc
     }
   }
   *num_copies = n;
+  // (fresh blocks come from the free list, shared sources are in use: the
+  // list is a valid batch for pagedkv_copy_blocks by construction)
+  return pagedkv_check_block_pairs(copy_pairs, n, p->num_blocks);
+}
+
+kv_status pagedkv_check_block_pairs(const int32_t* block_pairs, int num_pairs, int num_blocks) {
+  if (num_pairs < 0 || num_blocks <= 0 || (num_pairs > 0 && !block_pairs))
+    return fail(KV_ERR_INVALID_ARG, "pagedkv_check_block_pairs: bad arguments");
+  std::vector<uint8_t> role(num_blocks, 0);          // bit 0: a source, bit 1: a destination
+  for (int i = 0; i < num_pairs; ++i) {
+    const int32_t src = block_pairs[2 * i], dst = block_pairs[2 * i + 1];
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks)
+      return fail(KV_ERR_INVALID_ARG, "block pair %d (%d, %d): id outside [0, %d)", i, src, dst,
+                  num_blocks);
+    if (src != dst) role[src] |= 1;
+  }
+  for (int i = 0; i < num_pairs; ++i) {
+    const int32_t src = block_pairs[2 * i], dst = block_pairs[2 * i + 1];
+    if (src == dst) continue;
+    if (role[dst] & 2)
+      return fail(KV_ERR_INVALID_ARG, "block pair %d (%d, %d): destination %d appears twice", i,
+                  src, dst, dst);
+    if (role[dst] & 1)
+      return fail(KV_ERR_INVALID_ARG, "block pair %d (%d, %d): destination %d is also a source", i,
+                  src, dst, dst);
+    role[dst] |= 2;
+  }
   return KV_OK;
 }
 

@@ -10,42 +10,11 @@ from workloads import bf16_bits_to_f32
 
 
 def oracle_pool(wl, seqs=None, with_new_token=True):
-    """Oracle K/V pools for workload ``wl`` (optionally only sequences
-    ``seqs``): poisoned pools, the cached tokens appended through the oracle's
-    slot mapping, then (by default) the decode step's new token appended at
-    position L_b - 1.  Returns (k_cache, v_cache, k_scale, v_scale)."""
-    s = wl.spec
-    kc, vc = wl.poisoned_pool(), wl.poisoned_pool()
-    q8 = s.kv_dtype != "bf16"
-    ks = vs = None
-    if q8:
-        ks, vs = wl.scales(seqs)
-    for ch in wl.fill_chunks(seqs):
-        slots, rc = oracle.token_slots(wl.block_tables, ch.positions, s.block_size,
-                                       wl.num_blocks, seq_idx=ch.seq_idx)
-        assert rc == 0
-        rc = append_any(ch.k, ch.v, kc, vc, ks, vs, slots)
-        assert rc == 0
-    if with_new_token:
-        seq, pos = wl.new_positions()
-        slots, rc = oracle.token_slots(wl.block_tables, pos, s.block_size, wl.num_blocks,
-                                       seq_idx=seq)
-        assert rc == 0
-        if seqs is not None:
-            slots[~np.isin(seq, np.asarray(list(seqs)))] = -1
-        rc = append_any(wl.new_k, wl.new_v, kc, vc, ks, vs, slots)
-        assert rc == 0
-    return kc, vc, ks, vs
+    """Oracle K/V pools for workload ``wl``: ``oracle.workload_pools``."""
+    return oracle.workload_pools(wl, seqs, with_new_token)
 
 
-def append_any(k, v, kc, vc, ks, vs, slots):
-    """The oracle's append for the pool's dtype (uint16 bf16 bits, int8
-    codes, uint8 E4M3 codes)."""
-    if kc.dtype == np.int8:
-        return oracle.append_int8(k, v, kc, vc, ks, vs, slots)
-    if kc.dtype == np.uint8:
-        return oracle.append_fp8(k, v, kc, vc, ks, vs, slots)
-    return oracle.append_bf16(k, v, kc, vc, slots)
+append_any = oracle.append_any
 
 
 def decode_slots(wl):

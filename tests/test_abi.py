@@ -158,3 +158,60 @@ def test_empty_inputs_return_ok_without_a_device(pkv):
     assert lib.paged_attention_decode_noalloc(None, None, None, None, None, None, None, 4, None,
                                               -1, 8, 2, 64, 10, 16, 64, 0.125, 0,
                                               None) == pkv.KV_ERR_INVALID_ARG
+
+
+def test_noalloc_scratch_size_matches_the_header(pkv):
+    text = open(HEADER).read()
+    m = re.search(r"#define PAGEDKV_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", text)
+    assert m, "PAGEDKV_NOALLOC_SCRATCH_BYTES not found in the header"
+    assert pkv.noalloc_scratch_bytes() == int(m.group(1)) << int(m.group(2))
+
+
+def test_noalloc_leaves_bad_shapes_to_the_decode_checks(pkv):
+    # a shape paged_attention_decode rejects gets its message (before any
+    # device call), not a scratch-size one
+    lib = pkv.load()
+    P = 256
+    st = lib.paged_attention_decode_noalloc(P, P, P, P, None, None, P, 64, P, 4, 30, 8, 128,
+                                            1000, 16, 1024, 0.1, 0, None)
+    assert st == pkv.KV_ERR_INVALID_ARG
+    assert "bad sizes" in lib.pagedkv_last_error().decode()
+    st = lib.paged_attention_decode_noalloc(P, P, P, P, None, None, P, 64, P, 4, 32, 8, 96,
+                                            1000, 16, 1024, 0.1, 0, None)
+    assert st == pkv.KV_ERR_INVALID_ARG
+    assert "head_dim" in lib.pagedkv_last_error().decode()
+
+
+@pytest.mark.parametrize("pairs,ok", [
+    ([], True),
+    ([[3, 7], [4, 8], [3, 9]], True),              # one source copied twice: fine
+    ([[5, 5], [1, 2]], True),                      # src == dst is a no-op
+    ([[3, 7], [4, 7]], False),                     # a destination twice
+    ([[3, 7], [7, 8]], False),                     # a destination is another pair's source
+    ([[3, 7], [2, 3]], False),                     # (the other order)
+    ([[3, 16]], False),                            # id past the pool
+    ([[-1, 2]], False),
+])
+def test_block_pair_check(pkv, pairs, ok):
+    if ok:
+        pkv.check_block_pairs(np.array(pairs, np.int32).reshape(-1, 2), 16)
+    else:
+        with pytest.raises(pkv.KVError) as e:
+            pkv.check_block_pairs(np.array(pairs, np.int32).reshape(-1, 2), 16)
+        assert e.value.status == pkv.KV_ERR_INVALID_ARG
+
+
+def test_prepare_append_copies_are_a_valid_batch(pkv):
+    # forks of several sequences, then one step where every shared block is
+    # written: the copy list passes the check (distinct fresh destinations)
+    pool = pkv.KVPool(64, 16, 2, 64)
+    ids = pool.alloc(3)
+    tables = np.full((4, 8), -1, np.int32)
+    for b in range(4):
+        if b:
+            pool.fork(ids)
+        tables[b, :3] = ids
+    lens = np.array([40, 40, 40, 40], np.int32)             # all write into block 2 (shared by 4)
+    pairs = pool.prepare_append(tables, lens)
+    assert len(pairs) == 3
+    pkv.check_block_pairs(pairs, 64)

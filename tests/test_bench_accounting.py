@@ -9,6 +9,8 @@ block in use.  Per row of a block: K and V for every KV head, d elements each
 (the block layout [num_blocks, block_size, Hkv, d] of “LLM 推理引擎深度解析”,
 §2.1; the per-token KV size of “让 Agent 跑得快：LLM 推理服务”, §一).
 """
+import json
+
 import numpy as np
 import pytest
 
@@ -66,3 +68,20 @@ def test_default_workload_is_larger_than_l2():
     # the timed region relies on inputs larger than L2 instead of a flush
     nb = bench.algorithmic_bytes(workloads.make(bench.DEFAULT_CONFIG))
     assert nb["kv_unique"] > bench.L2_BYTES
+
+
+def test_stored_traffic_needs_the_current_kernel_source(tmp_path, monkeypatch):
+    # a capture counts only for its workload, its kernel and the hash of the
+    # kernel's current sources
+    name = workloads.make(2).spec.name
+    cur = bench.kernel_hash("decode_kernel")
+    f = tmp_path / "traffic.json"
+    f.write_text(json.dumps({"captures": [
+        {"workload": name, "kernel": "decode_kernel", "source_sha256_16": "0" * 16,
+         "dram_bytes_per_launch": 1},
+        {"workload": name, "kernel": "decode_kernel", "source_sha256_16": cur,
+         "dram_bytes_per_launch": 2}]}))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.stored_traffic(name, "decode_kernel") == 2
+    assert bench.stored_traffic(name, "multi_tc_kernel") is None
+    assert bench.stored_traffic("another workload", "decode_kernel") is None

@@ -42,8 +42,10 @@ appended in this step; cached tokens are positions ``0 .. L_b - 2``.
 from __future__ import annotations
 
 import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass
-from typing import Iterator, Optional, Sequence
+from typing import Callable, Iterable, Iterator, Optional, Sequence
 
 import numpy as np
 
@@ -58,8 +60,39 @@ SEED_BASE = 20260000
 def to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round fp32 to the nearest-even bf16 and return the 16-bit patterns."""
     u = np.ascontiguousarray(x, np.float32).view(np.uint32)
-    lsb = (u >> np.uint32(16)) & np.uint32(1)
-    return ((u + np.uint32(0x7FFF) + lsb) >> np.uint32(16)).astype(np.uint16)
+    t = np.right_shift(u, np.uint32(16))
+    np.bitwise_and(t, np.uint32(1), out=t)             # the kept part's lowest bit
+    np.add(t, np.uint32(0x7FFF), out=t)
+    np.add(t, u, out=t)
+    np.right_shift(t, np.uint32(16), out=t)
+    return t.astype(np.uint16)
+
+
+def default_workers() -> int:
+    """Threads for drawing per-sequence token values (numpy's generators and
+    ufuncs release the GIL on large arrays)."""
+    return max(1, min(16, os.cpu_count() or 1))
+
+
+def ordered_map(fn: Callable, items: Iterable, workers: int) -> Iterator:
+    """fn over items, results in input order, at most 2 x workers computed
+    ahead (so a long batch never holds all its values at once)."""
+    items = list(items)
+    if workers <= 1 or len(items) <= 1:
+        for it in items:
+            yield fn(it)
+        return
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        ahead = 2 * workers
+        futs = [ex.submit(fn, it) for it in items[:ahead]]
+        nxt = len(futs)
+        for i in range(len(items)):
+            res = futs[i].result()
+            futs[i] = None
+            if nxt < len(items):
+                futs.append(ex.submit(fn, items[nxt]))
+                nxt += 1
+            yield res
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
@@ -255,9 +288,13 @@ class Workload:
         v = to_bf16_bits(g.standard_normal(shp, np.float32))
         return np.arange(lo, hi, dtype=np.int32), k, v
 
-    def fill_chunks(self, seqs: Optional[Sequence[int]] = None) -> Iterator[FillChunk]:
+    def fill_chunks(self, seqs: Optional[Sequence[int]] = None,
+                    workers: Optional[int] = None) -> Iterator[FillChunk]:
         """Chunks of cached tokens to append before the step (the shared
-        prefix once, through sequence 0's table, then each sequence's own)."""
+        prefix once, through sequence 0's table, then each sequence's own).
+        Sequences are drawn on ``workers`` threads (default: the host's cores,
+        at most 16); each has its own stream, so the values do not depend on
+        the thread count."""
         s = self.spec
         seqs = range(s.batch) if seqs is None else seqs
         P = s.shared_prefix_tokens
@@ -265,8 +302,8 @@ class Workload:
             pk, pv = self._prefix_kv()
             first = 0 if seqs is None else min(seqs)
             yield FillChunk(np.full(P, first, np.int32), np.arange(P, dtype=np.int32), pk, pv)
-        for b in seqs:
-            pos, k, v = self.own_tokens(b)
+        nw = default_workers() if workers is None else workers
+        for b, (pos, k, v) in zip(seqs, ordered_map(self.own_tokens, seqs, nw)):
             if pos.size:
                 yield FillChunk(np.full(pos.size, b, np.int32), pos, k, v)
 
@@ -282,9 +319,8 @@ class Workload:
         seqs = range(s.batch) if seqs is None else seqs
         assert s.shared_prefix_tokens == 0, "8-bit workloads have no shared prefix"
         top = np.float32(CODE_MAX[s.kv_dtype])
-        for b in seqs:
+        for b, (pos, k, v) in zip(seqs, ordered_map(self.own_tokens, seqs, default_workers())):
             L = int(self.seq_lens[b])
-            pos, k, v = self.own_tokens(b)
             nk, nv = self.new_kv_of(b)
             kf = np.concatenate([bf16_bits_to_f32(k), bf16_bits_to_f32(nk)])
             vf = np.concatenate([bf16_bits_to_f32(v), bf16_bits_to_f32(nv)])
