@@ -374,7 +374,9 @@ kv_status pagedkv_decode_step(void *out, const void *q, const void *k,
  *   k, v               as pagedkv_decode_step, or both NULL to attend
  *                      without appending
  *   workspace          at least pagedkv_prefix_workspace_bytes(...) bytes
- * bf16 pools only (8-bit pools return KV_ERR_NOT_IMPLEMENTED). */
+ * bf16, int8 and E4M3 pools (for 8-bit pools the prefix product widens the
+ * codes exactly to fp16 and runs in fp16; k_scale and v_scale as for
+ * paged_attention_decode). */
 kv_status pagedkv_decode_step_prefix(void *out, const void *q, const void *k,
                                      const void *v, void *k_cache,
                                      void *v_cache, const float *k_scale,
@@ -463,9 +465,10 @@ size_t pagedkv_multi_workspace_bytes(int num_tokens, int num_q_heads,
  *   out[j, h, :] = softmax_t(scale * q[j, h, :] . K_t) . V_t.
  *   out           device bf16 [num_tokens, num_q_heads, head_dim]
  *   q             device bf16 [num_tokens, num_q_heads, head_dim]
- *   k_cache, v_cache, k_scale, v_scale   as for paged_attention_decode;
- *                 8-bit pools (int8, E4M3) take up to 4 * (8 / G) query tokens
- *                 per sequence (8 for G = 4), else KV_ERR_NOT_IMPLEMENTED
+ *   k_cache, v_cache, k_scale, v_scale   as for paged_attention_decode
+ *                 (bf16, int8 and E4M3 pools; with 8-bit pools the long-query
+ *                 kernel widens the codes exactly to fp16 and runs its
+ *                 products in fp16)
  *   block_tables, max_blocks_per_seq, seq_lens, batch  as for
  *                 paged_attention_decode (seq_lens counts the query tokens)
  *   query_start   device int32 [batch + 1], non-decreasing from 0 to

@@ -444,6 +444,59 @@ def decode_step(out, q, k, v, k_cache, v_cache, block_tables, seq_lens, max_seq_
     return out
 
 
+_raw_lib = None
+
+
+def _raw():
+    """A second handle on the library whose functions take ctypes objects
+    as they are (no per-call argument conversion): for prepared calls."""
+    global _raw_lib
+    if _raw_lib is None:
+        load()
+        _raw_lib = ctypes.CDLL(LIB_PATH)
+        _raw_lib.pagedkv_decode_step.restype = ctypes.c_int
+    return _raw_lib
+
+
+class DecodeStepPlan:
+    """pagedkv_decode_step with its arguments checked and marshalled once.
+
+    Arguments as ``decode_step``.  The plan holds the tensors (their memory
+    stays valid while it lives); they must keep their shapes and storage,
+    while their contents may change between calls -- the usual serving loop
+    writes the next step's q, k, v, tables and lengths in place.  Each call
+    runs one step on the current stream (or ``stream``) and returns ``out``;
+    only the stream is looked up per call, which keeps a small step's host
+    time near the C call itself."""
+
+    def __init__(self, out, q, k, v, k_cache, v_cache, block_tables, seq_lens, max_seq_len, scale,
+                 workspace, k_scale=None, v_scale=None):
+        import torch
+        wbytes = _check_decode(out, q, k_cache, v_cache, block_tables, seq_lens, k_scale, v_scale,
+                               workspace)
+        _need(k, torch.bfloat16, "k", 3)
+        _need(v, torch.bfloat16, "v", 3)
+        B, hq, d = q.shape
+        nb, bs, hkv, _ = k_cache.shape
+        if k.shape != (B, hkv, d) or v.shape != k.shape:
+            raise ValueError("k, v must be [batch, num_kv_heads, head_dim]")
+        self.out = out
+        self._keep = (q, k, v, k_cache, v_cache, block_tables, seq_lens, workspace, k_scale, v_scale)
+        P, I = ctypes.c_void_p, ctypes.c_int
+        self._fn = _raw().pagedkv_decode_step
+        self._args = (P(_ptr(out)), P(_ptr(q)), P(_ptr(k)), P(_ptr(v)), P(_ptr(k_cache)),
+                      P(_ptr(v_cache)), P(_ptr(k_scale)), P(_ptr(v_scale)), P(_ptr(block_tables)),
+                      I(block_tables.shape[1]), P(_ptr(seq_lens)), I(B), I(hq), I(hkv), I(d), I(nb),
+                      I(bs), I(int(max_seq_len)), ctypes.c_float(float(scale)),
+                      I(_pool_dtype(k_cache)), P(_ptr(workspace)), ctypes.c_size_t(wbytes))
+
+    def __call__(self, stream=None):
+        st = self._fn(*self._args, ctypes.c_void_p(_stream(stream)))
+        if st != KV_OK:
+            _check(st)
+        return self.out
+
+
 def prefix_workspace_bytes(batch, num_q_heads, head_dim, max_seq_len, block_size,
                            num_prefix_blocks) -> int:
     return load().pagedkv_prefix_workspace_bytes(batch, num_q_heads, head_dim, max_seq_len,

@@ -487,8 +487,6 @@ static kv_status decode_common(void* out, const void* q, const void* new_k, cons
     return fail(KV_ERR_INVALID_ARG,
                 "%s: the shared prefix needs 1..max_blocks_per_seq block ids and sequences "
                 "longer than it", who);
-  if (num_prefix_blocks > 0 && q8)
-    return fail(KV_ERR_NOT_IMPLEMENTED, "%s: the shared-prefix path supports bf16 pools only", who);
   DeviceInfo di;
   kv_status st = device_info(&di);
   if (st != KV_OK) return st;

@@ -237,17 +237,13 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
   const int GQ = num_q_heads / num_kv_heads;
   // Sequences with few query tokens (at most 4 x 8 / G): the decode
   // kernel's 8 columns per CTA hold (token, head) pairs, 8 / G tokens per
-  // column group.  Longer queries: the tensor-core kernel (bf16 pools), in the
-  // same call when both kinds occur.
+  // column group.  Longer queries: the tensor-core kernel, in the same call
+  // when both kinds occur.
   const int tpg = GQ <= kMaxGroup ? kMaxGroup / GQ : 0;
   const int col_max_n = tpg * kMaxVGroups;               // 0 when G > 8
   const int vgroups = tpg > 0 ? (min(max_query_len, col_max_n) + tpg - 1) / tpg : 0;
   const bool column_path = tpg > 0;                       // some sequences may use it
   const bool row_path = max_query_len > col_max_n;        // some sequences may need it
-  if (row_path && q8)
-    return fail(KV_ERR_NOT_IMPLEMENTED,
-                "%s: 8-bit pools support up to %d query tokens per sequence here", who,
-                tpg * kMaxVGroups);
   if (batch == 0 || num_tokens == 0) return KV_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !query_start)
     return fail(KV_ERR_INVALID_ARG, "%s: NULL pointer", who);

@@ -38,7 +38,8 @@
 // hold NaN).  Every wait is bounded; a CTA that gives up flags
 // PAGEDKV_FLAG_WAIT_TIMEOUT, drains its copies and tensor-core work, frees its
 // TMEM and marks its rows bad.  A warp whose 32 rows are all padding only
-// keeps the barrier phases.  bf16 pools.
+// keeps the barrier phases.  bf16, int8 and E4M3 pools (the 8-bit kinds in
+// fp16, described at the kernel).
 //
 // Shared-prefix mode (kPrefix): when every sequence's first blocks are the
 // same physical blocks (“让 Agent 跑得快”, §五 共享前缀), the prefix part of
@@ -87,9 +88,11 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
   return d;
 }
 
-// kind::f16 instruction descriptor: fp32 D, bf16 A and B, A/B major, N, M.
+// kind::f16 instruction descriptor: fp32 D, A and B both bf16 (or both
+// fp16: kF16), A K-major, B K- or MN-major, N, M.
+template <bool kF16>
 __host__ __device__ constexpr uint32_t mma_idesc(int M, int N, int b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn_major << 16) |
+  return (1u << 4) | (kF16 ? 0u : (1u << 7) | (1u << 10)) | ((uint32_t)b_mn_major << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
@@ -179,8 +182,16 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Largest raw score of a chunk row (keys past `lim` left out when kMask),
-// four independent partial maxima.
+// Scores of 32 consecutive keys of a chunk row times per-key factors: the
+// first 16 keys by f[0], the next 16 by f[1] (8-bit pools: each key's block
+// K scale with the score scale; blocks hold 16 or 32 keys).
+__device__ __forceinline__ void scale_keys(uint32_t (&raw)[32], const float (&f)[2]) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) raw[j] = __float_as_uint(__uint_as_float(raw[j]) * f[j >> 4]);
+}
+
+// Largest score of a chunk row (keys past `lim` left out when kMask), four
+// independent partial maxima.
 template <bool kMask, int kH>
 __device__ __forceinline__ float chunk_max(const uint32_t (&raw)[kH][32], int first_tok, int lim) {
   float mr[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -195,11 +206,14 @@ __device__ __forceinline__ float chunk_max(const uint32_t (&raw)[kH][32], int fi
   return fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3]));
 }
 
-// p = 2^(s * sl2 - ref) of a chunk row as bf16 pairs (0 for keys past `lim`
-// when kMask); returns the fp32 sum of the p.
-template <bool kMask, int kH>
+// p = 2^(s * sl2 - ref) of a chunk row (0 for keys past `lim` when kMask);
+// returns the fp32 sum of the p.  P goes out as bf16 pairs, or (kF16) as
+// fp16 pairs of p times the key's factor vr[h][j >> 4] (8-bit pools: the
+// block's V scale relative to the partition's largest; the sum keeps p).
+template <bool kMask, bool kF16, int kH>
 __device__ __forceinline__ float chunk_exp(const uint32_t (&raw)[kH][32], uint32_t (&pw)[kH][16],
-                                           int first_tok, int lim, float sl2, float ref) {
+                                           int first_tok, int lim, float sl2, float ref,
+                                           const float (&vr)[kH][2]) {
   float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
   for (int h = 0; h < kH; ++h)
@@ -214,10 +228,84 @@ __device__ __forceinline__ float chunk_exp(const uint32_t (&raw)[kH][32], uint32
       }
       ls[(2 * j) & 3] += p0;
       ls[(2 * j + 1) & 3] += p1;
-      __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
-      pw[h][j] = *reinterpret_cast<uint32_t*>(&pp);
+      if constexpr (kF16) {
+        const float f = vr[h][j >> 3];
+        pw[h][j] = pack2<true>(p0 * f, p1 * f);
+      } else {
+        pw[h][j] = pack2<false>(p0, p1);
+      }
     }
   return (ls[0] + ls[1]) + (ls[2] + ls[3]);
+}
+
+// Sixteen 8-bit codes as sixteen exact fp16 values (zeros when `zero`).
+template <bool kFp8>
+__device__ __forceinline__ void widen16(uint4 w, bool zero, uint4& lo, uint4& hi) {
+  const uint32_t x[4] = {w.x ^ kCodeBias<kFp8>, w.y ^ kCodeBias<kFp8>, w.z ^ kCodeBias<kFp8>,
+                         w.w ^ kCodeBias<kFp8>};
+  uint32_t h[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    h[2 * i] = zero ? 0u : codes_to_f16x2<kFp8>(x[i], 0x4140u);
+    h[2 * i + 1] = zero ? 0u : codes_to_f16x2<kFp8>(x[i], 0x4342u);
+  }
+  lo = make_uint4(h[0], h[1], h[2], h[3]);
+  hi = make_uint4(h[4], h[5], h[6], h[7]);
+}
+
+// 8-bit pools: the codes of chunk rows [0, nrows), landed by TMA in the
+// second half of the chunk's operand image (D bytes per row; 128-byte
+// swizzled rows when D = 128), widened exactly to fp16 in the image's own
+// layout (128 contiguous 128-byte-swizzled rows per 64-element band), rows
+// at or past `zero_from` written as zeros (the pool's rows past a sequence's
+// end may hold NaN patterns).  One warp; lane i takes rows i, i + 32, ...
+//   D = 128: a row's staged codes sit exactly under its fp16 row in band 1;
+//     taking its 16-code chunks in order, each fp16 write lands on codes
+//     already read (chunk c >= 4 writes band-1 chunks 2c - 8 and 2c - 7).
+//   D = 64: fp16 rows 64.. overwrite the staged codes of rows 2r - 128 and
+//     2r - 127, which other lanes of the same round may still need, so each
+//     round reads all its codes before any lane writes.
+template <int D, bool kFp8>
+__device__ __forceinline__ void widen_chunk(unsigned char* img, int nrows, int zero_from, int lane) {
+  const unsigned char* stg = img + D * kChunk;           // second half of the D * 2 * kChunk image
+  auto put = [&](int r, int e8, uint4 v) {               // 8-element chunk e8 of fp16 row r
+    const int band = e8 >> 3, cc = e8 & 7;
+    *reinterpret_cast<uint4*>(img + band * (kChunk * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) = v;
+  };
+#pragma unroll 1
+  for (int r0 = 0; r0 < nrows; r0 += 32) {
+    const int r = r0 + lane;
+    const bool live = r < nrows, zero = r >= zero_from;
+    if constexpr (D == 128) {
+      if (live) {
+#pragma unroll 2
+        for (int c = 0; c < 8; ++c) {
+          const uint4 w = *reinterpret_cast<const uint4*>(stg + r * 128 + ((c ^ (r & 7)) << 4));
+          uint4 lo, hi;
+          widen16<kFp8>(w, zero, lo, hi);
+          put(r, 2 * c, lo);
+          put(r, 2 * c + 1, hi);
+        }
+      }
+    } else {
+      uint4 w[4];
+      if (live) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const uint4*>(stg + r * 64 + c * 16);
+      }
+      __syncwarp();
+      if (live) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint4 lo, hi;
+          widen16<kFp8>(w[c], zero, lo, hi);
+          put(r, 2 * c, lo);
+          put(r, 2 * c + 1, hi);
+        }
+      }
+      __syncwarp();
+    }
+  }
 }
 
 // Row tiles of a sequence with n query tokens served here (n > col_max_n).
@@ -225,19 +313,31 @@ __device__ __forceinline__ int tc_tiles(int n, int GQ, int col_max_n) {
   return n > col_max_n ? (n * GQ + kTRows - 1) / kTRows : 0;
 }
 
-template <int D, int BS, bool kPrefix>
+// kKind: the pool's dtype (KV_DTYPE_BF16, KV_DTYPE_INT8, KV_DTYPE_FP8_E4M3).
+// 8-bit pools run the MMAs in fp16: Q is converted (scaled by a power of two
+// when its magnitude needs it, folded back into the score scale), the codes
+// are widened exactly by the load warp after each chunk lands, each key's
+// block K scale multiplies its score and each block's V scale, relative to
+// the partition's largest, multiplies P (the output takes that largest back).
+template <int D, int BS, bool kPrefix, int kKind>
 __global__ void __launch_bounds__(kTThreads, 2)
     multi_tc_kernel(const __grid_constant__ CUtensorMap k_map,
                     const __grid_constant__ CUtensorMap v_map, const DecodeArgs a) {
+  constexpr bool kQ8 = kKind != KV_DTYPE_BF16, kFp8 = kKind == KV_DTYPE_FP8_E4M3;
   using T = TcGeo<D>;
-  using Gm = Geo<D, BS, false>;                          // TMA box geometry of one block
+  using Gm = Geo<D, BS, kQ8>;                            // TMA box geometry of one block
   constexpr int kBlocksPerChunk = kChunk / BS;
+  constexpr int kMaxPartBlocks = kMaxPartTokens / 16;
   extern __shared__ unsigned char smem_raw[];
   __shared__ uint64_t k_full, k_empty, v_full, v_empty, s_bar, p_bar, o_bar, drain_bar;
+  __shared__ uint64_t k_conv, v_conv;                    // 8-bit: the chunk is widened to fp16
   __shared__ uint32_t tmem_base;
   __shared__ int scan[kTThreads];
   __shared__ int sh_b, sh_rt, sh_bad, sh_fail;
-  __shared__ int32_t blk_ids[kMaxPartTokens / 16];       // this partition's physical blocks
+  __shared__ int32_t blk_ids[kMaxPartBlocks];            // this partition's physical blocks
+  __shared__ float blk_ks[kQ8 ? kMaxPartBlocks : 1];     // 8-bit: their K scales
+  __shared__ float blk_vs[kQ8 ? kMaxPartBlocks : 1];     //        and V scales
+  __shared__ float sh_vmax;                              //        the largest |V scale|
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hq = a.num_q_heads, Hkv = a.num_kv_heads, GQ = Hq / Hkv;
@@ -289,6 +389,7 @@ __global__ void __launch_bounds__(kTThreads, 2)
     sh_b = -1;
     sh_bad = 0;
     sh_fail = 0;
+    sh_vmax = 0.0f;
   }
   __syncthreads();
   if (!kPrefix && x >= scan[tid] - mine && x < scan[tid]) {
@@ -329,8 +430,17 @@ __global__ void __launch_bounds__(kTThreads, 2)
   // holds partitions to kMaxPartTokens tokens)
   for (int j = first_blk + tid; j <= last_blk; j += kTThreads) {
     const int32_t p = bt[j];
-    if (p < 0 || p >= a.num_blocks) sh_bad = 1;
+    const bool ok = p >= 0 && p < a.num_blocks;
+    if (!ok) sh_bad = 1;
     blk_ids[j - first_blk] = p;
+    if constexpr (kQ8) {
+      if (ok) {
+        blk_ks[j - first_blk] = a.k_scale[(int64_t)p * Hkv + hk];
+        const float vs = a.v_scale[(int64_t)p * Hkv + hk];
+        blk_vs[j - first_blk] = vs;
+        atomicMax(reinterpret_cast<int*>(&sh_vmax), __float_as_int(fabsf(vs)));
+      }
+    }
   }
   // This thread's row (softmax warps): (query token, grouped head)
   const int r = row0 + tid;                              // meaningful for tid < 128
@@ -340,13 +450,43 @@ __global__ void __launch_bounds__(kTThreads, 2)
   // Q row into its swizzled bands (zeros for rows past the sequence's
   // queries).  A negative scale flips Q's signs instead (exact), so that the
   // softmax below scales S by |scale| and may take maxima of raw scores.
-  const float sl2 = fabsf(a.scale_log2);
+  float sl2 = fabsf(a.scale_log2);
   if (tid < kTRows) {
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) + qrow * D);
     const uint32_t flip = a.scale_log2 < 0.0f ? 0x80008000u : 0u;
+    float qscale = 1.0f;
+    if constexpr (kQ8) {
+      // fp16 holds |q| < 65504: rows with a larger entry are scaled by a
+      // power of two, undone in the score scale (exact either way)
+      float amax = 0.0f;
+      for (int c = 0; c < D / 8 && row_valid; ++c) {
+        const uint4 v = src[c];
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w4[i] << 16)),
+                                   fabsf(__uint_as_float(w4[i] & 0xffff0000u))));
+      }
+      int e = 0;
+      if (amax >= 16384.0f) {
+        frexpf(amax, &e);
+        e -= 14;
+      }
+      qscale = ldexpf(1.0f, -e);
+      sl2 = sl2 / qscale;
+    }
 #pragma unroll
     for (int c = 0; c < D / 8; ++c) {
       uint4 v = row_valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+      if constexpr (kQ8) {
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o4[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          o4[i] = pack2<true>(__uint_as_float(w4[i] << 16) * qscale,
+                              __uint_as_float(w4[i] & 0xffff0000u) * qscale);
+        v = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+      }
       v.x ^= flip;
       v.y ^= flip;
       v.z ^= flip;
@@ -363,6 +503,8 @@ __global__ void __launch_bounds__(kTThreads, 2)
     mbar_init(smem_addr(&p_bar), kTRows);
     mbar_init(smem_addr(&o_bar), 1);
     mbar_init(smem_addr(&drain_bar), 1);
+    mbar_init(smem_addr(&k_conv), 1);
+    mbar_init(smem_addr(&v_conv), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   const bool work = nch > 0;
@@ -390,11 +532,14 @@ __global__ void __launch_bounds__(kTThreads, 2)
       // S/P buffer; then P . V(c) once P(c) is written.  (The second CTA on
       // the SM keeps the tensor core busy while this one runs its softmax.)
       bool ok = true;
-      const uint32_t id_s = mma_idesc(kTRows, kChunk, 0);
-      const uint32_t id_o = mma_idesc(kTRows, D, 1);
+      const uint32_t id_s = mma_idesc<kQ8>(kTRows, kChunk, 0);
+      const uint32_t id_o = mma_idesc<kQ8>(kTRows, D, 1);
       const uint32_t s_tmem = tm + T::kSCol;
+      // 8-bit pools: the operands are ready once the load warp has widened them
+      const uint32_t k_ready = smem_addr(kQ8 ? &k_conv : &k_full);
+      const uint32_t v_ready = smem_addr(kQ8 ? &v_conv : &v_full);
       for (int c = 0; c < nch && ok; ++c) {
-        if (!warp_wait(smem_addr(&k_full), c & 1)) { ok = false; break; }
+        if (!warp_wait(k_ready, c & 1)) { ok = false; break; }
         if (c >= 1 && !warp_wait(smem_addr(&o_bar), (c - 1) & 1)) { ok = false; break; }
         if (lane == 0) {
           tc_fence_after();
@@ -408,10 +553,11 @@ __global__ void __launch_bounds__(kTThreads, 2)
           mma_commit(smem_addr(&k_empty));
         }
         __syncwarp();
-        if (!warp_wait(smem_addr(&v_full), c & 1)) { ok = false; break; }
-        // V rows at or past the sequence end in this chunk -> 0 (every band)
+        if (!warp_wait(v_ready, c & 1)) { ok = false; break; }
+        // V rows at or past the sequence end in this chunk -> 0 (every band;
+        // 8-bit pools: done while widening)
         const int cstart = t0 + c * kChunk;
-        if (L < cstart + kChunk && L > cstart && (L % BS) != 0) {
+        if (!kQ8 && L < cstart + kChunk && L > cstart && (L % BS) != 0) {
           const int row_lo = L - cstart, row_hi = min(kChunk, ((L + BS - 1) / BS) * BS - cstart);
           const int nrow = row_hi - row_lo;
           for (int i = lane; i < nrow * 8 * T::kAtoms; i += 32) {
@@ -449,19 +595,63 @@ __global__ void __launch_bounds__(kTThreads, 2)
         mbar_expect_tx(bar, (uint32_t)(nb * Gm::kTensorBytes));
         for (int j = 0; j < nb; ++j) {
           const int p = blk_ids[blk0 - first_blk + j];
+          if constexpr (kQ8) {
+            // codes of rows j*BS .. j*BS + BS - 1 into the image's second half
+            tma_load_4d(img + D * kChunk + j * (BS * D), map, bar, 0, hk, 0, p);
+          } else {
 #pragma unroll
-          for (int xx = 0; xx < Gm::kBoxes; ++xx)
-            // band xx of the chunk image, rows j*BS .. j*BS + BS - 1
-            tma_load_4d(img + xx * (kChunk * 128) + j * (BS * 128), map, bar, xx * Gm::kBoxElems, hk, 0, p);
+            for (int xx = 0; xx < Gm::kBoxes; ++xx)
+              // band xx of the chunk image, rows j*BS .. j*BS + BS - 1
+              tma_load_4d(img + xx * (kChunk * 128) + j * (BS * 128), map, bar, xx * Gm::kBoxElems, hk, 0, p);
+          }
         }
       };
-      for (int c = 0; c < nch; ++c) {
-        if (c >= 1 && !warp_wait(smem_addr(&k_empty), (c - 1) & 1)) { ok = false; break; }
-        if (lane == 0) load(&k_map, k_img, smem_addr(&k_full), c);
-        k_issued = c + 1;
-        if (c >= 1 && !warp_wait(smem_addr(&v_empty), (c - 1) & 1)) { ok = false; break; }
-        if (lane == 0) load(&v_map, v_img, smem_addr(&v_full), c);
-        v_issued = c + 1;
+      if constexpr (!kQ8) {
+        for (int c = 0; c < nch; ++c) {
+          if (c >= 1 && !warp_wait(smem_addr(&k_empty), (c - 1) & 1)) { ok = false; break; }
+          if (lane == 0) load(&k_map, k_img, smem_addr(&k_full), c);
+          k_issued = c + 1;
+          if (c >= 1 && !warp_wait(smem_addr(&v_empty), (c - 1) & 1)) { ok = false; break; }
+          if (lane == 0) load(&v_map, v_img, smem_addr(&v_full), c);
+          v_issued = c + 1;
+        }
+      } else {
+        // 8-bit: widen each chunk after it lands, K one chunk ahead (K(c+1)
+        // as soon as S(c) has read the K image, during the softmax of c),
+        // V(c) before P . V(c); then the MMA warp is released.
+        auto rows_of = [&](int c) {                      // rows of the chunk's loaded blocks
+          const int blk0 = first_blk + c * kBlocksPerChunk;
+          return min(kBlocksPerChunk, last_blk - blk0 + 1) * BS;
+        };
+        auto widen = [&](uint32_t img, uint32_t full, uint32_t ready, int c, int zero_from) {
+          if (!warp_wait(full, c & 1)) return false;
+          widen_chunk<D, kFp8>(gbase + (img - base), rows_of(c), zero_from, lane);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // fp16 -> tensor core
+          __syncwarp();
+          if (lane == 0) mbar_arrive(ready);
+          return true;
+        };
+        if (lane == 0) {
+          load(&k_map, k_img, smem_addr(&k_full), 0);
+          load(&v_map, v_img, smem_addr(&v_full), 0);
+        }
+        k_issued = v_issued = 1;
+        __syncwarp();
+        ok = widen(k_img, smem_addr(&k_full), smem_addr(&k_conv), 0, kChunk);
+        for (int c = 0; c < nch && ok; ++c) {
+          const int cstart = t0 + c * kChunk;
+          if (!(ok = widen(v_img, smem_addr(&v_full), smem_addr(&v_conv), c, L - cstart))) break;
+          if (c + 1 >= nch) break;
+          if (!(ok = warp_wait(smem_addr(&k_empty), c & 1))) break;
+          if (lane == 0) load(&k_map, k_img, smem_addr(&k_full), c + 1);
+          k_issued = c + 2;
+          __syncwarp();
+          if (!(ok = widen(k_img, smem_addr(&k_full), smem_addr(&k_conv), c + 1, kChunk))) break;
+          if (!(ok = warp_wait(smem_addr(&v_empty), c & 1))) break;
+          if (lane == 0) load(&v_map, v_img, smem_addr(&v_full), c + 1);
+          v_issued = c + 2;
+          __syncwarp();
+        }
       }
       if (!ok && lane == 0) sh_fail = 1;
       // every load issued has landed before the CTA moves on (bounded)
@@ -499,15 +689,36 @@ __global__ void __launch_bounds__(kTThreads, 2)
         const bool masked = __any_sync(0xffffffffu, cstart + kChunk - 1 > lim);
         uint32_t raw[kH][32];
         float mx_raw = -INFINITY;
+        // 8-bit pools: per-key factors of each 32-key group of a pass, the K
+        // scale of the key's block times the score scale (scores then leave
+        // the passes already in log2 units) and its relative V scale
+        auto key_factors = [&](int ps, float (&kf)[kH][2], float (&vf)[kH][2]) {
+          const float inv_vmax = sh_vmax > 0.0f ? 1.0f / sh_vmax : 1.0f;
+#pragma unroll
+          for (int h = 0; h < kH; ++h)
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              const int jb = (c * kChunk + 64 * ps + 32 * h + 16 * half) / BS;   // < kMaxPartBlocks
+              kf[h][half] = blk_ks[jb] * sl2;
+              vf[h][half] = blk_vs[jb] * inv_vmax;
+            }
+        };
 #pragma unroll
         for (int ps = 0; ps < kPasses; ++ps) {
 #pragma unroll
           for (int h = 0; h < kH; ++h) tmem_ld32(s_tmem + 64 * ps + 32 * h, raw[h]);
           tmem_wait_ld();
+          if constexpr (kQ8) {
+            float kf[kH][2], vf[kH][2];
+            key_factors(ps, kf, vf);
+#pragma unroll
+            for (int h = 0; h < kH; ++h) scale_keys(raw[h], kf[h]);
+          }
           const int first = cstart + 64 * ps;
           mx_raw = fmaxf(mx_raw, masked ? chunk_max<true>(raw, first, lim) : chunk_max<false>(raw, first, lim));
         }
-        const float mx = mx_raw == -INFINITY ? -INFINITY : mx_raw * sl2;
+        const float sl2c = kQ8 ? 1.0f : sl2;             // (8-bit: already applied)
+        const float mx = mx_raw == -INFINITY ? -INFINITY : mx_raw * sl2c;
         // move the reference maximum only when it is passed by > 2^8
         const bool need = m_ref == -INFINITY ? mx > -INFINITY : mx > m_ref + kRescaleLog2;
         const float m_new = need ? mx : m_ref;
@@ -537,10 +748,16 @@ __global__ void __launch_bounds__(kTThreads, 2)
 #pragma unroll
           for (int h = 0; h < kH; ++h) tmem_ld32(s_tmem + 64 * ps + 32 * h, raw[h]);
           tmem_wait_ld();
+          float kf[kH][2], vf[kH][2] = {};
+          if constexpr (kQ8) {
+            key_factors(ps, kf, vf);
+#pragma unroll
+            for (int h = 0; h < kH; ++h) scale_keys(raw[h], kf[h]);
+          }
           const int first = cstart + 64 * ps;
           uint32_t pw[kH][16];
-          lsum += masked ? chunk_exp<true>(raw, pw, first, lim, sl2, zero_ref)
-                         : chunk_exp<false>(raw, pw, first, lim, sl2, zero_ref);
+          lsum += masked ? chunk_exp<true, kQ8>(raw, pw, first, lim, sl2c, zero_ref, vf)
+                         : chunk_exp<false, kQ8>(raw, pw, first, lim, sl2c, zero_ref, vf);
           // P (bf16 pairs) of these 64 keys: packed columns [32 ps, 32 ps + 32)
 #pragma unroll
           for (int h = 0; h < kH; ++h) tmem_st16(s_tmem + 32 * ps + 16 * h, pw[h]);
@@ -575,7 +792,9 @@ __global__ void __launch_bounds__(kTThreads, 2)
     const bool split = kPrefix || a.max_parts > 1;
     const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
     const bool have = work && !failed;                   // CTA-uniform
-    const float inv = (have && l > 0.0f) ? 1.0f / l : 0.0f;
+    // 8-bit pools: P carried V scales relative to the partition's largest
+    const float oscale = kQ8 ? (sh_vmax > 0.0f ? sh_vmax : 1.0f) : 1.0f;
+    const float inv = (have && l > 0.0f) ? oscale / l : 0.0f;
     // prefix partials sit after the row's max_parts decode partitions
     const int64_t slot = kPrefix ? orow * a.slots + a.max_parts + part : orow * a.max_parts + part;
     if (split && mine_row) {
@@ -611,8 +830,8 @@ __global__ void __launch_bounds__(kTThreads, 2)
 #pragma unroll
         for (int j = 0; j < 32; j += 4)
           *reinterpret_cast<float4*>(acc + j) =
-              make_float4(__uint_as_float(ov[j]), __uint_as_float(ov[j + 1]),
-                          __uint_as_float(ov[j + 2]), __uint_as_float(ov[j + 3]));
+              make_float4(__uint_as_float(ov[j]) * oscale, __uint_as_float(ov[j + 1]) * oscale,
+                          __uint_as_float(ov[j + 2]) * oscale, __uint_as_float(ov[j + 3]) * oscale);
       }
     }
   }
@@ -629,6 +848,8 @@ __global__ void __launch_bounds__(kTThreads, 2)
     mbar_inval(smem_addr(&p_bar));
     mbar_inval(smem_addr(&o_bar));
     mbar_inval(smem_addr(&drain_bar));
+    mbar_inval(smem_addr(&k_conv));
+    mbar_inval(smem_addr(&v_conv));
   }
   }  // units
   tc_fence_before();
@@ -639,7 +860,7 @@ __global__ void __launch_bounds__(kTThreads, 2)
 }
 
 
-template <int D, int BS, bool kPrefix>
+template <int D, int BS, bool kPrefix, int kKind>
 kv_status launch_tc(const DecodeArgs& a, int ctas, cudaStream_t s) {
   using T = TcGeo<D>;
   static std::mutex mu;
@@ -650,22 +871,38 @@ kv_status launch_tc(const DecodeArgs& a, int ctas, cudaStream_t s) {
   {
     std::lock_guard<std::mutex> lock(mu);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-      st = cuda_check(cudaFuncSetAttribute(multi_tc_kernel<D, BS, kPrefix>,
+      st = cuda_check(cudaFuncSetAttribute(multi_tc_kernel<D, BS, kPrefix, kKind>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmemBytes),
                       "cudaFuncSetAttribute(multi_tc_kernel)");
       if (st != KV_OK) return st;
       attr_set[dev] = true;
     }
   }
-  alignas(64) CUtensorMap km, vm;
+  CUtensorMap km, vm;
   if ((st = make_kv_maps(a, &km, &vm)) != KV_OK) return st;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)ctas);
   cfg.blockDim = dim3(kTThreads);
   cfg.dynamicSmemBytes = T::kSmemBytes;
   cfg.stream = s;
-  return cuda_check(cudaLaunchKernelEx(&cfg, multi_tc_kernel<D, BS, kPrefix>, km, vm, a),
+  return cuda_check(cudaLaunchKernelEx(&cfg, multi_tc_kernel<D, BS, kPrefix, kKind>, km, vm, a),
                     "multi_tc_kernel launch");
+}
+
+template <bool kPrefix, int kKind>
+kv_status launch_tc_geo(const DecodeArgs& a, int ctas, cudaStream_t s) {
+  if (a.head_dim == 128)
+    return a.block_size == 32 ? launch_tc<128, 32, kPrefix, kKind>(a, ctas, s)
+                              : launch_tc<128, 16, kPrefix, kKind>(a, ctas, s);
+  return a.block_size == 32 ? launch_tc<64, 32, kPrefix, kKind>(a, ctas, s)
+                            : launch_tc<64, 16, kPrefix, kKind>(a, ctas, s);
+}
+
+template <bool kPrefix>
+kv_status launch_tc_kind(const DecodeArgs& a, int ctas, cudaStream_t s) {
+  if (a.dtype == KV_DTYPE_INT8) return launch_tc_geo<kPrefix, KV_DTYPE_INT8>(a, ctas, s);
+  if (a.dtype == KV_DTYPE_FP8_E4M3) return launch_tc_geo<kPrefix, KV_DTYPE_FP8_E4M3>(a, ctas, s);
+  return launch_tc_geo<kPrefix, KV_DTYPE_BF16>(a, ctas, s);
 }
 
 }  // namespace
@@ -673,23 +910,17 @@ kv_status launch_tc(const DecodeArgs& a, int ctas, cudaStream_t s) {
 kv_status launch_multi_tc(const DecodeArgs& a, int ctas, cudaStream_t s) {
   if (a.part_tokens > kMaxPartTokens || a.part_tokens % kChunk || ctas <= 0)
     return fail(KV_ERR_INVALID_ARG, "paged_attention_multi: bad tensor-core launch");
-  if (a.head_dim == 128)
-    return a.block_size == 32 ? launch_tc<128, 32, false>(a, ctas, s) : launch_tc<128, 16, false>(a, ctas, s);
-  return a.block_size == 32 ? launch_tc<64, 32, false>(a, ctas, s) : launch_tc<64, 16, false>(a, ctas, s);
+  return launch_tc_kind<false>(a, ctas, s);
 }
 
 kv_status launch_prefix_tc(const DecodeArgs& a, int ctas, cudaStream_t s) {
-  if (a.dtype != KV_DTYPE_BF16)
-    return fail(KV_ERR_NOT_IMPLEMENTED, "the shared-prefix path supports bf16 pools only");
   if (a.prefix_part_tokens <= 0 || a.prefix_part_tokens > kMaxPartTokens ||
       a.prefix_part_tokens % kChunk || a.prefix_chunks < 1 ||
       (int64_t)a.prefix_chunks * a.prefix_part_tokens < (int64_t)a.num_prefix_blocks * a.block_size ||
       (int64_t)(a.prefix_chunks - 1) * a.prefix_part_tokens >= (int64_t)a.num_prefix_blocks * a.block_size ||
       ctas <= 0)
     return fail(KV_ERR_INVALID_ARG, "shared prefix: bad tensor-core launch");
-  if (a.head_dim == 128)
-    return a.block_size == 32 ? launch_tc<128, 32, true>(a, ctas, s) : launch_tc<128, 16, true>(a, ctas, s);
-  return a.block_size == 32 ? launch_tc<64, 32, true>(a, ctas, s) : launch_tc<64, 16, true>(a, ctas, s);
+  return launch_tc_kind<true>(a, ctas, s);
 }
 
 }  // namespace pagedkv

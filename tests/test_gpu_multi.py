@@ -71,6 +71,17 @@ CASES = {
     # one query head, 43 tokens: with 3 partitions the (m, l) region holds 258
     # floats, so the acc region is 16-byte aligned only by its rounding
     "odd_rows_mha": lambda: multi([300, 700, 37], [41, 1, 1], hq=1, hkv=1, d=64, seed=48),
+    # long queries on 8-bit pools: the tensor-core kernel widens the codes to fp16
+    "row_int8_g4_d64": lambda: multi([20, 300, 1500], [2, 9, 200], hq=8, hkv=2, d=64, kv="int8",
+                                     seed=50),
+    "row_fp8_g8_d128_bs32": lambda: multi([33, 700, 2600], [9, 130, 1], hq=64, hkv=8, d=128, bs=32,
+                                          kv="fp8", seed=51),
+    "row_int8_g4_prefill_chunk": lambda: multi([3000, 40, 2000], [512, 1, 1], hq=32, hkv=8, d=128,
+                                               kv="int8", seed=52),
+    "row_fp8_mha_d64_bs32": lambda: multi([70, 600], [70, 16], hq=4, hkv=4, d=64, bs=32, kv="fp8",
+                                          seed=53),
+    "row_int8_g2_d128_bs32": lambda: multi([129, 1000, 5], [129, 40, 5], hq=4, hkv=2, d=128, bs=32,
+                                           kv="int8", seed=54),
 }
 
 
@@ -134,17 +145,6 @@ def test_bad_sequence_is_flagged_and_zeroed(qlens):
     assert not out[e:].any() and out[:e].any()
 
 
-@pytest.mark.parametrize("kv", ["int8", "fp8"])
-def test_multi_rejects_long_queries_on_8bit_pools(kv):
-    """8-bit pools take at most 4 x (8 / G) query tokens per sequence."""
-    wl = workloads.custom(batch=2, num_q_heads=8, num_kv_heads=2, head_dim=64, block_size=16,
-                          seq_lens=[20, 30], kv_dtype=kv, seed=40, query_lens=[2, 9])
-    g = GpuStep(wl)
-    with pytest.raises(pkv.KVError) as e:
-        g.attend_multi()
-    assert e.value.status == pkv.KV_ERR_NOT_IMPLEMENTED
-
-
 def sub_problem(wl, seqs):
     """The oracle inputs restricted to sequences `seqs` (tables, lengths,
     their q rows and offsets); the pool keeps its physical ids."""
@@ -154,9 +154,9 @@ def sub_problem(wl, seqs):
     return rows, wl.q[rows], wl.block_tables[seqs], wl.seq_lens[seqs], qs
 
 
-@pytest.mark.parametrize("cfg", [7, 8])
-def test_full_size_multi_workload_sampled_sequences(cfg):
-    wl = workloads.make(cfg)
+@pytest.mark.parametrize("cfg,kv", [(7, "bf16"), (8, "bf16"), (8, "int8"), (8, "fp8")])
+def test_full_size_multi_workload_sampled_sequences(cfg, kv):
+    wl = workloads.make(cfg, kv_dtype=kv)
     g = GpuStep(wl)
     got = out_f64(g.multi_step())
     torch.cuda.synchronize()
@@ -165,11 +165,12 @@ def test_full_size_multi_workload_sampled_sequences(cfg):
     L = wl.seq_lens
     rng = np.random.default_rng(cfg)
     seqs = sorted({0, int(np.argmax(L)), int(np.argmin(L)), int(rng.integers(len(L)))})
-    kc, vc, _, _ = oracle_pool(wl, seqs=seqs)
+    kc, vc, ks, vs = oracle_pool(wl, seqs=seqs)
     rows, q, bt, sl, qs = sub_problem(wl, seqs)
-    ref, rc = oracle.paged_attention_multi(q, kc, vc, bt, sl, qs, wl.spec.scale, threads=os.cpu_count())
+    ref, rc = oracle.paged_attention_multi(q, kc, vc, bt, sl, qs, wl.spec.scale, k_scale=ks,
+                                           v_scale=vs, threads=os.cpu_count())
     assert rc == 0
-    check(got[rows], ref, f"workload {cfg}")
+    check(got[rows], ref, f"workload {cfg}, {kv} pools", kv)
 
 
 @pytest.mark.parametrize("scale", [-0.125, 0.0, 1.0], ids=["negative", "zero", "sharp"])

@@ -265,6 +265,17 @@ PREFIX_CASES = {
     # two partials of 1152 tokens over 65 blocks of 32, G = 8
     "g8_d64_bs32_prefix_2080": lambda: small([2081, 2100, 3000], hq=16, hkv=2, d=64, bs=32,
                                              prefix=2080, seed=36),
+    # 8-bit pools: the prefix product widens the codes to fp16
+    "int8_g4_d128_bs16": lambda: small([33, 48, 49, 300, 1000, 2100], hq=32, hkv=8, d=128, prefix=32,
+                                       kv="int8", seed=37),
+    "fp8_g4_d128_bs16": lambda: small([33, 48, 49, 300, 1000, 2100], hq=32, hkv=8, d=128, prefix=32,
+                                      kv="fp8", seed=38),
+    "int8_g8_d64_bs32_prefix_2080": lambda: small([2081, 2100, 3000], hq=16, hkv=2, d=64, bs=32,
+                                                  prefix=2080, kv="int8", seed=39),
+    "fp8_g2_d64_bs16_long_prefix": lambda: small([600, 601, 640, 1200, 3000, 610], hq=4, hkv=2, d=64,
+                                                 prefix=592, kv="fp8", seed=40),
+    "fp8_g1_d128_bs32": lambda: small([33, 40, 333], hq=4, hkv=4, d=128, bs=32, prefix=32, kv="fp8",
+                                      seed=41),
 }
 
 
@@ -279,11 +290,11 @@ def test_prefix_step_matches_oracle(case):
     np.testing.assert_array_equal(bits_of(g.k_cache), kc)          # the append, bit for bit
     np.testing.assert_array_equal(bits_of(g.v_cache), vc)
     ref, rc = oracle.paged_attention(wl.q, kc, vc, wl.block_tables, wl.seq_lens, wl.spec.scale,
-                                     threads=os.cpu_count())
+                                     k_scale=ks, v_scale=vs, threads=os.cpu_count())
     assert rc == 0
-    assert_close(got, ref, "bf16", case)
+    assert_close(got, ref, wl.spec.kv_dtype, case)
     plain = out_f64(GpuStep(wl).fused_step())
-    assert_close(got, plain, "bf16", case + " vs plain step")
+    assert_close(got, plain, wl.spec.kv_dtype, case + " vs plain step")
 
 
 def test_prefix_attend_only_and_repeat():
@@ -307,21 +318,11 @@ def test_prefix_mismatch_is_flagged_and_zeroed():
     assert not out[2].any() and out[0].any() and out[3].any()
 
 
-@pytest.mark.parametrize("kv", ["int8", "fp8"])
-def test_prefix_rejects_8bit_pools(kv):
-    wl = small([65, 90], hq=64, hkv=8, d=128, bs=32, kv=kv, seed=35)
-    g = GpuStep(wl)
-    pb = g.block_tables[0, :1].contiguous()
-    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
-    with pytest.raises(pkv.KVError) as e:
-        pkv.decode_step_prefix(g.out, g.q, None, None, g.k_cache, g.v_cache, g.block_tables,
-                               g.seq_lens, g.max_seq_len, wl.spec.scale, pb, ws, k_scale=g.k_scale,
-                               v_scale=g.v_scale)
-    assert e.value.status == pkv.KV_ERR_NOT_IMPLEMENTED
-
-
-def test_full_size_shared_prefix_workload_sampled_rows():
-    wl = workloads.make(4)
+@pytest.mark.parametrize("kv", ["bf16", "int8", "fp8"])
+def test_full_size_shared_prefix_workload_sampled_rows(kv):
+    """256 sequences behind an 800-token shared prefix on bf16, int8 and E4M3
+    pools, through the shared-prefix path."""
+    wl = workloads.make(4, kv_dtype=kv)
     g = GpuStep(wl)
     got = out_f64(g.prefix_step())
     torch.cuda.synchronize()
@@ -329,9 +330,10 @@ def test_full_size_shared_prefix_workload_sampled_rows():
     seqs, rows = sample_rows(wl)
     kc, vc, ks, vs = oracle_pool(wl, seqs=seqs)
     ref, rc = oracle.paged_attention(wl.q, kc, vc, wl.block_tables, wl.seq_lens, wl.spec.scale,
-                                     rows=rows, threads=os.cpu_count())
+                                     k_scale=ks, v_scale=vs, rows=rows, threads=os.cpu_count())
     assert rc == 0
-    assert_close(got[rows[:, 0], rows[:, 1]], ref, "bf16", "256 sequences behind an 800-token prefix, shared-prefix path")
+    assert_close(got[rows[:, 0], rows[:, 1]], ref, kv,
+                 f"256 sequences behind an 800-token prefix, {kv} pools, shared-prefix path")
 
 
 # ---------------------------------------------------------------------------
@@ -476,3 +478,19 @@ def test_full_size_config_sampled_rows(cfg):
         blk, row = divmod(int(slots[b]), wl.spec.block_size)
         np.testing.assert_array_equal(bits_of(g.k_cache[blk, row]), kc[blk, row])
         np.testing.assert_array_equal(bits_of(g.v_cache[blk, row]), vc[blk, row])
+
+
+@pytest.mark.parametrize("case", ["ragged_g4_d128", "g8_int8_bs32", "fp8_d64_bs16"])
+def test_decode_step_plan_equals_decode_step(case):
+    """A prepared DecodeStepPlan (arguments checked and marshalled once) runs
+    the same step as decode_step: outputs and pools bit-identical."""
+    wl = CASES[case]()
+    a, b = GpuStep(wl), GpuStep(wl)
+    out_plan = bits_of(a.fused_step()).copy()
+    pkv.decode_step(b.out, b.q, b.new_k, b.new_v, b.k_cache, b.v_cache, b.block_tables, b.seq_lens,
+                    b.max_seq_len, wl.spec.scale, b.workspace, k_scale=b.k_scale, v_scale=b.v_scale)
+    torch.cuda.synchronize()
+    check_status()
+    np.testing.assert_array_equal(bits_of(b.out), out_plan)
+    np.testing.assert_array_equal(bits_of(a.k_cache), bits_of(b.k_cache))
+    np.testing.assert_array_equal(bits_of(a.v_cache), bits_of(b.v_cache))

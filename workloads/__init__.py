@@ -44,7 +44,7 @@ from __future__ import annotations
 import math
 import os
 from concurrent.futures import ThreadPoolExecutor
-from dataclasses import dataclass
+from dataclasses import dataclass, replace
 from typing import Callable, Iterable, Iterator, Optional, Sequence
 
 import numpy as np
@@ -311,28 +311,36 @@ class Workload:
     def scales(self, seqs: Optional[Sequence[int]] = None):
         """fp32 k_scale, v_scale [NB, Hkv]: max |x| / 127 (int8) or / 448
         (E4M3) over the bf16 values (cached plus new) that land in each
-        (block, KV head); 1.0 elsewhere."""
+        (block, KV head), the shared prefix's blocks included; 1.0 elsewhere."""
         s = self.spec
         NB, H, bs = self.num_blocks, s.num_kv_heads, s.block_size
         ks = np.ones((NB, H), np.float32)
         vs = np.ones((NB, H), np.float32)
         seqs = range(s.batch) if seqs is None else seqs
-        assert s.shared_prefix_tokens == 0, "8-bit workloads have no shared prefix"
+        P = s.shared_prefix_tokens
+        assert P % bs == 0, "a shared prefix fills whole blocks"
         top = np.float32(CODE_MAX[s.kv_dtype])
+
+        def put(rows_k, rows_v, phys):
+            # rows [n, H, d] fp32 of whole blocks phys (zero-padded at the end)
+            n = len(phys) * bs
+            pad = ((0, n - rows_k.shape[0]), (0, 0), (0, 0))
+            kmax = np.abs(np.pad(rows_k, pad)).reshape(len(phys), bs, H, -1).max(axis=(1, 3))
+            vmax = np.abs(np.pad(rows_v, pad)).reshape(len(phys), bs, H, -1).max(axis=(1, 3))
+            ks[phys] = np.where(kmax > 0, kmax / top, np.float32(1.0))
+            vs[phys] = np.where(vmax > 0, vmax / top, np.float32(1.0))
+
+        if P:
+            pk, pv = self._prefix_kv()
+            first = min(seqs) if len(seqs) else 0
+            put(bf16_bits_to_f32(pk), bf16_bits_to_f32(pv), self.block_tables[first, :P // bs])
         for b, (pos, k, v) in zip(seqs, ordered_map(self.own_tokens, seqs, default_workers())):
             L = int(self.seq_lens[b])
             nk, nv = self.new_kv_of(b)
             kf = np.concatenate([bf16_bits_to_f32(k), bf16_bits_to_f32(nk)])
             vf = np.concatenate([bf16_bits_to_f32(v), bf16_bits_to_f32(nv)])
             nblk = (L + bs - 1) // bs
-            pad = nblk * bs - L
-            kf = np.abs(np.concatenate([kf, np.zeros((pad,) + kf.shape[1:], np.float32)]))
-            vf = np.abs(np.concatenate([vf, np.zeros((pad,) + vf.shape[1:], np.float32)]))
-            kmax = kf.reshape(nblk, bs, H, -1).max(axis=(1, 3))
-            vmax = vf.reshape(nblk, bs, H, -1).max(axis=(1, 3))
-            phys = self.block_tables[b, :nblk]
-            ks[phys] = np.where(kmax > 0, kmax / top, np.float32(1.0))
-            vs[phys] = np.where(vmax > 0, vmax / top, np.float32(1.0))
+            put(kf, vf, self.block_tables[b, P // bs:nblk])
         return ks, vs
 
     # -- byte accounting -----------------------------------------------------
@@ -349,8 +357,13 @@ class Workload:
         return toks * 2 * s.num_kv_heads * s.head_dim * self.kv_elem_bytes
 
 
-def make(config: int, seed: Optional[int] = None, seq_lens=None) -> Workload:
+def make(config: int, seed: Optional[int] = None, seq_lens=None,
+         kv_dtype: Optional[str] = None) -> Workload:
+    """Workload `config`; with kv_dtype, the same shapes, lengths and values
+    on a pool of that type ("bf16", "int8" or "fp8")."""
     spec = CONFIGS[config]
+    if kv_dtype is not None and kv_dtype != spec.kv_dtype:
+        spec = replace(spec, kv_dtype=kv_dtype, name=f"{spec.name}, {kv_dtype} KV")
     return Workload(spec, SEED_BASE + config if seed is None else seed, seq_lens)
 
 
