@@ -398,13 +398,14 @@ def eager_us(step_fn, stream, dev, n=50):
     return e0.elapsed_time(e1) / n * 1e3
 
 
-def measure_config(config, pkv, dev, stream, peak, peak_kind, replays=40):
+def measure_config(config, pkv, dev, stream, peak, peak_kind, replays=40, kv_dtype=None):
     """One decode workload's step (the fused decode step; the shared-prefix
     step where the workload has a shared prefix), timed like the headline:
-    GRAPH_STEPS steps captured in one CUDA graph, replayed."""
+    GRAPH_STEPS steps captured in one CUDA graph, replayed.  kv_dtype: the
+    same workload on a pool of another type."""
     import torch
     from paged_kv_cache_97_gb300.batch import DecodeBatch
-    wl = workloads.make(config)
+    wl = workloads.make(config, kv_dtype=kv_dtype)
     g = DecodeBatch(wl, dev=dev)
     plan = StepPlan(wl, g, pkv)
     graph = capture(plan.fn, dev)
@@ -564,13 +565,13 @@ def multi_step_bytes(wl) -> int:
             + int(((wl.seq_lens + s.block_size - 1) // s.block_size).sum()) * 4)
 
 
-def measure_multi(config, pkv, dev, stream, peak, replays=40):
+def measure_multi(config, pkv, dev, stream, peak, replays=40, kv_dtype=None):
     """A multi-token workload's step (append of every query token through
     the general slot mapping + paged_attention_multi), timed like the
     headline: GRAPH_STEPS steps captured in one CUDA graph, replayed."""
     import torch
     from paged_kv_cache_97_gb300.batch import DecodeBatch
-    wl = workloads.make(config)
+    wl = workloads.make(config, kv_dtype=kv_dtype)
     g = DecodeBatch(wl, dev=dev)
     plan = StepPlan(wl, g, pkv)
     graph = capture(plan.fn, dev)
@@ -783,6 +784,14 @@ def gpu_arm(args, rank, world, local_rank, dist):
                         "fp8_kv": measure_config(6, pkv, dev, stream, peak, peak_kind),
                         "multi_token": {"speculative_verification": measure_multi(7, pkv, dev, stream, peak),
                                         "decode_maximal_batch": measure_multi(8, pkv, dev, stream, peak)},
+                        # the tensor-core paths (shared prefix, long queries) on 8-bit pools
+                        "kv8_tensor_core": {
+                            "shared_prefix_int8": measure_config(4, pkv, dev, stream, peak, peak_kind,
+                                                                 kv_dtype="int8"),
+                            "shared_prefix_fp8": measure_config(4, pkv, dev, stream, peak, peak_kind,
+                                                                kv_dtype="fp8"),
+                            "decode_maximal_batch_int8": measure_multi(8, pkv, dev, stream, peak,
+                                                                       kv_dtype="int8")},
                         "cow": measure_cow(pkv, dev, stream, peak)}
     return line, wl
 

@@ -547,13 +547,14 @@ static kv_status decode_common(void* out, const void* q, const void* new_k, cons
     // CTAs, enough loads in flight to keep its share of HBM bandwidth).
     // Workload of 256 sequences behind an 800-token prefix: 38 CTAs 123.4 us
     // per step, 76 CTAs 123.8, 152 CTAs 128.5, 304 CTAs 130.3 (three partials).
+    // (units: pairs of 128-row tiles x KV heads x prefix partials; one CTA per SM)
     const int G = num_q_heads / num_kv_heads;
-    const int64_t units = (int64_t)((batch * G + 127) / 128) * num_kv_heads * a.prefix_chunks;
-    const int64_t chunks = units * (a.prefix_part_tokens / 128);
+    const int64_t units = (int64_t)((batch * G + 255) / 256) * num_kv_heads * a.prefix_chunks;
+    const int64_t chunks = units * 2 * (a.prefix_part_tokens / 128);
     int64_t ctas = (chunks + 15) / 16;
     const int64_t quarter = di.num_sms / 4 > 0 ? di.num_sms / 4 : 1;
     if (ctas < quarter) ctas = quarter;
-    if (ctas > 2LL * di.num_sms) ctas = 2LL * di.num_sms;
+    if (ctas > di.num_sms) ctas = di.num_sms;
     if (ctas > units) ctas = units;
     if ((st = launch_prefix_tc(a, (int)ctas, s)) != KV_OK) return st;
   }

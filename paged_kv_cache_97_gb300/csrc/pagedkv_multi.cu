@@ -300,8 +300,8 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
     a.ws_acc = a.ws_ml + ml_region_floats((size_t)num_tokens * num_q_heads, a.max_parts);
   }
   cudaStream_t s = (cudaStream_t)stream;
-  // Persistent tensor-core CTAs, two per SM (measured best both beside the
-  // column groups and alone), never more than the units.
+  // Persistent tensor-core CTAs, one per SM (each takes the whole TMEM),
+  // never more than the units (pairs of row tiles <= tiles).
   auto tc_ctas = [&](int per_sm) {
     return (int)std::min<int64_t>(tiles * num_kv_heads * a.max_parts, (int64_t)di.num_sms * per_sm);
   };
@@ -311,7 +311,7 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
     if ((st = side_lane(di.device, &lane)) != KV_OK ||
         (st = cuda_check(cudaEventRecord(lane->fork, s), "cudaEventRecord")) != KV_OK ||
         (st = cuda_check(cudaStreamWaitEvent(lane->stream, lane->fork, 0), "cudaStreamWaitEvent")) != KV_OK ||
-        (st = launch_multi_tc(a, tc_ctas(2), lane->stream)) != KV_OK ||
+        (st = launch_multi_tc(a, tc_ctas(1), lane->stream)) != KV_OK ||
         (st = cuda_check(cudaEventRecord(lane->join, lane->stream), "cudaEventRecord")) != KV_OK)
       return st;
     st = launch_decode(a, s);
@@ -321,7 +321,7 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
   } else if (column_path) {
     if ((st = launch_decode(a, s)) != KV_OK) return st;
   } else if (row_path) {
-    if ((st = launch_multi_tc(a, tc_ctas(2), s)) != KV_OK) return st;
+    if ((st = launch_multi_tc(a, tc_ctas(1), s)) != KV_OK) return st;
   }
   return launch_multi_merge(a, s);
 }
