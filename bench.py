@@ -591,9 +591,12 @@ def measure_multi(config, pkv, dev, stream, peak, replays=40, kv_dtype=None):
             "roofline": {"bound": "hbm", "kernel": plan.kernels,
                          "achieved": round(step_bytes / us / 1e3, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(step_bytes / us / 1e3 / peak, 4),
-                         "algorithmic_bytes_per_launch": step_bytes},
+                         "algorithmic_bytes_per_launch": step_bytes,
+                         "traffic": stored_traffic(s.name, "decode_kernel"),
+                         "traffic_kernel": "decode_kernel (column groups)"},
             "tensor": {"achieved_tflops": round(fl / us / 1e6, 2), "peak_tflops": tpeak,
                        "frac": round(fl / us / 1e6 / tpeak, 4), "flops_per_step": fl,
+                       "multi_tc_kernel_dram_bytes": stored_traffic(s.name, "multi_tc_kernel"),
                        "note": "long queries on tcgen05 (TMEM accumulators), few on mma.sync "
                                "m16n8k16; peak = measured cuBLAS bf16 (burst)"}}
 
