@@ -244,11 +244,12 @@ def kernel_hash(kernel):
     return source_hash(KERNEL_SOURCES[kernel])
 
 
-def stored_traffic(workload_name, kernel="decode_kernel"):
-    """DRAM bytes per launch of `kernel` on this workload from a committed
-    ncu capture (read + write; scaled to a full launch where the capture ran
-    a smaller case), if it was taken on the kernel's current sources; else
-    None."""
+NOMINAL_HBM_GBS = 8000.0                              # GB300 HBM3e, nominal
+
+
+def stored_capture(workload_name, kernel="decode_kernel"):
+    """The committed ncu capture of `kernel` on this workload, if it was
+    taken on the kernel's current sources; else None."""
     try:
         with open(TRAFFIC_FILE) as f:
             captures = json.load(f)["captures"]
@@ -258,8 +259,27 @@ def stored_traffic(workload_name, kernel="decode_kernel"):
     for t in captures:
         if t.get("workload") == workload_name and t.get("kernel") == kernel and \
                 t.get("source_sha256_16") == want:
-            return t.get("dram_bytes_per_launch")
+            return t
     return None
+
+
+def stored_traffic(workload_name, kernel="decode_kernel"):
+    """DRAM bytes (read + write) per launch of `kernel` on this workload from
+    a committed ncu capture of the current sources, else None."""
+    t = stored_capture(workload_name, kernel)
+    return None if t is None else t.get("dram_bytes_per_launch")
+
+
+def ncu_bandwidth(workload_name, peak, kernel="decode_kernel"):
+    """The kernel's DRAM read rate as ncu measured it (bytes read / its
+    duration in that capture), against the measured copy peak and the
+    nominal 8 TB/s; None without a capture of the current sources."""
+    t = stored_capture(workload_name, kernel)
+    if t is None or not t.get("gpu_time_us") or not t.get("dram_bytes_read_per_launch"):
+        return None
+    gbs = t["dram_bytes_read_per_launch"] / t["gpu_time_us"] / 1e3
+    return {"kernel": kernel, "dram_read_gbs": round(gbs, 1), "us": t["gpu_time_us"],
+            "frac_of_measured": round(gbs / peak, 4), "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4)}
 
 
 def measured_peak_gbs():
@@ -377,7 +397,8 @@ def roofline_of(wl, plan, us, peak, peak_kind):
             "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
             "algorithmic_bytes_per_launch": nbytes["step"], "us_per_launch": round(us, 2),
             "traffic": traffic,
-            "traffic_over_algorithmic": round(traffic / nbytes["step"], 4) if traffic else None}
+            "traffic_over_algorithmic": round(traffic / nbytes["step"], 4) if traffic else None,
+            "ncu": ncu_bandwidth(wl.spec.name, peak)}
 
 
 def check_status(pkv):

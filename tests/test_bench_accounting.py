@@ -80,8 +80,13 @@ def test_stored_traffic_needs_the_current_kernel_source(tmp_path, monkeypatch):
         {"workload": name, "kernel": "decode_kernel", "source_sha256_16": "0" * 16,
          "dram_bytes_per_launch": 1},
         {"workload": name, "kernel": "decode_kernel", "source_sha256_16": cur,
-         "dram_bytes_per_launch": 2}]}))
+         "dram_bytes_per_launch": 2, "dram_bytes_read_per_launch": 8000, "gpu_time_us": 2.0}]}))
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
     assert bench.stored_traffic(name, "decode_kernel") == 2
     assert bench.stored_traffic(name, "multi_tc_kernel") is None
     assert bench.stored_traffic("another workload", "decode_kernel") is None
+    # the ncu read rate: 8000 B in 2 us = 4 GB/s, against a 5 GB/s peak and 8 TB/s nominal
+    bw = bench.ncu_bandwidth(name, 5.0)
+    assert bw["dram_read_gbs"] == 4.0 and bw["frac_of_measured"] == 0.8
+    assert bw["frac_of_nominal_8tbs"] == 0.0005
+    assert bench.ncu_bandwidth("another workload", 5.0) is None
