@@ -395,6 +395,7 @@ def roofline_of(wl, plan, us, peak, peak_kind):
     traffic = stored_traffic(wl.spec.name, "decode_kernel")
     return {"bound": "hbm", "kernel": plan.kernels, "achieved": round(achieved, 1), "peak": peak,
             "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+            "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
             "algorithmic_bytes_per_launch": nbytes["step"], "us_per_launch": round(us, 2),
             "traffic": traffic,
             "traffic_over_algorithmic": round(traffic / nbytes["step"], 4) if traffic else None,
