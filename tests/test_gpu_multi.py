@@ -82,6 +82,13 @@ CASES = {
                                           seed=53),
     "row_int8_g2_d128_bs32": lambda: multi([129, 1000, 5], [129, 40, 5], hq=4, hkv=2, d=128, bs=32,
                                            kv="int8", seed=54),
+    # tile-pair edges of the tensor-core kernel (rows = query tokens x G = 4):
+    # exactly one tile (128 rows), one row into the second tile (132), exactly
+    # one pair (256), one row into the next pair (260)
+    "pair_edges_g4": lambda: multi([700, 900, 1100, 1300], [32, 33, 64, 65], hq=32, hkv=8, d=128,
+                                   seed=55),
+    "pair_edges_fp8_bs32": lambda: multi([300, 257, 400, 2200], [32, 33, 64, 65], hq=32, hkv=8,
+                                         d=128, bs=32, kv="fp8", seed=56),
 }
 
 

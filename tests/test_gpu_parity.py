@@ -276,6 +276,14 @@ PREFIX_CASES = {
                                                  prefix=592, kv="fp8", seed=40),
     "fp8_g1_d128_bs32": lambda: small([33, 40, 333], hq=4, hkv=4, d=128, bs=32, prefix=32, kv="fp8",
                                       seed=41),
+    # prefix rows = batch x G at the tensor-core kernel's tile-pair edges:
+    # 32 x 4 = 128 (one tile), 33 x 4 = 132 (one row into the second), 65 x 4 = 260
+    "pair_edge_128_rows": lambda: small([40 + 9 * i for i in range(32)], hq=32, hkv=8, d=128,
+                                        prefix=32, seed=42),
+    "pair_edge_132_rows": lambda: small([40 + 9 * i for i in range(33)], hq=32, hkv=8, d=128,
+                                        prefix=32, seed=43),
+    "pair_edge_260_rows_int8": lambda: small([70 + 5 * i for i in range(65)], hq=16, hkv=4, d=64,
+                                             bs=32, prefix=64, kv="int8", seed=44),
 }
 
 
