@@ -719,36 +719,44 @@ def gpu_arm(args, rank, world, local_rank, dist):
     h_out = [torch.empty(sets[0][out_name].shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in h_in.values())
     d2h = h_out[0].numel() * h_out[0].element_size()
-    copy_s, back_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    # One side stream carries both directions: while step i computes, it
+    # reads back step i-1's output and then copies step i+1's inputs into the
+    # same buffer set (so the compute stream waits on one event per step).
+    io_s = torch.cuda.Stream(dev)
     K2 = max(args.steps // 4, 10)
     copied = [torch.cuda.Event() for _ in range(2)]
     done = [torch.cuda.Event() for _ in range(2)]
-    read = [torch.cuda.Event() for _ in range(2)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def copy_in(j):
+        for k, h in h_in.items():
+            sets[j % 2][k].copy_(h, non_blocking=True)
+        copied[j % 2].record(io_s)
+
+    def read_back(j):
+        io_s.wait_event(done[j % 2])
+        h_out[j % 2].copy_(sets[j % 2][out_name], non_blocking=True)
+
     torch.cuda.synchronize(dev)
     e0.record(stream)
-    copy_s.wait_event(e0)
-    back_s.wait_event(e0)
+    io_s.wait_event(e0)
+    with torch.cuda.stream(io_s):
+        copy_in(0)
     for i in range(K2):
         cur = sets[i % 2]
-        with torch.cuda.stream(copy_s):
-            if i >= 2:
-                copy_s.wait_event(done[i % 2])        # step i-2 is done with this set
-            for k, h in h_in.items():
-                cur[k].copy_(h, non_blocking=True)
-            copied[i % 2].record(copy_s)
-        stream.wait_event(copied[i % 2])
-        if i >= 2:
-            stream.wait_event(read[i % 2])            # step i-2's output has been read
+        stream.wait_event(copied[i % 2])              # its inputs landed (after step i-2's read-back)
         for k, v in cur.items():
             setattr(g, k, v)
         step_fn()
         done[i % 2].record(stream)
-        with torch.cuda.stream(back_s):
-            back_s.wait_event(done[i % 2])
-            h_out[i % 2].copy_(cur[out_name], non_blocking=True)
-            read[i % 2].record(back_s)
-    stream.wait_stream(back_s)
+        with torch.cuda.stream(io_s):
+            if i >= 1:
+                read_back(i - 1)
+            if i + 1 < K2:
+                copy_in(i + 1)
+    with torch.cuda.stream(io_s):
+        read_back(K2 - 1)
+    stream.wait_stream(io_s)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     for k, v in sets[0].items():
@@ -786,8 +794,9 @@ def gpu_arm(args, rank, world, local_rank, dist):
         "e2e": {"value": round(e2e_agg / 1e9, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5),
                 "note": "inputs of every step copied from pinned host memory and outputs read "
-                        "back inside the timed region; two buffer sets alternate so step i's "
-                        "copies overlap step i-1's compute"},
+                        "back inside the timed region; two buffer sets alternate, and one side "
+                        "stream reads back step i-1's output and copies step i+1's inputs while "
+                        "step i computes"},
         "gpu_launches": plan.launches * K,
         "clocks": sampler.summary(),
     }
