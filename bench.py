@@ -55,6 +55,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = {
     "decode_kernel": ("pagedkv_decode.cu", "pagedkv_device.cuh", "pagedkv_common.cuh"),
     "multi_tc_kernel": ("pagedkv_multi_tc.cu", "pagedkv_device.cuh", "pagedkv_common.cuh"),
+    "multi_m16_kernel": ("pagedkv_multi_m16.cu", "pagedkv_device.cuh", "pagedkv_common.cuh"),
 }
 
 
@@ -306,6 +307,7 @@ class StepPlan:
     def __init__(self, wl, g, pkv, no_shared_prefix=False):
         s = wl.spec
         self.multi = bool((wl.query_lens != 1).any())      # several query tokens per sequence
+        self.m16 = self.row = False
         self.prefix = s.shared_prefix_tokens > 0 and not no_shared_prefix and not self.multi
         if self.multi:
             self.fn = g.multi_step
@@ -313,15 +315,22 @@ class StepPlan:
                                                    max(int(wl.query_lens.max()), 1),
                                                    s.num_q_heads, s.num_kv_heads, g.max_seq_len)
             G = s.num_q_heads // s.num_kv_heads
-            col_max = (8 // G) * 4 if G <= 8 else 0
-            # token slot mapping + append + the column groups (few-query
-            # sequences) and/or the tensor-core kernel (long ones) + the merge
-            # when a sequence spans several partitions
-            self.launches = (2 + int(bool((wl.query_lens <= col_max).any()))
-                             + int(bool((wl.query_lens > col_max).any()))
+            tpg = 8 // G if G <= 8 else 0
+            col_max = 4 * tpg
+            maxq = max(int(wl.query_lens.max()), 1)
+            # the launches paged_attention_multi makes: token slot mapping +
+            # append; the decode kernel's column groups whenever G <= 8, and on
+            # bf16 pools the 16-column kernel beside them once a sequence may
+            # hold more than one group's tokens; the tensor-core kernel when
+            # one may need row tiles; the merge when a sequence may span
+            # several partitions
+            self.m16 = tpg > 0 and s.kv_dtype == "bf16" and maxq > tpg
+            self.row = maxq > col_max
+            self.launches = (2 + int(tpg > 0) + int(self.m16) + int(self.row)
                              + int(g.max_seq_len > self.part))
-            self.kernels = ("token slot mapping + append + decode_kernel column groups / "
-                            "multi_tc_kernel (+ multi_merge_kernel), paged_attention_multi")
+            self.kernels = ("token slot mapping + append + decode_kernel column groups "
+                            "/ multi_m16_kernel (16 columns, bf16) / multi_tc_kernel "
+                            "(+ multi_merge_kernel), paged_attention_multi")
         else:
             skip = s.shared_prefix_tokens if self.prefix else 0
             self.fn = g.prefix_step if self.prefix else g.fused_step
@@ -604,6 +613,8 @@ def measure_multi(config, pkv, dev, stream, peak, replays=40, kv_dtype=None):
     step_bytes = multi_step_bytes(wl)
     fl = multi_flops(wl)
     tpeak, _ = measured_peak_tflops()
+    # the few-query kernel whose DRAM traffic the roofline carries
+    col_kernel = "multi_m16_kernel" if plan.m16 else "decode_kernel"
     del graph, g
     torch.cuda.empty_cache()
     return {"workload": s.name, "kv_dtype": s.kv_dtype, "query_tokens": wl.num_tokens,
@@ -614,8 +625,8 @@ def measure_multi(config, pkv, dev, stream, peak, replays=40, kv_dtype=None):
                          "achieved": round(step_bytes / us / 1e3, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(step_bytes / us / 1e3 / peak, 4),
                          "algorithmic_bytes_per_launch": step_bytes,
-                         "traffic": stored_traffic(s.name, "decode_kernel"),
-                         "traffic_kernel": "decode_kernel (column groups)"},
+                         "traffic": stored_traffic(s.name, col_kernel),
+                         "traffic_kernel": col_kernel},
             "tensor": {"achieved_tflops": round(fl / us / 1e6, 2), "peak_tflops": tpeak,
                        "frac": round(fl / us / 1e6 / tpeak, 4), "flops_per_step": fl,
                        "multi_tc_kernel_dram_bytes": stored_traffic(s.name, "multi_tc_kernel"),

@@ -8,12 +8,16 @@
 // q rows query_start[b] .. query_start[b + 1] - 1.  Query token i sits at
 // position L_b - n_b + i and attends positions 0 .. L_b - n_b + i (causal).
 //
-// Each sequence goes to one of two kernels in the same call:
-//   * few query tokens (n_b <= 4 x 8 / G): the decode kernel, whose 8 MMA
+// Each sequence goes to one of three kernels in the same call:
+//   * one column group (n_b <= 8 / G): the decode kernel, whose 8 MMA
 //     columns per CTA then hold (token, head) pairs (pagedkv_decode.cu);
+//   * a few column groups (8 / G < n_b <= 4 x 8 / G): on bf16 pools the
+//     16-column kernel (pagedkv_multi_m16.cu), 16 / G tokens per CTA, so
+//     fewer CTAs read each block; on 8-bit pools the decode kernel's
+//     column groups;
 //   * longer queries: the tensor-core kernel with TMEM accumulators
 //     (pagedkv_multi_tc.cu), 128 rows per CTA.
-// Both write the normalised output (one partition) or per-row (m, l, acc)
+// All write the normalised output (one partition) or per-row (m, l, acc)
 // partials that the log-sum-exp merge below combines (“LLM 推理优化技术全景”,
 // 在线 Softmax; “Flash Attention v2 的改进”).
 #include <cuda.h>
@@ -26,11 +30,18 @@
 #include "pagedkv_device.cuh"
 
 namespace pagedkv {
+
+// pagedkv_multi_m16.cu: sequences with n_lo < n_b <= a.col_max_n query
+// tokens, `vgroups` 16-column CTAs per sequence (bf16 pools).
+kv_status launch_multi_m16(const DecodeArgs& a, int n_lo, int vgroups, cudaStream_t s);
+
 namespace {
 
 // Column groups the decode kernel may serve per sequence (8 columns each):
 // longer queries go to the tensor-core kernel.
 constexpr int kMaxVGroups = 4;
+// Columns of one 16-column CTA.
+constexpr int kM16Cols = 16;
 
 // Log-sum-exp merge of the partition partials of every (query token, head)
 // row: one warp per row, four heads per CTA.  Partials of partitions wholly
@@ -237,13 +248,17 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
   const int GQ = num_q_heads / num_kv_heads;
   // Sequences with few query tokens (at most 4 x 8 / G): the decode
   // kernel's 8 columns per CTA hold (token, head) pairs, 8 / G tokens per
-  // column group.  Longer queries: the tensor-core kernel, in the same call
-  // when both kinds occur.
+  // column group; on bf16 pools those with more than one group's tokens go
+  // to the 16-column kernel instead (16 / G tokens per CTA).  Longer
+  // queries: the tensor-core kernel, in the same call when both kinds occur.
   const int tpg = GQ <= kMaxGroup ? kMaxGroup / GQ : 0;
   const int col_max_n = tpg * kMaxVGroups;               // 0 when G > 8
   const int vgroups = tpg > 0 ? (min(max_query_len, col_max_n) + tpg - 1) / tpg : 0;
   const bool column_path = tpg > 0;                       // some sequences may use it
   const bool row_path = max_query_len > col_max_n;        // some sequences may need it
+  const bool m16_path = column_path && dtype == KV_DTYPE_BF16 && max_query_len > tpg;
+  const int tpg16 = column_path ? kM16Cols / GQ : 0;
+  const int vgroups16 = m16_path ? (min(max_query_len, col_max_n) + tpg16 - 1) / tpg16 : 0;
   if (batch == 0 || num_tokens == 0) return KV_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !query_start)
     return fail(KV_ERR_INVALID_ARG, "%s: NULL pointer", who);
@@ -305,6 +320,17 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
   auto tc_ctas = [&](int per_sm) {
     return (int)std::min<int64_t>(tiles * num_kv_heads * a.max_parts, (int64_t)di.num_sms * per_sm);
   };
+  // The few-query kernels on one stream: the decode kernel's column groups
+  // (with the 16-column kernel in the call, only sequences of one group)
+  // and the 16-column CTAs.
+  auto launch_columns = [&]() -> kv_status {
+    if (!m16_path) return launch_decode(a, s);
+    DecodeArgs one = a;
+    one.col_max_n = tpg;
+    one.vgroups = 1;
+    kv_status r = launch_decode(one, s);
+    return r != KV_OK ? r : launch_multi_m16(a, tpg, vgroups16, s);
+  };
   if (row_path && column_path) {
     // the tensor-core kernel (tensor-bound) beside the column groups (HBM-bound)
     SideLane* lane = nullptr;
@@ -314,12 +340,12 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
         (st = launch_multi_tc(a, tc_ctas(1), lane->stream)) != KV_OK ||
         (st = cuda_check(cudaEventRecord(lane->join, lane->stream), "cudaEventRecord")) != KV_OK)
       return st;
-    st = launch_decode(a, s);
+    st = launch_columns();
     const kv_status sj = cuda_check(cudaStreamWaitEvent(s, lane->join, 0), "cudaStreamWaitEvent");
     if (st != KV_OK) return st;
     if (sj != KV_OK) return sj;
   } else if (column_path) {
-    if ((st = launch_decode(a, s)) != KV_OK) return st;
+    if ((st = launch_columns()) != KV_OK) return st;
   } else if (row_path) {
     if ((st = launch_multi_tc(a, tc_ctas(1), s)) != KV_OK) return st;
   }

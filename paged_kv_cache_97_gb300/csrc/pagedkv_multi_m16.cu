@@ -1,0 +1,530 @@
+// pagedkv_multi_m16.cu -- few-token multi-token queries with 16 (query
+// token, grouped head) columns per CTA on the MMA's M side (speculative
+// verification, “让 Agent 跑得快：LLM 推理服务”, §六 投机解码: the target model
+// scores the draft tokens in one parallel pass).
+//
+// Sequence b's query token i (of n_b, its last tokens) sits at position
+// L_b - n_b + i and attends positions 0 .. L_b - n_b + i.  This kernel takes
+// the sequences whose n_b is too large for one 8-column group of the decode
+// kernel's multi-token mode (8 / G tokens) but small enough for its column
+// path (at most 4 x 8 / G tokens): a CTA serves one (KV head, sequence, token
+// partition) and a "group" of 16 / G query tokens times the G heads.  With
+// the columns on M (mma.sync m16n8k16, bf16, fp32 accumulate):
+//   S[16 cols x 16 keys] = Q[16 x d] . K^T   (B = K rows by ldmatrix)
+//   O[16 cols x d]      += P[16 x 16] . V    (B = V rows by ldmatrix.trans)
+// P is packed straight from the S accumulators (the fragment of S for keys
+// 0-7 and 8-15 is the A fragment of P), so no shuffles move it, and every K
+// and V fragment read from shared memory serves 16 columns instead of 8.
+// Each column keeps its own causal limit; the online softmax (“LLM 推理优化
+// 技术全景”, 在线 Softmax; “Flash Attention v2 的改进”: deferred
+// normalisation) runs per column in base 2.  Lane 4g + t holds columns g and
+// g + 8 (its S and O rows), so the softmax state of a column lives in the
+// four lanes that hold its scores.
+//
+// The pipeline is the decode kernel's: a producer warp walks the partition's
+// blocks and issues TMA tensor loads of K and V into an mbarrier ring, three
+// consumer warps take one block of each stage, then combine through shared
+// memory and write the output (one partition) or (m, l, acc) partials that
+// the multi-token merge combines.  Every wait is bounded.  bf16 pools.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "pagedkv_common.cuh"
+#include "pagedkv_device.cuh"
+
+namespace pagedkv {
+namespace {
+
+using namespace dev;
+
+constexpr int kCols = 16;                                // query columns per CTA (the MMA's M)
+constexpr int kThreads = (kConsumers + 1) * 32;          // + one producer warp
+constexpr int kMaxBlocks = kMaxColumnPartTokens / 16;    // blocks per partition (max)
+constexpr int kSpec = (kMaxBlocks + kThreads - 1) / kThreads;
+
+// 2^x on the special-function unit (PTX ex2.approx.ftz.f32; 2^-inf = +0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Stage ring of up to 72 KB (three stages of three bf16 d128 16-row
+// blocks): three CTAs of it fit an SM's 228 KB, and with two stages in flight
+// per CTA the loads cover the time the consumers take per stage.
+template <int D, int BS>
+struct Ring {
+  using G = Geo<D, BS, false>;
+  static constexpr int kStages0 = (72 * 1024) / G::kStageBytes;
+  static constexpr int kStages = kStages0 < 2 ? 2 : (kStages0 > kMaxStages ? kMaxStages : kStages0);
+  static constexpr int kSmemBytes = kStages * G::kStageBytes + 1024;   // + alignment slack
+  // CTAs per SM that shared memory admits (at most 3; 1 KB reserved per CTA
+  // and a little static memory): the register budget's divisor
+  static constexpr int kMinCtas = 3 * (kSmemBytes + 2048) <= 228 * 1024 ? 3 : 2;
+};
+
+template <int D, int BS>
+__global__ void __launch_bounds__(kThreads, Ring<D, BS>::kMinCtas)
+    multi_m16_kernel(const __grid_constant__ CUtensorMap k_map,
+                     const __grid_constant__ CUtensorMap v_map, const DecodeArgs a, int n_lo,
+                     int vgroups) {
+  using G = Geo<D, BS, false>;
+  constexpr int S = Ring<D, BS>::kStages;
+  constexpr int kKSteps = D / 16;                         // k-steps of S over d
+  constexpr int kDBlocks = D / 8;                         // 8-wide d blocks of O
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
+  __shared__ int cta_bad, cta_timeout;
+
+  const int hk = blockIdx.x;
+  const int part = a.reverse_parts ? (int)(gridDim.z - 1 - blockIdx.z) : (int)blockIdx.z;
+  const int b = (int)(blockIdx.y / vgroups), vg = (int)(blockIdx.y % vgroups);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int Hq = a.num_q_heads, Hkv = a.num_kv_heads;
+  const int GQ = Hq / Hkv;                               // grouped query heads (1..8)
+  const int TPG = kCols / GQ;                            // query tokens per group
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+
+  // This kernel's sequences: n_lo < n <= col_max_n (the decode kernel takes
+  // the shorter ones, the tensor-core kernel the longer).
+  const int q0 = a.query_start[b];
+  const int nq = a.query_start[b + 1] - q0;
+  if (nq <= n_lo || nq > a.col_max_n) return;
+  const bool rows_ok = q0 >= 0 && nq >= 0 && q0 + nq <= a.num_tokens;
+  // Row of the q / out tensors that column c serves (-1: padding): token
+  // vg * TPG + c / GQ of the sequence, head c % GQ of the group.
+  auto col_row = [&](int c) -> int64_t {
+    const int i = vg * TPG + c / GQ;
+    return (rows_ok && c < TPG * GQ && i < nq) ? (int64_t)(q0 + i) * Hq + (int64_t)hk * GQ + c % GQ
+                                                 : -1;
+  };
+
+  // Block ids of the partition and the consumers' Q fragments are loaded
+  // before the sequence length arrives (neither depends on it).
+  const int t0 = part * a.part_tokens;
+  const int first_blk = t0 / BS;
+  const int spec_blk = min(a.part_tokens / BS, a.max_blocks_per_seq - first_blk);
+  const int32_t* bt = a.block_tables + (int64_t)b * a.max_blocks_per_seq + first_blk;
+  int32_t spec_id[kSpec];
+#pragma unroll
+  for (int r = 0; r < kSpec; ++r) {
+    const int j = threadIdx.x + r * kThreads;
+    spec_id[r] = j < spec_blk ? bt[j] : -1;
+  }
+  // A fragments of Q (rows = columns g and g + 8, k = d): a0 = (g, 2t..2t+1),
+  // a1 = (g + 8, 2t..), a2 = (g, 2t + 8..), a3 = (g + 8, 2t + 8..) of each
+  // 16-wide k-step; padding columns are zero.
+  uint32_t qa[kKSteps][4];
+  if (warp < kConsumers) {
+    const int64_t r0 = col_row(g), r1 = col_row(g + 8);
+    const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.q);
+#pragma unroll
+    for (int ks = 0; ks < kKSteps; ++ks) {
+      const int d0 = 16 * ks + 2 * t;
+      qa[ks][0] = r0 >= 0 ? *reinterpret_cast<const uint32_t*>(qb + r0 * D + d0) : 0u;
+      qa[ks][1] = r1 >= 0 ? *reinterpret_cast<const uint32_t*>(qb + r1 * D + d0) : 0u;
+      qa[ks][2] = r0 >= 0 ? *reinterpret_cast<const uint32_t*>(qb + r0 * D + d0 + 8) : 0u;
+      qa[ks][3] = r1 >= 0 ? *reinterpret_cast<const uint32_t*>(qb + r1 * D + d0 + 8) : 0u;
+    }
+  }
+
+  // ---- sequence checks (uniform over the CTA) -----------------------------
+  const int L = a.seq_lens[b];
+  const int64_t table_tokens = (int64_t)a.max_blocks_per_seq * BS;
+  const bool len_bad = L <= 0 || L > a.max_seq_len || L > table_tokens || !rows_ok || nq > L ||
+                       nq > a.max_query_len;
+  if (len_bad) {
+    if (part == 0) {
+      if (threadIdx.x == 0 && vg == 0) atomicOr(a.flags, PAGEDKV_FLAG_BAD_SEQ_LEN);
+      // (with several partitions, the multi-token merge zeroes these rows)
+      if (a.max_parts == 1)
+        for (int i = threadIdx.x; i < kCols * D; i += blockDim.x) {
+          const int64_t r = col_row(i / D);
+          if (r >= 0) out[r * D + i % D] = __float2bfloat16_rn(0.0f);
+        }
+    }
+    return;
+  }
+  if (vg * TPG >= nq) return;                            // a group with no queries
+  if (t0 >= L) return;
+  // keys up to this group's last query position
+  int t1 = min(t0 + a.part_tokens, L);
+  t1 = min(t1, L - nq + min(nq - 1, vg * TPG + TPG - 1) + 1);
+  const bool direct = a.max_parts == 1;
+  if (t1 <= t0) {
+    // every query of this group precedes the partition: empty partials
+    for (int i = threadIdx.x; i < kCols * D; i += blockDim.x) {
+      const int64_t r = col_row(i / D);
+      if (r < 0) continue;
+      const int64_t sl = r * a.slots + part;
+      a.ws_acc[sl * D + i % D] = 0.0f;
+      if (i % D == 0) {
+        a.ws_ml[2 * sl] = -INFINITY;
+        a.ws_ml[2 * sl + 1] = 0.0f;
+      }
+    }
+    return;
+  }
+  const int nblk = (t1 - 1) / BS - first_blk + 1;        // >= 1, <= spec_blk
+  const uint32_t stages = (smem_addr(smem_raw) + 1023u) & ~1023u;
+
+  // ---- set-up: barriers, and a check of the partition's block ids ---------
+  if (threadIdx.x == 0) {
+    cta_bad = 0;
+    cta_timeout = 0;
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_addr(&full_bar[s]), 1);
+      mbar_init(smem_addr(&empty_bar[s]), kConsumers);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < kSpec; ++r) {
+    const int j = threadIdx.x + r * kThreads;
+    if (j >= nblk) continue;
+    const int32_t p = spec_id[r];
+    if (p < 0 || p >= a.num_blocks) cta_bad = 1;
+  }
+  __syncthreads();
+  const bool bad = cta_bad != 0;
+  const int n_iter = (nblk + kConsumers - 1) / kConsumers;
+
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};   // columns g, g + 8
+  float o[kDBlocks][4];
+#pragma unroll
+  for (int i = 0; i < kDBlocks; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
+
+  if (!bad && warp == kConsumers) {
+    // ======================= producer =======================================
+    // Block ids 32 at a time, lane l holding block 32 k + l of chunk k (the
+    // ids were checked above; the table is read again here, from L2, with
+    // the next chunk always in flight).
+    auto chunk_id = [&](int k) -> int32_t {
+      const int j = 32 * k + lane;
+      return j < nblk ? bt[j] : 0;
+    };
+    int32_t id_cur = chunk_id(0), id_nxt = chunk_id(1);
+    int k_cur = 0;
+    int issued = 0;
+    bool ok = true;
+    for (int it = 0; it < n_iter; ++it) {
+      const int s = it % S;
+      if (it >= S && !mbar_wait(smem_addr(&empty_bar[s]), ((it / S) - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      const int j0 = it * kConsumers;
+      const int cnt = min(kConsumers, nblk - j0);
+      const uint32_t fb = smem_addr(&full_bar[s]);
+      if (lane == 0) mbar_expect_tx(fb, (uint32_t)(cnt * G::kBlockBytes));
+      for (int c = 0; c < cnt; ++c) {
+        const int j = j0 + c;
+        if ((j >> 5) != k_cur) {                           // next chunk (warp-uniform)
+          id_cur = id_nxt;
+          ++k_cur;
+          id_nxt = chunk_id(k_cur + 1);
+        }
+        int32_t p = __shfl_sync(0xffffffffu, id_cur, j & 31);
+        p = (p >= 0 && p < a.num_blocks) ? p : 0;
+        if (lane == 0) {
+          const uint32_t kdst = stages + (uint32_t)((s * kConsumers + c) * G::kBlockBytes);
+          const uint32_t vdst = kdst + G::kTensorBytes;
+#pragma unroll
+          for (int x = 0; x < G::kBoxes; ++x) {
+            tma_load_4d(kdst + x * G::kBoxBytes, &k_map, fb, x * G::kBoxElems, hk, 0, p);
+            tma_load_4d(vdst + x * G::kBoxBytes, &v_map, fb, x * G::kBoxElems, hk, 0, p);
+          }
+        }
+      }
+      __syncwarp();
+      issued = it + 1;
+    }
+    // every fill issued lands before the CTA may reuse or release the stages
+    for (int s = 0; s < S && s < issued; ++s) {
+      const int last = s + S * ((issued - 1 - s) / S);
+      if (!mbar_wait(smem_addr(&full_bar[s]), (last / S) & 1)) ok = false;
+    }
+    if (!ok && lane == 0) cta_timeout = 1;
+  } else if (!bad) {
+    // ======================= consumers =====================================
+    const int w = warp;
+    const float kfac = a.scale_log2;
+    // causal limits of this lane's columns g and g + 8 (padding: no limit),
+    // and the group's first query position: a block whose last key is at or
+    // before it is visible to every column
+    const int pos_lo = L - nq + vg * TPG;
+    const int cpos0 = g < TPG * GQ ? pos_lo + g / GQ : 0x7fffffff;
+    const int cpos1 = g + 8 < TPG * GQ ? pos_lo + (g + 8) / GQ : 0x7fffffff;
+    // ldmatrix row addresses inside a block (the same for K and V): matrix
+    // q = lane / 8 covers keys 8 (q & 1) .. + 7 and 16-byte chunk
+    // 2 ks + (q >> 1); the next 16-key tile is 16 rows further on
+    uint32_t off[kKSteps];
+    {
+      const int row = ((lane >> 3) & 1) * 8 + (lane & 7);
+#pragma unroll
+      for (int ks = 0; ks < kKSteps; ++ks) off[ks] = chunk_off<G>(row, 2 * ks + (lane >> 4));
+    }
+    bool ok = true;
+    for (int it = 0; it < n_iter; ++it) {
+      const int s = it % S;
+      if (!mbar_wait(smem_addr(&full_bar[s]), (it / S) & 1)) {
+        ok = false;
+        break;
+      }
+      const int j = it * kConsumers + w;
+      if (j < nblk) {
+        const uint32_t kb = stages + (uint32_t)((s * kConsumers + w) * G::kBlockBytes);
+        const uint32_t vb = kb + G::kTensorBytes;
+        const int key0 = (first_blk + j) * BS;             // position of the block's first row
+        const int valid = min(BS, L - key0);
+        // interior block: every row written and visible to every column
+        const bool plain = valid == BS && key0 + BS - 1 <= pos_lo;
+
+        // ---- S for every 16-key tile: sc[tile][nb][...] for keys 8 nb + 2t, +1
+        // (r0 / r2 = keys 0-7, d low / high: B of n-block 0; r1 / r3 = keys
+        // 8-15: B of n-block 1; with one tile per block, even and odd k-steps
+        // accumulate apart, which halves the dependent MMA chains)
+        constexpr int kSplit = G::kTiles == 1 ? 2 : 1;
+        float sc[G::kTiles][2][4];
+#pragma unroll
+        for (int tile = 0; tile < G::kTiles; ++tile) {
+          float c[2 * kSplit][4] = {};
+#pragma unroll
+          for (int ks = 0; ks < kKSteps; ++ks) {
+            uint32_t r[4];
+            ldsm_x4(r, kb + off[ks] + tile * 16 * G::kBoxRow);
+            mma16816<false>(c[ks % kSplit], qa[ks], r[0], r[2]);
+            mma16816<false>(c[kSplit + ks % kSplit], qa[ks], r[1], r[3]);
+          }
+#pragma unroll
+          for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float x = c[kSplit * nb][e];
+              if constexpr (kSplit == 2) x += c[kSplit * nb + 1][e];
+              sc[tile][nb][e] = x * kfac;
+            }
+          if (!plain) {
+#pragma unroll
+            for (int nb = 0; nb < 2; ++nb) {
+              const int k0 = tile * 16 + 8 * nb + 2 * t;   // key row in the block
+              const bool v0 = k0 < valid, v1 = k0 + 1 < valid;
+              if (!(v0 && key0 + k0 <= cpos0)) sc[tile][nb][0] = -INFINITY;
+              if (!(v1 && key0 + k0 + 1 <= cpos0)) sc[tile][nb][1] = -INFINITY;
+              if (!(v0 && key0 + k0 <= cpos1)) sc[tile][nb][2] = -INFINITY;
+              if (!(v1 && key0 + k0 + 1 <= cpos1)) sc[tile][nb][3] = -INFINITY;
+            }
+          }
+        }
+
+        // ---- online softmax update of columns g (index 0) and g + 8 (1) ----
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int tile = 0; tile < G::kTiles; ++tile)
+#pragma unroll
+          for (int nb = 0; nb < 2; ++nb) {
+            mx0 = fmaxf(mx0, fmaxf(sc[tile][nb][0], sc[tile][nb][1]));
+            mx1 = fmaxf(mx1, fmaxf(sc[tile][nb][2], sc[tile][nb][3]));
+          }
+#pragma unroll
+        for (int o2 = 1; o2 < 4; o2 <<= 1) {              // the quad holding the column
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
+        }
+        const float mx0n = fmaxf(m_run[0], mx0), mx1n = fmaxf(m_run[1], mx1);
+        // a column with no key yet keeps m = -inf: subtract 0 then
+        const float mn0 = mx0n == -INFINITY ? 0.0f : mx0n;
+        const float mn1 = mx1n == -INFINITY ? 0.0f : mx1n;
+        // O is rescaled only when some column's maximum moved (warp-uniform)
+        if (__any_sync(0xffffffffu, mx0n != m_run[0] || mx1n != m_run[1])) {
+          const float al0 = ex2(m_run[0] - mn0), al1 = ex2(m_run[1] - mn1);
+          l_run[0] *= al0;
+          l_run[1] *= al1;
+#pragma unroll
+          for (int i = 0; i < kDBlocks; ++i) {
+            o[i][0] *= al0;
+            o[i][1] *= al0;
+            o[i][2] *= al1;
+            o[i][3] *= al1;
+          }
+        }
+        m_run[0] = mx0n;
+        m_run[1] = mx1n;
+
+#pragma unroll
+        for (int tile = 0; tile < G::kTiles; ++tile) {
+          if (tile * 16 >= valid) break;                  // whole tile masked
+          float p[2][4];
+#pragma unroll
+          for (int nb = 0; nb < 2; ++nb) {
+            p[nb][0] = ex2(sc[tile][nb][0] - mn0);
+            p[nb][1] = ex2(sc[tile][nb][1] - mn0);
+            p[nb][2] = ex2(sc[tile][nb][2] - mn1);
+            p[nb][3] = ex2(sc[tile][nb][3] - mn1);
+            l_run[0] += p[nb][0] + p[nb][1];
+            l_run[1] += p[nb][2] + p[nb][3];
+          }
+          // A fragment of P: (g, keys 2t..), (g + 8, 2t..), (g, 2t + 8..), (g + 8, 2t + 8..)
+          const uint32_t pa[4] = {pack2<false>(p[0][0], p[0][1]), pack2<false>(p[0][2], p[0][3]),
+                                  pack2<false>(p[1][0], p[1][1]), pack2<false>(p[1][2], p[1][3])};
+          // ldmatrix.x4.trans over the same rows: r0 / r1 = b0 / b1 of
+          // d-block 2 jj, r2 / r3 of d-block 2 jj + 1
+          if (valid == BS) {
+#pragma unroll
+            for (int jj = 0; jj < kDBlocks / 2; ++jj) {
+              uint32_t r[4];
+              ldsm_x4_t(r, vb + off[jj] + tile * 16 * G::kBoxRow);
+              mma16816<false>(o[2 * jj], pa, r[0], r[1]);
+              mma16816<false>(o[2 * jj + 1], pa, r[2], r[3]);
+            }
+          } else {
+            // V rows past `valid` are zeroed in the B fragments (keys 2t,
+            // 2t+1 in b0, 2t+8, 2t+9 in b1): p is 0 there, but the pool may
+            // hold NaN
+            const int k0 = tile * 16 + 2 * t;
+            const uint32_t mlo = (k0 < valid ? 0x0000ffffu : 0u) | (k0 + 1 < valid ? 0xffff0000u : 0u);
+            const uint32_t mhi = (k0 + 8 < valid ? 0x0000ffffu : 0u) | (k0 + 9 < valid ? 0xffff0000u : 0u);
+#pragma unroll
+            for (int jj = 0; jj < kDBlocks / 2; ++jj) {
+              uint32_t r[4];
+              ldsm_x4_t(r, vb + off[jj] + tile * 16 * G::kBoxRow);
+              mma16816<false>(o[2 * jj], pa, r[0] & mlo, r[1] & mhi);
+              mma16816<false>(o[2 * jj + 1], pa, r[2] & mlo, r[3] & mhi);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&empty_bar[s]));
+    }
+    if (!ok) cta_timeout = 1;
+  }
+
+  // ---- combine the consumer warps -----------------------------------------
+  __syncthreads();  // all fills landed and all stage reads done
+  const bool failed = bad || cta_timeout != 0;
+  float* red = reinterpret_cast<float*>(smem_raw + (stages - smem_addr(smem_raw)));
+  float* red_m = red;                              // [kConsumers][kCols]
+  float* red_l = red + kConsumers * kCols;         // [kConsumers][kCols]
+  float* red_acc = red + 2 * kConsumers * kCols;   // [kConsumers][kCols][D]
+  if (!failed && warp < kConsumers) {
+#pragma unroll
+    for (int off = 1; off < 4; off <<= 1) {
+      l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], off);
+      l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], off);
+    }
+    if (t == 0) {
+      red_m[warp * kCols + g] = m_run[0];
+      red_m[warp * kCols + g + 8] = m_run[1];
+      red_l[warp * kCols + g] = l_run[0];
+      red_l[warp * kCols + g + 8] = l_run[1];
+    }
+    float* acc = red_acc + warp * kCols * D;
+#pragma unroll
+    for (int i = 0; i < kDBlocks; ++i) {
+      const int d0 = 8 * i + 2 * t;
+      acc[g * D + d0] = o[i][0];
+      acc[g * D + d0 + 1] = o[i][1];
+      acc[(g + 8) * D + d0] = o[i][2];
+      acc[(g + 8) * D + d0 + 1] = o[i][3];
+    }
+  }
+  __syncthreads();
+
+  if (failed) {
+    if (threadIdx.x == 0)
+      atomicOr(a.flags, bad ? PAGEDKV_FLAG_BAD_BLOCK : PAGEDKV_FLAG_WAIT_TIMEOUT);
+    for (int i = threadIdx.x; i < kCols * D; i += blockDim.x) {
+      const int c = i / D, e = i % D;
+      const int64_t row = col_row(c);
+      if (row < 0) continue;
+      if (direct) {
+        out[row * D + e] = __float2bfloat16_rn(0.0f);
+      } else {
+        const int64_t r = row * a.slots + part;
+        a.ws_acc[r * D + e] = 0.0f;
+        if (e == 0) {
+          a.ws_ml[2 * r] = 0.0f;
+          a.ws_ml[2 * r + 1] = -1.0f;  // marks the row bad for the merge
+        }
+      }
+    }
+    return;
+  }
+
+  for (int i = threadIdx.x; i < kCols * D; i += blockDim.x) {
+    const int c = i / D, e = i % D;
+    const int64_t row = col_row(c);
+    if (row < 0) continue;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, red_m[w * kCols + c]);
+    const float Mz = M == -INFINITY ? 0.0f : M;    // a column with no key here
+    float num = 0.0f, den = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kConsumers; ++w) {
+      const float f = exp2f(red_m[w * kCols + c] - Mz);  // 0 for a warp that saw no key
+      num = fmaf(f, red_acc[(w * kCols + c) * D + e], num);
+      den = fmaf(f, red_l[w * kCols + c], den);
+    }
+    if (direct) {
+      out[row * D + e] = __float2bfloat16_rn(num / den);
+    } else {
+      const int64_t r = row * a.slots + part;
+      a.ws_acc[r * D + e] = num;
+      if (e == 0) {
+        a.ws_ml[2 * r] = M;
+        a.ws_ml[2 * r + 1] = den;
+      }
+    }
+  }
+}
+
+template <int D, int BS>
+kv_status launch_t(const DecodeArgs& a, int n_lo, int vgroups, cudaStream_t s) {
+  static std::mutex mu;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  kv_status st = cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
+  if (st != KV_OK) return st;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+      st = cuda_check(cudaFuncSetAttribute(multi_m16_kernel<D, BS>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           Ring<D, BS>::kSmemBytes),
+                      "cudaFuncSetAttribute(multi_m16_kernel)");
+      if (st != KV_OK) return st;
+      attr_set[dev] = true;
+    }
+  }
+  CUtensorMap km, vm;
+  if ((st = make_kv_maps(a, &km, &vm)) != KV_OK) return st;
+  const dim3 grid(a.num_kv_heads, a.batch * vgroups, a.max_parts);
+  multi_m16_kernel<D, BS><<<grid, kThreads, Ring<D, BS>::kSmemBytes, s>>>(km, vm, a, n_lo, vgroups);
+  return cuda_check(cudaGetLastError(), "multi_m16_kernel launch");
+}
+
+}  // namespace
+
+// Few-token multi-token queries with n_lo < n_b <= a.col_max_n on 16-column
+// CTAs (bf16 pools); `vgroups` 16-column groups per sequence.
+kv_status launch_multi_m16(const DecodeArgs& a, int n_lo, int vgroups, cudaStream_t s) {
+  if (a.dtype != KV_DTYPE_BF16 || vgroups <= 0)
+    return fail(KV_ERR_INVALID_ARG, "paged_attention_multi: bad 16-column launch");
+  if ((int64_t)a.batch * vgroups > 65535 || a.max_parts > 65535)
+    return fail(KV_ERR_INVALID_ARG, "batch x groups and the partition count must be at most 65535");
+  if (a.part_tokens / a.block_size > kMaxBlocks || a.part_tokens % a.block_size)
+    return fail(KV_ERR_INVALID_ARG, "partition must be a multiple of block_size, at most %d blocks",
+                kMaxBlocks);
+  if (a.head_dim == 128)
+    return a.block_size == 32 ? launch_t<128, 32>(a, n_lo, vgroups, s) : launch_t<128, 16>(a, n_lo, vgroups, s);
+  return a.block_size == 32 ? launch_t<64, 32>(a, n_lo, vgroups, s) : launch_t<64, 16>(a, n_lo, vgroups, s);
+}
+
+}  // namespace pagedkv

@@ -5,9 +5,10 @@ against the oracle (â€œè®© Agent è·‘å¾—å¿«ï¼šLLM æ¨ç†æœåŠ¡â€, Â§å…­ æŠ•æœºè§
 The step's tokens are appended with the general slot mapping and
 reshape_and_cache (pools compared bit for bit with the oracle's), then
 attended causally; outputs within max-abs 1e-2 / mean-abs 1e-3 of the fp64
-oracle (3e-2 / 1e-3 for 8-bit pools), on small cases covering both kernels
-(decode-kernel column groups for few query tokens, the tcgen05 tensor-core
-kernel for many), the one-partition path and the split path with its merge, and on
+oracle (3e-2 / 1e-3 for 8-bit pools), on small cases covering the three kernels
+(decode-kernel column groups for one group's query tokens, 16-column CTAs
+for a few groups' on bf16 pools, the tcgen05 tensor-core kernel for many),
+the one-partition path and the split path with its merge, and on
 sampled sequences of the full-size workloads.
 """
 import os
@@ -89,6 +90,14 @@ CASES = {
                                    seed=55),
     "pair_edges_fp8_bs32": lambda: multi([300, 257, 400, 2200], [32, 33, 64, 65], hq=32, hkv=8,
                                          d=128, bs=32, kv="fp8", seed=56),
+    # 16-column CTAs (bf16, more than one 8-column group's tokens): G = 3
+    # leaves column 15 as padding (5 tokens x 3 heads); G = 6 puts 2 tokens in
+    # a CTA and a sequence whose every token is a query (L = n = 2: the first
+    # query sees key 0 alone); at G = 4, n = 8 fills two CTAs exactly, n = 9
+    # is the first length for the tensor-core kernel, and L = 8 = n
+    "m16_g3_d64": lambda: multi([7, 300, 1000, 33], [3, 8, 5, 6], hq=6, hkv=2, d=64, seed=57),
+    "m16_g6_bs32": lambda: multi([2, 100, 2049], [2, 4, 3], hq=12, hkv=2, d=128, bs=32, seed=58),
+    "m16_edges_g4": lambda: multi([8, 9, 513, 4100], [8, 9, 8, 3], hq=32, hkv=8, d=128, seed=59),
 }
 
 
