@@ -319,13 +319,13 @@ class StepPlan:
             col_max = 4 * tpg
             maxq = max(int(wl.query_lens.max()), 1)
             # the launches paged_attention_multi makes: token slot mapping +
-            # append; the decode kernel's column groups whenever G <= 8, and on
-            # bf16 pools the 16-column kernel beside them once a sequence may
-            # hold more than one group's tokens; the tensor-core kernel when
-            # one may need row tiles; the merge when a sequence may span
+            # append; the decode kernel's column groups whenever G <= 8; the
+            # tensor-core kernel when a sequence may need row tiles, else on
+            # bf16 pools the 16-column kernel once a sequence may hold more
+            # than one group's tokens; the merge when a sequence may span
             # several partitions
-            self.m16 = tpg > 0 and s.kv_dtype == "bf16" and maxq > tpg
             self.row = maxq > col_max
+            self.m16 = tpg > 0 and s.kv_dtype == "bf16" and maxq > tpg and not self.row
             self.launches = (2 + int(tpg > 0) + int(self.m16) + int(self.row)
                              + int(g.max_seq_len > self.part))
             self.kernels = ("token slot mapping + append + decode_kernel column groups "

@@ -11,10 +11,10 @@
 // Each sequence goes to one of three kernels in the same call:
 //   * one column group (n_b <= 8 / G): the decode kernel, whose 8 MMA
 //     columns per CTA then hold (token, head) pairs (pagedkv_decode.cu);
-//   * a few column groups (8 / G < n_b <= 4 x 8 / G): on bf16 pools the
-//     16-column kernel (pagedkv_multi_m16.cu), 16 / G tokens per CTA, so
-//     fewer CTAs read each block; on 8-bit pools the decode kernel's
-//     column groups;
+//   * a few column groups (8 / G < n_b <= 4 x 8 / G): in calls without
+//     long queries on bf16 pools the 16-column kernel (pagedkv_multi_m16.cu),
+//     16 / G tokens per CTA, so fewer CTAs read each block; otherwise the
+//     decode kernel's column groups;
 //   * longer queries: the tensor-core kernel with TMEM accumulators
 //     (pagedkv_multi_tc.cu), 128 rows per CTA.
 // All write the normalised output (one partition) or per-row (m, l, acc)
@@ -32,8 +32,9 @@
 namespace pagedkv {
 
 // pagedkv_multi_m16.cu: sequences with n_lo < n_b <= a.col_max_n query
-// tokens, `vgroups` 16-column CTAs per sequence (bf16 pools).
-kv_status launch_multi_m16(const DecodeArgs& a, int n_lo, int vgroups, cudaStream_t s);
+// tokens, `vgroups` 16-column CTAs per sequence (bf16 pools), longest
+// sequences first when `rank` is set.
+kv_status launch_multi_m16(const DecodeArgs& a, int n_lo, int vgroups, bool rank, cudaStream_t s);
 
 namespace {
 
@@ -248,15 +249,18 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
   const int GQ = num_q_heads / num_kv_heads;
   // Sequences with few query tokens (at most 4 x 8 / G): the decode
   // kernel's 8 columns per CTA hold (token, head) pairs, 8 / G tokens per
-  // column group; on bf16 pools those with more than one group's tokens go
-  // to the 16-column kernel instead (16 / G tokens per CTA).  Longer
-  // queries: the tensor-core kernel, in the same call when both kinds occur.
+  // column group; in calls of few-query sequences alone on bf16 pools,
+  // those with more than one group's tokens go to the 16-column kernel
+  // instead (16 / G tokens per CTA).  Longer queries: the tensor-core kernel,
+  // in the same call when both kinds occur.
   const int tpg = GQ <= kMaxGroup ? kMaxGroup / GQ : 0;
   const int col_max_n = tpg * kMaxVGroups;               // 0 when G > 8
   const int vgroups = tpg > 0 ? (min(max_query_len, col_max_n) + tpg - 1) / tpg : 0;
   const bool column_path = tpg > 0;                       // some sequences may use it
   const bool row_path = max_query_len > col_max_n;        // some sequences may need it
-  const bool m16_path = column_path && dtype == KV_DTYPE_BF16 && max_query_len > tpg;
+  // (batches that also hold long queries keep the column groups for all
+  // few-query sequences: the tensor-core kernel shares the GPU with them)
+  const bool m16_path = column_path && !row_path && dtype == KV_DTYPE_BF16 && max_query_len > tpg;
   const int tpg16 = column_path ? kM16Cols / GQ : 0;
   const int vgroups16 = m16_path ? (min(max_query_len, col_max_n) + tpg16 - 1) / tpg16 : 0;
   if (batch == 0 || num_tokens == 0) return KV_OK;
@@ -320,18 +324,17 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
   auto tc_ctas = [&](int per_sm) {
     return (int)std::min<int64_t>(tiles * num_kv_heads * a.max_parts, (int64_t)di.num_sms * per_sm);
   };
-  // The few-query kernels on one stream: the decode kernel's column groups
-  // (with the 16-column kernel in the call, only sequences of one group)
-  // and the 16-column CTAs.
-  auto launch_columns = [&]() -> kv_status {
-    if (!m16_path) return launch_decode(a, s);
+  if (m16_path) {
+    // the decode kernel's column groups for sequences of one group's tokens
+    // (often none: its CTAs then only read the offsets), then the 16-column
+    // CTAs, longest sequences first
     DecodeArgs one = a;
     one.col_max_n = tpg;
     one.vgroups = 1;
-    kv_status r = launch_decode(one, s);
-    return r != KV_OK ? r : launch_multi_m16(a, tpg, vgroups16, s);
-  };
-  if (row_path && column_path) {
+    if ((st = launch_decode(one, s)) != KV_OK ||
+        (st = launch_multi_m16(a, tpg, vgroups16, true, s)) != KV_OK)
+      return st;
+  } else if (row_path && column_path) {
     // the tensor-core kernel (tensor-bound) beside the column groups (HBM-bound)
     SideLane* lane = nullptr;
     if ((st = side_lane(di.device, &lane)) != KV_OK ||
@@ -340,12 +343,12 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
         (st = launch_multi_tc(a, tc_ctas(1), lane->stream)) != KV_OK ||
         (st = cuda_check(cudaEventRecord(lane->join, lane->stream), "cudaEventRecord")) != KV_OK)
       return st;
-    st = launch_columns();
+    st = launch_decode(a, s);
     const kv_status sj = cuda_check(cudaStreamWaitEvent(s, lane->join, 0), "cudaStreamWaitEvent");
     if (st != KV_OK) return st;
     if (sj != KV_OK) return sj;
   } else if (column_path) {
-    if ((st = launch_columns()) != KV_OK) return st;
+    if ((st = launch_decode(a, s)) != KV_OK) return st;
   } else if (row_path) {
     if ((st = launch_multi_tc(a, tc_ctas(1), s)) != KV_OK) return st;
   }

@@ -44,6 +44,8 @@ constexpr int kCols = 16;                                // query columns per CT
 constexpr int kThreads = (kConsumers + 1) * 32;          // + one producer warp
 constexpr int kMaxBlocks = kMaxColumnPartTokens / 16;    // blocks per partition (max)
 constexpr int kSpec = (kMaxBlocks + kThreads - 1) / kThreads;
+// Batches of up to this many sequences may be taken longest first.
+constexpr int kRankMax = 128;
 
 // 2^x on the special-function unit (PTX ex2.approx.ftz.f32; 2^-inf = +0).
 __device__ __forceinline__ float ex2(float x) {
@@ -70,7 +72,7 @@ template <int D, int BS>
 __global__ void __launch_bounds__(kThreads, Ring<D, BS>::kMinCtas)
     multi_m16_kernel(const __grid_constant__ CUtensorMap k_map,
                      const __grid_constant__ CUtensorMap v_map, const DecodeArgs a, int n_lo,
-                     int vgroups) {
+                     int vgroups, int rank) {
   using G = Geo<D, BS, false>;
   constexpr int S = Ring<D, BS>::kStages;
   constexpr int kKSteps = D / 16;                         // k-steps of S over d
@@ -78,10 +80,34 @@ __global__ void __launch_bounds__(kThreads, Ring<D, BS>::kMinCtas)
   extern __shared__ unsigned char smem_raw[];
   __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
   __shared__ int cta_bad, cta_timeout;
+  __shared__ int rank_len[kRankMax];
+  __shared__ int rank_seq;
 
   const int hk = blockIdx.x;
   const int part = a.reverse_parts ? (int)(gridDim.z - 1 - blockIdx.z) : (int)blockIdx.z;
-  const int b = (int)(blockIdx.y / vgroups), vg = (int)(blockIdx.y % vgroups);
+  const int vg = (int)(blockIdx.y % vgroups);
+  int b = (int)(blockIdx.y / vgroups);
+  if (rank) {
+    // Longest sequences first: CTA row r takes the sequence of rank r by
+    // (length descending, index ascending), so that the last wave holds the
+    // short ones (with one partition per sequence, CTA lengths differ
+    // several-fold).  The ranks are a permutation: every sequence is taken
+    // exactly once.
+    const int r = b;
+    for (int i = threadIdx.x; i < a.batch; i += kThreads) rank_len[i] = a.seq_lens[i];
+    __syncthreads();
+    for (int i = threadIdx.x; i < a.batch; i += kThreads) {
+      const int li = rank_len[i];
+      int ri = 0;
+      for (int k = 0; k < a.batch; ++k) {
+        const int lk = rank_len[k];
+        ri += (lk > li || (lk == li && k < i)) ? 1 : 0;
+      }
+      if (ri == r) rank_seq = i;
+    }
+    __syncthreads();
+    b = rank_seq;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int Hq = a.num_q_heads, Hkv = a.num_kv_heads;
@@ -486,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, Ring<D, BS>::kMinCtas)
 }
 
 template <int D, int BS>
-kv_status launch_t(const DecodeArgs& a, int n_lo, int vgroups, cudaStream_t s) {
+kv_status launch_t(const DecodeArgs& a, int n_lo, int vgroups, int rank, cudaStream_t s) {
   static std::mutex mu;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -506,15 +532,16 @@ kv_status launch_t(const DecodeArgs& a, int n_lo, int vgroups, cudaStream_t s) {
   CUtensorMap km, vm;
   if ((st = make_kv_maps(a, &km, &vm)) != KV_OK) return st;
   const dim3 grid(a.num_kv_heads, a.batch * vgroups, a.max_parts);
-  multi_m16_kernel<D, BS><<<grid, kThreads, Ring<D, BS>::kSmemBytes, s>>>(km, vm, a, n_lo, vgroups);
+  multi_m16_kernel<D, BS><<<grid, kThreads, Ring<D, BS>::kSmemBytes, s>>>(km, vm, a, n_lo, vgroups, rank);
   return cuda_check(cudaGetLastError(), "multi_m16_kernel launch");
 }
 
 }  // namespace
 
 // Few-token multi-token queries with n_lo < n_b <= a.col_max_n on 16-column
-// CTAs (bf16 pools); `vgroups` 16-column groups per sequence.
-kv_status launch_multi_m16(const DecodeArgs& a, int n_lo, int vgroups, cudaStream_t s) {
+// CTAs (bf16 pools); `vgroups` 16-column groups per sequence; `rank`: take
+// the sequences longest first (batches of up to kRankMax sequences).
+kv_status launch_multi_m16(const DecodeArgs& a, int n_lo, int vgroups, bool rank, cudaStream_t s) {
   if (a.dtype != KV_DTYPE_BF16 || vgroups <= 0)
     return fail(KV_ERR_INVALID_ARG, "paged_attention_multi: bad 16-column launch");
   if ((int64_t)a.batch * vgroups > 65535 || a.max_parts > 65535)
@@ -522,9 +549,12 @@ kv_status launch_multi_m16(const DecodeArgs& a, int n_lo, int vgroups, cudaStrea
   if (a.part_tokens / a.block_size > kMaxBlocks || a.part_tokens % a.block_size)
     return fail(KV_ERR_INVALID_ARG, "partition must be a multiple of block_size, at most %d blocks",
                 kMaxBlocks);
+  const int rk = rank && a.batch <= kRankMax ? 1 : 0;
   if (a.head_dim == 128)
-    return a.block_size == 32 ? launch_t<128, 32>(a, n_lo, vgroups, s) : launch_t<128, 16>(a, n_lo, vgroups, s);
-  return a.block_size == 32 ? launch_t<64, 32>(a, n_lo, vgroups, s) : launch_t<64, 16>(a, n_lo, vgroups, s);
+    return a.block_size == 32 ? launch_t<128, 32>(a, n_lo, vgroups, rk, s)
+                              : launch_t<128, 16>(a, n_lo, vgroups, rk, s);
+  return a.block_size == 32 ? launch_t<64, 32>(a, n_lo, vgroups, rk, s)
+                            : launch_t<64, 16>(a, n_lo, vgroups, rk, s);
 }
 
 }  // namespace pagedkv
