@@ -27,6 +27,7 @@
 // memory and write the output (one partition) or (m, l, acc) partials that
 // the multi-token merge combines.  Every wait is bounded.  bf16 pools.
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -46,6 +47,21 @@ constexpr int kMaxBlocks = kMaxColumnPartTokens / 16;    // blocks per partition
 constexpr int kSpec = (kMaxBlocks + kThreads - 1) / kThreads;
 // Batches of up to this many sequences may be taken longest first.
 constexpr int kRankMax = 128;
+
+// One TMA request for a whole d128 K or V block of one head: a 5-D map
+// (d mod 64, row, d / 64, head, block) whose box holds both 64-element halves
+// of every row, laid out as two [bs][128 B] swizzled halves (the layout of
+// two 4-D boxes).  Each request carries a fixed cost in the SM's TMA unit:
+// with every block read by two CTAs, 2 KB boxes left the loads behind the
+// consumers.
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %2, %2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(c3), "r"(c4), "r"(bar)
+      : "memory");
+}
 
 // 2^x on the special-function unit (PTX ex2.approx.ftz.f32; 2^-inf = +0).
 __device__ __forceinline__ float ex2(float x) {
@@ -260,10 +276,12 @@ __global__ void __launch_bounds__(kThreads, Ring<D, BS>::kMinCtas)
         if (lane == 0) {
           const uint32_t kdst = stages + (uint32_t)((s * kConsumers + c) * G::kBlockBytes);
           const uint32_t vdst = kdst + G::kTensorBytes;
-#pragma unroll
-          for (int x = 0; x < G::kBoxes; ++x) {
-            tma_load_4d(kdst + x * G::kBoxBytes, &k_map, fb, x * G::kBoxElems, hk, 0, p);
-            tma_load_4d(vdst + x * G::kBoxBytes, &v_map, fb, x * G::kBoxElems, hk, 0, p);
+          if constexpr (D == 128) {
+            tma_load_5d(kdst, &k_map, fb, hk, p);
+            tma_load_5d(vdst, &v_map, fb, hk, p);
+          } else {
+            tma_load_4d(kdst, &k_map, fb, 0, hk, 0, p);
+            tma_load_4d(vdst, &v_map, fb, 0, hk, 0, p);
           }
         }
       }
@@ -511,6 +529,79 @@ __global__ void __launch_bounds__(kThreads, Ring<D, BS>::kMinCtas)
   }
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// The 5-D map of tma_load_5d over a bf16 d128 pool [NB, bs, Hkv, 128]:
+// dims (64, bs, 2, Hkv, NB) with byte strides (row, 128, head, block).
+kv_status make_map5(CUtensorMap* map, const void* pool, const DecodeArgs& a) {
+  auto fn = encode_fn();
+  if (!fn) return fail(KV_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+  const cuuint64_t head_bytes = 128 * 2, row_bytes = (cuuint64_t)a.num_kv_heads * head_bytes;
+  const cuuint64_t dims[5] = {64, (cuuint64_t)a.block_size, 2, (cuuint64_t)a.num_kv_heads,
+                              (cuuint64_t)a.num_blocks};
+  const cuuint64_t strides[4] = {row_bytes, 128, head_bytes, row_bytes * a.block_size};
+  const cuuint32_t box[5] = {64, (cuuint32_t)a.block_size, 2, 1, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(pool), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(KV_ERR_CUDA, "cuTensorMapEncodeTiled (5-D) failed (%d)", (int)r);
+  return KV_OK;
+}
+
+// Maps of this kernel: 5-D for d128, the shared 4-D maps for d64 (one
+// 128-byte box per row already).  The 5-D maps are encoded once per (device,
+// pools, geometry) and then served from a small cache.
+kv_status m16_maps(const DecodeArgs& a, CUtensorMap* km, CUtensorMap* vm) {
+  if (a.head_dim != 128) return make_kv_maps(a, km, vm);
+  struct Entry {
+    const void *k = nullptr, *v = nullptr;
+    int device = -1, block_size = 0, num_kv_heads = 0, num_blocks = 0;
+    CUtensorMap km, vm;
+  };
+  static std::mutex mu;
+  static Entry cache[8];
+  static int next = 0;
+  int dev = 0;
+  kv_status st = cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
+  if (st != KV_OK) return st;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Entry& e : cache)
+    if (e.device == dev && e.k == a.k_cache && e.v == a.v_cache && e.block_size == a.block_size &&
+        e.num_kv_heads == a.num_kv_heads && e.num_blocks == a.num_blocks) {
+      *km = e.km;
+      *vm = e.vm;
+      return KV_OK;
+    }
+  Entry& e = cache[next];
+  e.device = -1;
+  if ((st = make_map5(&e.km, a.k_cache, a)) != KV_OK || (st = make_map5(&e.vm, a.v_cache, a)) != KV_OK)
+    return st;
+  e.device = dev;
+  e.k = a.k_cache;
+  e.v = a.v_cache;
+  e.block_size = a.block_size;
+  e.num_kv_heads = a.num_kv_heads;
+  e.num_blocks = a.num_blocks;
+  next = (next + 1) % 8;
+  *km = e.km;
+  *vm = e.vm;
+  return KV_OK;
+}
+
 template <int D, int BS>
 kv_status launch_t(const DecodeArgs& a, int n_lo, int vgroups, int rank, cudaStream_t s) {
   static std::mutex mu;
@@ -530,7 +621,7 @@ kv_status launch_t(const DecodeArgs& a, int n_lo, int vgroups, int rank, cudaStr
     }
   }
   CUtensorMap km, vm;
-  if ((st = make_kv_maps(a, &km, &vm)) != KV_OK) return st;
+  if ((st = m16_maps(a, &km, &vm)) != KV_OK) return st;
   const dim3 grid(a.num_kv_heads, a.batch * vgroups, a.max_parts);
   multi_m16_kernel<D, BS><<<grid, kThreads, Ring<D, BS>::kSmemBytes, s>>>(km, vm, a, n_lo, vgroups, rank);
   return cuda_check(cudaGetLastError(), "multi_m16_kernel launch");
