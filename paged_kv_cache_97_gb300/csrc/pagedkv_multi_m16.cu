@@ -1,5 +1,5 @@
-// pagedkv_multi_m16.cu -- few-token multi-token queries with 16 (query
-// token, grouped head) columns per CTA on the MMA's M side (speculative
+// pagedkv_multi_m16.cu -- few-token multi-token queries with the (query
+// token, grouped head) columns on the MMA's M side, 16 per m-tile (speculative
 // verification, “让 Agent 跑得快：LLM 推理服务”, §六 投机解码: the target model
 // scores the draft tokens in one parallel pass).
 //
@@ -7,9 +7,11 @@
 // L_b - n_b + i and attends positions 0 .. L_b - n_b + i.  This kernel takes
 // the sequences whose n_b is too large for one 8-column group of the decode
 // kernel's multi-token mode (8 / G tokens) but small enough for its column
-// path (at most 4 x 8 / G tokens): a CTA serves one (KV head, sequence, token
-// partition) and a "group" of 16 / G query tokens times the G heads.  With
-// the columns on M (mma.sync m16n8k16, bf16, fp32 accumulate):
+// path (at most 4 x 8 / G tokens).  An m-tile holds 16 / G query tokens times
+// the G heads; a CTA serves one (KV head, sequence, token partition) and MT
+// m-tiles: MT = 1 when every sequence fits 16 columns, else MT = 2, which
+// covers every sequence of the path in one CTA.  With the columns on M
+// (mma.sync m16n8k16, bf16, fp32 accumulate):
 //   S[16 cols x 16 keys] = Q[16 x d] . K^T   (B = K rows by ldmatrix)
 //   O[16 cols x d]      += P[16 x 16] . V    (B = V rows by ldmatrix.trans)
 // P is packed straight from the S accumulators (the fragment of S for keys
@@ -22,10 +24,12 @@
 // four lanes that hold its scores.
 //
 // The pipeline is the decode kernel's: a producer warp walks the partition's
-// blocks and issues TMA tensor loads of K and V into an mbarrier ring, three
-// consumer warps take one block of each stage, then combine through shared
-// memory and write the output (one partition) or (m, l, acc) partials that
-// the multi-token merge combines.  Every wait is bounded.  bf16 pools.
+// blocks and issues TMA tensor loads of K and V into an mbarrier ring; each
+// block of a stage is taken by one consumer warp per m-tile (so a block is
+// loaded once for all the sequence's columns), and the warps then combine
+// through shared memory and write the output (one partition) or (m, l, acc)
+// partials that the multi-token merge combines.  Every wait is bounded.
+// bf16 pools.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -41,10 +45,12 @@ namespace {
 
 using namespace dev;
 
-constexpr int kCols = 16;                                // query columns per CTA (the MMA's M)
-constexpr int kThreads = (kConsumers + 1) * 32;          // + one producer warp
+constexpr int kCols = 16;                                // query columns per m-tile (the MMA's M)
 constexpr int kMaxBlocks = kMaxColumnPartTokens / 16;    // blocks per partition (max)
-constexpr int kSpec = (kMaxBlocks + kThreads - 1) / kThreads;
+// Threads of a CTA with MT m-tiles: kConsumers warps per m-tile + one
+// producer warp.
+template <int MT>
+constexpr int kThreadsOf = (kConsumers * MT + 1) * 32;
 // Batches of up to this many sequences may be taken longest first.
 constexpr int kRankMax = 128;
 
@@ -70,27 +76,42 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Stage ring of up to 72 KB (three stages of three bf16 d128 16-row
-// blocks): three CTAs of it fit an SM's 228 KB, and with two stages in flight
-// per CTA the loads cover the time the consumers take per stage.
-template <int D, int BS>
+// Shared memory of a CTA.  MT = 1: a stage ring of up to 72 KB (three
+// stages of three bf16 d128 16-row blocks), Q in registers: three CTAs fit
+// an SM's 228 KB, and with two stages in flight per CTA the loads cover the
+// time the consumers take per stage.  MT = 2: up to 100 KB of ring and the
+// Q tile (rows padded by 16 bytes, so ldmatrix reads it without bank
+// conflicts): two CTAs per SM, their registers freed of Q.
+template <int D, int BS, int MT>
 struct Ring {
   using G = Geo<D, BS, false>;
-  static constexpr int kStages0 = (72 * 1024) / G::kStageBytes;
+  static constexpr int kStages0 = (MT == 1 ? 72 * 1024 : 100 * 1024) / G::kStageBytes;
   static constexpr int kStages = kStages0 < 2 ? 2 : (kStages0 > kMaxStages ? kMaxStages : kStages0);
-  static constexpr int kSmemBytes = kStages * G::kStageBytes + 1024;   // + alignment slack
-  // CTAs per SM that shared memory admits (at most 3; 1 KB reserved per CTA
-  // and a little static memory): the register budget's divisor
-  static constexpr int kMinCtas = 3 * (kSmemBytes + 2048) <= 228 * 1024 ? 3 : 2;
+  static constexpr int kRingBytes = kStages * G::kStageBytes;
+  static constexpr int kQRow = (D + 8) * 2;                             // bytes per Q row
+  static constexpr int kQBytes = MT == 1 ? 0 : MT * kCols * kQRow;
+  static constexpr int kSmemBytes = kRingBytes + kQBytes + 1024;       // + alignment slack
+  // CTAs per SM that shared memory admits (1 KB reserved per CTA and a
+  // little static memory): the register budget's divisor
+  static constexpr int kWant = MT == 1 ? 3 : 2;
+  static constexpr int kMinCtas = kWant * (kSmemBytes + 2048) <= 228 * 1024 ? kWant : kWant - 1;
+  // the combine buffers reuse the ring
+  static_assert((2 * kConsumers * MT * kCols + kConsumers * MT * kCols * D) * 4 <= kRingBytes,
+                "combine buffers exceed the stage ring");
 };
 
-template <int D, int BS>
-__global__ void __launch_bounds__(kThreads, Ring<D, BS>::kMinCtas)
+template <int D, int BS, int MT>
+__global__ void __launch_bounds__(kThreadsOf<MT>, Ring<D, BS, MT>::kMinCtas)
     multi_m16_kernel(const __grid_constant__ CUtensorMap k_map,
                      const __grid_constant__ CUtensorMap v_map, const DecodeArgs a, int n_lo,
                      int vgroups, int rank) {
   using G = Geo<D, BS, false>;
-  constexpr int S = Ring<D, BS>::kStages;
+  using R = Ring<D, BS, MT>;
+  constexpr int S = R::kStages;
+  constexpr int kThreads = kThreadsOf<MT>;
+  constexpr int kWarpsC = kConsumers * MT;                // consumer warps
+  constexpr int kColsC = kCols * MT;                      // columns of the CTA
+  constexpr int kSpec = (kMaxBlocks + kThreads - 1) / kThreads;
   constexpr int kKSteps = D / 16;                         // k-steps of S over d
   constexpr int kDBlocks = D / 8;                         // 8-wide d blocks of O
   extern __shared__ unsigned char smem_raw[];
@@ -128,7 +149,8 @@ __global__ void __launch_bounds__(kThreads, Ring<D, BS>::kMinCtas)
   const int g = lane >> 2, t = lane & 3;
   const int Hq = a.num_q_heads, Hkv = a.num_kv_heads;
   const int GQ = Hq / Hkv;                               // grouped query heads (1..8)
-  const int TPG = kCols / GQ;                            // query tokens per group
+  const int TPG = kCols / GQ;                            // query tokens per m-tile
+  const int tok0 = vg * MT * TPG;                        // the CTA's first query token
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
 
   // This kernel's sequences: n_lo < n <= col_max_n (the decode kernel takes
@@ -137,12 +159,14 @@ __global__ void __launch_bounds__(kThreads, Ring<D, BS>::kMinCtas)
   const int nq = a.query_start[b + 1] - q0;
   if (nq <= n_lo || nq > a.col_max_n) return;
   const bool rows_ok = q0 >= 0 && nq >= 0 && q0 + nq <= a.num_tokens;
-  // Row of the q / out tensors that column c serves (-1: padding): token
-  // vg * TPG + c / GQ of the sequence, head c % GQ of the group.
+  // Row of the q / out tensors that column c (m-tile c / 16) serves (-1:
+  // padding): token tok0 + (c / 16) TPG + (c % 16) / GQ of the sequence, head
+  // (c % 16) % GQ of the group.
   auto col_row = [&](int c) -> int64_t {
-    const int i = vg * TPG + c / GQ;
-    return (rows_ok && c < TPG * GQ && i < nq) ? (int64_t)(q0 + i) * Hq + (int64_t)hk * GQ + c % GQ
-                                                 : -1;
+    const int cc = c % kCols;
+    const int i = tok0 + (c / kCols) * TPG + cc / GQ;
+    return (rows_ok && cc < TPG * GQ && i < nq) ? (int64_t)(q0 + i) * Hq + (int64_t)hk * GQ + cc % GQ
+                                                  : -1;
   };
 
   // Block ids of the partition and the consumers' Q fragments are loaded
@@ -157,20 +181,35 @@ __global__ void __launch_bounds__(kThreads, Ring<D, BS>::kMinCtas)
     const int j = threadIdx.x + r * kThreads;
     spec_id[r] = j < spec_blk ? bt[j] : -1;
   }
-  // A fragments of Q (rows = columns g and g + 8, k = d): a0 = (g, 2t..2t+1),
+  // Q: A fragments (rows = columns g and g + 8, k = d): a0 = (g, 2t..2t+1),
   // a1 = (g + 8, 2t..), a2 = (g, 2t + 8..), a3 = (g + 8, 2t + 8..) of each
-  // 16-wide k-step; padding columns are zero.
-  uint32_t qa[kKSteps][4];
-  if (warp < kConsumers) {
-    const int64_t r0 = col_row(g), r1 = col_row(g + 8);
-    const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.q);
+  // 16-wide k-step; padding columns are zero.  MT = 1: in registers; MT = 2:
+  // 16-byte pieces of the Q rows, stored to the shared Q tile after the
+  // checks and read by ldmatrix per k-step.
+  const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.q);
+  constexpr int kQPieces = kColsC * D / 8;                // 16-byte pieces of the Q tile
+  constexpr int kQPer = MT == 1 ? 1 : (kQPieces + kThreads - 1) / kThreads;
+  uint32_t qa[MT == 1 ? kKSteps : 1][4];
+  uint4 qpiece[kQPer];
+  if constexpr (MT == 1) {
+    if (warp < kWarpsC) {
+      const int64_t r0 = col_row(g), r1 = col_row(g + 8);
 #pragma unroll
-    for (int ks = 0; ks < kKSteps; ++ks) {
-      const int d0 = 16 * ks + 2 * t;
-      qa[ks][0] = r0 >= 0 ? *reinterpret_cast<const uint32_t*>(qb + r0 * D + d0) : 0u;
-      qa[ks][1] = r1 >= 0 ? *reinterpret_cast<const uint32_t*>(qb + r1 * D + d0) : 0u;
-      qa[ks][2] = r0 >= 0 ? *reinterpret_cast<const uint32_t*>(qb + r0 * D + d0 + 8) : 0u;
-      qa[ks][3] = r1 >= 0 ? *reinterpret_cast<const uint32_t*>(qb + r1 * D + d0 + 8) : 0u;
+      for (int ks = 0; ks < kKSteps; ++ks) {
+        const int d0 = 16 * ks + 2 * t;
+        qa[ks][0] = r0 >= 0 ? *reinterpret_cast<const uint32_t*>(qb + r0 * D + d0) : 0u;
+        qa[ks][1] = r1 >= 0 ? *reinterpret_cast<const uint32_t*>(qb + r1 * D + d0) : 0u;
+        qa[ks][2] = r0 >= 0 ? *reinterpret_cast<const uint32_t*>(qb + r0 * D + d0 + 8) : 0u;
+        qa[ks][3] = r1 >= 0 ? *reinterpret_cast<const uint32_t*>(qb + r1 * D + d0 + 8) : 0u;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int r = 0; r < kQPer; ++r) {
+      const int i = threadIdx.x + r * kThreads;
+      const int64_t row = i < kQPieces ? col_row(i / (D / 8)) : -1;
+      qpiece[r] = row >= 0 ? *reinterpret_cast<const uint4*>(qb + row * D + (i % (D / 8)) * 8)
+                           : make_uint4(0u, 0u, 0u, 0u);
     }
   }
 
@@ -184,22 +223,22 @@ __global__ void __launch_bounds__(kThreads, Ring<D, BS>::kMinCtas)
       if (threadIdx.x == 0 && vg == 0) atomicOr(a.flags, PAGEDKV_FLAG_BAD_SEQ_LEN);
       // (with several partitions, the multi-token merge zeroes these rows)
       if (a.max_parts == 1)
-        for (int i = threadIdx.x; i < kCols * D; i += blockDim.x) {
+        for (int i = threadIdx.x; i < kColsC * D; i += blockDim.x) {
           const int64_t r = col_row(i / D);
           if (r >= 0) out[r * D + i % D] = __float2bfloat16_rn(0.0f);
         }
     }
     return;
   }
-  if (vg * TPG >= nq) return;                            // a group with no queries
+  if (tok0 >= nq) return;                                // a group with no queries
   if (t0 >= L) return;
-  // keys up to this group's last query position
+  // keys up to the CTA's last query position
   int t1 = min(t0 + a.part_tokens, L);
-  t1 = min(t1, L - nq + min(nq - 1, vg * TPG + TPG - 1) + 1);
+  t1 = min(t1, L - nq + min(nq - 1, tok0 + MT * TPG - 1) + 1);
   const bool direct = a.max_parts == 1;
   if (t1 <= t0) {
-    // every query of this group precedes the partition: empty partials
-    for (int i = threadIdx.x; i < kCols * D; i += blockDim.x) {
+    // every query of this CTA precedes the partition: empty partials
+    for (int i = threadIdx.x; i < kColsC * D; i += blockDim.x) {
       const int64_t r = col_row(i / D);
       if (r < 0) continue;
       const int64_t sl = r * a.slots + part;
@@ -213,6 +252,19 @@ __global__ void __launch_bounds__(kThreads, Ring<D, BS>::kMinCtas)
   }
   const int nblk = (t1 - 1) / BS - first_blk + 1;        // >= 1, <= spec_blk
   const uint32_t stages = (smem_addr(smem_raw) + 1023u) & ~1023u;
+  const uint32_t qtile = stages + R::kRingBytes;           // MT = 2: [MT x 16][kQRow]
+  if constexpr (MT > 1) {
+#pragma unroll
+    for (int r = 0; r < kQPer; ++r) {
+      const int i = threadIdx.x + r * kThreads;
+      if (i < kQPieces) {
+        const uint32_t dst = qtile + (uint32_t)((i / (D / 8)) * R::kQRow + (i % (D / 8)) * 16);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(qpiece[r].x),
+                     "r"(qpiece[r].y), "r"(qpiece[r].z), "r"(qpiece[r].w)
+                     : "memory");
+      }
+    }
+  }
 
   // ---- set-up: barriers, and a check of the partition's block ids ---------
   if (threadIdx.x == 0) {
@@ -220,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, Ring<D, BS>::kMinCtas)
     cta_timeout = 0;
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_addr(&full_bar[s]), 1);
-      mbar_init(smem_addr(&empty_bar[s]), kConsumers);
+      mbar_init(smem_addr(&empty_bar[s]), kWarpsC);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -241,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, Ring<D, BS>::kMinCtas)
 #pragma unroll
   for (int i = 0; i < kDBlocks; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
 
-  if (!bad && warp == kConsumers) {
+  if (!bad && warp == kWarpsC) {
     // ======================= producer =======================================
     // Block ids 32 at a time, lane l holding block 32 k + l of chunk k (the
     // ids were checked above; the table is read again here, from L2, with
@@ -296,12 +348,13 @@ __global__ void __launch_bounds__(kThreads, Ring<D, BS>::kMinCtas)
     if (!ok && lane == 0) cta_timeout = 1;
   } else if (!bad) {
     // ======================= consumers =====================================
-    const int w = warp;
+    // warp = mt * kConsumers + w: block w of every stage, columns of m-tile mt
+    const int w = warp % kConsumers, mt = warp / kConsumers;
     const float kfac = a.scale_log2;
     // causal limits of this lane's columns g and g + 8 (padding: no limit),
-    // and the group's first query position: a block whose last key is at or
+    // and the m-tile's first query position: a block whose last key is at or
     // before it is visible to every column
-    const int pos_lo = L - nq + vg * TPG;
+    const int pos_lo = L - nq + tok0 + mt * TPG;
     const int cpos0 = g < TPG * GQ ? pos_lo + g / GQ : 0x7fffffff;
     const int cpos1 = g + 8 < TPG * GQ ? pos_lo + (g + 8) / GQ : 0x7fffffff;
     // ldmatrix row addresses inside a block (the same for K and V): matrix
@@ -313,6 +366,10 @@ __global__ void __launch_bounds__(kThreads, Ring<D, BS>::kMinCtas)
 #pragma unroll
       for (int ks = 0; ks < kKSteps; ++ks) off[ks] = chunk_off<G>(row, 2 * ks + (lane >> 4));
     }
+    // MT = 2: this lane's ldmatrix row of the m-tile's Q (matrix q = lane / 8
+    // covers columns 8 (q & 1) .. + 7 and d 8 (q >> 1) .. + 7 of a k-step)
+    const uint32_t qrow = qtile + (uint32_t)((mt * kCols + ((lane >> 3) & 1) * 8 + (lane & 7)) * R::kQRow +
+                                             (lane >> 4) * 16);
     bool ok = true;
     for (int it = 0; it < n_iter; ++it) {
       const int s = it % S;
@@ -342,8 +399,15 @@ __global__ void __launch_bounds__(kThreads, Ring<D, BS>::kMinCtas)
           for (int ks = 0; ks < kKSteps; ++ks) {
             uint32_t r[4];
             ldsm_x4(r, kb + off[ks] + tile * 16 * G::kBoxRow);
-            mma16816<false>(c[ks % kSplit], qa[ks], r[0], r[2]);
-            mma16816<false>(c[kSplit + ks % kSplit], qa[ks], r[1], r[3]);
+            if constexpr (MT == 1) {
+              mma16816<false>(c[ks % kSplit], qa[ks], r[0], r[2]);
+              mma16816<false>(c[kSplit + ks % kSplit], qa[ks], r[1], r[3]);
+            } else {
+              uint32_t qf[4];
+              ldsm_x4(qf, qrow + ks * 32);
+              mma16816<false>(c[ks % kSplit], qf, r[0], r[2]);
+              mma16816<false>(c[kSplit + ks % kSplit], qf, r[1], r[3]);
+            }
           }
 #pragma unroll
           for (int nb = 0; nb < 2; ++nb)
@@ -453,10 +517,10 @@ __global__ void __launch_bounds__(kThreads, Ring<D, BS>::kMinCtas)
   __syncthreads();  // all fills landed and all stage reads done
   const bool failed = bad || cta_timeout != 0;
   float* red = reinterpret_cast<float*>(smem_raw + (stages - smem_addr(smem_raw)));
-  float* red_m = red;                              // [kConsumers][kCols]
-  float* red_l = red + kConsumers * kCols;         // [kConsumers][kCols]
-  float* red_acc = red + 2 * kConsumers * kCols;   // [kConsumers][kCols][D]
-  if (!failed && warp < kConsumers) {
+  float* red_m = red;                              // [kWarpsC][kCols]
+  float* red_l = red + kWarpsC * kCols;            // [kWarpsC][kCols]
+  float* red_acc = red + 2 * kWarpsC * kCols;      // [kWarpsC][kCols][D]
+  if (!failed && warp < kWarpsC) {
 #pragma unroll
     for (int off = 1; off < 4; off <<= 1) {
       l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], off);
@@ -483,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, Ring<D, BS>::kMinCtas)
   if (failed) {
     if (threadIdx.x == 0)
       atomicOr(a.flags, bad ? PAGEDKV_FLAG_BAD_BLOCK : PAGEDKV_FLAG_WAIT_TIMEOUT);
-    for (int i = threadIdx.x; i < kCols * D; i += blockDim.x) {
+    for (int i = threadIdx.x; i < kColsC * D; i += blockDim.x) {
       const int c = i / D, e = i % D;
       const int64_t row = col_row(c);
       if (row < 0) continue;
@@ -501,20 +565,22 @@ __global__ void __launch_bounds__(kThreads, Ring<D, BS>::kMinCtas)
     return;
   }
 
-  for (int i = threadIdx.x; i < kCols * D; i += blockDim.x) {
+  for (int i = threadIdx.x; i < kColsC * D; i += blockDim.x) {
     const int c = i / D, e = i % D;
     const int64_t row = col_row(c);
     if (row < 0) continue;
+    // the m-tile's warps mt * kConsumers .. + kConsumers - 1, its column cc
+    const int w0 = (c / kCols) * kConsumers, cc = c % kCols;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, red_m[w * kCols + c]);
+    for (int w = w0; w < w0 + kConsumers; ++w) M = fmaxf(M, red_m[w * kCols + cc]);
     const float Mz = M == -INFINITY ? 0.0f : M;    // a column with no key here
     float num = 0.0f, den = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kConsumers; ++w) {
-      const float f = exp2f(red_m[w * kCols + c] - Mz);  // 0 for a warp that saw no key
-      num = fmaf(f, red_acc[(w * kCols + c) * D + e], num);
-      den = fmaf(f, red_l[w * kCols + c], den);
+    for (int w = w0; w < w0 + kConsumers; ++w) {
+      const float f = exp2f(red_m[w * kCols + cc] - Mz);  // 0 for a warp that saw no key
+      num = fmaf(f, red_acc[(w * kCols + cc) * D + e], num);
+      den = fmaf(f, red_l[w * kCols + cc], den);
     }
     if (direct) {
       out[row * D + e] = __float2bfloat16_rn(num / den);
@@ -602,8 +668,9 @@ kv_status m16_maps(const DecodeArgs& a, CUtensorMap* km, CUtensorMap* vm) {
   return KV_OK;
 }
 
-template <int D, int BS>
-kv_status launch_t(const DecodeArgs& a, int n_lo, int vgroups, int rank, cudaStream_t s) {
+template <int D, int BS, int MT>
+kv_status launch_t(const DecodeArgs& a, int n_lo, int groups, int rank, cudaStream_t s) {
+  using R = Ring<D, BS, MT>;
   static std::mutex mu;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -612,9 +679,9 @@ kv_status launch_t(const DecodeArgs& a, int n_lo, int vgroups, int rank, cudaStr
   {
     std::lock_guard<std::mutex> lock(mu);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-      st = cuda_check(cudaFuncSetAttribute(multi_m16_kernel<D, BS>,
+      st = cuda_check(cudaFuncSetAttribute(multi_m16_kernel<D, BS, MT>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           Ring<D, BS>::kSmemBytes),
+                                           R::kSmemBytes),
                       "cudaFuncSetAttribute(multi_m16_kernel)");
       if (st != KV_OK) return st;
       attr_set[dev] = true;
@@ -622,15 +689,24 @@ kv_status launch_t(const DecodeArgs& a, int n_lo, int vgroups, int rank, cudaStr
   }
   CUtensorMap km, vm;
   if ((st = m16_maps(a, &km, &vm)) != KV_OK) return st;
-  const dim3 grid(a.num_kv_heads, a.batch * vgroups, a.max_parts);
-  multi_m16_kernel<D, BS><<<grid, kThreads, Ring<D, BS>::kSmemBytes, s>>>(km, vm, a, n_lo, vgroups, rank);
+  const dim3 grid(a.num_kv_heads, a.batch * groups, a.max_parts);
+  multi_m16_kernel<D, BS, MT><<<grid, kThreadsOf<MT>, R::kSmemBytes, s>>>(km, vm, a, n_lo, groups, rank);
   return cuda_check(cudaGetLastError(), "multi_m16_kernel launch");
+}
+
+// One m-tile per CTA when every sequence fits 16 columns (vgroups == 1),
+// else two, which cover every sequence of the path (at most 4 x 8 / G
+// tokens = 32 columns) in one CTA.
+template <int D, int BS>
+kv_status launch_mt(const DecodeArgs& a, int n_lo, int vgroups, int rank, cudaStream_t s) {
+  if (vgroups == 1) return launch_t<D, BS, 1>(a, n_lo, 1, rank, s);
+  return launch_t<D, BS, 2>(a, n_lo, (vgroups + 1) / 2, rank, s);
 }
 
 }  // namespace
 
 // Few-token multi-token queries with n_lo < n_b <= a.col_max_n on 16-column
-// CTAs (bf16 pools); `vgroups` 16-column groups per sequence; `rank`: take
+// m-tiles (bf16 pools); `vgroups` m-tiles per sequence at most; `rank`: take
 // the sequences longest first (batches of up to kRankMax sequences).
 kv_status launch_multi_m16(const DecodeArgs& a, int n_lo, int vgroups, bool rank, cudaStream_t s) {
   if (a.dtype != KV_DTYPE_BF16 || vgroups <= 0)
@@ -642,10 +718,10 @@ kv_status launch_multi_m16(const DecodeArgs& a, int n_lo, int vgroups, bool rank
                 kMaxBlocks);
   const int rk = rank && a.batch <= kRankMax ? 1 : 0;
   if (a.head_dim == 128)
-    return a.block_size == 32 ? launch_t<128, 32>(a, n_lo, vgroups, rk, s)
-                              : launch_t<128, 16>(a, n_lo, vgroups, rk, s);
-  return a.block_size == 32 ? launch_t<64, 32>(a, n_lo, vgroups, rk, s)
-                            : launch_t<64, 16>(a, n_lo, vgroups, rk, s);
+    return a.block_size == 32 ? launch_mt<128, 32>(a, n_lo, vgroups, rk, s)
+                              : launch_mt<128, 16>(a, n_lo, vgroups, rk, s);
+  return a.block_size == 32 ? launch_mt<64, 32>(a, n_lo, vgroups, rk, s)
+                            : launch_mt<64, 16>(a, n_lo, vgroups, rk, s);
 }
 
 }  // namespace pagedkv

@@ -98,6 +98,10 @@ CASES = {
     "m16_g3_d64": lambda: multi([7, 300, 1000, 33], [3, 8, 5, 6], hq=6, hkv=2, d=64, seed=57),
     "m16_g6_bs32": lambda: multi([2, 100, 2049], [2, 4, 3], hq=12, hkv=2, d=128, bs=32, seed=58),
     "m16_edges_g4": lambda: multi([8, 9, 513, 4100], [8, 9, 8, 3], hq=32, hkv=8, d=128, seed=59),
+    # every sequence within 16 columns: one m-tile per CTA (Q in registers)
+    "m16_one_tile_g4": lambda: multi([700, 33, 1500], [3, 4, 4], hq=32, hkv=8, d=128, seed=61),
+    "m16_one_tile_g2_bs32": lambda: multi([300, 1000, 77], [5, 8, 6], hq=4, hkv=2, d=64, bs=32,
+                                          seed=62),
     # few-query batches are taken longest first: equal lengths tie-break by index
     "m16_equal_lens": lambda: multi([300, 300, 40, 300, 40], [5, 3, 5, 4, 8], hq=32, hkv=8, d=128,
                                     seed=60),
