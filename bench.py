@@ -318,19 +318,21 @@ class StepPlan:
             tpg = 8 // G if G <= 8 else 0
             col_max = 4 * tpg
             maxq = max(int(wl.query_lens.max()), 1)
-            # the launches paged_attention_multi makes: token slot mapping +
-            # append; the decode kernel's column groups whenever G <= 8; the
-            # tensor-core kernel when a sequence may need row tiles, else on
-            # bf16 pools the 16-column kernel once a sequence may hold more
-            # than one group's tokens; the merge when a sequence may span
-            # several partitions
+            # the launches pagedkv_multi_step makes: the append (slot mapping
+            # fused in); the decode kernel's column groups whenever G <= 8,
+            # except beside the 16-column kernel on a batch whose sequences
+            # all have max_query_len tokens; the tensor-core kernel when a
+            # sequence may need row tiles, else on bf16 pools the 16-column
+            # kernel once a sequence may hold more than one group's tokens;
+            # the merge when a sequence may span several partitions
             self.row = maxq > col_max
             self.m16 = tpg > 0 and s.kv_dtype == "bf16" and maxq > tpg and not self.row
-            self.launches = (2 + int(tpg > 0) + int(self.m16) + int(self.row)
-                             + int(g.max_seq_len > self.part))
-            self.kernels = ("token slot mapping + append + decode_kernel column groups "
-                            "/ multi_m16_kernel (16 columns, bf16) / multi_tc_kernel "
-                            "(+ multi_merge_kernel), paged_attention_multi")
+            uniform = wl.num_tokens == s.batch * maxq
+            self.launches = (1 + int(tpg > 0 and not (self.m16 and uniform)) + int(self.m16)
+                             + int(self.row) + int(g.max_seq_len > self.part))
+            self.kernels = ("append_tokens_kernel + decode_kernel column groups / multi_m16_kernel "
+                            "(16-column tiles, bf16) / multi_tc_kernel (+ multi_merge_kernel), "
+                            "one pagedkv_multi_step")
         else:
             skip = s.shared_prefix_tokens if self.prefix else 0
             self.fn = g.prefix_step if self.prefix else g.fused_step

@@ -482,11 +482,14 @@ size_t pagedkv_multi_workspace_bytes(int num_tokens, int num_q_heads,
  * PAGEDKV_FLAG_BAD_SEQ_LEN or PAGEDKV_FLAG_BAD_BLOCK; offsets outside
  * [0, num_tokens] leave that sequence's rows unwritten and set
  * PAGEDKV_FLAG_BAD_SEQ_LEN (rows past max_query_len are not written).
- * Asynchronous on `stream`: one attention launch, plus a log-sum-exp merge
- * launch when the keys are split into partitions.  With at most 4 * (8 / G)
- * query tokens per sequence the decode kernel serves them (8 (token, head)
- * columns per CTA); longer queries go to a tensor-core kernel with TMEM
- * accumulators (128 query rows per CTA). */
+ * Asynchronous on `stream`: the attention launches, plus a log-sum-exp
+ * merge launch when the keys are split into partitions.  Sequences with at
+ * most 8 / G query tokens go to the decode kernel (8 (token, head) columns
+ * per CTA); with at most 4 * (8 / G), in calls without longer queries on
+ * bf16 pools, to a kernel with 16 columns per MMA tile (up to 32 per CTA,
+ * the decode kernel's launch left out when every sequence has max_query_len
+ * tokens), else to the decode kernel's column groups; longer queries go to
+ * a tensor-core kernel with TMEM accumulators (128 query rows per CTA). */
 kv_status paged_attention_multi(void *out, const void *q, const void *k_cache,
                                 const void *v_cache, const float *k_scale,
                                 const float *v_scale, const int32_t *block_tables,
@@ -498,6 +501,41 @@ kv_status paged_attention_multi(void *out, const void *q, const void *k_cache,
                                 int max_seq_len, float scale, kv_dtype dtype,
                                 void *workspace, size_t workspace_bytes,
                                 void *stream);
+
+/* One multi-token step: the step's new K/V rows appended to the pool, then
+ * paged_attention_multi over its query tokens, on `stream` in that order
+ * (the multi-token counterpart of pagedkv_decode_step; the append as in
+ * reshape_and_cache, “让 Agent 跑得快”, §一 KV Cache, the attention as in the
+ * passages cited for paged_attention_multi).  Results are identical to
+ * pagedkv_token_slot_mapping + reshape_and_cache + paged_attention_multi.
+ *   new_k, new_v  device bf16 [num_tokens, num_kv_heads, head_dim]: row
+ *                 query_start[b] + i is the K/V of sequence b's token at
+ *                 position seq_lens[b] - n_b + i (quantised on 8-bit pools
+ *                 under k_scale / v_scale of its block, as reshape_and_cache)
+ *   every other argument as for paged_attention_multi (seq_lens already
+ *   counts the new tokens).
+ * The append is one launch: each 16-byte piece of a new row finds its
+ * sequence (the last b with query_start[b] <= row) and its slot from the
+ * block table (block_tables[b][pos / block_size] * block_size +
+ * pos % block_size) and is written there.  A sequence whose offsets do not
+ * fit (rows outside [0, num_tokens], n_b > seq_lens[b] or > max_query_len)
+ * appends nothing and sets PAGEDKV_FLAG_BAD_SEQ_LEN; a position past the
+ * table sets PAGEDKV_FLAG_BAD_SEQ_LEN and an entry outside the pool
+ * PAGEDKV_FLAG_BAD_BLOCK, and that row is skipped.  The attention then
+ * flags and zeroes as paged_attention_multi (offsets that decrease are
+ * flagged there).  Arguments are checked before the first launch;
+ * KV_ERR_INVALID_ARG on a bad one (new_k and new_v must be non-NULL and
+ * 16-byte aligned). */
+kv_status pagedkv_multi_step(void *out, const void *q, const void *new_k,
+                             const void *new_v, void *k_cache, void *v_cache,
+                             const float *k_scale, const float *v_scale,
+                             const int32_t *block_tables, int max_blocks_per_seq,
+                             const int32_t *seq_lens, const int32_t *query_start,
+                             int batch, int num_tokens, int max_query_len,
+                             int num_q_heads, int num_kv_heads, int head_dim,
+                             int num_blocks, int block_size, int max_seq_len,
+                             float scale, kv_dtype dtype, void *workspace,
+                             size_t workspace_bytes, void *stream);
 
 /* ------------------------------------------------------------------------ */
 /* Status                                                                   */

@@ -46,6 +46,8 @@ SIGNATURES = {
     "kv_pool_cached_blocks": (_I, [_P]),
     "paged_attention_multi": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I,
                                    _I, _I, _I, _F, _I, _P, _SZ, _P]),
+    "pagedkv_multi_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I,
+                                _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "pagedkv_pool_tensor_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "pagedkv_slot_mapping": (_I, [_P, _I, _P, _I, _I, _I, _P, _P]),
     "pagedkv_token_slot_mapping": (_I, [_P, _I, _P, _P, _I, _I, _I, _P, _P]),
@@ -380,6 +382,40 @@ def paged_attention_multi(out, q, k_cache, v_cache, block_tables, seq_lens, quer
                                         hq, hkv, d, nb, bs, int(max_seq_len), float(scale), dt,
                                         ws_ptr, ws_n,
                                         _stream(stream)))
+
+
+def multi_step(out, q, new_k, new_v, k_cache, v_cache, block_tables, seq_lens, query_start,
+               max_seq_len, max_query_len, scale, workspace=None, k_scale=None, v_scale=None,
+               stream=None):
+    """One multi-token step: the step's new K/V rows (bf16 [T, Hkv, d], row
+    query_start[b] + i at position seq_lens[b] - n_b + i) appended to the
+    pool, then paged_attention_multi over the query tokens."""
+    import torch
+    dt = _pool_dtype(k_cache)
+    _need(out, torch.bfloat16, "out", 3)
+    _need(q, torch.bfloat16, "q", 3)
+    _need(new_k, torch.bfloat16, "new_k", 3)
+    _need(new_v, torch.bfloat16, "new_v", 3)
+    _need(k_cache, k_cache.dtype, "k_cache", 4)
+    _need(v_cache, k_cache.dtype, "v_cache", 4)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _need(query_start, torch.int32, "query_start", 1)
+    nb, bs, hkv, d = k_cache.shape
+    T, hq, d2 = q.shape
+    B = seq_lens.shape[0]
+    if (out.shape != q.shape or d2 != d or query_start.shape[0] != B + 1 or
+            block_tables.shape[0] != B or tuple(new_k.shape) != (T, hkv, d) or
+            new_v.shape != new_k.shape):
+        raise ValueError("shapes of out, q, new_k, new_v, the pools, the table, seq_lens and "
+                         "query_start disagree")
+    ws_ptr, ws_n = (None, 0) if workspace is None else (_ptr(workspace), workspace.numel() * workspace.element_size())
+    _check(load().pagedkv_multi_step(_ptr(out), _ptr(q), _ptr(new_k), _ptr(new_v), _ptr(k_cache),
+                                     _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                     _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
+                                     _ptr(query_start), B, T, int(max_query_len), hq, hkv, d, nb,
+                                     bs, int(max_seq_len), float(scale), dt, ws_ptr, ws_n,
+                                     _stream(stream)))
 
 
 def workspace_bytes(batch, num_q_heads, head_dim, max_seq_len, block_size) -> int:

@@ -132,8 +132,7 @@ class DecodeBatch:
         pkv.reshape_and_cache(self.new_k, self.new_v, self.k_cache, self.v_cache, self.tok_slots,
                               self.k_scale, self.v_scale)
 
-    def attend_multi(self):
-        """paged_attention_multi over the step's query tokens."""
+    def _multi_buffers(self):
         s = self.wl.spec
         if not hasattr(self, "query_start"):
             self.query_start = torch.from_numpy(self.wl.query_start).to(self.dev)
@@ -142,13 +141,28 @@ class DecodeBatch:
             ws = pkv.multi_workspace_bytes(self.wl.num_tokens, s.num_q_heads, s.head_dim,
                                            self.max_seq_len, s.block_size)
             self.ws_multi = torch.empty(max(ws, 16), dtype=torch.uint8, device=self.dev)
+
+    def attend_multi(self):
+        """paged_attention_multi over the step's query tokens."""
+        self._multi_buffers()
         pkv.paged_attention_multi(self.out_multi, self.q, self.k_cache, self.v_cache,
                                   self.block_tables, self.seq_lens, self.query_start,
-                                  self.max_seq_len, max(int(self.wl.query_lens.max()), 1), s.scale,
-                                  self.ws_multi, self.k_scale, self.v_scale)
+                                  self.max_seq_len, max(int(self.wl.query_lens.max()), 1),
+                                  self.wl.spec.scale, self.ws_multi, self.k_scale, self.v_scale)
         return self.out_multi
 
     def multi_step(self):
+        """pagedkv_multi_step: the step's append and attention in one call."""
+        self._multi_buffers()
+        pkv.multi_step(self.out_multi, self.q, self.new_k, self.new_v, self.k_cache, self.v_cache,
+                       self.block_tables, self.seq_lens, self.query_start, self.max_seq_len,
+                       max(int(self.wl.query_lens.max()), 1), self.wl.spec.scale, self.ws_multi,
+                       self.k_scale, self.v_scale)
+        return self.out_multi
+
+    def multi_step_unfused(self):
+        """The same step as three calls: token slot mapping, reshape_and_cache,
+        paged_attention_multi."""
         self.append_tokens()
         return self.attend_multi()
 

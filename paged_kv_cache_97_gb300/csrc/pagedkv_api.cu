@@ -167,6 +167,100 @@ __global__ void append_kernel(const uint4* __restrict__ k, const uint4* __restri
   }
 }
 
+// Append of a multi-token step: the slot mapping and reshape_and_cache in
+// one pass.  Sequence b's n_b new tokens are rows query_start[b] ..
+// query_start[b] + n_b - 1 of new_k / new_v ([T, Hkv, D] bf16) and go to
+// positions L_b - n_b .. L_b - 1 (its last tokens: seq_lens already counts
+// them).  One thread per 16-byte piece of a row; a row's sequence is the last
+// b with query_start[b] <= row.  A sequence whose offsets do
+// not fit (rows outside [0, T), n_b > L_b or n_b > max_query_len) writes
+// nothing and sets PAGEDKV_FLAG_BAD_SEQ_LEN; a position past the table or an
+// entry outside the pool sets the flag slot_of sets and skips the write.
+template <int kKind>
+__global__ void append_tokens_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                                     void* __restrict__ k_cache, void* __restrict__ v_cache,
+                                     const float* __restrict__ k_scale,
+                                     const float* __restrict__ v_scale,
+                                     const int32_t* __restrict__ block_tables, int max_blocks,
+                                     const int32_t* __restrict__ seq_lens,
+                                     const int32_t* __restrict__ query_start, int batch,
+                                     int num_tokens, int max_query_len, int num_blocks, int bs,
+                                     int num_kv_heads, int head_dim, unsigned int* flags) {
+  const int chunks_per_head = head_dim / 8;
+  const int chunks_per_token = num_kv_heads * chunks_per_head;
+  // The sequence of the CTA's first row, found by the whole CTA in rounds of
+  // blockDim.x samples of query_start (one round for up to 256 sequences);
+  // each thread then walks on to its own row's sequence (a CTA spans few
+  // rows).
+  const int64_t idx0 = (int64_t)blockIdx.x * blockDim.x;
+  const int t0 = (int)(idx0 / chunks_per_token);
+  int lo = 0, hi = batch;                                // b in [lo, hi)
+  while (hi - lo > 1) {
+    const int step = (hi - lo + (int)blockDim.x - 1) / (int)blockDim.x;
+    const int j = lo + (int)threadIdx.x * step;
+    const int cnt = __syncthreads_count(j < hi && query_start[j] <= t0);
+    if (cnt == 0) break;                                 // before every sequence: start at lo
+    lo += (cnt - 1) * step;
+    hi = min(lo + step, hi);
+  }
+  const int64_t idx = idx0 + threadIdx.x;
+  if (idx >= (int64_t)num_tokens * chunks_per_token) return;
+  const int t = (int)(idx / chunks_per_token);           // row of new_k / new_v
+  const int c = (int)(idx % chunks_per_token);
+  int b = lo;
+  while (b + 1 < batch && query_start[b + 1] <= t) ++b;
+  const int q0 = query_start[b], n = query_start[b + 1] - q0;
+  if (t < q0 || t - q0 >= n) return;                     // a row of no sequence
+  const int L = seq_lens[b];
+  if (q0 < 0 || q0 > num_tokens - n || n > L || n > max_query_len) {
+    if (t == q0 && c == 0) atomicOr(flags, PAGEDKV_FLAG_BAD_SEQ_LEN);
+    return;
+  }
+  const int i = t - q0;
+  const int64_t slot = slot_of(block_tables, max_blocks, b, L - n + i, bs, num_blocks, flags);
+  if (slot < 0) return;
+  const int h = c / chunks_per_head;
+  const int64_t dst = (slot * num_kv_heads + h) * chunks_per_head + (c % chunks_per_head);
+  const uint4 kx = k[idx], vx = v[idx];
+  if (kKind != KV_DTYPE_BF16) {
+    const int64_t sidx = (slot / bs) * num_kv_heads + h;
+    constexpr bool kFp8 = kKind == KV_DTYPE_FP8_E4M3;
+    reinterpret_cast<uint2*>(k_cache)[dst] = quantize8<kFp8>(kx, k_scale[sidx]);
+    reinterpret_cast<uint2*>(v_cache)[dst] = quantize8<kFp8>(vx, v_scale[sidx]);
+  } else {
+    reinterpret_cast<uint4*>(k_cache)[dst] = kx;
+    reinterpret_cast<uint4*>(v_cache)[dst] = vx;
+  }
+}
+
+// Launches append_tokens_kernel (arguments checked by the caller).
+kv_status launch_append_tokens(const void* new_k, const void* new_v, void* k_cache, void* v_cache,
+                               const float* k_scale, const float* v_scale,
+                               const int32_t* block_tables, int max_blocks,
+                               const int32_t* seq_lens, const int32_t* query_start, int batch,
+                               int num_tokens, int max_query_len, int num_blocks, int block_size,
+                               int num_kv_heads, int head_dim, kv_dtype dtype, unsigned int* flags,
+                               cudaStream_t s) {
+  const int64_t threads = (int64_t)num_tokens * num_kv_heads * (head_dim / 8);
+  const int block = 256;
+  const int64_t grid = (threads + block - 1) / block;
+  if (grid > 0x7fffffffLL) return fail(KV_ERR_INVALID_ARG, "multi-token append: too many tokens");
+  const uint4 *k = static_cast<const uint4*>(new_k), *v = static_cast<const uint4*>(new_v);
+  if (dtype == KV_DTYPE_INT8)
+    append_tokens_kernel<KV_DTYPE_INT8><<<(unsigned)grid, block, 0, s>>>(
+        k, v, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks, seq_lens, query_start,
+        batch, num_tokens, max_query_len, num_blocks, block_size, num_kv_heads, head_dim, flags);
+  else if (dtype == KV_DTYPE_FP8_E4M3)
+    append_tokens_kernel<KV_DTYPE_FP8_E4M3><<<(unsigned)grid, block, 0, s>>>(
+        k, v, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks, seq_lens, query_start,
+        batch, num_tokens, max_query_len, num_blocks, block_size, num_kv_heads, head_dim, flags);
+  else
+    append_tokens_kernel<KV_DTYPE_BF16><<<(unsigned)grid, block, 0, s>>>(
+        k, v, k_cache, v_cache, nullptr, nullptr, block_tables, max_blocks, seq_lens, query_start,
+        batch, num_tokens, max_query_len, num_blocks, block_size, num_kv_heads, head_dim, flags);
+  return cuda_check(cudaGetLastError(), "append_tokens_kernel launch");
+}
+
 // ---------------------------------------------------------------------------
 // Log-sum-exp merge.  One CTA per (sequence, KV head), `wpr` warps per query
 // head; a row's partials are its partitions of tokens [skip, L) (slots

@@ -31,6 +31,15 @@
 
 namespace pagedkv {
 
+// pagedkv_api.cu: slot mapping + append of a multi-token step's new rows.
+kv_status launch_append_tokens(const void* new_k, const void* new_v, void* k_cache, void* v_cache,
+                               const float* k_scale, const float* v_scale,
+                               const int32_t* block_tables, int max_blocks,
+                               const int32_t* seq_lens, const int32_t* query_start, int batch,
+                               int num_tokens, int max_query_len, int num_blocks, int block_size,
+                               int num_kv_heads, int head_dim, kv_dtype dtype, unsigned int* flags,
+                               cudaStream_t s);
+
 // pagedkv_multi_m16.cu: sequences with n_lo < n_b <= a.col_max_n query
 // tokens, `vgroups` 16-column CTAs per sequence (bf16 pools), longest
 // sequences first when `rank` is set.
@@ -226,15 +235,20 @@ int pagedkv_multi_partition_tokens(int batch, int num_tokens, int max_query_len,
                            max_seq_len, di.num_sms);
 }
 
-kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
-                                const void* v_cache, const float* k_scale, const float* v_scale,
-                                const int32_t* block_tables, int max_blocks_per_seq,
-                                const int32_t* seq_lens, const int32_t* query_start, int batch,
-                                int num_tokens, int max_query_len, int num_q_heads,
-                                int num_kv_heads, int head_dim, int num_blocks, int block_size,
-                                int max_seq_len, float scale, kv_dtype dtype, void* workspace,
-                                size_t workspace_bytes, void* stream) {
-  const char* who = "paged_attention_multi";
+}  // extern "C"
+
+// paged_attention_multi, and with new_k / new_v set the append of the step's
+// tokens before it on the same stream (pagedkv_multi_step): every argument
+// is checked before the first launch.
+static kv_status multi_impl(const char* who, bool append, void* out, const void* q, const void* new_k,
+                            const void* new_v, const void* k_cache, const void* v_cache,
+                            const float* k_scale, const float* v_scale,
+                            const int32_t* block_tables, int max_blocks_per_seq,
+                            const int32_t* seq_lens, const int32_t* query_start, int batch,
+                            int num_tokens, int max_query_len, int num_q_heads, int num_kv_heads,
+                            int head_dim, int num_blocks, int block_size, int max_seq_len,
+                            float scale, kv_dtype dtype, void* workspace, size_t workspace_bytes,
+                            void* stream) {
   if (batch < 0 || num_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
       num_q_heads % num_kv_heads || max_blocks_per_seq <= 0 || num_blocks <= 0 ||
       max_seq_len <= 0 || max_query_len <= 0 || !valid_dtype(dtype))
@@ -264,10 +278,13 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
   const int tpg16 = column_path ? kM16Cols / GQ : 0;
   const int vgroups16 = m16_path ? (min(max_query_len, col_max_n) + tpg16 - 1) / tpg16 : 0;
   if (batch == 0 || num_tokens == 0) return KV_OK;
-  if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !query_start)
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !query_start ||
+      (append && (!new_k || !new_v)))
     return fail(KV_ERR_INVALID_ARG, "%s: NULL pointer", who);
-  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
-    return fail(KV_ERR_INVALID_ARG, "%s: out, q and the pools must be 16-byte aligned", who);
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(new_k) || !aligned16(new_v))
+    return fail(KV_ERR_INVALID_ARG, "%s: out, q, the new rows and the pools must be 16-byte aligned",
+                who);
   if (num_kv_heads > 65535) return fail(KV_ERR_INVALID_ARG, "%s: too many KV heads", who);
   DeviceInfo di;
   kv_status st = device_info(&di);
@@ -324,14 +341,24 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
   auto tc_ctas = [&](int per_sm) {
     return (int)std::min<int64_t>(tiles * num_kv_heads * a.max_parts, (int64_t)di.num_sms * per_sm);
   };
+  if (append &&
+      (st = launch_append_tokens(new_k, new_v, const_cast<void*>(k_cache),
+                                 const_cast<void*>(v_cache), k_scale, v_scale, block_tables,
+                                 max_blocks_per_seq, seq_lens, query_start, batch, num_tokens,
+                                 max_query_len, num_blocks, block_size, num_kv_heads, head_dim,
+                                 dtype, di.flags, s)) != KV_OK)
+    return st;
   if (m16_path) {
-    // the decode kernel's column groups for sequences of one group's tokens
-    // (often none: its CTAs then only read the offsets), then the 16-column
-    // CTAs, longest sequences first
+    // the decode kernel's column groups for sequences of one group's tokens,
+    // then the 16-column CTAs, longest sequences first.  When every sequence
+    // has max_query_len tokens (T = batch x max_query_len, none above the
+    // bound: a longer one is flagged by the 16-column kernel) none has one
+    // group's tokens, and the decode launch is left out.
+    const bool uniform = (int64_t)num_tokens == (int64_t)batch * max_query_len;
     DecodeArgs one = a;
     one.col_max_n = tpg;
     one.vgroups = 1;
-    if ((st = launch_decode(one, s)) != KV_OK ||
+    if ((!uniform && (st = launch_decode(one, s)) != KV_OK) ||
         (st = launch_multi_m16(a, tpg, vgroups16, true, s)) != KV_OK)
       return st;
   } else if (row_path && column_path) {
@@ -353,6 +380,37 @@ kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
     if ((st = launch_multi_tc(a, tc_ctas(1), s)) != KV_OK) return st;
   }
   return launch_multi_merge(a, s);
+}
+
+extern "C" {
+
+kv_status paged_attention_multi(void* out, const void* q, const void* k_cache,
+                                const void* v_cache, const float* k_scale, const float* v_scale,
+                                const int32_t* block_tables, int max_blocks_per_seq,
+                                const int32_t* seq_lens, const int32_t* query_start, int batch,
+                                int num_tokens, int max_query_len, int num_q_heads,
+                                int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                                int max_seq_len, float scale, kv_dtype dtype, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  return multi_impl("paged_attention_multi", false, out, q, nullptr, nullptr, k_cache, v_cache, k_scale,
+                    v_scale, block_tables, max_blocks_per_seq, seq_lens, query_start, batch,
+                    num_tokens, max_query_len, num_q_heads, num_kv_heads, head_dim, num_blocks,
+                    block_size, max_seq_len, scale, dtype, workspace, workspace_bytes, stream);
+}
+
+kv_status pagedkv_multi_step(void* out, const void* q, const void* new_k, const void* new_v,
+                             void* k_cache, void* v_cache, const float* k_scale,
+                             const float* v_scale, const int32_t* block_tables,
+                             int max_blocks_per_seq, const int32_t* seq_lens,
+                             const int32_t* query_start, int batch, int num_tokens,
+                             int max_query_len, int num_q_heads, int num_kv_heads, int head_dim,
+                             int num_blocks, int block_size, int max_seq_len, float scale,
+                             kv_dtype dtype, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  return multi_impl("pagedkv_multi_step", true, out, q, new_k, new_v, k_cache, v_cache, k_scale,
+                    v_scale, block_tables, max_blocks_per_seq, seq_lens, query_start, batch,
+                    num_tokens, max_query_len, num_q_heads, num_kv_heads, head_dim, num_blocks,
+                    block_size, max_seq_len, scale, dtype, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -153,11 +153,12 @@ __global__ void __launch_bounds__(kThreadsOf<MT>, Ring<D, BS, MT>::kMinCtas)
   const int tok0 = vg * MT * TPG;                        // the CTA's first query token
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
 
-  // This kernel's sequences: n_lo < n <= col_max_n (the decode kernel takes
-  // the shorter ones, the tensor-core kernel the longer).
+  // This kernel's sequences: n > n_lo (the decode kernel takes the shorter
+  // ones; it runs only in calls without long queries, so a sequence above
+  // col_max_n is above max_query_len too, and flagged below).
   const int q0 = a.query_start[b];
   const int nq = a.query_start[b + 1] - q0;
-  if (nq <= n_lo || nq > a.col_max_n) return;
+  if (nq <= n_lo) return;
   const bool rows_ok = q0 >= 0 && nq >= 0 && q0 + nq <= a.num_tokens;
   // Row of the q / out tensors that column c (m-tile c / 16) serves (-1:
   // padding): token tok0 + (c / 16) TPG + (c % 16) / GQ of the sequence, head

@@ -118,6 +118,16 @@ def test_host_checks_fail_before_touching_the_gpu(pkv):
     st = lib.paged_attention_decode(P, P, P, P, P, P, P, 4, P, 2, 8, 2, 64, 10, 16, 100,
                                     0.1, 0, None, 0, None)
     assert st == pkv.KV_ERR_INVALID_ARG and b"NULL" in lib.pagedkv_last_error()   # bf16 + scales
+    # the multi-token step: new rows are required, aligned, and checked first
+    st = lib.pagedkv_multi_step(P, P, None, P, P, P, None, None, P, 4, P, P, 2, 6, 3, 8, 2, 64,
+                                10, 16, 100, 0.1, 0, P, 1 << 20, None)
+    assert st == pkv.KV_ERR_INVALID_ARG and b"NULL" in lib.pagedkv_last_error()
+    st = lib.pagedkv_multi_step(P, P, P + 8, P, P, P, None, None, P, 4, P, P, 2, 6, 3, 8, 2, 64,
+                                10, 16, 100, 0.1, 0, P, 1 << 20, None)
+    assert st == pkv.KV_ERR_INVALID_ARG and b"aligned" in lib.pagedkv_last_error()
+    st = lib.pagedkv_multi_step(P, P, P, P, P, P, None, None, P, 4, P, P, 2, 6, 3, 8, 2, 96,
+                                10, 16, 100, 0.1, 0, P, 1 << 20, None)
+    assert st == pkv.KV_ERR_INVALID_ARG and b"head_dim" in lib.pagedkv_last_error()
     st = lib.reshape_and_cache(P, P, P, P, None, None, P, 3, 10, 16, 2, 80, 0, None)
     assert st == pkv.KV_ERR_INVALID_ARG
     st = lib.reshape_and_cache(P + 8, P, P, P, None, None, P, 3, 10, 16, 2, 64, 0, None)
@@ -146,6 +156,9 @@ def test_empty_inputs_return_ok_without_a_device(pkv):
                                           0, None) == pkv.KV_OK
     assert lib.paged_attention_multi(None, None, None, None, None, None, None, 4, None, None, 0, 0,
                                      1, 8, 2, 64, 10, 16, 64, 0.125, 0, None, 0, None) == pkv.KV_OK
+    assert lib.pagedkv_multi_step(None, None, None, None, None, None, None, None, None, 4, None,
+                                  None, 0, 0, 1, 8, 2, 64, 10, 16, 64, 0.125, 0, None, 0,
+                                  None) == pkv.KV_OK
     assert lib.pagedkv_copy_blocks(None, None, None, None, None, 0, 10, 16, 2, 64, 0,
                                    None) == pkv.KV_OK
     assert lib.pagedkv_workspace_bytes(0, 8, 64, 64, 16) == 0

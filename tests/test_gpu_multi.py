@@ -129,6 +129,58 @@ def test_multi_matches_oracle(monkeypatch, case, part):
     check(got, ref, case, wl.spec.kv_dtype)
 
 
+@pytest.mark.parametrize("part", ["", "256"])
+@pytest.mark.parametrize("case", ["g4_d128_spec", "col_g4_mixed", "g4_d64_mixed", "zero_query_seq",
+                                  "m16_one_tile_g4", "col_int8_g8", "col_fp8_g4",
+                                  "row_int8_g4_d64", "g2_prefill_chunk"])
+def test_fused_multi_step_equals_three_calls(monkeypatch, case, part):
+    """pagedkv_multi_step (one append launch, then the attention) leaves the
+    pools and the output bit-identical to token slot mapping +
+    reshape_and_cache + paged_attention_multi, on every kernel of the path
+    (uniform batches, where the decode kernel's launch is left out, and
+    mixed ones) and on 8-bit pools."""
+    if part:
+        monkeypatch.setenv("PAGEDKV_PARTITION_TOKENS", part)
+    wl = CASES[case]()
+    fused, three = GpuStep(wl), GpuStep(wl)
+    out_f = fused.multi_step().clone()
+    out_u = three.multi_step_unfused().clone()
+    torch.cuda.synchronize()
+    st, flags = pkv.get_status()
+    assert flags == 0, hex(flags)
+    np.testing.assert_array_equal(bits_of(fused.k_cache), bits_of(three.k_cache))
+    np.testing.assert_array_equal(bits_of(fused.v_cache), bits_of(three.v_cache))
+    assert torch.equal(out_f.view(torch.int16), out_u.view(torch.int16))
+
+
+def test_fused_multi_step_skips_a_sequence_with_bad_offsets():
+    """A sequence with more queries than tokens appends nothing, is flagged
+    and zeroed; the other sequences' rows and outputs are the unfused path's."""
+    wl = multi([30, 40, 50], [3, 4, 5], seed=63)
+    fused, three = GpuStep(wl), GpuStep(wl)
+    lens = wl.seq_lens.copy()
+    lens[1] = 3                                                   # 4 queries in 3 tokens
+    for g in (fused, three):
+        g.seq_lens = torch.from_numpy(lens).cuda()
+    k_before = bits_of(fused.k_cache).copy()
+    out_f = bits_of(fused.multi_step()).copy()
+    torch.cuda.synchronize()
+    st, flags = pkv.get_status()
+    assert flags & pkv.FLAG_BAD_SEQ_LEN
+    e0, e1 = int(wl.query_start[1]), int(wl.query_start[2])
+    assert not out_f[e0:e1].any() and out_f[:e0].any() and out_f[e1:].any()
+    # sequence 1's block rows are untouched; sequences 0 and 2 as three calls
+    three.multi_step_unfused()
+    torch.cuda.synchronize()
+    pkv.get_status()
+    kf, ku = bits_of(fused.k_cache), bits_of(three.k_cache)
+    for b in (0, 2):
+        for blk in wl.block_tables[b][: -(-int(lens[b]) // wl.spec.block_size)]:
+            np.testing.assert_array_equal(kf[blk], ku[blk])
+    for blk in wl.block_tables[1][: -(-int(wl.seq_lens[1]) // wl.spec.block_size)]:
+        np.testing.assert_array_equal(kf[blk], k_before[blk])
+
+
 def test_one_query_per_sequence_matches_decode():
     """n_b = 1 everywhere: the multi-token kernel and the decode kernel agree
     with the oracle on the same step."""
