@@ -102,6 +102,13 @@ CASES = {
     "m16_one_tile_g4": lambda: multi([700, 33, 1500], [3, 4, 4], hq=32, hkv=8, d=128, seed=61),
     "m16_one_tile_g2_bs32": lambda: multi([300, 1000, 77], [5, 8, 6], hq=4, hkv=2, d=64, bs=32,
                                           seed=62),
+    # uniform batches (every sequence max_query_len tokens: the decode
+    # kernel's launch is left out); with 256-token partitions the new rows of
+    # the first two sequences straddle a partition boundary
+    "m16_uniform_cross": lambda: multi([258, 515, 40, 1030], [5, 5, 5, 5], hq=32, hkv=8, d=128,
+                                       seed=64),
+    "m16_uniform_one_tile": lambda: multi([130, 257, 600], [4, 4, 4], hq=32, hkv=8, d=128,
+                                          seed=65),
     # few-query batches are taken longest first: equal lengths tie-break by index
     "m16_equal_lens": lambda: multi([300, 300, 40, 300, 40], [5, 3, 5, 4, 8], hq=32, hkv=8, d=128,
                                     seed=60),
@@ -130,15 +137,16 @@ def test_multi_matches_oracle(monkeypatch, case, part):
 
 
 @pytest.mark.parametrize("part", ["", "256"])
-@pytest.mark.parametrize("case", ["g4_d128_spec", "col_g4_mixed", "g4_d64_mixed", "zero_query_seq",
+@pytest.mark.parametrize("case", ["g4_d128_spec", "m16_uniform_cross", "m16_uniform_one_tile",
+                                  "col_g4_mixed", "g4_d64_mixed", "zero_query_seq",
                                   "m16_one_tile_g4", "col_int8_g8", "col_fp8_g4",
                                   "row_int8_g4_d64", "g2_prefill_chunk"])
 def test_fused_multi_step_equals_three_calls(monkeypatch, case, part):
-    """pagedkv_multi_step (one append launch, then the attention) leaves the
-    pools and the output bit-identical to token slot mapping +
-    reshape_and_cache + paged_attention_multi, on every kernel of the path
-    (uniform batches, where the decode kernel's launch is left out, and
-    mixed ones) and on 8-bit pools."""
+    """pagedkv_multi_step (the append, then the attention) leaves the pools
+    and the output bit-identical to token slot mapping + reshape_and_cache +
+    paged_attention_multi, on every kernel of the path (uniform few-query
+    batches, whose decode launch is left out, and mixed ones) and on 8-bit
+    pools."""
     if part:
         monkeypatch.setenv("PAGEDKV_PARTITION_TOKENS", part)
     wl = CASES[case]()
