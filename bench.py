@@ -308,6 +308,7 @@ class StepPlan:
         s = wl.spec
         self.multi = bool((wl.query_lens != 1).any())      # several query tokens per sequence
         self.m16 = self.row = False
+        self.traffic_kernel = "decode_kernel"               # the kernel the roofline's traffic is of
         self.prefix = s.shared_prefix_tokens > 0 and not no_shared_prefix and not self.multi
         if self.multi:
             self.fn = g.multi_step
@@ -327,6 +328,8 @@ class StepPlan:
             # the merge when a sequence may span several partitions
             self.row = maxq > col_max
             self.m16 = tpg > 0 and s.kv_dtype == "bf16" and maxq > tpg and not self.row
+            if self.m16:
+                self.traffic_kernel = "multi_m16_kernel"
             uniform = wl.num_tokens == s.batch * maxq
             self.launches = (1 + int(tpg > 0 and not (self.m16 and uniform)) + int(self.m16)
                              + int(self.row) + int(g.max_seq_len > self.part))
@@ -403,14 +406,15 @@ def roofline_of(wl, plan, us, peak, peak_kind):
     over the measured step time, against the measured copy peak."""
     nbytes = algorithmic_bytes(wl)
     achieved = nbytes["step"] / us / 1e3
-    traffic = stored_traffic(wl.spec.name, "decode_kernel")
+    traffic = stored_traffic(wl.spec.name, plan.traffic_kernel)
     return {"bound": "hbm", "kernel": plan.kernels, "achieved": round(achieved, 1), "peak": peak,
             "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
             "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
             "algorithmic_bytes_per_launch": nbytes["step"], "us_per_launch": round(us, 2),
             "traffic": traffic,
             "traffic_over_algorithmic": round(traffic / nbytes["step"], 4) if traffic else None,
-            "ncu": ncu_bandwidth(wl.spec.name, peak)}
+            "traffic_kernel": plan.traffic_kernel,
+            "ncu": ncu_bandwidth(wl.spec.name, peak, plan.traffic_kernel)}
 
 
 def check_status(pkv):
@@ -615,8 +619,7 @@ def measure_multi(config, pkv, dev, stream, peak, replays=40, kv_dtype=None):
     step_bytes = multi_step_bytes(wl)
     fl = multi_flops(wl)
     tpeak, _ = measured_peak_tflops()
-    # the few-query kernel whose DRAM traffic the roofline carries
-    col_kernel = "multi_m16_kernel" if plan.m16 else "decode_kernel"
+    col_kernel = plan.traffic_kernel
     del graph, g
     torch.cuda.empty_cache()
     return {"workload": s.name, "kv_dtype": s.kv_dtype, "query_tokens": wl.num_tokens,
