@@ -57,9 +57,8 @@ constexpr int kRankMax = 128;
 // One TMA request for a whole d128 K or V block of one head: a 5-D map
 // (d mod 64, row, d / 64, head, block) whose box holds both 64-element halves
 // of every row, laid out as two [bs][128 B] swizzled halves (the layout of
-// two 4-D boxes).  Each request carries a fixed cost in the SM's TMA unit:
-// with every block read by two CTAs, 2 KB boxes left the loads behind the
-// consumers.
+// two 4-D boxes).  Each request carries a fixed cost in the SM's TMA unit,
+// which 2 KB boxes (two requests per K or V block) made the loads' limit.
 __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int c3, int c4) {
   asm volatile(
