@@ -4,17 +4,19 @@
 // chunked prefill batched with decodes (“LLM 推理优化技术全景”, SARATHI: a
 // 512-token prefill chunk plus as many decodes as fit).
 //
-// Sequence b has n_b query tokens, already appended: its last n_b tokens,
-// q rows query_start[b] .. query_start[b + 1] - 1.  Query token i sits at
+// Sequence b has n_b query tokens, its last n_b tokens (appended before the
+// attention: by the caller, or by pagedkv_multi_step's append launch), q rows
+// query_start[b] .. query_start[b + 1] - 1.  Query token i sits at
 // position L_b - n_b + i and attends positions 0 .. L_b - n_b + i (causal).
 //
 // Each sequence goes to one of three kernels in the same call:
 //   * one column group (n_b <= 8 / G): the decode kernel, whose 8 MMA
 //     columns per CTA then hold (token, head) pairs (pagedkv_decode.cu);
 //   * a few column groups (8 / G < n_b <= 4 x 8 / G): in calls without
-//     long queries on bf16 pools the 16-column kernel (pagedkv_multi_m16.cu),
-//     16 / G tokens per CTA, so fewer CTAs read each block; otherwise the
-//     decode kernel's column groups;
+//     long queries on bf16 pools the 16-column kernel (pagedkv_multi_m16.cu):
+//     16 / G tokens per m-tile, every such sequence in one CTA, so each block
+//     is read once per (sequence, KV head); otherwise the decode kernel's
+//     column groups;
 //   * longer queries: the tensor-core kernel with TMEM accumulators
 //     (pagedkv_multi_tc.cu), 128 rows per CTA.
 // All write the normalised output (one partition) or per-row (m, l, acc)
@@ -40,8 +42,8 @@ kv_status launch_append_tokens(const void* new_k, const void* new_v, void* k_cac
                                int num_kv_heads, int head_dim, kv_dtype dtype, unsigned int* flags,
                                cudaStream_t s);
 
-// pagedkv_multi_m16.cu: sequences with n_lo < n_b <= a.col_max_n query
-// tokens, `vgroups` 16-column CTAs per sequence (bf16 pools), longest
+// pagedkv_multi_m16.cu: sequences with more than n_lo query tokens,
+// `vgroups` 16-column m-tiles per sequence at most (bf16 pools), longest
 // sequences first when `rank` is set.
 kv_status launch_multi_m16(const DecodeArgs& a, int n_lo, int vgroups, bool rank, cudaStream_t s);
 
@@ -50,7 +52,7 @@ namespace {
 // Column groups the decode kernel may serve per sequence (8 columns each):
 // longer queries go to the tensor-core kernel.
 constexpr int kMaxVGroups = 4;
-// Columns of one 16-column CTA.
+// Columns of one m-tile of the 16-column kernel.
 constexpr int kM16Cols = 16;
 
 // Log-sum-exp merge of the partition partials of every (query token, head)
