@@ -109,6 +109,9 @@ CASES = {
                                        seed=64),
     "m16_uniform_one_tile": lambda: multi([130, 257, 600], [4, 4, 4], hq=32, hkv=8, d=128,
                                           seed=65),
+    # more sequences than the in-kernel ranking takes (128): grid order
+    "m16_unranked_130": lambda: multi([20 + (37 * i) % 181 for i in range(130)], [5] * 130,
+                                      hq=8, hkv=2, d=64, seed=66),
     # few-query batches are taken longest first: equal lengths tie-break by index
     "m16_equal_lens": lambda: multi([300, 300, 40, 300, 40], [5, 3, 5, 4, 8], hq=32, hkv=8, d=128,
                                     seed=60),
